@@ -1,0 +1,373 @@
+"""Pins of the CPU oracle against something other than itself.
+
+Each test checks one oracle function against values the pages print (fixtures in
+tests/golden, each with its citation), a closed form, a library routine, brute force
+on tiny inputs, or an invariant the method fixes.  They are chosen so that a dropped
+term, a wrong sign or index, or a transposed operand fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ================================================================ formats
+def test_bf16_decoder_matches_torch():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 1 << 16, 20000, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16_to_f64(bits)
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def test_e4m3_decoder_exhaustive_vs_torch_and_spec_points():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(ref)], ref[~np.isnan(ref)])
+    # OCP E4M3 landmarks: largest finite, smallest normal, smallest subnormal, one, NaN codes
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0
+    assert got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def test_e2m1_levels_are_the_pages_magnitudes():
+    g = gold("fp4_course_lesson.json")
+    pos = O.e2m1_to_f64(np.arange(8))
+    neg = O.e2m1_to_f64(np.arange(8, 16))
+    assert pos.tolist() == g["e2m1_magnitudes"]
+    assert (-neg).tolist() == g["e2m1_magnitudes"]
+
+
+def test_fp4_dequant_page_examples_and_layout():
+    g = gold("fp4_course_lesson.json")
+    level3 = 0b0101  # e=2, m=1 -> 3
+    for scale, expect in g["level3_times_scale"]:
+        scode = int(torch.tensor([scale]).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+        codes = np.array([[level3 | (level3 << 4)] * 8], np.uint8)  # 16 channels
+        vals = O.fp4_to_f64(codes, np.array([[scode]], np.uint8), 16)
+        assert np.all(vals == expect)
+    # nibble order (low nibble = even channel) and one scale per group
+    codes = np.zeros((1, 16), np.uint8)  # 32 channels
+    codes[0, 0] = 0x2 | (0xB << 4)  # ch0 = +1.0, ch1 = -1.5
+    codes[0, 8] = 0x7  # ch16 = +6
+    s_half = 0x30  # E4M3 0.5
+    s_two = 0x40  # E4M3 2.0
+    v16 = O.fp4_to_f64(codes, np.array([[s_half, s_two]], np.uint8), 16)
+    assert v16[0, 0] == 0.5 and v16[0, 1] == -0.75 and v16[0, 16] == 12.0
+    v32 = O.fp4_to_f64(codes, np.array([[s_two]], np.uint8), 32)
+    assert v32[0, 0] == 2.0 and v32[0, 1] == -3.0 and v32[0, 16] == 12.0
+    # record size at group 16: 4.5 bits per channel, 288 B per 512-channel latent
+    assert (512 // 2 + 512 // 16) == g["bytes_per_512_latent_group16"]
+    assert (16 * 4 + 8) / 16 == g["bits_per_channel_group16"]
+
+
+def test_generator_fp4_encoder_page_example():
+    g = gold("fp4_course_lesson.json")
+    x = torch.zeros(1, 32)
+    x[0, 0] = 3.2
+    x[0, 1] = 6.0  # makes the group scale exactly 1
+    codes, scales = synth.fp4_groups(x, 32)
+    vals = O.fp4_to_f64(codes, scales, 32)
+    assert vals[0, 0] == g["store_3p2_scale1_level"] and vals[0, 1] == 6.0
+
+
+def test_fp8_row_scale():
+    codes = np.array([[0x38, 0xB8, 0x7E]], np.uint8)
+    v = O.fp8_rows_to_f64(codes, np.array([0.25], np.float32))
+    assert v.tolist() == [[0.25, -0.25, 112.0]]
+
+
+# ================================================================ indexer score
+def test_index_score_hand_case():
+    q = np.array([[1.0, 2.0], [-1.0, 0.0]])
+    k = np.array([[3.0, 1.0], [1.0, -1.0], [-2.0, -1.0]])
+    w = np.array([0.5, 2.0])
+    # head 0 dots 5, -1, -4; head 1 dots -3, -1, 2 -> 0.5*5, 0, 2*2
+    assert O.index_scores(q, w, k).tolist() == [2.5, 0.0, 4.0]
+
+
+def test_index_score_one_hot_weight_is_relu_dot():
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((32, 128))
+    k = rng.standard_normal((50, 128))
+    for h in (0, 7, 31):
+        w = np.zeros(32)
+        w[h] = 1.0
+        ref = np.array([max(0.0, float(np.dot(q[h], kj))) for kj in k])
+        assert np.allclose(O.index_scores(q, w, k), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_index_score_all_negative_dots_give_zero():
+    q = np.ones((4, 8))
+    k = -np.ones((3, 8))
+    assert np.all(O.index_scores(q, np.ones(4), k) == 0.0)
+
+
+# ================================================================ top-K
+def test_topk_select_values_cases():
+    for c in gold("select_values_course06.json")["cases"]:
+        order = O.topk_order(c["scores"], c["k"])
+        assert order.tolist() == c["positions_desc"]
+        assert [c["values"][i] for i in order] == c["values_read"]
+        assert O.topk_set(c["scores"], c["k"]).tolist() == sorted(c["positions_desc"])
+
+
+def test_topk_matches_rank_definition_bruteforce():
+    rng = np.random.default_rng(2)
+    for trial in range(300):
+        n = int(rng.integers(1, 24))
+        k = int(rng.integers(1, 30))
+        s = rng.integers(-3, 4, n).astype(np.float64)  # many ties
+        # j is selected iff fewer than k entries precede it in (score desc, index asc)
+        expect = [j for j in range(n)
+                  if sum(1 for i in range(n) if s[i] > s[j] or (s[i] == s[j] and i < j)) < k]
+        assert O.topk_set(s, k).tolist() == expect
+
+
+def test_topk_special_cases():
+    assert O.topk_set(np.zeros(10), 4).tolist() == [0, 1, 2, 3]
+    assert O.topk_set(np.array([1.0, 5.0]), 8).tolist() == [0, 1]
+    assert O.topk_set(np.array([0.0, -0.0, -1.0]), 1).tolist() == [0]
+    assert O.topk_set(np.array([-0.0, 0.0, -1.0]), 1).tolist() == [0]
+
+
+# ================================================================ block pool
+def test_block_pool_course_toy():
+    g = gold("hierarchical_toy_course07.json")
+    s = np.full(g["n_positions"], 0.1)
+    s[6] = 0.9   # block [5-8] (1-based)
+    s[17] = 0.8  # block [17-20]
+    s[0] = 0.5
+    s[23] = 0.4
+    pool, bm, kept = O.block_pool(s, g["block_size"], g["n_keep"])
+    assert (pool + 1).tolist() == g["pool_1based"]
+    assert kept.tolist() == [1, 4]
+
+
+def test_block_pool_invariants():
+    rng = np.random.default_rng(3)
+    for trial in range(100):
+        n = int(rng.integers(1, 300))
+        bs = int(rng.integers(1, 17))
+        nk = int(rng.integers(1, 12))
+        s = rng.integers(-5, 6, n).astype(np.float64)
+        pool, bm, kept = O.block_pool(s, bs, nk)
+        nb = (n + bs - 1) // bs
+        assert len(bm) == nb
+        for c in range(nb):
+            assert bm[c] == s[c * bs:min(n, (c + 1) * bs)].max()
+        dropped = np.setdiff1d(np.arange(nb), kept)
+        if len(dropped) and len(kept):
+            assert bm[kept].min() >= bm[dropped].max()
+        assert int(np.argmax(bm)) in kept.tolist()
+        assert np.all(np.diff(pool) > 0) and pool.max() < n
+        if nk * bs >= n:
+            assert pool.tolist() == list(range(n))
+    s = rng.standard_normal(200)
+    pool, _, _ = O.block_pool(s, 1, 17)
+    assert pool.tolist() == O.topk_set(s, 17).tolist()
+
+
+def test_hierarchy_scored_positions_count():
+    g = gold("hierarchy_count_v41.json")
+    assert g["n_keep_blocks"] * g["block_size"] == g["pool_positions"]
+    got = O.scored_positions(g["n_visible"], g["n_later"], g["n_keep_blocks"], g["block_size"])
+    assert got == g["scored"]
+    assert round(g["five_full_scans"] / got, 2) == g["ratio_printed"]
+
+
+# ================================================================ RoPE
+def test_rope_page_pair():
+    g = gold("rope_v4_pair_toy.json")
+    x = np.array([0.0, 0.0] + g["pair"])  # D=4, rotary on the last 2
+    y = O.rope(x, 3, 1e4, 2)
+    assert abs(y[2] - g["rotated"][0]) <= g["tol"] and abs(y[3] - g["rotated"][1]) <= g["tol"]
+    assert y[0] == 0.0 and y[1] == 0.0
+
+
+def test_rope_frequencies_and_placement():
+    # theta^(-2i/64) at theta=1e4: pair 24 turns 1e-3 rad per position, pair 8 turns 0.1
+    D, R = 512, 64
+    x = np.zeros(D)
+    x[:D - R] = 7.0
+    x[D - R + 2 * 24] = 1.0
+    x[D - R + 2 * 8 + 1] = 1.0
+    y = O.rope(x, 1000, 1e4, R)
+    assert np.all(y[:D - R] == 7.0)
+    assert abs(y[D - R + 48] - math.cos(1.0)) < 1e-12 and abs(y[D - R + 49] - math.sin(1.0)) < 1e-12
+    # (0, 1) turned by 100 rad -> (-sin 100, cos 100)
+    assert abs(y[D - R + 16] + math.sin(100.0)) < 1e-10 and abs(y[D - R + 17] - math.cos(100.0)) < 1e-10
+
+
+def test_rope_inverse_norm_and_relative_position():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal(512)
+    k = rng.standard_normal(512)
+    for p in (0, 5, 2047, 1048576):
+        qp = O.rope(q, p, 1e4, 64)
+        assert np.allclose(O.rope(qp, p, 1e4, 64, sign=-1), q, atol=1e-9)
+        assert abs(np.linalg.norm(qp) - np.linalg.norm(q)) < 1e-9
+    d1 = O.rope(q, 100, 1e4, 64) @ O.rope(k, 40, 1e4, 64)
+    d2 = O.rope(q, 1100, 1e4, 64) @ O.rope(k, 1040, 1e4, 64)
+    assert abs(d1 - d2) < 1e-9
+    assert abs(d1 - q @ k) > 1e-3  # the rotation is not the identity
+
+
+# ================================================================ sink softmax and attention
+@pytest.mark.parametrize("name", ["sink_softmax_v4_swa_toy.json", "sink_softmax_v4_csa_toy.json"])
+def test_sink_softmax_page_values(name):
+    g = gold(name)
+    z = np.array(g["logits"]) if "logits" in g else g["scale"] * np.array(g["qk"])
+    p, sm = O.sink_softmax(z, g["sink"])
+    assert np.all(np.abs(p - np.array(g["weights"])) <= g["tol"])
+    assert abs(sm - g["sink_mass"]) <= g["tol"]
+    assert p.sum() + sm == pytest.approx(1.0, abs=1e-15)
+    if "denominator" in g:
+        assert abs(np.exp(z).sum() + math.exp(g["sink"]) - g["denominator"]) <= g["tol"]
+
+
+def test_sink_lowers_mass_below_one():
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal(640)
+    p, sm = O.sink_softmax(z, 0.3)
+    assert 0.0 < sm < 1.0 and p.sum() < 1.0
+    p, sm = O.sink_softmax(z, -np.inf)
+    assert sm == 0.0 and abs(p.sum() - 1.0) < 1e-14
+
+
+def test_attend_course_two_query_example():
+    g = gold("reuse_two_query_course06.json")
+    K, V = np.array(g["keys"], float), np.array(g["values"], float)
+    q = np.array([g["query_A"], g["query_B"]], float)
+    o, sm = O.attend(q, K, V, g["scale"], np.array([-np.inf, -np.inf]))
+    z = g["scale"] * (q[0] @ K.T)
+    pA, _ = O.sink_softmax(z, -np.inf)
+    assert np.all(np.abs(pA - g["weights_A"]) <= g["tol"])
+    assert np.all(np.abs(o[0] - g["output_A"]) <= g["tol"])
+    assert np.all(np.abs(o[1] - g["output_B"]) <= g["tol"])
+    assert np.all(sm == 0.0)
+
+
+def test_attend_dense_special_case_matches_torch_sdpa():
+    rng = np.random.default_rng(6)
+    H, D, n = 8, 64, 37
+    q = rng.standard_normal((H, D))
+    kv = rng.standard_normal((n, D)) / 8
+    o, _ = O.attend(q, kv, kv, D ** -0.5, np.full(H, -np.inf))
+    t = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(kv), torch.from_numpy(kv), scale=D ** -0.5)
+    assert np.allclose(o, t.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_row_closed_form_constant_rows():
+    # all rows equal c with a zero rotary part: o_h = (1 - sigma_h) c
+    H, D, R = 4, 512, 64
+    rng = np.random.default_rng(7)
+    c = rng.standard_normal(D) / 16
+    c[D - R:] = 0.0
+    q = rng.standard_normal((H, D))
+    sink = rng.standard_normal(H)
+    sel = np.tile(c, (5, 1))
+    swa = np.tile(c, (3, 1))
+    o, sm = O.csa2_attention_row(q, 1234, sel, swa, sink, 1e4, R, D ** -0.5)
+    z = D ** -0.5 * (q @ c)
+    sigma = np.exp(sink) / (8 * np.exp(z) + np.exp(sink))
+    assert np.allclose(sm, sigma, rtol=1e-12)
+    assert np.allclose(o, (1 - sigma)[:, None] * c[None, :], rtol=1e-12, atol=1e-15)
+
+
+def test_attention_row_is_rope_sdpa_inverse_rope_without_sink():
+    rng = np.random.default_rng(8)
+    H, D, R = 6, 512, 64
+    q = rng.standard_normal((H, D))
+    sel = rng.standard_normal((9, D)) / 20
+    swa = rng.standard_normal((4, D)) / 20
+    pos = 777
+    o, sm = O.csa2_attention_row(q, pos, sel, swa, np.full(H, -np.inf), 1e4, R, D ** -0.5)
+    kv = np.concatenate([sel, swa])
+    qr = O.rope(q, pos, 1e4, R)
+    t = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qr), torch.from_numpy(kv), torch.from_numpy(kv), scale=D ** -0.5).numpy()
+    assert np.allclose(o, O.rope(t, pos, 1e4, R, sign=-1), rtol=1e-11, atol=1e-13)
+    assert not np.allclose(o, t, atol=1e-6)  # the output rotation is applied
+
+
+# ================================================================ drivers: invariants of the step
+def _small(name, **kw):
+    return synth.make_inputs(synth.scaled(synth.WORKLOADS[name], **kw), seed=11)
+
+
+def test_causality_future_records_and_window_do_not_matter():
+    inp = _small("tiny_decode", N=700)
+    inp["rows"]["n_visible"][:] = 600
+    base = O.csa2_group(inp)[0]
+    c = inp["cache"]
+    c["k_idx"][:, 600:] = c["k_idx"][:, 600:][:, ::-1]
+    c["lat"][:, 600:] ^= np.uint16(0x0101)
+    again = O.csa2_group(inp)[0]
+    assert np.array_equal(base["idx"], again["idx"])
+    assert np.array_equal(base["o"], again["o"])
+    assert base["idx"].max() < 600
+
+
+def test_window_rows_outside_the_window_do_not_matter():
+    wl = synth.scaled(synth.WORKLOADS["prefill_chunk"], N=900, T=20, P0=880)
+    inp = synth.make_inputs(wl, seed=3)
+    rows = [0, 5, 19]
+    base = O.csa2_group(inp, rows=rows)[0]
+    swa = inp["layers"][0]["swa"]
+    # row t=0 (position 880) sees window positions 753..880 = buffer rows 0..127
+    swa[0, 128:] ^= np.uint16(0x1111)
+    r0 = O.csa2_layer(inp, 0, rows=[0])
+    assert np.array_equal(r0["o"][0], base["o"][0])
+
+
+def test_reuse_same_indices_different_queries_differ():
+    inp = _small("hierarchical", N=3000, B=2)
+    res = O.csa2_group(inp)
+    r4, r5 = res[4], res[5]
+    assert r4["mode"] == "reuse" and r5["mode"] == "reuse"
+    assert np.array_equal(r4["idx"], r5["idx"]) and np.array_equal(r4["idx"], res[3]["idx"])
+    rms = np.sqrt(np.mean(r4["o"] ** 2))
+    assert np.max(np.abs(r4["o"] - r5["o"])) > 0.1 * rms
+    # same query, same indices -> identical output
+    inp["layers"][5]["q"] = inp["layers"][4]["q"]
+    inp["layers"][5]["swa"] = inp["layers"][4]["swa"]
+    inp["layers"][5]["sink"] = inp["layers"][4]["sink"]
+    again = O.csa2_layer(inp, 5, res[4])
+    assert np.array_equal(again["o"], r4["o"])
+
+
+def test_pool_covering_everything_makes_reindex_equal_full():
+    inp = _small("hierarchical", N=1000, B=2, n_keep=16, block_size=64)
+    inp["layers"][1]["q_idx"] = inp["layers"][0]["q_idx"]
+    inp["layers"][1]["w"] = inp["layers"][0]["w"]
+    res = O.csa2_group(inp)
+    assert np.array_equal(res[0]["pool"][:, :1000], np.tile(np.arange(1000), (2, 1)))
+    assert np.array_equal(res[1]["idx"], res[0]["idx"])
+
+
+def test_grid_mode_scores_are_exact_integers_over_16():
+    inp = _small("tiny_decode", N=500)
+    g = synth.make_inputs(synth.scaled(synth.WORKLOADS["tiny_decode"], N=500), seed=2, mode="grid")
+    s = O.index_scores_rows(g, 0)
+    assert np.all(s * 16 == np.round(s * 16))
+    assert np.all(np.abs(s) < 2 ** 16)
+    assert inp["params"]["mode"] == "gauss"
