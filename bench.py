@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA2 attention step on GB300: prints one JSON line (rank 0).
+
+A step is one CSA2 decode layer of the batched-decode workload (B=32 sequences, N=65,536
+visible records each, bf16 indexer keys and latents, top-512, window 128, 64x512 heads):
+indexer scan + per-segment top-K -> top-K merge -> sparse attention -> split combine, all
+through the library's C ABI (csa2_fused_decode).  `value` is queries/s with the cache
+resident in HBM; `e2e` is the same metric with every step's query inputs copied from
+pinned host memory and the outputs read back.  The indexer scan (the dominant kernel) is
+timed live with CUDA events recorded by the library at its stage boundaries.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own batch (independent
+sequences, no data-path collective); the timed region is bracketed by barriers and the
+slowest rank's time is used: weak scaling.
+
+`--impl reference` times the CPU oracle (the reference for this method) on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode queries/s and HBM GB/s at N=64K; prefill indexer TFLOP/s"
+SCAN_SOURCES = ["index_scan.cu", "select.cuh", "common.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--batch", type=int, default=32, help="sequences per GPU (32 = the workload)")
+    ap.add_argument("--records", type=int, default=65536)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+def workload(args):
+    import synth
+    return synth.scaled(synth.WORKLOADS["batched_decode"], B=args.batch, N=args.records)
+
+
+def workload_desc(wl) -> str:
+    return (f"batched decode: B={wl.B}, N={wl.N} visible records per sequence, query at position N, "
+            f"bf16 indexer keys 32x128, bf16 512-d latents, top-{wl.K}, window {wl.W}, 64x512 heads, "
+            f"fused index->select->attend")
+
+
+def algorithmic_bytes(wl):
+    """Bytes the step must move per query (workload recipe): indexer keys and query, the
+    selected latents, the window rows, the main query and the fp32 output."""
+    scan = wl.N * wl.DI * 2 + wl.HI * wl.DI * 2 + wl.HI * 4
+    attn = (wl.K + wl.W) * wl.D * 2 + wl.H * wl.D * 2 + wl.H * wl.D * 4
+    return scan, scan + attn
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_attention_csa2_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, src_hash: str, units: float):
+    """Per-launch DRAM bytes of the kernel from the committed ncu summary, scaled to this
+    launch's units, or None when the summary is missing or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", f"{kernel_key}.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != src_hash or not d.get("units"):
+        return None
+    return float(d["dram_bytes_per_launch"]) * units / float(d["units"])
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def __exit__(self, *exc):
+        self.stop()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows[-3:]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_units: float, local_seconds: float):
+    """Whole-job throughput: units of every rank over the slowest rank's time.  Uses
+    torch.distributed when initialised (any backend), else the local numbers."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_units / local_seconds, local_seconds
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(u.item()) / float(t.item()), float(t.item())
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def oracle_rate(inp, seconds: float, rows_per_call: int = 1):
+    """Queries/s of the CPU oracle on whole decode rows of the bundle (index + top-K +
+    attention per row), rows taken in order until `seconds` of work; returns (rate, rows)."""
+    import oracle
+    n_rows = inp["params"]["Bq"]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        r = done % n_rows
+        oracle.csa2_group(inp, rows=list(range(r, min(n_rows, r + rows_per_call))))
+        done += min(rows_per_call, n_rows - r)
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+def host_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gb300(args, world, rank, local)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import synth
+    wl = workload(args)
+    inp = synth.make_inputs(wl, seed=2)
+    import oracle
+    for w in range(args.warmup):
+        oracle.csa2_group(inp, rows=[w % wl.Bq])
+    t0 = time.perf_counter()
+    rows = 0
+    for s in range(args.steps):
+        r = s % wl.Bq
+        oracle.csa2_group(inp, rows=[r])
+        rows += 1
+    el = time.perf_counter() - t0
+    value = rows / el
+    cores = host_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(wl), "global_batch": wl.B, "seq_len": wl.N,
+                                            "parallelism": "none (host CPU)"},
+            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                             "sample": "one decode row of the batch per step (index over all N records, "
+                                       "top-512, attention), rows in order"},
+            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+    import synth
+    import sparse_attention_csa2_gb300 as S
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    wl = workload(args)
+    inp = synth.make_inputs(wl, seed=2 + rank)
+    dv = synth.to_device(inp, f"cuda:{local}")
+    p, rw, c, lay = dv["params"], dv["rows"], dv["cache"], dv["layers"][0]
+    layer = S.DecodeLayer("full", q_idx=lay["q_idx"], w=lay["w"], k_idx=c["k_idx"], k_scale=c["k_scale"],
+                          seq_of_row=rw["seq_of_row"], n_visible=rw["n_visible"], q=lay["q"], q_pos=rw["q_pos"],
+                          latents=c["lat"], lat_scale=c["lat_scales"], swa=lay["swa"], swa_scale=lay["swa_scale"],
+                          swa_pos0=rw["swa_pos0"], window=p["W"], sink=lay["sink"], K=p["K"], theta=p["theta"],
+                          softmax_scale=p["softmax_scale"])
+    stream = torch.cuda.current_stream()
+    launches_per_step = layer.launches
+
+    # ---- warm-up (first calls set kernel attributes)
+    for _ in range(max(3, args.warmup)):
+        layer()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, scan bracketed by library stage events each step
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall0 = time.time()
+        start.record(stream)
+        for s in range(args.steps):
+            layer.set_stage_events(ev[s])
+            layer()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        clocks.stop()
+        clk = clocks.summary(t_wall0, t_wall1)
+    if world > 1:
+        dist.barrier()
+    elapsed = start.elapsed_time(stop) / 1e3
+    scan_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    topk_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    attn_ms = [ev[s][2].elapsed_time(ev[s][3]) for s in range(args.steps)]
+    layer.set_stage_events([])
+    value, max_elapsed = aggregate(wl.B * args.steps, elapsed)
+
+    # ---- end to end: per-step query inputs from pinned host memory, outputs read back
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (lay["q_idx"], lay["w"], lay["q"], rw["q_pos"], rw["n_visible"])]
+        dev_in = [lay["q_idx"], lay["w"], lay["q"], rw["q_pos"], rw["n_visible"]]
+        host_out = [torch.empty_like(layer.out, device="cpu").pin_memory(),
+                    torch.empty_like(layer.idx, device="cpu").pin_memory()]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        e_steps = max(10, args.steps // 4)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            layer()
+            host_out[0].copy_(layer.out, non_blocking=True)
+            host_out[1].copy_(layer.idx, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_val, _ = aggregate(wl.B * e_steps, e0.elapsed_time(e1) / 1e3)
+        e2e = {"value": e_val, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e_steps, "note": "KV cache resident in HBM; per-step query inputs host->device, "
+                                         "attention output and indices device->host"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (indexer scan + per-segment top-K)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        peaks = json.load(open(peaks_path))
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        peak, peak_src = 6800.0, "fallback"
+    scan_bytes_q, step_bytes_q = algorithmic_bytes(wl)
+    scan_bytes = scan_bytes_q * wl.B
+    scan_avg = statistics.mean(scan_ms) / 1e3
+    achieved = scan_bytes / scan_avg / 1e9
+    src_hash = source_hash(SCAN_SOURCES)
+    traffic = ncu_traffic("index_scan_batched_decode", src_hash, wl.B * wl.N)
+    roofline = {"bound": "hbm", "kernel": "index_scan_kernel<bf16> (indexer scan + per-segment top-K)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
+                "fallback 6.8 TB/s", "traffic": traffic,
+                "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_avg * 1e3,
+                "source_hash": src_hash}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, rows, secs = oracle_rate(inp, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "queries/s", "cores": host_threads(), "kind": "oracle",
+               "sample": f"{rows} decode rows of this workload's batch (full oracle layer: scores over all "
+                         f"{wl.N} records, top-{wl.K}, attention) in {secs:.1f} s; numpy float64, BLAS threads "
+                         f"for the score matmul"}
+
+    step_s = max_elapsed / args.steps
+    line = {"metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "global_batch": wl.B * world, "seq_len": wl.N,
+                       "parallelism": f"replicas x{world} (independent sequences per GPU)",
+                       "l2": "inputs larger than L2 (537 MB of indexer keys streamed per step)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+            "extra": {"step_hbm_gbs": step_bytes_q * wl.B * world / step_s / 1e9,
+                      "step_algorithmic_bytes": step_bytes_q * wl.B,
+                      "stage_ms": {"scan": statistics.mean(scan_ms), "topk_merge": statistics.mean(topk_ms),
+                                   "attention": statistics.mean(attn_ms)},
+                      "launches_per_step": launches_per_step}}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

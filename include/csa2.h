@@ -1,0 +1,270 @@
+/*
+ * csa2.h - C ABI of the CSA2 attention step (DeepSeek-V4.1-Flash) on sm_103a.
+ *
+ * The step, as the pages describe it ("DeepSeek-V4.1-Flash explained", sections 2 and 3;
+ * "Every layer, connected", "The global and index paths" and "The query and output
+ * paths"; "DeepSeek V4 Inside", CSA section and eq. (27)):
+ *
+ *   1. the lightning indexer scores every causally visible global record,
+ *        score_j = sum_{h<32} w_h * ReLU(q^I_h . k^I_j);
+ *   2. top-K (512) selection of record addresses, directly or from a block-max pool
+ *      built by the first decoder indexer (hierarchical indexing); Reuse layers take
+ *      the preceding layer's selection;
+ *   3. 64-head x 512 shared-latent MQA over the selected latents (each latent is key and
+ *      value at once) plus the layer's 128-token sliding window, one sink logit per head
+ *      in the softmax denominator, RoPE on the last 64 dims of q and inverse RoPE on the
+ *      output's rotary coordinates.
+ *
+ * Conventions shared by every call
+ *   - Every pointer in an args struct is a DEVICE pointer owned by the caller, unless a
+ *     field says otherwise.  The library keeps no pointer after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).  They never synchronize and never allocate; scratch memory
+ *     comes from the caller through `workspace` (size from the matching *_workspace_size).
+ *   - Arrays are dense row-major; base pointers must be 16-byte aligned.
+ *   - Arguments are validated on the host before anything is launched.  An invalid call
+ *     returns CSA2_EINVAL (or CSA2_EUNSUPPORTED for a valid request outside the
+ *     implemented sizes) and launches nothing.  CSA2_ECUDA reports a failed launch.
+ *   - Device pointer contents are not inspected by the host.  Attention skips a selected
+ *     record index outside [0, n_records) (other than the -1 pad) and, when `dev_status` is
+ *     given, stores CSA2_EDEVICE_INDEX there.  Other out-of-range device data (a sequence
+ *     index >= n_seq, a candidate position >= n_records, n_visible > n_records) is
+ *     undefined behaviour.
+ *   - Fixed sizes: 32 indexer heads x 128 dims; 64 query heads x 512 dims; RoPE on the
+ *     last 64 dims (adjacent pairs, frequency theta^(-2i/64)).
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA2_IDX_HEADS 32
+#define CSA2_IDX_DIM 128
+#define CSA2_HEADS 64
+#define CSA2_HEAD_DIM 512
+#define CSA2_ROPE_DIM 64
+#define CSA2_MAX_TOPK 1024
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_EINVAL = 1,          /* bad shape, dtype, null pointer or alignment; nothing launched */
+  CSA2_EUNSUPPORTED = 2,    /* a valid request outside the implemented sizes */
+  CSA2_ECUDA = 3,           /* a CUDA launch or runtime call failed */
+  CSA2_ETIMEOUT = 4,        /* a device-side bounded wait gave up (reported in dev_status) */
+  CSA2_EWORKSPACE = 5,      /* workspace missing or smaller than *_workspace_size */
+  CSA2_EDEVICE_INDEX = 6    /* a kernel met (and skipped) an out-of-range device index */
+} csa2_status;
+
+/* Storage formats of cached rows. */
+typedef enum csa2_dtype {
+  CSA2_BF16 = 0,              /* bf16 values */
+  CSA2_FP8_E4M3_ROWSCALE = 1, /* OCP E4M3 codes, one fp32 scale per row: value = code * scale */
+  CSA2_FP4_E2M1_G32 = 2,      /* E2M1 codes, two per byte (low nibble = even channel), and one
+                                 E4M3 scale per 32 channels in a separate array:
+                                 value = level * scale ("DeepSeek-V4.1-Flash explained", section 7) */
+  CSA2_FP4_E2M1_G16 = 3       /* the same with one scale per 16 channels, as the pages state */
+} csa2_dtype;
+
+/* Layer modes of a CSA2 sharing group ("DeepSeek-V4.1-Flash explained", section 2, mode
+ * table; section 3 for the pool). */
+typedef enum csa2_mode {
+  CSA2_MODE_FULL = 0,       /* score all visible records, fresh top-K, attend */
+  CSA2_MODE_FULL_POOL = 1,  /* FULL, and also build the block pool for later indexers */
+  CSA2_MODE_REINDEX = 2,    /* score only the pool with this layer's indexer query, top-K, attend */
+  CSA2_MODE_REUSE = 3       /* no indexing: attend over the given selection */
+} csa2_mode;
+
+/* ------------------------------------------------------------------------------------
+ * csa2_index_scores - lightning-indexer scores.
+ *
+ * The indexer adds up the rectified query-key dot products of 32 heads, each with its own
+ * weight, and only causally visible records may be selected ("Every layer, connected",
+ * "The global and index paths").
+ *   scores[r, j] = sum_h w[r, h] * max(0, q_idx[r, h, :] . key(j))       for a candidate j
+ *   scores[r, j] = -inf                                                   otherwise
+ * One indexer key per record, shared by all 32 heads.  FP8 keys: key(j) = code * k_scale[j].
+ * Without `cand`, j runs over records 0..n_records-1 and records >= n_visible[r] are not
+ * candidates.  With `cand`, j runs over cand[r, 0..L) (record positions, strictly
+ * ascending, e.g. a block pool) and entries >= n_cand[r] are not candidates.
+ * Optionally also the block maxima: block_max[r, c] = max over the candidate records of
+ * block c = [c*block_size, (c+1)*block_size) (-inf if none), for the block pool.
+ * ------------------------------------------------------------------------------------ */
+typedef struct csa2_index_args {
+  const void* q_idx;          /* [n_rows, 32, 128] bf16 */
+  const float* w;             /* [n_rows, 32] */
+  const void* k_idx;          /* [n_seq, n_records, 128]: bf16, or E4M3 bytes (k_dtype FP8) */
+  const float* k_scale;       /* [n_seq, n_records] row scales for FP8 keys, else NULL */
+  int32_t k_dtype;            /* CSA2_BF16 or CSA2_FP8_E4M3_ROWSCALE */
+  int32_t n_rows;             /* query rows (>= 0) */
+  int32_t n_seq;              /* sequences sharing the key layout */
+  int64_t n_records;          /* records per sequence (>= 1) */
+  const int32_t* seq_of_row;  /* [n_rows] sequence of each query row */
+  const int32_t* n_visible;   /* [n_rows] records 0..n_visible-1 are visible (<= n_records) */
+  const int32_t* cand;        /* [n_rows, L] candidate record positions, or NULL */
+  const int32_t* n_cand;      /* [n_rows] valid candidates per row (required with cand) */
+  int64_t L;                  /* candidates per row when cand != NULL */
+  float* scores;              /* out [n_rows, L or n_records] fp32 */
+  float* block_max;           /* out [n_rows, ceil(n_records / block_size)] or NULL (no cand) */
+  int32_t block_size;         /* > 0 when block_max != NULL */
+} csa2_index_args;
+
+csa2_status csa2_index_scores(const csa2_index_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * csa2_topk - exact top-K of every row, returned as addresses.
+ *
+ * Selection yields record addresses, not scores, and equal scores go to the lower
+ * position (course lesson "06 / Indexer and attention", select_values).  Entries 0..n_valid[r]-1 of row r are the
+ * candidates; the K best by (score descending, entry index ascending) are selected, with
+ * -0.0 == +0.0.  idx[r] holds their record positions (cand[r, j], or j when cand is NULL)
+ * as an ASCENDING set, padded with -1 when fewer than K are valid.  Scores must not be NaN.
+ * ------------------------------------------------------------------------------------ */
+typedef struct csa2_topk_args {
+  const float* scores;        /* [n_rows, L] */
+  const int32_t* cand;        /* [n_rows, L] strictly ascending record positions, or NULL */
+  const int32_t* n_valid;     /* [n_rows] in [0, L] */
+  int32_t n_rows;
+  int64_t L;                  /* 1 .. 2^24 */
+  int32_t K;                  /* 1 .. CSA2_MAX_TOPK */
+  int32_t* idx;               /* out [n_rows, K] */
+  void* workspace;            /* csa2_topk_workspace_size bytes */
+  size_t workspace_bytes;
+} csa2_topk_args;
+
+size_t csa2_topk_workspace_size(const csa2_topk_args* a);
+csa2_status csa2_topk(const csa2_topk_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * csa2_block_pool - the hierarchical candidate pool of the first decoder indexer.
+ *
+ * The first decoder indexer cuts the positions into blocks, rates each block by its best
+ * position and keeps the best blocks; later Reindex layers select only among those
+ * ("DeepSeek-V4.1-Flash explained", section 3; course lesson "07 / Hierarchical
+ * indexing").  Of the ceil(n_visible[r] / block_size) blocks of row r, the n_keep best by
+ * (block max descending, block index ascending) are kept; pool[r] lists every visible
+ * position of the kept blocks in ascending order, -1 padded; n_pool[r] is its length.
+ * ------------------------------------------------------------------------------------ */
+typedef struct csa2_block_pool_args {
+  const float* block_max;     /* [n_rows, n_blocks] from csa2_index_scores */
+  const int32_t* n_visible;   /* [n_rows] */
+  int32_t n_rows;
+  int32_t n_blocks;           /* ceil(n_records / block_size) */
+  int32_t block_size;         /* 1 .. 4096 */
+  int32_t n_keep;             /* 1 .. n_keep * block_size <= 2^20 */
+  int32_t* pool;              /* out [n_rows, n_keep * block_size] */
+  int32_t* n_pool;            /* out [n_rows] */
+  void* workspace;            /* csa2_block_pool_workspace_size bytes */
+  size_t workspace_bytes;
+} csa2_block_pool_args;
+
+size_t csa2_block_pool_workspace_size(const csa2_block_pool_args* a);
+csa2_status csa2_block_pool(const csa2_block_pool_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * csa2_sparse_attn - shared-latent MQA over the selected latents plus the sliding window.
+ *
+ * For query row r at position p = q_pos[r] of sequence b = seq_of_row[r]:
+ *   q'_h  = RoPE_p(q[r, h])            on dims 448..511, pairs (448+2i, 449+2i), angle
+ *                                      p * rope_theta^(-2i/64)
+ *   rows  = latents[b, idx[r, k]] for idx != -1, then the window rows of positions
+ *           max(p - window + 1, swa_pos0[b]) .. p (the current token included), read from
+ *           swa[b, position - swa_pos0[b]]
+ *   z_hj  = softmax_scale * q'_h . row_j
+ *   o_h   = sum_j exp(z_hj) row_j / (sum_j exp(z_hj) + exp(sink[h]))    ("DeepSeek V4
+ *           Inside", eq. (27): the sink logit is in the denominator only)
+ *   out   = RoPE_{-p}(o_h) on dims 448..511 ("Every layer, connected", "The query and output
+ *           paths": inverse RoPE on the output's rotary coordinates)
+ *   sink_mass[r, h] = exp(sink[h]) / (sum_j exp(z_hj) + exp(sink[h]))
+ * Latents and window rows are used as stored: the cache holds them already rotated.
+ * Requires p - swa_pos0[b] < swa_rows.  FP8 window rows: row = code * swa_scale[row].
+ * ------------------------------------------------------------------------------------ */
+typedef struct csa2_attn_args {
+  const void* q;              /* [n_rows, 64, 512] bf16, before RoPE */
+  const int64_t* q_pos;       /* [n_rows] */
+  const int32_t* seq_of_row;  /* [n_rows] */
+  int32_t n_rows;
+  int32_t n_seq;
+  int64_t n_records;
+  const void* latents;        /* bf16 [n_seq, n_records, 512] or FP4 codes [n_seq, n_records, 256] */
+  const uint8_t* lat_scale;   /* FP4: E4M3 [n_seq, n_records, 512/group], else NULL */
+  int32_t lat_dtype;          /* CSA2_BF16, CSA2_FP4_E2M1_G32 or CSA2_FP4_E2M1_G16 */
+  const int32_t* idx;         /* [n_rows, K] record positions in [0, n_records) or -1 */
+  int32_t K;                  /* 0 .. CSA2_MAX_TOPK */
+  const void* swa;            /* bf16 [n_seq, swa_rows, 512] or E4M3 [n_seq, swa_rows, 512] */
+  const float* swa_scale;     /* FP8: [n_seq, swa_rows], else NULL */
+  int32_t swa_dtype;          /* CSA2_BF16 or CSA2_FP8_E4M3_ROWSCALE */
+  int64_t swa_rows;
+  const int64_t* swa_pos0;    /* [n_seq] absolute position of window row 0 */
+  int32_t window;             /* 0 .. 1024 */
+  const float* sink;          /* [64] sink logits */
+  float rope_theta;           /* > 0 */
+  float softmax_scale;
+  float* out;                 /* out [n_rows, 64, 512] fp32 */
+  float* sink_mass;           /* out [n_rows, 64] or NULL */
+  void* workspace;            /* csa2_sparse_attn_workspace_size bytes */
+  size_t workspace_bytes;
+  int32_t* dev_status;        /* optional device int32, set to CSA2_EDEVICE_INDEX when idx holds a
+                                 record index outside [0, n_records) other than -1; or NULL */
+} csa2_attn_args;
+
+size_t csa2_sparse_attn_workspace_size(const csa2_attn_args* a);
+csa2_status csa2_sparse_attn(const csa2_attn_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * csa2_fused_decode - one CSA2 layer of a decode step, with no host round trip.
+ *
+ * FULL:      index (all visible records) -> top-K -> attention.
+ * FULL_POOL: FULL, and the block pool (block_size, n_keep) written to pool / n_pool.
+ * REINDEX:   index over pool / n_pool (inputs) with this layer's q_idx and w -> top-K ->
+ *            attention.
+ * REUSE:     attention over idx (input).
+ * Each layer has a fixed mode (course lesson "05 / Sharing memory"); a sharing group is a
+ * sequence of calls on one stream.
+ * The `index` member is read for FULL, FULL_POOL and REINDEX; its scores / block_max /
+ * cand fields are ignored (the fused path keeps scores on chip).  The `attn` member's idx
+ * field is ignored: attention reads `idx` below.
+ * ------------------------------------------------------------------------------------ */
+typedef struct csa2_decode_args {
+  int32_t mode;               /* csa2_mode */
+  csa2_index_args index;
+  int32_t K;                  /* top-K (1 .. CSA2_MAX_TOPK) */
+  int32_t block_size;         /* FULL_POOL */
+  int32_t n_keep;             /* FULL_POOL */
+  int32_t pool_len;           /* columns of pool: n_keep * block_size */
+  int32_t* pool;              /* FULL_POOL: out; REINDEX: in  [n_rows, pool_len] */
+  int32_t* n_pool;            /* FULL_POOL: out; REINDEX: in  [n_rows] */
+  int32_t* idx;               /* FULL, FULL_POOL, REINDEX: out; REUSE: in  [n_rows, K] */
+  csa2_attn_args attn;
+  void* workspace;            /* csa2_fused_decode_workspace_size bytes */
+  size_t workspace_bytes;
+  /* Optional tracing: cudaEvent_t handles (as void*) recorded on `stream` at the stage
+   * boundaries: [0] before indexing, [1] after the indexer scan, [2] after the top-K merge
+   * and block pool, [3] after attention.  NULL entries are skipped.  The events belong to
+   * the caller, who must have created them (cudaEventCreate). */
+  void* stage_events[4];
+} csa2_decode_args;
+
+size_t csa2_fused_decode_workspace_size(const csa2_decode_args* a);
+/* Number of kernels one csa2_fused_decode call with these arguments launches. */
+int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a);
+csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Utilities
+ * ------------------------------------------------------------------------------------ */
+const char* csa2_status_string(csa2_status s);
+/* Copies the device status word written by kernels (device index checks) to the host.
+ * Synchronizes `stream` first.  Returns CSA2_OK and stores the word in *host_out. */
+csa2_status csa2_read_device_status(const int32_t* dev_status, int32_t* host_out, void* stream);
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t csa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

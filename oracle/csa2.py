@@ -63,8 +63,8 @@ def e2m1_to_f64(nibbles) -> np.ndarray:
 
 def fp4_to_f64(codes, scales, group: int) -> np.ndarray:
     """Dequantize FP4 main-KV records: value = E2M1 level x the E4M3 scale of its group
-    ("reconstructed value = stored level x shared scale", course FP4 lesson; one E4M3 scale
-    per 16 channels in section 7 of "DeepSeek-V4.1-Flash explained").
+    (course FP4 lesson, section 3: a code picks a level and the group's shared scale sets its
+    size; one E4M3 scale per 16 channels in section 7 of "DeepSeek-V4.1-Flash explained").
 
     codes [..., D/2] hold two codes per byte, the low nibble being the even channel;
     scales [..., D/group] hold one E4M3 code per group (the group size is a parameter:
@@ -86,7 +86,7 @@ def index_scores(q_idx, w, keys) -> np.ndarray:
     """Lightning-indexer score of every given record:
     score_j = sum_h w_h * ReLU(q^I_h . k^I_j) over the indexer heads.
 
-    "Indexer scores combine rectified query-key products across 32 weighted heads"
+    The indexer sums the rectified query-key dot products of its 32 heads, each weighted
     ("Every layer, connected", "The global and index paths").  Reading: one indexer key per
     record, shared by all heads (the pages call the keys compact and give them no head index),
     no scaling or bias, and one weight per head for this query row.
@@ -195,8 +195,8 @@ def csa2_attention_row(q, q_pos, sel_rows, swa_rows, sink, theta, R, scale):
     coordinates turned back by -q_pos ("DeepSeek V4 Inside", CSA section; "Every layer,
     connected", "The query and output paths" and "The global and index paths").
 
-    Stored latents and window rows are taken as already rotated ("Quantize after RoPE",
-    course FP4 lesson), so only q is rotated here."""
+    Stored latents and window rows are taken as already rotated (the course FP4 lesson has
+    the cache quantized after RoPE is applied), so only q is rotated here."""
     qr = rope(q, q_pos, theta, R)
     kv = np.concatenate([np.asarray(sel_rows, np.float64).reshape(-1, qr.shape[1]),
                          np.asarray(swa_rows, np.float64).reshape(-1, qr.shape[1])], 0)
@@ -225,8 +225,8 @@ def latents_of(inp, b: int, positions) -> np.ndarray:
 
 def swa_rows_of(inp, layer: int, b: int, q_pos: int) -> np.ndarray:
     """The layer's own sliding-window rows seen by a query at q_pos: absolute positions
-    max(q_pos-W+1, swa_pos0) .. q_pos, the current token included (window of 128 with the
-    current token, "DeepSeek V4 Inside", layer-0 SWA: "p sees the previous e and itself")."""
+    max(q_pos-W+1, swa_pos0) .. q_pos, the current token included ("DeepSeek V4 Inside",
+    layer-0 SWA: with a window of 2 the query attends to the previous token and to itself)."""
     p, rows, lay = inp["params"], inp["rows"], inp["layers"][layer]
     W = p["W"]
     pos0 = int(rows["swa_pos0"][b])

@@ -1,0 +1,308 @@
+"""Python binding of libcsa2.so, the C ABI of the CSA2 attention step on sm_103a.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  Tensors are
+torch CUDA tensors; outputs and workspaces are allocated here with torch and passed as
+device pointers; calls are queued on torch's current CUDA stream.  The library must be
+built (``python sparse_attention_csa2_gb300/_build.py``); importing this package without
+it raises immediately - there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libcsa2.so")
+
+# ------------------------------------------------------------------ constants (csa2.h)
+OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EWORKSPACE, EDEVICE_INDEX = range(7)
+BF16, FP8_E4M3_ROWSCALE, FP4_E2M1_G32, FP4_E2M1_G16 = range(4)
+MODE_FULL, MODE_FULL_POOL, MODE_REINDEX, MODE_REUSE = range(4)
+IDX_HEADS, IDX_DIM, HEADS, HEAD_DIM, ROPE_DIM, MAX_TOPK = 32, 128, 64, 512, 64, 1024
+MODES = {"full": MODE_FULL, "full_pool": MODE_FULL_POOL, "reindex": MODE_REINDEX, "reuse": MODE_REUSE}
+
+
+class CSA2Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_lib.csa2_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libcsa2.so is not built ({_LIB_PATH}); run python sparse_attention_csa2_gb300/_build.py")
+_lib = C.CDLL(_LIB_PATH)
+LIB_PATH = _LIB_PATH
+
+_vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
+
+
+class IndexArgs(C.Structure):
+    _fields_ = [("q_idx", _vp), ("w", _vp), ("k_idx", _vp), ("k_scale", _vp), ("k_dtype", _i32),
+                ("n_rows", _i32), ("n_seq", _i32), ("n_records", _i64), ("seq_of_row", _vp),
+                ("n_visible", _vp), ("cand", _vp), ("n_cand", _vp), ("L", _i64), ("scores", _vp),
+                ("block_max", _vp), ("block_size", _i32)]
+
+
+class TopkArgs(C.Structure):
+    _fields_ = [("scores", _vp), ("cand", _vp), ("n_valid", _vp), ("n_rows", _i32), ("L", _i64),
+                ("K", _i32), ("idx", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class BlockPoolArgs(C.Structure):
+    _fields_ = [("block_max", _vp), ("n_visible", _vp), ("n_rows", _i32), ("n_blocks", _i32),
+                ("block_size", _i32), ("n_keep", _i32), ("pool", _vp), ("n_pool", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class AttnArgs(C.Structure):
+    _fields_ = [("q", _vp), ("q_pos", _vp), ("seq_of_row", _vp), ("n_rows", _i32), ("n_seq", _i32),
+                ("n_records", _i64), ("latents", _vp), ("lat_scale", _vp), ("lat_dtype", _i32),
+                ("idx", _vp), ("K", _i32), ("swa", _vp), ("swa_scale", _vp), ("swa_dtype", _i32),
+                ("swa_rows", _i64), ("swa_pos0", _vp), ("window", _i32), ("sink", _vp),
+                ("rope_theta", _f32), ("softmax_scale", _f32), ("out", _vp), ("sink_mass", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz), ("dev_status", _vp)]
+
+
+class DecodeArgs(C.Structure):
+    _fields_ = [("mode", _i32), ("index", IndexArgs), ("K", _i32), ("block_size", _i32),
+                ("n_keep", _i32), ("pool_len", _i32), ("pool", _vp), ("n_pool", _vp), ("idx", _vp),
+                ("attn", AttnArgs), ("workspace", _vp), ("workspace_bytes", _sz),
+                ("stage_events", _vp * 4)]
+
+
+def _sig(name, argtypes, restype):
+    f = getattr(_lib, name)
+    f.argtypes = argtypes
+    f.restype = restype
+    return f
+
+
+_lib.csa2_status_string.argtypes = [C.c_int]
+_lib.csa2_status_string.restype = C.c_char_p
+_index_scores = _sig("csa2_index_scores", [C.POINTER(IndexArgs), _vp], C.c_int)
+_topk_ws = _sig("csa2_topk_workspace_size", [C.POINTER(TopkArgs)], _sz)
+_topk = _sig("csa2_topk", [C.POINTER(TopkArgs), _vp], C.c_int)
+_pool_ws = _sig("csa2_block_pool_workspace_size", [C.POINTER(BlockPoolArgs)], _sz)
+_block_pool = _sig("csa2_block_pool", [C.POINTER(BlockPoolArgs), _vp], C.c_int)
+_attn_ws = _sig("csa2_sparse_attn_workspace_size", [C.POINTER(AttnArgs)], _sz)
+_sparse_attn = _sig("csa2_sparse_attn", [C.POINTER(AttnArgs), _vp], C.c_int)
+_decode_ws = _sig("csa2_fused_decode_workspace_size", [C.POINTER(DecodeArgs)], _sz)
+_fused_decode = _sig("csa2_fused_decode", [C.POINTER(DecodeArgs), _vp], C.c_int)
+_decode_launches = _sig("csa2_fused_decode_launch_count", [C.POINTER(DecodeArgs)], C.c_int32)
+_version = _sig("csa2_version", [], C.c_int32)
+_read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
+
+
+def version() -> int:
+    return int(_version())
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise CSA2Error(status, what)
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(t):
+    return t.device
+
+
+def _ws(nbytes: int, device):
+    if nbytes == 0:
+        return None, 0
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return buf, nbytes
+
+
+def _key_dtype(k_idx, k_scale):
+    if k_idx.element_size() == 2:
+        return BF16
+    if k_idx.element_size() == 1 and k_scale is not None:
+        return FP8_E4M3_ROWSCALE
+    raise ValueError("indexer keys must be bf16 (2-byte) or E4M3 bytes with row scales")
+
+
+def _lat_dtype(lat, lat_scale):
+    if lat.element_size() == 2:
+        return BF16
+    g = HEAD_DIM // lat_scale.shape[-1]
+    return FP4_E2M1_G32 if g == 32 else FP4_E2M1_G16
+
+
+def _i32t(x, device):
+    return torch.as_tensor(x, dtype=torch.int32, device=device).contiguous()
+
+
+def _i64t(x, device):
+    return torch.as_tensor(x, dtype=torch.int64, device=device).contiguous()
+
+
+def _index_args(q_idx, w, k_idx, k_scale, seq_of_row, n_visible, cand=None, n_cand=None):
+    a = IndexArgs()
+    a.q_idx, a.w, a.k_idx, a.k_scale = _ptr(q_idx), _ptr(w), _ptr(k_idx), _ptr(k_scale)
+    a.k_dtype = _key_dtype(k_idx, k_scale)
+    a.n_rows = q_idx.shape[0]
+    a.n_seq, a.n_records = k_idx.shape[0], k_idx.shape[1]
+    a.seq_of_row, a.n_visible = _ptr(seq_of_row), _ptr(n_visible)
+    if cand is not None:
+        a.cand, a.n_cand, a.L = _ptr(cand), _ptr(n_cand), cand.shape[1]
+    return a
+
+
+# ------------------------------------------------------------------ public calls
+def index_scores(q_idx, w, k_idx, k_scale, seq_of_row, n_visible, cand=None, n_cand=None,
+                 block_size: int = 0):
+    """Indexer scores [n_rows, L] (fp32, -inf where not a candidate) and, with block_size > 0,
+    the block maxima [n_rows, ceil(N / block_size)]."""
+    dev = _dev(q_idx)
+    a = _index_args(q_idx, w, k_idx, k_scale, seq_of_row, n_visible, cand, n_cand)
+    L = cand.shape[1] if cand is not None else k_idx.shape[1]
+    scores = torch.empty((a.n_rows, L), dtype=torch.float32, device=dev)
+    a.scores = _ptr(scores)
+    bmax = None
+    if block_size > 0:
+        bmax = torch.empty((a.n_rows, (k_idx.shape[1] + block_size - 1) // block_size), dtype=torch.float32,
+                           device=dev)
+        a.block_max, a.block_size = _ptr(bmax), block_size
+    _check(_index_scores(C.byref(a), _stream()), "csa2_index_scores")
+    return (scores, bmax) if block_size > 0 else scores
+
+
+def topk(scores, n_valid, K: int, cand=None):
+    """Top-K of each row as an ascending set of positions, -1 padded: [n_rows, K] int32."""
+    dev = _dev(scores)
+    a = TopkArgs()
+    a.scores, a.cand, a.n_valid = _ptr(scores), _ptr(cand), _ptr(n_valid)
+    a.n_rows, a.L, a.K = scores.shape[0], scores.shape[1], K
+    idx = torch.empty((a.n_rows, K), dtype=torch.int32, device=dev)
+    a.idx = _ptr(idx)
+    ws, nb = _ws(int(_topk_ws(C.byref(a))), dev)
+    a.workspace, a.workspace_bytes = _ptr(ws), nb
+    _check(_topk(C.byref(a), _stream()), "csa2_topk")
+    return idx
+
+
+def block_pool(block_max, n_visible, block_size: int, n_keep: int):
+    """Hierarchical pool: ([n_rows, n_keep*block_size] ascending positions -1 padded, [n_rows] sizes)."""
+    dev = _dev(block_max)
+    a = BlockPoolArgs()
+    a.block_max, a.n_visible = _ptr(block_max), _ptr(n_visible)
+    a.n_rows, a.n_blocks, a.block_size, a.n_keep = block_max.shape[0], block_max.shape[1], block_size, n_keep
+    pool = torch.empty((a.n_rows, n_keep * block_size), dtype=torch.int32, device=dev)
+    n_pool = torch.empty((a.n_rows,), dtype=torch.int32, device=dev)
+    a.pool, a.n_pool = _ptr(pool), _ptr(n_pool)
+    ws, nb = _ws(int(_pool_ws(C.byref(a))), dev)
+    a.workspace, a.workspace_bytes = _ptr(ws), nb
+    _check(_block_pool(C.byref(a), _stream()), "csa2_block_pool")
+    return pool, n_pool
+
+
+def _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, K, swa, swa_scale, swa_pos0, window, sink,
+               theta, softmax_scale, out, sink_mass):
+    a = AttnArgs()
+    a.q, a.q_pos, a.seq_of_row = _ptr(q), _ptr(q_pos), _ptr(seq_of_row)
+    a.n_rows, a.n_seq, a.n_records = q.shape[0], latents.shape[0], latents.shape[1]
+    a.latents, a.lat_scale, a.lat_dtype = _ptr(latents), _ptr(lat_scale), _lat_dtype(latents, lat_scale)
+    a.idx, a.K = _ptr(idx), K
+    a.swa, a.swa_scale = _ptr(swa), _ptr(swa_scale)
+    a.swa_dtype = BF16 if swa.element_size() == 2 else FP8_E4M3_ROWSCALE
+    a.swa_rows, a.swa_pos0, a.window = swa.shape[1], _ptr(swa_pos0), window
+    a.sink, a.rope_theta, a.softmax_scale = _ptr(sink), float(theta), float(softmax_scale)
+    a.out, a.sink_mass = _ptr(out), _ptr(sink_mass)
+    return a
+
+
+def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, swa_pos0, window: int, sink,
+                theta: float = 1e4, softmax_scale: float = HEAD_DIM ** -0.5):
+    """Attention output [n_rows, 64, 512] fp32 and sink mass [n_rows, 64]."""
+    dev = _dev(q)
+    out = torch.empty((q.shape[0], HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+    sm = torch.empty((q.shape[0], HEADS), dtype=torch.float32, device=dev)
+    a = _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, idx.shape[1], swa, swa_scale, swa_pos0, window,
+                   sink, theta, softmax_scale, out, sm)
+    ws, nb = _ws(int(_attn_ws(C.byref(a))), dev)
+    a.workspace, a.workspace_bytes = _ptr(ws), nb
+    _check(_sparse_attn(C.byref(a), _stream()), "csa2_sparse_attn")
+    return out, sm
+
+
+class DecodeLayer:
+    """One prepared csa2_fused_decode call: argument struct, outputs and workspace are built
+    once, so that repeated calls (and CUDA-graph capture) only launch kernels."""
+
+    def __init__(self, mode, *, q_idx=None, w=None, k_idx=None, k_scale=None, seq_of_row, n_visible, q, q_pos,
+                 latents, lat_scale, swa, swa_scale, swa_pos0, window, sink, K=512, theta=1e4,
+                 softmax_scale=HEAD_DIM ** -0.5, block_size=64, n_keep=64, pool=None, n_pool=None, idx=None):
+        self.mode = MODES[mode] if isinstance(mode, str) else int(mode)
+        dev = _dev(q)
+        n_rows = q.shape[0]
+        self.out = torch.empty((n_rows, HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+        self.sink_mass = torch.empty((n_rows, HEADS), dtype=torch.float32, device=dev)
+        if self.mode == MODE_REUSE:
+            if idx is None:
+                raise ValueError("REUSE needs the preceding layer's idx")
+            self.idx = idx
+        else:
+            self.idx = torch.empty((n_rows, K), dtype=torch.int32, device=dev)
+        if self.mode == MODE_FULL_POOL:
+            self.pool = torch.empty((n_rows, n_keep * block_size), dtype=torch.int32, device=dev)
+            self.n_pool = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+        else:
+            self.pool, self.n_pool = pool, n_pool
+        a = DecodeArgs()
+        a.mode, a.K, a.block_size, a.n_keep = self.mode, K, block_size, n_keep
+        if self.mode != MODE_REUSE:
+            a.index = _index_args(q_idx, w, k_idx, k_scale, seq_of_row, n_visible)
+        a.pool, a.n_pool = _ptr(self.pool), _ptr(self.n_pool)
+        a.pool_len = self.pool.shape[1] if self.pool is not None else 0
+        a.idx = _ptr(self.idx)
+        a.attn = _attn_args(q, q_pos, seq_of_row, latents, lat_scale, self.idx, K, swa, swa_scale, swa_pos0,
+                            window, sink, theta, softmax_scale, self.out, self.sink_mass)
+        nbytes = int(_decode_ws(C.byref(a)))
+        self._ws, a.workspace_bytes = _ws(nbytes, dev)
+        a.workspace = _ptr(self._ws)
+        self._args = a
+        self._keep = (q_idx, w, k_idx, k_scale, seq_of_row, n_visible, q, q_pos, latents, lat_scale, swa, swa_scale,
+                      swa_pos0, sink, pool, n_pool)
+
+    @property
+    def launches(self) -> int:
+        """Kernels one call launches."""
+        return int(_decode_launches(C.byref(self._args)))
+
+    def set_stage_events(self, events):
+        """Record the given torch.cuda.Event objects (up to 4, None to skip) at the stage
+        boundaries of every later call: before indexing, after the scan, after top-K merge /
+        block pool, after attention."""
+        self._events = list(events) + [None] * (4 - len(events))
+        for i, ev in enumerate(self._events[:4]):
+            if ev is not None and ev.cuda_event == 0:
+                ev.record()  # torch creates the CUDA event lazily
+            self._args.stage_events[i] = ev.cuda_event if ev is not None else None
+
+    def __call__(self):
+        _check(_fused_decode(C.byref(self._args), _stream()), "csa2_fused_decode")
+        return self.out
+
+
+def fused_decode(mode, **kw):
+    """One CSA2 decode layer; returns the DecodeLayer after running it (outputs: .out, .sink_mass,
+    .idx, .pool, .n_pool)."""
+    layer = DecodeLayer(mode, **kw)
+    layer()
+    return layer

@@ -1,0 +1,487 @@
+// The C ABI of the CSA2 attention step (include/csa2.h): host-side validation, workspace
+// layout, work decomposition and launch sequencing.  Nothing here synchronizes or allocates.
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/csa2.h"
+#include "kernels.h"
+
+namespace csa2 {
+namespace {
+
+constexpr int kScanMaxK = 512;  // per-warp survivor buffers of the fused scan fit K <= 512
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
+size_t align_up(size_t v, size_t a = 256) { return (v + a - 1) / a * a; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : dflt;
+}
+
+// Segments per row of the indexer scan (one resident block per SM): the smallest count that
+// keeps the whole grid within 5% of full waves, with at least ~4 tiles per warp.
+int scan_segments(int n_rows, long long L) {
+  const int forced = env_int("CSA2_SCAN_SEGMENTS", 0);
+  if (forced > 0) return forced;
+  const int slots = sm_count();
+  const long long cap = L / 1024;
+  if (cap <= 1 || n_rows >= slots) return 1;
+  int best = 1;
+  double best_u = 0.0;
+  for (int s = 1; s <= 64 && s <= cap; ++s) {
+    const long long ctas = (long long)n_rows * s;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double u = (double)ctas / (double)(waves * slots);
+    if (u > best_u + 1e-9) {
+      best_u = u;
+      best = s;
+    }
+    if (u >= 0.95) return s;
+  }
+  return best;
+}
+
+int attn_splits(int n_rows, int K, int window) {
+  const int forced = env_int("CSA2_ATTN_SPLITS", 0);
+  const int n_tiles = (K + window + 63) / 64;
+  if (forced > 0) return forced < n_tiles ? forced : (n_tiles > 0 ? n_tiles : 1);
+  int s = sm_count() / (n_rows > 0 ? n_rows : 1);
+  if (s > n_tiles) s = n_tiles;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : s;
+}
+
+csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ECUDA; }
+
+// ---- workspace carving
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = align_up(off + count * sizeof(T));
+    return p;
+  }
+};
+
+// ------------------------------------------------------------------ index validation
+csa2_status check_index(const csa2_index_args* a, bool need_outputs) {
+  if (!a) return CSA2_EINVAL;
+  if (a->n_rows < 0 || a->n_seq < 1 || a->n_records < 1 || a->n_records > (1LL << 31) - 1) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->q_idx || !a->w || !a->k_idx || !a->seq_of_row || !a->n_visible) return CSA2_EINVAL;
+  if (!aligned(a->q_idx, 16) || !aligned(a->k_idx, 16) || !aligned(a->w, 4)) return CSA2_EINVAL;
+  if (a->k_dtype != CSA2_BF16 && a->k_dtype != CSA2_FP8_E4M3_ROWSCALE) return CSA2_EINVAL;
+  if (a->k_dtype == CSA2_FP8_E4M3_ROWSCALE && (!a->k_scale || !aligned(a->k_scale, 4))) return CSA2_EINVAL;
+  if (a->cand) {
+    if (!a->n_cand || a->L < 1 || a->L > (1LL << 31) - 1) return CSA2_EINVAL;
+  }
+  if (need_outputs && !a->scores && !a->block_max) return CSA2_EINVAL;
+  if (a->block_max) {
+    if (a->cand) return CSA2_EINVAL;
+    if (!pow2(a->block_size) || a->block_size < 16 || a->block_size > 4096) return CSA2_EUNSUPPORTED;
+  }
+  return CSA2_OK;
+}
+
+ScanParams scan_params(const csa2_index_args* a) {
+  ScanParams p{};
+  p.q_idx = a->q_idx;
+  p.w = a->w;
+  p.k_idx = a->k_idx;
+  p.k_scale = a->k_scale;
+  p.N = a->n_records;
+  p.seq_of_row = a->seq_of_row;
+  p.n_visible = a->n_visible;
+  p.cand = a->cand;
+  p.n_cand = a->n_cand;
+  p.cand_stride = a->cand ? a->L : 0;
+  p.n_rows = a->n_rows;
+  p.unit = 16;
+  return p;
+}
+
+// ------------------------------------------------------------------ attention validation
+csa2_status check_attn(const csa2_attn_args* a, bool need_idx) {
+  if (!a) return CSA2_EINVAL;
+  if (a->n_rows < 0 || a->n_seq < 1 || a->n_records < 1 || a->n_records > (1LL << 31) - 1) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->q || !a->q_pos || !a->seq_of_row || !a->sink || !a->out || !a->swa_pos0) return CSA2_EINVAL;
+  if (a->K < 0 || a->K > CSA2_MAX_TOPK || a->window < 0 || a->window > 1024) return CSA2_EUNSUPPORTED;
+  if (a->K + a->window < 1) return CSA2_EINVAL;
+  if (a->K > 0 && (!a->latents || (need_idx && !a->idx))) return CSA2_EINVAL;
+  if (!aligned(a->q, 16) || !aligned(a->out, 16) || (a->latents && !aligned(a->latents, 16))) return CSA2_EINVAL;
+  if (a->lat_dtype == CSA2_FP4_E2M1_G32 || a->lat_dtype == CSA2_FP4_E2M1_G16) {
+    if (a->K > 0 && !a->lat_scale) return CSA2_EINVAL;
+  } else if (a->lat_dtype != CSA2_BF16) {
+    return CSA2_EINVAL;
+  }
+  if (a->window > 0) {
+    if (!a->swa || !aligned(a->swa, 16) || a->swa_rows < 1) return CSA2_EINVAL;
+    if (a->swa_dtype == CSA2_FP8_E4M3_ROWSCALE) {
+      if (!a->swa_scale) return CSA2_EINVAL;
+    } else if (a->swa_dtype != CSA2_BF16) {
+      return CSA2_EINVAL;
+    }
+  }
+  if (!(a->rope_theta > 0.f)) return CSA2_EINVAL;
+  return CSA2_OK;
+}
+
+AttnParams attn_params(const csa2_attn_args* a, const int32_t* idx) {
+  AttnParams p{};
+  p.q = a->q;
+  p.q_pos = a->q_pos;
+  p.seq_of_row = a->seq_of_row;
+  p.n_rows = a->n_rows;
+  p.N = a->n_records;
+  p.lat = a->latents;
+  p.lat_scale = a->lat_scale;
+  p.lat_fmt = a->lat_dtype;
+  p.idx = idx;
+  p.K = a->K;
+  p.swa = a->swa;
+  p.swa_scale = a->swa_scale;
+  p.swa_fmt = a->swa_dtype;
+  p.swa_rows = a->swa_rows;
+  p.swa_pos0 = a->swa_pos0;
+  p.window = a->window;
+  p.sink = a->sink;
+  p.theta = a->rope_theta;
+  p.scale = a->softmax_scale;
+  p.out = a->out;
+  p.sink_mass = a->sink_mass;
+  p.dev_status = a->dev_status;
+  return p;
+}
+
+size_t attn_workspace(const csa2_attn_args* a, int n_split) {
+  if (n_split <= 1) return 0;
+  return align_up((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM * 4) +
+         align_up((size_t)a->n_rows * n_split * CSA2_HEADS * 2 * 4);
+}
+
+csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, cudaStream_t s) {
+  const int n_split = attn_splits(a->n_rows, a->K, a->window);
+  AttnParams p = attn_params(a, idx);
+  if (n_split > 1) {
+    Carve c{ws};
+    p.part_o = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM);
+    p.part_ml = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * 2);
+  }
+  return cuda_status(launch_sparse_attn(p, n_split, s));
+}
+
+// ------------------------------------------------------------------ top-K plumbing
+struct TopkPlan {
+  int n_seg;
+};
+
+TopkPlan topk_plan(int n_rows, long long L) {
+  TopkPlan t{1};
+  const int slots = sm_count();
+  if (n_rows < slots) {
+    long long s = slots / (n_rows > 0 ? n_rows : 1);
+    const long long by_len = (L + 8191) / 8192;
+    if (s > by_len) s = by_len;
+    if (s > 64) s = 64;
+    t.n_seg = s < 1 ? 1 : (int)s;
+  }
+  return t;
+}
+
+size_t lists_bytes(int n_rows, int n_seg, int K) {
+  if (n_seg <= 1) return 0;
+  return 2 * align_up((size_t)n_rows * n_seg * K * 4) + align_up((size_t)n_rows * n_seg * 4);
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+const char* csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_EINVAL: return "invalid argument";
+    case CSA2_EUNSUPPORTED: return "unsupported size or format";
+    case CSA2_ECUDA: return "CUDA launch or runtime error";
+    case CSA2_ETIMEOUT: return "device-side wait timed out";
+    case CSA2_EWORKSPACE: return "workspace missing or too small";
+    case CSA2_EDEVICE_INDEX: return "device index out of range";
+  }
+  return "unknown status";
+}
+
+int32_t csa2_version(void) { return 0x000100; }
+
+csa2_status csa2_read_device_status(const int32_t* dev_status, int32_t* host_out, void* stream) {
+  if (!dev_status || !host_out) return CSA2_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CSA2_ECUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? CSA2_OK : CSA2_ECUDA;
+}
+
+// ---------------------------------------------------------------------- index scores
+csa2_status csa2_index_scores(const csa2_index_args* a, void* stream) {
+  csa2_status st = check_index(a, true);
+  if (st != CSA2_OK || a->n_rows == 0) return st;
+  ScanParams p = scan_params(a);
+  const long long L = a->cand ? a->L : a->n_records;
+  p.scores = a->scores;
+  p.scores_stride = L;
+  p.scores_len = L;
+  if (a->block_max) {
+    p.block_max = a->block_max;
+    p.n_blocks = (a->n_records + a->block_size - 1) / a->block_size;
+    p.bmax_stride = p.n_blocks;
+    p.unit = a->block_size;
+  }
+  p.K = 0;
+  const int n_seg = scan_segments(a->n_rows, L);
+  return cuda_status(launch_index_scan(p, a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->cand != nullptr, n_seg,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------- top-K
+size_t csa2_topk_workspace_size(const csa2_topk_args* a) {
+  if (!a || a->n_rows <= 0 || a->K < 1) return 0;
+  const TopkPlan t = topk_plan(a->n_rows, a->L);
+  return lists_bytes(a->n_rows, t.n_seg, a->K);
+}
+
+csa2_status csa2_topk(const csa2_topk_args* a, void* stream) {
+  if (!a || a->n_rows < 0) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->scores || !a->n_valid || !a->idx || a->L < 1 || a->L > (1LL << 24)) return CSA2_EINVAL;
+  if (a->K < 1 || a->K > CSA2_MAX_TOPK) return CSA2_EUNSUPPORTED;
+  const size_t need = csa2_topk_workspace_size(a);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need)) return CSA2_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const TopkPlan t = topk_plan(a->n_rows, a->L);
+  FeedParams f{};
+  f.n_rows = a->n_rows;
+  f.K = a->K;
+  f.scores = a->scores;
+  f.scores_stride = a->L;
+  f.n_valid = a->n_valid;
+  f.valid_div = 1;
+  f.cand = a->cand;
+  f.cand_stride = a->L;
+  if (t.n_seg == 1) {
+    f.idx = a->idx;
+    return cuda_status(launch_topk_feed(f, false, 1, s));
+  }
+  Carve c{static_cast<uint8_t*>(a->workspace)};
+  f.out_keys = c.take<uint32_t>((size_t)a->n_rows * t.n_seg * a->K);
+  f.out_pos = c.take<int32_t>((size_t)a->n_rows * t.n_seg * a->K);
+  f.out_cnt = c.take<int32_t>((size_t)a->n_rows * t.n_seg);
+  cudaError_t e = launch_topk_feed(f, false, t.n_seg, s);
+  if (e != cudaSuccess) return CSA2_ECUDA;
+  FeedParams m{};
+  m.n_rows = a->n_rows;
+  m.K = a->K;
+  m.in_keys = f.out_keys;
+  m.in_pos = f.out_pos;
+  m.in_cnt = f.out_cnt;
+  m.in_seg = t.n_seg;
+  m.in_K = a->K;
+  m.idx = a->idx;
+  return cuda_status(launch_topk_feed(m, true, 1, s));
+}
+
+// ---------------------------------------------------------------------- block pool
+static size_t block_pool_ws(int n_rows, int n_keep) { return align_up((size_t)n_rows * n_keep * 4); }
+
+size_t csa2_block_pool_workspace_size(const csa2_block_pool_args* a) {
+  if (!a || a->n_rows <= 0 || a->n_keep < 1) return 0;
+  return block_pool_ws(a->n_rows, a->n_keep);
+}
+
+csa2_status csa2_block_pool(const csa2_block_pool_args* a, void* stream) {
+  if (!a || a->n_rows < 0) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->block_max || !a->n_visible || !a->pool || !a->n_pool || a->n_blocks < 1) return CSA2_EINVAL;
+  if (a->block_size < 1 || a->block_size > 4096 || a->n_keep < 1) return CSA2_EINVAL;
+  if (a->n_keep > CSA2_MAX_TOPK || (long long)a->n_keep * a->block_size > (1LL << 20)) return CSA2_EUNSUPPORTED;
+  const size_t need = csa2_block_pool_workspace_size(a);
+  if (!a->workspace || a->workspace_bytes < need) return CSA2_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* kept = static_cast<int32_t*>(a->workspace);
+  FeedParams f{};
+  f.n_rows = a->n_rows;
+  f.K = a->n_keep;
+  f.scores = a->block_max;
+  f.scores_stride = a->n_blocks;
+  f.n_valid = a->n_visible;
+  f.valid_div = a->block_size;
+  f.idx = kept;
+  cudaError_t e = launch_topk_feed(f, false, 1, s);
+  if (e != cudaSuccess) return CSA2_ECUDA;
+  return cuda_status(launch_pool_expand(kept, a->n_visible, a->n_rows, a->n_keep, a->block_size, a->pool,
+                                        a->n_pool, s));
+}
+
+// ---------------------------------------------------------------------- sparse attention
+size_t csa2_sparse_attn_workspace_size(const csa2_attn_args* a) {
+  if (!a || a->n_rows <= 0) return 0;
+  return attn_workspace(a, attn_splits(a->n_rows, a->K, a->window));
+}
+
+csa2_status csa2_sparse_attn(const csa2_attn_args* a, void* stream) {
+  csa2_status st = check_attn(a, true);
+  if (st != CSA2_OK || a->n_rows == 0) return st;
+  const size_t need = csa2_sparse_attn_workspace_size(a);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need)) return CSA2_EWORKSPACE;
+  return run_attn(a, a->idx, static_cast<uint8_t*>(a->workspace), static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------- fused decode layer
+// Workspace: [segment lists | block maxima | kept blocks | attention partials]
+static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
+  const csa2_index_args* ix = &a->index;
+  const int n_rows = a->attn.n_rows;
+  size_t ws = 0;
+  int n_seg = 1;
+  if (a->mode != CSA2_MODE_REUSE) {
+    const long long L = a->mode == CSA2_MODE_REINDEX ? a->pool_len : ix->n_records;
+    n_seg = scan_segments(n_rows, L);
+    ws += lists_bytes(n_rows, n_seg, a->K);
+    if (a->mode == CSA2_MODE_FULL_POOL) {
+      const long long nb = (ix->n_records + a->block_size - 1) / a->block_size;
+      ws += align_up((size_t)n_rows * nb * 4) + align_up((size_t)n_rows * a->n_keep * 4);
+    }
+  }
+  ws += attn_workspace(&a->attn, attn_splits(n_rows, a->K, a->attn.window));
+  if (n_seg_out) *n_seg_out = n_seg;
+  return ws;
+}
+
+size_t csa2_fused_decode_workspace_size(const csa2_decode_args* a) {
+  if (!a || a->attn.n_rows <= 0 || a->K < 1) return 0;
+  return decode_ws(a, nullptr);
+}
+
+csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
+  if (!a) return CSA2_EINVAL;
+  if (a->mode < CSA2_MODE_FULL || a->mode > CSA2_MODE_REUSE) return CSA2_EINVAL;
+  if (a->K < 1 || a->K > kScanMaxK) return CSA2_EUNSUPPORTED;
+  if (!a->idx) return CSA2_EINVAL;
+  csa2_attn_args at = a->attn;
+  at.K = a->K;
+  csa2_status st = check_attn(&at, false);
+  if (st != CSA2_OK || at.n_rows == 0) return st;
+  const csa2_index_args* ix = &a->index;
+  if (a->mode != CSA2_MODE_REUSE) {
+    csa2_index_args ic = *ix;
+    ic.cand = nullptr;
+    ic.scores = nullptr;
+    ic.block_max = nullptr;
+    st = check_index(&ic, false);
+    if (st != CSA2_OK) return st;
+    if (ix->n_rows != at.n_rows || ix->n_records != at.n_records) return CSA2_EINVAL;
+  }
+  if (a->mode == CSA2_MODE_FULL_POOL) {
+    if (!pow2(a->block_size) || a->block_size < 16 || a->block_size > 4096) return CSA2_EUNSUPPORTED;
+    if (a->n_keep < 1 || a->n_keep > CSA2_MAX_TOPK) return CSA2_EUNSUPPORTED;
+    if (a->pool_len != a->n_keep * a->block_size || !a->pool || !a->n_pool) return CSA2_EINVAL;
+  }
+  if (a->mode == CSA2_MODE_REINDEX && (!a->pool || !a->n_pool || a->pool_len < 1)) return CSA2_EINVAL;
+  int n_seg = 1;
+  const size_t need = decode_ws(a, &n_seg);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need)) return CSA2_EWORKSPACE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n_rows = at.n_rows;
+  Carve c{static_cast<uint8_t*>(a->workspace)};
+  cudaError_t e = cudaSuccess;
+  auto mark = [&](int i) {
+    if (a->stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(a->stage_events[i]), s);
+  };
+  mark(0);
+  if (a->mode != CSA2_MODE_REUSE) {
+    ScanParams p = scan_params(ix);
+    p.K = a->K;
+    p.idx = a->idx;
+    if (n_seg > 1) {
+      p.seg_keys = c.take<uint32_t>((size_t)n_rows * n_seg * a->K);
+      p.seg_pos = c.take<int32_t>((size_t)n_rows * n_seg * a->K);
+      p.seg_cnt = c.take<int32_t>((size_t)n_rows * n_seg);
+    }
+    int32_t* kept = nullptr;
+    if (a->mode == CSA2_MODE_FULL_POOL) {
+      p.n_blocks = (ix->n_records + a->block_size - 1) / a->block_size;
+      p.bmax_stride = p.n_blocks;
+      p.block_max = c.take<float>((size_t)n_rows * p.n_blocks);
+      p.unit = a->block_size;
+      kept = c.take<int32_t>((size_t)n_rows * a->n_keep);
+    }
+    if (a->mode == CSA2_MODE_REINDEX) {
+      p.cand = a->pool;
+      p.n_cand = a->n_pool;
+      p.cand_stride = a->pool_len;
+    }
+    e = launch_index_scan(p, ix->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->mode == CSA2_MODE_REINDEX, n_seg, s);
+    if (e != cudaSuccess) return CSA2_ECUDA;
+    mark(1);
+    if (n_seg > 1) {
+      FeedParams m{};
+      m.n_rows = n_rows;
+      m.K = a->K;
+      m.in_keys = p.seg_keys;
+      m.in_pos = p.seg_pos;
+      m.in_cnt = p.seg_cnt;
+      m.in_seg = n_seg;
+      m.in_K = a->K;
+      m.idx = a->idx;
+      e = launch_topk_feed(m, true, 1, s);
+      if (e != cudaSuccess) return CSA2_ECUDA;
+    }
+    if (a->mode == CSA2_MODE_FULL_POOL) {
+      FeedParams f{};
+      f.n_rows = n_rows;
+      f.K = a->n_keep;
+      f.scores = p.block_max;
+      f.scores_stride = p.n_blocks;
+      f.n_valid = ix->n_visible;
+      f.valid_div = a->block_size;
+      f.idx = kept;
+      e = launch_topk_feed(f, false, 1, s);
+      if (e != cudaSuccess) return CSA2_ECUDA;
+      e = launch_pool_expand(kept, ix->n_visible, n_rows, a->n_keep, a->block_size, a->pool, a->n_pool, s);
+      if (e != cudaSuccess) return CSA2_ECUDA;
+    }
+  }
+  mark(2);
+  st = run_attn(&at, a->idx, static_cast<uint8_t*>(a->workspace) + c.off, s);
+  mark(3);
+  return st;
+}
+
+int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
+  if (!a || a->attn.n_rows <= 0) return 0;
+  int n_seg = 1;
+  decode_ws(a, &n_seg);
+  int n = 0;
+  if (a->mode != CSA2_MODE_REUSE) {
+    n += 1 + (n_seg > 1 ? 1 : 0);
+    if (a->mode == CSA2_MODE_FULL_POOL) n += 2;
+  }
+  n += 1 + (attn_splits(a->attn.n_rows, a->K, a->attn.window) > 1 ? 1 : 0);
+  return n;
+}
+
+}  // extern "C"

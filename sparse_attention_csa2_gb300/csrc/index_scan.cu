@@ -1,0 +1,291 @@
+// Lightning-indexer scan for decode rows: score_j = sum_h w_h * ReLU(q^I_h . k^I_j)
+// ("Every layer, connected", "The global and index paths"), fused with the causal mask,
+// block maxima for the hierarchical pool and an exact per-segment top-K.
+//
+// One thread block (16 warps) handles one segment of one query row.  Each warp streams its
+// own contiguous range of 16-record tiles through a private cp.async ring in shared memory
+// (every thread reads back only the bytes it copied, so no block barrier is needed in the
+// hot loop) and multiplies them on the tensor cores with warp-level bf16 MMA:
+//   M = 16 records, N = 8 indexer heads (x4 tiles = 32 heads), K = 128 dims (8 steps).
+// The indexer query is held in registers as B fragments for the whole scan.  The 128 dims
+// are consumed in a permuted order chosen so that each thread's 16-byte copies are the
+// exact A-fragment words it needs; q uses the same permutation, so the dot products are
+// unchanged.  FP8 keys are widened to bf16 in registers (exact) and their row scale is
+// applied to each head's dot product before the ReLU.
+#include "select.cuh"
+#include "kernels.h"
+
+namespace csa2 {
+
+namespace {
+
+constexpr int kScanWarps = 16;
+constexpr int kScanThreads = kScanWarps * 32;
+constexpr int kRoundTiles = kRoundEntries / 16;  // 8 tiles of 16 records between checks
+
+template <bool FP8>
+struct ScanCfg {
+  static constexpr int kRowBytes = FP8 ? 128 : 256;  // bytes of one indexer key
+  static constexpr int kStageBytes = 16 * kRowBytes;  // one 16-record tile
+  static constexpr int kStages = FP8 ? 4 : 2;
+  static constexpr int kRingBytes = kScanWarps * kStages * kStageBytes;
+};
+
+// Index (in 32-bit words of a 128-dim bf16 row) of the q^I pair that meets A-fragment word
+// `hi` (0 = k-lo pair, 1 = k-hi pair) of k-step s for the thread with c = lane % 4.
+template <bool FP8>
+__device__ __forceinline__ int q_word(int s, int c, int hi) {
+  if (FP8) {
+    // 16-byte chunk (4*(s/4) + c) of the 128-byte FP8 row holds 16 dims; k-step s uses its
+    // word s%4: dims 16*chunk + 4*(s%4) + {0,1} (lo) and {2,3} (hi).
+    const int chunk = 4 * (s >> 2) + c;
+    return 8 * chunk + 2 * (s & 3) + hi;
+  } else {
+    // 16-byte chunk u = 4*(s/2) + c of the 256-byte bf16 row holds 8 dims; k-step s uses
+    // dims 8u + 4*(s%2) + {0,1} (lo) and {2,3} (hi).
+    const int u = 4 * (s >> 1) + c;
+    return 4 * u + 2 * (s & 1) + hi;
+  }
+}
+
+template <bool FP8, bool GATHER>
+__global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanParams p) {
+  using Cfg = ScanCfg<FP8>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  SelectShared* sh = reinterpret_cast<SelectShared*>(smem + Cfg::kRingBytes);
+  TopkEngine eng;
+  eng.cap = p.K + kRoundEntries;
+  eng.keys = reinterpret_cast<uint32_t*>(smem + Cfg::kRingBytes + sizeof(SelectShared));
+  eng.pos = reinterpret_cast<int32_t*>(eng.keys + kSelWarps * eng.cap);
+  eng.sh = sh;
+
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
+  const int b = p.seq_of_row[row];
+  const long long L_row = GATHER ? min((long long)p.n_cand[row], p.cand_stride)
+                                  : min((long long)p.n_visible[row], p.N);
+
+  // ---- this warp's entry range: units of U entries split over segments, then warps
+  const int U = p.unit;
+  const long long n_units = (L_row + U - 1) / U;
+  long long u0, u1, w0, w1;
+  split_range(n_units, n_seg, seg, u0, u1);
+  split_range(u1 - u0, kScanWarps, wid, w0, w1);
+  const long long e0 = (u0 + w0) * U;
+  const long long e1 = min((u0 + w1) * U, L_row);
+  const long long tb = e0 / 16, te = (e1 + 15) / 16;
+
+  // ---- indexer query as B fragments, weights for this thread's heads
+  uint32_t qf[8][4][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q_idx) + (size_t)row * kIdxHeads * (kIdxDim / 2);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint32_t* qh = qrow + (8 * nt + g) * (kIdxDim / 2);
+        qf[s][nt][0] = __ldg(qh + q_word<FP8>(s, c, 0));
+        qf[s][nt][1] = __ldg(qh + q_word<FP8>(s, c, 1));
+      }
+  }
+  float wv[4][2];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    wv[nt][0] = __ldg(p.w + (size_t)row * kIdxHeads + 8 * nt + 2 * c);
+    wv[nt][1] = __ldg(p.w + (size_t)row * kIdxHeads + 8 * nt + 2 * c + 1);
+  }
+
+  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_idx);
+  const size_t seq_off = (size_t)b * (size_t)p.N;
+  uint8_t* my_ring = ring + (size_t)wid * Cfg::kStages * Cfg::kStageBytes;
+
+  auto record_of = [&](long long j) -> long long {
+    if (GATHER) return (long long)__ldg(p.cand + (size_t)row * p.cand_stride + j);
+    return j;
+  };
+  // Issues the copies of tile t into its ring stage (zero-fill past the warp's range).
+  auto issue = [&](long long t) {
+    uint8_t* st = my_ring + (int)(t % Cfg::kStages) * Cfg::kStageBytes;
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) {
+      const long long j = t * 16 + g + 8 * rh;
+      const bool valid = j < e1;
+      const long long rec = valid ? record_of(j) : 0;
+      const uint8_t* src = kbase + (seq_off + (size_t)rec) * Cfg::kRowBytes;
+      if (FP8) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          cp_async16(st + (2 * i + rh) * 512 + lane * 16, src + (4 * i + c) * 16, valid);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          cp_async16(st + (2 * i + rh) * 512 + lane * 16, src + (4 * i + c) * 16, valid);
+      }
+    }
+  };
+
+  const bool do_topk = p.K > 0;
+  if (do_topk) engine_init(eng);
+  int cnt = 0;
+  uint32_t thr = 0u;
+
+  // rounds: every warp runs the same number so that the block can meet between rounds
+  const long long max_tiles_w = ((u1 - u0 + kScanWarps - 1) / kScanWarps) * (U / 16) + 1;
+  const int rounds = (int)((max_tiles_w + kRoundTiles - 1) / kRoundTiles);
+
+#pragma unroll
+  for (int k = 0; k < Cfg::kStages - 1; ++k) {
+    if (tb + k < te) issue(tb + k);
+    cp_async_commit();
+  }
+
+  float bmax = -INFINITY;  // running block max (warp-uniform)
+  long long t = tb;
+  for (int r = 0; r < rounds; ++r) {
+    for (int k = 0; k < kRoundTiles; ++k, ++t) {
+      if (t < te) {
+        if (t + Cfg::kStages - 1 < te) issue(t + Cfg::kStages - 1);
+        cp_async_commit();
+        cp_async_wait<Cfg::kStages - 1>();
+        const uint8_t* st = my_ring + (int)(t % Cfg::kStages) * Cfg::kStageBytes;
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        if (FP8) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint4 r0 = *reinterpret_cast<const uint4*>(st + (2 * i) * 512 + lane * 16);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(st + (2 * i + 1) * 512 + lane * 16);
+            const uint32_t w0v[4] = {r0.x, r0.y, r0.z, r0.w};
+            const uint32_t w1v[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int jw = 0; jw < 4; ++jw) {
+              const int s = 4 * i + jw;
+              const uint32_t a0 = e4m3x2_to_bf16x2((uint16_t)(w0v[jw] & 0xffffu));
+              const uint32_t a2 = e4m3x2_to_bf16x2((uint16_t)(w0v[jw] >> 16));
+              const uint32_t a1 = e4m3x2_to_bf16x2((uint16_t)(w1v[jw] & 0xffffu));
+              const uint32_t a3 = e4m3x2_to_bf16x2((uint16_t)(w1v[jw] >> 16));
+#pragma unroll
+              for (int nt = 0; nt < 4; ++nt) mma_bf16(acc[nt], a0, a1, a2, a3, qf[s][nt][0], qf[s][nt][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 r0 = *reinterpret_cast<const uint4*>(st + (2 * i) * 512 + lane * 16);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(st + (2 * i + 1) * 512 + lane * 16);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+              mma_bf16(acc[nt], r0.x, r1.x, r0.y, r1.y, qf[2 * i][nt][0], qf[2 * i][nt][1]);
+              mma_bf16(acc[nt], r0.z, r1.z, r0.w, r1.w, qf[2 * i + 1][nt][0], qf[2 * i + 1][nt][1]);
+            }
+          }
+        }
+        // ---- epilogue: ReLU, head weights, sum over the 32 heads
+        const long long j_lo = t * 16 + g, j_hi = j_lo + 8;
+        const bool v_lo = j_lo < e1, v_hi = j_hi < e1;
+        float sc_lo = 1.f, sc_hi = 1.f;
+        long long rec_lo = j_lo, rec_hi = j_hi;
+        if (GATHER || FP8) {
+          rec_lo = v_lo ? record_of(j_lo) : 0;
+          rec_hi = v_hi ? record_of(j_hi) : 0;
+        }
+        if (FP8) {
+          sc_lo = __ldg(p.k_scale + seq_off + rec_lo);
+          sc_hi = __ldg(p.k_scale + seq_off + rec_hi);
+        }
+        float s_lo = 0.f, s_hi = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          if (FP8) {
+            s_lo = fmaf(wv[nt][0], fmaxf(acc[nt][0] * sc_lo, 0.f), s_lo);
+            s_lo = fmaf(wv[nt][1], fmaxf(acc[nt][1] * sc_lo, 0.f), s_lo);
+            s_hi = fmaf(wv[nt][0], fmaxf(acc[nt][2] * sc_hi, 0.f), s_hi);
+            s_hi = fmaf(wv[nt][1], fmaxf(acc[nt][3] * sc_hi, 0.f), s_hi);
+          } else {
+            s_lo = fmaf(wv[nt][0], fmaxf(acc[nt][0], 0.f), s_lo);
+            s_lo = fmaf(wv[nt][1], fmaxf(acc[nt][1], 0.f), s_lo);
+            s_hi = fmaf(wv[nt][0], fmaxf(acc[nt][2], 0.f), s_hi);
+            s_hi = fmaf(wv[nt][1], fmaxf(acc[nt][3], 0.f), s_hi);
+          }
+        }
+        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 1);
+        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 2);
+        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 1);
+        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
+
+        if (p.scores != nullptr && c == 0) {
+          float* so = p.scores + (size_t)row * p.scores_stride;
+          if (v_lo) so[j_lo] = s_lo;
+          if (v_hi) so[j_hi] = s_hi;
+        }
+        if (p.block_max != nullptr) {
+          // U == block_size here, so a block is bs/16 consecutive tiles of this warp
+          bmax = fmaxf(bmax, warp_max(fmaxf(v_lo ? s_lo : -INFINITY, v_hi ? s_hi : -INFINITY)));
+          const long long tile_end = t * 16 + 16;
+          if (tile_end % U == 0 || t + 1 == te) {
+            if (lane == 0) p.block_max[(size_t)row * p.bmax_stride + (t * 16) / U] = bmax;
+            bmax = -INFINITY;
+          }
+        }
+        if (do_topk) {
+          warp_append(eng, wid, cnt, thr, c == 0 && v_lo, score_key(s_lo), (int32_t)rec_lo);
+          warp_append(eng, wid, cnt, thr, c == 0 && v_hi, score_key(s_hi), (int32_t)rec_hi);
+        }
+      }
+    }
+    if (do_topk) thr = engine_round_end(eng, p.K, wid, lane, cnt);
+  }
+  cp_async_wait<0>();
+
+  // ---- entries past the candidates: -inf scores and empty blocks (last segment only)
+  if (seg == n_seg - 1) {
+    if (p.scores != nullptr)
+      for (long long j = L_row + tid; j < p.scores_len; j += kScanThreads)
+        p.scores[(size_t)row * p.scores_stride + j] = -INFINITY;
+    if (p.block_max != nullptr)
+      for (long long blk = (L_row + U - 1) / U + tid; blk < p.n_blocks; blk += kScanThreads)
+        p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
+  }
+  if (!do_topk) return;
+  if (n_seg == 1) {
+    engine_finish(eng, p.K, wid, lane, cnt, p.idx + (size_t)row * p.K, nullptr, nullptr, nullptr);
+  } else {
+    const size_t o = ((size_t)row * n_seg + seg) * p.K;
+    engine_finish(eng, p.K, wid, lane, cnt, nullptr, p.seg_keys + o, p.seg_pos + o,
+                  p.seg_cnt + (size_t)row * n_seg + seg);
+  }
+}
+
+}  // namespace
+
+size_t scan_smem_bytes(bool fp8, int K) {
+  const size_t ring = fp8 ? ScanCfg<true>::kRingBytes : ScanCfg<false>::kRingBytes;
+  size_t s = ring + sizeof(SelectShared);
+  if (K > 0) s += (size_t)kSelWarps * (K + kRoundEntries) * 8;
+  return s;
+}
+
+cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_seg, cudaStream_t stream) {
+  const size_t smem = scan_smem_bytes(fp8, p.K);
+  dim3 grid(n_seg, p.n_rows), block(kScanThreads);
+  if (p.n_rows == 0) return cudaSuccess;
+#define CSA2_LAUNCH_SCAN(F, G)                                                                         \
+  do {                                                                                                 \
+    cudaError_t e = cudaFuncSetAttribute(index_scan_kernel<F, G>,                                      \
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
+    if (e != cudaSuccess) return e;                                                                    \
+    index_scan_kernel<F, G><<<grid, block, smem, stream>>>(p);                                         \
+  } while (0)
+  if (fp8) {
+    if (gather) CSA2_LAUNCH_SCAN(true, true); else CSA2_LAUNCH_SCAN(true, false);
+  } else {
+    if (gather) CSA2_LAUNCH_SCAN(false, true); else CSA2_LAUNCH_SCAN(false, false);
+  }
+#undef CSA2_LAUNCH_SCAN
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

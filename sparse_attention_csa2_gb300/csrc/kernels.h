@@ -1,0 +1,99 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace csa2 {
+
+// Indexer scan over one query row per grid row, n_seg segments per row.
+struct ScanParams {
+  const void* q_idx;          // [n_rows, 32, 128] bf16
+  const float* w;             // [n_rows, 32]
+  const void* k_idx;          // [n_seq, N, 128] bf16 | E4M3
+  const float* k_scale;       // [n_seq, N] (FP8)
+  long long N;
+  const int32_t* seq_of_row;
+  const int32_t* n_visible;
+  const int32_t* cand;        // gather mode: [n_rows, cand_stride]
+  const int32_t* n_cand;
+  long long cand_stride;
+  int n_rows;
+  int unit;                   // entries per scheduling unit (16, or block_size with block_max)
+  float* scores;              // optional [n_rows, scores_stride]
+  long long scores_stride;
+  long long scores_len;       // columns to fill (-inf past the candidates)
+  float* block_max;           // optional [n_rows, bmax_stride]
+  long long bmax_stride;
+  long long n_blocks;
+  int K;                      // 0 = no top-K
+  int32_t* idx;               // final [n_rows, K] when n_seg == 1
+  uint32_t* seg_keys;         // [n_rows, n_seg, K] when n_seg > 1
+  int32_t* seg_pos;
+  int32_t* seg_cnt;           // [n_rows, n_seg]
+};
+
+size_t scan_smem_bytes(bool fp8, int K);
+cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_seg, cudaStream_t stream);
+
+// Streaming top-K over per-row entry streams (scores, or the lists of earlier segments).
+struct FeedParams {
+  int n_rows;
+  int K;
+  // source A: scores[row, j], j < n_valid[row]; position cand[row, j] or j
+  const float* scores;
+  long long scores_stride;
+  const int32_t* n_valid;
+  int valid_div;              // entries of row r: ceil(n_valid[r] / valid_div)
+  const int32_t* cand;
+  long long cand_stride;
+  // source B: segment lists (key, pos) [n_rows, in_seg, in_K] with counts [n_rows, in_seg]
+  const uint32_t* in_keys;
+  const int32_t* in_pos;
+  const int32_t* in_cnt;
+  int in_seg;
+  int in_K;
+  // output: final idx [n_rows, K] (out_seg == 1) or lists [n_rows, out_seg, K]
+  int32_t* idx;
+  uint32_t* out_keys;
+  int32_t* out_pos;
+  int32_t* out_cnt;
+};
+
+size_t feed_smem_bytes(int K);
+cudaError_t launch_topk_feed(const FeedParams& p, bool from_lists, int out_seg, cudaStream_t stream);
+cudaError_t launch_pool_expand(const int32_t* kept, const int32_t* n_visible, int n_rows, int n_keep,
+                               int block_size, int32_t* pool, int32_t* n_pool, cudaStream_t stream);
+
+struct AttnParams {
+  const void* q;
+  const int64_t* q_pos;
+  const int32_t* seq_of_row;
+  int n_rows;
+  long long N;
+  const void* lat;
+  const uint8_t* lat_scale;
+  int lat_fmt;
+  const int32_t* idx;
+  int K;
+  const void* swa;
+  const float* swa_scale;
+  int swa_fmt;
+  long long swa_rows;
+  const int64_t* swa_pos0;
+  int window;
+  const float* sink;
+  float theta;
+  float scale;
+  float* part_o;              // [n_rows, n_split, 64, 512]
+  float* part_ml;             // [n_rows, n_split, 64, 2]
+  float* out;
+  float* sink_mass;
+  int32_t* dev_status;        // optional: CSA2_EDEVICE_INDEX on an out-of-range record index
+};
+
+int attn_smem_bytes();
+cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream);
+
+}  // namespace csa2

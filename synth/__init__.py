@@ -237,3 +237,27 @@ def make_inputs(wl: Workload, seed: int, mode: str = "gauss") -> dict:
                   lat_group=wl.lat_group, swa_fmt=wl.swa_fmt, block_size=wl.block_size,
                   n_keep=wl.n_keep, B=B, N=N, Bq=Bq, mode=mode, seed=seed, name=wl.name)
     return dict(params=params, rows=rows, cache=cache, layers=layers)
+
+
+# ---------------------------------------------------------------- device transfer
+def _t(a, device):
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        if a.dtype == np.uint16:  # bf16 bit patterns
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.to(device, non_blocking=False)
+    return a
+
+
+def to_device(inp: dict, device="cuda") -> dict:
+    """The same bundle with every array as a torch tensor on ``device`` (bf16 bit patterns
+    become torch.bfloat16; E4M3 / E2M1 codes stay uint8)."""
+    out = {"params": dict(inp["params"])}
+    out["rows"] = {k: (_t(v, device) if isinstance(v, np.ndarray) else v) for k, v in inp["rows"].items()}
+    out["cache"] = {k: _t(v, device) for k, v in inp["cache"].items()}
+    out["layers"] = [{k: (_t(v, device) if isinstance(v, np.ndarray) else v) for k, v in lay.items()}
+                     for lay in inp["layers"]]
+    return out

@@ -1,0 +1,224 @@
+"""Parity of the CUDA library with the CPU oracle, call by call, on seeded inputs.
+
+Sizes span several tiles, segments and a ragged tail while keeping the oracle to seconds.
+Bars: selected indices and pools bit-exact (grid mode, where every score is exact in fp32,
+and whenever both sides select from the same fp32 scores); outputs within 2e-3 x RMS for
+bf16 caches and 1e-2 x RMS for FP8/FP4 caches.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from csa2_testlib import (check_idx_near_ties, gpu_group, out_tol, rel_err, score_bound, set_rows)
+
+pytestmark = pytest.mark.gpu
+
+S = pytest.importorskip("sparse_attention_csa2_gb300")
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def small(name, seed=7, mode="gauss", **kw):
+    return synth.make_inputs(synth.scaled(synth.WORKLOADS[name], **kw), seed=seed, mode=mode)
+
+
+# ------------------------------------------------------------------ index scores
+@pytest.mark.parametrize("key_fmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_index_scores(key_fmt, mode):
+    _cuda()
+    inp = small("batched_decode", seed=3, mode=mode, B=3, N=5003, key_fmt=key_fmt)
+    set_rows(inp, [5003, 4321, 37])
+    dv = synth.to_device(inp)
+    c, lay, rw = dv["cache"], dv["layers"][0], dv["rows"]
+    s, bmax = S.index_scores(lay["q_idx"], lay["w"], c["k_idx"], c["k_scale"], rw["seq_of_row"], rw["n_visible"],
+                             block_size=64)
+    s = s.cpu().numpy().astype(np.float64)
+    ref = O.index_scores_rows(inp, 0)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(s), fin)
+    if mode == "grid":
+        assert np.array_equal(s[fin], ref[fin])
+    else:
+        bound = score_bound(inp, 0)
+        assert np.all(np.abs(s - ref)[fin] <= np.repeat(bound[:, None], s.shape[1], 1)[fin])
+    bm = bmax.cpu().numpy().astype(np.float64)
+    for r in range(3):
+        nv = int(inp["rows"]["n_visible"][r])
+        ref_bm = O.block_max(s[r, :nv], 64)  # block maxima of the GPU's own scores: exact
+        assert np.array_equal(bm[r, :len(ref_bm)], ref_bm)
+        assert np.all(np.isneginf(bm[r, len(ref_bm):]))
+
+
+def test_index_scores_over_candidates():
+    _cuda()
+    inp = small("hierarchical", seed=5, mode="grid", B=2, N=3000)
+    rng = np.random.default_rng(0)
+    L = 700
+    cand = np.full((2, L), -1, np.int32)
+    n_cand = np.array([700, 333], np.int32)
+    for r in range(2):
+        cand[r, :n_cand[r]] = np.sort(rng.choice(3000, n_cand[r], replace=False))
+    dv = synth.to_device(inp)
+    c, lay, rw = dv["cache"], dv["layers"][0], dv["rows"]
+    s = S.index_scores(lay["q_idx"], lay["w"], c["k_idx"], c["k_scale"], rw["seq_of_row"], rw["n_visible"],
+                       cand=torch.from_numpy(cand).cuda(), n_cand=torch.from_numpy(n_cand).cuda())
+    ref = O.index_scores_rows(inp, 0, cand=cand.astype(np.int64), n_cand=n_cand)
+    s = s.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isfinite(s), np.isfinite(ref))
+    assert np.array_equal(s[np.isfinite(ref)], ref[np.isfinite(ref)])
+
+
+# ------------------------------------------------------------------ top-K
+@pytest.mark.parametrize("L,K", [(3001, 512), (100_003, 512), (70_000, 37), (600, 1024), (9, 4)])
+def test_topk_exact_on_seeded_scores(L, K):
+    _cuda()
+    rows = 5
+    sc = synth.integers((rows, L), 9, L % 97, -50, 50).float() / 4.0  # many ties
+    sc[1] = synth.normal((L,), 9, 1)  # no ties
+    sc[2, ::3] = -0.0
+    sc[2, 1::3] = 0.0
+    n_valid = np.array([L, L - 1, L // 2, min(K, L), 1], np.int32)
+    idx = S.topk(sc.cuda(), torch.from_numpy(n_valid).cuda(), K).cpu().numpy()
+    ref = O.topk_rows(sc.numpy().astype(np.float64), n_valid, K)
+    assert np.array_equal(idx, ref)
+
+
+def test_topk_with_candidate_map():
+    _cuda()
+    L, K = 5000, 300
+    sc = synth.integers((2, L), 4, 1, 0, 9).float()
+    cand = np.sort(np.random.default_rng(1).choice(10 ** 6, (2, L), replace=False), axis=1).astype(np.int32)
+    n_valid = np.array([L, 1234], np.int32)
+    idx = S.topk(sc.cuda(), torch.from_numpy(n_valid).cuda(), K, cand=torch.from_numpy(cand).cuda()).cpu().numpy()
+    ref = O.topk_rows(sc.numpy().astype(np.float64), n_valid, K, cand=cand)
+    assert np.array_equal(idx, ref)
+
+
+# ------------------------------------------------------------------ block pool
+@pytest.mark.parametrize("N,bs,keep", [(131_072, 64, 64), (5003, 64, 16), (1000, 16, 100), (777, 128, 3)])
+def test_block_pool(N, bs, keep):
+    _cuda()
+    rows = 3
+    sc = synth.integers((rows, N), 6, bs, -20, 20).float()
+    n_vis = np.array([N, N - 5, max(1, N // 3)], np.int32)
+    bm = np.full((rows, (N + bs - 1) // bs), -np.inf, np.float32)
+    for r in range(rows):
+        b = O.block_max(sc[r, :n_vis[r]].numpy().astype(np.float64), bs)
+        bm[r, :len(b)] = b
+    pool, n_pool = S.block_pool(torch.from_numpy(bm).cuda(), torch.from_numpy(n_vis).cuda(), bs, keep)
+    ref_pool, ref_n = O.block_pool_rows(sc.numpy().astype(np.float64), n_vis, bs, keep)
+    assert np.array_equal(n_pool.cpu().numpy(), ref_n)
+    assert np.array_equal(pool.cpu().numpy(), ref_pool)
+
+
+# ------------------------------------------------------------------ sparse attention
+@pytest.mark.parametrize("lat_fmt,group,swa_fmt", [("bf16", 32, "bf16"), ("fp4", 32, "fp8"), ("fp4", 16, "bf16")])
+def test_sparse_attn(lat_fmt, group, swa_fmt):
+    _cuda()
+    inp = small("batched_decode", seed=11, B=3, N=4000, lat_fmt=lat_fmt, lat_group=group, swa_fmt=swa_fmt)
+    set_rows(inp, [4000, 3000, 100])
+    rng = np.random.default_rng(2)
+    K = 512
+    idx = np.full((3, K), -1, np.int64)
+    for r, nv in enumerate([4000, 3000, 100]):
+        sel = np.sort(rng.choice(nv, min(K, nv), replace=False))
+        idx[r, :len(sel)] = sel
+    dv = synth.to_device(inp)
+    c, lay, rw, p = dv["cache"], dv["layers"][0], dv["rows"], dv["params"]
+    out, sm = S.sparse_attn(lay["q"], rw["q_pos"], rw["seq_of_row"], c["lat"], c["lat_scales"],
+                            torch.from_numpy(idx.astype(np.int32)).cuda(), lay["swa"], lay["swa_scale"],
+                            rw["swa_pos0"], p["W"], lay["sink"], p["theta"], p["softmax_scale"])
+    o_ref, sm_ref = O.sparse_attn_rows(inp, 0, idx)
+    err = rel_err(out.cpu().numpy(), o_ref)
+    assert err <= out_tol(inp["params"]), err
+    assert np.max(np.abs(sm.cpu().numpy() - sm_ref)) < 1e-4
+    assert np.all(sm.cpu().numpy() < 1.0)  # the sink keeps the attention mass below one
+
+
+# ------------------------------------------------------------------ fused decode layers
+@pytest.mark.parametrize("key_fmt,lat_fmt,swa_fmt", [("bf16", "bf16", "bf16"), ("fp8", "fp4", "fp8")])
+def test_fused_full_grid_exact_indices(key_fmt, lat_fmt, swa_fmt):
+    _cuda()
+    inp = small("batched_decode", seed=4, mode="grid", B=3, N=9001, key_fmt=key_fmt, lat_fmt=lat_fmt,
+                swa_fmt=swa_fmt)
+    set_rows(inp, [9001, 5000, 300])
+    g = gpu_group(synth.to_device(inp))
+    ref = O.csa2_group(inp)
+    assert np.array_equal(g[0].idx.cpu().numpy(), ref[0]["idx"])
+    assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
+
+
+def test_fused_full_gauss():
+    _cuda()
+    inp = small("batched_decode", seed=8, B=4, N=20_000)
+    set_rows(inp, [20_000, 19_999, 12_345, 513])
+    g = gpu_group(synth.to_device(inp))
+    ref = O.csa2_group(inp)
+    swaps = check_idx_near_ties(g[0].idx.cpu().numpy(), ref[0]["idx"], ref[0]["scores"], score_bound(inp, 0))
+    assert swaps == 0
+    assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
+
+
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_fused_hierarchical_group(mode):
+    _cuda()
+    inp = small("hierarchical", seed=12, mode=mode, B=2, N=9000, n_keep=16, n_hot_blocks=10)
+    set_rows(inp, [9000, 7001])
+    g = gpu_group(synth.to_device(inp))
+    ref = O.csa2_group(inp)
+    assert np.array_equal(g[0].n_pool.cpu().numpy(), ref[0]["n_pool"])
+    if mode == "grid":
+        assert np.array_equal(g[0].pool.cpu().numpy(), ref[0]["pool"])
+    for l in range(len(ref)):
+        gi = g[l].idx.cpu().numpy()
+        if mode == "grid":
+            assert np.array_equal(gi, ref[l]["idx"]), l
+        assert rel_err(g[l].out.cpu().numpy(), ref[l]["o"]) <= out_tol(inp["params"]), l
+    # Reuse layers: the same selection as the last Reindex layer, different outputs
+    assert np.array_equal(g[4].idx.cpu().numpy(), g[3].idx.cpu().numpy())
+    o4, o5 = g[4].out.cpu().numpy(), g[5].out.cpu().numpy()
+    assert np.max(np.abs(o4 - o5)) > 0.1 * np.sqrt(np.mean(o4 ** 2))
+
+
+def test_fused_decode_is_deterministic_and_causal():
+    _cuda()
+    inp = small("batched_decode", seed=21, B=2, N=6000)
+    set_rows(inp, [5000, 4000])
+    a = gpu_group(synth.to_device(inp))
+    b = gpu_group(synth.to_device(inp))
+    assert torch.equal(a[0].idx, b[0].idx) and torch.equal(a[0].out, b[0].out)
+    # records at or past n_visible do not matter
+    inp["cache"]["k_idx"][:, 5000:] = inp["cache"]["k_idx"][:, 5000:][:, ::-1]
+    inp["cache"]["lat"][:, 5000:] ^= np.uint16(0x0101)
+    c = gpu_group(synth.to_device(inp))
+    assert torch.equal(a[0].idx, c[0].idx) and torch.equal(a[0].out, c[0].out)
+    assert int(a[0].idx.max()) < 5000
+
+
+def test_decode_equals_prefill_row():
+    _cuda()
+    # a prefill chunk, and the same query rows run as decode rows with the same visibility
+    wl = synth.scaled(synth.WORKLOADS["prefill_chunk"], N=2100, T=40, P0=2060)
+    inp = synth.make_inputs(wl, seed=5)
+    ref = O.csa2_layer(inp, 0, rows=[0, 17, 39])
+    dv = synth.to_device(inp)
+    g = gpu_group(dv)
+    got = g[0].out.cpu().numpy()
+    for i, t in enumerate([0, 17, 39]):
+        assert rel_err(got[t][None], ref["o"][i][None]) <= 2e-3
+        # decode call on the single row t (batch of one, sequence 0)
+        one = {k: (v[t:t + 1] if k in ("q_pos", "n_visible", "seq_of_row") else v) for k, v in dv["rows"].items()}
+        lay = dict(dv["layers"][0])
+        for k in ("q_idx", "w", "q"):
+            lay[k] = lay[k][t:t + 1].contiguous()
+        d1 = dict(dv, rows=one, layers=[lay])
+        d1["params"] = dict(dv["params"], Bq=1)
+        g1 = gpu_group(d1)
+        assert torch.equal(g1[0].idx[0], g[0].idx[t])
+        assert rel_err(g1[0].out[0].cpu().numpy()[None], ref["o"][i][None]) <= 2e-3
