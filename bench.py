@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-iters", type=int, default=10)
     return ap.parse_args(argv)
 
 
@@ -231,6 +233,63 @@ def run_reference(args, world, rank):
     return 0
 
 
+def prefill_flops(wl) -> float:
+    """Indexer flops of a prefill chunk counting causally visible (query, record) pairs only."""
+    visible = sum(min(wl.P0 + t + 1, wl.N) for t in range(wl.T))
+    return 2.0 * wl.HI * wl.DI * visible
+
+
+def run_prefill(args, local, peaks):
+    """Prefill chunk (B=1, T=4096 queries at positions 32768.., N=36864 bf16 keys): the
+    indexer GEMM on the tensor cores alone, then the whole chunk (scores -> per-query top-512
+    -> attention with each query's window)."""
+    import torch
+    import synth
+    import sparse_attention_csa2_gb300 as S
+    wl = synth.WORKLOADS["prefill_chunk"]
+    inp = synth.make_inputs(wl, seed=4)
+    dv = synth.to_device(inp, f"cuda:{local}")
+    p, rw, c, lay = dv["params"], dv["rows"], dv["cache"], dv["layers"][0]
+    idx_call = lambda: S.index_scores(lay["q_idx"], lay["w"], c["k_idx"], c["k_scale"], rw["seq_of_row"],
+                                      rw["n_visible"])
+    for _ in range(3):
+        scores = idx_call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.prefill_iters)]
+    for e0, e1 in ev:
+        e0.record()
+        scores = idx_call()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    flops = prefill_flops(wl)
+    tflops = flops / (ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
+
+    def chunk():
+        sc = idx_call()
+        idx = S.topk(sc, rw["n_visible"], p["K"])
+        return S.sparse_attn(lay["q"], rw["q_pos"], rw["seq_of_row"], c["lat"], c["lat_scales"], idx, lay["swa"],
+                             lay["swa_scale"], rw["swa_pos0"], p["W"], lay["sink"], p["theta"], p["softmax_scale"])
+    chunk()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_chunk = 3
+    e0.record()
+    for _ in range(n_chunk):
+        chunk()
+    e1.record()
+    torch.cuda.synchronize()
+    chunk_ms = e0.elapsed_time(e1) / n_chunk
+    return {"workload": f"prefill chunk: B=1, T={wl.T} queries at positions {wl.P0}..{wl.P0 + wl.T - 1}, "
+                        f"N={wl.N} bf16 indexer keys, causal, top-{wl.K}, window {wl.W}",
+            "indexer_ms": ms, "indexer_tflops": tflops, "indexer_flops": flops,
+            "roofline": {"bound": "tensor", "kernel": "idx_mma_prefill_kernel (tcgen05, M=128 records x N=256)",
+                         "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"},
+            "chunk_ms": chunk_ms, "chunk_tokens_per_s": wl.T / (chunk_ms / 1e3)}
+
+
 def run_gb300(args, world, rank, local):
     import torch
     import torch.distributed as dist
@@ -336,6 +395,12 @@ def run_gb300(args, world, rank, local):
                 "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_avg * 1e3,
                 "source_hash": src_hash}
 
+    prefill = None
+    if not args.no_prefill:
+        del layer, dv
+        torch.cuda.empty_cache()
+        prefill = run_prefill(args, local, peaks if peak_src == "measured" else None)
+
     cpu = None
     if not args.no_cpu_baseline:
         rate, rows, secs = oracle_rate(inp, args.cpu_seconds)
@@ -357,7 +422,7 @@ def run_gb300(args, world, rank, local):
                       "step_algorithmic_bytes": step_bytes_q * wl.B,
                       "stage_ms": {"scan": statistics.mean(scan_ms), "topk_merge": statistics.mean(topk_ms),
                                    "attention": statistics.mean(attn_ms)},
-                      "launches_per_step": launches_per_step}}
+                      "launches_per_step": launches_per_step, "prefill": prefill}}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -1,5 +1,6 @@
 // The C ABI of the CSA2 attention step (include/csa2.h): host-side validation, workspace
 // layout, work decomposition and launch sequencing.  Nothing here synchronizes or allocates.
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 
@@ -27,27 +28,18 @@ int env_int(const char* name, int dflt) {
   return v ? std::atoi(v) : dflt;
 }
 
-// Segments per row of the indexer scan (one resident block per SM): the smallest count that
-// keeps the whole grid within 5% of full waves, with at least ~4 tiles per warp.
+// Segments per row of the indexer scan: one resident block per SM, one wave; every segment
+// keeps at least 4096 records so the per-segment top-K and pipeline start-up stay small.
 int scan_segments(int n_rows, long long L) {
   const int forced = env_int("CSA2_SCAN_SEGMENTS", 0);
   if (forced > 0) return forced;
   const int slots = sm_count();
-  const long long cap = L / 1024;
-  if (cap <= 1 || n_rows >= slots) return 1;
-  int best = 1;
-  double best_u = 0.0;
-  for (int s = 1; s <= 64 && s <= cap; ++s) {
-    const long long ctas = (long long)n_rows * s;
-    const long long waves = (ctas + slots - 1) / slots;
-    const double u = (double)ctas / (double)(waves * slots);
-    if (u > best_u + 1e-9) {
-      best_u = u;
-      best = s;
-    }
-    if (u >= 0.95) return s;
-  }
-  return best;
+  if (n_rows >= slots) return 1;
+  long long s = slots / (n_rows > 0 ? n_rows : 1);
+  const long long cap = L / 4096;
+  if (s > cap) s = cap;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : (int)s;
 }
 
 int attn_splits(int n_rows, int K, int window) {
@@ -61,6 +53,47 @@ int attn_splits(int n_rows, int K, int window) {
 }
 
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ECUDA; }
+
+// Which indexer kernel runs a scan: the tcgen05 kernels take bf16 keys read in place; FP8
+// keys and candidate lists (Reindex over a pool) take the warp-MMA scan.
+enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill };
+
+ScanPath scan_path(const csa2_index_args* a, bool want_topk) {
+  if (a->k_dtype != CSA2_BF16 || a->cand != nullptr || !mma_indexer_available()) return ScanPath::kWarpMma;
+  if (!want_topk && a->block_max == nullptr && a->n_seq == 1 && a->n_rows >= 64) return ScanPath::kTc05Prefill;
+  return ScanPath::kTc05Decode;
+}
+
+// Segments per row for the tcgen05 decode scan: whole waves of resident blocks, each
+// segment's blocks (for the block maxima) within the kernel's shared-memory table.
+int tc05_segments(int n_rows, long long L, int unit) {
+  int n = scan_segments(n_rows, L);
+  const long long units = (L + unit - 1) / unit;
+  const int max_blocks = mma_decode_max_seg_blocks();
+  while ((units + n - 1) / n > max_blocks) ++n;
+  return n;
+}
+
+cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk, int n_seg, cudaStream_t s) {
+  switch (scan_path(a, want_topk)) {
+    case ScanPath::kTc05Prefill: {
+      // work items: (8-query tile, share of its key tiles); enough items to balance the
+      // persistent grid, none shorter than ~16 key tiles
+      const int n_qt = (p.n_rows + 7) / 8;
+      const int ctas = sm_count();
+      const long long tiles = (a->n_records + 127) / 128;
+      int parts = 1;
+      while (n_qt * parts < 6 * ctas && tiles / (2 * parts) >= 16 && parts < 64) parts *= 2;
+      return launch_mma_prefill(p, ctas, parts, s);
+    }
+    case ScanPath::kTc05Decode: {
+      const int seg_blocks = p.block_max ? (int)(((a->n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg) : 0;
+      return launch_mma_decode(p, (long long)a->n_seq * a->n_records, n_seg, seg_blocks, s);
+    }
+    default:
+      return launch_index_scan(p, a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->cand != nullptr, n_seg, s);
+  }
+}
 
 // ---- workspace carving
 struct Carve {
@@ -159,6 +192,8 @@ AttnParams attn_params(const csa2_attn_args* a, const int32_t* idx) {
   p.sink = a->sink;
   p.theta = a->rope_theta;
   p.scale = a->softmax_scale;
+  for (int i = 0; i < CSA2_ROPE_DIM / 2; ++i)
+    p.inv_freq[i] = std::pow((double)a->rope_theta, -2.0 * i / (double)CSA2_ROPE_DIM);
   p.out = a->out;
   p.sink_mass = a->sink_mass;
   p.dev_status = a->dev_status;
@@ -202,7 +237,7 @@ TopkPlan topk_plan(int n_rows, long long L) {
 
 size_t lists_bytes(int n_rows, int n_seg, int K) {
   if (n_seg <= 1) return 0;
-  return 2 * align_up((size_t)n_rows * n_seg * K * 4) + align_up((size_t)n_rows * n_seg * 4);
+  return 2 * align_up((size_t)n_rows * n_seg * K * 4) + 2 * align_up((size_t)n_rows * n_seg * 4);
 }
 
 }  // namespace
@@ -251,9 +286,10 @@ csa2_status csa2_index_scores(const csa2_index_args* a, void* stream) {
     p.unit = a->block_size;
   }
   p.K = 0;
-  const int n_seg = scan_segments(a->n_rows, L);
-  return cuda_status(launch_index_scan(p, a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->cand != nullptr, n_seg,
-                                       static_cast<cudaStream_t>(stream)));
+  const ScanPath path = scan_path(a, false);
+  if (path == ScanPath::kTc05Decode && !a->block_max) p.unit = 128;
+  const int n_seg = path == ScanPath::kTc05Decode ? tc05_segments(a->n_rows, L, p.unit) : scan_segments(a->n_rows, L);
+  return cuda_status(launch_scan(p, a, false, n_seg, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------------- top-K
@@ -289,6 +325,7 @@ csa2_status csa2_topk(const csa2_topk_args* a, void* stream) {
   f.out_keys = c.take<uint32_t>((size_t)a->n_rows * t.n_seg * a->K);
   f.out_pos = c.take<int32_t>((size_t)a->n_rows * t.n_seg * a->K);
   f.out_cnt = c.take<int32_t>((size_t)a->n_rows * t.n_seg);
+  f.out_thr = c.take<uint32_t>((size_t)a->n_rows * t.n_seg);
   cudaError_t e = launch_topk_feed(f, false, t.n_seg, s);
   if (e != cudaSuccess) return CSA2_ECUDA;
   FeedParams m{};
@@ -297,6 +334,7 @@ csa2_status csa2_topk(const csa2_topk_args* a, void* stream) {
   m.in_keys = f.out_keys;
   m.in_pos = f.out_pos;
   m.in_cnt = f.out_cnt;
+  m.in_thr = f.out_thr;
   m.in_seg = t.n_seg;
   m.in_K = a->K;
   m.idx = a->idx;
@@ -358,7 +396,13 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
   int n_seg = 1;
   if (a->mode != CSA2_MODE_REUSE) {
     const long long L = a->mode == CSA2_MODE_REINDEX ? a->pool_len : ix->n_records;
-    n_seg = scan_segments(n_rows, L);
+    csa2_index_args ic = *ix;
+    ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
+    ic.block_max = nullptr;
+    if (scan_path(&ic, true) == ScanPath::kTc05Decode)
+      n_seg = tc05_segments(n_rows, L, a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128);
+    else
+      n_seg = scan_segments(n_rows, L);
     ws += lists_bytes(n_rows, n_seg, a->K);
     if (a->mode == CSA2_MODE_FULL_POOL) {
       const long long nb = (ix->n_records + a->block_size - 1) / a->block_size;
@@ -420,6 +464,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       p.seg_keys = c.take<uint32_t>((size_t)n_rows * n_seg * a->K);
       p.seg_pos = c.take<int32_t>((size_t)n_rows * n_seg * a->K);
       p.seg_cnt = c.take<int32_t>((size_t)n_rows * n_seg);
+      p.seg_thr = c.take<uint32_t>((size_t)n_rows * n_seg);
     }
     int32_t* kept = nullptr;
     if (a->mode == CSA2_MODE_FULL_POOL) {
@@ -429,12 +474,19 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       p.unit = a->block_size;
       kept = c.take<int32_t>((size_t)n_rows * a->n_keep);
     }
+    csa2_index_args ic = *ix;
+    ic.cand = nullptr;
+    ic.block_max = nullptr;
     if (a->mode == CSA2_MODE_REINDEX) {
       p.cand = a->pool;
       p.n_cand = a->n_pool;
       p.cand_stride = a->pool_len;
+      ic.cand = a->pool;
+      ic.L = a->pool_len;
     }
-    e = launch_index_scan(p, ix->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->mode == CSA2_MODE_REINDEX, n_seg, s);
+    if (scan_path(&ic, true) == ScanPath::kTc05Decode && a->mode != CSA2_MODE_FULL_POOL) p.unit = 128;
+    p.dev_status = at.dev_status;
+    e = launch_scan(p, &ic, true, n_seg, s);
     if (e != cudaSuccess) return CSA2_ECUDA;
     mark(1);
     if (n_seg > 1) {
@@ -444,6 +496,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       m.in_keys = p.seg_keys;
       m.in_pos = p.seg_pos;
       m.in_cnt = p.seg_cnt;
+      m.in_thr = p.seg_thr;
       m.in_seg = n_seg;
       m.in_K = a->K;
       m.idx = a->idx;

@@ -58,15 +58,22 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return (code & 0x80u) ? -mag : mag;
 }
 
-// Rotary angles of position `pos` (computed in double: positions reach 2^20 and more).
-__device__ __forceinline__ void rope_table(float* cs, long long pos, float theta, float sign) {
+// cos and sin of the rotary angle sign * pos * inv_freq.  The angle (up to ~2^31 rad) is
+// formed and reduced modulo 2*pi in double (Cody-Waite with a two-part 2*pi), then the
+// reduced angle (|r| <= pi) goes through single-precision sincosf.
+__device__ __forceinline__ void rope_cs(long long pos, double inv_freq, float sign, float* c, float* s) {
+  const double a = (double)pos * inv_freq;
+  const double k = rint(a * 0.15915494309189535);  // 1 / (2 pi)
+  double r = fma(-k, 6.283185307179586, a);
+  r = fma(-k, 2.4492935982947064e-16, r);
+  sincosf(sign * (float)r, s, c);
+}
+
+// Rotary cos/sin table of one position: cs[i] = cos, cs[32 + i] = sin.
+__device__ __forceinline__ void rope_table(float* cs, const AttnParams& p, long long pos, float sign) {
   if (threadIdx.x < kRopeDim / 2) {
     const int i = threadIdx.x;
-    const double a = (double)sign * (double)pos * pow((double)theta, -2.0 * i / (double)kRopeDim);
-    double s, c;
-    sincos(a, &s, &c);
-    cs[i] = (float)c;
-    cs[kRopeDim / 2 + i] = (float)s;
+    rope_cs(pos, p.inv_freq[i], sign, &cs[i], &cs[kRopeDim / 2 + i]);
   }
 }
 
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_split_kernel(const AttnP
   const int t0 = (int)(((long long)n_tiles * split) / n_split);
   const int t1 = (int)(((long long)n_tiles * (split + 1)) / n_split);
 
-  rope_table(sm.cs, qp, p.theta, 1.f);
+  rope_table(sm.cs, p, qp, 1.f);
   if (t0 < t1) load_tile(p, sm, KV, 0, row, b, qp, lo, pos0, t0);
   cp_async_commit();
   __syncthreads();
@@ -380,7 +387,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_split_kernel(const AttnP
       if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + tid] = __expf(sk - M) / den;
     }
     __syncthreads();
-    rope_table(sm.cs, qp, p.theta, -1.f);
+    rope_table(sm.cs, p, qp, -1.f);
     __syncthreads();
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
@@ -427,55 +434,79 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_split_kernel(const AttnP
   }
 }
 
-// Merges the splits of one row for 8 heads: log-sum-exp over splits plus the sink,
-// normalisation, inverse RoPE on dims 448..511.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p, int n_split) {
-  __shared__ float cs[kRopeDim];
-  __shared__ float fac[8][64];  // per head: weight of each split (n_split <= 64)
-  __shared__ float den_s[8];
-  const int row = blockIdx.x, h0 = blockIdx.y * 8;
+// Merges the splits of one row for 4 heads: log-sum-exp over splits plus the sink,
+// normalisation, inverse RoPE on dims 448..511.  Thread -> (head h0 + tid/32, 16 dims).
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int n_split) {
+  __shared__ float fac[4][64];  // per head: weight of each split (n_split <= 64)
+  __shared__ float inv_den[4];
+  const int row = blockIdx.x, hl = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 4 + hl;
   const long long qp = p.q_pos[row];
-  rope_table(cs, qp, p.theta, -1.f);
-  if (threadIdx.x < 8) {
-    const int h = h0 + threadIdx.x;
+  {
+    // warp hl: per-split statistics of head h, two splits per lane
     const float sk = __ldg(p.sink + h);
-    float M = sk;
-    for (int s = 0; s < n_split; ++s)
-      M = fmaxf(M, p.part_ml[(((size_t)row * n_split + s) * kHeads + h) * 2]);
-    float den = __expf(sk - M);
-    for (int s = 0; s < n_split; ++s) {
-      const float m = p.part_ml[(((size_t)row * n_split + s) * kHeads + h) * 2];
-      const float l = p.part_ml[(((size_t)row * n_split + s) * kHeads + h) * 2 + 1];
-      const float f = m == -INFINITY ? 0.f : __expf(m - M);
-      fac[threadIdx.x][s] = f;
-      den += l * f;
+    float m[2], l[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int s = lane + 32 * k;
+      m[k] = -INFINITY;
+      l[k] = 0.f;
+      if (s < n_split) {
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (((size_t)row * n_split + s) * kHeads + h) * 2);
+        m[k] = ml.x;
+        l[k] = ml.y;
+      }
     }
-    den_s[threadIdx.x] = den;
-    if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + h] = __expf(sk - M) / den;
+    const float M = fmaxf(warp_max(fmaxf(m[0], m[1])), sk);
+    float f[2], den = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      f[k] = m[k] == -INFINITY ? 0.f : __expf(m[k] - M);
+      den += l[k] * f[k];
+      const int s = lane + 32 * k;
+      if (s < n_split) fac[hl][s] = f[k];
+    }
+    den = warp_sum(den) + __expf(sk - M);
+    if (lane == 0) {
+      inv_den[hl] = 1.f / den;
+      if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + h] = __expf(sk - M) / den;
+    }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 8 * kHeadDim / 2; i += blockDim.x) {
-    const int hl = i / (kHeadDim / 2), d = 2 * (i % (kHeadDim / 2));
-    const int h = h0 + hl;
-    float x = 0.f, y = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      const float2 v = *reinterpret_cast<const float2*>(
-          p.part_o + (((size_t)row * n_split + s) * kHeads + h) * kHeadDim + d);
-      const float f = fac[hl][s];
-      x = fmaf(f, v.x, x);
-      y = fmaf(f, v.y, y);
+  const int d0 = lane * 16;
+  float4 acc[4] = {};
+  const float* base = p.part_o + ((size_t)row * n_split * kHeads + h) * kHeadDim + d0;
+  const size_t split_stride = (size_t)kHeads * kHeadDim;
+  for (int s = 0; s < n_split; ++s) {
+    const float4* src = reinterpret_cast<const float4*>(base + s * split_stride);
+    const float f = fac[hl][s];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = __ldg(src + k);
+      acc[k].x = fmaf(f, v.x, acc[k].x);
+      acc[k].y = fmaf(f, v.y, acc[k].y);
+      acc[k].z = fmaf(f, v.z, acc[k].z);
+      acc[k].w = fmaf(f, v.w, acc[k].w);
     }
-    const float inv = 1.f / den_s[hl];
-    x *= inv;
-    y *= inv;
+  }
+  const float inv = inv_den[hl];
+  float* dst = p.out + ((size_t)row * kHeads + h) * kHeadDim + d0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float v[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv};
+    const int d = d0 + 4 * k;
     if (d >= kHeadDim - kRopeDim) {
-      const int pi = (d - (kHeadDim - kRopeDim)) >> 1;
-      const float c = cs[pi], s = cs[32 + pi];
-      const float xr = x * c - y * s, yr = x * s + y * c;
-      x = xr;
-      y = yr;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int pi = (d + 2 * j - (kHeadDim - kRopeDim)) >> 1;
+        float c, sn;
+        rope_cs(qp, p.inv_freq[pi], -1.f, &c, &sn);
+        const float x = v[2 * j], y = v[2 * j + 1];
+        v[2 * j] = x * c - y * sn;
+        v[2 * j + 1] = x * sn + y * c;
+      }
     }
-    *reinterpret_cast<float2*>(p.out + ((size_t)row * kHeads + h) * kHeadDim + d) = make_float2(x, y);
+    *reinterpret_cast<float4*>(dst + 4 * k) = make_float4(v[0], v[1], v[2], v[3]);
   }
 }
 
@@ -491,7 +522,7 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   attn_split_kernel<<<dim3(n_split, p.n_rows), kAttnThreads, kAttnSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
-  attn_combine_kernel<<<dim3(p.n_rows, kHeads / 8), 256, 0, stream>>>(p, n_split);
+  attn_combine_kernel<<<dim3(p.n_rows, kHeads / 4), 128, 0, stream>>>(p, n_split);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,553 @@
+// Lightning indexer on the 5th-generation tensor cores (tcgen05, TMA, tensor memory).
+//
+// score_j = sum_h w_h * ReLU(q^I_h . k^I_j) ("Every layer, connected", "The global and index
+// paths") as one dense contraction per 128-record tile:
+//   D[128 records x 32*NQ] = K_tile[128 x 128] * Q[32*NQ x 128]^T      (bf16 in, fp32 in TMEM)
+// with the records along M (TMEM lanes) and (query, head) along N (TMEM columns), so that
+// every epilogue thread owns one record and reads its 32 head dot products per query with a
+// single tcgen05.ld, then applies ReLU, the head weights and the head sum in registers.
+//
+// Roles (one thread block): warp 0 issues TMA tile loads into a ring of shared-memory stages,
+// warp 1 allocates tensor memory and one of its threads issues the MMAs, and the epilogue
+// warps drain the double-buffered accumulators.  Every mbarrier wait is bounded: on a
+// timeout the block records CSA2_ETIMEOUT, finishes its loops without waiting, drains what it
+// issued (bounded again), frees its tensor memory and returns.
+//
+//   decode  (NQ = 1): one query row per block, one contiguous segment of its visible records;
+//                     the epilogue feeds the exact top-K engine and the block maxima.
+//   prefill (NQ = 8): a persistent grid walks (8-query tile, key range) work items of one
+//                     sequence; causal masking per query; scores are written out.
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "select.cuh"
+#include "tc05.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kTileKeys = 128;
+constexpr int kKeyHalf = kTileKeys * 128;   // one K-half (64 dims) of a key tile: 16 KB
+constexpr int kKeyTile = 2 * kKeyHalf;      // 32 KB
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ void report_timeout(int* flag, int32_t* dev_status) {
+  *flag = 1;
+  if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
+}
+
+// ===================================================================================== decode
+constexpr int kDecStages = 5;
+constexpr int kDecEpiFirst = 4;
+constexpr int kDecEpiWarps = 8;  // two groups of 4 warps (one per TMEM lane quarter), alternate tiles
+constexpr int kDecThreads = (kDecEpiFirst + kDecEpiWarps) * 32;  // warp 0 TMA, warp 1 MMA + TMEM
+constexpr int kDecQHalf = 32 * 128;  // 32 heads x 64 dims x 2 B
+constexpr uint32_t kDecTmemCols = 64;
+
+struct DecBars {
+  uint64_t full[kDecStages], empty[kDecStages], tfull[2], tempty[2], qfull;
+  uint32_t tmem_base;
+  int timeout;
+  int issued;     // tiles whose TMA loads were issued
+  int consumed;   // tiles whose MMAs were issued
+  int drained;    // tiles whose accumulators the epilogue read
+};
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+    idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                          const ScanParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ring = smem;
+  uint8_t* qs = ring + kDecStages * kKeyTile;
+  DecBars& bars = *reinterpret_cast<DecBars*>(qs + 2 * kDecQHalf);
+  uint8_t* rest = reinterpret_cast<uint8_t*>(&bars + 1);
+  rest = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rest) + 15) & ~static_cast<uintptr_t>(15));
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
+  const int b = p.seq_of_row[row];
+  const long long L_row = min((long long)p.n_visible[row], p.N);
+  const int U = p.unit;
+  const long long n_units = (L_row + U - 1) / U;
+  long long u0, u1;
+  split_range(n_units, n_seg, seg, u0, u1);
+  const long long e0 = u0 * U, e1 = min(u1 * U, L_row);
+  const int n_tiles = e1 > e0 ? (int)((e1 - e0 + kTileKeys - 1) / kTileKeys) : 0;
+
+  const bool do_topk = p.K > 0;
+  Engine<kDecEpiWarps> eng;
+  eng.sh = reinterpret_cast<EngShared*>(rest);
+  eng.cap = p.K + kRoundEntries;
+  eng.keys = reinterpret_cast<uint32_t*>(rest + sizeof(EngShared));
+  eng.js = reinterpret_cast<int32_t*>(eng.keys + kDecEpiWarps * eng.cap);
+  eng.out_key = reinterpret_cast<uint32_t*>(eng.js + kDecEpiWarps * eng.cap);
+  eng.out_j = reinterpret_cast<int32_t*>(eng.out_key + p.K);
+  eng.bar_id = 1;
+  eng.tid = tid - kDecEpiFirst * 32;
+  uint32_t* bkeys = reinterpret_cast<uint32_t*>(do_topk ? reinterpret_cast<uint8_t*>(eng.out_j + p.K)
+                                                         : rest + sizeof(EngShared));
+  const int bs = p.block_max ? U : 1;
+  const int seg_blocks = p.block_max ? (int)((e1 - e0 + bs - 1) / bs) : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      tc05::mbar_init(&bars.full[s], 1);
+      tc05::mbar_init(&bars.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc05::mbar_init(&bars.tfull[a], 1);
+      tc05::mbar_init(&bars.tempty[a], kDecEpiWarps / 2);  // one arrive per warp of the draining group
+    }
+    tc05::mbar_init(&bars.qfull, 1);
+    bars.timeout = 0;
+    bars.issued = bars.consumed = bars.drained = 0;
+    tc05::fence_barrier_init();
+  }
+  if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, kDecTmemCols);
+  if (warp >= kDecEpiFirst)
+    for (int i = eng.tid; i < seg_blocks; i += kDecEpiWarps * 32) bkeys[i] = 0u;
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      tc05::mbar_expect_tx(&bars.qfull, 2 * kDecQHalf);
+      tc05::tma_load_2d(qs, &tmQ, 0, row * 32, &bars.qfull);
+      tc05::tma_load_2d(qs + kDecQHalf, &tmQ, 64, row * 32, &bars.qfull);
+      const int y0 = (int)((long long)b * p.N + e0);
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kDecStages;
+        if (!tc05::mbar_wait(&bars.empty[s], ((t / kDecStages) & 1) ^ 1)) {
+          report_timeout(&bars.timeout, p.dev_status);
+          break;
+        }
+        tc05::mbar_expect_tx(&bars.full[s], kKeyTile);
+        uint8_t* dst = ring + s * kKeyTile;
+        tc05::tma_load_2d(dst, &tmK, 0, y0 + t * kTileKeys, &bars.full[s]);
+        tc05::tma_load_2d(dst + kKeyHalf, &tmK, 64, y0 + t * kTileKeys, &bars.full[s]);
+        bars.issued = t + 1;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idesc = tc05::idesc_bf16(128, 32);
+      bool ok = tc05::mbar_wait(&bars.qfull, 0);
+      const uint32_t q_u = smem_u32(qs);
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int s = t % kDecStages, a = t & 1;
+        if (!tc05::mbar_wait(&bars.full[s], (t / kDecStages) & 1) ||
+            !tc05::mbar_wait(&bars.tempty[a], ((t >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc05::fence_after();
+        const uint32_t a_u = smem_u32(ring + s * kKeyTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kKeyHalf + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * kDecQHalf + (kk & 3) * 32;
+          tc05::mma_bf16(tmem + a * 32, tc05::sw128_desc(a_u + off), tc05::sw128_desc(q_u + qoff), idesc, kk > 0);
+        }
+        tc05::mma_commit(&bars.empty[s]);
+        tc05::mma_commit(&bars.tfull[a]);
+        bars.consumed = t + 1;
+      }
+      if (!ok) report_timeout(&bars.timeout, p.dev_status);
+    }
+  } else if (warp >= kDecEpiFirst) {
+    // ---------------------------------------------------------------- epilogue
+    // group g = 0 drains the even tiles (accumulator 0), group 1 the odd ones (accumulator 1)
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int grp = (warp - kDecEpiFirst) >> 2;
+    float w[32];
+#pragma unroll
+    for (int h = 0; h < 32; ++h) w[h] = __ldg(p.w + (size_t)row * kIdxHeads + h);
+    if (do_topk) eng_init(eng);
+    int cnt = 0;
+    uint32_t thr = 0u;
+    bool dead = false;
+    float* srow = p.scores ? p.scores + (size_t)row * p.scores_stride : nullptr;
+    const int n_pairs = (n_tiles + 1) / 2;
+    for (int pr = 0; pr < n_pairs; ++pr) {
+      const int t = 2 * pr + grp, a = grp;
+      const bool have = t < n_tiles;
+      if (have && !dead && !tc05::mbar_wait(&bars.tfull[a], pr & 1)) {
+        dead = true;
+        if (lane == 0) report_timeout(&bars.timeout, p.dev_status);
+      }
+      float sc = 0.f;
+      if (have && !dead) {
+        tc05::fence_after();
+        uint32_t v[32];
+        tc05::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * 32), v);
+        tc05::tmem_ld_wait();
+        tc05::fence_before();
+        __syncwarp();
+        if (lane == 0) tc05::mbar_arrive(&bars.tempty[a]);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) sc = fmaf(w[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
+        if (warp == kDecEpiFirst + 4 * grp && lane == 0) atomicMax(&bars.drained, t + 1);
+      }
+      const long long j = e0 + (long long)t * kTileKeys + 32 * quarter + lane;
+      const bool valid = have && !dead && j < e1;
+      if (srow && valid) srow[j] = sc;
+      if (seg_blocks && valid) atomicMax(&bkeys[(j - e0) / bs], score_key(sc));
+      if (do_topk) {
+        eng_append(eng, cnt, thr, valid, score_key(sc), (int32_t)j);
+        if ((pr & 3) == 3) thr = eng_check(eng, p.K, cnt);
+      }
+    }
+    if (seg_blocks) {
+      asm volatile("bar.sync 1, %0;\n" ::"n"(kDecEpiWarps * 32) : "memory");
+      for (int i = eng.tid; i < seg_blocks; i += kDecEpiWarps * 32)
+        p.block_max[(size_t)row * p.bmax_stride + e0 / bs + i] = bkeys[i] ? key_score(bkeys[i]) : -INFINITY;
+    }
+    if (seg == n_seg - 1) {
+      if (srow)
+        for (long long jj = L_row + eng.tid; jj < p.scores_len; jj += kDecEpiWarps * 32) srow[jj] = -INFINITY;
+      if (p.block_max)
+        for (long long blk = (L_row + bs - 1) / bs + eng.tid; blk < p.n_blocks; blk += kDecEpiWarps * 32)
+          p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
+    }
+    if (do_topk) {
+      uint32_t* thr_out = n_seg > 1 ? p.seg_thr + (size_t)row * n_seg + seg : nullptr;
+      const int n = eng_finish(eng, p.K, cnt, thr_out);
+      if (n_seg == 1) {
+        int32_t* out = p.idx + (size_t)row * p.K;
+        for (int i = eng.tid; i < p.K; i += kDecEpiWarps * 32) out[i] = i < n ? eng.out_j[i] : -1;
+      } else {
+        const size_t o = ((size_t)row * n_seg + seg) * p.K;
+        for (int i = eng.tid; i < n; i += kDecEpiWarps * 32) {
+          p.seg_keys[o + i] = eng.out_key[i];
+          p.seg_pos[o + i] = eng.out_j[i];
+        }
+        if (eng.tid == 0) p.seg_cnt[(size_t)row * n_seg + seg] = n;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (bars.timeout && tid == 0) {
+    // drain loads and MMAs still in flight (bounded), then free tensor memory
+    for (int t = bars.consumed; t < bars.issued; ++t)
+      tc05::mbar_wait(&bars.full[t % kDecStages], (t / kDecStages) & 1);
+    for (int t = max(0, bars.drained - 1); t < bars.consumed; ++t)
+      tc05::mbar_wait(&bars.tfull[t & 1], (t >> 1) & 1);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc05::fence_after();
+    tc05::tmem_dealloc(tmem, kDecTmemCols);
+  }
+}
+
+// ===================================================================================== prefill
+constexpr int kPreNQ = 8;                         // queries per MMA tile (N = 256)
+constexpr int kPreN = 32 * kPreNQ;
+constexpr int kPreStages = 4;
+constexpr int kPreEpiFirst = 4;
+constexpr int kPreEpiWarps = 8;
+constexpr int kPreThreads = (kPreEpiFirst + kPreEpiWarps) * 32;  // 384
+constexpr int kPreQHalf = kPreN * 128;            // 32 KB
+constexpr uint32_t kPreTmemCols = 2 * kPreN;      // 512: two accumulators
+
+struct PreBars {
+  uint64_t full[kPreStages], empty[kPreStages], tfull[2], tempty[2], qfull, qempty;
+  uint32_t tmem_base;
+  int timeout;
+  int issued, consumed, drained, q_issued, q_used;
+  float w[kPreNQ][32];
+  int nv[kPreNQ];
+};
+
+struct PreItem {
+  int qt;        // query tile
+  int t0, t1;    // key tiles [t0, t1)
+};
+
+// Work item i of the grid: query tile i / n_parts and the part-th share of its key tiles.
+__device__ __forceinline__ PreItem pre_item(const ScanParams& p, int i, int n_parts) {
+  PreItem it;
+  it.qt = i / n_parts;
+  const int part = i % n_parts;
+  // the tile's key range is the widest causal range among its rows
+  long long L = 0;
+  for (int r = it.qt * kPreNQ; r < min(p.n_rows, (it.qt + 1) * kPreNQ); ++r)
+    L = max(L, min((long long)p.n_visible[r], p.N));
+  const int nt = (int)((L + kTileKeys - 1) / kTileKeys);
+  it.t0 = (int)(((long long)nt * part) / n_parts);
+  it.t1 = (int)(((long long)nt * (part + 1)) / n_parts);
+  return it;
+}
+
+__global__ void __launch_bounds__(kPreThreads, 1)
+    idx_mma_prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                           const ScanParams p, int n_items, int n_parts) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ring = smem;
+  uint8_t* qs = ring + kPreStages * kKeyTile;
+  PreBars& bars = *reinterpret_cast<PreBars*>(qs + 2 * kPreQHalf);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kPreStages; ++s) {
+      tc05::mbar_init(&bars.full[s], 1);
+      tc05::mbar_init(&bars.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc05::mbar_init(&bars.tfull[a], 1);
+      tc05::mbar_init(&bars.tempty[a], kPreEpiWarps);
+    }
+    tc05::mbar_init(&bars.qfull, 1);
+    tc05::mbar_init(&bars.qempty, 1);
+    bars.timeout = 0;
+    bars.issued = bars.consumed = bars.drained = bars.q_issued = bars.q_used = 0;
+    tc05::fence_barrier_init();
+  }
+  if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, kPreTmemCols);
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int t_glob = 0, n_item = 0;  // n_item counts the non-empty items (Q-buffer phases)
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        const PreItem it = pre_item(p, i, n_parts);
+        if (it.t1 <= it.t0) continue;
+        // the query tile buffer is free once every MMA of the previous item has completed
+        if (!tc05::mbar_wait(&bars.qempty, (n_item & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc05::mbar_expect_tx(&bars.qfull, 2 * kPreQHalf);
+        tc05::tma_load_2d(qs, &tmQ, 0, it.qt * kPreN, &bars.qfull);
+        tc05::tma_load_2d(qs + kPreQHalf, &tmQ, 64, it.qt * kPreN, &bars.qfull);
+        bars.q_issued = n_item + 1;
+        for (int t = it.t0; t < it.t1; ++t, ++t_glob) {
+          const int s = t_glob % kPreStages;
+          if (!tc05::mbar_wait(&bars.empty[s], ((t_glob / kPreStages) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          tc05::mbar_expect_tx(&bars.full[s], kKeyTile);
+          uint8_t* dst = ring + s * kKeyTile;
+          tc05::tma_load_2d(dst, &tmK, 0, t * kTileKeys, &bars.full[s]);
+          tc05::tma_load_2d(dst + kKeyHalf, &tmK, 64, t * kTileKeys, &bars.full[s]);
+          bars.issued = t_glob + 1;
+        }
+        ++n_item;
+      }
+      if (!ok) report_timeout(&bars.timeout, p.dev_status);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc05::idesc_bf16(128, kPreN);
+      const uint32_t q_u = smem_u32(qs);
+      int t_glob = 0, n_item = 0;  // non-empty items, as counted by the producer
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        const PreItem it = pre_item(p, i, n_parts);
+        if (it.t1 <= it.t0) continue;
+        if (!tc05::mbar_wait(&bars.qfull, n_item & 1)) {
+          ok = false;
+          break;
+        }
+        for (int t = it.t0; t < it.t1; ++t, ++t_glob) {
+          const int s = t_glob % kPreStages, a = t_glob & 1;
+          if (!tc05::mbar_wait(&bars.full[s], (t_glob / kPreStages) & 1) ||
+              !tc05::mbar_wait(&bars.tempty[a], ((t_glob >> 1) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          const uint32_t a_u = smem_u32(ring + s * kKeyTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kKeyHalf + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * kPreQHalf + (kk & 3) * 32;
+            tc05::mma_bf16(tmem + a * kPreN, tc05::sw128_desc(a_u + off), tc05::sw128_desc(q_u + qoff), idesc,
+                           kk > 0);
+          }
+          tc05::mma_commit(&bars.empty[s]);
+          tc05::mma_commit(&bars.tfull[a]);
+          bars.consumed = t_glob + 1;
+        }
+        if (ok) {
+          tc05::mma_commit(&bars.qempty);
+          bars.q_used = n_item + 1;
+        }
+        ++n_item;
+      }
+      if (!ok) report_timeout(&bars.timeout, p.dev_status);
+    }
+  } else if (warp >= kPreEpiFirst) {
+    // ---------------------------------------------------------------- epilogue
+    const int e = warp - kPreEpiFirst;       // 0..7
+    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+    const int qhalf = e >> 2;                // queries 4*qhalf .. +3
+    const int etid = tid - kPreEpiFirst * 32;
+    int t_glob = 0;
+    bool dead = false;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+      const PreItem it = pre_item(p, i, n_parts);
+      if (it.t1 <= it.t0) continue;
+      asm volatile("bar.sync 1, %0;\n" ::"n"(kPreEpiWarps * 32) : "memory");
+      if (etid < kPreNQ * 32) {
+        const int c = etid >> 5, h = etid & 31, r = it.qt * kPreNQ + c;
+        bars.w[c][h] = r < p.n_rows ? __ldg(p.w + (size_t)r * kIdxHeads + h) : 0.f;
+        if (h == 0) bars.nv[c] = r < p.n_rows ? (int)min((long long)p.n_visible[r], p.N) : 0;
+      }
+      asm volatile("bar.sync 1, %0;\n" ::"n"(kPreEpiWarps * 32) : "memory");
+      for (int t = it.t0; t < it.t1; ++t, ++t_glob) {
+        const int a = t_glob & 1;
+        if (!dead && !tc05::mbar_wait(&bars.tfull[a], (t_glob >> 1) & 1)) {
+          dead = true;
+          if (lane == 0) report_timeout(&bars.timeout, p.dev_status);
+        }
+        if (dead) continue;
+        tc05::fence_after();
+        float sc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int q = 4 * qhalf + c;
+          uint32_t v[32];
+          tc05::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * kPreN + q * 32), v);
+          tc05::tmem_ld_wait();
+          float s = 0.f;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s = fmaf(bars.w[q][h], fmaxf(__uint_as_float(v[h]), 0.f), s);
+          sc[c] = s;
+        }
+        tc05::fence_before();
+        __syncwarp();
+        if (lane == 0) tc05::mbar_arrive(&bars.tempty[a]);
+        if (e == 0 && lane == 0) bars.drained = t_glob + 1;
+        const long long j = (long long)t * kTileKeys + 32 * quarter + lane;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int q = 4 * qhalf + c, r = it.qt * kPreNQ + q;
+          if (r < p.n_rows && j < p.N)
+            p.scores[(size_t)r * p.scores_stride + j] = j < bars.nv[q] ? sc[c] : -INFINITY;
+        }
+      }
+      // past the last tile of the query tile: -inf (done by the item holding the last tile)
+      const PreItem last = pre_item(p, (it.qt + 1) * n_parts - 1, n_parts);
+      if (it.t1 == last.t1) {
+        const long long from = (long long)it.t1 * kTileKeys;
+        for (int c = 0; c < kPreNQ; ++c) {
+          const int r = it.qt * kPreNQ + c;
+          if (r >= p.n_rows) break;
+          for (long long jj = from + etid; jj < p.scores_len; jj += kPreEpiWarps * 32)
+            p.scores[(size_t)r * p.scores_stride + jj] = -INFINITY;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (bars.timeout && tid == 0) {
+    for (int t = bars.consumed; t < bars.issued; ++t)
+      tc05::mbar_wait(&bars.full[t % kPreStages], (t / kPreStages) & 1);
+    for (int t = bars.drained; t < bars.consumed; ++t) tc05::mbar_wait(&bars.tfull[t & 1], (t >> 1) & 1);
+    if (bars.q_issued > bars.q_used) tc05::mbar_wait(&bars.qfull, (bars.q_issued - 1) & 1);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc05::fence_after();
+    tc05::tmem_dealloc(tmem, kPreTmemCols);
+  }
+}
+
+// ===================================================================================== host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// Row-major [rows x 128] bf16 matrix, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* tm, const void* base, unsigned long long rows, unsigned box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t dec_smem_bytes(int K, int max_seg_blocks) {
+  size_t s = 1024 + (size_t)kDecStages * kKeyTile + 2 * kDecQHalf + sizeof(DecBars) + 16 + sizeof(EngShared);
+  if (K > 0) s += (size_t)kDecEpiWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;
+  s += (size_t)max_seg_blocks * 4;
+  return s;
+}
+
+}  // namespace
+
+bool mma_indexer_available() { return encode_fn() != nullptr; }
+
+int mma_decode_max_seg_blocks() { return 2048; }
+
+size_t mma_decode_smem_bytes(int K, int max_seg_blocks) { return dec_smem_bytes(K, max_seg_blocks); }
+
+cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
+                              cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  if (dec_smem_bytes(p.K, max_seg_blocks) > 232448) return cudaErrorInvalidValue;
+  CUtensorMap tmK, tmQ;
+  if (!make_tmap(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys) ||
+      !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, 32))
+    return cudaErrorInvalidValue;
+  const size_t smem = dec_smem_bytes(p.K, max_seg_blocks);
+  cudaError_t e = cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  idx_mma_decode_kernel<<<dim3(n_seg, p.n_rows), kDecThreads, smem, stream>>>(tmK, tmQ, p);
+  return cudaGetLastError();
+}
+
+size_t mma_prefill_smem_bytes() { return 1024 + (size_t)kPreStages * kKeyTile + 2 * kPreQHalf + sizeof(PreBars); }
+
+cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  CUtensorMap tmK, tmQ;
+  if (!make_tmap(&tmK, p.k_idx, (unsigned long long)p.N, kTileKeys) ||
+      !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, kPreN))
+    return cudaErrorInvalidValue;
+  const int n_qt = (p.n_rows + kPreNQ - 1) / kPreNQ;
+  const int n_items = n_qt * n_parts;
+  const size_t smem = mma_prefill_smem_bytes();
+  cudaError_t e =
+      cudaFuncSetAttribute(idx_mma_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  idx_mma_prefill_kernel<<<n_ctas < n_items ? n_ctas : n_items, kPreThreads, smem, stream>>>(tmK, tmQ, p, n_items,
+                                                                                            n_parts);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -53,12 +53,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
   using Cfg = ScanCfg<FP8>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  SelectShared* sh = reinterpret_cast<SelectShared*>(smem + Cfg::kRingBytes);
-  TopkEngine eng;
+  Engine<kScanWarps> eng;
+  eng.sh = reinterpret_cast<EngShared*>(smem + Cfg::kRingBytes);
   eng.cap = p.K + kRoundEntries;
-  eng.keys = reinterpret_cast<uint32_t*>(smem + Cfg::kRingBytes + sizeof(SelectShared));
-  eng.pos = reinterpret_cast<int32_t*>(eng.keys + kSelWarps * eng.cap);
-  eng.sh = sh;
+  eng.keys = reinterpret_cast<uint32_t*>(smem + Cfg::kRingBytes + sizeof(EngShared));
+  eng.js = reinterpret_cast<int32_t*>(eng.keys + kScanWarps * eng.cap);
+  eng.out_key = reinterpret_cast<uint32_t*>(eng.js + kScanWarps * eng.cap);
+  eng.out_j = reinterpret_cast<int32_t*>(eng.out_key + p.K);
+  eng.bar_id = 0;
+  eng.tid = threadIdx.x;
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
   };
 
   const bool do_topk = p.K > 0;
-  if (do_topk) engine_init(eng);
+  if (do_topk) eng_init(eng);
   int cnt = 0;
   uint32_t thr = 0u;
 
@@ -231,12 +234,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
           }
         }
         if (do_topk) {
-          warp_append(eng, wid, cnt, thr, c == 0 && v_lo, score_key(s_lo), (int32_t)rec_lo);
-          warp_append(eng, wid, cnt, thr, c == 0 && v_hi, score_key(s_hi), (int32_t)rec_hi);
+          eng_append(eng, cnt, thr, c == 0 && v_lo, score_key(s_lo), (int32_t)j_lo);
+          eng_append(eng, cnt, thr, c == 0 && v_hi, score_key(s_hi), (int32_t)j_hi);
         }
       }
     }
-    if (do_topk) thr = engine_round_end(eng, p.K, wid, lane, cnt);
+    if (do_topk) thr = eng_check(eng, p.K, cnt);
   }
   cp_async_wait<0>();
 
@@ -250,12 +253,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
         p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
   }
   if (!do_topk) return;
+  uint32_t* thr_out = n_seg > 1 ? p.seg_thr + (size_t)row * n_seg + seg : nullptr;
+  const int n = eng_finish(eng, p.K, cnt, thr_out);
   if (n_seg == 1) {
-    engine_finish(eng, p.K, wid, lane, cnt, p.idx + (size_t)row * p.K, nullptr, nullptr, nullptr);
+    int32_t* out = p.idx + (size_t)row * p.K;
+    for (int i = tid; i < p.K; i += kScanThreads) out[i] = i < n ? (int32_t)record_of(eng.out_j[i]) : -1;
   } else {
     const size_t o = ((size_t)row * n_seg + seg) * p.K;
-    engine_finish(eng, p.K, wid, lane, cnt, nullptr, p.seg_keys + o, p.seg_pos + o,
-                  p.seg_cnt + (size_t)row * n_seg + seg);
+    for (int i = tid; i < n; i += kScanThreads) {
+      p.seg_keys[o + i] = eng.out_key[i];
+      p.seg_pos[o + i] = (int32_t)record_of(eng.out_j[i]);
+    }
+    if (tid == 0) p.seg_cnt[(size_t)row * n_seg + seg] = n;
   }
 }
 
@@ -263,8 +272,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
 
 size_t scan_smem_bytes(bool fp8, int K) {
   const size_t ring = fp8 ? ScanCfg<true>::kRingBytes : ScanCfg<false>::kRingBytes;
-  size_t s = ring + sizeof(SelectShared);
-  if (K > 0) s += (size_t)kSelWarps * (K + kRoundEntries) * 8;
+  size_t s = ring + sizeof(EngShared);
+  if (K > 0) s += (size_t)kScanWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;
   return s;
 }
 

@@ -32,9 +32,18 @@ struct ScanParams {
   uint32_t* seg_keys;         // [n_rows, n_seg, K] when n_seg > 1
   int32_t* seg_pos;
   int32_t* seg_cnt;           // [n_rows, n_seg]
+  uint32_t* seg_thr;          // [n_rows, n_seg] K-th key of each full segment list, else 0
+  int32_t* dev_status;        // optional: CSA2_ETIMEOUT when a bounded wait gives up
 };
 
 size_t scan_smem_bytes(bool fp8, int K);
+
+// tcgen05 indexer (bf16 keys, records in place): decode rows and prefill tiles.
+bool mma_indexer_available();
+int mma_decode_max_seg_blocks();
+cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
+                              cudaStream_t stream);
+cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream);
 cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_seg, cudaStream_t stream);
 
 // Streaming top-K over per-row entry streams (scores, or the lists of earlier segments).
@@ -52,6 +61,7 @@ struct FeedParams {
   const uint32_t* in_keys;
   const int32_t* in_pos;
   const int32_t* in_cnt;
+  const uint32_t* in_thr;     // optional [n_rows, in_seg]: K-th key of each full list
   int in_seg;
   int in_K;
   // output: final idx [n_rows, K] (out_seg == 1) or lists [n_rows, out_seg, K]
@@ -59,6 +69,7 @@ struct FeedParams {
   uint32_t* out_keys;
   int32_t* out_pos;
   int32_t* out_cnt;
+  uint32_t* out_thr;
 };
 
 size_t feed_smem_bytes(int K);
@@ -86,6 +97,7 @@ struct AttnParams {
   const float* sink;
   float theta;
   float scale;
+  double inv_freq[32];        // theta^(-2i/64), i = 0..31 (computed on the host in double)
   float* part_o;              // [n_rows, n_split, 64, 512]
   float* part_ml;             // [n_rows, n_split, 64, 2]
   float* out;

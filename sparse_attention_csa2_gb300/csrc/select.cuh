@@ -1,45 +1,38 @@
-// Exact streaming top-K for one row per thread block (512 threads = 16 warps).
+// Exact streaming top-K of one row, run by a group of NW warps of a thread block.
 //
-// Selection rule ("06 / Indexer and attention", select_values, and its note that ties use
-// the lower position first): keep the K entries that are best by (score descending, entry
-// order ascending).  Scores are compared through order-preserving uint32 keys
-// (score_key), so -0.0 == +0.0 and the comparison is exact.
+// Selection rule (course lesson "06 / Indexer and attention", select_values, and its note on
+// ties): keep the K entries that are best by (score descending, entry index ascending).
+// Scores are compared through order-preserving uint32 keys (score_key), so -0.0 == +0.0
+// and every comparison is exact.
 //
-// State: every warp owns a buffer of (key, position) pairs holding ITS surviving entries in
-// entry order; warps own consecutive entry ranges in warp order, so the concatenation of
-// the buffers is in entry order.  A warp appends survivors of each 32-entry group with a
-// ballot (order preserved).  An entry survives if its key exceeds `thr`, the K-th best key
-// seen so far (0 until K entries have been seen): a later entry with a key <= thr ranks
-// behind at least K earlier entries and can never be selected.  When a buffer nears its
-// capacity the block runs `engine_select`: an MSB-first 8-bit radix select finds the K-th
-// key and how many entries equal to it to keep, then every warp compacts its buffer in
-// place.  The result after the last select is exactly the top-K, in entry order.
+// Every warp of the group owns a buffer of (key, entry index j) pairs, in any order.  A
+// warp appends the entries of each 32-lane group whose key is at least `thr` with a ballot.
+// `thr` is the K-th best key among the entries kept so far (0 until K entries have been
+// seen): an entry with a smaller key ranks behind K others whatever its index, so it can
+// be dropped in any feeding order; ties with thr are kept and decided by index at the next
+// select.  When a buffer nears capacity the group runs `eng_select`: an
+// MSB-first 8-bit radix select finds the K-th key thr and how many entries equal to it to
+// keep; if that is fewer than all of them, a second radix select over the indices of the
+// tied entries finds the last index to keep.  Each warp then compacts its buffer.
+// `eng_finish` emits the survivors sorted by index (rank counting).
 #pragma once
 
 #include "common.cuh"
 
 namespace csa2 {
 
-constexpr int kSelThreads = 512;
-constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kRoundEntries = 128;  // most entries one warp appends between two checks
+constexpr int kEngMaxWarps = 16;
+constexpr int kEngMaxK = 1024;
 
-struct SelectShared {
+struct EngShared {
   int hist[256];
   int tmp[32];
-  int warp_cnt[kSelWarps];
-  int warp_eq[kSelWarps];
+  int warp_cnt[kEngMaxWarps];
   uint32_t thr;
   int sel_digit;
-  int sel_above;
-  int total;
-};
-
-struct TopkEngine {
-  uint32_t* keys;  // [kSelWarps * cap]
-  int32_t* pos;    // [kSelWarps * cap]
-  int cap;         // per-warp capacity, >= K + kRoundEntries
-  SelectShared* sh;
+  int sel_before;
+  int sel_count;
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -48,149 +41,257 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-__device__ __forceinline__ void engine_init(TopkEngine& e) {
-  if (threadIdx.x < kSelWarps) e.sh->warp_cnt[threadIdx.x] = 0;
-  if (threadIdx.x == 0) e.sh->thr = 0u;
-  __syncthreads();
+template <int NW>
+struct Engine {
+  static constexpr int NT = NW * 32;
+  uint32_t* keys;     // [NW * cap]
+  int32_t* js;        // [NW * cap] entry indices
+  uint32_t* out_key;  // [K] emission scratch
+  int32_t* out_j;     // [K]
+  int cap;            // per-warp capacity, >= K + kRoundEntries
+  EngShared* sh;
+  int bar_id;         // 0: __syncthreads (the group is the whole block); else a named barrier
+  int tid;            // 0 .. NT-1 within the group
+
+  __device__ __forceinline__ void sync() const {
+    if (bar_id == 0)
+      __syncthreads();
+    else
+      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "n"(NT) : "memory");
+  }
+  __device__ __forceinline__ int lane() const { return tid & 31; }
+  __device__ __forceinline__ int warp() const { return tid >> 5; }
+
+  // Exclusive prefix sum over the group; *total gets the sum.
+  __device__ __forceinline__ int scan(int v, int* total) const {
+    const int ln = lane(), w = warp();
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (ln >= o) x += y;
+    }
+    if (ln == 31) sh->tmp[w] = x;
+    sync();
+    if (w == 0) {
+      int t = ln < NW ? sh->tmp[ln] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (ln >= o) t += y;
+      }
+      if (ln < NW) sh->tmp[ln] = t;
+    }
+    sync();
+    const int before = w ? sh->tmp[w - 1] : 0;
+    *total = sh->tmp[NW - 1];
+    sync();
+    return before + x - v;
+  }
+};
+
+template <int NW>
+__device__ __forceinline__ void eng_init(const Engine<NW>& e, uint32_t thr0 = 0u) {
+  if (e.tid < NW) e.sh->warp_cnt[e.tid] = 0;
+  if (e.tid == 0) e.sh->thr = thr0;
+  e.sync();
 }
 
-// Appends, in lane order, the lanes' entries that are valid and beat `thr`.  `cnt` is the
-// warp's buffer fill (warp-uniform register).  The caller guarantees room for 32 more.
-__device__ __forceinline__ void warp_append(const TopkEngine& e, int wid, int& cnt, uint32_t thr,
-                                            bool valid, uint32_t key, int32_t pos) {
-  const bool keep = valid && key > thr;
+// Appends, as one 32-lane group, the lanes' entries that are valid with key >= thr.
+// `cnt` is this warp's fill (warp-uniform).  The caller guarantees room for 32 more.
+template <int NW>
+__device__ __forceinline__ void eng_append(const Engine<NW>& e, int& cnt, uint32_t thr, bool valid, uint32_t key,
+                                           int32_t j) {
+  const bool keep = valid && key >= thr && key != 0u;
   const unsigned m = __ballot_sync(0xffffffffu, keep);
   if (keep) {
-    const int o = wid * e.cap + cnt + __popc(m & lanemask_lt());
+    const int o = e.warp() * e.cap + cnt + __popc(m & lanemask_lt());
     e.keys[o] = key;
-    e.pos[o] = pos;
+    e.js[o] = j;
   }
   cnt += __popc(m);
 }
 
-// Block-wide: keep the top-k of the concatenated warp buffers (counts in sh->warp_cnt).
-// Updates sh->warp_cnt and sh->thr.  Must be called by all threads.
-__device__ inline void engine_select(const TopkEngine& e, int k) {
-  SelectShared& s = *e.sh;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int mycnt = s.warp_cnt[wid];
+// One radix digit search over sh->hist: the digit at which the running count (from the top
+// digit down when `desc`, else from digit 0 up) first reaches `need`.  Stores the digit, the
+// count before it and its own count in sh.
+template <int NW>
+__device__ __forceinline__ void eng_pick_digit(const Engine<NW>& e, int need, bool desc) {
+  constexpr int NT = NW * 32;
+  constexpr int BPT = NT >= 256 ? 1 : 256 / NT;  // bins per thread
+  const int t = e.tid;
+  int h[BPT];
+  int local = 0;
+#pragma unroll
+  for (int k = 0; k < BPT; ++k) {
+    const int r = t * BPT + k;  // rank of the bin in search order
+    h[k] = r < 256 ? e.sh->hist[desc ? 255 - r : r] : 0;
+    local += h[k];
+  }
+  int tot;
+  int before = e.scan(local, &tot);
+#pragma unroll
+  for (int k = 0; k < BPT; ++k) {
+    const int r = t * BPT + k;
+    if (r < 256 && before < need && before + h[k] >= need) {
+      e.sh->sel_digit = desc ? 255 - r : r;
+      e.sh->sel_before = before;
+      e.sh->sel_count = h[k];
+    }
+    before += h[k];
+  }
+  e.sync();
+}
+
+// Keeps the top-k of the group's buffers.  Updates warp counts and sh->thr.  All threads of
+// the group must call it.
+template <int NW>
+__device__ __noinline__ void eng_select(const Engine<NW> e, int k) {
+  constexpr int NT = NW * 32;
+  EngShared& s = *e.sh;
+  const int t = e.tid, ln = e.lane(), w = e.warp();
+  const int mycnt = s.warp_cnt[w];
   int total = 0;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) total += s.warp_cnt[w];
+  for (int i = 0; i < NW; ++i) total += s.warp_cnt[i];
   if (total <= k) {
-    __syncthreads();
+    e.sync();
     return;
   }
-  const uint32_t* kb = e.keys + wid * e.cap;
-  int32_t* pb = e.pos + wid * e.cap;
+  uint32_t* kb = e.keys + w * e.cap;
+  int32_t* jb = e.js + w * e.cap;
+  // ---- the k-th best key: MSB-first radix over the keys
   uint32_t prefix = 0u, mask = 0u;
-  int krem = k;
+  int krem = k, n_tied = 0;
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    if (tid < 256) s.hist[tid] = 0;
-    __syncthreads();
-    for (int i = lane; i < mycnt; i += 32) {
+    for (int i = t; i < 256; i += NT) s.hist[i] = 0;
+    e.sync();
+    for (int i = ln; i < mycnt; i += 32) {
       const uint32_t key = kb[i];
       if ((key & mask) == prefix) atomicAdd(&s.hist[(key >> shift) & 255u], 1);
     }
-    __syncthreads();
-    const int c = tid < 256 ? s.hist[255 - tid] : 0;
-    int tot;
-    const int above = block_excl_scan<kSelThreads>(c, s.tmp, &tot);  // entries with a larger digit
-    if (tid < 256 && above < krem && above + c >= krem) {
-      s.sel_digit = 255 - tid;
-      s.sel_above = above;
-    }
-    __syncthreads();
+    e.sync();
+    eng_pick_digit(e, krem, true);
     prefix |= static_cast<uint32_t>(s.sel_digit) << shift;
     mask |= 0xffu << shift;
-    krem -= s.sel_above;
+    krem -= s.sel_before;
+    n_tied = s.sel_count;
   }
-  const uint32_t thr = prefix;  // the k-th best key
-  const int n_eq = krem;        // entries equal to thr to keep, first ones in entry order
-
-  int eq = 0;
-  for (int i = lane; i < mycnt; i += 32) eq += (kb[i] == thr);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  if (lane == 0) s.warp_eq[wid] = eq;
-  __syncthreads();
-  int eq_before = 0;
-  for (int w = 0; w < wid; ++w) eq_before += s.warp_eq[w];
-  const int take = max(0, min(eq, n_eq - eq_before));
-
-  int wr = 0, eq_seen = 0;
-  uint32_t* kw = e.keys + wid * e.cap;
+  const uint32_t thr = prefix;
+  // ---- ties at thr: keep the krem lowest indices (indices are distinct)
+  uint32_t jthr = 0xffffffffu;
+  if (krem < n_tied) {
+    uint32_t jp = 0u, jm = 0u;
+    int jrem = krem;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = t; i < 256; i += NT) s.hist[i] = 0;
+      e.sync();
+      for (int i = ln; i < mycnt; i += 32) {
+        const uint32_t j = static_cast<uint32_t>(jb[i]);
+        if (kb[i] == thr && (j & jm) == jp) atomicAdd(&s.hist[(j >> shift) & 255u], 1);
+      }
+      e.sync();
+      eng_pick_digit(e, jrem, false);
+      jp |= static_cast<uint32_t>(s.sel_digit) << shift;
+      jm |= 0xffu << shift;
+      jrem -= s.sel_before;
+    }
+    jthr = jp;
+  }
+  // ---- compact every warp's buffer in place (writes never pass the read position)
+  int wr = 0;
   for (int base = 0; base < mycnt; base += 32) {
-    const int i = base + lane;
+    const int i = base + ln;
     const bool in = i < mycnt;
-    const uint32_t key = in ? kw[i] : 0u;
-    const int32_t p = in ? pb[i] : 0;
-    const bool is_eq = in && key == thr;
-    const unsigned em = __ballot_sync(0xffffffffu, is_eq);
-    const int eq_rank = eq_seen + __popc(em & lanemask_lt());
-    const bool keep = in && (key > thr || (is_eq && eq_rank < take));
+    const uint32_t key = in ? kb[i] : 0u;
+    const int32_t j = in ? jb[i] : 0;
+    const bool keep = in && (key > thr || (key == thr && static_cast<uint32_t>(j) <= jthr));
     const unsigned km = __ballot_sync(0xffffffffu, keep);
     if (keep) {
       const int o = wr + __popc(km & lanemask_lt());
-      kw[o] = key;
-      pb[o] = p;
+      kb[o] = key;
+      jb[o] = j;
     }
     wr += __popc(km);
-    eq_seen += __popc(em);
     __syncwarp();
   }
-  __syncthreads();
-  if (lane == 0) s.warp_cnt[wid] = wr;
-  if (tid == 0) s.thr = thr;
-  __syncthreads();
+  e.sync();
+  if (ln == 0) s.warp_cnt[w] = wr;
+  if (t == 0) s.thr = thr;
+  e.sync();
 }
 
-// Publishes the warp counts and selects when some buffer could overflow in the next round.
-// Returns the (possibly raised) threshold; `cnt` is refreshed.  All threads must call it.
-__device__ __forceinline__ uint32_t engine_round_end(const TopkEngine& e, int k, int wid, int lane,
-                                                     int& cnt) {
-  if (lane == 0) e.sh->warp_cnt[wid] = cnt;
-  __syncthreads();
+// Publishes the warp counts and selects when some buffer could overflow before the next
+// check.  Returns the (possibly raised) threshold and refreshes `cnt`.
+template <int NW>
+__device__ __forceinline__ uint32_t eng_check(const Engine<NW>& e, int k, int& cnt) {
+  if (e.lane() == 0) e.sh->warp_cnt[e.warp()] = cnt;
+  e.sync();
   bool need = false;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) need |= e.sh->warp_cnt[w] > e.cap - kRoundEntries;
-  if (need) engine_select(e, k);  // uniform branch: every thread read the same counts
-  cnt = e.sh->warp_cnt[wid];
+  for (int i = 0; i < NW; ++i) need |= e.sh->warp_cnt[i] > e.cap - kRoundEntries;
+  if (need) eng_select(e, k);  // uniform: every thread read the same counts
+  cnt = e.sh->warp_cnt[e.warp()];
   const uint32_t thr = e.sh->thr;
-  __syncthreads();
+  e.sync();
   return thr;
 }
 
-// Final select, then writes the kept entries in entry order.  With `final_idx`, writes
-// positions to final_idx[0..k) padded with -1; otherwise writes keys/positions to
-// out_keys/out_pos[0..n) and n to *out_cnt.
-__device__ inline void engine_finish(const TopkEngine& e, int k, int wid, int lane, int cnt, int32_t* final_idx,
-                              uint32_t* out_keys, int32_t* out_pos, int32_t* out_cnt) {
-  if (lane == 0) e.sh->warp_cnt[wid] = cnt;
-  __syncthreads();
-  engine_select(e, k);
-  const int mycnt = e.sh->warp_cnt[wid];
+// Final select; the survivors, sorted by entry index, go to out_key / out_j [0..n) and n is
+// returned.  *thr_out gets the k-th key when k survive, else 0 (every dropped entry has a
+// key <= it, and the row's k-th key is at least it).  k <= kEngMaxK.
+template <int NW>
+__device__ int eng_finish(const Engine<NW>& e, int k, int cnt, uint32_t* thr_out) {
+  constexpr int NT = NW * 32;
+  constexpr int PER = (kEngMaxK + NT - 1) / NT;
+  if (e.lane() == 0) e.sh->warp_cnt[e.warp()] = cnt;
+  e.sync();
+  eng_select(e, k);
   int off = 0, total = 0;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
-    const int c = e.sh->warp_cnt[w];
-    off += (w < wid) ? c : 0;
+  for (int i = 0; i < NW; ++i) {
+    const int c = e.sh->warp_cnt[i];
+    off += (i < e.warp()) ? c : 0;
     total += c;
   }
-  const uint32_t* kb = e.keys + wid * e.cap;
-  const int32_t* pb = e.pos + wid * e.cap;
-  if (final_idx) {
-    for (int i = lane; i < mycnt; i += 32) final_idx[off + i] = pb[i];
-    for (int i = total + threadIdx.x; i < k; i += kSelThreads) final_idx[i] = -1;
-  } else {
-    for (int i = lane; i < mycnt; i += 32) {
-      out_keys[off + i] = kb[i];
-      out_pos[off + i] = pb[i];
-    }
-    if (threadIdx.x == 0) *out_cnt = total;
+  const int mycnt = e.sh->warp_cnt[e.warp()];
+  const uint32_t* gk = e.keys + e.warp() * e.cap;
+  const int32_t* gj = e.js + e.warp() * e.cap;
+  for (int i = e.lane(); i < mycnt; i += 32) {
+    e.out_key[off + i] = gk[i];
+    e.out_j[off + i] = gj[i];
   }
+  e.sync();
+  // rank of an entry = number of survivors with a smaller index
+  uint32_t mk[PER];
+  int32_t mj[PER], mr[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int i = e.tid + q * NT;
+    mr[q] = -1;
+    if (i < total) {
+      mk[q] = e.out_key[i];
+      mj[q] = e.out_j[i];
+      int r = 0;
+      for (int m = 0; m < total; ++m) r += e.out_j[m] < mj[q];
+      mr[q] = r;
+    }
+  }
+  e.sync();
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    if (mr[q] >= 0) {
+      e.out_key[mr[q]] = mk[q];
+      e.out_j[mr[q]] = mj[q];
+    }
+  }
+  if (e.tid == 0 && thr_out) *thr_out = total >= k ? e.sh->thr : 0u;
+  e.sync();
+  return total;
 }
 
 // Balanced split of [0, n) into `parts` contiguous ranges; range `i`.

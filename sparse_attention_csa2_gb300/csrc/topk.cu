@@ -9,63 +9,95 @@ namespace csa2 {
 
 namespace {
 
+constexpr int kFeedWarps = 16;
+constexpr int kFeedThreads = kFeedWarps * 32;
+
 // One thread block per (output segment, row).  Entries of the row are a flat stream split
 // into contiguous ranges: output segments, then warps; each warp feeds 128 entries per round.
+// Source A (scores): entry j = column j, its position cand[row, j] (or j).  Source B (lists
+// of earlier segments): the entries are the lists' (key, position) pairs and the position
+// itself orders them.
 template <bool FROM_LISTS>
-__global__ void __launch_bounds__(kSelThreads, 1) topk_feed_kernel(const FeedParams p) {
+__global__ void __launch_bounds__(kFeedThreads, 1) topk_feed_kernel(const FeedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  SelectShared* sh = reinterpret_cast<SelectShared*>(smem);
-  TopkEngine eng;
-  eng.cap = p.K + kRoundEntries;
-  eng.keys = reinterpret_cast<uint32_t*>(smem + sizeof(SelectShared));
-  eng.pos = reinterpret_cast<int32_t*>(eng.keys + kSelWarps * eng.cap);
-  eng.sh = sh;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  Engine<kFeedWarps> e;
+  e.sh = reinterpret_cast<EngShared*>(smem);
+  e.cap = p.K + kRoundEntries;
+  e.keys = reinterpret_cast<uint32_t*>(smem + sizeof(EngShared));
+  e.js = reinterpret_cast<int32_t*>(e.keys + kFeedWarps * e.cap);
+  e.out_key = reinterpret_cast<uint32_t*>(e.js + kFeedWarps * e.cap);
+  e.out_j = reinterpret_cast<int32_t*>(e.out_key + p.K);
+  e.bar_id = 0;
+  e.tid = threadIdx.x;
+  const int wid = threadIdx.x >> 5;
   const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
 
   const long long total = FROM_LISTS ? (long long)p.in_seg * p.in_K
                                       : ((long long)p.n_valid[row] + p.valid_div - 1) / p.valid_div;
   long long s0, s1, w0, w1;
   split_range(total, n_seg, seg, s0, s1);
-  split_range(s1 - s0, kSelWarps, wid, w0, w1);
+  split_range(s1 - s0, kFeedWarps, wid, w0, w1);
   const long long f0 = s0 + w0, f1 = s0 + w1;
-  const long long per_warp_max = ((s1 - s0) + kSelWarps - 1) / kSelWarps;
+  const long long per_warp_max = ((s1 - s0) + kFeedWarps - 1) / kFeedWarps;
   const int rounds = (int)((per_warp_max + kRoundEntries - 1) / kRoundEntries);
 
-  engine_init(eng);
+  // Lists of earlier segments: the row's K-th key is at least the K-th key of every full
+  // list, so any entry below the largest of those cannot be selected.
+  uint32_t thr0 = 0u;
+  if (FROM_LISTS && p.in_thr != nullptr)
+    for (int s = 0; s < p.in_seg; ++s) thr0 = max(thr0, p.in_thr[(size_t)row * p.in_seg + s]);
+  eng_init(e, thr0);
   int cnt = 0;
-  uint32_t thr = 0u;
-  long long f = f0 + lane;
+  uint32_t thr = thr0;
+  constexpr int G = kRoundEntries / 32;
+  long long f = f0 + e.lane();
   for (int r = 0; r < rounds; ++r) {
+    // all loads of the round first, then the appends
+    bool valid[G];
+    uint32_t key[G];
+    int32_t j[G];
 #pragma unroll
-    for (int k = 0; k < kRoundEntries / 32; ++k, f += 32) {
-      bool valid = f < f1;
-      uint32_t key = 0u;
-      int32_t pos = 0;
-      if (valid) {
+    for (int k = 0; k < G; ++k) {
+      const long long fk = f + 32 * k;
+      valid[k] = fk < f1;
+      key[k] = 0u;
+      j[k] = 0;
+      if (valid[k]) {
         if (FROM_LISTS) {
-          const long long s = f / p.in_K, i = f % p.in_K;
-          valid = i < p.in_cnt[(size_t)row * p.in_seg + s];
-          if (valid) {
-            const size_t o = ((size_t)row * p.in_seg + s) * p.in_K + i;
-            key = p.in_keys[o];
-            pos = p.in_pos[o];
+          const long long s = fk / p.in_K, i = fk % p.in_K;
+          valid[k] = i < __ldg(p.in_cnt + (size_t)row * p.in_seg + s);
+          const size_t o = ((size_t)row * p.in_seg + s) * p.in_K + i;
+          if (valid[k]) {
+            key[k] = __ldg(p.in_keys + o);
+            j[k] = __ldg(p.in_pos + o);
           }
         } else {
-          key = score_key(p.scores[(size_t)row * p.scores_stride + f]);
-          pos = p.cand ? p.cand[(size_t)row * p.cand_stride + f] : (int32_t)f;
+          key[k] = score_key(__ldg(p.scores + (size_t)row * p.scores_stride + fk));
+          j[k] = (int32_t)fk;
         }
       }
-      warp_append(eng, wid, cnt, thr, valid, key, pos);
     }
-    thr = engine_round_end(eng, p.K, wid, lane, cnt);
+#pragma unroll
+    for (int k = 0; k < G; ++k) eng_append(e, cnt, thr, valid[k], key[k], j[k]);
+    f += kRoundEntries;
+    thr = eng_check(e, p.K, cnt);
   }
+  uint32_t* thr_out = (n_seg > 1 && p.out_thr) ? p.out_thr + (size_t)row * n_seg + seg : nullptr;
+  const int n = eng_finish(e, p.K, cnt, thr_out);
+  auto position = [&](int32_t j) -> int32_t {
+    if (!FROM_LISTS && p.cand != nullptr) return p.cand[(size_t)row * p.cand_stride + j];
+    return j;
+  };
   if (n_seg == 1) {
-    engine_finish(eng, p.K, wid, lane, cnt, p.idx + (size_t)row * p.K, nullptr, nullptr, nullptr);
+    int32_t* out = p.idx + (size_t)row * p.K;
+    for (int i = threadIdx.x; i < p.K; i += kFeedThreads) out[i] = i < n ? position(e.out_j[i]) : -1;
   } else {
     const size_t o = ((size_t)row * n_seg + seg) * p.K;
-    engine_finish(eng, p.K, wid, lane, cnt, nullptr, p.out_keys + o, p.out_pos + o,
-                  p.out_cnt + (size_t)row * n_seg + seg);
+    for (int i = threadIdx.x; i < n; i += kFeedThreads) {
+      p.out_keys[o + i] = e.out_key[i];
+      p.out_pos[o + i] = position(e.out_j[i]);
+    }
+    if (threadIdx.x == 0) p.out_cnt[(size_t)row * n_seg + seg] = n;
   }
 }
 
@@ -98,12 +130,14 @@ __global__ void pool_expand_kernel(const int32_t* __restrict__ kept, const int32
 
 }  // namespace
 
-size_t feed_smem_bytes(int K) { return sizeof(SelectShared) + (size_t)kSelWarps * (K + kRoundEntries) * 8; }
+size_t feed_smem_bytes(int K) {
+  return sizeof(EngShared) + (size_t)kFeedWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;
+}
 
 cudaError_t launch_topk_feed(const FeedParams& p, bool from_lists, int out_seg, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
   const size_t smem = feed_smem_bytes(p.K);
-  dim3 grid(out_seg, p.n_rows), block(kSelThreads);
+  dim3 grid(out_seg, p.n_rows), block(kFeedThreads);
   cudaError_t e;
   if (from_lists) {
     e = cudaFuncSetAttribute(topk_feed_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -222,3 +222,28 @@ def test_decode_equals_prefill_row():
         g1 = gpu_group(d1)
         assert torch.equal(g1[0].idx[0], g[0].idx[t])
         assert rel_err(g1[0].out[0].cpu().numpy()[None], ref["o"][i][None]) <= 2e-3
+
+
+# ------------------------------------------------------------------ prefill indexer (tcgen05, persistent)
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_prefill_index_scores(mode):
+    _cuda()
+    wl = synth.scaled(synth.WORKLOADS["prefill_chunk"], N=3077, T=203, P0=2874)
+    inp = synth.make_inputs(wl, seed=9, mode=mode)
+    dv = synth.to_device(inp)
+    c, lay, rw = dv["cache"], dv["layers"][0], dv["rows"]
+    s = S.index_scores(lay["q_idx"], lay["w"], c["k_idx"], c["k_scale"], rw["seq_of_row"], rw["n_visible"])
+    s = s.cpu().numpy().astype(np.float64)
+    rows = [0, 1, 7, 8, 100, 201, 202]
+    ref = O.index_scores_rows(inp, 0, rows=rows)
+    got = s[rows]
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    if mode == "grid":
+        assert np.array_equal(got[fin], ref[fin])
+    else:
+        bound = score_bound(inp, 0, rows)
+        assert np.all(np.abs(got - ref)[fin] <= np.repeat(bound[:, None], got.shape[1], 1)[fin])
+    # every row: -inf exactly from its causal boundary on
+    nv = inp["rows"]["n_visible"]
+    assert all(np.isfinite(s[r, :nv[r]]).all() and np.isneginf(s[r, nv[r]:]).all() for r in range(wl.T))
