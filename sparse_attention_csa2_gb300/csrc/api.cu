@@ -46,7 +46,8 @@ int attn_splits(int n_rows, int K, int window) {
   const int forced = env_int("CSA2_ATTN_SPLITS", 0);
   const int n_tiles = (K + window + 63) / 64;
   if (forced > 0) return forced < n_tiles ? forced : (n_tiles > 0 ? n_tiles : 1);
-  int s = sm_count() / (n_rows > 0 ? n_rows : 1);
+  // blocks are (row, 16-head group, split): fill the SMs, at most one split per tile
+  int s = sm_count() / (4 * (n_rows > 0 ? n_rows : 1));
   if (s > n_tiles) s = n_tiles;
   if (s > 64) s = 64;
   return s < 1 ? 1 : s;

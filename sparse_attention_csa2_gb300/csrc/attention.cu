@@ -24,21 +24,29 @@ namespace csa2 {
 
 namespace {
 
-constexpr int kAttnThreads = 512;
-constexpr int kTile = 64;
-constexpr int kQBytes = kHeads * kHeadDim * 2;      // 64 KB
-constexpr int kKVBytes = kTile * kHeadDim * 2;      // 64 KB per stage
-constexpr int kPBytes = kHeads * kTile * 2;         // 8 KB
+constexpr int kAttnThreads = 256;  // 8 warps
+constexpr int kTile = 64;          // attended entries per tile
+constexpr int kHG = 16;            // heads per block (one m16 MMA tile)
+constexpr int kQBytes = kHG * kHeadDim * 2;     // 16 KB
+constexpr int kKVBytes = kTile * kHeadDim * 2;  // 64 KB per stage
+constexpr int kPBytes = kHG * kTile * 2;        // 2 KB
+constexpr int kStages = 3;                      // gather pipeline depth (tiles in flight)
+constexpr int kMetaSlots = kStages + 1;         // tile sources, prepared one iteration ahead
+
+struct TileMeta {
+  const uint8_t* ptr[kTile];   // first byte of each entry's row (codes for FP formats)
+  const uint8_t* sptr[kTile];  // FP4 group scales
+  float rs[kTile];             // FP8 row scale (1 otherwise)
+  int fmt[kTile];              // storage format, -1 = masked entry
+};
 
 struct AttnSmem {
-  float red_max[4][kHeads];
-  float red_sum[4][kHeads];
-  float alpha[kHeads];
-  float rowscale[2][kTile];
-  int rowvalid[2][kTile];
+  TileMeta meta[kMetaSlots];
+  float red_max[4][kHG];
+  float red_sum[4][kHG];
   float cs[kRopeDim];  // cos (0..31) and sin (32..63) of the row's rotary angles
 };
-constexpr int kAttnSmemBytes = kQBytes + 2 * kKVBytes + kPBytes + (int)sizeof(AttnSmem);
+constexpr int kAttnSmemBytes = kQBytes + kStages * kKVBytes + kPBytes + (int)sizeof(AttnSmem);
 
 // Byte offset of 16-byte chunk `c` of row `r` in a tile with 1024-byte rows: the low three
 // chunk bits are XOR-ed with the row so that 8 rows at the same chunk hit 8 bank groups.
@@ -121,75 +129,99 @@ __device__ __forceinline__ EntrySrc entry_source(const AttnParams& p, int row, i
   return s;
 }
 
-// Gathers tile `tile` of the row into KV stage `kv` (64 rows x 512 bf16, swizzled).
-// Thread -> (row = tid/8, part = tid%8); part covers dims 64*part .. 64*part+63.
-__device__ __forceinline__ void load_tile(const AttnParams& p, AttnSmem& sm, uint8_t* kv, int stage, int row,
-                                          int b, long long qp, long long lo, long long pos0, int tile) {
-  const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
-  const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTile + r);
-  if (part == 0) {
-    sm.rowvalid[stage][r] = s.valid;
-    sm.rowscale[stage][r] = s.rs;
-  }
-  if (!s.valid || s.fmt == CSA2_BF16) {
-    const uint8_t* src = s.valid ? s.ptr : reinterpret_cast<const uint8_t*>(p.q);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int c = part + 8 * k;
-      cp_async16(kv + swz1k(r, c), src + c * 16, s.valid);
-    }
-    return;
-  }
-  uint32_t outw[32];  // 64 bf16 of dims 64*part ..
-  if (s.fmt == CSA2_FP8_E4M3_ROWSCALE) {
-    const uint4* src = reinterpret_cast<const uint4*>(s.ptr + part * 64);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const uint4 v = __ldg(src + q4);
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        outw[q4 * 8 + 2 * k] = e4m3x2_to_bf16x2((uint16_t)(w4[k] & 0xffffu));
-        outw[q4 * 8 + 2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(w4[k] >> 16));
-      }
-    }
-  } else {
-    const int gsz = s.fmt == CSA2_FP4_E2M1_G32 ? 32 : 16;
-    const uint4* src = reinterpret_cast<const uint4*>(s.ptr + part * 32);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 v = __ldg(src + h);
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-#pragma unroll
-        for (int byte = 0; byte < 4; ++byte) {
-          const int ch = part * 64 + h * 32 + k * 8 + byte * 2;  // even channel of this byte
-          const float sc = e4m3_value(__ldg(s.sptr + ch / gsz));
-          const uint32_t code = (w4[k] >> (8 * byte)) & 0xffu;
-          outw[h * 16 + k * 4 + byte] = pack_bf16x2(e2m1_level(code & 15u) * sc, e2m1_level(code >> 4) * sc);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int c = part * 8 + k;
-    *reinterpret_cast<uint4*>(kv + swz1k(r, c)) =
-        make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]);
+// Source of every entry of tile `tile` (threads 0..63, one entry each).
+__device__ __forceinline__ void tile_meta(const AttnParams& p, TileMeta& m, int row, int b, long long qp, long long lo,
+                                          long long pos0, int tile) {
+  if (threadIdx.x < kTile) {
+    const int r = threadIdx.x;
+    const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTile + r);
+    m.ptr[r] = s.valid ? s.ptr : nullptr;
+    m.sptr[r] = s.sptr;
+    m.rs[r] = s.rs;
+    m.fmt[r] = s.valid ? s.fmt : -1;
   }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_split_kernel(const AttnParams p) {
+// Gathers one tile into a KV stage (64 rows x 512 bf16, swizzled).  bf16 rows go by cp.async,
+// a warp copying 512 contiguous bytes per instruction; FP4 latents and FP8 window rows are
+// widened to bf16 in registers (exact) by four threads per row.
+__device__ __forceinline__ void load_tile(const TileMeta& m, uint8_t* kv, const void* any_valid) {
+  const int t = threadIdx.x;
+#pragma unroll 4
+  for (int k = 0; k < kTile / 4; ++k) {
+    const int r = 4 * k + (t >> 6), c = t & 63;
+    const int f = m.fmt[r];
+    if (f == CSA2_BF16 || f < 0) {
+      const uint8_t* src = f < 0 ? reinterpret_cast<const uint8_t*>(any_valid) : m.ptr[r];
+      cp_async16(kv + swz1k(r, c), src + c * 16, f >= 0);
+    }
+  }
+  const int r = t >> 2, quarter = t & 3;  // 128 dims per thread
+  const int f = m.fmt[r];
+  if (f == CSA2_FP8_E4M3_ROWSCALE) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int d0 = quarter * 128 + half * 64;
+      const uint4* src = reinterpret_cast<const uint4*>(m.ptr[r] + d0);
+      uint32_t outw[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 v = __ldg(src + q4);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          outw[q4 * 8 + 2 * k] = e4m3x2_to_bf16x2((uint16_t)(w4[k] & 0xffffu));
+          outw[q4 * 8 + 2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(w4[k] >> 16));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(kv + swz1k(r, d0 / 8 + k)) =
+            make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]);
+    }
+  } else if (f == CSA2_FP4_E2M1_G32 || f == CSA2_FP4_E2M1_G16) {
+    const int gsz = f == CSA2_FP4_E2M1_G32 ? 32 : 16;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int d0 = quarter * 128 + half * 64;
+      const uint4* src = reinterpret_cast<const uint4*>(m.ptr[r] + d0 / 2);
+      uint32_t outw[32];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint4 v = __ldg(src + h2);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+          for (int byte = 0; byte < 4; ++byte) {
+            const int ch = d0 + h2 * 32 + k * 8 + byte * 2;  // even channel of this byte
+            const float sc = e4m3_value(__ldg(m.sptr[r] + ch / gsz));
+            const uint32_t code = (w4[k] >> (8 * byte)) & 0xffu;
+            outw[h2 * 16 + k * 4 + byte] = pack_bf16x2(e2m1_level(code & 15u) * sc, e2m1_level(code >> 4) * sc);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(kv + swz1k(r, d0 / 8 + k)) =
+            make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]);
+    }
+  }
+}
+
+// One block: query row blockIdx.z, heads 16*blockIdx.y .. +15, split blockIdx.x of the row's
+// tiles.  Gathers run kStages tiles ahead.  Warps 0..3: QK for rows 16w..16w+15 of each tile
+// and the softmax; all 8 warps: PV for dims 64w..64w+63.
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_hg_kernel(const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* Qs = smem;
   uint8_t* KV = smem + kQBytes;
-  uint8_t* Ps = KV + 2 * kKVBytes;
+  uint8_t* Ps = KV + kStages * kKVBytes;
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(Ps + kPBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int row = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
+  const int row = blockIdx.z, hg = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
   const int b = p.seq_of_row[row];
   const long long qp = p.q_pos[row];
   const long long pos0 = p.swa_pos0[b];
@@ -199,238 +231,229 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_split_kernel(const AttnP
   const int t1 = (int)(((long long)n_tiles * (split + 1)) / n_split);
 
   rope_table(sm.cs, p, qp, 1.f);
-  if (t0 < t1) load_tile(p, sm, KV, 0, row, b, qp, lo, pos0, t0);
-  cp_async_commit();
-  __syncthreads();
-
-  // ---- q' = RoPE(q): head h = tid/8, dims 64*part .. ; part 7 holds the rotary dims
-  {
-    const int h = tid >> 3, part = tid & 7;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q) + ((size_t)row * kHeads + h) * (kHeadDim / 8) + part * 8;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint4 v = __ldg(src + k);
-      if (part == 7) {
+  for (int k = 0; k < kStages; ++k)
+    if (t0 + k < t1) tile_meta(p, sm.meta[(t0 + k) % kMetaSlots], row, b, qp, lo, pos0, t0 + k);
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kStages - 1; ++k) {
+    if (t0 + k < t1) load_tile(sm.meta[(t0 + k) % kMetaSlots], KV + ((t0 + k) % kStages) * kKVBytes, p.q);
+    cp_async_commit();
+  }
+  // ---- q' = RoPE(q) for this block's 16 heads (coalesced: consecutive threads, consecutive chunks)
+  {
+    const uint4* qsrc = reinterpret_cast<const uint4*>(p.q) + ((size_t)row * kHeads + kHG * hg) * (kHeadDim / 8);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = k * kAttnThreads + tid, h = idx >> 6, ch = idx & 63;
+      uint4 v = __ldg(qsrc + idx);
+      if (ch >= 56) {
         uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int i = k * 4 + j;  // rotary pair index
+          const int i = (ch - 56) * 4 + j;  // rotary pair index
           const float x = bf16_lo(w4[j]), y = bf16_hi(w4[j]);
           const float cs = sm.cs[i], sn = sm.cs[32 + i];
           w4[j] = pack_bf16x2(x * cs - y * sn, x * sn + y * cs);
         }
         v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      *reinterpret_cast<uint4*>(Qs + swz1k(h, part * 8 + k)) = v;
+      *reinterpret_cast<uint4*>(Qs + swz1k(h, ch)) = v;
     }
   }
 
-  const int hq = 16 * (wid & 3);   // QK: head block of this warp
-  const int rq = 16 * (wid >> 2);  // QK: row block of this warp
-  float m_run[2] = {-INFINITY, -INFINITY};  // heads hq+g, hq+g+8
+  float m_run[2] = {-INFINITY, -INFINITY};  // heads g, g+8 of the group
   float l_run[2] = {0.f, 0.f};
-  float acc_o[4][4][4];
+  float acc_o[8][4];
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) acc_o[mt][nt][0] = acc_o[mt][nt][1] = acc_o[mt][nt][2] = acc_o[mt][nt][3] = 0.f;
+  for (int nt = 0; nt < 8; ++nt) acc_o[nt][0] = acc_o[nt][1] = acc_o[nt][2] = acc_o[nt][3] = 0.f;
 
   const uint32_t qs_u = smem_u32(Qs), ps_u = smem_u32(Ps);
+  const int mi = lane >> 3, ri = lane & 7;
   for (int t = t0; t < t1; ++t) {
-    const int stage = (t - t0) & 1;
-    uint8_t* kv = KV + stage * kKVBytes;
-    if (t + 1 < t1) load_tile(p, sm, KV + (stage ^ 1) * kKVBytes, stage ^ 1, row, b, qp, lo, pos0, t + 1);
-    cp_async_commit();
-    cp_async_wait<1>();
+    const int st = t % kStages;
+    uint8_t* kv = KV + st * kKVBytes;
+    {
+      const int tn = t + kStages - 1;  // sources of tn were prepared one iteration ago
+      if (tn < t1) load_tile(sm.meta[tn % kMetaSlots], KV + (tn % kStages) * kKVBytes, p.q);
+      cp_async_commit();
+    }
+    cp_async_wait<kStages - 1>();
     __syncthreads();
     const uint32_t kv_u = smem_u32(kv);
+    const TileMeta& md = sm.meta[t % kMetaSlots];
 
-    // ---- S = q' K^T for heads hq..hq+15, rows rq..rq+15
-    float sacc[2][4];
+    float alpha[2] = {1.f, 1.f};
+    if (wid < 4) {
+      // ---- S = q' K^T: 16 heads x rows 16*wid .. +15 (two 8-row MMA tiles, two chains each)
+      float sa[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-    {
-      const int mi = lane >> 3, ri = lane & 7;
-      const int qh = hq + ri + (mi & 1) * 8;
-      const int kr = rq + ri + (mi >> 1) * 8;
-#pragma unroll 8
+      for (int a = 0; a < 4; ++a) sa[a][0] = sa[a][1] = sa[a][2] = sa[a][3] = 0.f;
+      const int qh = ri + (mi & 1) * 8;
+      const int kr = 16 * wid + ri + (mi >> 1) * 8;
+#pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
         ldsm_x4(a0, a1, a2, a3, qs_u + swz1k(qh, 2 * ks + (mi >> 1)));
         ldsm_x4(b0, b1, b2, b3, kv_u + swz1k(kr, 2 * ks + (mi & 1)));
-        mma_bf16(sacc[0], a0, a1, a2, a3, b0, b1);
-        mma_bf16(sacc[1], a0, a1, a2, a3, b2, b3);
+        mma_bf16(sa[(ks & 1) * 2 + 0], a0, a1, a2, a3, b0, b1);
+        mma_bf16(sa[(ks & 1) * 2 + 1], a0, a1, a2, a3, b2, b3);
       }
-    }
-    // ---- online softmax over the tile
-    float tmax[2] = {-INFINITY, -INFINITY};
+      // sacc[nt][e]: n-tile nt = rows 16*wid + 8*nt .. ; e as in the MMA C fragment
+      float sacc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = rq + 8 * nt + 2 * c + (e & 1);
-        const float z = sm.rowvalid[stage][r] ? sacc[nt][e] * p.scale * sm.rowscale[stage][r] : -INFINITY;
-        sacc[nt][e] = z;
-        tmax[e >> 1] = fmaxf(tmax[e >> 1], z);
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = sa[nt][e] + sa[2 + nt][e];
+      float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 16 * wid + 8 * nt + 2 * c + (e & 1);
+          const float z = md.fmt[r] >= 0 ? sacc[nt][e] * p.scale * md.rs[r] : -INFINITY;
+          sacc[nt][e] = z;
+          tmax[e >> 1] = fmaxf(tmax[e >> 1], z);
+        }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 1));
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 2));
+      }
+      if (c == 0) {
+        sm.red_max[wid][g] = tmax[0];
+        sm.red_max[wid][g + 8] = tmax[1];
+      }
+      asm volatile("bar.sync 2, 128;\n" ::: "memory");
+      float m_use[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = g + 8 * hh;
+        const float tm = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]), fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
+        const float m_new = fmaxf(m_run[hh], tm);
+        m_use[hh] = m_new == -INFINITY ? 0.f : m_new;
+        alpha[hh] = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - m_use[hh]);
+        m_run[hh] = m_new;
+      }
+      float psum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float pe[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pe[e] = __expf(sacc[nt][e] - m_use[e >> 1]);
+          psum[e >> 1] += pe[e];
+        }
+        const int r = 16 * wid + 8 * nt + 2 * c;
+        const float rs0 = md.rs[r], rs1 = md.rs[r + 1];
+        // P[h][r], P[h][r+1] as fp16 pairs; the FP8 row scale multiplies the weights
+        *reinterpret_cast<uint32_t*>(Ps + swzp(g, r >> 3) + (r & 7) * 2) = pack_f16x2(pe[0] * rs0, pe[1] * rs1);
+        *reinterpret_cast<uint32_t*>(Ps + swzp(g + 8, r >> 3) + (r & 7) * 2) = pack_f16x2(pe[2] * rs0, pe[3] * rs1);
       }
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 1));
-      tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 2));
-    }
-    if (c == 0) {
-      sm.red_max[wid >> 2][hq + g] = tmax[0];
-      sm.red_max[wid >> 2][hq + g + 8] = tmax[1];
+      for (int hh = 0; hh < 2; ++hh) {
+        psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 1);
+        psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 2);
+      }
+      if (c == 0) {
+        sm.red_sum[wid][g] = psum[0];
+        sm.red_sum[wid][g + 8] = psum[1];
+      }
     }
     __syncthreads();
-    float m_new[2], m_use[2], alpha[2];
+    // every warp: the running statistics of heads g, g+8 (identical in all warps)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const int h = hq + g + 8 * hh;
-      const float tm = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]), fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
-      m_new[hh] = fmaxf(m_run[hh], tm);
-      m_use[hh] = m_new[hh] == -INFINITY ? 0.f : m_new[hh];
-      alpha[hh] = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - m_use[hh]);
-    }
-    float psum[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int r = rq + 8 * nt + 2 * c;
-      float pe[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pe[e] = __expf(sacc[nt][e] - m_use[e >> 1]);
-        psum[e >> 1] += pe[e];
+      const int h = g + 8 * hh;
+      if (wid >= 4) {
+        const float tm = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]), fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
+        const float m_new = fmaxf(m_run[hh], tm);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        alpha[hh] = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - m_use);
+        m_run[hh] = m_new;
       }
-      const float rs0 = sm.rowscale[stage][r], rs1 = sm.rowscale[stage][r + 1];
-      // P[h][r], P[h][r+1] as fp16 pairs; the FP8 row scale multiplies the weights
-      *reinterpret_cast<uint32_t*>(Ps + swzp(hq + g, r >> 3) + (r & 7) * 2) = pack_f16x2(pe[0] * rs0, pe[1] * rs1);
-      *reinterpret_cast<uint32_t*>(Ps + swzp(hq + g + 8, r >> 3) + (r & 7) * 2) = pack_f16x2(pe[2] * rs0, pe[3] * rs1);
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 1);
-      psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 2);
-    }
-    if (c == 0) {
-      sm.red_sum[wid >> 2][hq + g] = psum[0];
-      sm.red_sum[wid >> 2][hq + g + 8] = psum[1];
-      if ((wid >> 2) == 0) {
-        sm.alpha[hq + g] = alpha[0];
-        sm.alpha[hq + g + 8] = alpha[1];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = hq + g + 8 * hh;
-      const float ts = sm.red_sum[0][h] + sm.red_sum[1][h] + sm.red_sum[2][h] + sm.red_sum[3][h];
+      const float ts = (sm.red_sum[0][h] + sm.red_sum[1][h]) + (sm.red_sum[2][h] + sm.red_sum[3][h]);
       l_run[hh] = l_run[hh] * alpha[hh] + ts;
-      m_run[hh] = m_new[hh];
     }
-    // ---- O = alpha O + P V for dims 32*wid .. 32*wid+31, all heads
+    // ---- O = alpha O + P V for dims 64*wid .. +63
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const float a_lo = sm.alpha[16 * mt + g], a_hi = sm.alpha[16 * mt + g + 8];
+    for (int nt = 0; nt < 8; ++nt) {
+      acc_o[nt][0] *= alpha[0];
+      acc_o[nt][1] *= alpha[0];
+      acc_o[nt][2] *= alpha[1];
+      acc_o[nt][3] *= alpha[1];
+    }
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        acc_o[mt][nt][0] *= a_lo;
-        acc_o[mt][nt][1] *= a_lo;
-        acc_o[mt][nt][2] *= a_hi;
-        acc_o[mt][nt][3] *= a_hi;
+    for (int ks = 0; ks < kTile / 16; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(a0, a1, a2, a3, ps_u + swzp(ri + (mi & 1) * 8, 2 * ks + (mi >> 1)));
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t vb[4];
+        const int vr = 16 * ks + ri + (mi & 1) * 8;
+        const int vc = (64 * wid + 16 * np) / 8 + (mi >> 1);
+        ldsm_x4_t(vb[0], vb[1], vb[2], vb[3], kv_u + swz1k(vr, vc));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vb[k] = bf16x2_to_f16x2(vb[k]);
+        mma_f16(acc_o[2 * np], a0, a1, a2, a3, vb[0], vb[1]);
+        mma_f16(acc_o[2 * np + 1], a0, a1, a2, a3, vb[2], vb[3]);
       }
     }
-    {
-      const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-      for (int ks = 0; ks < kTile / 16; ++ks) {
-        uint32_t vb[2][4];
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          const int vr = 16 * ks + ri + (mi & 1) * 8;
-          const int vc = (32 * wid + 16 * np) / 8 + (mi >> 1);
-          ldsm_x4_t(vb[np][0], vb[np][1], vb[np][2], vb[np][3], kv_u + swz1k(vr, vc));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) vb[np][k] = bf16x2_to_f16x2(vb[np][k]);
-        }
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          const int ph = 16 * mt + ri + (mi & 1) * 8;
-          ldsm_x4(a0, a1, a2, a3, ps_u + swzp(ph, 2 * ks + (mi >> 1)));
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt)
-            mma_f16(acc_o[mt][nt], a0, a1, a2, a3, vb[nt >> 1][2 * (nt & 1)], vb[nt >> 1][2 * (nt & 1) + 1]);
-        }
-      }
-    }
+    if (t + kStages < t1) tile_meta(p, sm.meta[(t + kStages) % kMetaSlots], row, b, qp, lo, pos0, t + kStages);
     __syncthreads();
   }
   cp_async_wait<0>();
 
+  const int h_lo = kHG * hg + g, h_hi = h_lo + 8;  // absolute heads of this thread
   if (n_split == 1) {
     // ---- finish the row: sink in the denominator, normalise, inverse RoPE
-    // per-head statistics from the QK warps (replicated across the 4 row blocks)
-    if ((wid >> 2) == 0 && c == 0) {
-      sm.red_max[0][hq + g] = m_run[0];
-      sm.red_max[0][hq + g + 8] = m_run[1];
-      sm.red_sum[0][hq + g] = l_run[0];
-      sm.red_sum[0][hq + g + 8] = l_run[1];
+    float f[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float sk = __ldg(p.sink + (hh ? h_hi : h_lo));
+      const float M = fmaxf(m_run[hh], sk);
+      const float em = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - M);
+      const float den = l_run[hh] * em + __expf(sk - M);
+      f[hh] = em / den;
+      if (p.sink_mass && wid == 0 && c == 0) p.sink_mass[(size_t)row * kHeads + (hh ? h_hi : h_lo)] = __expf(sk - M) / den;
     }
-    __syncthreads();
-    if (tid < kHeads) {
-      const float m = sm.red_max[0][tid], l = sm.red_sum[0][tid], sk = __ldg(p.sink + tid);
-      const float M = fmaxf(m, sk);
-      const float em = m == -INFINITY ? 0.f : __expf(m - M);
-      const float den = l * em + __expf(sk - M);
-      sm.alpha[tid] = em / den;  // multiplies the unnormalised output
-      if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + tid] = __expf(sk - M) / den;
-    }
-    __syncthreads();
     rope_table(sm.cs, p, qp, -1.f);
     __syncthreads();
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int hh = 0; hh < 2; ++hh) {
+      float* orow = p.out + ((size_t)row * kHeads + (hh ? h_hi : h_lo)) * kHeadDim;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int h = 16 * mt + g + 8 * hh;
-        const float f = sm.alpha[h];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const int d = 32 * wid + 8 * nt + 2 * c;
-          float x = acc_o[mt][nt][2 * hh] * f, y = acc_o[mt][nt][2 * hh + 1] * f;
-          if (d >= kHeadDim - kRopeDim) {
-            const int i = (d - (kHeadDim - kRopeDim)) >> 1;
-            const float cs = sm.cs[i], sn = sm.cs[32 + i];
-            const float xr = x * cs - y * sn, yr = x * sn + y * cs;
-            x = xr;
-            y = yr;
-          }
-          *reinterpret_cast<float2*>(p.out + ((size_t)row * kHeads + h) * kHeadDim + d) = make_float2(x, y);
+      for (int nt = 0; nt < 8; ++nt) {
+        const int d = 64 * wid + 8 * nt + 2 * c;
+        float x = acc_o[nt][2 * hh] * f[hh], y = acc_o[nt][2 * hh + 1] * f[hh];
+        if (d >= kHeadDim - kRopeDim) {
+          const int i = (d - (kHeadDim - kRopeDim)) >> 1;
+          const float cs = sm.cs[i], sn = sm.cs[32 + i];
+          const float xr = x * cs - y * sn, yr = x * sn + y * cs;
+          x = xr;
+          y = yr;
         }
+        *reinterpret_cast<float2*>(orow + d) = make_float2(x, y);
       }
+    }
     return;
   }
   // ---- partial results of this split
-  float* po = p.part_o + ((size_t)row * n_split + split) * kHeads * kHeadDim;
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
+  for (int hh = 0; hh < 2; ++hh) {
+    float* po = p.part_o + (((size_t)row * n_split + split) * kHeads + (hh ? h_hi : h_lo)) * kHeadDim;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = 16 * mt + g + 8 * hh;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int d = 32 * wid + 8 * nt + 2 * c;
-        *reinterpret_cast<float2*>(po + (size_t)h * kHeadDim + d) =
-            make_float2(acc_o[mt][nt][2 * hh], acc_o[mt][nt][2 * hh + 1]);
-      }
+    for (int nt = 0; nt < 8; ++nt) {
+      const int d = 64 * wid + 8 * nt + 2 * c;
+      *reinterpret_cast<float2*>(po + d) = make_float2(acc_o[nt][2 * hh], acc_o[nt][2 * hh + 1]);
     }
-  if ((wid >> 2) == 0 && c == 0) {
+  }
+  if (wid == 0 && c == 0) {
     float* pm = p.part_ml + ((size_t)row * n_split + split) * kHeads * 2;
-    pm[2 * (hq + g)] = m_run[0];
-    pm[2 * (hq + g) + 1] = l_run[0];
-    pm[2 * (hq + g + 8)] = m_run[1];
-    pm[2 * (hq + g + 8) + 1] = l_run[1];
+    pm[2 * h_lo] = m_run[0];
+    pm[2 * h_lo + 1] = l_run[0];
+    pm[2 * h_hi] = m_run[1];
+    pm[2 * h_hi + 1] = l_run[1];
   }
 }
 
@@ -516,10 +539,10 @@ int attn_smem_bytes() { return kAttnSmemBytes; }
 
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kAttnSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_hg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_split_kernel<<<dim3(n_split, p.n_rows), kAttnThreads, kAttnSmemBytes, stream>>>(p);
+  attn_hg_kernel<<<dim3(n_split, kHeads / kHG, p.n_rows), kAttnThreads, kAttnSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
   attn_combine_kernel<<<dim3(p.n_rows, kHeads / 4), 128, 0, stream>>>(p, n_split);

@@ -41,6 +41,17 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+// Histogram increment aggregated over the warp: lanes with equal bins add once (scores of a
+// row share their leading key bits, so plain per-lane atomics would serialise on one bin).
+// `bin` < 0 adds nothing.  All lanes of the warp must call it.
+__device__ __forceinline__ void warp_hist_add(int* hist, int bin) {
+  const unsigned act = __ballot_sync(0xffffffffu, bin >= 0);
+  if (bin >= 0) {
+    const unsigned peers = __match_any_sync(act, bin);
+    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+  }
+}
+
 template <int NW>
 struct Engine {
   static constexpr int NT = NW * 32;
@@ -168,9 +179,10 @@ __device__ __noinline__ void eng_select(const Engine<NW> e, int k) {
     const int shift = 24 - 8 * pass;
     for (int i = t; i < 256; i += NT) s.hist[i] = 0;
     e.sync();
-    for (int i = ln; i < mycnt; i += 32) {
-      const uint32_t key = kb[i];
-      if ((key & mask) == prefix) atomicAdd(&s.hist[(key >> shift) & 255u], 1);
+    for (int base = 0; base < mycnt; base += 32) {
+      const int i = base + ln;
+      const uint32_t key = i < mycnt ? kb[i] : 0u;
+      warp_hist_add(s.hist, (i < mycnt && (key & mask) == prefix) ? (int)((key >> shift) & 255u) : -1);
     }
     e.sync();
     eng_pick_digit(e, krem, true);
@@ -190,9 +202,11 @@ __device__ __noinline__ void eng_select(const Engine<NW> e, int k) {
       const int shift = 24 - 8 * pass;
       for (int i = t; i < 256; i += NT) s.hist[i] = 0;
       e.sync();
-      for (int i = ln; i < mycnt; i += 32) {
-        const uint32_t j = static_cast<uint32_t>(jb[i]);
-        if (kb[i] == thr && (j & jm) == jp) atomicAdd(&s.hist[(j >> shift) & 255u], 1);
+      for (int base = 0; base < mycnt; base += 32) {
+        const int i = base + ln;
+        const bool in = i < mycnt;
+        const uint32_t j = in ? static_cast<uint32_t>(jb[i]) : 0u;
+        warp_hist_add(s.hist, (in && kb[i] == thr && (j & jm) == jp) ? (int)((j >> shift) & 255u) : -1);
       }
       e.sync();
       eng_pick_digit(e, jrem, false);
