@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "CSA2 decode queries/s and HBM GB/s at N=64K; prefill indexer TFLOP/s"
-SCAN_SOURCES = ["index_scan.cu", "select.cuh", "common.cuh"]
+SCAN_SOURCES = ["idx_mma.cu", "tc05.cuh", "select.cuh", "common.cuh"]
 
 
 def parse_args(argv=None):
@@ -387,8 +387,8 @@ def run_gb300(args, world, rank, local):
     scan_avg = statistics.mean(scan_ms) / 1e3
     achieved = scan_bytes / scan_avg / 1e9
     src_hash = source_hash(SCAN_SOURCES)
-    traffic = ncu_traffic("index_scan_batched_decode", src_hash, wl.B * wl.N)
-    roofline = {"bound": "hbm", "kernel": "index_scan_kernel<bf16> (indexer scan + per-segment top-K)",
+    traffic = ncu_traffic("idx_mma_decode_batched_decode", src_hash, wl.B * wl.N)
+    roofline = {"bound": "hbm", "kernel": "idx_mma_decode_kernel (tcgen05 indexer scan + fused per-segment top-K)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
                 "fallback 6.8 TB/s", "traffic": traffic,
