@@ -140,6 +140,30 @@ size_t csa2_topk_workspace_size(const csa2_topk_args* a);
 csa2_status csa2_topk(const csa2_topk_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * csa2_topk_static - csa2_topk without a caller-provided workspace.  (The pages describe no
+ * counterpart: this is a library convenience, not part of the method.)
+ *
+ * For callers that cannot allocate device memory - a framework capturing the stream into a
+ * CUDA graph while it owns every allocation, or a runtime with a fixed memory budget that
+ * admits no allocation once it runs - the scratch memory of csa2_topk comes from a
+ * device-global array inside the library, CSA2_TOPK_STATIC_SCRATCH_BYTES bytes that every
+ * GPU loading the library holds until the process exits.  The call allocates nothing; the
+ * caller passes inputs and outputs exactly as for csa2_topk (a->workspace is ignored).
+ *   - Results are those of csa2_topk.
+ *   - Requests whose scratch would exceed the array return CSA2_EUNSUPPORTED.  The scratch
+ *     is 8 bytes per (row segment, K) pair plus 8 per row segment, and rows are split into
+ *     at most one segment per SM in total, so up to K = 1024 on a 240-SM GPU it fits.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls that may overlap on the GPU - on
+ *     different streams without ordering between them - race on it and must be serialised
+ *     by the caller.
+ * ------------------------------------------------------------------------------------ */
+#define CSA2_TOPK_STATIC_SCRATCH_BYTES (2u << 20)
+csa2_status csa2_topk_static(const csa2_topk_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * csa2_block_pool - the hierarchical candidate pool of the first decoder indexer.
  *
  * The first decoder indexer cuts the positions into blocks, rates each block by its best

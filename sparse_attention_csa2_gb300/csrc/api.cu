@@ -242,6 +242,9 @@ size_t lists_bytes(int n_rows, int n_seg, int K) {
 }
 
 }  // namespace
+
+int topk_segments(int n_rows, long long L) { return topk_plan(n_rows, L).n_seg; }
+
 }  // namespace csa2
 
 using namespace csa2;
