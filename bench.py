@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-iters", type=int, default=10)
+    ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
+    ap.add_argument("--prefill-t", type=int, default=4096, help="queries of the prefill chunk (profiling)")
     return ap.parse_args(argv)
 
 
@@ -247,6 +249,8 @@ def run_prefill(args, local, peaks):
     import synth
     import sparse_attention_csa2_gb300 as S
     wl = synth.WORKLOADS["prefill_chunk"]
+    if args.prefill_t != wl.T:
+        wl = synth.scaled(wl, T=args.prefill_t, N=wl.P0 + args.prefill_t)
     inp = synth.make_inputs(wl, seed=4)
     dv = synth.to_device(inp, f"cuda:{local}")
     p, rw, c, lay = dv["params"], dv["rows"], dv["cache"], dv["layers"][0]
@@ -297,6 +301,13 @@ def run_gb300(args, world, rank, local):
     import sparse_attention_csa2_gb300 as S
 
     torch.cuda.set_device(local)
+    if args.prefill_only:
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except (OSError, ValueError):
+            peaks = None
+        print(json.dumps({"prefill": run_prefill(args, local, peaks)}), flush=True)
+        return 0
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     wl = workload(args)

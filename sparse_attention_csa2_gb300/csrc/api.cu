@@ -71,7 +71,8 @@ int tc05_segments(int n_rows, long long L, int unit) {
   int n = scan_segments(n_rows, L);
   const long long units = (L + unit - 1) / unit;
   const int max_blocks = mma_decode_max_seg_blocks();
-  while ((units + n - 1) / n > max_blocks) ++n;
+  const long long max_units = mma_decode_max_segment() / unit;  // a segment's keys fit in shared memory
+  while ((units + n - 1) / n > max_blocks || (units + n - 1) / n > max_units) ++n;
   return n;
 }
 
@@ -408,6 +409,7 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     else
       n_seg = scan_segments(n_rows, L);
     ws += lists_bytes(n_rows, n_seg, a->K);
+    if (n_seg > 1) ws += align_up((size_t)n_rows * 4);  // per-row completion counters
     if (a->mode == CSA2_MODE_FULL_POOL) {
       const long long nb = (ix->n_records + a->block_size - 1) / a->block_size;
       ws += align_up((size_t)n_rows * nb * 4) + align_up((size_t)n_rows * a->n_keep * 4);
@@ -488,12 +490,19 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       ic.cand = a->pool;
       ic.L = a->pool_len;
     }
-    if (scan_path(&ic, true) == ScanPath::kTc05Decode && a->mode != CSA2_MODE_FULL_POOL) p.unit = 128;
+    const bool tc05 = scan_path(&ic, true) == ScanPath::kTc05Decode;
+    if (tc05 && a->mode != CSA2_MODE_FULL_POOL) p.unit = 128;
     p.dev_status = at.dev_status;
+    const bool fused_merge = tc05 && mma_decode_can_merge(n_seg, a->K);
+    if (n_seg > 1) {
+      p.row_done = c.take<int32_t>((size_t)n_rows);
+      if (fused_merge && cudaMemsetAsync(p.row_done, 0, (size_t)n_rows * 4, s) != cudaSuccess) return CSA2_ECUDA;
+      if (!fused_merge) p.row_done = nullptr;
+    }
     e = launch_scan(p, &ic, true, n_seg, s);
     if (e != cudaSuccess) return CSA2_ECUDA;
     mark(1);
-    if (n_seg > 1) {
+    if (n_seg > 1 && !fused_merge) {
       FeedParams m{};
       m.n_rows = n_rows;
       m.K = a->K;
@@ -534,7 +543,11 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
   decode_ws(a, &n_seg);
   int n = 0;
   if (a->mode != CSA2_MODE_REUSE) {
-    n += 1 + (n_seg > 1 ? 1 : 0);
+    csa2_index_args ic = a->index;
+    ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
+    ic.block_max = nullptr;
+    const bool fused_merge = scan_path(&ic, true) == ScanPath::kTc05Decode && mma_decode_can_merge(n_seg, a->K);
+    n += 1 + (n_seg > 1 && !fused_merge ? 1 : 0);  // the tcgen05 scan merges its segments itself
     if (a->mode == CSA2_MODE_FULL_POOL) n += 2;
   }
   n += 1 + (attn_splits(a->attn.n_rows, a->K, a->attn.window) > 1 ? 1 : 0);

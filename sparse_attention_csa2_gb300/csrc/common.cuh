@@ -151,6 +151,13 @@ __device__ __forceinline__ int block_sum(int v, int* warp_tmp) {
   return total;
 }
 
+// Bit mask of the lanes below the calling one.
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
+#include "array_topk.cuh"
 #include "select.cuh"
 #include "tc05.cuh"
 
@@ -40,12 +41,13 @@ __device__ __forceinline__ void report_timeout(int* flag, int32_t* dev_status) {
 }
 
 // ===================================================================================== decode
-constexpr int kDecStages = 5;
+constexpr int kDecStages = 4;
 constexpr int kDecEpiFirst = 4;
 constexpr int kDecEpiWarps = 8;  // two groups of 4 warps (one per TMEM lane quarter), alternate tiles
 constexpr int kDecThreads = (kDecEpiFirst + kDecEpiWarps) * 32;  // warp 0 TMA, warp 1 MMA + TMEM
 constexpr int kDecQHalf = 32 * 128;  // 32 heads x 64 dims x 2 B
 constexpr uint32_t kDecTmemCols = 64;
+constexpr int kDecSegMax = 16384;    // records of one segment (their keys stay in shared memory)
 
 struct DecBars {
   uint64_t full[kDecStages], empty[kDecStages], tfull[2], tempty[2], qfull;
@@ -54,7 +56,63 @@ struct DecBars {
   int issued;     // tiles whose TMA loads were issued
   int consumed;   // tiles whose MMAs were issued
   int drained;    // tiles whose accumulators the epilogue read
+  int last;       // this block is the last segment of its row to finish
 };
+
+// The last segment block of a row merges the row's lists: every list entry's key goes into
+// the key array (entries below the largest per-segment K-th key cannot be selected and are
+// left out, and the level-1 histogram is counted on the way), and the K best, in position
+// order, become the row's indices.  The lists (and, with room in the scratch, their
+// positions) come into shared memory in one batch of asynchronous copies, so the merge waits
+// for the L2 only once.
+template <int NW>
+__device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const ScanParams& p, int row, int n_seg) {
+  constexpr int NT = NW * 32;
+  const int K = p.K, n = n_seg * K;
+  const uint32_t* lists = p.seg_keys + (size_t)row * n_seg * K;
+  const int32_t* pos = p.seg_pos + (size_t)row * n_seg * K;
+  const int lw = ArrSel<NW>::list_words(n);
+  int32_t* pos_s = sel.scratch != nullptr && lw + n <= sel.scratch_cap
+                       ? reinterpret_cast<int32_t*>(sel.scratch + lw) : nullptr;
+  const bool vec = (K & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.seg_keys) | reinterpret_cast<uintptr_t>(p.seg_pos)) & 15) == 0;
+  if (vec) {
+    for (int c = sel.tid; c < n / 4; c += NT) {
+      cp_async16(keys + 4 * c, lists + 4 * c, true);
+      if (pos_s) cp_async16(pos_s + 4 * c, pos + 4 * c, true);
+    }
+    cp_async_commit();
+  } else {
+    pos_s = nullptr;
+    for (int f = sel.tid; f < n; f += NT) keys[f] = __ldcg(lists + f);
+  }
+  // segment counts and K-th keys staged in shared memory (n_seg <= 64)
+  int* cnt_s = reinterpret_cast<int*>(sel.sh->aux);
+  uint32_t* thr_s = sel.sh->aux + 64;
+  for (int s = sel.tid; s < n_seg; s += NT) {
+    cnt_s[s] = __ldcg(p.seg_cnt + (size_t)row * n_seg + s);
+    thr_s[s] = __ldcg(p.seg_thr + (size_t)row * n_seg + s);
+  }
+  sel.zero_hist(kHistBins);
+  cp_async_wait<0>();
+  sel.sync();
+  uint32_t thr0 = 0u;
+  for (int s = 0; s < n_seg; ++s) thr0 = max(thr0, thr_s[s]);
+  // unused list slots and keys below thr0 leave the candidates
+  for (int sg = 0; sg < n_seg; ++sg) {
+    const int cnt = cnt_s[sg];
+    for (int j = sel.tid; j < K; j += NT) {
+      uint32_t key = keys[sg * K + j];
+      if (j >= cnt || key < thr0) key = 0u;
+      keys[sg * K + j] = key;
+      hist_add(sel.sh->hist, key >> 20, key != 0u);
+    }
+  }
+  sel.sync();
+  arr_threshold(sel, keys, n, K, true);
+  int32_t* out = p.idx + (size_t)row * K;
+  const int kept = arr_compact(sel, keys, n, [&](int r, int f) { out[r] = pos_s ? pos_s[f] : __ldcg(pos + f); });
+  for (int i = kept + sel.tid; i < K; i += NT) out[i] = -1;
+}
 
 __global__ void __launch_bounds__(kDecThreads, 1)
     idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
@@ -66,6 +124,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   DecBars& bars = *reinterpret_cast<DecBars*>(qs + 2 * kDecQHalf);
   uint8_t* rest = reinterpret_cast<uint8_t*>(&bars + 1);
   rest = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rest) + 15) & ~static_cast<uintptr_t>(15));
+  ArrSelShared* selsh = reinterpret_cast<ArrSelShared*>(rest);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(selsh + 1);  // [kDecSegMax] keys in record order
+  uint32_t* bkeys = keys + kDecSegMax;                      // block maxima of the segment (keys)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
@@ -77,19 +138,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   split_range(n_units, n_seg, seg, u0, u1);
   const long long e0 = u0 * U, e1 = min(u1 * U, L_row);
   const int n_tiles = e1 > e0 ? (int)((e1 - e0 + kTileKeys - 1) / kTileKeys) : 0;
+  const int seg_len = (int)(e1 - e0);
 
   const bool do_topk = p.K > 0;
-  Engine<kDecEpiWarps> eng;
-  eng.sh = reinterpret_cast<EngShared*>(rest);
-  eng.cap = p.K + kRoundEntries;
-  eng.keys = reinterpret_cast<uint32_t*>(rest + sizeof(EngShared));
-  eng.js = reinterpret_cast<int32_t*>(eng.keys + kDecEpiWarps * eng.cap);
-  eng.out_key = reinterpret_cast<uint32_t*>(eng.js + kDecEpiWarps * eng.cap);
-  eng.out_j = reinterpret_cast<int32_t*>(eng.out_key + p.K);
-  eng.bar_id = 1;
-  eng.tid = tid - kDecEpiFirst * 32;
-  uint32_t* bkeys = reinterpret_cast<uint32_t*>(do_topk ? reinterpret_cast<uint8_t*>(eng.out_j + p.K)
-                                                         : rest + sizeof(EngShared));
+  ArrSel<kDecThreads / 32> sel;  // the whole block, once the stream is done
+  sel.sh = selsh;
+  sel.bar_id = 0;
+  sel.tid = tid;
   const int bs = p.block_max ? U : 1;
   const int seg_blocks = p.block_max ? (int)((e1 - e0 + bs - 1) / bs) : 0;
 
@@ -108,8 +163,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     tc05::fence_barrier_init();
   }
   if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, kDecTmemCols);
-  if (warp >= kDecEpiFirst)
-    for (int i = eng.tid; i < seg_blocks; i += kDecEpiWarps * 32) bkeys[i] = 0u;
+  for (int i = tid; i < seg_blocks; i += kDecThreads) bkeys[i] = 0u;
+  if (do_topk) sel.zero_hist(kHistBins);
   tc05::fence_before();
   __syncthreads();
   tc05::fence_after();
@@ -135,6 +190,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         bars.issued = t + 1;
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
@@ -162,29 +218,28 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       if (!ok) report_timeout(&bars.timeout, p.dev_status);
     }
+    __syncwarp();
   } else if (warp >= kDecEpiFirst) {
     // ---------------------------------------------------------------- epilogue
-    // group g = 0 drains the even tiles (accumulator 0), group 1 the odd ones (accumulator 1)
+    // group g = 0 drains the even tiles (accumulator 0), group 1 the odd ones (accumulator 1);
+    // each record's score goes to the key array (in record order) and the level-1 histogram
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int grp = (warp - kDecEpiFirst) >> 2;
     float w[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) w[h] = __ldg(p.w + (size_t)row * kIdxHeads + h);
-    if (do_topk) eng_init(eng);
-    int cnt = 0;
-    uint32_t thr = 0u;
     bool dead = false;
     float* srow = p.scores ? p.scores + (size_t)row * p.scores_stride : nullptr;
     const int n_pairs = (n_tiles + 1) / 2;
     for (int pr = 0; pr < n_pairs; ++pr) {
       const int t = 2 * pr + grp, a = grp;
-      const bool have = t < n_tiles;
-      if (have && !dead && !tc05::mbar_wait(&bars.tfull[a], pr & 1)) {
+      if (t >= n_tiles) continue;
+      if (!dead && !tc05::mbar_wait(&bars.tfull[a], pr & 1)) {
         dead = true;
         if (lane == 0) report_timeout(&bars.timeout, p.dev_status);
       }
       float sc = 0.f;
-      if (have && !dead) {
+      if (!dead) {
         tc05::fence_after();
         uint32_t v[32];
         tc05::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * 32), v);
@@ -196,40 +251,68 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int h = 0; h < 32; ++h) sc = fmaf(w[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
         if (warp == kDecEpiFirst + 4 * grp && lane == 0) atomicMax(&bars.drained, t + 1);
       }
-      const long long j = e0 + (long long)t * kTileKeys + 32 * quarter + lane;
-      const bool valid = have && !dead && j < e1;
-      if (srow && valid) srow[j] = sc;
-      if (seg_blocks && valid) atomicMax(&bkeys[(j - e0) / bs], score_key(sc));
-      if (do_topk) {
-        eng_append(eng, cnt, thr, valid, score_key(sc), (int32_t)j);
-        if ((pr & 3) == 3) thr = eng_check(eng, p.K, cnt);
+      const int jl = t * kTileKeys + 32 * quarter + lane;  // record index within the segment
+      const bool valid = !dead && jl < seg_len;
+      const uint32_t key = valid ? score_key(sc) : 0u;
+      if (do_topk && jl < seg_len) {
+        keys[jl] = key;
+        if (valid) atomicAdd(&selsh->hist[key >> 20], 1);
       }
+      if (srow && valid) srow[e0 + jl] = sc;
+      if (seg_blocks && valid) atomicMax(&bkeys[jl / bs], key);
     }
-    if (seg_blocks) {
-      asm volatile("bar.sync 1, %0;\n" ::"n"(kDecEpiWarps * 32) : "memory");
-      for (int i = eng.tid; i < seg_blocks; i += kDecEpiWarps * 32)
-        p.block_max[(size_t)row * p.bmax_stride + e0 / bs + i] = bkeys[i] ? key_score(bkeys[i]) : -INFINITY;
-    }
+  }
+
+  // ---------------------------------------------------------------- tail (whole block)
+  __syncthreads();
+  {
+    // Once every tile has been drained no copy or MMA touches the ring and the query tile any
+    // more (the copies and MMAs completed through the mbarriers the epilogue waited on), so
+    // they serve as the selection's scratch (not after a timeout: copies may be in flight
+    // then).
+    constexpr int kScratchWords = (kDecStages * kKeyTile + 2 * kDecQHalf) / 4;
+    uint32_t* scratch = bars.timeout ? nullptr : reinterpret_cast<uint32_t*>(ring);
+    sel.scratch = scratch;
+    sel.scratch_cap = scratch ? kScratchWords : 0;
+    for (int i = tid; i < seg_blocks; i += kDecThreads)
+      p.block_max[(size_t)row * p.bmax_stride + e0 / bs + i] = bkeys[i] ? key_score(bkeys[i]) : -INFINITY;
     if (seg == n_seg - 1) {
+      float* srow = p.scores ? p.scores + (size_t)row * p.scores_stride : nullptr;
       if (srow)
-        for (long long jj = L_row + eng.tid; jj < p.scores_len; jj += kDecEpiWarps * 32) srow[jj] = -INFINITY;
+        for (long long jj = L_row + tid; jj < p.scores_len; jj += kDecThreads) srow[jj] = -INFINITY;
       if (p.block_max)
-        for (long long blk = (L_row + bs - 1) / bs + eng.tid; blk < p.n_blocks; blk += kDecEpiWarps * 32)
+        for (long long blk = (L_row + bs - 1) / bs + tid; blk < p.n_blocks; blk += kDecThreads)
           p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
     }
     if (do_topk) {
-      uint32_t* thr_out = n_seg > 1 ? p.seg_thr + (size_t)row * n_seg + seg : nullptr;
-      const int n = eng_finish(eng, p.K, cnt, thr_out);
+      arr_threshold(sel, keys, seg_len, p.K, true);
       if (n_seg == 1) {
         int32_t* out = p.idx + (size_t)row * p.K;
-        for (int i = eng.tid; i < p.K; i += kDecEpiWarps * 32) out[i] = i < n ? eng.out_j[i] : -1;
+        const int kept = arr_compact(sel, keys, seg_len, [&](int r, int i) { out[r] = (int32_t)(e0 + i); });
+        for (int i = kept + tid; i < p.K; i += kDecThreads) out[i] = -1;
       } else {
         const size_t o = ((size_t)row * n_seg + seg) * p.K;
-        for (int i = eng.tid; i < n; i += kDecEpiWarps * 32) {
-          p.seg_keys[o + i] = eng.out_key[i];
-          p.seg_pos[o + i] = eng.out_j[i];
+        const int kept = arr_compact(sel, keys, seg_len, [&](int r, int i) {
+          p.seg_keys[o + r] = keys[i];
+          p.seg_pos[o + r] = (int32_t)(e0 + i);
+        });
+        if (sel.tid == 0) {
+          p.seg_cnt[(size_t)row * n_seg + seg] = kept;
+          p.seg_thr[(size_t)row * n_seg + seg] = kept >= p.K ? selsh->thr : 0u;
         }
-        if (eng.tid == 0) p.seg_cnt[(size_t)row * n_seg + seg] = n;
+        if (p.row_done != nullptr) {
+          // The last segment of the row to finish merges every segment's list (no waiting:
+          // the block that sees the count reach n_seg - 1 knows the others have published).
+          __threadfence();
+          sel.sync();
+          if (sel.tid == 0) bars.last = atomicAdd(p.row_done + row, 1) == n_seg - 1;
+          sel.sync();
+          if (bars.last) {
+            __threadfence();
+            merge_row_lists(sel, keys, p, row, n_seg);
+            if (sel.tid == 0) p.row_done[row] = 0;
+          }
+        }
       }
     }
   }
@@ -353,6 +436,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
       if (!ok) report_timeout(&bars.timeout, p.dev_status);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -395,6 +479,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
       if (!ok) report_timeout(&bars.timeout, p.dev_status);
     }
+    __syncwarp();
   } else if (warp >= kPreEpiFirst) {
     // ---------------------------------------------------------------- epilogue
     const int e = warp - kPreEpiFirst;       // 0..7
@@ -502,10 +587,9 @@ bool make_tmap(CUtensorMap* tm, const void* base, unsigned long long rows, unsig
 }
 
 size_t dec_smem_bytes(int K, int max_seg_blocks) {
-  size_t s = 1024 + (size_t)kDecStages * kKeyTile + 2 * kDecQHalf + sizeof(DecBars) + 16 + sizeof(EngShared);
-  if (K > 0) s += (size_t)kDecEpiWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;
-  s += (size_t)max_seg_blocks * 4;
-  return s;
+  (void)K;
+  return 1024 + (size_t)kDecStages * kKeyTile + 2 * kDecQHalf + sizeof(DecBars) + 16 + sizeof(ArrSelShared) +
+         (size_t)kDecSegMax * 4 + (size_t)max_seg_blocks * 4;
 }
 
 }  // namespace
@@ -513,6 +597,9 @@ size_t dec_smem_bytes(int K, int max_seg_blocks) {
 bool mma_indexer_available() { return encode_fn() != nullptr; }
 
 int mma_decode_max_seg_blocks() { return 2048; }
+
+int mma_decode_max_segment() { return kDecSegMax; }
+bool mma_decode_can_merge(int n_seg, int K) { return n_seg <= 64 && (long long)n_seg * K <= kDecSegMax; }
 
 size_t mma_decode_smem_bytes(int K, int max_seg_blocks) { return dec_smem_bytes(K, max_seg_blocks); }
 

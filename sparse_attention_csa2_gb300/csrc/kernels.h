@@ -33,6 +33,7 @@ struct ScanParams {
   int32_t* seg_pos;
   int32_t* seg_cnt;           // [n_rows, n_seg]
   uint32_t* seg_thr;          // [n_rows, n_seg] K-th key of each full segment list, else 0
+  int32_t* row_done;          // tcgen05 decode: [n_rows] zeroed counters; the last segment merges
   int32_t* dev_status;        // optional: CSA2_ETIMEOUT when a bounded wait gives up
 };
 
@@ -41,6 +42,8 @@ size_t scan_smem_bytes(bool fp8, int K);
 // tcgen05 indexer (bf16 keys, records in place): decode rows and prefill tiles.
 bool mma_indexer_available();
 int mma_decode_max_seg_blocks();
+int mma_decode_max_segment();  // most records one decode segment may hold
+bool mma_decode_can_merge(int n_seg, int K);  // the decode scan can merge its segments' lists itself
 cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
                               cudaStream_t stream);
 cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream);

@@ -14,7 +14,8 @@
 // MSB-first 8-bit radix select finds the K-th key thr and how many entries equal to it to
 // keep; if that is fewer than all of them, a second radix select over the indices of the
 // tied entries finds the last index to keep.  Each warp then compacts its buffer.
-// `eng_finish` emits the survivors sorted by index (rank counting).
+// Feeders append each warp's entries in ascending index order and compaction keeps order, so
+// every buffer stays sorted by index; `eng_finish` merges them by binary search.
 #pragma once
 
 #include "common.cuh"
@@ -33,23 +34,15 @@ struct EngShared {
   int sel_digit;
   int sel_before;
   int sel_count;
+  uint32_t all_and;  // AND / OR of every key: bits where they agree need no radix pass
+  uint32_t all_or;
 };
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// Histogram increment aggregated over the warp: lanes with equal bins add once (scores of a
-// row share their leading key bits, so plain per-lane atomics would serialise on one bin).
-// `bin` < 0 adds nothing.  All lanes of the warp must call it.
+// Histogram increment; `bin` < 0 adds nothing.  A plain shared atomic: on sm_103a
+// aggregating equal bins over the warp first (match.any) costs far more than the atomics' own
+// serialisation, even when every lane hits the same bin.
 __device__ __forceinline__ void warp_hist_add(int* hist, int bin) {
-  const unsigned act = __ballot_sync(0xffffffffu, bin >= 0);
-  if (bin >= 0) {
-    const unsigned peers = __match_any_sync(act, bin);
-    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-  }
+  if (bin >= 0) atomicAdd(&hist[bin], 1);
 }
 
 template <int NW>
@@ -171,25 +164,52 @@ __device__ __noinline__ void eng_select(const Engine<NW> e, int k) {
   }
   uint32_t* kb = e.keys + w * e.cap;
   int32_t* jb = e.js + w * e.cap;
-  // ---- the k-th best key: MSB-first radix over the keys
-  uint32_t prefix = 0u, mask = 0u;
-  int krem = k, n_tied = 0;
+  // ---- bits shared by every key: no pass needed for them
+  uint32_t k_and = 0xffffffffu, k_or = 0u;
+  for (int i = ln; i < mycnt; i += 32) {
+    k_and &= kb[i];
+    k_or |= kb[i];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    k_and &= __shfl_xor_sync(0xffffffffu, k_and, o);
+    k_or |= __shfl_xor_sync(0xffffffffu, k_or, o);
+  }
+  if (t == 0) {
+    s.all_and = 0xffffffffu;
+    s.all_or = 0u;
+  }
+  e.sync();
+  if (ln == 0 && mycnt > 0) {
+    atomicAnd(&s.all_and, k_and);
+    atomicOr(&s.all_or, k_or);
+  }
+  e.sync();
+  const uint32_t diff = s.all_and ^ s.all_or;
+  // ---- the k-th best key: MSB-first radix over the bits where keys differ
+  int hi = diff ? 31 - __clz(diff) : -1;
+  uint32_t mask = hi >= 0 ? ~((2u << hi) - 1u) : 0xffffffffu;  // (2u << 31) wraps to 0: all bits differ
+  if (hi == 31) mask = 0u;
+  uint32_t prefix = s.all_and & mask;
+  int krem = k, n_tied = total;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
+  while (hi >= 0) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (hi - lo == 31) ? 0xffffffffu : ((1u << (hi - lo + 1)) - 1u);
     for (int i = t; i < 256; i += NT) s.hist[i] = 0;
     e.sync();
     for (int base = 0; base < mycnt; base += 32) {
       const int i = base + ln;
       const uint32_t key = i < mycnt ? kb[i] : 0u;
-      warp_hist_add(s.hist, (i < mycnt && (key & mask) == prefix) ? (int)((key >> shift) & 255u) : -1);
+      warp_hist_add(s.hist, (i < mycnt && (key & mask) == prefix) ? (int)((key >> lo) & dmask) : -1);
     }
     e.sync();
     eng_pick_digit(e, krem, true);
-    prefix |= static_cast<uint32_t>(s.sel_digit) << shift;
-    mask |= 0xffu << shift;
+    prefix |= static_cast<uint32_t>(s.sel_digit) << lo;
+    mask |= dmask << lo;
     krem -= s.sel_before;
     n_tied = s.sel_count;
+    hi = lo - 1;
   }
   const uint32_t thr = prefix;
   // ---- ties at thr: keep the krem lowest indices (indices are distinct)
@@ -260,48 +280,35 @@ __device__ __forceinline__ uint32_t eng_check(const Engine<NW>& e, int k, int& c
 // key <= it, and the row's k-th key is at least it).  k <= kEngMaxK.
 template <int NW>
 __device__ int eng_finish(const Engine<NW>& e, int k, int cnt, uint32_t* thr_out) {
-  constexpr int NT = NW * 32;
-  constexpr int PER = (kEngMaxK + NT - 1) / NT;
   if (e.lane() == 0) e.sh->warp_cnt[e.warp()] = cnt;
   e.sync();
   eng_select(e, k);
-  int off = 0, total = 0;
+  int total = 0;
 #pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    const int c = e.sh->warp_cnt[i];
-    off += (i < e.warp()) ? c : 0;
-    total += c;
-  }
-  const int mycnt = e.sh->warp_cnt[e.warp()];
-  const uint32_t* gk = e.keys + e.warp() * e.cap;
-  const int32_t* gj = e.js + e.warp() * e.cap;
+  for (int i = 0; i < NW; ++i) total += e.sh->warp_cnt[i];
+  // Every warp's buffer is in ascending entry order (appends arrive in order and compaction
+  // keeps it), so an entry's rank among all survivors is its index in its own buffer plus,
+  // for every other warp, the number of that warp's survivors with a smaller index.
+  const int w = e.warp();
+  const int mycnt = e.sh->warp_cnt[w];
+  const uint32_t* gk = e.keys + w * e.cap;
+  const int32_t* gj = e.js + w * e.cap;
   for (int i = e.lane(); i < mycnt; i += 32) {
-    e.out_key[off + i] = gk[i];
-    e.out_j[off + i] = gj[i];
-  }
-  e.sync();
-  // rank of an entry = number of survivors with a smaller index
-  uint32_t mk[PER];
-  int32_t mj[PER], mr[PER];
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int i = e.tid + q * NT;
-    mr[q] = -1;
-    if (i < total) {
-      mk[q] = e.out_key[i];
-      mj[q] = e.out_j[i];
-      int r = 0;
-      for (int m = 0; m < total; ++m) r += e.out_j[m] < mj[q];
-      mr[q] = r;
+    const int32_t ji = gj[i];
+    int r = i;
+#pragma unroll 1
+    for (int w2 = 0; w2 < NW; ++w2) {
+      if (w2 == w) continue;
+      const int32_t* bj = e.js + w2 * e.cap;
+      int lo2 = 0, hi2 = e.sh->warp_cnt[w2];
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2) >> 1;
+        if (bj[mid] < ji) lo2 = mid + 1; else hi2 = mid;
+      }
+      r += lo2;
     }
-  }
-  e.sync();
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    if (mr[q] >= 0) {
-      e.out_key[mr[q]] = mk[q];
-      e.out_j[mr[q]] = mj[q];
-    }
+    e.out_key[r] = gk[i];
+    e.out_j[r] = ji;
   }
   if (e.tid == 0 && thr_out) *thr_out = total >= k ? e.sh->thr : 0u;
   e.sync();
