@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "CSA2 decode queries/s and HBM GB/s at N=64K; prefill indexer TFLOP/s"
-SCAN_SOURCES = ["idx_mma.cu", "tc05.cuh", "select.cuh", "common.cuh"]
+SCAN_SOURCES = ["idx_mma.cu", "array_topk.cuh", "tc05.cuh", "select.cuh", "common.cuh"]
 
 
 def parse_args(argv=None):
