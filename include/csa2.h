@@ -230,10 +230,13 @@ typedef struct csa2_attn_args {
   float softmax_scale;
   float* out;                 /* out [n_rows, 64, 512] fp32 */
   float* sink_mass;           /* out [n_rows, 64] or NULL */
-  void* workspace;            /* csa2_sparse_attn_workspace_size bytes */
+  void* workspace;            /* csa2_sparse_attn_workspace_size bytes: the partial results of
+                                 each 128-entry tile (K + window entries per row) */
   size_t workspace_bytes;
   int32_t* dev_status;        /* optional device int32, set to CSA2_EDEVICE_INDEX when idx holds a
-                                 record index outside [0, n_records) other than -1; or NULL */
+                                 record index outside [0, n_records) other than -1, or to
+                                 CSA2_ETIMEOUT when a bounded wait on the tensor cores gave up
+                                 (outputs then undefined); or NULL */
 } csa2_attn_args;
 
 size_t csa2_sparse_attn_workspace_size(const csa2_attn_args* a);

@@ -42,15 +42,12 @@ int scan_segments(int n_rows, long long L) {
   return s < 1 ? 1 : (int)s;
 }
 
+// Tiles of 128 attended entries per row: one attention block each (K + window <= 2048, so
+// at most 16).
 int attn_splits(int n_rows, int K, int window) {
-  const int forced = env_int("CSA2_ATTN_SPLITS", 0);
-  const int n_tiles = (K + window + 63) / 64;
-  if (forced > 0) return forced < n_tiles ? forced : (n_tiles > 0 ? n_tiles : 1);
-  // blocks are (row, 16-head group, split): fill the SMs, at most one split per tile
-  int s = sm_count() / (4 * (n_rows > 0 ? n_rows : 1));
-  if (s > n_tiles) s = n_tiles;
-  if (s > 64) s = 64;
-  return s < 1 ? 1 : s;
+  (void)n_rows;
+  const int n_tiles = (K + window + 127) / 128;
+  return n_tiles < 1 ? 1 : n_tiles;
 }
 
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ECUDA; }
@@ -203,7 +200,6 @@ AttnParams attn_params(const csa2_attn_args* a, const int32_t* idx) {
 }
 
 size_t attn_workspace(const csa2_attn_args* a, int n_split) {
-  if (n_split <= 1) return 0;
   return align_up((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM * 4) +
          align_up((size_t)a->n_rows * n_split * CSA2_HEADS * 2 * 4);
 }
@@ -211,11 +207,9 @@ size_t attn_workspace(const csa2_attn_args* a, int n_split) {
 csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, cudaStream_t s) {
   const int n_split = attn_splits(a->n_rows, a->K, a->window);
   AttnParams p = attn_params(a, idx);
-  if (n_split > 1) {
-    Carve c{ws};
-    p.part_o = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM);
-    p.part_ml = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * 2);
-  }
+  Carve c{ws};
+  p.part_o = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM);
+  p.part_ml = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * 2);
   return cuda_status(launch_sparse_attn(p, n_split, s));
 }
 
@@ -550,7 +544,7 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
     n += 1 + (n_seg > 1 && !fused_merge ? 1 : 0);  // the tcgen05 scan merges its segments itself
     if (a->mode == CSA2_MODE_FULL_POOL) n += 2;
   }
-  n += 1 + (attn_splits(a->attn.n_rows, a->K, a->attn.window) > 1 ? 1 : 0);
+  n += 2;  // attention tiles and their merge
   return n;
 }
 

@@ -2,57 +2,85 @@
 // window, with one sink logit per head ("DeepSeek V4 Inside", CSA core attention and
 // eq. (27); "Every layer, connected", "The query and output paths").
 //
-// Split-K flash decode: the K + W attended entries of a row are cut into tiles of 64; a
-// thread block (16 warps) handles a contiguous range of tiles of one row and keeps, per
-// head, the running max m, the running sum l and the unnormalised output O (64 x 512 fp32,
-// 64 registers per thread).  Each tile is gathered into shared memory (bf16 rows by
-// cp.async; FP4 latents and FP8 window rows are widened to bf16 in registers on the way,
-// which is exact), then
-//   S = q' K^T   on the tensor cores in bf16 (64 heads x 64 rows x 512), fp32 accumulate;
-//   P = exp(S - m) written as fp16 (10-bit mantissa keeps the rounding of P at ~2^-12);
-//   O = alpha O + P V  in fp16 x fp16 -> fp32 (V widened from the bf16 tile in registers).
-// The FP8 window rows' scale multiplies their logits and their weights in P.  A second
-// kernel merges the splits (log-sum-exp), adds the sink to the denominator, normalises and
-// turns the output's rotary coordinates back by -position.  With one split per row the
-// first kernel finishes the row itself.
+// The K + W attended entries of a row are cut into tiles of 128; one thread block takes one
+// tile of one row for all 64 heads, on the fifth-generation tensor cores:
+//   gather   the tile's 128 latent rows (bf16 by cp.async; FP4 latents and FP8 window rows
+//            widened to bf16 in registers, which is exact) and the row's query q' = RoPE(q)
+//            into shared memory, both in the 128-byte-swizzled K-major layout;
+//   S^T      = K q'^T: M = 128 entries x N = 64 heads x K = 512, bf16 in, fp32 in TMEM;
+//   softmax  one thread per entry reads its 64 logits from TMEM, scales them (FP8 window
+//            rows: times their row scale), and the tile's per-head maximum M_h and sum l_h
+//            are reduced over the 128 entries; P = exp(S - M) is written back to shared
+//            memory as two bf16 terms P = P_hi + P_lo (about 16 significant bits; FP8 rows'
+//            weights times their row scale);
+//   O^T      = V^T P^T with V = the same latent tile read transposed (MN-major operand):
+//            four M = 128-dim chunks x N = 128 (P_hi and P_lo side by side, 64 heads each)
+//            x K = 128 entries, fp32 in TMEM (the two halves are added when read out);
+//   partial  (M_h, l_h, O) of the tile go to the workspace.
+// A second kernel merges a row's tiles (log-sum-exp), adds the sink to the denominator,
+// normalises and turns the output's rotary coordinates back by -position.
 #include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc05.cuh"
 
 namespace csa2 {
 
 namespace {
 
-constexpr int kAttnThreads = 256;  // 8 warps
-constexpr int kTile = 64;          // attended entries per tile
-constexpr int kHG = 16;            // heads per block (one m16 MMA tile)
-constexpr int kQBytes = kHG * kHeadDim * 2;     // 16 KB
-constexpr int kKVBytes = kTile * kHeadDim * 2;  // 64 KB per stage
-constexpr int kPBytes = kHG * kTile * 2;        // 2 KB
-constexpr int kStages = 3;                      // gather pipeline depth (tiles in flight)
-constexpr int kMetaSlots = kStages + 1;         // tile sources, prepared one iteration ahead
+constexpr int kAttnThreads = 256;                  // 8 warps
+constexpr int kTileE = 128;                        // attended entries per block (MMA M)
+constexpr int kQPanel = kHeads * 128;              // 8 KB: 64 heads x 64 dims (bf16)
+constexpr int kKPanel = kTileE * 128;              // 16 KB: 128 entries x 64 dims
+constexpr int kQBytes = 8 * kQPanel;               // 64 KB (P_hi, P_lo after the first GEMM)
+constexpr int kKBytes = 8 * kKPanel;               // 128 KB
+constexpr int kPBytes = kTileE * 128;              // 16 KB: 128 entries x 64 heads (bf16)
+constexpr uint32_t kTmemCols = 512;                // S^T in columns 0..63, then O^T in all 512
 
-struct TileMeta {
-  const uint8_t* ptr[kTile];   // first byte of each entry's row (codes for FP formats)
-  const uint8_t* sptr[kTile];  // FP4 group scales
-  float rs[kTile];             // FP8 row scale (1 otherwise)
-  int fmt[kTile];              // storage format, -1 = masked entry
+struct TileSrc {
+  const uint8_t* ptr[kTileE];   // first byte of each entry's row (codes for FP formats)
+  const uint8_t* sptr[kTileE];  // FP4 group scales
+  float rs[kTileE];             // FP8 row scale (1 otherwise)
+  int fmt[kTileE];              // storage format, -1 = masked entry
 };
 
-struct AttnSmem {
-  TileMeta meta[kMetaSlots];
-  float red_max[4][kHG];
-  float red_sum[4][kHG];
-  float cs[kRopeDim];  // cos (0..31) and sin (32..63) of the row's rotary angles
+struct AttnShared {
+  TileSrc src;
+  float red[4][kHeads];      // per TMEM lane quarter: the per-head maximum over its 32 entries
+  float red_sum[4][kHeads];  // ... and the per-head sum of P
+  float mfin[kHeads];    // the tile's per-head maximum logit
+  float cs[kRopeDim];    // cos (0..31) and sin (32..63) of the row's rotary angles
+  uint64_t bar_s, bar_o;  // first and second GEMM completed
+  uint32_t tmem_base;
+  int timeout;
+  int s_issued, o_issued;
 };
-constexpr int kAttnSmemBytes = kQBytes + kStages * kKVBytes + kPBytes + (int)sizeof(AttnSmem);
+constexpr int kAttnSmemBytes = 1024 + kQBytes + kKBytes + (int)sizeof(AttnShared);
 
-// Byte offset of 16-byte chunk `c` of row `r` in a tile with 1024-byte rows: the low three
-// chunk bits are XOR-ed with the row so that 8 rows at the same chunk hit 8 bank groups.
-__device__ __forceinline__ int swz1k(int r, int c) { return r * 1024 + ((c ^ (r & 7)) << 4); }
-// Same for the P tile (128-byte rows of 64 fp16).
-__device__ __forceinline__ int swzp(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+__device__ __forceinline__ uint8_t* align_1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// Byte offset of 16-byte chunk c (dims 8c .. 8c+7) of row r in a tile stored as eight
+// 64-dim panels of `rows` rows x 128 bytes, the 16-byte chunks of each row XOR-ed with the
+// row's low three bits (the tensor cores' 128-byte swizzle).
+__device__ __forceinline__ int sw128_off(int r, int c, int rows) {
+  return (c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// Shared-memory descriptor of a 128-byte-swizzled operand with explicit leading and stride
+// byte offsets (MN-major operands: leading = distance between 64-element chunks along M or N,
+// stride = distance between groups of 8 rows along K).
+__device__ __forceinline__ uint64_t sw128_desc_lbo(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3ffffu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
 
 __device__ __forceinline__ float e2m1_level(uint32_t nib) {
   // magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign
@@ -93,6 +121,8 @@ struct EntrySrc {
   bool valid;
 };
 
+// Entry e of a row's attended list: e < K are the selected latents (idx; -1 = none), then
+// the window rows of positions lo .. qp.
 __device__ __forceinline__ EntrySrc entry_source(const AttnParams& p, int row, int b, long long qp, long long lo,
                                                  long long pos0, int e) {
   EntrySrc s{nullptr, nullptr, 1.f, CSA2_BF16, false};
@@ -129,39 +159,27 @@ __device__ __forceinline__ EntrySrc entry_source(const AttnParams& p, int row, i
   return s;
 }
 
-// Source of every entry of tile `tile` (threads 0..63, one entry each).
-__device__ __forceinline__ void tile_meta(const AttnParams& p, TileMeta& m, int row, int b, long long qp, long long lo,
-                                          long long pos0, int tile) {
-  if (threadIdx.x < kTile) {
-    const int r = threadIdx.x;
-    const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTile + r);
-    m.ptr[r] = s.valid ? s.ptr : nullptr;
-    m.sptr[r] = s.sptr;
-    m.rs[r] = s.rs;
-    m.fmt[r] = s.valid ? s.fmt : -1;
-  }
-}
-
-// Gathers one tile into a KV stage (64 rows x 512 bf16, swizzled).  bf16 rows go by cp.async,
-// a warp copying 512 contiguous bytes per instruction; FP4 latents and FP8 window rows are
-// widened to bf16 in registers (exact) by four threads per row.
-__device__ __forceinline__ void load_tile(const TileMeta& m, uint8_t* kv, const void* any_valid) {
+// Gathers the block's tile (128 entries x 512 dims, bf16, panel layout) into `ks`.  bf16 rows
+// go by cp.async, a warp copying 512 contiguous bytes per instruction (masked entries are
+// zero-filled, so they add nothing to P V); FP4 latents and FP8 window rows are widened to
+// bf16 in registers (exact), two threads per row.
+__device__ __forceinline__ void gather_tile(const TileSrc& m, uint8_t* ks, const void* any_valid) {
   const int t = threadIdx.x;
 #pragma unroll 4
-  for (int k = 0; k < kTile / 4; ++k) {
+  for (int k = 0; k < kTileE / 4; ++k) {
     const int r = 4 * k + (t >> 6), c = t & 63;
     const int f = m.fmt[r];
     if (f == CSA2_BF16 || f < 0) {
       const uint8_t* src = f < 0 ? reinterpret_cast<const uint8_t*>(any_valid) : m.ptr[r];
-      cp_async16(kv + swz1k(r, c), src + c * 16, f >= 0);
+      cp_async16(ks + sw128_off(r, c, kTileE), src + c * 16, f >= 0);
     }
   }
-  const int r = t >> 2, quarter = t & 3;  // 128 dims per thread
+  const int r = t >> 1, half = t & 1;  // 256 dims per thread
   const int f = m.fmt[r];
   if (f == CSA2_FP8_E4M3_ROWSCALE) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int d0 = quarter * 128 + half * 64;
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      const int d0 = half * 256 + g * 64;
       const uint4* src = reinterpret_cast<const uint4*>(m.ptr[r] + d0);
       uint32_t outw[32];
 #pragma unroll
@@ -176,14 +194,14 @@ __device__ __forceinline__ void load_tile(const TileMeta& m, uint8_t* kv, const 
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(kv + swz1k(r, d0 / 8 + k)) =
+        *reinterpret_cast<uint4*>(ks + sw128_off(r, d0 / 8 + k, kTileE)) =
             make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]);
     }
   } else if (f == CSA2_FP4_E2M1_G32 || f == CSA2_FP4_E2M1_G16) {
     const int gsz = f == CSA2_FP4_E2M1_G32 ? 32 : 16;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int d0 = quarter * 128 + half * 64;
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      const int d0 = half * 256 + g * 64;
       const uint4* src = reinterpret_cast<const uint4*>(m.ptr[r] + d0 / 2);
       uint32_t outw[32];
 #pragma unroll
@@ -203,261 +221,269 @@ __device__ __forceinline__ void load_tile(const TileMeta& m, uint8_t* kv, const 
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(kv + swz1k(r, d0 / 8 + k)) =
+        *reinterpret_cast<uint4*>(ks + sw128_off(r, d0 / 8 + k, kTileE)) =
             make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]);
     }
   }
 }
 
-// One block: query row blockIdx.z, heads 16*blockIdx.y .. +15, split blockIdx.x of the row's
-// tiles.  Gathers run kStages tiles ahead.  Warps 0..3: QK for rows 16w..16w+15 of each tile
-// and the softmax; all 8 warps: PV for dims 64w..64w+63.
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_hg_kernel(const AttnParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* Qs = smem;
-  uint8_t* KV = smem + kQBytes;
-  uint8_t* Ps = KV + kStages * kKVBytes;
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(Ps + kPBytes);
+// q' = RoPE(q) of the row's 64 heads into `qs` (panel layout, 64 rows): consecutive threads
+// take consecutive 16-byte chunks; the rotary pairs are dims 448 + 2i, 448 + 2i + 1.
+__device__ __forceinline__ void load_query(const AttnParams& p, int row, uint8_t* qs, const float* cs) {
+  const uint4* qsrc = reinterpret_cast<const uint4*>(p.q) + (size_t)row * kHeads * (kHeadDim / 8);
+#pragma unroll 4
+  for (int k = 0; k < kHeads * kHeadDim / 8 / kAttnThreads; ++k) {
+    const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 6, ch = idx & 63;
+    uint4 v = __ldg(qsrc + idx);
+    if (ch >= 56) {
+      uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = (ch - 56) * 4 + j;  // rotary pair index
+        const float x = bf16_lo(w4[j]), y = bf16_hi(w4[j]);
+        const float c = cs[i], s = cs[32 + i];
+        w4[j] = pack_bf16x2(x * c - y * s, x * s + y * c);
+      }
+      v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    *reinterpret_cast<uint4*>(qs + sw128_off(h, ch, kHeads)) = v;
+  }
+}
 
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int g = lane >> 2, c = lane & 3;
-  const int row = blockIdx.z, hg = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
+// Reduces v[0..8) over the warp's 32 lanes: three halving exchange steps leave lane l with
+// element (l >> 2) & 7 reduced over the 8 lanes that share bits 0..1 of l, two more steps
+// complete it over all 32 lanes (result in v[0]; 9 shuffles).
+template <bool MAX>
+__device__ __forceinline__ void group_reduce8(float (&v)[8]) {
+  const int ln = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < 3; ++s) {
+    const int half = 4 >> s, o = 16 >> s;
+    const bool upper = (ln & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i < half) {
+        const float keep = upper ? v[i + half] : v[i];
+        const float send = upper ? v[i] : v[i + half];
+        const float got = __shfl_xor_sync(0xffffffffu, send, o);
+        v[i] = MAX ? fmaxf(keep, got) : keep + got;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 2; o >= 1; o >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], o);
+    v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+  }
+}
+
+__device__ __forceinline__ void report_timeout_attn(int* flag, int32_t* dev_status) {
+  atomicExch(flag, 1);
+  if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
+}
+
+// One block: tile blockIdx.x (entries 128*x .. 128*x+127) of query row blockIdx.y, all 64
+// heads.  Warp 0 allocates tensor memory and issues the MMAs (one thread); every warp
+// gathers, runs the softmax for 32 entries x 32 heads (one thread per TMEM lane = entry)
+// and writes partials.
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1k(smem_raw);
+  uint8_t* qs = smem;              // q' (first GEMM), then P_hi | P_lo (second GEMM)
+  uint8_t* ks = smem + kQBytes;    // the latent tile
+  AttnShared& sh = *reinterpret_cast<AttnShared*>(ks + kKBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x, n_tiles = gridDim.x, row = blockIdx.y;
   const int b = p.seq_of_row[row];
   const long long qp = p.q_pos[row];
   const long long pos0 = p.swa_pos0[b];
   const long long lo = max(qp - (long long)p.window + 1, pos0);
-  const int n_tiles = (p.K + p.window + kTile - 1) / kTile;
-  const int t0 = (int)(((long long)n_tiles * split) / n_split);
-  const int t1 = (int)(((long long)n_tiles * (split + 1)) / n_split);
 
-  rope_table(sm.cs, p, qp, 1.f);
-#pragma unroll
-  for (int k = 0; k < kStages; ++k)
-    if (t0 + k < t1) tile_meta(p, sm.meta[(t0 + k) % kMetaSlots], row, b, qp, lo, pos0, t0 + k);
+  if (tid == 0) {
+    tc05::mbar_init(&sh.bar_s, 1);
+    tc05::mbar_init(&sh.bar_o, 1);
+    sh.timeout = 0;
+    sh.s_issued = sh.o_issued = 0;
+    tc05::fence_barrier_init();
+  }
+  if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kTmemCols);
+  rope_table(sh.cs, p, qp, 1.f);
+  if (tid < kTileE) {
+    const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTileE + tid);
+    sh.src.ptr[tid] = s.valid ? s.ptr : nullptr;
+    sh.src.sptr[tid] = s.sptr;
+    sh.src.rs[tid] = s.rs;
+    sh.src.fmt[tid] = s.valid ? s.fmt : -1;
+  }
+  tc05::fence_before();
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < kStages - 1; ++k) {
-    if (t0 + k < t1) load_tile(sm.meta[(t0 + k) % kMetaSlots], KV + ((t0 + k) % kStages) * kKVBytes, p.q);
-    cp_async_commit();
-  }
-  // ---- q' = RoPE(q) for this block's 16 heads (coalesced: consecutive threads, consecutive chunks)
-  {
-    const uint4* qsrc = reinterpret_cast<const uint4*>(p.q) + ((size_t)row * kHeads + kHG * hg) * (kHeadDim / 8);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int idx = k * kAttnThreads + tid, h = idx >> 6, ch = idx & 63;
-      uint4 v = __ldg(qsrc + idx);
-      if (ch >= 56) {
-        uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = (ch - 56) * 4 + j;  // rotary pair index
-          const float x = bf16_lo(w4[j]), y = bf16_hi(w4[j]);
-          const float cs = sm.cs[i], sn = sm.cs[32 + i];
-          w4[j] = pack_bf16x2(x * cs - y * sn, x * sn + y * cs);
-        }
-        v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      *reinterpret_cast<uint4*>(Qs + swz1k(h, ch)) = v;
-    }
-  }
+  tc05::fence_after();
+  const uint32_t tmem = sh.tmem_base;
 
-  float m_run[2] = {-INFINITY, -INFINITY};  // heads g, g+8 of the group
-  float l_run[2] = {0.f, 0.f};
-  float acc_o[8][4];
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) acc_o[nt][0] = acc_o[nt][1] = acc_o[nt][2] = acc_o[nt][3] = 0.f;
-
-  const uint32_t qs_u = smem_u32(Qs), ps_u = smem_u32(Ps);
-  const int mi = lane >> 3, ri = lane & 7;
-  for (int t = t0; t < t1; ++t) {
-    const int st = t % kStages;
-    uint8_t* kv = KV + st * kKVBytes;
-    {
-      const int tn = t + kStages - 1;  // sources of tn were prepared one iteration ago
-      if (tn < t1) load_tile(sm.meta[tn % kMetaSlots], KV + (tn % kStages) * kKVBytes, p.q);
-      cp_async_commit();
-    }
-    cp_async_wait<kStages - 1>();
-    __syncthreads();
-    const uint32_t kv_u = smem_u32(kv);
-    const TileMeta& md = sm.meta[t % kMetaSlots];
-
-    float alpha[2] = {1.f, 1.f};
-    if (wid < 4) {
-      // ---- S = q' K^T: 16 heads x rows 16*wid .. +15 (two 8-row MMA tiles, two chains each)
-      float sa[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) sa[a][0] = sa[a][1] = sa[a][2] = sa[a][3] = 0.f;
-      const int qh = ri + (mi & 1) * 8;
-      const int kr = 16 * wid + ri + (mi >> 1) * 8;
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(a0, a1, a2, a3, qs_u + swz1k(qh, 2 * ks + (mi >> 1)));
-        ldsm_x4(b0, b1, b2, b3, kv_u + swz1k(kr, 2 * ks + (mi & 1)));
-        mma_bf16(sa[(ks & 1) * 2 + 0], a0, a1, a2, a3, b0, b1);
-        mma_bf16(sa[(ks & 1) * 2 + 1], a0, a1, a2, a3, b2, b3);
-      }
-      // sacc[nt][e]: n-tile nt = rows 16*wid + 8*nt .. ; e as in the MMA C fragment
-      float sacc[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] = sa[nt][e] + sa[2 + nt][e];
-      float tmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = 16 * wid + 8 * nt + 2 * c + (e & 1);
-          const float z = md.fmt[r] >= 0 ? sacc[nt][e] * p.scale * md.rs[r] : -INFINITY;
-          sacc[nt][e] = z;
-          tmax[e >> 1] = fmaxf(tmax[e >> 1], z);
-        }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 1));
-        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 2));
-      }
-      if (c == 0) {
-        sm.red_max[wid][g] = tmax[0];
-        sm.red_max[wid][g + 8] = tmax[1];
-      }
-      asm volatile("bar.sync 2, 128;\n" ::: "memory");
-      float m_use[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int h = g + 8 * hh;
-        const float tm = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]), fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
-        const float m_new = fmaxf(m_run[hh], tm);
-        m_use[hh] = m_new == -INFINITY ? 0.f : m_new;
-        alpha[hh] = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - m_use[hh]);
-        m_run[hh] = m_new;
-      }
-      float psum[2] = {0.f, 0.f};
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float pe[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          pe[e] = __expf(sacc[nt][e] - m_use[e >> 1]);
-          psum[e >> 1] += pe[e];
-        }
-        const int r = 16 * wid + 8 * nt + 2 * c;
-        const float rs0 = md.rs[r], rs1 = md.rs[r + 1];
-        // P[h][r], P[h][r+1] as fp16 pairs; the FP8 row scale multiplies the weights
-        *reinterpret_cast<uint32_t*>(Ps + swzp(g, r >> 3) + (r & 7) * 2) = pack_f16x2(pe[0] * rs0, pe[1] * rs1);
-        *reinterpret_cast<uint32_t*>(Ps + swzp(g + 8, r >> 3) + (r & 7) * 2) = pack_f16x2(pe[2] * rs0, pe[3] * rs1);
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 1);
-        psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 2);
-      }
-      if (c == 0) {
-        sm.red_sum[wid][g] = psum[0];
-        sm.red_sum[wid][g + 8] = psum[1];
-      }
-    }
-    __syncthreads();
-    // every warp: the running statistics of heads g, g+8 (identical in all warps)
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = g + 8 * hh;
-      if (wid >= 4) {
-        const float tm = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]), fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
-        const float m_new = fmaxf(m_run[hh], tm);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        alpha[hh] = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - m_use);
-        m_run[hh] = m_new;
-      }
-      const float ts = (sm.red_sum[0][h] + sm.red_sum[1][h]) + (sm.red_sum[2][h] + sm.red_sum[3][h]);
-      l_run[hh] = l_run[hh] * alpha[hh] + ts;
-    }
-    // ---- O = alpha O + P V for dims 64*wid .. +63
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      acc_o[nt][0] *= alpha[0];
-      acc_o[nt][1] *= alpha[0];
-      acc_o[nt][2] *= alpha[1];
-      acc_o[nt][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int ks = 0; ks < kTile / 16; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(a0, a1, a2, a3, ps_u + swzp(ri + (mi & 1) * 8, 2 * ks + (mi >> 1)));
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t vb[4];
-        const int vr = 16 * ks + ri + (mi & 1) * 8;
-        const int vc = (64 * wid + 16 * np) / 8 + (mi >> 1);
-        ldsm_x4_t(vb[0], vb[1], vb[2], vb[3], kv_u + swz1k(vr, vc));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) vb[k] = bf16x2_to_f16x2(vb[k]);
-        mma_f16(acc_o[2 * np], a0, a1, a2, a3, vb[0], vb[1]);
-        mma_f16(acc_o[2 * np + 1], a0, a1, a2, a3, vb[2], vb[3]);
-      }
-    }
-    if (t + kStages < t1) tile_meta(p, sm.meta[(t + kStages) % kMetaSlots], row, b, qp, lo, pos0, t + kStages);
-    __syncthreads();
-  }
+  gather_tile(sh.src, ks, p.q);
+  cp_async_commit();
+  load_query(p, row, qs, sh.cs);
   cp_async_wait<0>();
+  // generic-proxy writes (cp.async and stores) become visible to the tensor cores
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
 
-  const int h_lo = kHG * hg + g, h_hi = h_lo + 8;  // absolute heads of this thread
-  if (n_split == 1) {
-    // ---- finish the row: sink in the denominator, normalise, inverse RoPE
-    float f[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float sk = __ldg(p.sink + (hh ? h_hi : h_lo));
-      const float M = fmaxf(m_run[hh], sk);
-      const float em = m_run[hh] == -INFINITY ? 0.f : __expf(m_run[hh] - M);
-      const float den = l_run[hh] * em + __expf(sk - M);
-      f[hh] = em / den;
-      if (p.sink_mass && wid == 0 && c == 0) p.sink_mass[(size_t)row * kHeads + (hh ? h_hi : h_lo)] = __expf(sk - M) / den;
-    }
-    rope_table(sm.cs, p, qp, -1.f);
-    __syncthreads();
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float* orow = p.out + ((size_t)row * kHeads + (hh ? h_hi : h_lo)) * kHeadDim;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int d = 64 * wid + 8 * nt + 2 * c;
-        float x = acc_o[nt][2 * hh] * f[hh], y = acc_o[nt][2 * hh + 1] * f[hh];
-        if (d >= kHeadDim - kRopeDim) {
-          const int i = (d - (kHeadDim - kRopeDim)) >> 1;
-          const float cs = sm.cs[i], sn = sm.cs[32 + i];
-          const float xr = x * cs - y * sn, yr = x * sn + y * cs;
-          x = xr;
-          y = yr;
-        }
-        *reinterpret_cast<float2*>(orow + d) = make_float2(x, y);
+  const uint32_t qs_u = smem_u32(qs), ks_u = smem_u32(ks);
+  // ---------------------------------------------------------------- S^T = K q'^T
+  if (warp == 0) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc05::idesc_bf16(128, kHeads);
+#pragma unroll 1
+      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        const uint32_t sub = (kk & 3) * 32;
+        tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + (kk >> 2) * kKPanel + sub),
+                       tc05::sw128_desc(qs_u + (kk >> 2) * kQPanel + sub), idesc, kk > 0);
       }
+      tc05::mma_commit(&sh.bar_s);
+      sh.s_issued = 1;
     }
-    return;
+    __syncwarp();
   }
-  // ---- partial results of this split
+
+  // ---------------------------------------------------------------- softmax over the tile
+  // warp w: TMEM lanes 32*(w&3) .. +31 (entry e = one lane), heads 32*(w>>2) .. +31, in four
+  // groups of 8 heads read from TMEM as needed (rolled loops keep this run-once code small
+  // enough for the instruction cache)
+  const int qw = warp & 3, hb = 32 * (warp >> 2), e = 32 * qw + lane;
+  const int lh = (lane >> 2) & 7;  // head within a group of 8 whose result this lane ends with
+  {
+    const bool ok = tc05::mbar_wait(&sh.bar_s, 0);
+    if (!ok && lane == 0) report_timeout_attn(&sh.timeout, p.dev_status);
+    tc05::fence_after();
+    const int f = sh.src.fmt[e];
+    const float rs = sh.src.rs[e];
+    const bool on = ok && f >= 0;  // off: masked entry (logit -inf)
+    const float zs = p.scale * rs;
+    const uint32_t trow = tmem + ((uint32_t)(32 * qw) << 16) + (uint32_t)hb;
+    // per-head maximum over the tile's entries
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      uint32_t v[8];
+      tc05::tmem_ld8(trow + 8 * g, v);
+      tc05::tmem_ld_wait();
+      float z[8];
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float* po = p.part_o + (((size_t)row * n_split + split) * kHeads + (hh ? h_hi : h_lo)) * kHeadDim;
+      for (int k = 0; k < 8; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
+      group_reduce8<true>(z);
+      if ((lane & 3) == 0) sh.red[qw][hb + 8 * g + lh] = z[0];
+    }
+    __syncthreads();
+    if (qw == 0)
+      sh.mfin[hb + lane] = fmaxf(fmaxf(sh.red[0][hb + lane], sh.red[1][hb + lane]),
+                                 fmaxf(sh.red[2][hb + lane], sh.red[3][hb + lane]));
+    __syncthreads();
+    // P = exp(z - M) as P_hi | P_lo rows (entry e, MN-major for the second GEMM), the FP8
+    // row scale on the weights; per-head sums of the unscaled P
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      uint32_t v[8];
+      tc05::tmem_ld8(trow + 8 * g, v);
+      const float4 m0 = *reinterpret_cast<const float4*>(&sh.mfin[hb + 8 * g]);
+      const float4 m1 = *reinterpret_cast<const float4*>(&sh.mfin[hb + 8 * g + 4]);
+      const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      tc05::tmem_ld_wait();
+      float pe[8];
+      uint32_t hi[4], lw[4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int d = 64 * wid + 8 * nt + 2 * c;
-      *reinterpret_cast<float2*>(po + d) = make_float2(acc_o[nt][2 * hh], acc_o[nt][2 * hh + 1]);
+      for (int k = 0; k < 8; ++k)
+        pe[k] = on ? __expf(__uint_as_float(v[k]) * zs - (M[k] == -INFINITY ? 0.f : M[k])) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a0 = pe[2 * k] * rs, a1 = pe[2 * k + 1] * rs;
+        hi[k] = pack_bf16x2(a0, a1);
+        lw[k] = pack_bf16x2(a0 - bf16_lo(hi[k]), a1 - bf16_hi(hi[k]));
+      }
+      const int off = e * 128 + (((hb / 8 + g) ^ (e & 7)) << 4);
+      *reinterpret_cast<uint4*>(qs + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(qs + kPBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      group_reduce8<false>(pe);
+      if ((lane & 3) == 0) sh.red_sum[qw][hb + 8 * g + lh] = pe[0];
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+
+  // ---------------------------------------------------------------- O^T = V^T [P_hi | P_lo]^T
+  // S^T is dead now: chunk c of 128 dims accumulates into columns 128c .. 128c+127, the
+  // P_hi products in the first 64, the P_lo products in the last 64.
+  if (warp == 0) {
+    if (lane == 0 && !sh.timeout) {
+      // A = V^T (dims x entries, MN-major: 64-dim panels 16 KB apart, 8-entry groups 1 KB
+      // apart); B = [P_hi | P_lo]^T (entries x 128, MN-major: two 64-column chunks 16 KB
+      // apart, 8-entry groups 1 KB apart)
+      constexpr uint32_t idesc = tc05::idesc_bf16(128, 2 * kHeads) | (1u << 15) | (1u << 16);
+#pragma unroll 1
+      for (int i = 0; i < 4 * (kTileE / 16); ++i) {
+        const int c = i >> 3, kk = i & 7;
+        tc05::mma_bf16(tmem + 128 * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel + kk * 2048, kKPanel, 1024),
+                       sw128_desc_lbo(qs_u + kk * 2048, kPBytes, 1024), idesc, kk > 0);
+      }
+      tc05::mma_commit(&sh.bar_o);
+      sh.o_issued = 1;
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- partial results
+  // part_o[row][tile][h][d] = O[h][d] (relative to M_h); warp w reads TMEM lanes 32*(w&3) of
+  // dim chunks 2*(w>>2), 2*(w>>2)+1: thread -> one dim, 8 heads per step
+  const bool live = sh.o_issued && tc05::mbar_wait(&sh.bar_o, 0);
+  if (!live && sh.o_issued && lane == 0) report_timeout_attn(&sh.timeout, p.dev_status);
+  tc05::fence_after();
+  if (live) {
+    float* po = p.part_o + ((size_t)row * n_tiles + tile) * kHeads * kHeadDim;
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+      const int c = 2 * (warp >> 2) + (i >> 3), g = i & 7;
+      const int d = 128 * c + 32 * qw + lane;
+      uint32_t vh[8], vl[8];
+      const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + 128 * c + 8 * g;
+      tc05::tmem_ld8(ta, vh);
+      tc05::tmem_ld8(ta + 64, vl);
+      tc05::tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        po[(size_t)(8 * g + k) * kHeadDim + d] = __uint_as_float(vh[k]) + __uint_as_float(vl[k]);
     }
   }
-  if (wid == 0 && c == 0) {
-    float* pm = p.part_ml + ((size_t)row * n_split + split) * kHeads * 2;
-    pm[2 * h_lo] = m_run[0];
-    pm[2 * h_lo + 1] = l_run[0];
-    pm[2 * h_hi] = m_run[1];
-    pm[2 * h_hi + 1] = l_run[1];
+  if (warp == 4) {
+    float* pm = p.part_ml + ((size_t)row * n_tiles + tile) * kHeads * 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = 2 * lane + j;
+      const float l = (sh.red_sum[0][h] + sh.red_sum[1][h]) + (sh.red_sum[2][h] + sh.red_sum[3][h]);
+      pm[2 * h] = live ? sh.mfin[h] : -INFINITY;
+      pm[2 * h + 1] = live ? l : 0.f;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc05::fence_before();
+  __syncthreads();
+  if (sh.timeout && tid == 0) {
+    // let issued MMAs finish (bounded) before the tensor memory is freed
+    if (sh.s_issued) tc05::mbar_wait(&sh.bar_s, 0);
+    if (sh.o_issued) tc05::mbar_wait(&sh.bar_o, 0);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc05::fence_after();
+    tc05::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// Merges the splits of one row for 4 heads: log-sum-exp over splits plus the sink,
+// Merges the tiles of one row for 4 heads: log-sum-exp over tiles plus the sink,
 // normalisation, inverse RoPE on dims 448..511.  Thread -> (head h0 + tid/32, 16 dims).
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int n_split) {
   __shared__ float fac[4][64];  // per head: weight of each split (n_split <= 64)
@@ -540,11 +566,11 @@ int attn_smem_bytes() { return kAttnSmemBytes; }
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
   cudaError_t e =
-      cudaFuncSetAttribute(attn_hg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+      cudaFuncSetAttribute(attn_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_hg_kernel<<<dim3(n_split, kHeads / kHG, p.n_rows), kAttnThreads, kAttnSmemBytes, stream>>>(p);
+  attn_tc05_kernel<<<dim3(n_split, p.n_rows), kAttnThreads, kAttnSmemBytes, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess || n_split == 1) return e;
+  if (e != cudaSuccess) return e;
   attn_combine_kernel<<<dim3(p.n_rows, kHeads / 4), 128, 0, stream>>>(p, n_split);
   return cudaGetLastError();
 }
