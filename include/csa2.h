@@ -270,9 +270,10 @@ typedef struct csa2_decode_args {
   void* workspace;            /* csa2_fused_decode_workspace_size bytes */
   size_t workspace_bytes;
   /* Optional tracing: cudaEvent_t handles (as void*) recorded on `stream` at the stage
-   * boundaries: [0] before indexing, [1] after the indexer scan, [2] after the top-K merge
-   * and block pool, [3] after attention.  NULL entries are skipped.  The events belong to
-   * the caller, who must have created them (cudaEventCreate). */
+   * boundaries: [0] right before the indexer scan kernel (after the reset of its row
+   * counters), [1] after it, [2] after the top-K merge and block pool (if any), [3] after
+   * attention.  NULL entries are skipped.  Each record adds a short gap between the
+   * kernels.  The events belong to the caller, who must have created them (cudaEventCreate). */
   void* stage_events[4];
 } csa2_decode_args;
 

@@ -455,7 +455,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
   auto mark = [&](int i) {
     if (a->stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(a->stage_events[i]), s);
   };
-  mark(0);
+  if (a->mode == CSA2_MODE_REUSE) mark(0);
   if (a->mode != CSA2_MODE_REUSE) {
     ScanParams p = scan_params(ix);
     p.K = a->K;
@@ -493,6 +493,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       if (fused_merge && cudaMemsetAsync(p.row_done, 0, (size_t)n_rows * 4, s) != cudaSuccess) return CSA2_ECUDA;
       if (!fused_merge) p.row_done = nullptr;
     }
+    mark(0);  // stage 0: the indexer scan kernel alone
     e = launch_scan(p, &ic, true, n_seg, s);
     if (e != cudaSuccess) return CSA2_ECUDA;
     mark(1);

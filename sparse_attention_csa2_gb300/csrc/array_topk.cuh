@@ -1,5 +1,5 @@
-// Exact top-K of an array of keys held in shared memory, in entry order, by a group of NW
-// warps (named barrier `bar_id`, or __syncthreads when it is 0).
+// Exact top-K of an array of keys held in shared memory, in entry order, by the NW warps of a
+// thread block.
 //
 // Rule (course lesson "06 / Indexer and attention", select_values and its note on ties): the
 // K entries best by (key descending, entry index ascending) are kept; keys are the
@@ -11,9 +11,12 @@
 // the array copies, per warp and in entry order, every entry whose key is at or above the
 // threshold's level-1 bin (key and index) to a list in scratch memory.  The two finer levels,
 // the counts and the output all walk those lists only, which hold about K entries plus the
-// population of one bin, so the array is read once after its histogram.  Without scratch
-// (or not enough of it) the finer levels and the output walk the whole array instead.  The
-// first level's histogram may be filled by the caller while the keys are produced.
+// population of one bin, so the array is read once after its histogram.  The first level's
+// histogram may be filled by the caller while the keys are produced.
+//
+// The selection runs once per thread block, so its code is never warm in the instruction
+// cache: the functions are kept out of line (every caller in a kernel shares one copy) and
+// their loops rolled.
 #pragma once
 
 #include "common.cuh"
@@ -30,13 +33,13 @@ struct alignas(16) ArrSelShared {
   int bin;            // chosen bin of the current level
   int before;         // candidates above it
   int total;
-  int lists;          // the per-warp lists hold the candidates
   uint32_t thr;       // the K-th key (0 when at most K candidates)
   int n_eq;           // entries equal to thr that are kept, lowest indices first
 };
 
 // hist[bin] += 1 when `valid`.  A plain shared atomic: on sm_103a aggregating equal bins over
-// the warp first (match.any) costs far more than the atomics' own serialisation.
+// the warp first (match.any) costs far more than the atomics' own serialisation, even when
+// every lane hits the same bin.
 __device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool valid) {
   if (valid) atomicAdd(&hist[bin], 1);
 }
@@ -45,17 +48,10 @@ template <int NW>
 struct ArrSel {
   static constexpr int NT = NW * 32;
   ArrSelShared* sh;
-  int bar_id;
   int tid;
-  uint32_t* scratch = nullptr;  // per-warp lists (may be null); 16-byte aligned
-  int scratch_cap = 0;          // its capacity in 32-bit words
+  uint32_t* scratch = nullptr;  // per-warp lists, list_words(n) words, 16-byte aligned
 
-  __device__ __forceinline__ void sync() const {
-    if (bar_id == 0)
-      __syncthreads();
-    else
-      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "n"(NT) : "memory");
-  }
+  __device__ __forceinline__ void sync() const { __syncthreads(); }
   __device__ __forceinline__ int lane() const { return tid & 31; }
   __device__ __forceinline__ int warp() const { return tid >> 5; }
 
@@ -97,7 +93,7 @@ struct ArrSel {
   // thread takes an odd number of consecutive bins (no bank conflicts), holds them in
   // registers, and the thread whose share holds the crossing finds it there.
   template <int NBINS>
-  __device__ void pick(int need) const {
+  __device__ __noinline__ void pick(int need) const {
     constexpr int PER = ((NBINS + NT - 1) / NT) | 1;
     const int r0 = tid * PER;  // rank from the top of this thread's first bin
     int c[PER];
@@ -127,50 +123,46 @@ struct ArrSel {
   }
 };
 
-// Finds the K-th key of keys[0..n) (0 = not a candidate) and, with enough scratch, lists the
-// candidates at or above its level-1 bin.  `keys` is 16-byte aligned and readable up to n
-// rounded up to a multiple of 4.  `hist_ready`: the caller has filled sh->hist with the
-// level-1 histogram (key >> 20) of the candidates.  Afterwards sh->thr and sh->n_eq describe
-// the selection: keys > thr, and the first n_eq keys == thr in entry order (thr = 0, n_eq = 0
-// when at most k candidates exist: all are kept).
+// Finds the K-th key of keys[0..n) (0 = not a candidate) and lists the candidates at or
+// above its level-1 bin.  `keys` is 16-byte aligned and readable up to n rounded up to a
+// multiple of 4.  `hist_ready`: the caller has filled sh->hist with the level-1 histogram
+// (key >> 20) of the candidates.  Afterwards sh->thr and sh->n_eq describe the selection:
+// keys > thr, and the first n_eq keys == thr in entry order (thr = 0, n_eq = 0 when at most k
+// candidates exist: all are kept).
 template <int NW>
-__device__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* keys, int n, int k, bool hist_ready) {
+__device__ __noinline__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* keys, int n, int k,
+                                           bool hist_ready) {
   constexpr int NT = NW * 32;
   ArrSelShared& sh = *s.sh;
   const int w = s.warp(), ln = s.lane();
   if (!hist_ready) {
     s.zero_hist(kHistBins);
     s.sync();
-    for (int i0 = w * 32; i0 < n; i0 += 4 * NT) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) kk[u] = i0 + u * NT + ln < n ? keys[i0 + u * NT + ln] : 0u;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) hist_add(sh.hist, kk[u] >> 20, kk[u] != 0u);
-    }
+#pragma unroll 1
+    for (int i = s.tid; i < n; i += NT)
+      if (keys[i] != 0u) atomicAdd(&sh.hist[keys[i] >> 20], 1);
     s.sync();
   }
   s.template pick<kHistBins>(k);
   const bool all = sh.total <= k;  // at most k candidates: keep them all
   const uint32_t b1 = all ? 0u : (uint32_t)sh.bin;
   int need = k - sh.before;
-  const bool lists = s.scratch != nullptr && ArrSel<NW>::list_words(n) <= s.scratch_cap;
   const int per = ArrSel<NW>::range(n);
   s.sync();  // every thread has read bin / before / total
-  int n_list = 0;
-  uint32_t* lk = lists ? s.scratch + (size_t)w * 2 * per : nullptr;  // keys of the list
-  uint32_t* li = lists ? lk + per : nullptr;                          // their entry indices
-  if (lists) {
-    // Lane l of the warp owns entries [lo + l*q, lo + (l+1)*q) of the warp's range (q = per/32,
-    // a multiple of 4).  A first walk counts the lane's entries at or above bin b1, one warp
-    // scan places each lane's share in the list, and a second walk writes them: the list is
-    // in entry order, and the walks are plain vector loads with no warp votes.
+  uint32_t* lk = s.scratch + (size_t)w * 2 * per;  // keys of the warp's list
+  uint32_t* li = lk + per;                         // their entry indices
+  // Lane l of the warp owns entries [lo + l*q, lo + (l+1)*q) of the warp's range (q = per/32,
+  // a multiple of 4).  A first walk counts the lane's entries at or above bin b1, one warp
+  // scan places each lane's share in the list, and a second walk writes them: the list is in
+  // entry order, and the walks are plain vector loads with no warp votes.
+  int n_list;
+  {
     const int lo = min(n, w * per), hi = min(n, lo + per);
     const int q = per / 32;
     const int a0 = min(hi, lo + ln * q), a1 = min(hi, a0 + q);
     auto listed = [&](uint32_t key) { return key != 0u && (key >> 20) >= b1; };
     int c = 0;
-#pragma unroll 4
+#pragma unroll 1
     for (int i = a0; i < a1; i += 4) {
       const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
       c += listed(v.x) + (i + 1 < a1 && listed(v.y)) + (i + 2 < a1 && listed(v.z)) + (i + 3 < a1 && listed(v.w));
@@ -183,18 +175,18 @@ __device__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* keys, int n, 
     }
     n_list = __shfl_sync(0xffffffffu, inc, 31);
     int at = inc - c;
-    if (c > 0) {
-      for (int i = a0; i < a1; i += 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
-        const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+    for (int i = a0; c > 0 && i < a1; i += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (i + u < a1 && listed(kv[u])) {
-            lk[at] = kv[u];
-            li[at] = (uint32_t)(i + u);
-            ++at;
-          }
-      }
+      for (int u = 0; u < 4; ++u)
+        if (i + u < a1 && listed(kv[u])) {
+          lk[at] = kv[u];
+          li[at] = (uint32_t)(i + u);
+          ++at;
+          --c;
+        }
     }
     if (ln == 0) sh.w_list[w] = n_list;
   }
@@ -202,83 +194,56 @@ __device__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* keys, int n, 
     if (s.tid == 0) {
       sh.thr = 0u;
       sh.n_eq = 0;
-      sh.lists = lists;
     }
     s.sync();
     return;
   }
   s.zero_hist(kHistBins);
   s.sync();
-  // level 2: bits 19..8 of the keys in bin b1
-  if (lists) {
-    for (int j0 = 0; j0 < n_list; j0 += 32) {
-      const uint32_t key = j0 + ln < n_list ? lk[j0 + ln] : 0u;
-      hist_add(sh.hist, (key >> 8) & 0xfffu, key != 0u && (key >> 20) == b1);
-    }
-  } else {
-    for (int i0 = w * 32; i0 < n; i0 += 4 * NT) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) kk[u] = i0 + u * NT + ln < n ? keys[i0 + u * NT + ln] : 0u;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        hist_add(sh.hist, (kk[u] >> 8) & 0xfffu, kk[u] != 0u && (kk[u] >> 20) == b1);
-    }
-  }
+  // level 2: bits 19..8 of the listed keys in bin b1
+#pragma unroll 1
+  for (int j = ln; j < n_list; j += 32)
+    if ((lk[j] >> 20) == b1) atomicAdd(&sh.hist[(lk[j] >> 8) & 0xfffu], 1);
   s.sync();
   s.template pick<kHistBins>(need);
   const uint32_t b2 = (uint32_t)sh.bin;
   need -= sh.before;
-  // level 3: bits 7..0 of the keys matching b1, b2
+  // level 3: bits 7..0 of the listed keys matching b1, b2
   const uint32_t hi24 = (b1 << 12) | b2;
   s.sync();
   s.zero_hist(256);
   s.sync();
-  if (lists) {
-    for (int j0 = 0; j0 < n_list; j0 += 32) {
-      const uint32_t key = j0 + ln < n_list ? lk[j0 + ln] : 0u;
-      hist_add(sh.hist, key & 0xffu, key != 0u && (key >> 8) == hi24);
-    }
-  } else {
-    for (int i0 = w * 32; i0 < n; i0 += 4 * NT) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) kk[u] = i0 + u * NT + ln < n ? keys[i0 + u * NT + ln] : 0u;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) hist_add(sh.hist, kk[u] & 0xffu, kk[u] != 0u && (kk[u] >> 8) == hi24);
-    }
-  }
+#pragma unroll 1
+  for (int j = ln; j < n_list; j += 32)
+    if ((lk[j] >> 8) == hi24) atomicAdd(&sh.hist[lk[j] & 0xffu], 1);
   s.sync();
   s.template pick<256>(need);
   if (s.tid == 0) {
     sh.thr = (hi24 << 8) | (uint32_t)sh.bin;
     sh.n_eq = need - sh.before;
-    sh.lists = lists;
   }
   s.sync();
 }
 
-// Writes the selected entries of keys[0..n) in entry order: calls emit(rank, i) for every kept
-// entry i (rank = its position in the output).  Returns the number kept.  Must follow
-// arr_threshold on the same keys, n and group, with the scratch untouched in between.
-template <int NW, class Emit>
-__device__ int arr_compact(const ArrSel<NW>& s, const uint32_t* keys, int n, Emit emit) {
+// Writes the entry indices of the selected entries, in entry order, to sel[0 .. kept) and
+// returns kept.  Follows arr_threshold on the same n and group with the lists untouched in
+// between.  n < 65536.
+template <int NW>
+__device__ __noinline__ int arr_compact(const ArrSel<NW>& s, int n, int32_t* sel) {
   ArrSelShared& sh = *s.sh;
   const uint32_t thr = sh.thr;
   const int n_eq = sh.n_eq;
-  const bool lists = sh.lists;
   const int w = s.warp(), ln = s.lane();
   const unsigned lt = lanemask_lt();
-  const int per = lists ? ArrSel<NW>::range(n) : (n + NW - 1) / NW;
-  const int lo = min(n, w * per), hi = min(n, lo + per);
-  const uint32_t* lk = lists ? s.scratch + (size_t)w * 2 * per : keys + lo;
-  const uint32_t* li = lists ? lk + per : nullptr;
-  const int len = lists ? sh.w_list[w] : hi - lo;  // entries this warp walks
+  const int per = ArrSel<NW>::range(n);
+  const uint32_t* lk = s.scratch + (size_t)w * 2 * per;
+  const uint32_t* li = lk + per;
+  const int len = sh.w_list[w];
   int gt = 0, eq = 0;
+#pragma unroll 1
   for (int j = ln; j < len; j += 32) {
-    const uint32_t key = lk[j];
-    gt += key != 0u && key > thr;
-    eq += key != 0u && key == thr;
+    gt += lk[j] > thr;
+    eq += lk[j] == thr;
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -286,17 +251,17 @@ __device__ int arr_compact(const ArrSel<NW>& s, const uint32_t* keys, int n, Emi
     eq += __shfl_xor_sync(0xffffffffu, eq, o);
   }
   // One scan of the warps' counts packed in one int (above thr in the high half, equal in the
-  // low half; n < 65536): the entries equal to thr are taken in warp order, so a warp's
-  // output starts after the entries above thr of the warps before it and the taken equal
-  // ones among theirs.
+  // low half): the entries equal to thr are taken in warp order, so a warp's output starts
+  // after the entries above thr of the warps before it and the taken equal ones among theirs.
   int tot_packed;
-  const int before = s.scan(ln == 0 ? (gt << 16) | eq : 0, &tot_packed);  // lane 0 carries the warp's counts
+  const int before = s.scan(ln == 0 ? (gt << 16) | eq : 0, &tot_packed);  // lane 0 carries the counts
   const int pb = __shfl_sync(0xffffffffu, before, 0);
   const int eq_b = pb & 0xffff;
   const int take = max(0, min(eq, n_eq - eq_b));
   int base = (pb >> 16) + min(eq_b, n_eq);
   const int tot = (tot_packed >> 16) + min(tot_packed & 0xffff, n_eq);
   int eq_seen = 0;
+#pragma unroll 1
   for (int j0 = 0; j0 < len; j0 += 32) {
     const int j = j0 + ln;
     const uint32_t key = j < len ? lk[j] : 0u;
@@ -304,7 +269,7 @@ __device__ int arr_compact(const ArrSel<NW>& s, const uint32_t* keys, int n, Emi
     const unsigned em = __ballot_sync(0xffffffffu, is_eq);
     const bool keep = key != 0u && (key > thr || (is_eq && eq_seen + __popc(em & lt) < take));
     const unsigned km = __ballot_sync(0xffffffffu, keep);
-    if (keep) emit(base + __popc(km & lt), lists ? (int)li[j] : lo + j);
+    if (keep) sel[base + __popc(km & lt)] = (int32_t)li[j];
     base += __popc(km);
     eq_seen += __popc(em);
   }

@@ -66,14 +66,14 @@ struct DecBars {
 // positions) come into shared memory in one batch of asynchronous copies, so the merge waits
 // for the L2 only once.
 template <int NW>
-__device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const ScanParams& p, int row, int n_seg) {
+__device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const ScanParams& p, int row, int n_seg,
+                                int32_t* sel_idx, int list_room) {
   constexpr int NT = NW * 32;
   const int K = p.K, n = n_seg * K;
   const uint32_t* lists = p.seg_keys + (size_t)row * n_seg * K;
   const int32_t* pos = p.seg_pos + (size_t)row * n_seg * K;
   const int lw = ArrSel<NW>::list_words(n);
-  int32_t* pos_s = sel.scratch != nullptr && lw + n <= sel.scratch_cap
-                       ? reinterpret_cast<int32_t*>(sel.scratch + lw) : nullptr;
+  int32_t* pos_s = lw + n <= list_room ? reinterpret_cast<int32_t*>(sel.scratch + lw) : nullptr;
   const bool vec = (K & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.seg_keys) | reinterpret_cast<uintptr_t>(p.seg_pos)) & 15) == 0;
   if (vec) {
     for (int c = sel.tid; c < n / 4; c += NT) {
@@ -109,9 +109,9 @@ __device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const Sca
   }
   sel.sync();
   arr_threshold(sel, keys, n, K, true);
+  const int kept = arr_compact(sel, n, sel_idx);
   int32_t* out = p.idx + (size_t)row * K;
-  const int kept = arr_compact(sel, keys, n, [&](int r, int f) { out[r] = pos_s ? pos_s[f] : __ldcg(pos + f); });
-  for (int i = kept + sel.tid; i < K; i += NT) out[i] = -1;
+  for (int r = sel.tid; r < K; r += NT) out[r] = r < kept ? (pos_s ? pos_s[sel_idx[r]] : __ldcg(pos + sel_idx[r])) : -1;
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1)
@@ -143,7 +143,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const bool do_topk = p.K > 0;
   ArrSel<kDecThreads / 32> sel;  // the whole block, once the stream is done
   sel.sh = selsh;
-  sel.bar_id = 0;
   sel.tid = tid;
   const int bs = p.block_max ? U : 1;
   const int seg_blocks = p.block_max ? (int)((e1 - e0 + bs - 1) / bs) : 0;
@@ -268,12 +267,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   {
     // Once every tile has been drained no copy or MMA touches the ring and the query tile any
     // more (the copies and MMAs completed through the mbarriers the epilogue waited on), so
-    // they serve as the selection's scratch (not after a timeout: copies may be in flight
-    // then).
+    // they serve as the selection's scratch: the candidate lists, and the selected entries'
+    // indices (CSA2_MAX_TOPK words at the end).  After a timeout copies may be in flight: the
+    // selection is skipped (the status reports the timeout).
     constexpr int kScratchWords = (kDecStages * kKeyTile + 2 * kDecQHalf) / 4;
-    uint32_t* scratch = bars.timeout ? nullptr : reinterpret_cast<uint32_t*>(ring);
-    sel.scratch = scratch;
-    sel.scratch_cap = scratch ? kScratchWords : 0;
+    constexpr int kListRoom = kScratchWords - CSA2_MAX_TOPK;
+    static_assert(2 * (kDecThreads / 32) * ((kDecSegMax / (kDecThreads / 32) + 1 + 127) & ~127) <= kListRoom,
+                  "selection lists fit in the scratch");
+    sel.scratch = reinterpret_cast<uint32_t*>(ring);
+    int32_t* sel_idx = reinterpret_cast<int32_t*>(ring) + kListRoom;
+    const bool live = !bars.timeout;
     for (int i = tid; i < seg_blocks; i += kDecThreads)
       p.block_max[(size_t)row * p.bmax_stride + e0 / bs + i] = bkeys[i] ? key_score(bkeys[i]) : -INFINITY;
     if (seg == n_seg - 1) {
@@ -284,19 +287,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (long long blk = (L_row + bs - 1) / bs + tid; blk < p.n_blocks; blk += kDecThreads)
           p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
     }
-    if (do_topk) {
+    if (do_topk && live) {
       arr_threshold(sel, keys, seg_len, p.K, true);
+      const int kept = arr_compact(sel, seg_len, sel_idx);
       if (n_seg == 1) {
         int32_t* out = p.idx + (size_t)row * p.K;
-        const int kept = arr_compact(sel, keys, seg_len, [&](int r, int i) { out[r] = (int32_t)(e0 + i); });
-        for (int i = kept + tid; i < p.K; i += kDecThreads) out[i] = -1;
+        for (int r = tid; r < p.K; r += kDecThreads) out[r] = r < kept ? (int32_t)(e0 + sel_idx[r]) : -1;
       } else {
         const size_t o = ((size_t)row * n_seg + seg) * p.K;
-        const int kept = arr_compact(sel, keys, seg_len, [&](int r, int i) {
-          p.seg_keys[o + r] = keys[i];
-          p.seg_pos[o + r] = (int32_t)(e0 + i);
-        });
-        if (sel.tid == 0) {
+        for (int r = tid; r < kept; r += kDecThreads) {
+          p.seg_keys[o + r] = keys[sel_idx[r]];
+          p.seg_pos[o + r] = (int32_t)(e0 + sel_idx[r]);
+        }
+        if (tid == 0) {
           p.seg_cnt[(size_t)row * n_seg + seg] = kept;
           p.seg_thr[(size_t)row * n_seg + seg] = kept >= p.K ? selsh->thr : 0u;
         }
@@ -304,13 +307,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // The last segment of the row to finish merges every segment's list (no waiting:
           // the block that sees the count reach n_seg - 1 knows the others have published).
           __threadfence();
-          sel.sync();
-          if (sel.tid == 0) bars.last = atomicAdd(p.row_done + row, 1) == n_seg - 1;
-          sel.sync();
+          __syncthreads();
+          if (tid == 0) bars.last = atomicAdd(p.row_done + row, 1) == n_seg - 1;
+          __syncthreads();
           if (bars.last) {
             __threadfence();
-            merge_row_lists(sel, keys, p, row, n_seg);
-            if (sel.tid == 0) p.row_done[row] = 0;
+            merge_row_lists(sel, keys, p, row, n_seg, sel_idx, kListRoom);
+            if (tid == 0) p.row_done[row] = 0;
           }
         }
       }
