@@ -294,7 +294,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   AttnShared& sh = *reinterpret_cast<AttnShared*>(ks + kKBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, n_tiles = gridDim.x, row = blockIdx.y;
+  // blockIdx.y = k orders the tiles so that the window-only tiles (which need nothing from
+  // the previous kernel) come first; tile = (k + tiles holding selected entries) mod tiles
+  const int row = blockIdx.x, n_tiles = gridDim.y;
+  const int sel_tiles = min(n_tiles, (p.K + kTileE - 1) / kTileE);
+  const int tile = (blockIdx.y + sel_tiles) % n_tiles;
+  const bool needs_idx = tile * kTileE < p.K;
   const int b = p.seq_of_row[row];
   const long long qp = p.q_pos[row];
   const long long pos0 = p.swa_pos0[b];
@@ -309,6 +314,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   }
   if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kTmemCols);
   rope_table(sh.cs, p, qp, 1.f);
+  // the merge kernel may launch now (it waits for this grid before reading the partials)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  load_query(p, row, qs, sh.cs);  // the query is an input of the step, not of the previous kernel
+  // With programmatic dependent launch this block may run while the kernel that writes the
+  // selected indices is still finishing: tiles with selected entries wait for it here.
+  if (needs_idx) asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (tid < kTileE) {
     const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTileE + tid);
     sh.src.ptr[tid] = s.valid ? s.ptr : nullptr;
@@ -316,14 +332,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
     sh.src.rs[tid] = s.rs;
     sh.src.fmt[tid] = s.valid ? s.fmt : -1;
   }
-  tc05::fence_before();
   __syncthreads();
-  tc05::fence_after();
-  const uint32_t tmem = sh.tmem_base;
-
   gather_tile(sh.src, ks, p.q);
   cp_async_commit();
-  load_query(p, row, qs, sh.cs);
   cp_async_wait<0>();
   // generic-proxy writes (cp.async and stores) become visible to the tensor cores
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -488,6 +499,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int n_split) {
   __shared__ float fac[4][64];  // per head: weight of each split (n_split <= 64)
   __shared__ float inv_den[4];
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the tiles' partials are complete
   const int row = blockIdx.x, hl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + hl;
   const long long qp = p.q_pos[row];
@@ -526,16 +538,26 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
   float4 acc[4] = {};
   const float* base = p.part_o + ((size_t)row * n_split * kHeads + h) * kHeadDim + d0;
   const size_t split_stride = (size_t)kHeads * kHeadDim;
-  for (int s = 0; s < n_split; ++s) {
-    const float4* src = reinterpret_cast<const float4*>(base + s * split_stride);
-    const float f = fac[hl][s];
+  // four tiles' partials in flight per step (one memory round trip per four tiles)
+#pragma unroll 1
+  for (int s0 = 0; s0 < n_split; s0 += 4) {
+    float4 v[4][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v = __ldg(src + k);
-      acc[k].x = fmaf(f, v.x, acc[k].x);
-      acc[k].y = fmaf(f, v.y, acc[k].y);
-      acc[k].z = fmaf(f, v.z, acc[k].z);
-      acc[k].w = fmaf(f, v.w, acc[k].w);
+    for (int u = 0; u < 4; ++u) {
+      const float4* src = reinterpret_cast<const float4*>(base + (size_t)(s0 + u) * split_stride);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[u][k] = s0 + u < n_split ? __ldcg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float f = s0 + u < n_split ? fac[hl][s0 + u] : 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x = fmaf(f, v[u][k].x, acc[k].x);
+        acc[k].y = fmaf(f, v[u][k].y, acc[k].y);
+        acc[k].z = fmaf(f, v[u][k].z, acc[k].z);
+        acc[k].w = fmaf(f, v[u][k].w, acc[k].w);
+      }
     }
   }
   const float inv = inv_den[hl];
@@ -568,11 +590,24 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   cudaError_t e =
       cudaFuncSetAttribute(attn_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc05_kernel<<<dim3(n_split, p.n_rows), kAttnThreads, kAttnSmemBytes, stream>>>(p);
-  e = cudaGetLastError();
+  // Both kernels may start before their predecessor in the stream has finished
+  // (programmatic dependent launch); each waits for it where it reads its results.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_rows, n_split);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = kAttnSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc05_kernel, p);
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(p.n_rows, kHeads / 4), 128, 0, stream>>>(p, n_split);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(p.n_rows, kHeads / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, n_split);
 }
 
 }  // namespace csa2

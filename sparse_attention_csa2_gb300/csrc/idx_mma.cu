@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   tc05::fence_after();
   const uint32_t tmem = bars.tmem_base;
+  // Every block of a single-wave grid is resident: a dependent kernel (the attention) may be
+  // scheduled onto the SMs left free; it waits for this grid before it reads the indices.
+  if (p.pdl_trigger) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -617,7 +620,11 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
   const size_t smem = dec_smem_bytes(p.K, max_seg_blocks);
   cudaError_t e = cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  idx_mma_decode_kernel<<<dim3(n_seg, p.n_rows), kDecThreads, smem, stream>>>(tmK, tmQ, p);
+  ScanParams q = p;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    q.pdl_trigger = (long long)n_seg * p.n_rows <= sms;  // one CTA per SM: a single wave
+  idx_mma_decode_kernel<<<dim3(n_seg, p.n_rows), kDecThreads, smem, stream>>>(tmK, tmQ, q);
   return cudaGetLastError();
 }
 

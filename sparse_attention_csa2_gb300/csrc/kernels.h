@@ -35,6 +35,8 @@ struct ScanParams {
   uint32_t* seg_thr;          // [n_rows, n_seg] K-th key of each full segment list, else 0
   int32_t* row_done;          // tcgen05 decode: [n_rows] zeroed counters; the last segment merges
   int32_t* dev_status;        // optional: CSA2_ETIMEOUT when a bounded wait gives up
+  int pdl_trigger;            // set by the launcher: the grid is one wave, so a kernel launched
+                              // after it with programmatic dependent launch may start early
 };
 
 size_t scan_smem_bytes(bool fp8, int K);
