@@ -267,7 +267,9 @@ typedef struct csa2_decode_args {
   int32_t* n_pool;            /* FULL_POOL: out; REINDEX: in  [n_rows] */
   int32_t* idx;               /* FULL, FULL_POOL, REINDEX: out; REUSE: in  [n_rows, K] */
   csa2_attn_args attn;
-  void* workspace;            /* csa2_fused_decode_workspace_size bytes */
+  void* workspace;            /* csa2_fused_decode_workspace_size bytes, any contents (the
+                                 per-row completion counters it holds carry a per-call tag,
+                                 so nothing needs clearing between calls) */
   size_t workspace_bytes;
   /* Optional tracing: cudaEvent_t handles (as void*) recorded on `stream` at the stage
    * boundaries: [0] right before the indexer scan kernel (after the reset of its row

@@ -1,5 +1,7 @@
 // The C ABI of the CSA2 attention step (include/csa2.h): host-side validation, workspace
 // layout, work decomposition and launch sequencing.  Nothing here synchronizes or allocates.
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -9,6 +11,16 @@
 
 namespace csa2 {
 namespace {
+
+// Tag of one fused decode call for the scan's per-row completion counters: consecutive calls
+// get different tags, so a counter left by an earlier call (or never written) is recognised
+// and restarted instead of being cleared before every call.  Starts from a clock reading so
+// that a workspace shared across processes is unlikely to hold a matching stale tag.
+uint32_t next_call_tag() {
+  static std::atomic<uint32_t> tag{static_cast<uint32_t>(
+      std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull)};
+  return tag.fetch_add(1, std::memory_order_relaxed) + 1;
+}
 
 constexpr int kScanMaxK = 512;  // per-warp survivor buffers of the fused scan fit K <= 512
 
@@ -403,7 +415,7 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     else
       n_seg = scan_segments(n_rows, L);
     ws += lists_bytes(n_rows, n_seg, a->K);
-    if (n_seg > 1) ws += align_up((size_t)n_rows * 4);  // per-row completion counters
+    if (n_seg > 1) ws += align_up((size_t)n_rows * 8);  // per-row completion counters
     if (a->mode == CSA2_MODE_FULL_POOL) {
       const long long nb = (ix->n_records + a->block_size - 1) / a->block_size;
       ws += align_up((size_t)n_rows * nb * 4) + align_up((size_t)n_rows * a->n_keep * 4);
@@ -489,8 +501,8 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
     p.dev_status = at.dev_status;
     const bool fused_merge = tc05 && mma_decode_can_merge(n_seg, a->K);
     if (n_seg > 1) {
-      p.row_done = c.take<int32_t>((size_t)n_rows);
-      if (fused_merge && cudaMemsetAsync(p.row_done, 0, (size_t)n_rows * 4, s) != cudaSuccess) return CSA2_ECUDA;
+      p.row_done = c.take<unsigned long long>((size_t)n_rows);
+      p.call_tag = next_call_tag();
       if (!fused_merge) p.row_done = nullptr;
     }
     mark(0);  // stage 0: the indexer scan kernel alone

@@ -500,6 +500,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
   __shared__ float fac[4][64];  // per head: weight of each split (n_split <= 64)
   __shared__ float inv_den[4];
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the tiles' partials are complete
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int row = blockIdx.x, hl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + hl;
   const long long qp = p.q_pos[row];

@@ -59,6 +59,25 @@ struct DecBars {
   int last;       // this block is the last segment of its row to finish
 };
 
+// Counts one finished segment of a row in `ctr` (tag << 32 | count; another tag means an
+// earlier call: the count restarts).  Returns true for the segment that completes the row.
+// Once a block of this call has installed the tag (one compare-and-swap), every other block
+// counts with a single atomic add; the retries are bounded all the same.
+__device__ bool count_segment_done(unsigned long long* ctr, uint32_t tag, int n_seg, int32_t* dev_status) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int tries = 0; tries < 64; ++tries) {
+    if ((uint32_t)(cur >> 32) == tag) {
+      const unsigned long long old = atomicAdd(ctr, 1ull);  // the tag stays for the whole call
+      return (uint32_t)old + 1u == (uint32_t)n_seg;
+    }
+    const unsigned long long prev = atomicCAS(ctr, cur, ((unsigned long long)tag << 32) | 1ull);
+    if (prev == cur) return n_seg == 1;
+    cur = prev;
+  }
+  if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
+  return false;
+}
+
 // The last segment block of a row merges the row's lists: every list entry's key goes into
 // the key array (entries below the largest per-segment K-th key cannot be selected and are
 // left out, and the level-1 histogram is counted on the way), and the K best, in position
@@ -117,6 +136,9 @@ __device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const Sca
 __global__ void __launch_bounds__(kDecThreads, 1)
     idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                           const ScanParams p) {
+  // launched with programmatic dependent launch: wait for the previous kernel in the stream
+  // before reading any input
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* ring = smem;
@@ -309,14 +331,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (p.row_done != nullptr) {
           // The last segment of the row to finish merges every segment's list (no waiting:
           // the block that sees the count reach n_seg - 1 knows the others have published).
+          // The counter carries the call's tag in its high half: a stale value from an
+          // earlier call restarts at 1, so the workspace needs no clearing between calls.
           __threadfence();
           __syncthreads();
-          if (tid == 0) bars.last = atomicAdd(p.row_done + row, 1) == n_seg - 1;
+          if (tid == 0) bars.last = count_segment_done(p.row_done + row, p.call_tag, n_seg, p.dev_status);
           __syncthreads();
           if (bars.last) {
             __threadfence();
             merge_row_lists(sel, keys, p, row, n_seg, sel_idx, kListRoom);
-            if (tid == 0) p.row_done[row] = 0;
           }
         }
       }
@@ -624,7 +647,20 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
     q.pdl_trigger = (long long)n_seg * p.n_rows <= sms;  // one CTA per SM: a single wave
-  idx_mma_decode_kernel<<<dim3(n_seg, p.n_rows), kDecThreads, smem, stream>>>(tmK, tmQ, q);
+  // Programmatic dependent launch: the blocks may become resident while the previous kernel
+  // in the stream finishes; they wait for it before reading anything.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_seg, p.n_rows);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, idx_mma_decode_kernel, tmK, tmQ, q);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -33,7 +33,9 @@ struct ScanParams {
   int32_t* seg_pos;
   int32_t* seg_cnt;           // [n_rows, n_seg]
   uint32_t* seg_thr;          // [n_rows, n_seg] K-th key of each full segment list, else 0
-  int32_t* row_done;          // tcgen05 decode: [n_rows] zeroed counters; the last segment merges
+  unsigned long long* row_done;  // tcgen05 decode: [n_rows] (call tag << 32 | finished segments);
+                                 // the last segment of a row to finish merges the row's lists
+  uint32_t call_tag;             // differs between consecutive calls (no clearing of row_done)
   int32_t* dev_status;        // optional: CSA2_ETIMEOUT when a bounded wait gives up
   int pdl_trigger;            // set by the launcher: the grid is one wave, so a kernel launched
                               // after it with programmatic dependent launch may start early
