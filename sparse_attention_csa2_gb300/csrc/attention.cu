@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   }
   if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kTmemCols);
   rope_table(sh.cs, p, qp, 1.f);
-  // the merge kernel may launch now (it waits for this grid before reading the partials)
+  // the next kernel in the stream may launch now (it waits for this grid before reading)
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   tc05::fence_before();
   __syncthreads();
@@ -494,92 +494,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   }
 }
 
-// Merges the tiles of one row for 4 heads: log-sum-exp over tiles plus the sink,
-// normalisation, inverse RoPE on dims 448..511.  Thread -> (head h0 + tid/32, 16 dims).
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int n_split) {
-  __shared__ float fac[4][64];  // per head: weight of each split (n_split <= 64)
-  __shared__ float inv_den[4];
+// Merges the tiles of one row for one head (block = (row, head), thread = 4 dims): per head
+// the log-sum-exp over the tiles plus the sink (in the denominator only), the normalised sum
+// of the tiles' outputs, and the inverse RoPE on dims 448..511.  Every tile's partial of the
+// thread's dims is loaded at once (one memory round trip).
+constexpr int kMaxTiles = 16;  // K + window <= 2048 entries
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int n_tiles) {
+  __shared__ float fac[kMaxTiles];
+  __shared__ float inv_den;
+  __shared__ float cs[kRopeDim];
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the tiles' partials are complete
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const int row = blockIdx.x, hl = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 4 + hl;
+  const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const long long qp = p.q_pos[row];
-  {
-    // warp hl: per-split statistics of head h, two splits per lane
+  if (tid < 32) {
+    // the row's tile statistics for head h, one tile per lane
     const float sk = __ldg(p.sink + h);
-    float m[2], l[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int s = lane + 32 * k;
-      m[k] = -INFINITY;
-      l[k] = 0.f;
-      if (s < n_split) {
-        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (((size_t)row * n_split + s) * kHeads + h) * 2);
-        m[k] = ml.x;
-        l[k] = ml.y;
-      }
+    float m = -INFINITY, l = 0.f;
+    if (tid < n_tiles) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + ((size_t)row * n_tiles + tid) * kHeads + h);
+      m = v.x;
+      l = v.y;
     }
-    const float M = fmaxf(warp_max(fmaxf(m[0], m[1])), sk);
-    float f[2], den = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      f[k] = m[k] == -INFINITY ? 0.f : __expf(m[k] - M);
-      den += l[k] * f[k];
-      const int s = lane + 32 * k;
-      if (s < n_split) fac[hl][s] = f[k];
-    }
-    den = warp_sum(den) + __expf(sk - M);
-    if (lane == 0) {
-      inv_den[hl] = 1.f / den;
+    const float M = fmaxf(warp_max(m), sk);
+    const float f = m == -INFINITY ? 0.f : __expf(m - M);
+    const float den = warp_sum(l * f) + __expf(sk - M);
+    if (tid < n_tiles) fac[tid] = f;
+    if (tid == 0) {
+      inv_den = 1.f / den;
       if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + h] = __expf(sk - M) / den;
     }
+  } else if (tid < 64) {
+    rope_cs(qp, p.inv_freq[tid - 32], -1.f, &cs[tid - 32], &cs[tid]);
   }
+  const int d = 4 * tid;
+  const float* base = p.part_o + ((size_t)row * n_tiles * kHeads + h) * kHeadDim + d;
+  float4 v[kMaxTiles];
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t)
+    v[t] = t < n_tiles ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)t * kHeads * kHeadDim))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
-  const int d0 = lane * 16;
-  float4 acc[4] = {};
-  const float* base = p.part_o + ((size_t)row * n_split * kHeads + h) * kHeadDim + d0;
-  const size_t split_stride = (size_t)kHeads * kHeadDim;
-  // four tiles' partials in flight per step (one memory round trip per four tiles)
-#pragma unroll 1
-  for (int s0 = 0; s0 < n_split; s0 += 4) {
-    float4 v[4][4];
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float4* src = reinterpret_cast<const float4*>(base + (size_t)(s0 + u) * split_stride);
+  for (int t = 0; t < kMaxTiles; ++t) {
+    const float f = t < n_tiles ? fac[t] : 0.f;
+    acc.x = fmaf(f, v[t].x, acc.x);
+    acc.y = fmaf(f, v[t].y, acc.y);
+    acc.z = fmaf(f, v[t].z, acc.z);
+    acc.w = fmaf(f, v[t].w, acc.w);
+  }
+  float o[4] = {acc.x * inv_den, acc.y * inv_den, acc.z * inv_den, acc.w * inv_den};
+  if (d >= kHeadDim - kRopeDim) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[u][k] = s0 + u < n_split ? __ldcg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float f = s0 + u < n_split ? fac[hl][s0 + u] : 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[k].x = fmaf(f, v[u][k].x, acc[k].x);
-        acc[k].y = fmaf(f, v[u][k].y, acc[k].y);
-        acc[k].z = fmaf(f, v[u][k].z, acc[k].z);
-        acc[k].w = fmaf(f, v[u][k].w, acc[k].w);
-      }
+    for (int j = 0; j < 2; ++j) {
+      const int pi = (d + 2 * j - (kHeadDim - kRopeDim)) >> 1;
+      const float c = cs[pi], sn = cs[32 + pi];
+      const float x = o[2 * j], y = o[2 * j + 1];
+      o[2 * j] = x * c - y * sn;
+      o[2 * j + 1] = x * sn + y * c;
     }
   }
-  const float inv = inv_den[hl];
-  float* dst = p.out + ((size_t)row * kHeads + h) * kHeadDim + d0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float v[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv};
-    const int d = d0 + 4 * k;
-    if (d >= kHeadDim - kRopeDim) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int pi = (d + 2 * j - (kHeadDim - kRopeDim)) >> 1;
-        float c, sn;
-        rope_cs(qp, p.inv_freq[pi], -1.f, &c, &sn);
-        const float x = v[2 * j], y = v[2 * j + 1];
-        v[2 * j] = x * c - y * sn;
-        v[2 * j + 1] = x * sn + y * c;
-      }
-    }
-    *reinterpret_cast<float4*>(dst + 4 * k) = make_float4(v[0], v[1], v[2], v[3]);
-  }
+  *reinterpret_cast<float4*>(p.out + ((size_t)row * kHeads + h) * kHeadDim + d) = make_float4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace
@@ -591,8 +567,8 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   cudaError_t e =
       cudaFuncSetAttribute(attn_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
   if (e != cudaSuccess) return e;
-  // Both kernels may start before their predecessor in the stream has finished
-  // (programmatic dependent launch); each waits for it where it reads its results.
+  // Both kernels may start before their predecessor in the stream has finished (programmatic
+  // dependent launch); each waits for it where it reads its results.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -605,7 +581,7 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_tc05_kernel, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(p.n_rows, kHeads / 4);
+  cfg.gridDim = dim3(p.n_rows, kHeads);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, n_split);

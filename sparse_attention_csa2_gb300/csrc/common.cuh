@@ -169,4 +169,25 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ----------------------------------------------------------------------------- arrivals
+// Counts one arrival (a finished part of a row) in `ctr` = tag << 32 | count, where another
+// tag means an earlier call: the count restarts, so the counters need no clearing between
+// calls.  Returns true for the arrival that completes the n parts.  Once a block of this call
+// has installed the tag (one compare-and-swap), every other block counts with a single atomic
+// add; the retries are bounded all the same.
+__device__ __forceinline__ bool count_arrival(unsigned long long* ctr, uint32_t tag, int n, int32_t* dev_status) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int tries = 0; tries < 64; ++tries) {
+    if ((uint32_t)(cur >> 32) == tag) {
+      const unsigned long long old = atomicAdd(ctr, 1ull);  // the tag stays for the whole call
+      return (uint32_t)old + 1u == (uint32_t)n;
+    }
+    const unsigned long long prev = atomicCAS(ctr, cur, ((unsigned long long)tag << 32) | 1ull);
+    if (prev == cur) return n == 1;
+    cur = prev;
+  }
+  if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
+  return false;
+}
+
 }  // namespace csa2

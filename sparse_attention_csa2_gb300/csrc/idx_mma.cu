@@ -59,25 +59,6 @@ struct DecBars {
   int last;       // this block is the last segment of its row to finish
 };
 
-// Counts one finished segment of a row in `ctr` (tag << 32 | count; another tag means an
-// earlier call: the count restarts).  Returns true for the segment that completes the row.
-// Once a block of this call has installed the tag (one compare-and-swap), every other block
-// counts with a single atomic add; the retries are bounded all the same.
-__device__ bool count_segment_done(unsigned long long* ctr, uint32_t tag, int n_seg, int32_t* dev_status) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int tries = 0; tries < 64; ++tries) {
-    if ((uint32_t)(cur >> 32) == tag) {
-      const unsigned long long old = atomicAdd(ctr, 1ull);  // the tag stays for the whole call
-      return (uint32_t)old + 1u == (uint32_t)n_seg;
-    }
-    const unsigned long long prev = atomicCAS(ctr, cur, ((unsigned long long)tag << 32) | 1ull);
-    if (prev == cur) return n_seg == 1;
-    cur = prev;
-  }
-  if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
-  return false;
-}
-
 // The last segment block of a row merges the row's lists: every list entry's key goes into
 // the key array (entries below the largest per-segment K-th key cannot be selected and are
 // left out, and the level-1 histogram is counted on the way), and the K best, in position
@@ -335,7 +316,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // earlier call restarts at 1, so the workspace needs no clearing between calls.
           __threadfence();
           __syncthreads();
-          if (tid == 0) bars.last = count_segment_done(p.row_done + row, p.call_tag, n_seg, p.dev_status);
+          if (tid == 0) bars.last = count_arrival(p.row_done + row, p.call_tag, n_seg, p.dev_status);
           __syncthreads();
           if (bars.last) {
             __threadfence();
