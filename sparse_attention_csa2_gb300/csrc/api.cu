@@ -499,17 +499,20 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
     const bool tc05 = scan_path(&ic, true) == ScanPath::kTc05Decode;
     if (tc05 && a->mode != CSA2_MODE_FULL_POOL) p.unit = 128;
     p.dev_status = at.dev_status;
-    const bool fused_merge = tc05 && mma_decode_can_merge(n_seg, a->K);
+    const int seg_blocks = p.block_max ? (int)(((ic.n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg) : 0;
+    p.cluster_merge = tc05 && env_int("CSA2_SCAN_CLUSTER", 1) != 0 && mma_decode_cluster_ok(n_seg, n_rows, a->K, seg_blocks);
+    const bool fused_merge = tc05 && !p.cluster_merge && mma_decode_can_merge(n_seg, a->K);
     if (n_seg > 1) {
       p.row_done = c.take<unsigned long long>((size_t)n_rows);
       p.call_tag = next_call_tag();
       if (!fused_merge) p.row_done = nullptr;
     }
+    if (p.cluster_merge) p.seg_keys = nullptr, p.seg_pos = nullptr, p.seg_cnt = nullptr, p.seg_thr = nullptr;
     mark(0);  // stage 0: the indexer scan kernel alone
     e = launch_scan(p, &ic, true, n_seg, s);
     if (e != cudaSuccess) return CSA2_ECUDA;
     mark(1);
-    if (n_seg > 1 && !fused_merge) {
+    if (n_seg > 1 && !fused_merge && !p.cluster_merge) {
       FeedParams m{};
       m.n_rows = n_rows;
       m.K = a->K;
@@ -553,8 +556,14 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
     csa2_index_args ic = a->index;
     ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
     ic.block_max = nullptr;
-    const bool fused_merge = scan_path(&ic, true) == ScanPath::kTc05Decode && mma_decode_can_merge(n_seg, a->K);
-    n += 1 + (n_seg > 1 && !fused_merge ? 1 : 0);  // the tcgen05 scan merges its segments itself
+    const bool tc05 = scan_path(&ic, true) == ScanPath::kTc05Decode;
+    const int unit = a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128;
+    const int seg_blocks =
+        a->mode == CSA2_MODE_FULL_POOL ? (int)(((ic.n_records + unit - 1) / unit + n_seg - 1) / n_seg) : 0;
+    const bool merged = tc05 && ((env_int("CSA2_SCAN_CLUSTER", 1) != 0 &&
+                                  mma_decode_cluster_ok(n_seg, a->attn.n_rows, a->K, seg_blocks)) ||
+                                 mma_decode_can_merge(n_seg, a->K));
+    n += 1 + (n_seg > 1 && !merged ? 1 : 0);  // the tcgen05 scan merges its segments itself
     if (a->mode == CSA2_MODE_FULL_POOL) n += 2;
   }
   n += 2;  // attention tiles and their merge

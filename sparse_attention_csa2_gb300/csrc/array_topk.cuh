@@ -129,9 +129,56 @@ struct ArrSel {
 // (key >> 20) of the candidates.  Afterwards sh->thr and sh->n_eq describe the selection:
 // keys > thr, and the first n_eq keys == thr in entry order (thr = 0, n_eq = 0 when at most k
 // candidates exist: all are kept).
+// The histogram levels' bin choice, for a block on its own: the block's histogram.
 template <int NW>
-__device__ __noinline__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* keys, int n, int k,
-                                           bool hist_ready) {
+struct LocalPick {
+  template <int NBINS>
+  __device__ __forceinline__ void run(const ArrSel<NW>& s, int need) const {
+    s.template pick<NBINS>(need);
+  }
+};
+
+// The bin choice for the blocks of a thread-block cluster that select over the union of their
+// arrays (the segments of one row): block 0 adds the others' histograms into its own (through
+// distributed shared memory), picks, and writes bin / before / total into every block.  All
+// blocks of the cluster call it at the same points.
+template <int NW>
+struct ClusterPick {
+  uint32_t rank, n_cta;
+  template <int NBINS>
+  __device__ __forceinline__ void run(const ArrSel<NW>& s, int need) const {
+    constexpr int NT = NW * 32;
+    ArrSelShared& sh = *s.sh;
+    cluster_sync();  // every block's histogram is final
+    if (rank == 0) {
+#pragma unroll 1
+      for (int i = s.tid; i < NBINS / 4; i += NT) {
+        int4 acc = *reinterpret_cast<const int4*>(&sh.hist[4 * i]);
+#pragma unroll 4
+        for (uint32_t c = 1; c < n_cta; ++c) {
+          const uint4 v = cluster_ld_v4(cluster_map(&sh.hist[4 * i], c));
+          acc.x += (int)v.x;
+          acc.y += (int)v.y;
+          acc.z += (int)v.z;
+          acc.w += (int)v.w;
+        }
+        *reinterpret_cast<int4*>(&sh.hist[4 * i]) = acc;
+      }
+      s.sync();
+      s.template pick<NBINS>(need);
+      if (s.tid > 0 && (uint32_t)s.tid < n_cta) {
+        cluster_st_s32(cluster_map(&sh.bin, s.tid), sh.bin);
+        cluster_st_s32(cluster_map(&sh.before, s.tid), sh.before);
+        cluster_st_s32(cluster_map(&sh.total, s.tid), sh.total);
+      }
+    }
+    cluster_sync();  // the choice is visible in every block; the histograms may be reused
+  }
+};
+
+template <int NW, class Pick>
+__device__ __noinline__ void arr_threshold_impl(const ArrSel<NW>& s, const uint32_t* keys, int n, int k,
+                                                bool hist_ready, Pick picker) {
   constexpr int NT = NW * 32;
   ArrSelShared& sh = *s.sh;
   const int w = s.warp(), ln = s.lane();
@@ -143,7 +190,7 @@ __device__ __noinline__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* 
       if (keys[i] != 0u) atomicAdd(&sh.hist[keys[i] >> 20], 1);
     s.sync();
   }
-  s.template pick<kHistBins>(k);
+  picker.template run<kHistBins>(s, k);
   const bool all = sh.total <= k;  // at most k candidates: keep them all
   const uint32_t b1 = all ? 0u : (uint32_t)sh.bin;
   int need = k - sh.before;
@@ -205,7 +252,7 @@ __device__ __noinline__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* 
   for (int j = ln; j < n_list; j += 32)
     if ((lk[j] >> 20) == b1) atomicAdd(&sh.hist[(lk[j] >> 8) & 0xfffu], 1);
   s.sync();
-  s.template pick<kHistBins>(need);
+  picker.template run<kHistBins>(s, need);
   const uint32_t b2 = (uint32_t)sh.bin;
   need -= sh.before;
   // level 3: bits 7..0 of the listed keys matching b1, b2
@@ -217,12 +264,18 @@ __device__ __noinline__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* 
   for (int j = ln; j < n_list; j += 32)
     if ((lk[j] >> 8) == hi24) atomicAdd(&sh.hist[lk[j] & 0xffu], 1);
   s.sync();
-  s.template pick<256>(need);
+  picker.template run<256>(s, need);
   if (s.tid == 0) {
     sh.thr = (hi24 << 8) | (uint32_t)sh.bin;
     sh.n_eq = need - sh.before;
   }
   s.sync();
+}
+
+template <int NW>
+__device__ __forceinline__ void arr_threshold(const ArrSel<NW>& s, const uint32_t* keys, int n, int k,
+                                              bool hist_ready) {
+  arr_threshold_impl(s, keys, n, k, hist_ready, LocalPick<NW>{});
 }
 
 // Writes the entry indices of the selected entries, in entry order, to sel[0 .. kept) and
@@ -275,6 +328,65 @@ __device__ __noinline__ int arr_compact(const ArrSel<NW>& s, int n, int32_t* sel
   }
   s.sync();
   return tot;
+}
+
+// Cluster mode (the blocks of a cluster select over the union of their arrays, in block order):
+// after arr_threshold_impl with ClusterPick, each block publishes how many of its listed
+// entries lie above the threshold and how many equal it; the entries equal to the threshold
+// are taken in block order, then entry order.  Writes this block's selected entries (entry
+// indices, in order) to sel and returns their number; *base gets the row offset of the first,
+// *total the row's number of selected entries.
+template <int NW>
+__device__ __noinline__ int arr_compact_cluster(const ArrSel<NW>& s, int n, int32_t* sel, uint32_t rank,
+                                                uint32_t n_cta, int* base, int* total) {
+  ArrSelShared& sh = *s.sh;
+  const uint32_t thr = sh.thr;
+  const int n_eq = sh.n_eq;
+  const int w = s.warp(), ln = s.lane();
+  const int per = ArrSel<NW>::range(n);
+  const uint32_t* lk = s.scratch + (size_t)w * 2 * per;
+  const int len = sh.w_list[w];
+  int gt = 0, eq = 0;
+#pragma unroll 1
+  for (int j = ln; j < len; j += 32) {
+    gt += lk[j] > thr;
+    eq += lk[j] == thr;
+  }
+  int tot;
+  const int packed_before = s.scan((gt << 16) | eq, &tot);  // per-thread packed counts
+  (void)packed_before;
+  if (s.tid == 0) {
+    sh.aux[0] = (uint32_t)(tot >> 16);     // above the threshold in this block
+    sh.aux[1] = (uint32_t)(tot & 0xffff);  // equal to it
+  }
+  cluster_sync();  // every block's counts are published
+  if (w == 0) {
+    int g = 0, e = 0;
+    if ((uint32_t)ln < n_cta) {
+      g = cluster_ld_s32(cluster_map(&sh.aux[0], ln));
+      e = cluster_ld_s32(cluster_map(&sh.aux[1], ln));
+    }
+    int gb = (uint32_t)ln < rank ? g : 0, eb = (uint32_t)ln < rank ? e : 0, G = g, E = e;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      gb += __shfl_xor_sync(0xffffffffu, gb, o);
+      eb += __shfl_xor_sync(0xffffffffu, eb, o);
+      G += __shfl_xor_sync(0xffffffffu, G, o);
+      E += __shfl_xor_sync(0xffffffffu, E, o);
+    }
+    const int e_mine = __shfl_sync(0xffffffffu, e, (int)rank);
+    if (ln == 0) {
+      sh.aux[2] = (uint32_t)(gb + min(eb, n_eq));
+      sh.aux[3] = (uint32_t)max(0, min(e_mine, n_eq - eb));
+      sh.aux[4] = (uint32_t)(G + min(E, n_eq));
+    }
+  }
+  cluster_sync();  // every block has read the others' counts
+  if (s.tid == 0) sh.n_eq = (int)sh.aux[3];
+  s.sync();
+  *base = (int)sh.aux[2];
+  *total = (int)sh.aux[4];
+  return arr_compact(s, n, sel);
 }
 
 }  // namespace csa2

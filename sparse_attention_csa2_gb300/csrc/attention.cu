@@ -227,26 +227,32 @@ __device__ __forceinline__ void gather_tile(const TileSrc& m, uint8_t* ks, const
   }
 }
 
-// q' = RoPE(q) of the row's 64 heads into `qs` (panel layout, 64 rows): consecutive threads
-// take consecutive 16-byte chunks; the rotary pairs are dims 448 + 2i, 448 + 2i + 1.
-__device__ __forceinline__ void load_query(const AttnParams& p, int row, uint8_t* qs, const float* cs) {
-  const uint4* qsrc = reinterpret_cast<const uint4*>(p.q) + (size_t)row * kHeads * (kHeadDim / 8);
+// The row's query (64 heads x 512 dims) into `qs` (panel layout, 64 rows) by cp.async, one
+// 16-byte chunk per copy (consecutive threads on consecutive chunks); rotate_query then turns
+// the rotary pairs (dims 448 + 2i, 448 + 2i + 1) in place once the copies have landed.
+__device__ __forceinline__ void copy_query(const AttnParams& p, int row, uint8_t* qs) {
+  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q) + (size_t)row * kHeads * kHeadDim * 2;
 #pragma unroll 4
   for (int k = 0; k < kHeads * kHeadDim / 8 / kAttnThreads; ++k) {
     const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 6, ch = idx & 63;
-    uint4 v = __ldg(qsrc + idx);
-    if (ch >= 56) {
-      uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    cp_async16(qs + sw128_off(h, ch, kHeads), qsrc + (size_t)idx * 16, true);
+  }
+}
+__device__ __forceinline__ void rotate_query(uint8_t* qs, const float* cs) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = (ch - 56) * 4 + j;  // rotary pair index
-        const float x = bf16_lo(w4[j]), y = bf16_hi(w4[j]);
-        const float c = cs[i], s = cs[32 + i];
-        w4[j] = pack_bf16x2(x * c - y * s, x * s + y * c);
-      }
-      v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  for (int k = 0; k < kHeads * 8 / kAttnThreads; ++k) {
+    const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 3, ch = 56 + (idx & 7);
+    uint4* q4 = reinterpret_cast<uint4*>(qs + sw128_off(h, ch, kHeads));
+    const uint4 v = *q4;
+    uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = (ch - 56) * 4 + j;  // rotary pair index
+      const float x = bf16_lo(w4[j]), y = bf16_hi(w4[j]);
+      const float c = cs[i], sn = cs[32 + i];
+      w4[j] = pack_bf16x2(x * c - y * sn, x * sn + y * c);
     }
-    *reinterpret_cast<uint4*>(qs + sw128_off(h, ch, kHeads)) = v;
+    *q4 = make_uint4(w4[0], w4[1], w4[2], w4[3]);
   }
 }
 
@@ -321,9 +327,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   tc05::fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  load_query(p, row, qs, sh.cs);  // the query is an input of the step, not of the previous kernel
+  copy_query(p, row, qs);  // the query is an input of the step, not of the previous kernel
+  cp_async_commit();
   // With programmatic dependent launch this block may run while the kernel that writes the
-  // selected indices is still finishing: tiles with selected entries wait for it here.
+  // selected indices is still finishing: tiles with selected entries wait for it here (the
+  // query copies are in flight meanwhile).
   if (needs_idx) asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (tid < kTileE) {
     const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTileE + tid);
@@ -336,6 +344,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   gather_tile(sh.src, ks, p.q);
   cp_async_commit();
   cp_async_wait<0>();
+  __syncthreads();
+  rotate_query(qs, sh.cs);
   // generic-proxy writes (cp.async and stores) become visible to the tensor cores
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   tc05::fence_before();

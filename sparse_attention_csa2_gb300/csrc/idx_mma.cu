@@ -18,6 +18,7 @@
 //   prefill (NQ = 8): a persistent grid walks (8-query tile, key range) work items of one
 //                     sequence; causal masking per query; scores are written out.
 #include <cudaTypedefs.h>
+#include <mutex>
 
 #include "kernels.h"
 #include "array_topk.cuh"
@@ -293,7 +294,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (long long blk = (L_row + bs - 1) / bs + tid; blk < p.n_blocks; blk += kDecThreads)
           p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
     }
-    if (do_topk && live) {
+    if (do_topk && p.cluster_merge) {
+      // The row's segments form a thread-block cluster (rank = segment): the histogram
+      // levels are summed over the cluster, so the blocks select the row's top-K together and
+      // each writes its share of the row's indices at its offset; no lists leave the chip.
+      // Every block takes part in every cluster step, also after a timeout (then with no
+      // entries: the status reports the timeout).
+      const uint32_t rank = cluster_rank();
+      const int n_here = live ? seg_len : 0;
+      arr_threshold_impl(sel, keys, n_here, p.K, true, ClusterPick<kDecThreads / 32>{rank, (uint32_t)n_seg});
+      int base = 0, total = 0;
+      const int kept = arr_compact_cluster(sel, n_here, sel_idx, rank, (uint32_t)n_seg, &base, &total);
+      int32_t* out = p.idx + (size_t)row * p.K;
+      for (int r = tid; r < kept; r += kDecThreads)
+        if (base + r < p.K) out[base + r] = (int32_t)(e0 + sel_idx[r]);
+      if (rank == (uint32_t)n_seg - 1)
+        for (int r = total + tid; r < p.K; r += kDecThreads) out[r] = -1;
+      cluster_sync();  // no block leaves while another may still read its shared memory
+    } else if (do_topk && live) {
       arr_threshold(sel, keys, seg_len, p.K, true);
       const int kept = arr_compact(sel, seg_len, sel_idx);
       if (n_seg == 1) {
@@ -609,6 +627,59 @@ bool mma_indexer_available() { return encode_fn() != nullptr; }
 int mma_decode_max_seg_blocks() { return 2048; }
 
 int mma_decode_max_segment() { return kDecSegMax; }
+// The segments of a row can run as one thread-block cluster (2..16 blocks, every cluster of
+// the grid resident at once).
+bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks);
+
+bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks) {
+  if (n_seg < 2 || n_seg > 16 || K > CSA2_MAX_TOPK) return false;
+  // the answer depends on the device and the launch shape only: remembered per shape
+  struct Entry {
+    int dev, n_seg, n_rows, smem_key;
+    bool ok;
+  };
+  static Entry cache[32];
+  static int n_cache = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const int smem_key = (int)dec_smem_bytes(K, max_seg_blocks);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].dev == dev && cache[i].n_seg == n_seg && cache[i].n_rows == n_rows && cache[i].smem_key == smem_key)
+      return cache[i].ok;
+  const bool ok = cluster_ok_query(n_seg, n_rows, K, max_seg_blocks);
+  cache[n_cache % 32] = Entry{dev, n_seg, n_rows, smem_key, ok};
+  if (n_cache < 32) ++n_cache;
+  return ok;
+}
+
+bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks) {
+  const size_t smem = dec_smem_bytes(K, max_seg_blocks);
+  if (cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return false;
+  if (n_seg > 8 &&
+      cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_seg, n_rows);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)n_seg;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, idx_mma_decode_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters >= n_rows;
+}
+
 bool mma_decode_can_merge(int n_seg, int K) { return n_seg <= 64 && (long long)n_seg * K <= kDecSegMax; }
 
 size_t mma_decode_smem_bytes(int K, int max_seg_blocks) { return dec_smem_bytes(K, max_seg_blocks); }
@@ -640,6 +711,20 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaLaunchAttribute attr2[2] = {attr[0], {}};
+  if (p.cluster_merge) {
+    // the segments of a row form one cluster
+    attr2[1].id = cudaLaunchAttributeClusterDimension;
+    attr2[1].val.clusterDim.x = (unsigned)n_seg;
+    attr2[1].val.clusterDim.y = 1;
+    attr2[1].val.clusterDim.z = 1;
+    cfg.attrs = attr2;
+    cfg.numAttrs = 2;
+    if (n_seg > 8) {
+      e = cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+  }
   e = cudaLaunchKernelEx(&cfg, idx_mma_decode_kernel, tmK, tmQ, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

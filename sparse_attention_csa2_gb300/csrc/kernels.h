@@ -36,6 +36,8 @@ struct ScanParams {
   unsigned long long* row_done;  // tcgen05 decode: [n_rows] (call tag << 32 | finished segments);
                                  // the last segment of a row to finish merges the row's lists
   uint32_t call_tag;             // differs between consecutive calls (no clearing of row_done)
+  int cluster_merge;             // tcgen05 decode: the segments of a row form a cluster and
+                                 // select the row's top-K together (no lists, no merge)
   int32_t* dev_status;        // optional: CSA2_ETIMEOUT when a bounded wait gives up
   int pdl_trigger;            // set by the launcher: the grid is one wave, so a kernel launched
                               // after it with programmatic dependent launch may start early
@@ -47,7 +49,8 @@ size_t scan_smem_bytes(bool fp8, int K);
 bool mma_indexer_available();
 int mma_decode_max_seg_blocks();
 int mma_decode_max_segment();  // most records one decode segment may hold
-bool mma_decode_can_merge(int n_seg, int K);  // the decode scan can merge its segments' lists itself
+bool mma_decode_can_merge(int n_seg, int K);
+bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks);  // segments of a row as a cluster  // the decode scan can merge its segments' lists itself
 cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
                               cudaStream_t stream);
 cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream);
