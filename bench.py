@@ -49,6 +49,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the tiny / hierarchical / long-context lines")
+    ap.add_argument("--only-config", choices=["tiny_decode", "hierarchical", "long_decode"],
+                    help="time only this decode workload (profiling)")
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
     ap.add_argument("--prefill-t", type=int, default=4096, help="queries of the prefill chunk (profiling)")
@@ -241,6 +244,79 @@ def prefill_flops(wl) -> float:
     return 2.0 * wl.HI * wl.DI * visible
 
 
+def decode_group(dv, K):
+    """DecodeLayer objects for every layer of a device bundle (FULL, or FULL_POOL -> REINDEX
+    -> REUSE), each reading the preceding layer's pool / selection."""
+    import sparse_attention_csa2_gb300 as S
+    p, rw, c = dv["params"], dv["rows"], dv["cache"]
+    layers, prev = [], None
+    for lay in dv["layers"]:
+        kw = dict(seq_of_row=rw["seq_of_row"], n_visible=rw["n_visible"], q=lay["q"], q_pos=rw["q_pos"],
+                  latents=c["lat"], lat_scale=c["lat_scales"], swa=lay["swa"], swa_scale=lay["swa_scale"],
+                  swa_pos0=rw["swa_pos0"], window=p["W"], sink=lay["sink"], K=K, theta=p["theta"],
+                  softmax_scale=p["softmax_scale"], block_size=p["block_size"], n_keep=p["n_keep"])
+        if lay["mode"] != "reuse":
+            kw.update(q_idx=lay["q_idx"], w=lay["w"], k_idx=c["k_idx"], k_scale=c["k_scale"])
+        if lay["mode"] == "reindex":
+            kw.update(pool=prev.pool, n_pool=prev.n_pool)
+        if lay["mode"] == "reuse":
+            kw.update(idx=prev.idx, pool=prev.pool, n_pool=prev.n_pool)
+        prev = S.DecodeLayer(lay["mode"], **kw)
+        layers.append(prev)
+    return layers
+
+
+def group_bytes(wl) -> float:
+    """Algorithmic bytes of one decode step of a layer group (all rows): indexer keys of the
+    full scan, the pool's keys for every Reindex layer, and per layer the selected latents,
+    the window rows, q, q^I (scoring layers) and the fp32 output."""
+    key_rec = wl.DI + 4 if wl.key_fmt == "fp8" else wl.DI * 2
+    lat_rec = wl.D // 2 + wl.D // wl.lat_group if wl.lat_fmt == "fp4" else wl.D * 2
+    swa_row = wl.D + 4 if wl.swa_fmt == "fp8" else wl.D * 2
+    per_q = wl.N * key_rec
+    n_layers = 1
+    if wl.hierarchical:
+        n_layers = 1 + wl.n_reindex + wl.n_reuse
+        per_q += wl.n_reindex * wl.n_keep * wl.block_size * key_rec
+    per_layer = wl.K * lat_rec + wl.W * swa_row + wl.H * wl.D * 2 + wl.H * wl.D * 4
+    n_scoring = 1 + (wl.n_reindex if wl.hierarchical else 0)
+    per_q += n_layers * per_layer + n_scoring * (wl.HI * wl.DI * 2 + wl.HI * 4)
+    return float(wl.Bq * per_q)
+
+
+def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "long_decode")):
+    """The other decode workloads, each timed as back-to-back group steps with CUDA events
+    after 3 warm-up steps: tiny decode (latency), hierarchical group (6 layers), long-context
+    decode (FP8 keys, FP4 latents, FP8 window)."""
+    import torch
+    import synth
+    hbm = float(peaks.get("hbm_gbs", 6800.0)) if peaks else 6800.0
+    out = {}
+    for name in names:
+        wl = synth.WORKLOADS[name]
+        dv = synth.to_device(synth.make_inputs(wl, seed=11), f"cuda:{local}")
+        layers = decode_group(dv, dv["params"]["K"])
+        step = lambda: [l() for l in layers]
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        nbytes = group_bytes(wl)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"B": wl.B, "N": wl.N, "layers": len(layers), "ms_per_step": ms,
+                     "queries_per_s": wl.Bq / (ms / 1e3), "algorithmic_bytes": nbytes, "gbs": gbs,
+                     "hbm_frac": gbs / hbm, "launches_per_step": sum(l.launches for l in layers)}
+        del layers, dv
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill(args, local, peaks):
     """Prefill chunk (B=1, T=4096 queries at positions 32768.., N=36864 bf16 keys): the
     indexer GEMM on the tensor cores alone, then the whole chunk (scores -> per-query top-512
@@ -301,6 +377,14 @@ def run_gb300(args, world, rank, local):
     import sparse_attention_csa2_gb300 as S
 
     torch.cuda.set_device(local)
+    if args.only_config:
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except (OSError, ValueError):
+            peaks = None
+        print(json.dumps({"configs": run_configs(local, peaks, steps=args.steps, names=(args.only_config,))}),
+              flush=True)
+        return 0
     if args.prefill_only:
         try:
             peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -414,10 +498,14 @@ def run_gb300(args, world, rank, local):
                 "source_hash": src_hash}
 
     prefill = None
-    if not args.no_prefill:
+    configs = None
+    if not (args.no_prefill and args.no_configs):
         del layer, dv
         torch.cuda.empty_cache()
+    if not args.no_prefill:
         prefill = run_prefill(args, local, peaks if peak_src == "measured" else None)
+    if not args.no_configs:
+        configs = run_configs(local, peaks if peak_src == "measured" else None)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -440,7 +528,7 @@ def run_gb300(args, world, rank, local):
                       "step_algorithmic_bytes": step_bytes_q * wl.B,
                       "stage_ms": {"scan": statistics.mean(scan_ms), "topk_merge": statistics.mean(topk_ms),
                                    "attention": statistics.mean(attn_ms)},
-                      "launches_per_step": launches_per_step, "prefill": prefill}}
+                      "launches_per_step": launches_per_step, "prefill": prefill, "configs": configs}}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -1,0 +1,110 @@
+"""Parity at the workloads' full sizes, in the launch configuration the benchmark times.
+
+Every layer runs through the library on the whole batch (csa2_fused_decode for the decode
+workloads; index scores -> top-K -> sparse attention for the prefill chunk); the oracle then
+recomputes sampled rows one by one.  Grid-mode inputs (integer keys and queries, weights in
+sixteenths) make every fp32 score exact, so the indices must be bit-identical; Gaussian
+inputs check the indices up to swaps between near-tied scores at the K-boundary and the
+outputs against the oracle's attention over the GPU's own selection (so that a near-tie swap,
+allowed, does not mask an attention error).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from csa2_testlib import check_idx_near_ties, gpu_group, out_tol, rel_err, score_bound
+
+pytestmark = pytest.mark.gpu
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def _decode_case(name: str, mode: str, seed: int, rows: list[int]):
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl, seed=seed, mode=mode)
+    g = gpu_group(synth.to_device(inp))
+    return inp, g
+
+
+def _check_layers(inp, g, rows, mode, exact_layers):
+    """Indices of the scoring layers, then outputs, for the sampled rows."""
+    ref, prev = [], None
+    for l in range(len(inp["layers"])):
+        prev = O.csa2_layer(inp, l, prev, rows)
+        ref.append(prev)
+    for l, r in enumerate(ref):
+        gi = g[l].idx.cpu().numpy()[rows]
+        if mode == "grid" or l not in exact_layers:
+            if mode == "grid":
+                assert np.array_equal(gi, r["idx"]), l
+        else:
+            swaps = check_idx_near_ties(gi, r["idx"], r["scores"], score_bound(inp, l, rows))
+            print(f"layer {l}: {swaps} near-tie swaps at the K-boundary")
+        # outputs against the oracle's attention over the GPU's own selection
+        o_ref, _ = O.sparse_attn_rows(inp, l, gi.astype(np.int64), rows)
+        got = g[l].out.cpu().numpy()[rows]
+        assert rel_err(got, o_ref) <= out_tol(inp["params"]), l
+        if mode == "grid":
+            assert rel_err(got, r["o"]) <= out_tol(inp["params"]), l
+
+
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_batched_decode_full_size(mode):
+    """B=32 sequences x N=65,536 bf16 records, top-512, window 128: the benchmark's step."""
+    _cuda()
+    rows = [0, 13, 31]
+    inp, g = _decode_case("batched_decode", mode, seed=2, rows=rows)
+    _check_layers(inp, g, rows, mode, exact_layers={0})
+
+
+def test_hierarchical_full_size_grid():
+    """B=8 x N=131,072: FULL_POOL (blocks of 64, keep 64), three Reindex, two Reuse layers."""
+    _cuda()
+    rows = [0, 5, 7]
+    inp, g = _decode_case("hierarchical", "grid", seed=3, rows=rows)
+    ref0 = O.csa2_layer(inp, 0, None, rows)
+    assert np.array_equal(g[0].n_pool.cpu().numpy()[rows], ref0["n_pool"])
+    assert np.array_equal(g[0].pool.cpu().numpy()[rows], ref0["pool"])
+    _check_layers(inp, g, rows, "grid", exact_layers=set())
+    assert np.array_equal(g[4].idx.cpu().numpy(), g[3].idx.cpu().numpy())
+
+
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_long_context_full_size(mode):
+    """B=4 x N=1,048,576: FP8 indexer keys with row scales, FP4-E2M1 latents (E4M3 per 32),
+    FP8 window rows with row scales."""
+    _cuda()
+    rows = [0, 3]
+    inp, g = _decode_case("long_decode", mode, seed=5, rows=rows)
+    _check_layers(inp, g, rows, mode, exact_layers={0})
+
+
+def test_prefill_chunk_full_size():
+    """T=4,096 queries at positions 32,768.. over N=36,864 records: 256 sampled query rows
+    including the first and the last, indices (Gaussian: near-ties only) and outputs."""
+    _cuda()
+    import sparse_attention_csa2_gb300 as S
+    wl = synth.WORKLOADS["prefill_chunk"]
+    inp = synth.make_inputs(wl, seed=4)
+    dv = synth.to_device(inp)
+    p, rw, c, lay = dv["params"], dv["rows"], dv["cache"], dv["layers"][0]
+    sc = S.index_scores(lay["q_idx"], lay["w"], c["k_idx"], c["k_scale"], rw["seq_of_row"], rw["n_visible"])
+    idx = S.topk(sc, rw["n_visible"], p["K"])
+    out, _ = S.sparse_attn(lay["q"], rw["q_pos"], rw["seq_of_row"], c["lat"], c["lat_scales"], idx, lay["swa"],
+                        lay["swa_scale"], rw["swa_pos0"], p["W"], lay["sink"], p["theta"], p["softmax_scale"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    rows = sorted({0, wl.T - 1} | set(int(x) for x in rng.choice(wl.T, 254, replace=False)))
+    ref = O.csa2_layer(inp, 0, None, rows)
+    gi = idx.cpu().numpy()[rows]
+    swaps = check_idx_near_ties(gi, ref["idx"], ref["scores"], score_bound(inp, 0, rows))
+    print(f"prefill: {swaps} near-tie swaps over {len(rows)} rows")
+    o_ref, _ = O.sparse_attn_rows(inp, 0, gi.astype(np.int64), rows)
+    assert rel_err(out.cpu().numpy()[rows], o_ref) <= out_tol(inp["params"])
