@@ -41,14 +41,15 @@ int env_int(const char* name, int dflt) {
 }
 
 // Segments per row of the indexer scan: one resident block per SM, one wave; every segment
-// keeps at least 4096 records so the per-segment top-K and pipeline start-up stay small.
-int scan_segments(int n_rows, long long L) {
+// keeps at least min_seg records (4096 for full scans) so the per-segment top-K and pipeline
+// start-up stay small.
+int scan_segments(int n_rows, long long L, long long min_seg = 4096) {
   const int forced = env_int("CSA2_SCAN_SEGMENTS", 0);
   if (forced > 0) return forced;
   const int slots = sm_count();
   if (n_rows >= slots) return 1;
   long long s = slots / (n_rows > 0 ? n_rows : 1);
-  const long long cap = L / 4096;
+  const long long cap = L / min_seg;
   if (s > cap) s = cap;
   if (s > 64) s = 64;
   return s < 1 ? 1 : (int)s;
@@ -412,8 +413,8 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     ic.block_max = nullptr;
     if (scan_path(&ic, true) == ScanPath::kTc05Decode)
       n_seg = tc05_segments(n_rows, L, a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128);
-    else
-      n_seg = scan_segments(n_rows, L);
+    else  // candidate lists (Reindex) are short: smaller segments keep enough blocks busy
+      n_seg = scan_segments(n_rows, L, a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
     ws += lists_bytes(n_rows, n_seg, a->K);
     if (n_seg > 1) ws += align_up((size_t)n_rows * 8);  // per-row completion counters
     if (a->mode == CSA2_MODE_FULL_POOL) {
