@@ -69,16 +69,19 @@ csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA
 // keys and candidate lists (Reindex over a pool) take the warp-MMA scan.
 enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill };
 
-ScanPath scan_path(const csa2_index_args* a, bool want_topk) {
-  if (a->k_dtype != CSA2_BF16 || a->cand != nullptr || !mma_indexer_available()) return ScanPath::kWarpMma;
+// cand_run: the candidates come in runs of that many consecutive records (a Reindex pool of
+// whole blocks); runs of a multiple of 64 let the tcgen05 scan load them with TMA.
+ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0) {
+  if (a->k_dtype != CSA2_BF16 || !mma_indexer_available()) return ScanPath::kWarpMma;
+  if (a->cand != nullptr && !(want_topk && cand_run > 0 && cand_run % 64 == 0)) return ScanPath::kWarpMma;
   if (!want_topk && a->block_max == nullptr && a->n_seq == 1 && a->n_rows >= 64) return ScanPath::kTc05Prefill;
   return ScanPath::kTc05Decode;
 }
 
 // Segments per row for the tcgen05 decode scan: whole waves of resident blocks, each
 // segment's blocks (for the block maxima) within the kernel's shared-memory table.
-int tc05_segments(int n_rows, long long L, int unit) {
-  int n = scan_segments(n_rows, L);
+int tc05_segments(int n_rows, long long L, int unit, long long min_seg = 4096) {
+  int n = scan_segments(n_rows, L, min_seg);
   const long long units = (L + unit - 1) / unit;
   const int max_blocks = mma_decode_max_seg_blocks();
   const long long max_units = mma_decode_max_segment() / unit;  // a segment's keys fit in shared memory
@@ -87,7 +90,7 @@ int tc05_segments(int n_rows, long long L, int unit) {
 }
 
 cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk, int n_seg, cudaStream_t s) {
-  switch (scan_path(a, want_topk)) {
+  switch (scan_path(a, want_topk, p.cand_run)) {
     case ScanPath::kTc05Prefill: {
       // work items: (8-query tile, share of its key tiles); enough items to balance the
       // persistent grid, none shorter than ~16 key tiles
@@ -99,7 +102,11 @@ cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk,
       return launch_mma_prefill(p, ctas, parts, s);
     }
     case ScanPath::kTc05Decode: {
-      const int seg_blocks = p.block_max ? (int)(((a->n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg) : 0;
+      // shared-memory table per segment: block maxima, or the candidates' 64-slot run starts
+      const int seg_blocks =
+          p.block_max ? (int)(((a->n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg)
+          : p.cand   ? (int)(2 * (((a->L + p.unit - 1) / p.unit + n_seg - 1) / n_seg))
+                     : 0;
       return launch_mma_decode(p, (long long)a->n_seq * a->n_records, n_seg, seg_blocks, s);
     }
     default:
@@ -411,8 +418,10 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     csa2_index_args ic = *ix;
     ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
     ic.block_max = nullptr;
-    if (scan_path(&ic, true) == ScanPath::kTc05Decode)
-      n_seg = tc05_segments(n_rows, L, a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128);
+    const int cand_run = a->mode == CSA2_MODE_REINDEX ? a->block_size : 0;
+    if (scan_path(&ic, true, cand_run) == ScanPath::kTc05Decode)
+      n_seg = tc05_segments(n_rows, L, a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128,
+                            a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
     else  // candidate lists (Reindex) are short: smaller segments keep enough blocks busy
       n_seg = scan_segments(n_rows, L, a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
     ws += lists_bytes(n_rows, n_seg, a->K);
@@ -494,13 +503,16 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       p.cand = a->pool;
       p.n_cand = a->n_pool;
       p.cand_stride = a->pool_len;
+      p.cand_run = a->block_size;
       ic.cand = a->pool;
       ic.L = a->pool_len;
     }
-    const bool tc05 = scan_path(&ic, true) == ScanPath::kTc05Decode;
+    const bool tc05 = scan_path(&ic, true, p.cand_run) == ScanPath::kTc05Decode;
     if (tc05 && a->mode != CSA2_MODE_FULL_POOL) p.unit = 128;
     p.dev_status = at.dev_status;
-    const int seg_blocks = p.block_max ? (int)(((ic.n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg) : 0;
+    const int seg_blocks = p.block_max ? (int)(((ic.n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg)
+                           : p.cand   ? (int)(2 * (((ic.L + p.unit - 1) / p.unit + n_seg - 1) / n_seg))
+                                      : 0;
     p.cluster_merge = tc05 && env_int("CSA2_SCAN_CLUSTER", 1) != 0 && mma_decode_cluster_ok(n_seg, n_rows, a->K, seg_blocks);
     const bool fused_merge = tc05 && !p.cluster_merge && mma_decode_can_merge(n_seg, a->K);
     if (n_seg > 1) {
@@ -557,10 +569,13 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
     csa2_index_args ic = a->index;
     ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
     ic.block_max = nullptr;
-    const bool tc05 = scan_path(&ic, true) == ScanPath::kTc05Decode;
+    if (a->mode == CSA2_MODE_REINDEX) ic.L = a->pool_len;
+    const bool tc05 = scan_path(&ic, true, a->mode == CSA2_MODE_REINDEX ? a->block_size : 0) == ScanPath::kTc05Decode;
     const int unit = a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128;
     const int seg_blocks =
-        a->mode == CSA2_MODE_FULL_POOL ? (int)(((ic.n_records + unit - 1) / unit + n_seg - 1) / n_seg) : 0;
+        a->mode == CSA2_MODE_FULL_POOL ? (int)(((ic.n_records + unit - 1) / unit + n_seg - 1) / n_seg)
+        : a->mode == CSA2_MODE_REINDEX ? (int)(2 * (((ic.L + unit - 1) / unit + n_seg - 1) / n_seg))
+                                       : 0;
     const bool merged = tc05 && ((env_int("CSA2_SCAN_CLUSTER", 1) != 0 &&
                                   mma_decode_cluster_ok(n_seg, a->attn.n_rows, a->K, seg_blocks)) ||
                                  mma_decode_can_merge(n_seg, a->K));

@@ -117,7 +117,7 @@ __device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const Sca
 
 __global__ void __launch_bounds__(kDecThreads, 1)
     idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
-                          const ScanParams p) {
+                          const __grid_constant__ CUtensorMap tmK64, const ScanParams p) {
   // launched with programmatic dependent launch: wait for the previous kernel in the stream
   // before reading any input
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -131,11 +131,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   ArrSelShared* selsh = reinterpret_cast<ArrSelShared*>(rest);
   uint32_t* keys = reinterpret_cast<uint32_t*>(selsh + 1);  // [kDecSegMax] keys in record order
   uint32_t* bkeys = keys + kDecSegMax;                      // block maxima of the segment (keys)
+  // candidate mode: the record position where each 64-slot run of the segment starts
+  int32_t* hstart = reinterpret_cast<int32_t*>(bkeys);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
   const int b = p.seq_of_row[row];
-  const long long L_row = min((long long)p.n_visible[row], p.N);
+  // Candidate mode (Reindex over a block pool): the row's records are its candidate slots,
+  // ascending positions in runs of cand_run consecutive records; every 64-slot half of a tile
+  // is one contiguous run, loaded by its own 64-row TMA box.
+  const bool cmode = p.cand != nullptr;
+  const long long L_row = cmode ? (long long)p.n_cand[row] : min((long long)p.n_visible[row], p.N);
   const int U = p.unit;
   const long long n_units = (L_row + U - 1) / U;
   long long u0, u1;
@@ -167,6 +173,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, kDecTmemCols);
   for (int i = tid; i < seg_blocks; i += kDecThreads) bkeys[i] = 0u;
+  if (cmode)
+    for (int i = tid; i < (seg_len + 63) / 64; i += kDecThreads)
+      hstart[i] = p.cand[(size_t)row * p.cand_stride + e0 + 64 * i];
   if (do_topk) sel.zero_hist(kHistBins);
   tc05::fence_before();
   __syncthreads();
@@ -189,10 +198,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           report_timeout(&bars.timeout, p.dev_status);
           break;
         }
-        tc05::mbar_expect_tx(&bars.full[s], kKeyTile);
         uint8_t* dst = ring + s * kKeyTile;
-        tc05::tma_load_2d(dst, &tmK, 0, y0 + t * kTileKeys, &bars.full[s]);
-        tc05::tma_load_2d(dst + kKeyHalf, &tmK, 64, y0 + t * kTileKeys, &bars.full[s]);
+        if (cmode) {
+          // one or two 64-slot runs (rows 0..63 and 64..127 of the tile's swizzled halves)
+          const int halves = min(2, (seg_len - t * kTileKeys + 63) / 64);
+          tc05::mbar_expect_tx(&bars.full[s], (uint32_t)halves * (kKeyTile / 2));
+          for (int h = 0; h < halves; ++h) {
+            const int y = (int)((long long)b * p.N + hstart[2 * t + h]);
+            tc05::tma_load_2d(dst + h * (kKeyHalf / 2), &tmK64, 0, y, &bars.full[s]);
+            tc05::tma_load_2d(dst + kKeyHalf + h * (kKeyHalf / 2), &tmK64, 64, y, &bars.full[s]);
+          }
+        } else {
+          tc05::mbar_expect_tx(&bars.full[s], kKeyTile);
+          tc05::tma_load_2d(dst, &tmK, 0, y0 + t * kTileKeys, &bars.full[s]);
+          tc05::tma_load_2d(dst + kKeyHalf, &tmK, 64, y0 + t * kTileKeys, &bars.full[s]);
+        }
         bars.issued = t + 1;
       }
     }
@@ -283,6 +303,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                   "selection lists fit in the scratch");
     sel.scratch = reinterpret_cast<uint32_t*>(ring);
     int32_t* sel_idx = reinterpret_cast<int32_t*>(ring) + kListRoom;
+    // record position of the segment's entry i
+    auto pos_of = [&](int i) -> int32_t { return cmode ? hstart[i >> 6] + (i & 63) : (int32_t)(e0 + i); };
     const bool live = !bars.timeout;
     for (int i = tid; i < seg_blocks; i += kDecThreads)
       p.block_max[(size_t)row * p.bmax_stride + e0 / bs + i] = bkeys[i] ? key_score(bkeys[i]) : -INFINITY;
@@ -307,7 +329,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int kept = arr_compact_cluster(sel, n_here, sel_idx, rank, (uint32_t)n_seg, &base, &total);
       int32_t* out = p.idx + (size_t)row * p.K;
       for (int r = tid; r < kept; r += kDecThreads)
-        if (base + r < p.K) out[base + r] = (int32_t)(e0 + sel_idx[r]);
+        if (base + r < p.K) out[base + r] = pos_of(sel_idx[r]);
       if (rank == (uint32_t)n_seg - 1)
         for (int r = total + tid; r < p.K; r += kDecThreads) out[r] = -1;
       cluster_sync();  // no block leaves while another may still read its shared memory
@@ -316,12 +338,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int kept = arr_compact(sel, seg_len, sel_idx);
       if (n_seg == 1) {
         int32_t* out = p.idx + (size_t)row * p.K;
-        for (int r = tid; r < p.K; r += kDecThreads) out[r] = r < kept ? (int32_t)(e0 + sel_idx[r]) : -1;
+        for (int r = tid; r < p.K; r += kDecThreads) out[r] = r < kept ? pos_of(sel_idx[r]) : -1;
       } else {
         const size_t o = ((size_t)row * n_seg + seg) * p.K;
         for (int r = tid; r < kept; r += kDecThreads) {
           p.seg_keys[o + r] = keys[sel_idx[r]];
-          p.seg_pos[o + r] = (int32_t)(e0 + sel_idx[r]);
+          p.seg_pos[o + r] = pos_of(sel_idx[r]);
         }
         if (tid == 0) {
           p.seg_cnt[(size_t)row * n_seg + seg] = kept;
@@ -688,10 +710,12 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
                               cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
   if (dec_smem_bytes(p.K, max_seg_blocks) > 232448) return cudaErrorInvalidValue;
-  CUtensorMap tmK, tmQ;
+  CUtensorMap tmK, tmQ, tmK64;
   if (!make_tmap(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys) ||
-      !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, 32))
+      !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, 32) ||
+      !make_tmap(&tmK64, p.k_idx, (unsigned long long)n_seq_rows, 64))
     return cudaErrorInvalidValue;
+  if (p.cand != nullptr && (p.cand_run <= 0 || p.cand_run % 64 != 0)) return cudaErrorInvalidValue;
   const size_t smem = dec_smem_bytes(p.K, max_seg_blocks);
   cudaError_t e = cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -725,7 +749,7 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
       if (e != cudaSuccess) return e;
     }
   }
-  e = cudaLaunchKernelEx(&cfg, idx_mma_decode_kernel, tmK, tmQ, q);
+  e = cudaLaunchKernelEx(&cfg, idx_mma_decode_kernel, tmK, tmQ, tmK64, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

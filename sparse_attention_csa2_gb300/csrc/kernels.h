@@ -19,6 +19,8 @@ struct ScanParams {
   const int32_t* cand;        // gather mode: [n_rows, cand_stride]
   const int32_t* n_cand;
   long long cand_stride;
+  int cand_run;               // tcgen05 decode over candidates: they come in runs of cand_run
+                              // consecutive positions (a multiple of 64) from the pool's blocks
   int n_rows;
   int unit;                   // entries per scheduling unit (16, or block_size with block_max)
   float* scores;              // optional [n_rows, scores_stride]
