@@ -82,16 +82,17 @@ __device__ __forceinline__ uint64_t sw128_desc_lbo(uint32_t saddr, uint32_t lbo,
   return d;
 }
 
-__device__ __forceinline__ float e2m1_level(uint32_t nib) {
-  // magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign
-  const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
-  const float mag = e == 0 ? 0.5f * (float)m : (1.0f + 0.5f * (float)m) * (float)(1u << (e - 1));
-  return (nib & 8u) ? -mag : mag;
+// Two E4M3 codes (low byte first) -> two floats, exact (every E4M3 value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
+  uint32_t h;
+  asm("{\n .reg .b32 t;\n cvt.rn.f16x2.e4m3x2 t, %1;\n mov.b32 %0, t;\n}\n" : "=r"(h) : "h"(v));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
-__device__ __forceinline__ float e4m3_value(uint32_t code) {
-  const uint32_t e = (code >> 3) & 15u, m = code & 7u;
-  const float mag = e == 0 ? (float)m * 0.001953125f /* 2^-9 */ : ldexpf(1.0f + 0.125f * (float)m, (int)e - 7);
-  return (code & 0x80u) ? -mag : mag;
+// Two E2M1 codes in one byte (low nibble first) -> two floats, exact.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n" : "=r"(h) : "r"(byte));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
 // cos and sin of the rotary angle sign * pos * inv_freq.  The angle (up to ~2^31 rad) is
@@ -198,10 +199,27 @@ __device__ __forceinline__ void gather_tile(const TileSrc& m, uint8_t* ks, const
             make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]);
     }
   } else if (f == CSA2_FP4_E2M1_G32 || f == CSA2_FP4_E2M1_G16) {
-    const int gsz = f == CSA2_FP4_E2M1_G32 ? 32 : 16;
+    // This thread's 256 dims use 8 (groups of 32) or 16 (groups of 16) E4M3 scale bytes,
+    // loaded once; codes and scales are widened by the hardware conversions (E2M1 pair -> f16
+    // pair, E4M3 pair -> f16 pair, both exact) and each product level x scale (at most 6
+    // significant bits) is exact in bf16.
+    const bool g16 = f == CSA2_FP4_E2M1_G16;
+    uint4 sv;
+    if (g16) {
+      sv = __ldg(reinterpret_cast<const uint4*>(m.sptr[r] + half * 16));
+    } else {
+      const uint2 t2 = __ldg(reinterpret_cast<const uint2*>(m.sptr[r] + half * 8));
+      sv = make_uint4(t2.x, t2.y, 0u, 0u);
+    }
 #pragma unroll 1
     for (int g = 0; g < 4; ++g) {
       const int d0 = half * 256 + g * 64;
+      // the scales of dims d0 .. d0+63: four bytes (groups of 16) or two (groups of 32)
+      const uint32_t sw = g16 ? (g == 0 ? sv.x : g == 1 ? sv.y : g == 2 ? sv.z : sv.w)
+                              : ((g < 2 ? sv.x : sv.y) >> (16 * (g & 1))) & 0xffffu;
+      const float2 s01 = e4m3x2_to_f32x2((uint16_t)(sw & 0xffffu));
+      const float2 s23 = e4m3x2_to_f32x2((uint16_t)(sw >> 16));
+      const float sc[4] = {s01.x, s01.y, s23.x, s23.y};
       const uint4* src = reinterpret_cast<const uint4*>(m.ptr[r] + d0 / 2);
       uint32_t outw[32];
 #pragma unroll
@@ -212,10 +230,10 @@ __device__ __forceinline__ void gather_tile(const TileSrc& m, uint8_t* ks, const
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
           for (int byte = 0; byte < 4; ++byte) {
-            const int ch = d0 + h2 * 32 + k * 8 + byte * 2;  // even channel of this byte
-            const float sc = e4m3_value(__ldg(m.sptr[r] + ch / gsz));
-            const uint32_t code = (w4[k] >> (8 * byte)) & 0xffu;
-            outw[h2 * 16 + k * 4 + byte] = pack_bf16x2(e2m1_level(code & 15u) * sc, e2m1_level(code >> 4) * sc);
+            const int lc = h2 * 32 + k * 8 + byte * 2;  // even channel of this byte within the 64
+            const float s = sc[g16 ? lc / 16 : lc / 32];
+            const float2 lv = e2m1x2_to_f32x2((w4[k] >> (8 * byte)) & 0xffu);
+            outw[h2 * 16 + k * 4 + byte] = pack_bf16x2(lv.x * s, lv.y * s);
           }
         }
       }
