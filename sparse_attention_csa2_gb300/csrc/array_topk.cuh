@@ -136,6 +136,36 @@ struct LocalPick {
   __device__ __forceinline__ void run(const ArrSel<NW>& s, int need) const {
     s.template pick<NBINS>(need);
   }
+  // Levels 2 (bits 19..8) and 3 (bits 7..0) over the warp lists' keys in bin b1; sets
+  // sh->thr and sh->n_eq.
+  __device__ __forceinline__ void refine(const ArrSel<NW>& s, const uint32_t* lk, int n_list, uint32_t b1,
+                                         int need, uint32_t* local_keys) const {
+    (void)local_keys;
+    ArrSelShared& sh = *s.sh;
+    const int ln = s.lane();
+    s.zero_hist(kHistBins);
+    s.sync();
+#pragma unroll 1
+    for (int j = ln; j < n_list; j += 32)
+      if ((lk[j] >> 20) == b1) atomicAdd(&sh.hist[(lk[j] >> 8) & 0xfffu], 1);
+    s.sync();
+    s.template pick<kHistBins>(need);
+    const uint32_t hi24 = (b1 << 12) | (uint32_t)sh.bin;
+    need -= sh.before;
+    s.sync();
+    s.zero_hist(256);
+    s.sync();
+#pragma unroll 1
+    for (int j = ln; j < n_list; j += 32)
+      if ((lk[j] >> 8) == hi24) atomicAdd(&sh.hist[lk[j] & 0xffu], 1);
+    s.sync();
+    s.template pick<256>(need);
+    if (s.tid == 0) {
+      sh.thr = (hi24 << 8) | (uint32_t)sh.bin;
+      sh.n_eq = need - sh.before;
+    }
+    s.sync();
+  }
 };
 
 // The bin choice for the blocks of a thread-block cluster that select over the union of their
@@ -145,26 +175,31 @@ struct LocalPick {
 template <int NW>
 struct ClusterPick {
   uint32_t rank, n_cta;
+  int local_cap;  // capacity of block 0's key array (words) for the keys of bin b1
+  // Level 1: every block adds one slice of the bins over the cluster into block 0's
+  // histogram, block 0 picks and writes bin / before / total into every block.
   template <int NBINS>
   __device__ __forceinline__ void run(const ArrSel<NW>& s, int need) const {
     constexpr int NT = NW * 32;
     ArrSelShared& sh = *s.sh;
     cluster_sync();  // every block's histogram is final
-    if (rank == 0) {
+    const int n_v4 = NBINS / 4, per = (n_v4 + (int)n_cta - 1) / (int)n_cta;
+    const int lo = (int)rank * per, hi = min(n_v4, lo + per);
 #pragma unroll 1
-      for (int i = s.tid; i < NBINS / 4; i += NT) {
-        int4 acc = *reinterpret_cast<const int4*>(&sh.hist[4 * i]);
+    for (int i = lo + s.tid; i < hi; i += NT) {
+      uint4 acc = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 4
-        for (uint32_t c = 1; c < n_cta; ++c) {
-          const uint4 v = cluster_ld_v4(cluster_map(&sh.hist[4 * i], c));
-          acc.x += (int)v.x;
-          acc.y += (int)v.y;
-          acc.z += (int)v.z;
-          acc.w += (int)v.w;
-        }
-        *reinterpret_cast<int4*>(&sh.hist[4 * i]) = acc;
+      for (uint32_t c = 0; c < n_cta; ++c) {
+        const uint4 v = cluster_ld_v4(cluster_map(&sh.hist[4 * i], c));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
       }
-      s.sync();
+      cluster_st_v4(cluster_map(&sh.hist[4 * i], 0), acc);
+    }
+    cluster_sync();  // block 0 holds the cluster's histogram
+    if (rank == 0) {
       s.template pick<NBINS>(need);
       if (s.tid > 0 && (uint32_t)s.tid < n_cta) {
         cluster_st_s32(cluster_map(&sh.bin, s.tid), sh.bin);
@@ -173,6 +208,107 @@ struct ClusterPick {
       }
     }
     cluster_sync();  // the choice is visible in every block; the histograms may be reused
+  }
+  // Levels 2 and 3 by block 0 alone over every block's listed keys in bin b1 (few): warp w of
+  // block 0 gathers list w of every block through distributed shared memory (lane c first
+  // reads block c's list length and layout, then the lanes take the concatenated lists' entries
+  // in strides, all loads independent), keeps the keys in bin b1 in its own key array (free
+  // once its lists exist) and counts level 2; level 3 reads that local copy.  Each block has
+  // published its warps' list lengths (w_list) and its range per warp (aux[5]).
+  __device__ __forceinline__ void refine(const ArrSel<NW>& s, const uint32_t* lk, int n_list, uint32_t b1,
+                                         int need, uint32_t* local_keys) const {
+    (void)lk;
+    (void)n_list;
+    ArrSelShared& sh = *s.sh;
+    const int w = s.warp(), ln = s.lane();
+    cluster_sync();  // every block's lists are complete
+    if (rank == 0) {
+      int my_len = 0, my_per = 0;
+      if ((uint32_t)ln < n_cta) {
+        my_len = cluster_ld_s32(cluster_map(&sh.w_list[w], ln));
+        my_per = cluster_ld_s32(cluster_map(&sh.aux[5], ln));
+      }
+      int incl = my_len;  // inclusive prefix of the lists' lengths over the blocks
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (ln >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      s.zero_hist(kHistBins);
+      if (s.tid == 0) sh.aux[6] = 0u;  // keys kept in bin b1
+      s.sync();
+      const unsigned lt = lanemask_lt();
+#pragma unroll 1
+      for (int f0 = 0; f0 < total; f0 += 32) {
+        const int f = f0 + ln;
+        // the block holding entry f of the concatenation, and its index there
+        int c = 0, start = 0;
+#pragma unroll 1
+        for (int q = 0; q < (int)n_cta; ++q) {
+          const int end = __shfl_sync(0xffffffffu, incl, q);
+          if (f >= end) {
+            c = q + 1;
+            start = end;
+          }
+        }
+        uint32_t key = 0u;
+        const int per_c = __shfl_sync(0xffffffffu, my_per, min(c, (int)n_cta - 1));
+        if (f < total)
+          key = (uint32_t)cluster_ld_s32(cluster_map(s.scratch + (size_t)w * 2 * per_c + (f - start), (uint32_t)c));
+        const bool in = f < total && (key >> 20) == b1;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        int base = 0;
+        if (ln == 0 && m) base = (int)atomicAdd(&sh.aux[6], (uint32_t)__popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (in) {
+          const int slot = base + __popc(m & lt);
+          if (slot < local_cap) local_keys[slot] = key;
+          atomicAdd(&sh.hist[(key >> 8) & 0xfffu], 1);
+        }
+      }
+      s.sync();
+      s.template pick<kHistBins>(need);
+      const uint32_t hi24 = (b1 << 12) | (uint32_t)sh.bin;
+      const int need3 = need - sh.before;
+      const int n_b1 = (int)sh.aux[6];
+      s.sync();
+      s.zero_hist(256);
+      s.sync();
+      if (n_b1 <= local_cap) {
+#pragma unroll 1
+        for (int j = s.tid; j < n_b1; j += NW * 32)
+          if ((local_keys[j] >> 8) == hi24) atomicAdd(&sh.hist[local_keys[j] & 0xffu], 1);
+      } else {
+        // more keys in bin b1 than the local copy holds: read the blocks' lists again
+#pragma unroll 1
+        for (int f0 = 0; f0 < total; f0 += 32) {
+          const int f = f0 + ln;
+          int c = 0, start = 0;
+#pragma unroll 1
+          for (int q = 0; q < (int)n_cta; ++q) {
+            const int end = __shfl_sync(0xffffffffu, incl, q);
+            if (f >= end) {
+              c = q + 1;
+              start = end;
+            }
+          }
+          const int per_c = __shfl_sync(0xffffffffu, my_per, min(c, (int)n_cta - 1));
+          if (f < total) {
+            const uint32_t key =
+                (uint32_t)cluster_ld_s32(cluster_map(s.scratch + (size_t)w * 2 * per_c + (f - start), (uint32_t)c));
+            if ((key >> 8) == hi24) atomicAdd(&sh.hist[key & 0xffu], 1);
+          }
+        }
+      }
+      s.sync();
+      s.template pick<256>(need3);
+      if ((uint32_t)s.tid < n_cta) {
+        cluster_st_s32(cluster_map(&sh.thr, s.tid), (int)((hi24 << 8) | (uint32_t)sh.bin));
+        cluster_st_s32(cluster_map(&sh.n_eq, s.tid), need3 - sh.before);
+      }
+    }
+    cluster_sync();  // thr / n_eq are visible in every block
   }
 };
 
@@ -237,6 +373,7 @@ __device__ __noinline__ void arr_threshold_impl(const ArrSel<NW>& s, const uint3
     }
     if (ln == 0) sh.w_list[w] = n_list;
   }
+  if (s.tid == 0) sh.aux[5] = (uint32_t)per;  // the lists' layout, for a cluster's block 0
   if (all) {
     if (s.tid == 0) {
       sh.thr = 0u;
@@ -245,31 +382,8 @@ __device__ __noinline__ void arr_threshold_impl(const ArrSel<NW>& s, const uint3
     s.sync();
     return;
   }
-  s.zero_hist(kHistBins);
   s.sync();
-  // level 2: bits 19..8 of the listed keys in bin b1
-#pragma unroll 1
-  for (int j = ln; j < n_list; j += 32)
-    if ((lk[j] >> 20) == b1) atomicAdd(&sh.hist[(lk[j] >> 8) & 0xfffu], 1);
-  s.sync();
-  picker.template run<kHistBins>(s, need);
-  const uint32_t b2 = (uint32_t)sh.bin;
-  need -= sh.before;
-  // level 3: bits 7..0 of the listed keys matching b1, b2
-  const uint32_t hi24 = (b1 << 12) | b2;
-  s.sync();
-  s.zero_hist(256);
-  s.sync();
-#pragma unroll 1
-  for (int j = ln; j < n_list; j += 32)
-    if ((lk[j] >> 8) == hi24) atomicAdd(&sh.hist[lk[j] & 0xffu], 1);
-  s.sync();
-  picker.template run<256>(s, need);
-  if (s.tid == 0) {
-    sh.thr = (hi24 << 8) | (uint32_t)sh.bin;
-    sh.n_eq = need - sh.before;
-  }
-  s.sync();
+  picker.refine(s, lk, n_list, b1, need, const_cast<uint32_t*>(keys));
 }
 
 template <int NW>

@@ -196,6 +196,10 @@ __device__ __forceinline__ int cluster_ld_s32(uint32_t addr) {
   asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ void cluster_st_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ void cluster_st_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
 }

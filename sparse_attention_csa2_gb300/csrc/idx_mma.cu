@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // entries: the status reports the timeout).
       const uint32_t rank = cluster_rank();
       const int n_here = live ? seg_len : 0;
-      arr_threshold_impl(sel, keys, n_here, p.K, true, ClusterPick<kDecThreads / 32>{rank, (uint32_t)n_seg});
+      arr_threshold_impl(sel, keys, n_here, p.K, true, ClusterPick<kDecThreads / 32>{rank, (uint32_t)n_seg, kDecSegMax});
       int base = 0, total = 0;
       const int kept = arr_compact_cluster(sel, n_here, sel_idx, rank, (uint32_t)n_seg, &base, &total);
       int32_t* out = p.idx + (size_t)row * p.K;
