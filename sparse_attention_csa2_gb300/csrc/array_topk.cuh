@@ -211,9 +211,12 @@ struct ClusterPick {
   }
   // Levels 2 and 3 by block 0 alone over every block's listed keys in bin b1 (few): warp w of
   // block 0 gathers list w of every block through distributed shared memory (lane c first
-  // reads block c's list length and layout, then the lanes take the concatenated lists' entries
-  // in strides, all loads independent), keeps the keys in bin b1 in its own key array (free
-  // once its lists exist) and counts level 2; level 3 reads that local copy.  Each block has
+  // reads block c's list length and layout, then the lanes take the concatenated lists'
+  // entries in strides), keeps the keys in bin b1 with their block in its own key array (free
+  // once its lists exist) and counts level 2; level 3 reads that local copy.  Block 0 then
+  // knows, per block, how many of its entries lie above the threshold and how many equal it,
+  // and writes into every block its threshold, its number of tied entries to keep (n_eq), its
+  // row offset (aux[2]) and the row's number of selected entries (aux[4]).  Each block has
   // published its warps' list lengths (w_list) and its range per warp (aux[5]).
   __device__ __forceinline__ void refine(const ArrSel<NW>& s, const uint32_t* lk, int n_list, uint32_t b1,
                                          int need, uint32_t* local_keys) const {
@@ -221,6 +224,12 @@ struct ClusterPick {
     (void)n_list;
     ArrSelShared& sh = *s.sh;
     const int w = s.warp(), ln = s.lane();
+    uint32_t* cnt_all = sh.aux + 16;  // per block: listed entries
+    uint32_t* cnt_gt = sh.aux + 32;   // ... above the threshold (bins above b1 included later)
+    uint32_t* cnt_b1 = sh.aux + 48;   // ... in bin b1
+    uint32_t* cnt_eq = sh.aux + 64;   // ... equal to the threshold
+    const int cap = local_cap / 2;    // local copy: keys, then their blocks
+    uint32_t* local_src = local_keys + cap;
     cluster_sync();  // every block's lists are complete
     if (rank == 0) {
       int my_len = 0, my_per = 0;
@@ -236,14 +245,15 @@ struct ClusterPick {
       }
       const int total = __shfl_sync(0xffffffffu, incl, 31);
       s.zero_hist(kHistBins);
+      if (s.tid < 64) sh.aux[16 + s.tid] = 0u;
       if (s.tid == 0) sh.aux[6] = 0u;  // keys kept in bin b1
       s.sync();
+      if ((uint32_t)ln < n_cta) atomicAdd(&cnt_all[ln], (uint32_t)my_len);
       const unsigned lt = lanemask_lt();
-#pragma unroll 1
-      for (int f0 = 0; f0 < total; f0 += 32) {
-        const int f = f0 + ln;
-        // the block holding entry f of the concatenation, and its index there
-        int c = 0, start = 0;
+      // entry f of warp w's concatenated lists: its block and its key
+      auto entry = [&](int f, int& c) -> uint32_t {
+        int start = 0;
+        c = 0;
 #pragma unroll 1
         for (int q = 0; q < (int)n_cta; ++q) {
           const int end = __shfl_sync(0xffffffffu, incl, q);
@@ -252,10 +262,16 @@ struct ClusterPick {
             start = end;
           }
         }
-        uint32_t key = 0u;
         const int per_c = __shfl_sync(0xffffffffu, my_per, min(c, (int)n_cta - 1));
-        if (f < total)
-          key = (uint32_t)cluster_ld_s32(cluster_map(s.scratch + (size_t)w * 2 * per_c + (f - start), (uint32_t)c));
+        return f < total ? (uint32_t)cluster_ld_s32(
+                               cluster_map(s.scratch + (size_t)w * 2 * per_c + (f - start), (uint32_t)min(c, (int)n_cta - 1)))
+                         : 0u;
+      };
+#pragma unroll 1
+      for (int f0 = 0; f0 < total; f0 += 32) {
+        const int f = f0 + ln;
+        int c;
+        const uint32_t key = entry(f, c);
         const bool in = f < total && (key >> 20) == b1;
         const unsigned m = __ballot_sync(0xffffffffu, in);
         int base = 0;
@@ -263,8 +279,12 @@ struct ClusterPick {
         base = __shfl_sync(0xffffffffu, base, 0);
         if (in) {
           const int slot = base + __popc(m & lt);
-          if (slot < local_cap) local_keys[slot] = key;
+          if (slot < cap) {
+            local_keys[slot] = key;
+            local_src[slot] = (uint32_t)c;
+          }
           atomicAdd(&sh.hist[(key >> 8) & 0xfffu], 1);
+          atomicAdd(&cnt_b1[c], 1u);
         }
       }
       s.sync();
@@ -275,40 +295,70 @@ struct ClusterPick {
       s.sync();
       s.zero_hist(256);
       s.sync();
-      if (n_b1 <= local_cap) {
+      const bool local = n_b1 <= cap;
+      if (local) {
 #pragma unroll 1
         for (int j = s.tid; j < n_b1; j += NW * 32)
           if ((local_keys[j] >> 8) == hi24) atomicAdd(&sh.hist[local_keys[j] & 0xffu], 1);
-      } else {
-        // more keys in bin b1 than the local copy holds: read the blocks' lists again
+      } else {  // more keys in bin b1 than the local copy holds: read the blocks' lists again
 #pragma unroll 1
         for (int f0 = 0; f0 < total; f0 += 32) {
-          const int f = f0 + ln;
-          int c = 0, start = 0;
-#pragma unroll 1
-          for (int q = 0; q < (int)n_cta; ++q) {
-            const int end = __shfl_sync(0xffffffffu, incl, q);
-            if (f >= end) {
-              c = q + 1;
-              start = end;
-            }
-          }
-          const int per_c = __shfl_sync(0xffffffffu, my_per, min(c, (int)n_cta - 1));
-          if (f < total) {
-            const uint32_t key =
-                (uint32_t)cluster_ld_s32(cluster_map(s.scratch + (size_t)w * 2 * per_c + (f - start), (uint32_t)c));
-            if ((key >> 8) == hi24) atomicAdd(&sh.hist[key & 0xffu], 1);
-          }
+          int c;
+          const uint32_t key = entry(f0 + ln, c);
+          if (f0 + ln < total && (key >> 8) == hi24) atomicAdd(&sh.hist[key & 0xffu], 1);
         }
       }
       s.sync();
       s.template pick<256>(need3);
-      if ((uint32_t)s.tid < n_cta) {
-        cluster_st_s32(cluster_map(&sh.thr, s.tid), (int)((hi24 << 8) | (uint32_t)sh.bin));
-        cluster_st_s32(cluster_map(&sh.n_eq, s.tid), need3 - sh.before);
+      const uint32_t thr = (hi24 << 8) | (uint32_t)sh.bin;
+      const int n_eq_row = need3 - sh.before;
+      // per block: its keys of bin b1 above the threshold and equal to it
+      if (local) {
+#pragma unroll 1
+        for (int j = s.tid; j < n_b1; j += NW * 32) {
+          if (local_keys[j] > thr) atomicAdd(&cnt_gt[local_src[j]], 1u);
+          if (local_keys[j] == thr) atomicAdd(&cnt_eq[local_src[j]], 1u);
+        }
+      } else {
+#pragma unroll 1
+        for (int f0 = 0; f0 < total; f0 += 32) {
+          int c;
+          const uint32_t key = entry(f0 + ln, c);
+          if (f0 + ln < total && (key >> 20) == b1) {
+            if (key > thr) atomicAdd(&cnt_gt[c], 1u);
+            if (key == thr) atomicAdd(&cnt_eq[c], 1u);
+          }
+        }
+      }
+      s.sync();
+      if (w == 0) {
+        // offsets in block order: every listed entry above bin b1 is kept, then those of bin
+        // b1 above the threshold, then the first n_eq_row ties in block order
+        int g = 0, e = 0;
+        if ((uint32_t)ln < n_cta) {
+          g = (int)(cnt_all[ln] - cnt_b1[ln] + cnt_gt[ln]);
+          e = (int)cnt_eq[ln];
+        }
+        int gi = g, ei = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
+          if (ln >= o) {
+            gi += yg;
+            ei += ye;
+          }
+        }
+        const int gb = gi - g, eb = ei - e;
+        const int G = __shfl_sync(0xffffffffu, gi, 31), E = __shfl_sync(0xffffffffu, ei, 31);
+        if ((uint32_t)ln < n_cta) {
+          cluster_st_s32(cluster_map(&sh.thr, ln), (int)thr);
+          cluster_st_s32(cluster_map(&sh.n_eq, ln), max(0, min(e, n_eq_row - eb)));
+          cluster_st_s32(cluster_map(&sh.aux[2], ln), gb + min(eb, n_eq_row));
+          cluster_st_s32(cluster_map(&sh.aux[4], ln), G + min(E, n_eq_row));
+        }
       }
     }
-    cluster_sync();  // thr / n_eq are visible in every block
+    cluster_sync();  // thresholds and offsets are visible in every block
   }
 };
 

@@ -325,8 +325,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const uint32_t rank = cluster_rank();
       const int n_here = live ? seg_len : 0;
       arr_threshold_impl(sel, keys, n_here, p.K, true, ClusterPick<kDecThreads / 32>{rank, (uint32_t)n_seg, kDecSegMax});
-      int base = 0, total = 0;
-      const int kept = arr_compact_cluster(sel, n_here, sel_idx, rank, (uint32_t)n_seg, &base, &total);
+      int base = 0, total = 0, kept = 0;
+      if (selsh->thr == 0u) {
+        // at most K candidates in the row: every block keeps all its entries; offsets by
+        // exchanging the blocks' counts
+        kept = arr_compact_cluster(sel, n_here, sel_idx, rank, (uint32_t)n_seg, &base, &total);
+      } else {
+        // block 0 wrote this block's number of ties to keep, its offset and the row's total
+        base = (int)selsh->aux[2];
+        total = (int)selsh->aux[4];
+        kept = arr_compact(sel, n_here, sel_idx);
+      }
       int32_t* out = p.idx + (size_t)row * p.K;
       for (int r = tid; r < kept; r += kDecThreads)
         if (base + r < p.K) out[base + r] = pos_of(sel_idx[r]);
