@@ -307,11 +307,24 @@ def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "l
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
+        # stage breakdown per layer (a separate run: scan, top-K merge, attention)
+        n_st = 10
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers] for _ in range(n_st)]
+        for r in range(n_st):
+            for l, lay in zip(evs[r], layers):
+                lay.set_stage_events(l)
+            step()
+        torch.cuda.synchronize()
+        for lay in layers:
+            lay.set_stage_events([])
+        stage = [[statistics.mean(evs[r][i][k].elapsed_time(evs[r][i][k + 1]) for r in range(n_st)) for k in range(3)]
+                 for i in range(len(layers))]
         nbytes = group_bytes(wl)
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"B": wl.B, "N": wl.N, "layers": len(layers), "ms_per_step": ms,
                      "queries_per_s": wl.Bq / (ms / 1e3), "algorithmic_bytes": nbytes, "gbs": gbs,
-                     "hbm_frac": gbs / hbm, "launches_per_step": sum(l.launches for l in layers)}
+                     "hbm_frac": gbs / hbm, "launches_per_step": sum(l.launches for l in layers),
+                     "stage_ms_per_layer": {"scan_topk_merge_attn": stage}}
         del layers, dv
         torch.cuda.empty_cache()
     return out

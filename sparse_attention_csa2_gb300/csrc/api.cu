@@ -357,7 +357,7 @@ csa2_status csa2_topk(const csa2_topk_args* a, void* stream) {
   m.in_seg = t.n_seg;
   m.in_K = a->K;
   m.idx = a->idx;
-  return cuda_status(launch_topk_feed(m, true, 1, s));
+  return cuda_status(launch_lists_merge(m, s));
 }
 
 // ---------------------------------------------------------------------- block pool
@@ -536,7 +536,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       m.in_seg = n_seg;
       m.in_K = a->K;
       m.idx = a->idx;
-      e = launch_topk_feed(m, true, 1, s);
+      e = launch_lists_merge(m, s);
       if (e != cudaSuccess) return CSA2_ECUDA;
     }
     if (a->mode == CSA2_MODE_FULL_POOL) {

@@ -87,6 +87,7 @@ struct FeedParams {
 size_t feed_smem_bytes(int K);
 int topk_segments(int n_rows, long long L);  // segments csa2_topk splits each row into
 cudaError_t launch_topk_feed(const FeedParams& p, bool from_lists, int out_seg, cudaStream_t stream);
+cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream);  // segment lists -> final idx
 cudaError_t launch_pool_expand(const int32_t* kept, const int32_t* n_visible, int n_rows, int n_keep,
                                int block_size, int32_t* pool, int32_t* n_pool, cudaStream_t stream);
 

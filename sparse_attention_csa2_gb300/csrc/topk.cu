@@ -2,6 +2,7 @@
 // engine of select.cuh fed from global memory), and the expansion of kept blocks into the
 // hierarchical candidate pool ("DeepSeek-V4.1-Flash explained", section 3: a block is
 // scored by its best position and every position of a kept block enters the pool).
+#include "array_topk.cuh"
 #include "select.cuh"
 #include "kernels.h"
 
@@ -128,7 +129,148 @@ __global__ void pool_expand_kernel(const int32_t* __restrict__ kept, const int32
   }
 }
 
+// Merge of per-segment lists (source B) into a row's final top-K, one block per row.  The
+// row's list keys are staged once in shared memory (keys below the largest per-segment K-th key
+// zeroed: that segment alone holds K entries at or above it), then histogram passes run there:
+// level 1 over all keys, levels 2 and 3 over the keys of the chosen bins, one pass counting per
+// warp what it keeps and one writing the kept entries' list slots in order; the row's indices
+// are those slots' positions.  Warp w owns a contiguous range of segments, so warp order
+// followed by slot order is position order.
+constexpr int kMergeWarps = 12;
+constexpr int kMergeThreads = kMergeWarps * 32;
+constexpr size_t kMergeSmemMax = 200u * 1024u;
+
+__global__ void __launch_bounds__(kMergeThreads, 1) lists_merge_kernel(const FeedParams p) {
+  extern __shared__ __align__(16) uint32_t kv[];  // [in_seg * in_K]
+  __shared__ ArrSelShared sh;
+  __shared__ int32_t sel_f[CSA2_MAX_TOPK];
+  ArrSel<kMergeWarps> s;
+  s.sh = &sh;
+  s.tid = threadIdx.x;
+  const int row = blockIdx.x, S = p.in_seg, Kin = p.in_K, K = p.K;
+  const int w = s.warp(), ln = s.lane();
+  int* cnt = reinterpret_cast<int*>(sh.aux);  // [S <= 64]
+  uint32_t* thr_s = sh.aux + 64;
+  for (int i = s.tid; i < S; i += kMergeThreads) {
+    cnt[i] = min(__ldcg(p.in_cnt + (size_t)row * S + i), Kin);
+    thr_s[i] = p.in_thr ? __ldcg(p.in_thr + (size_t)row * S + i) : 0u;
+  }
+  s.zero_hist(kHistBins);
+  s.sync();
+  uint32_t thr0 = 0u;
+  for (int i = 0; i < S; ++i) thr0 = max(thr0, thr_s[i]);
+  const int n = S * Kin;
+  const uint32_t* gk = p.in_keys + (size_t)row * n;
+  auto filt = [&](uint32_t key, int f) -> uint32_t { return (f % Kin < cnt[f / Kin] && key >= thr0) ? key : 0u; };
+  if ((n & 3) == 0) {
+    const uint4* g4 = reinterpret_cast<const uint4*>(gk);
+    uint4* s4 = reinterpret_cast<uint4*>(kv);
+#pragma unroll 4
+    for (int i = s.tid; i < n / 4; i += kMergeThreads) {
+      uint4 v = __ldcg(g4 + i);
+      v.x = filt(v.x, 4 * i), v.y = filt(v.y, 4 * i + 1), v.z = filt(v.z, 4 * i + 2), v.w = filt(v.w, 4 * i + 3);
+      s4[i] = v;
+    }
+  } else {
+#pragma unroll 4
+    for (int i = s.tid; i < n; i += kMergeThreads) kv[i] = filt(__ldcg(gk + i), i);
+  }
+  s.sync();
+  // level-1 histogram: every thread over a strided share of all slots
+  for (int i = s.tid; i < n; i += kMergeThreads) {
+    const uint32_t key = kv[i];
+    if (key) atomicAdd(&sh.hist[key >> 20], 1);
+  }
+  s.sync();
+  s.template pick<kHistBins>(K);
+  uint32_t thr = 0u;
+  int n_eq = 0;
+  if (sh.total > K) {
+    const uint32_t b1 = (uint32_t)sh.bin;
+    int need = K - sh.before;
+    s.sync();
+    s.zero_hist(kHistBins);
+    s.sync();
+    for (int i = s.tid; i < n; i += kMergeThreads) {
+      const uint32_t key = kv[i];
+      if (key && (key >> 20) == b1) atomicAdd(&sh.hist[(key >> 8) & 0xfffu], 1);
+    }
+    s.sync();
+    s.template pick<kHistBins>(need);
+    const uint32_t hi24 = (b1 << 12) | (uint32_t)sh.bin;
+    need -= sh.before;
+    s.sync();
+    s.zero_hist(256);
+    s.sync();
+    for (int i = s.tid; i < n; i += kMergeThreads) {
+      const uint32_t key = kv[i];
+      if (key && (key >> 8) == hi24) atomicAdd(&sh.hist[key & 0xffu], 1);
+    }
+    s.sync();
+    s.template pick<256>(need);
+    thr = (hi24 << 8) | (uint32_t)sh.bin;
+    n_eq = need - sh.before;
+  }
+  // warp w: slots [f0, f1) of whole segments, in order
+  const int f0 = (int)(((long long)S * w) / kMergeWarps) * Kin, f1 = (int)(((long long)S * (w + 1)) / kMergeWarps) * Kin;
+  int gt = 0, eq = 0;
+  for (int f = f0 + ln; f < f1; f += 32) {
+    const uint32_t key = kv[f];
+    gt += key != 0u && key > thr;
+    eq += key != 0u && key == thr;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+  }
+  // gt <= K in every warp and in sum; equal keys beyond K per warp never change what is taken,
+  // so clamping keeps both halves of the packed scan below 2^16
+  eq = min(eq, K);
+  int tot_packed;
+  const int before = s.scan(ln == 0 ? (gt << 16) | eq : 0, &tot_packed);
+  const int pb = __shfl_sync(0xffffffffu, before, 0);
+  const int eq_b = pb & 0xffff;
+  const int take = max(0, min(eq, n_eq - eq_b));
+  int base = (pb >> 16) + min(eq_b, n_eq);
+  const int kept = min(K, (tot_packed >> 16) + min(tot_packed & 0xffff, n_eq));
+  int eq_seen = 0;
+  const unsigned lt = lanemask_lt();
+  for (int f0r = f0; f0r < f1; f0r += 32) {  // warp-uniform trip count
+    const int f = f0r + ln;
+    const uint32_t key = f < f1 ? kv[f] : 0u;
+    const bool is_eq = key != 0u && key == thr;
+    const unsigned em = __ballot_sync(0xffffffffu, is_eq);
+    const bool keep = key != 0u && (key > thr || (is_eq && eq_seen + __popc(em & lt) < take));
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    const int r = base + __popc(km & lt);
+    if (keep && r < K) sel_f[r] = f;
+    base += __popc(km);
+    eq_seen += __popc(em);
+  }
+  s.sync();
+  const int32_t* pos = p.in_pos + (size_t)row * n;
+  int32_t* out = p.idx + (size_t)row * K;
+  for (int r = s.tid; r < K; r += kMergeThreads) out[r] = r < kept ? __ldcg(pos + sel_f[r]) : -1;
+}
+
 }  // namespace
+
+cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  const size_t smem = (size_t)p.in_seg * p.in_K * sizeof(uint32_t);
+  if (p.in_seg > 64 || p.K > CSA2_MAX_TOPK || smem > kMergeSmemMax)
+    return launch_topk_feed(p, true, 1, stream);  // beyond the staged segment table or shared memory
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(lists_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  lists_merge_kernel<<<p.n_rows, kMergeThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
 
 size_t feed_smem_bytes(int K) {
   return sizeof(EngShared) + (size_t)kFeedWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;

@@ -95,5 +95,5 @@ extern "C" csa2_status csa2_topk_static(const csa2_topk_args* a, void* stream) {
   m.in_seg = n_seg;
   m.in_K = a->K;
   m.idx = a->idx;
-  return launch_topk_feed(m, true, 1, s) == cudaSuccess ? CSA2_OK : CSA2_ECUDA;
+  return launch_lists_merge(m, s) == cudaSuccess ? CSA2_OK : CSA2_ECUDA;
 }
