@@ -65,22 +65,34 @@ int attn_splits(int n_rows, int K, int window) {
 
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ECUDA; }
 
-// Which indexer kernel runs a scan: the tcgen05 kernels take bf16 keys read in place; FP8
-// keys and candidate lists (Reindex over a pool) take the warp-MMA scan.
+// Which indexer kernel runs a scan: the tcgen05 decode kernel takes bf16 or FP8 keys read in
+// place, the tcgen05 prefill kernel bf16 keys; other FP8 scans and candidate lists not in runs
+// of 64 records take the warp-MMA scan.
 enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill };
 
 // cand_run: the candidates come in runs of that many consecutive records (a Reindex pool of
 // whole blocks); runs of a multiple of 64 let the tcgen05 scan load them with TMA.
+int tc05_segments(int n_rows, long long L, int unit, long long min_seg = 4096);
+
 ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0) {
-  if (a->k_dtype != CSA2_BF16 || !mma_indexer_available()) return ScanPath::kWarpMma;
+  if (!mma_indexer_available() || env_int("CSA2_SCAN_WARP_MMA", 0) != 0) return ScanPath::kWarpMma;
   if (a->cand != nullptr && !(want_topk && cand_run > 0 && cand_run % 64 == 0)) return ScanPath::kWarpMma;
-  if (!want_topk && a->block_max == nullptr && a->n_seq == 1 && a->n_rows >= 64) return ScanPath::kTc05Prefill;
+  const bool fp8 = a->k_dtype == CSA2_FP8_E4M3_ROWSCALE;
+  if (!want_topk && a->block_max == nullptr && a->n_seq == 1 && a->n_rows >= 64)
+    return fp8 ? ScanPath::kWarpMma : ScanPath::kTc05Prefill;
+  if (fp8) {
+    // A tcgen05 block streams FP8 tiles at about a third of the rate it streams bf16 ones, so
+    // the FP8 scan takes it only where its grid is one wave (a second, partial wave of
+    // 16K-record segments costs more than the warp-MMA scan's one wave of longer segments).
+    const long long L = a->cand != nullptr ? a->L : a->n_records;
+    if ((long long)a->n_rows * tc05_segments(a->n_rows, L, 128) > sm_count()) return ScanPath::kWarpMma;
+  }
   return ScanPath::kTc05Decode;
 }
 
 // Segments per row for the tcgen05 decode scan: whole waves of resident blocks, each
 // segment's blocks (for the block maxima) within the kernel's shared-memory table.
-int tc05_segments(int n_rows, long long L, int unit, long long min_seg = 4096) {
+int tc05_segments(int n_rows, long long L, int unit, long long min_seg) {
   int n = scan_segments(n_rows, L, min_seg);
   const long long units = (L + unit - 1) / unit;
   const int max_blocks = mma_decode_max_seg_blocks();
@@ -107,7 +119,8 @@ cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk,
           p.block_max ? (int)(((a->n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg)
           : p.cand   ? (int)(2 * (((a->L + p.unit - 1) / p.unit + n_seg - 1) / n_seg))
                      : 0;
-      return launch_mma_decode(p, (long long)a->n_seq * a->n_records, n_seg, seg_blocks, s);
+      return launch_mma_decode(p, (long long)a->n_seq * a->n_records, n_seg, seg_blocks,
+                               a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, s);
     }
     default:
       return launch_index_scan(p, a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->cand != nullptr, n_seg, s);
@@ -513,7 +526,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
     const int seg_blocks = p.block_max ? (int)(((ic.n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg)
                            : p.cand   ? (int)(2 * (((ic.L + p.unit - 1) / p.unit + n_seg - 1) / n_seg))
                                       : 0;
-    p.cluster_merge = tc05 && env_int("CSA2_SCAN_CLUSTER", 1) != 0 && mma_decode_cluster_ok(n_seg, n_rows, a->K, seg_blocks);
+    p.cluster_merge = tc05 && env_int("CSA2_SCAN_CLUSTER", 1) != 0 && mma_decode_cluster_ok(n_seg, n_rows, a->K, seg_blocks, ic.k_dtype == CSA2_FP8_E4M3_ROWSCALE);
     const bool fused_merge = tc05 && !p.cluster_merge && mma_decode_can_merge(n_seg, a->K);
     if (n_seg > 1) {
       p.row_done = c.take<unsigned long long>((size_t)n_rows);
@@ -577,7 +590,7 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
         : a->mode == CSA2_MODE_REINDEX ? (int)(2 * (((ic.L + unit - 1) / unit + n_seg - 1) / n_seg))
                                        : 0;
     const bool merged = tc05 && ((env_int("CSA2_SCAN_CLUSTER", 1) != 0 &&
-                                  mma_decode_cluster_ok(n_seg, a->attn.n_rows, a->K, seg_blocks)) ||
+                                  mma_decode_cluster_ok(n_seg, a->attn.n_rows, a->K, seg_blocks, ic.k_dtype == CSA2_FP8_E4M3_ROWSCALE)) ||
                                  mma_decode_can_merge(n_seg, a->K));
     n += 1 + (n_seg > 1 && !merged ? 1 : 0);  // the tcgen05 scan merges its segments itself
     if (a->mode == CSA2_MODE_FULL_POOL) n += 2;

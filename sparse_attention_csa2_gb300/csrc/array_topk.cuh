@@ -57,9 +57,9 @@ struct ArrSel {
 
   // Entries of the array owned by each warp (a multiple of 128, so every warp's range starts
   // on a 16-byte boundary and is read in whole 128-entry steps).
-  __host__ __device__ __forceinline__ static int range(int n) { return ((n + NW - 1) / NW + 127) & ~127; }
+  __host__ __device__ static constexpr int range(int n) { return ((n + NW - 1) / NW + 127) & ~127; }
   // Scratch words the lists of an n-entry array take.
-  __host__ __device__ __forceinline__ static int list_words(int n) { return 2 * NW * range(n); }
+  __host__ __device__ static constexpr int list_words(int n) { return 2 * NW * range(n); }
 
   // Exclusive prefix sum over the group in thread order; *total gets the sum.
   __device__ __forceinline__ int scan(int v, int* total) const {

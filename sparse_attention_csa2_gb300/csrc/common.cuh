@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "../../include/csa2.h"
 
@@ -93,6 +94,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   float2 f = __half22float2(hh);
   __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
   return *reinterpret_cast<uint32_t*>(&b);
+}
+// Two OCP E4M3 codes (low byte = first) -> two f16 (packed, exact: every E4M3 value is an f16
+// value), by the hardware conversion.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h;
+  asm("{\n .reg .b32 t;\n cvt.rn.f16x2.e4m3x2 t, %1;\n mov.b32 %0, t;\n}\n" : "=r"(h) : "h"(v));
+  return h;
 }
 // Two bf16 (packed) -> two fp16 (packed), round to nearest.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {

@@ -42,22 +42,44 @@ __device__ __forceinline__ void report_timeout(int* flag, int32_t* dev_status) {
 }
 
 // ===================================================================================== decode
-constexpr int kDecStages = 4;
+// bf16 keys: TMA tiles of 128 records x 256 bytes; D[128 x 32] += K_tile * Q^T in eight
+// kind::f16 K-steps of 16.
+// FP8 keys (E4M3 with one fp32 scale per record): TMA tiles of 128 records x 128 bytes used as
+// they are, in four kind::f8f6f4 K-steps of 32.  q^I (bf16) becomes three E4M3 terms per
+// element: each head is scaled by the power of two that puts its largest element in
+// [128, 256), then x = t1 + t2 / 16 + t3 / 256 with t1 = rn(x), t2 = rn(16 (x - t1)),
+// t3 = rn(16 (16 (x - t1) - t2)), every residual exact in fp32.  Two terms already hold any
+// element whose exponent is at least 2^-6 (8 significant bits against E4M3's 4); the third
+// carries smaller ones down to 2^-10 exactly, that is every element within 2^-17 of its
+// head's largest.  B is the [96 x 128] E4M3 matrix of the terms (row 32 * term + head), D
+// the [128 x 96] products, and the epilogue sums D1 + D2 / 16 + D3 / 256 per head, takes the
+// record's scale, then ReLU and the head weight (times the inverse power of two).
+template <bool FP8>
+struct DecCfg {
+  static constexpr int kStages = FP8 ? 8 : 4;
+  static constexpr int kTileBytes = FP8 ? kTileKeys * 128 : kKeyTile;
+  static constexpr int kThreads = 12 * 32;  // warp 0 TMA, warp 1 MMA + TMEM, warps 4..11 epilogue
+  static constexpr int kQBytes = FP8 ? 96 * 128 : 2 * 32 * 128;  // E4M3 terms, or the bf16 query tile
+  static constexpr int kN = FP8 ? 96 : 32;                         // MMA N
+  static constexpr uint32_t kAccCols = FP8 ? 128 : 32;             // columns per accumulator
+  static constexpr uint32_t kTmemCols = FP8 ? 256 : 64;
+  static_assert(kStages * kTileBytes == 4 * kKeyTile, "both rings have the same size");
+};
+constexpr int kDecRingBytes = 4 * kKeyTile;
 constexpr int kDecEpiFirst = 4;
 constexpr int kDecEpiWarps = 8;  // two groups of 4 warps (one per TMEM lane quarter), alternate tiles
-constexpr int kDecThreads = (kDecEpiFirst + kDecEpiWarps) * 32;  // warp 0 TMA, warp 1 MMA + TMEM
-constexpr int kDecQHalf = 32 * 128;  // 32 heads x 64 dims x 2 B
-constexpr uint32_t kDecTmemCols = 64;
+constexpr int kDecQHalf = 32 * 128;  // bf16: 32 heads x 64 dims x 2 B
 constexpr int kDecSegMax = 16384;    // records of one segment (their keys stay in shared memory)
 
 struct DecBars {
-  uint64_t full[kDecStages], empty[kDecStages], tfull[2], tempty[2], qfull;
+  uint64_t full[8], empty[8], tfull[2], tempty[2], qfull, qready;
   uint32_t tmem_base;
   int timeout;
   int issued;     // tiles whose TMA loads were issued
   int consumed;   // tiles whose MMAs were issued
   int drained;    // tiles whose accumulators the epilogue read
   int last;       // this block is the last segment of its row to finish
+  int qexp[32];   // FP8: power-of-two exponent applied to each head of q^I
 };
 
 // The last segment block of a row merges the row's lists: every list entry's key goes into
@@ -115,17 +137,20 @@ __device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const Sca
   for (int r = sel.tid; r < K; r += NT) out[r] = r < kept ? (pos_s ? pos_s[sel_idx[r]] : __ldcg(pos + sel_idx[r])) : -1;
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1)
+template <bool FP8>
+__global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK64, const ScanParams p) {
   // launched with programmatic dependent launch: wait for the previous kernel in the stream
   // before reading any input
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  using C = DecCfg<FP8>;
+  constexpr int kStages = C::kStages, kThreads = C::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* ring = smem;
-  uint8_t* qs = ring + kDecStages * kKeyTile;
-  DecBars& bars = *reinterpret_cast<DecBars*>(qs + 2 * kDecQHalf);
+  uint8_t* qs = ring + kDecRingBytes;
+  DecBars& bars = *reinterpret_cast<DecBars*>(qs + C::kQBytes);
   uint8_t* rest = reinterpret_cast<uint8_t*>(&bars + 1);
   rest = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rest) + 15) & ~static_cast<uintptr_t>(15));
   ArrSelShared* selsh = reinterpret_cast<ArrSelShared*>(rest);
@@ -151,17 +176,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int seg_len = (int)(e1 - e0);
 
   const bool do_topk = p.K > 0;
-  ArrSel<kDecThreads / 32> sel;  // the whole block, once the stream is done
+  ArrSel<kThreads / 32> sel;  // the whole block, once the stream is done
   sel.sh = selsh;
   sel.tid = tid;
   const int bs = p.block_max ? U : 1;
   const int seg_blocks = p.block_max ? (int)((e1 - e0 + bs - 1) / bs) : 0;
 
   if (tid == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc05::mbar_init(&bars.full[s], 1);
       tc05::mbar_init(&bars.empty[s], 1);
     }
+    tc05::mbar_init(&bars.qready, kDecEpiWarps);  // FP8: the epilogue warps built the E4M3 terms
     for (int a = 0; a < 2; ++a) {
       tc05::mbar_init(&bars.tfull[a], 1);
       tc05::mbar_init(&bars.tempty[a], kDecEpiWarps / 2);  // one arrive per warp of the draining group
@@ -171,10 +197,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     bars.issued = bars.consumed = bars.drained = 0;
     tc05::fence_barrier_init();
   }
-  if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, kDecTmemCols);
-  for (int i = tid; i < seg_blocks; i += kDecThreads) bkeys[i] = 0u;
+  if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, C::kTmemCols);
+  for (int i = tid; i < seg_blocks; i += kThreads) bkeys[i] = 0u;
   if (cmode)
-    for (int i = tid; i < (seg_len + 63) / 64; i += kDecThreads)
+    for (int i = tid; i < (seg_len + 63) / 64; i += kThreads)
       hstart[i] = p.cand[(size_t)row * p.cand_stride + e0 + 64 * i];
   if (do_topk) sel.zero_hist(kHistBins);
   tc05::fence_before();
@@ -188,18 +214,32 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && n_tiles > 0) {
-      tc05::mbar_expect_tx(&bars.qfull, 2 * kDecQHalf);
-      tc05::tma_load_2d(qs, &tmQ, 0, row * 32, &bars.qfull);
-      tc05::tma_load_2d(qs + kDecQHalf, &tmQ, 64, row * 32, &bars.qfull);
+      if (!FP8) {
+        tc05::mbar_expect_tx(&bars.qfull, 2 * kDecQHalf);
+        tc05::tma_load_2d(qs, &tmQ, 0, row * 32, &bars.qfull);
+        tc05::tma_load_2d(qs + kDecQHalf, &tmQ, 64, row * 32, &bars.qfull);
+      }
       const int y0 = (int)((long long)b * p.N + e0);
       for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % kDecStages;
-        if (!tc05::mbar_wait(&bars.empty[s], ((t / kDecStages) & 1) ^ 1)) {
+        const int s = t % kStages;
+        if (!tc05::mbar_wait(&bars.empty[s], ((t / kStages) & 1) ^ 1)) {
           report_timeout(&bars.timeout, p.dev_status);
           break;
         }
-        uint8_t* dst = ring + s * kKeyTile;
-        if (cmode) {
+        uint8_t* dst = ring + s * C::kTileBytes;
+        if (FP8) {
+          // one 128-byte row per record; candidate mode: one 64-row box per run
+          if (cmode) {
+            const int halves = min(2, (seg_len - t * kTileKeys + 63) / 64);
+            tc05::mbar_expect_tx(&bars.full[s], (uint32_t)halves * (C::kTileBytes / 2));
+            for (int h = 0; h < halves; ++h)
+              tc05::tma_load_2d(dst + h * (C::kTileBytes / 2), &tmK64, 0, (int)((long long)b * p.N + hstart[2 * t + h]),
+                                &bars.full[s]);
+          } else {
+            tc05::mbar_expect_tx(&bars.full[s], C::kTileBytes);
+            tc05::tma_load_2d(dst, &tmK, 0, y0 + t * kTileKeys, &bars.full[s]);
+          }
+        } else if (cmode) {
           // one or two 64-slot runs (rows 0..63 and 64..127 of the tile's swizzled halves)
           const int halves = min(2, (seg_len - t * kTileKeys + 63) / 64);
           tc05::mbar_expect_tx(&bars.full[s], (uint32_t)halves * (kKeyTile / 2));
@@ -220,23 +260,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t idesc = tc05::idesc_bf16(128, 32);
-      bool ok = tc05::mbar_wait(&bars.qfull, 0);
+      constexpr uint32_t idesc = FP8 ? tc05::idesc_e4m3(128, C::kN) : tc05::idesc_bf16(128, C::kN);
+      bool ok = tc05::mbar_wait(FP8 ? &bars.qready : &bars.qfull, 0);
       const uint32_t q_u = smem_u32(qs);
       for (int t = 0; ok && t < n_tiles; ++t) {
-        const int s = t % kDecStages, a = t & 1;
-        if (!tc05::mbar_wait(&bars.full[s], (t / kDecStages) & 1) ||
+        const int s = t % kStages, a = t & 1;
+        if (!tc05::mbar_wait(&bars.full[s], (t / kStages) & 1) ||
             !tc05::mbar_wait(&bars.tempty[a], ((t >> 1) & 1) ^ 1)) {
           ok = false;
           break;
         }
         tc05::fence_after();
-        const uint32_t a_u = smem_u32(ring + s * kKeyTile);
+        const uint32_t a_u = smem_u32(ring + s * C::kTileBytes);
+        const uint32_t d_t = tmem + (uint32_t)a * C::kAccCols;
+        if (FP8) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kKeyHalf + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * kDecQHalf + (kk & 3) * 32;
-          tc05::mma_bf16(tmem + a * 32, tc05::sw128_desc(a_u + off), tc05::sw128_desc(q_u + qoff), idesc, kk > 0);
+          for (int kk = 0; kk < 4; ++kk)
+            tc05::mma_e4m3(d_t, tc05::sw128_desc(a_u + kk * 32), tc05::sw128_desc(q_u + kk * 32), idesc, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kKeyHalf + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * kDecQHalf + (kk & 3) * 32;
+            tc05::mma_bf16(d_t, tc05::sw128_desc(a_u + off), tc05::sw128_desc(q_u + qoff), idesc, kk > 0);
+          }
         }
         tc05::mma_commit(&bars.empty[s]);
         tc05::mma_commit(&bars.tfull[a]);
@@ -255,8 +302,65 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
     for (int h = 0; h < 32; ++h) w[h] = __ldg(p.w + (size_t)row * kIdxHeads + h);
     bool dead = false;
+    if (FP8 && n_tiles > 0) {
+      // E4M3 terms of q^I: thread (head h, chunk c) takes dims 16c .. 16c+15 of head h
+      const int et = tid - kDecEpiFirst * 32, h = et >> 3, c = et & 7;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_idx) + ((size_t)row * 32 + h) * 16 + 2 * c;
+      const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+      const uint32_t qw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx = max(mx, max(qw[k] & 0x7fffu, (qw[k] >> 16) & 0x7fffu));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      // largest magnitude 2^ex * m, m in [1, 2): scale by 2^(7 - ex) into [128, 256)
+      const int ex = (int)((mx >> 7) & 0xffu) - 127;
+      const int e = mx == 0u ? 0 : min(126, max(-126, 7 - ex));
+      const float f = __int_as_float((e + 127) << 23);
+      uint32_t term[3][4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float x[2] = {__uint_as_float(qw[k] << 16) * f, __uint_as_float(qw[k] & 0xffff0000u) * f};
+#pragma unroll
+        for (int tm = 0; tm < 3; ++tm) {
+          const uint16_t b2 = __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hb = e4m3x2_to_f16x2(b2);
+          const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hb));
+          x[0] = (x[0] - back.x) * 16.f;  // exact: the residual has at most 4 significant bits
+          x[1] = (x[1] - back.y) * 16.f;
+          if (k & 1) term[tm][k >> 1] |= (uint32_t)b2 << 16;
+          else term[tm][k >> 1] = b2;
+        }
+      }
+#pragma unroll
+      for (int tm = 0; tm < 3; ++tm) {
+        const int n = 32 * tm + h;  // B row; 16-byte chunk c sits at slot c ^ (n & 7)
+        *reinterpret_cast<uint4*>(qs + n * 128 + ((c ^ (n & 7)) << 4)) =
+            make_uint4(term[tm][0], term[tm][1], term[tm][2], term[tm][3]);
+      }
+      if (c == 0) bars.qexp[h] = e;
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the MMA reads B through the async proxy
+      __syncwarp();
+      if (lane == 0) tc05::mbar_arrive(&bars.qready);
+      // the heads of q^I were scaled by 2^qexp[h]: the weights take the inverse factor
+      dead = !tc05::mbar_wait(&bars.qready, 0);
+      if (dead && lane == 0) report_timeout(&bars.timeout, p.dev_status);
+#pragma unroll
+      for (int h = 0; h < 32; ++h) w[h] *= __int_as_float((127 - bars.qexp[h]) << 23);
+    }
     float* srow = p.scores ? p.scores + (size_t)row * p.scores_stride : nullptr;
+    const float* kscale = FP8 ? p.k_scale + (size_t)b * p.N : nullptr;
     const int n_pairs = (n_tiles + 1) / 2;
+    // FP8: the scale of this thread's record in the group's next tiles, loaded kScalePre
+    // tiles ahead (an HBM load per tile would otherwise stall every iteration)
+    constexpr int kScalePre = 4;
+    auto scale_of = [&](int pr) -> float {
+      const int jl = (2 * pr + grp) * kTileKeys + 32 * quarter + lane;
+      return jl < seg_len ? __ldg(kscale + (cmode ? hstart[jl >> 6] + (jl & 63) : e0 + jl)) : 1.f;
+    };
+    float kpre[kScalePre];
+#pragma unroll
+    for (int i = 0; i < kScalePre; ++i) kpre[i] = FP8 ? scale_of(i) : 1.f;
     for (int pr = 0; pr < n_pairs; ++pr) {
       const int t = 2 * pr + grp, a = grp;
       if (t >= n_tiles) continue;
@@ -265,19 +369,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (lane == 0) report_timeout(&bars.timeout, p.dev_status);
       }
       float sc = 0.f;
+      const int jl = t * kTileKeys + 32 * quarter + lane;  // record index within the segment
+      const float ksc = kpre[0];
+      if (FP8) {
+#pragma unroll
+        for (int i = 0; i + 1 < kScalePre; ++i) kpre[i] = kpre[i + 1];
+        kpre[kScalePre - 1] = scale_of(pr + kScalePre);
+      }
       if (!dead) {
         tc05::fence_after();
+        const uint32_t d_t = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)a * C::kAccCols;
         uint32_t v[32];
-        tc05::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * 32), v);
-        tc05::tmem_ld_wait();
-        tc05::fence_before();
-        __syncwarp();
-        if (lane == 0) tc05::mbar_arrive(&bars.tempty[a]);
+        tc05::tmem_ld32(d_t, v);
+        if (FP8) {
+          // D1 + (D2 + D3 / 16) / 16 per head
+          uint32_t v2[32], v3[32];
+          tc05::tmem_ld32(d_t + 32, v2);
+          tc05::tmem_ld32(d_t + 64, v3);
+          tc05::tmem_ld_wait();
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) tc05::mbar_arrive(&bars.tempty[a]);
 #pragma unroll
-        for (int h = 0; h < 32; ++h) sc = fmaf(w[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
+          for (int h = 0; h < 32; ++h) {
+            const float x = fmaf(fmaf(__uint_as_float(v3[h]), 0.0625f, __uint_as_float(v2[h])), 0.0625f,
+                                 __uint_as_float(v[h]));
+            sc = fmaf(w[h], fmaxf(x * ksc, 0.f), sc);
+          }
+        } else {
+          tc05::tmem_ld_wait();
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) tc05::mbar_arrive(&bars.tempty[a]);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) sc = fmaf(w[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
+        }
         if (warp == kDecEpiFirst + 4 * grp && lane == 0) atomicMax(&bars.drained, t + 1);
       }
-      const int jl = t * kTileKeys + 32 * quarter + lane;  // record index within the segment
       const bool valid = !dead && jl < seg_len;
       const uint32_t key = valid ? score_key(sc) : 0u;
       if (do_topk && jl < seg_len) {
@@ -297,23 +425,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // they serve as the selection's scratch: the candidate lists, and the selected entries'
     // indices (CSA2_MAX_TOPK words at the end).  After a timeout copies may be in flight: the
     // selection is skipped (the status reports the timeout).
-    constexpr int kScratchWords = (kDecStages * kKeyTile + 2 * kDecQHalf) / 4;
+    constexpr int kScratchWords = (kDecRingBytes + C::kQBytes) / 4;
     constexpr int kListRoom = kScratchWords - CSA2_MAX_TOPK;
-    static_assert(2 * (kDecThreads / 32) * ((kDecSegMax / (kDecThreads / 32) + 1 + 127) & ~127) <= kListRoom,
-                  "selection lists fit in the scratch");
+    static_assert(ArrSel<kThreads / 32>::list_words(kDecSegMax) <= kListRoom, "selection lists fit in the scratch");
     sel.scratch = reinterpret_cast<uint32_t*>(ring);
     int32_t* sel_idx = reinterpret_cast<int32_t*>(ring) + kListRoom;
     // record position of the segment's entry i
     auto pos_of = [&](int i) -> int32_t { return cmode ? hstart[i >> 6] + (i & 63) : (int32_t)(e0 + i); };
     const bool live = !bars.timeout;
-    for (int i = tid; i < seg_blocks; i += kDecThreads)
+    for (int i = tid; i < seg_blocks; i += kThreads)
       p.block_max[(size_t)row * p.bmax_stride + e0 / bs + i] = bkeys[i] ? key_score(bkeys[i]) : -INFINITY;
     if (seg == n_seg - 1) {
       float* srow = p.scores ? p.scores + (size_t)row * p.scores_stride : nullptr;
       if (srow)
-        for (long long jj = L_row + tid; jj < p.scores_len; jj += kDecThreads) srow[jj] = -INFINITY;
+        for (long long jj = L_row + tid; jj < p.scores_len; jj += kThreads) srow[jj] = -INFINITY;
       if (p.block_max)
-        for (long long blk = (L_row + bs - 1) / bs + tid; blk < p.n_blocks; blk += kDecThreads)
+        for (long long blk = (L_row + bs - 1) / bs + tid; blk < p.n_blocks; blk += kThreads)
           p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
     }
     if (do_topk && p.cluster_merge) {
@@ -324,7 +451,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // entries: the status reports the timeout).
       const uint32_t rank = cluster_rank();
       const int n_here = live ? seg_len : 0;
-      arr_threshold_impl(sel, keys, n_here, p.K, true, ClusterPick<kDecThreads / 32>{rank, (uint32_t)n_seg, kDecSegMax});
+      arr_threshold_impl(sel, keys, n_here, p.K, true, ClusterPick<kThreads / 32>{rank, (uint32_t)n_seg, kDecSegMax});
       int base = 0, total = 0, kept = 0;
       if (selsh->thr == 0u) {
         // at most K candidates in the row: every block keeps all its entries; offsets by
@@ -337,20 +464,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         kept = arr_compact(sel, n_here, sel_idx);
       }
       int32_t* out = p.idx + (size_t)row * p.K;
-      for (int r = tid; r < kept; r += kDecThreads)
+      for (int r = tid; r < kept; r += kThreads)
         if (base + r < p.K) out[base + r] = pos_of(sel_idx[r]);
       if (rank == (uint32_t)n_seg - 1)
-        for (int r = total + tid; r < p.K; r += kDecThreads) out[r] = -1;
+        for (int r = total + tid; r < p.K; r += kThreads) out[r] = -1;
       cluster_sync();  // no block leaves while another may still read its shared memory
     } else if (do_topk && live) {
       arr_threshold(sel, keys, seg_len, p.K, true);
       const int kept = arr_compact(sel, seg_len, sel_idx);
       if (n_seg == 1) {
         int32_t* out = p.idx + (size_t)row * p.K;
-        for (int r = tid; r < p.K; r += kDecThreads) out[r] = r < kept ? pos_of(sel_idx[r]) : -1;
+        for (int r = tid; r < p.K; r += kThreads) out[r] = r < kept ? pos_of(sel_idx[r]) : -1;
       } else {
         const size_t o = ((size_t)row * n_seg + seg) * p.K;
-        for (int r = tid; r < kept; r += kDecThreads) {
+        for (int r = tid; r < kept; r += kThreads) {
           p.seg_keys[o + r] = keys[sel_idx[r]];
           p.seg_pos[o + r] = pos_of(sel_idx[r]);
         }
@@ -380,15 +507,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   if (bars.timeout && tid == 0) {
     // drain loads and MMAs still in flight (bounded), then free tensor memory
-    for (int t = bars.consumed; t < bars.issued; ++t)
-      tc05::mbar_wait(&bars.full[t % kDecStages], (t / kDecStages) & 1);
+    // (only the last kStages loads can be outstanding: each stage's latest phase)
+    for (int t = max(0, bars.issued - kStages); t < bars.issued; ++t)
+      tc05::mbar_wait(&bars.full[t % kStages], (t / kStages) & 1);
     for (int t = max(0, bars.drained - 1); t < bars.consumed; ++t)
       tc05::mbar_wait(&bars.tfull[t & 1], (t >> 1) & 1);
   }
   __syncthreads();
   if (warp == 1) {
     tc05::fence_after();
-    tc05::tmem_dealloc(tmem, kDecTmemCols);
+    tc05::tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -645,9 +773,24 @@ bool make_tmap(CUtensorMap* tm, const void* base, unsigned long long rows, unsig
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t dec_smem_bytes(int K, int max_seg_blocks) {
+// Row-major [rows x 128] byte matrix (FP8 keys), boxes of 128 columns x box_rows rows,
+// 128-byte swizzle.
+bool make_tmap_u8(CUtensorMap* tm, const void* base, unsigned long long rows, unsigned box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t dec_smem_bytes(int K, int max_seg_blocks, bool fp8) {
   (void)K;
-  return 1024 + (size_t)kDecStages * kKeyTile + 2 * kDecQHalf + sizeof(DecBars) + 16 + sizeof(ArrSelShared) +
+  return 1024 + (size_t)kDecRingBytes + (fp8 ? DecCfg<true>::kQBytes : DecCfg<false>::kQBytes) + sizeof(DecBars) +
+         16 + sizeof(ArrSelShared) +
          (size_t)kDecSegMax * 4 + (size_t)max_seg_blocks * 4;
 }
 
@@ -660,41 +803,44 @@ int mma_decode_max_seg_blocks() { return 2048; }
 int mma_decode_max_segment() { return kDecSegMax; }
 // The segments of a row can run as one thread-block cluster (2..16 blocks, every cluster of
 // the grid resident at once).
-bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks);
+bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks, bool fp8);
 
-bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks) {
+bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks, bool fp8) {
   if (n_seg < 2 || n_seg > 16 || K > CSA2_MAX_TOPK) return false;
-  // the answer depends on the device and the launch shape only: remembered per shape
+  // the answer depends on the device, the kernel and the launch shape only: remembered
   struct Entry {
     int dev, n_seg, n_rows, smem_key;
-    bool ok;
+    bool fp8, ok;
   };
   static Entry cache[32];
   static int n_cache = 0;
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const int smem_key = (int)dec_smem_bytes(K, max_seg_blocks);
+  const int smem_key = (int)dec_smem_bytes(K, max_seg_blocks, fp8);
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_cache; ++i)
-    if (cache[i].dev == dev && cache[i].n_seg == n_seg && cache[i].n_rows == n_rows && cache[i].smem_key == smem_key)
+    if (cache[i].dev == dev && cache[i].n_seg == n_seg && cache[i].n_rows == n_rows && cache[i].smem_key == smem_key &&
+        cache[i].fp8 == fp8)
       return cache[i].ok;
-  const bool ok = cluster_ok_query(n_seg, n_rows, K, max_seg_blocks);
-  cache[n_cache % 32] = Entry{dev, n_seg, n_rows, smem_key, ok};
+  const bool ok = cluster_ok_query(n_seg, n_rows, K, max_seg_blocks, fp8);
+  cache[n_cache % 32] = Entry{dev, n_seg, n_rows, smem_key, fp8, ok};
   if (n_cache < 32) ++n_cache;
   return ok;
 }
 
-bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks) {
-  const size_t smem = dec_smem_bytes(K, max_seg_blocks);
-  if (cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+template <bool FP8>
+bool cluster_ok_query_t(int n_seg, int n_rows, int K, int max_seg_blocks) {
+  const size_t smem = dec_smem_bytes(K, max_seg_blocks, FP8);
+  if (cudaFuncSetAttribute(idx_mma_decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return false;
   if (n_seg > 8 &&
-      cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      cudaFuncSetAttribute(idx_mma_decode_kernel<FP8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_seg, n_rows);
-  cfg.blockDim = dim3(kDecThreads);
+  cfg.blockDim = dim3(DecCfg<FP8>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -704,29 +850,34 @@ bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, idx_mma_decode_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, idx_mma_decode_kernel<FP8>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   return clusters >= n_rows;
 }
 
+bool cluster_ok_query(int n_seg, int n_rows, int K, int max_seg_blocks, bool fp8) {
+  return fp8 ? cluster_ok_query_t<true>(n_seg, n_rows, K, max_seg_blocks)
+             : cluster_ok_query_t<false>(n_seg, n_rows, K, max_seg_blocks);
+}
+
 bool mma_decode_can_merge(int n_seg, int K) { return n_seg <= 64 && (long long)n_seg * K <= kDecSegMax; }
 
-size_t mma_decode_smem_bytes(int K, int max_seg_blocks) { return dec_smem_bytes(K, max_seg_blocks); }
+size_t mma_decode_smem_bytes(int K, int max_seg_blocks, bool fp8) { return dec_smem_bytes(K, max_seg_blocks, fp8); }
 
-cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
-                              cudaStream_t stream) {
-  if (p.n_rows == 0) return cudaSuccess;
-  if (dec_smem_bytes(p.K, max_seg_blocks) > 232448) return cudaErrorInvalidValue;
+template <bool FP8>
+cudaError_t launch_mma_decode_t(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
+                                cudaStream_t stream) {
   CUtensorMap tmK, tmQ, tmK64;
-  if (!make_tmap(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys) ||
-      !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, 32) ||
-      !make_tmap(&tmK64, p.k_idx, (unsigned long long)n_seq_rows, 64))
-    return cudaErrorInvalidValue;
-  if (p.cand != nullptr && (p.cand_run <= 0 || p.cand_run % 64 != 0)) return cudaErrorInvalidValue;
-  const size_t smem = dec_smem_bytes(p.K, max_seg_blocks);
-  cudaError_t e = cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool maps = FP8 ? make_tmap_u8(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys) &&
+                              make_tmap_u8(&tmK64, p.k_idx, (unsigned long long)n_seq_rows, 64)
+                        : make_tmap(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys) &&
+                              make_tmap(&tmK64, p.k_idx, (unsigned long long)n_seq_rows, 64);
+  if (!maps || !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, 32)) return cudaErrorInvalidValue;
+  const size_t smem = dec_smem_bytes(p.K, max_seg_blocks, FP8);
+  auto kern = idx_mma_decode_kernel<FP8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ScanParams q = p;
   int dev = 0, sms = 0;
@@ -734,33 +885,41 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
     q.pdl_trigger = (long long)n_seg * p.n_rows <= sms;  // one CTA per SM: a single wave
   // Programmatic dependent launch: the blocks may become resident while the previous kernel
   // in the stream finishes; they wait for it before reading anything.
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2] = {};
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_seg, p.n_rows);
-  cfg.blockDim = dim3(kDecThreads);
+  cfg.blockDim = dim3(DecCfg<FP8>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchAttribute attr2[2] = {attr[0], {}};
   if (p.cluster_merge) {
     // the segments of a row form one cluster
-    attr2[1].id = cudaLaunchAttributeClusterDimension;
-    attr2[1].val.clusterDim.x = (unsigned)n_seg;
-    attr2[1].val.clusterDim.y = 1;
-    attr2[1].val.clusterDim.z = 1;
-    cfg.attrs = attr2;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)n_seg;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
     if (n_seg > 8) {
-      e = cudaFuncSetAttribute(idx_mma_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
   }
-  e = cudaLaunchKernelEx(&cfg, idx_mma_decode_kernel, tmK, tmQ, tmK64, q);
+  e = cudaLaunchKernelEx(&cfg, kern, tmK, tmQ, tmK64, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks, bool fp8,
+                              cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  if (dec_smem_bytes(p.K, max_seg_blocks, fp8) > 232448) return cudaErrorInvalidValue;
+  if (p.cand != nullptr && (p.cand_run <= 0 || p.cand_run % 64 != 0)) return cudaErrorInvalidValue;
+  if (fp8 && p.k_scale == nullptr) return cudaErrorInvalidValue;
+  return fp8 ? launch_mma_decode_t<true>(p, n_seq_rows, n_seg, max_seg_blocks, stream)
+             : launch_mma_decode_t<false>(p, n_seq_rows, n_seg, max_seg_blocks, stream);
 }
 
 size_t mma_prefill_smem_bytes() { return 1024 + (size_t)kPreStages * kKeyTile + 2 * kPreQHalf + sizeof(PreBars); }

@@ -47,13 +47,13 @@ struct ScanParams {
 
 size_t scan_smem_bytes(bool fp8, int K);
 
-// tcgen05 indexer (bf16 keys, records in place): decode rows and prefill tiles.
+// tcgen05 indexer: decode rows (bf16 or FP8 keys, records in place) and prefill tiles (bf16).
 bool mma_indexer_available();
 int mma_decode_max_seg_blocks();
 int mma_decode_max_segment();  // most records one decode segment may hold
-bool mma_decode_can_merge(int n_seg, int K);
-bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks);  // segments of a row as a cluster  // the decode scan can merge its segments' lists itself
-cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks,
+bool mma_decode_can_merge(int n_seg, int K);  // the decode scan can merge its segments' lists itself
+bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks, bool fp8);  // segments of a row as a cluster
+cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks, bool fp8,
                               cudaStream_t stream);
 cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream);
 cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_seg, cudaStream_t stream);

@@ -131,11 +131,14 @@ __global__ void pool_expand_kernel(const int32_t* __restrict__ kept, const int32
 
 // Merge of per-segment lists (source B) into a row's final top-K, one block per row.  The
 // row's list keys are staged once in shared memory (keys below the largest per-segment K-th key
-// zeroed: that segment alone holds K entries at or above it), then histogram passes run there:
-// level 1 over all keys, levels 2 and 3 over the keys of the chosen bins, one pass counting per
-// warp what it keeps and one writing the kept entries' list slots in order; the row's indices
-// are those slots' positions.  Warp w owns a contiguous range of segments, so warp order
-// followed by slot order is position order.
+// zeroed: that segment alone holds K entries at or above it), then histogram passes run there.
+// The candidates are a row's best keys and share their leading bits, so the levels are taken
+// on the bits below the highest bit in which the smallest and largest candidate differ (a
+// 12-bit window, then the next 12, then the rest): the level-1 bins spread the candidates
+// instead of piling them onto a few counters.  One pass then counts per warp what it keeps
+// and one writes the kept entries' list slots in order; the row's indices are those slots'
+// positions.  Warp w owns a contiguous range of segments, so warp order followed by slot order
+// is position order.
 constexpr int kMergeWarps = 12;
 constexpr int kMergeThreads = kMergeWarps * 32;
 constexpr size_t kMergeSmemMax = 200u * 1024u;
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) lists_merge_kernel(const Fee
   extern __shared__ __align__(16) uint32_t kv[];  // [in_seg * in_K]
   __shared__ ArrSelShared sh;
   __shared__ int32_t sel_f[CSA2_MAX_TOPK];
+  __shared__ uint32_t kext[2];  // smallest and largest candidate key
   ArrSel<kMergeWarps> s;
   s.sh = &sh;
   s.tid = threadIdx.x;
@@ -155,61 +159,87 @@ __global__ void __launch_bounds__(kMergeThreads, 1) lists_merge_kernel(const Fee
     cnt[i] = min(__ldcg(p.in_cnt + (size_t)row * S + i), Kin);
     thr_s[i] = p.in_thr ? __ldcg(p.in_thr + (size_t)row * S + i) : 0u;
   }
+  if (s.tid == 0) kext[0] = 0xffffffffu, kext[1] = 0u;
   s.zero_hist(kHistBins);
   s.sync();
   uint32_t thr0 = 0u;
   for (int i = 0; i < S; ++i) thr0 = max(thr0, thr_s[i]);
   const int n = S * Kin;
   const uint32_t* gk = p.in_keys + (size_t)row * n;
-  auto filt = [&](uint32_t key, int f) -> uint32_t { return (f % Kin < cnt[f / Kin] && key >= thr0) ? key : 0u; };
-  if ((n & 3) == 0) {
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  auto filt = [&](uint32_t key, int sg, int j) -> uint32_t {
+    key = (j < cnt[sg] && key >= thr0) ? key : 0u;
+    if (key) kmin = min(kmin, key), kmax = max(kmax, key);
+    return key;
+  };
+  if ((Kin & 3) == 0) {
     const uint4* g4 = reinterpret_cast<const uint4*>(gk);
     uint4* s4 = reinterpret_cast<uint4*>(kv);
 #pragma unroll 4
     for (int i = s.tid; i < n / 4; i += kMergeThreads) {
       uint4 v = __ldcg(g4 + i);
-      v.x = filt(v.x, 4 * i), v.y = filt(v.y, 4 * i + 1), v.z = filt(v.z, 4 * i + 2), v.w = filt(v.w, 4 * i + 3);
+      const int sg = (4 * i) / Kin, j = 4 * i - sg * Kin;
+      v.x = filt(v.x, sg, j), v.y = filt(v.y, sg, j + 1), v.z = filt(v.z, sg, j + 2), v.w = filt(v.w, sg, j + 3);
       s4[i] = v;
     }
   } else {
 #pragma unroll 4
-    for (int i = s.tid; i < n; i += kMergeThreads) kv[i] = filt(__ldcg(gk + i), i);
+    for (int i = s.tid; i < n; i += kMergeThreads) kv[i] = filt(__ldcg(gk + i), i / Kin, i % Kin);
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (ln == 0 && kmax != 0u) atomicMin(&kext[0], kmin), atomicMax(&kext[1], kmax);
   s.sync();
-  // level-1 histogram: every thread over a strided share of all slots
+  kmin = kext[0], kmax = kext[1];
+  // bits above d are common to every candidate
+  const int d = kmax > kmin ? 31 - __clz(kmin ^ kmax) : 0;
+  const int s1 = max(d - 11, 0), s2 = max(s1 - 12, 0);
+  const uint32_t m1 = (2u << (d - s1)) - 1u;
   for (int i = s.tid; i < n; i += kMergeThreads) {
     const uint32_t key = kv[i];
-    if (key) atomicAdd(&sh.hist[key >> 20], 1);
+    if (key) atomicAdd(&sh.hist[(key >> s1) & m1], 1);
   }
   s.sync();
   s.template pick<kHistBins>(K);
   uint32_t thr = 0u;
   int n_eq = 0;
   if (sh.total > K) {
-    const uint32_t b1 = (uint32_t)sh.bin;
+    // T: the threshold's bits above the current shift
+    uint32_t T = ((kmax >> s1) & ~m1) | (uint32_t)sh.bin;
     int need = K - sh.before;
-    s.sync();
-    s.zero_hist(kHistBins);
-    s.sync();
-    for (int i = s.tid; i < n; i += kMergeThreads) {
-      const uint32_t key = kv[i];
-      if (key && (key >> 20) == b1) atomicAdd(&sh.hist[(key >> 8) & 0xfffu], 1);
+    if (s1 > 0) {
+      const uint32_t m2 = (1u << (s1 - s2)) - 1u;
+      s.sync();
+      s.zero_hist(kHistBins);
+      s.sync();
+      for (int i = s.tid; i < n; i += kMergeThreads) {
+        const uint32_t key = kv[i];
+        if (key && (key >> s1) == T) atomicAdd(&sh.hist[(key >> s2) & m2], 1);
+      }
+      s.sync();
+      s.template pick<kHistBins>(need);
+      T = (T << (s1 - s2)) | (uint32_t)sh.bin;
+      need -= sh.before;
+      if (s2 > 0) {
+        const uint32_t m3 = (1u << s2) - 1u;  // s2 <= 8
+        s.sync();
+        s.zero_hist(256);
+        s.sync();
+        for (int i = s.tid; i < n; i += kMergeThreads) {
+          const uint32_t key = kv[i];
+          if (key && (key >> s2) == T) atomicAdd(&sh.hist[key & m3], 1);
+        }
+        s.sync();
+        s.template pick<256>(need);
+        T = (T << s2) | (uint32_t)sh.bin;
+        need -= sh.before;
+      }
     }
-    s.sync();
-    s.template pick<kHistBins>(need);
-    const uint32_t hi24 = (b1 << 12) | (uint32_t)sh.bin;
-    need -= sh.before;
-    s.sync();
-    s.zero_hist(256);
-    s.sync();
-    for (int i = s.tid; i < n; i += kMergeThreads) {
-      const uint32_t key = kv[i];
-      if (key && (key >> 8) == hi24) atomicAdd(&sh.hist[key & 0xffu], 1);
-    }
-    s.sync();
-    s.template pick<256>(need);
-    thr = (hi24 << 8) | (uint32_t)sh.bin;
-    n_eq = need - sh.before;
+    thr = T;
+    n_eq = need;
   }
   // warp w: slots [f0, f1) of whole segments, in order
   const int f0 = (int)(((long long)S * w) / kMergeWarps) * Kin, f1 = (int)(((long long)S * (w + 1)) / kMergeWarps) * Kin;

@@ -55,6 +55,32 @@ def test_index_scores(key_fmt, mode):
         assert np.all(np.isneginf(bm[r, len(ref_bm):]))
 
 
+@pytest.mark.parametrize("key_fmt", ["bf16", "fp8"])
+def test_index_scores_heads_of_wide_magnitude(key_fmt):
+    """q^I heads scaled by powers of two from 2^-100 to 2^60 (one head all zero), the head
+    weights by the inverse: every head still weighs alike in the score, so a head whose
+    magnitude the kernel mishandles (FP8 keys widen q^I to f16 with a per-head scale) shows."""
+    _cuda()
+    inp = small("batched_decode", seed=9, mode="gauss", B=2, N=3001, key_fmt=key_fmt)
+    set_rows(inp, [3001, 1777])
+    lay = inp["layers"][0]
+    HI = lay["q_idx"].shape[1]
+    ex = np.array([(-100, -60, -30, -8, 0, 7, 25, 60)[h % 8] for h in range(HI)], np.float64)
+    q = O.bf16_to_f64(lay["q_idx"]) * np.exp2(ex)[None, :, None]
+    q[:, 3, :] = 0.0
+    lay["q_idx"] = synth.bf16_bits(torch.from_numpy(q.astype(np.float32)))
+    lay["w"] = (np.asarray(lay["w"], np.float64) * np.exp2(-ex)[None, :]).astype(np.float32)
+    dv = synth.to_device(inp)
+    c, dl, rw = dv["cache"], dv["layers"][0], dv["rows"]
+    s = S.index_scores(dl["q_idx"], dl["w"], c["k_idx"], c["k_scale"], rw["seq_of_row"], rw["n_visible"])
+    s = s.cpu().numpy().astype(np.float64)
+    ref = O.index_scores_rows(inp, 0)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(s), fin)
+    bound = score_bound(inp, 0)
+    assert np.all(np.abs(s - ref)[fin] <= np.repeat(bound[:, None], s.shape[1], 1)[fin])
+
+
 def test_index_scores_over_candidates():
     _cuda()
     inp = small("hierarchical", seed=5, mode="grid", B=2, N=3000)
@@ -165,10 +191,10 @@ def test_fused_full_gauss():
     assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
 
 
-@pytest.mark.parametrize("mode", ["grid", "gauss"])
-def test_fused_hierarchical_group(mode):
+@pytest.mark.parametrize("mode,key_fmt", [("grid", "bf16"), ("gauss", "bf16"), ("grid", "fp8")])
+def test_fused_hierarchical_group(mode, key_fmt):
     _cuda()
-    inp = small("hierarchical", seed=12, mode=mode, B=2, N=9000, n_keep=16, n_hot_blocks=10)
+    inp = small("hierarchical", seed=12, mode=mode, B=2, N=9000, n_keep=16, n_hot_blocks=10, key_fmt=key_fmt)
     set_rows(inp, [9000, 7001])
     g = gpu_group(synth.to_device(inp))
     ref = O.csa2_group(inp)
