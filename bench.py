@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
     ap.add_argument("--prefill-t", type=int, default=4096, help="queries of the prefill chunk (profiling)")
+    ap.add_argument("--scan-only", metavar="FMT:ROWS:N",
+                    help="time only the indexer scores of ROWS rows of N records (FMT bf16 or fp8; profiling)")
     return ap.parse_args(argv)
 
 
@@ -330,6 +332,39 @@ def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "l
     return out
 
 
+def run_scan_only(args, local):
+    """Indexer scores alone (no selection) for ROWS rows of N records: random bf16 keys, or
+    E4M3 keys with fp32 row scales in [0.5, 1.5); median of CUDA-event times after 3 calls."""
+    import torch
+    import sparse_attention_csa2_gb300 as S
+    fmt, rows, n = args.scan_only.split(":")
+    rows, n = int(rows), int(n)
+    dev = f"cuda:{local}"
+    g = torch.Generator().manual_seed(0)
+    if fmt == "bf16":
+        k = torch.randn(rows, n, 128, generator=g).to(torch.bfloat16).to(dev)
+        ks, rec = None, 256
+    else:
+        k = (torch.randn(rows, n, 128, generator=g) * 64).clamp(-448, 448).to(torch.float8_e4m3fn)
+        k = k.view(torch.uint8).to(dev)
+        ks, rec = (torch.rand(rows, n, generator=g) + 0.5).to(dev), 132
+    q = torch.randn(rows, 32, 128, generator=g).to(torch.bfloat16).to(dev)
+    w = torch.rand(rows, 32, generator=g).to(dev)
+    seq = torch.arange(rows, dtype=torch.int32, device=dev)
+    nv = torch.full((rows,), n, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        S.index_scores(q, w, k, ks, seq, nv)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(max(3, args.steps))]
+    for e0, e1 in ev:
+        e0.record()
+        S.index_scores(q, w, k, ks, seq, nv)
+        e1.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    return {"fmt": fmt, "rows": rows, "records": n, "ms": ms, "key_gbs": rows * n * rec / (ms / 1e3) / 1e9}
+
+
 def run_prefill(args, local, peaks):
     """Prefill chunk (B=1, T=4096 queries at positions 32768.., N=36864 bf16 keys): the
     indexer GEMM on the tensor cores alone, then the whole chunk (scores -> per-query top-512
@@ -397,6 +432,9 @@ def run_gb300(args, world, rank, local):
             peaks = None
         print(json.dumps({"configs": run_configs(local, peaks, steps=args.steps, names=(args.only_config,))}),
               flush=True)
+        return 0
+    if args.scan_only:
+        print(json.dumps({"scan": run_scan_only(args, local)}), flush=True)
         return 0
     if args.prefill_only:
         try:

@@ -402,17 +402,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
     const bool on = ok && f >= 0;  // off: masked entry (logit -inf)
     const float zs = p.scale * rs;
     const uint32_t trow = tmem + ((uint32_t)(32 * qw) << 16) + (uint32_t)hb;
-    // per-head maximum over the tile's entries
-#pragma unroll 1
-    for (int g = 0; g < 4; ++g) {
-      uint32_t v[8];
-      tc05::tmem_ld8(trow + 8 * g, v);
+    // the thread's 32 logits (entry e, heads hb .. hb+31) stay in registers for both passes
+    float z[32];
+    {
+      uint32_t v[32];
+      tc05::tmem_ld32(trow, v);
       tc05::tmem_ld_wait();
-      float z[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
-      group_reduce8<true>(z);
-      if ((lane & 3) == 0) sh.red[qw][hb + 8 * g + lh] = z[0];
+      for (int k = 0; k < 32; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
+    }
+    // per-head maximum over the tile's entries
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float m[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m[k] = z[8 * g + k];
+      group_reduce8<true>(m);
+      if ((lane & 3) == 0) sh.red[qw][hb + 8 * g + lh] = m[0];
     }
     __syncthreads();
     if (qw == 0)
@@ -421,19 +427,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
     __syncthreads();
     // P = exp(z - M) as P_hi | P_lo rows (entry e, MN-major for the second GEMM), the FP8
     // row scale on the weights; per-head sums of the unscaled P
-#pragma unroll 1
+#pragma unroll
     for (int g = 0; g < 4; ++g) {
-      uint32_t v[8];
-      tc05::tmem_ld8(trow + 8 * g, v);
       const float4 m0 = *reinterpret_cast<const float4*>(&sh.mfin[hb + 8 * g]);
       const float4 m1 = *reinterpret_cast<const float4*>(&sh.mfin[hb + 8 * g + 4]);
       const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      tc05::tmem_ld_wait();
       float pe[8];
       uint32_t hi[4], lw[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        pe[k] = on ? __expf(__uint_as_float(v[k]) * zs - (M[k] == -INFINITY ? 0.f : M[k])) : 0.f;
+      for (int k = 0; k < 8; ++k) pe[k] = on ? __expf(z[8 * g + k] - (M[k] == -INFINITY ? 0.f : M[k])) : 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float a0 = pe[2 * k] * rs, a1 = pe[2 * k + 1] * rs;
@@ -483,17 +485,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   if (live) {
     float* po = p.part_o + ((size_t)row * n_tiles + tile) * kHeads * kHeadDim;
 #pragma unroll 1
-    for (int i = 0; i < 16; ++i) {
-      const int c = 2 * (warp >> 2) + (i >> 3), g = i & 7;
+    for (int i = 0; i < 4; ++i) {
+      const int c = 2 * (warp >> 2) + (i >> 1), g = i & 1;  // heads 32g .. 32g+31 of dim chunk c
       const int d = 128 * c + 32 * qw + lane;
-      uint32_t vh[8], vl[8];
-      const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + 128 * c + 8 * g;
-      tc05::tmem_ld8(ta, vh);
-      tc05::tmem_ld8(ta + 64, vl);
+      uint32_t vh[32], vl[32];
+      const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + 128 * c + 32 * g;
+      tc05::tmem_ld32(ta, vh);
+      tc05::tmem_ld32(ta + 64, vl);
       tc05::tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        po[(size_t)(8 * g + k) * kHeadDim + d] = __uint_as_float(vh[k]) + __uint_as_float(vl[k]);
+      for (int k = 0; k < 32; ++k)
+        po[(size_t)(32 * g + k) * kHeadDim + d] = __uint_as_float(vh[k]) + __uint_as_float(vl[k]);
     }
   }
   if (warp == 4) {

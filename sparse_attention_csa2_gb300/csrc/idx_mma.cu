@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
         if (base + r < p.K) out[base + r] = pos_of(sel_idx[r]);
       if (rank == (uint32_t)n_seg - 1)
         for (int r = total + tid; r < p.K; r += kThreads) out[r] = -1;
-      cluster_sync();  // no block leaves while another may still read its shared memory
+      // (the selection's last cluster barrier follows every access to another block's
+      // shared memory, so the blocks may leave independently)
     } else if (do_topk && live) {
       arr_threshold(sel, keys, seg_len, p.K, true);
       const int kept = arr_compact(sel, seg_len, sel_idx);

@@ -2,6 +2,8 @@
 // engine of select.cuh fed from global memory), and the expansion of kept blocks into the
 // hierarchical candidate pool ("DeepSeek-V4.1-Flash explained", section 3: a block is
 // scored by its best position and every position of a kept block enters the pool).
+#include <algorithm>
+
 #include "array_topk.cuh"
 #include "select.cuh"
 #include "kernels.h"
@@ -129,176 +131,149 @@ __global__ void pool_expand_kernel(const int32_t* __restrict__ kept, const int32
   }
 }
 
-// Merge of per-segment lists (source B) into a row's final top-K, one block per row.  The
-// row's list keys are staged once in shared memory (keys below the largest per-segment K-th key
-// zeroed: that segment alone holds K entries at or above it), then histogram passes run there.
-// The candidates are a row's best keys and share their leading bits, so the levels are taken
-// on the bits below the highest bit in which the smallest and largest candidate differ (a
-// 12-bit window, then the next 12, then the rest): the level-1 bins spread the candidates
-// instead of piling them onto a few counters.  One pass then counts per warp what it keeps
-// and one writes the kept entries' list slots in order; the row's indices are those slots'
-// positions.  Warp w owns a contiguous range of segments, so warp order followed by slot order
-// is position order.
+// Merge of per-segment lists (source B) into a row's final top-K.  A row's lists are spread
+// over a thread-block cluster (up to 8 blocks, each a contiguous range of segments, so block
+// order followed by slot order is position order).  Each block stages its lists' keys in
+// shared memory, keys below the largest per-segment K-th key zeroed (that segment alone holds
+// K entries at or above it).  The candidates are a row's best keys and share their leading
+// bits: the blocks exchange their smallest and largest candidate, and every key is shifted
+// left past the bits all candidates share (bit 0 set so that no candidate becomes 0; order
+// and ties are unchanged), so the histogram levels of the cluster selection spread the
+// candidates instead of piling them onto a few counters.  The cluster then selects the K best
+// exactly as the indexer scan's cluster does, and each block writes its share of the row's
+// positions at its offset.
 constexpr int kMergeWarps = 12;
 constexpr int kMergeThreads = kMergeWarps * 32;
-constexpr size_t kMergeSmemMax = 200u * 1024u;
+constexpr int kMergeMaxCta = 8;
 
-__global__ void __launch_bounds__(kMergeThreads, 1) lists_merge_kernel(const FeedParams p) {
-  extern __shared__ __align__(16) uint32_t kv[];  // [in_seg * in_K]
+struct MergeShared {
+  int cnt[64];
+  uint32_t thr[64];
+  uint32_t kext[2 + 2 * kMergeMaxCta];  // this block's extremes; block 0: every block's
+};
+
+__global__ void __launch_bounds__(kMergeThreads, 1) lists_merge_kernel(const FeedParams p, int seg_per_cta) {
+  extern __shared__ __align__(16) uint8_t msm[];
   __shared__ ArrSelShared sh;
-  __shared__ int32_t sel_f[CSA2_MAX_TOPK];
-  __shared__ uint32_t kext[2];  // smallest and largest candidate key
+  __shared__ MergeShared ms;
+  const int row = blockIdx.y, S = p.in_seg, Kin = p.in_K, K = p.K;
+  const uint32_t rank = cluster_rank(), n_cta = gridDim.x;
+  const int sg0 = min(S, (int)rank * seg_per_cta), sg1 = min(S, sg0 + seg_per_cta);
+  const int n_here = (sg1 - sg0) * Kin, cap = seg_per_cta * Kin;
+  // every region starts on a 16-byte boundary (the lists' room takes 16-byte stores)
+  uint32_t* keys = reinterpret_cast<uint32_t*>(msm);                    // [cap, padded to 4]
+  int32_t* sel_idx = reinterpret_cast<int32_t*>(keys + ((cap + 3) & ~3));  // [K, padded to 4]
   ArrSel<kMergeWarps> s;
   s.sh = &sh;
   s.tid = threadIdx.x;
-  const int row = blockIdx.x, S = p.in_seg, Kin = p.in_K, K = p.K;
-  const int w = s.warp(), ln = s.lane();
-  int* cnt = reinterpret_cast<int*>(sh.aux);  // [S <= 64]
-  uint32_t* thr_s = sh.aux + 64;
+  s.scratch = reinterpret_cast<uint32_t*>(sel_idx + ((K + 3) & ~3));  // lists, 16-byte aligned
+  const int ln = s.lane();
   for (int i = s.tid; i < S; i += kMergeThreads) {
-    cnt[i] = min(__ldcg(p.in_cnt + (size_t)row * S + i), Kin);
-    thr_s[i] = p.in_thr ? __ldcg(p.in_thr + (size_t)row * S + i) : 0u;
+    ms.cnt[i] = min(__ldcg(p.in_cnt + (size_t)row * S + i), Kin);
+    ms.thr[i] = p.in_thr ? __ldcg(p.in_thr + (size_t)row * S + i) : 0u;
   }
-  if (s.tid == 0) kext[0] = 0xffffffffu, kext[1] = 0u;
+  if (s.tid < 2) ms.kext[s.tid] = s.tid == 0 ? 0xffffffffu : 0u;
   s.zero_hist(kHistBins);
   s.sync();
   uint32_t thr0 = 0u;
-  for (int i = 0; i < S; ++i) thr0 = max(thr0, thr_s[i]);
-  const int n = S * Kin;
-  const uint32_t* gk = p.in_keys + (size_t)row * n;
+  for (int i = 0; i < S; ++i) thr0 = max(thr0, ms.thr[i]);
+  const uint32_t* gk = p.in_keys + ((size_t)row * S + sg0) * Kin;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  auto filt = [&](uint32_t key, int sg, int j) -> uint32_t {
-    key = (j < cnt[sg] && key >= thr0) ? key : 0u;
+  auto stage = [&](uint32_t key, int i) -> uint32_t {
+    const int sg = sg0 + i / Kin, j = i - (sg - sg0) * Kin;
+    key = (j < ms.cnt[sg] && key >= thr0) ? key : 0u;
     if (key) kmin = min(kmin, key), kmax = max(kmax, key);
     return key;
   };
-  if ((Kin & 3) == 0) {
+  if ((Kin & 3) == 0) {  // the lists' rows are 16-byte aligned
     const uint4* g4 = reinterpret_cast<const uint4*>(gk);
-    uint4* s4 = reinterpret_cast<uint4*>(kv);
-#pragma unroll 4
-    for (int i = s.tid; i < n / 4; i += kMergeThreads) {
+#pragma unroll 2
+    for (int i = s.tid; i < n_here / 4; i += kMergeThreads) {
       uint4 v = __ldcg(g4 + i);
-      const int sg = (4 * i) / Kin, j = 4 * i - sg * Kin;
-      v.x = filt(v.x, sg, j), v.y = filt(v.y, sg, j + 1), v.z = filt(v.z, sg, j + 2), v.w = filt(v.w, sg, j + 3);
-      s4[i] = v;
+      v.x = stage(v.x, 4 * i), v.y = stage(v.y, 4 * i + 1), v.z = stage(v.z, 4 * i + 2), v.w = stage(v.w, 4 * i + 3);
+      reinterpret_cast<uint4*>(keys)[i] = v;
     }
   } else {
 #pragma unroll 4
-    for (int i = s.tid; i < n; i += kMergeThreads) kv[i] = filt(__ldcg(gk + i), i / Kin, i % Kin);
+    for (int i = s.tid; i < n_here; i += kMergeThreads) keys[i] = stage(__ldcg(gk + i), i);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
-  if (ln == 0 && kmax != 0u) atomicMin(&kext[0], kmin), atomicMax(&kext[1], kmax);
+  if (ln == 0 && kmax != 0u) atomicMin(&ms.kext[0], kmin), atomicMax(&ms.kext[1], kmax);
   s.sync();
-  kmin = kext[0], kmax = kext[1];
-  // bits above d are common to every candidate
+  // every block's extremes into block 0, then every block reads them all
+  if (s.tid < 2) cluster_st_s32(cluster_map(&ms.kext[2 + 2 * rank + s.tid], 0), (int)ms.kext[s.tid]);
+  cluster_sync();
+  kmin = 0xffffffffu, kmax = 0u;
+  for (uint32_t c = 0; c < n_cta; ++c) {
+    const uint32_t lo = (uint32_t)cluster_ld_s32(cluster_map(&ms.kext[2 + 2 * c], 0));
+    const uint32_t hi = (uint32_t)cluster_ld_s32(cluster_map(&ms.kext[3 + 2 * c], 0));
+    if (hi != 0u) kmin = min(kmin, lo), kmax = max(kmax, hi);
+  }
+  // the bits above d are common to every candidate: shift them out
   const int d = kmax > kmin ? 31 - __clz(kmin ^ kmax) : 0;
-  const int s1 = max(d - 11, 0), s2 = max(s1 - 12, 0);
-  const uint32_t m1 = (2u << (d - s1)) - 1u;
-  for (int i = s.tid; i < n; i += kMergeThreads) {
-    const uint32_t key = kv[i];
-    if (key) atomicAdd(&sh.hist[(key >> s1) & m1], 1);
+  const int shl = kmax != 0u ? 31 - d : 0;
+  for (int i = s.tid; i < n_here; i += kMergeThreads) {
+    uint32_t key = keys[i];
+    if (key != 0u && shl > 0) key = (key << shl) | 1u;
+    keys[i] = key;
+    if (key != 0u) atomicAdd(&sh.hist[key >> 20], 1);
   }
   s.sync();
-  s.template pick<kHistBins>(K);
-  uint32_t thr = 0u;
-  int n_eq = 0;
-  if (sh.total > K) {
-    // T: the threshold's bits above the current shift
-    uint32_t T = ((kmax >> s1) & ~m1) | (uint32_t)sh.bin;
-    int need = K - sh.before;
-    if (s1 > 0) {
-      const uint32_t m2 = (1u << (s1 - s2)) - 1u;
-      s.sync();
-      s.zero_hist(kHistBins);
-      s.sync();
-      for (int i = s.tid; i < n; i += kMergeThreads) {
-        const uint32_t key = kv[i];
-        if (key && (key >> s1) == T) atomicAdd(&sh.hist[(key >> s2) & m2], 1);
-      }
-      s.sync();
-      s.template pick<kHistBins>(need);
-      T = (T << (s1 - s2)) | (uint32_t)sh.bin;
-      need -= sh.before;
-      if (s2 > 0) {
-        const uint32_t m3 = (1u << s2) - 1u;  // s2 <= 8
-        s.sync();
-        s.zero_hist(256);
-        s.sync();
-        for (int i = s.tid; i < n; i += kMergeThreads) {
-          const uint32_t key = kv[i];
-          if (key && (key >> s2) == T) atomicAdd(&sh.hist[key & m3], 1);
-        }
-        s.sync();
-        s.template pick<256>(need);
-        T = (T << s2) | (uint32_t)sh.bin;
-        need -= sh.before;
-      }
-    }
-    thr = T;
-    n_eq = need;
+  arr_threshold_impl(s, keys, n_here, K, true, ClusterPick<kMergeWarps>{rank, n_cta, cap});
+  int base = 0, total = 0, kept = 0;
+  if (sh.thr == 0u) {
+    kept = arr_compact_cluster(s, n_here, sel_idx, rank, n_cta, &base, &total);
+  } else {
+    base = (int)sh.aux[2];
+    total = (int)sh.aux[4];
+    kept = arr_compact(s, n_here, sel_idx);
   }
-  // warp w: slots [f0, f1) of whole segments, in order
-  const int f0 = (int)(((long long)S * w) / kMergeWarps) * Kin, f1 = (int)(((long long)S * (w + 1)) / kMergeWarps) * Kin;
-  int gt = 0, eq = 0;
-  for (int f = f0 + ln; f < f1; f += 32) {
-    const uint32_t key = kv[f];
-    gt += key != 0u && key > thr;
-    eq += key != 0u && key == thr;
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  }
-  // gt <= K in every warp and in sum; equal keys beyond K per warp never change what is taken,
-  // so clamping keeps both halves of the packed scan below 2^16
-  eq = min(eq, K);
-  int tot_packed;
-  const int before = s.scan(ln == 0 ? (gt << 16) | eq : 0, &tot_packed);
-  const int pb = __shfl_sync(0xffffffffu, before, 0);
-  const int eq_b = pb & 0xffff;
-  const int take = max(0, min(eq, n_eq - eq_b));
-  int base = (pb >> 16) + min(eq_b, n_eq);
-  const int kept = min(K, (tot_packed >> 16) + min(tot_packed & 0xffff, n_eq));
-  int eq_seen = 0;
-  const unsigned lt = lanemask_lt();
-  for (int f0r = f0; f0r < f1; f0r += 32) {  // warp-uniform trip count
-    const int f = f0r + ln;
-    const uint32_t key = f < f1 ? kv[f] : 0u;
-    const bool is_eq = key != 0u && key == thr;
-    const unsigned em = __ballot_sync(0xffffffffu, is_eq);
-    const bool keep = key != 0u && (key > thr || (is_eq && eq_seen + __popc(em & lt) < take));
-    const unsigned km = __ballot_sync(0xffffffffu, keep);
-    const int r = base + __popc(km & lt);
-    if (keep && r < K) sel_f[r] = f;
-    base += __popc(km);
-    eq_seen += __popc(em);
-  }
-  s.sync();
-  const int32_t* pos = p.in_pos + (size_t)row * n;
+  const int32_t* pos = p.in_pos + ((size_t)row * S + sg0) * Kin;
   int32_t* out = p.idx + (size_t)row * K;
-  for (int r = s.tid; r < K; r += kMergeThreads) out[r] = r < kept ? __ldcg(pos + sel_f[r]) : -1;
+  for (int r = s.tid; r < kept; r += kMergeThreads)
+    if (base + r < K) out[base + r] = __ldcg(pos + sel_idx[r]);
+  if (rank == n_cta - 1)
+    for (int r = total + s.tid; r < K; r += kMergeThreads) out[r] = -1;
+  // (the selection's last cluster barrier follows every access to another block's shared
+  // memory, so the blocks may leave independently)
+}
+
+size_t merge_smem_bytes(int seg_per_cta, int Kin, int K) {
+  const int cap = seg_per_cta * Kin;
+  // the lists' room doubles as the cluster histogram sum (4096 words)
+  return (size_t)((cap + 3) & ~3) * 4 + (size_t)((K + 3) & ~3) * 4 +
+         (size_t)std::max(ArrSel<kMergeWarps>::list_words(cap), kHistBins) * 4;
 }
 
 }  // namespace
 
 cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
-  const size_t smem = (size_t)p.in_seg * p.in_K * sizeof(uint32_t);
-  if (p.in_seg > 64 || p.K > CSA2_MAX_TOPK || smem > kMergeSmemMax)
+  const int n_cta = std::min(kMergeMaxCta, std::max(2, p.in_seg));
+  const int per = (p.in_seg + n_cta - 1) / n_cta;
+  const size_t smem = merge_smem_bytes(per, p.in_K, p.K);
+  if (p.in_seg > 64 || p.K > CSA2_MAX_TOPK || per * p.in_K >= 65536 || smem > 160u * 1024u)
     return launch_topk_feed(p, true, 1, stream);  // beyond the staged segment table or shared memory
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(lists_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmemMax);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  lists_merge_kernel<<<p.n_rows, kMergeThreads, smem, stream>>>(p);
+  cudaError_t e = cudaFuncSetAttribute(lists_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_cta, p.n_rows);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)n_cta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lists_merge_kernel, p, per);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
