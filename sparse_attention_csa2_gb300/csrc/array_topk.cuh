@@ -178,40 +178,13 @@ template <int NW>
 struct ClusterPick {
   uint32_t rank, n_cta;
   int local_cap;  // capacity of block 0's key array (words) for the keys of bin b1
-  // Level 1.  Up to 8 blocks: every block sums the whole histogram over the cluster into its
-  // scratch (free until the list pass) and picks on its own, all to the same bin, with one
-  // cluster barrier; the blocks' histograms stay untouched until a later barrier (block 0
-  // reuses its own only after the refine's first one).  More blocks: every block adds one
-  // slice of the bins into block 0's histogram, block 0 picks and writes bin / before /
-  // total into every block.
+  // Level 1: every block adds one slice of the bins over the cluster into block 0's
+  // histogram, block 0 picks and writes bin / before / total into every block.
   template <int NBINS>
   __device__ __forceinline__ void run(const ArrSel<NW>& s, int need) const {
     constexpr int NT = NW * 32;
     ArrSelShared& sh = *s.sh;
     cluster_sync();  // every block's histogram is final
-    if (n_cta <= 8) {
-      int* sum = reinterpret_cast<int*>(s.scratch);
-#pragma unroll 1
-      for (int i = s.tid; i < NBINS / 4; i += NT) {
-        // all the blocks' loads in flight before the first add
-        uint4 v[8];
-#pragma unroll
-        for (uint32_t c = 0; c < 8; ++c)
-          v[c] = c < n_cta ? cluster_ld_v4(cluster_map(&sh.hist[4 * i], c)) : make_uint4(0u, 0u, 0u, 0u);
-        uint4 acc = v[0];
-#pragma unroll
-        for (int c = 1; c < 8; ++c) {
-          acc.x += v[c].x;
-          acc.y += v[c].y;
-          acc.z += v[c].z;
-          acc.w += v[c].w;
-        }
-        *reinterpret_cast<uint4*>(sum + 4 * i) = acc;
-      }
-      s.sync();
-      s.template pick<NBINS>(need, sum);
-      return;
-    }
     const int n_v4 = NBINS / 4, per = (n_v4 + (int)n_cta - 1) / (int)n_cta;
     const int lo = (int)rank * per, hi = min(n_v4, lo + per);
 #pragma unroll 1
