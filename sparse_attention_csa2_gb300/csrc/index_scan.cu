@@ -10,7 +10,10 @@
 // The indexer query is held in registers as B fragments for the whole scan.  The 128 dims
 // are consumed in a permuted order chosen so that each thread's 16-byte copies are the
 // exact A-fragment words it needs; q uses the same permutation, so the dot products are
-// unchanged.  FP8 keys are widened to bf16 in registers (exact) and their row scale is
+// unchanged.  FP8 keys are widened to f16 in registers by one hardware conversion per pair
+// (exact) and meet q^I widened once to f16 (exact for every element within ~2^-38 of its
+// head's largest: each head is scaled by the power of two that puts its largest element in
+// [2^14, 2^15), the inverse factor going into the head weight); the record's row scale is
 // applied to each head's dot product before the ReLU.
 #include "select.cuh"
 #include "kernels.h"
@@ -99,6 +102,34 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
     wv[nt][0] = __ldg(p.w + (size_t)row * kIdxHeads + 8 * nt + 2 * c);
     wv[nt][1] = __ldg(p.w + (size_t)row * kIdxHeads + 8 * nt + 2 * c + 1);
   }
+  if (FP8) {
+    // q^I to f16: the four lanes of a group hold head 8nt+g's 128 dims between them
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) mx = max(mx, max(qf[s][nt][h2] & 0x7fffu, (qf[s][nt][h2] >> 16) & 0x7fffu));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const int ex = (int)((mx >> 7) & 0xffu) - 127;
+      const int e = mx == 0u ? 0 : min(126, max(-126, 14 - ex));
+      const float f = __int_as_float((e + 127) << 23);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t v = qf[s][nt][h2];
+          const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16) * f, __uint_as_float(v & 0xffff0000u) * f);
+          qf[s][nt][h2] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+      // this lane's accumulator columns are heads 8nt+2c and 8nt+2c+1 (groups 2c, 2c+1)
+      const int e0 = __shfl_sync(0xffffffffu, e, 8 * c), e1 = __shfl_sync(0xffffffffu, e, 8 * c + 4);
+      wv[nt][0] *= __int_as_float((127 - e0) << 23);
+      wv[nt][1] *= __int_as_float((127 - e1) << 23);
+    }
+  }
 
   const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_idx);
   const size_t seq_off = (size_t)b * (size_t)p.N;
@@ -166,12 +197,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
 #pragma unroll
             for (int jw = 0; jw < 4; ++jw) {
               const int s = 4 * i + jw;
-              const uint32_t a0 = e4m3x2_to_bf16x2((uint16_t)(w0v[jw] & 0xffffu));
-              const uint32_t a2 = e4m3x2_to_bf16x2((uint16_t)(w0v[jw] >> 16));
-              const uint32_t a1 = e4m3x2_to_bf16x2((uint16_t)(w1v[jw] & 0xffffu));
-              const uint32_t a3 = e4m3x2_to_bf16x2((uint16_t)(w1v[jw] >> 16));
+              const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(w0v[jw] & 0xffffu));
+              const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(w0v[jw] >> 16));
+              const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(w1v[jw] & 0xffffu));
+              const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(w1v[jw] >> 16));
 #pragma unroll
-              for (int nt = 0; nt < 4; ++nt) mma_bf16(acc[nt], a0, a1, a2, a3, qf[s][nt][0], qf[s][nt][1]);
+              for (int nt = 0; nt < 4; ++nt) mma_f16(acc[nt], a0, a1, a2, a3, qf[s][nt][0], qf[s][nt][1]);
             }
           }
         } else {
