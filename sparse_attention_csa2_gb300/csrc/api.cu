@@ -399,10 +399,10 @@ csa2_status csa2_block_pool(const csa2_block_pool_args* a, void* stream) {
   f.n_valid = a->n_visible;
   f.valid_div = a->block_size;
   f.idx = kept;
-  cudaError_t e = launch_topk_feed(f, false, 1, s);
-  if (e != cudaSuccess) return CSA2_ECUDA;
-  return cuda_status(launch_pool_expand(kept, a->n_visible, a->n_rows, a->n_keep, a->block_size, a->pool,
-                                        a->n_pool, s));
+  f.pool = a->pool;
+  f.n_pool = a->n_pool;
+  f.pool_bs = a->block_size;
+  return cuda_status(launch_topk_feed(f, false, 1, s));
 }
 
 // ---------------------------------------------------------------------- sparse attention
@@ -561,9 +561,10 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       f.n_valid = ix->n_visible;
       f.valid_div = a->block_size;
       f.idx = kept;
-      e = launch_topk_feed(f, false, 1, s);
-      if (e != cudaSuccess) return CSA2_ECUDA;
-      e = launch_pool_expand(kept, ix->n_visible, n_rows, a->n_keep, a->block_size, a->pool, a->n_pool, s);
+      f.pool = a->pool;
+      f.n_pool = a->n_pool;
+      f.pool_bs = a->block_size;
+      e = launch_topk_feed(f, false, 1, s);  // block selection and the pool's positions
       if (e != cudaSuccess) return CSA2_ECUDA;
     }
   }
@@ -593,7 +594,7 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
                                   mma_decode_cluster_ok(n_seg, a->attn.n_rows, a->K, seg_blocks, ic.k_dtype == CSA2_FP8_E4M3_ROWSCALE)) ||
                                  mma_decode_can_merge(n_seg, a->K));
     n += 1 + (n_seg > 1 && !merged ? 1 : 0);  // the tcgen05 scan merges its segments itself
-    if (a->mode == CSA2_MODE_FULL_POOL) n += 2;
+    if (a->mode == CSA2_MODE_FULL_POOL) n += 1;  // block selection writing the pool
   }
   n += 2;  // attention tiles and their merge
   return n;

@@ -78,6 +78,12 @@ struct FeedParams {
   int in_K;
   // output: final idx [n_rows, K] (out_seg == 1) or lists [n_rows, out_seg, K]
   int32_t* idx;
+  // optional, source A with out_seg == 1: the kept entries are blocks of pool_bs positions
+  // (n_valid counts positions) and expand to pool [n_rows, K * pool_bs] (-1 past the visible
+  // positions and for missing blocks) with n_pool [n_rows] valid positions
+  int32_t* pool;
+  int32_t* n_pool;
+  int pool_bs;
   uint32_t* out_keys;
   int32_t* out_pos;
   int32_t* out_cnt;
@@ -88,9 +94,6 @@ size_t feed_smem_bytes(int K);
 int topk_segments(int n_rows, long long L);  // segments csa2_topk splits each row into
 cudaError_t launch_topk_feed(const FeedParams& p, bool from_lists, int out_seg, cudaStream_t stream);
 cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream);  // segment lists -> final idx
-cudaError_t launch_pool_expand(const int32_t* kept, const int32_t* n_visible, int n_rows, int n_keep,
-                               int block_size, int32_t* pool, int32_t* n_pool, cudaStream_t stream);
-
 struct AttnParams {
   const void* q;
   const int64_t* q_pos;

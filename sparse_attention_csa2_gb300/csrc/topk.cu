@@ -92,8 +92,30 @@ __global__ void __launch_bounds__(kFeedThreads, 1) topk_feed_kernel(const FeedPa
     return j;
   };
   if (n_seg == 1) {
-    int32_t* out = p.idx + (size_t)row * p.K;
-    for (int i = threadIdx.x; i < p.K; i += kFeedThreads) out[i] = i < n ? position(e.out_j[i]) : -1;
+    if (p.idx) {
+      int32_t* out = p.idx + (size_t)row * p.K;
+      for (int i = threadIdx.x; i < p.K; i += kFeedThreads) out[i] = i < n ? position(e.out_j[i]) : -1;
+    }
+    if (!FROM_LISTS && p.pool) {
+      // Kept blocks, ascending, to their positions.  Only the block holding the last visible
+      // position can be partial, and it has the largest id of all blocks, so the visible
+      // positions of the kept blocks form a prefix of the pool.
+      const int bs = p.pool_bs;
+      const long long nv = p.n_valid[row];
+      int32_t* pr = p.pool + (size_t)row * p.K * bs;
+      for (long long i = threadIdx.x; i < (long long)p.K * bs; i += kFeedThreads) {
+        const int r = (int)(i / bs);
+        const long long blk = r < n ? position(e.out_j[r]) : -1;
+        long long pos = blk >= 0 ? blk * bs + i % bs : -1;
+        if (pos >= nv) pos = -1;
+        pr[i] = (int32_t)pos;
+      }
+      if (threadIdx.x == 0) {
+        long long np = 0;
+        if (n > 0) np = (long long)(n - 1) * bs + min((long long)bs, nv - (long long)position(e.out_j[n - 1]) * bs);
+        p.n_pool[row] = (int32_t)np;
+      }
+    }
   } else {
     const size_t o = ((size_t)row * n_seg + seg) * p.K;
     for (int i = threadIdx.x; i < n; i += kFeedThreads) {
@@ -101,33 +123,6 @@ __global__ void __launch_bounds__(kFeedThreads, 1) topk_feed_kernel(const FeedPa
       p.out_pos[o + i] = position(e.out_j[i]);
     }
     if (threadIdx.x == 0) p.out_cnt[(size_t)row * n_seg + seg] = n;
-  }
-}
-
-// kept[row] = ascending kept block ids (-1 padded).  Only the block holding the last visible
-// position can be partial, and it has the largest id of all blocks, so the visible positions
-// of the kept blocks form a prefix of the pool.
-__global__ void pool_expand_kernel(const int32_t* __restrict__ kept, const int32_t* __restrict__ n_visible,
-                                   int n_keep, int bs, int32_t* __restrict__ pool, int32_t* __restrict__ n_pool) {
-  const int row = blockIdx.x;
-  const long long nv = n_visible[row];
-  const int32_t* kr = kept + (size_t)row * n_keep;
-  int32_t* pr = pool + (size_t)row * n_keep * bs;
-  for (long long i = threadIdx.x; i < (long long)n_keep * bs; i += blockDim.x) {
-    const int blk = kr[i / bs];
-    long long pos = blk >= 0 ? (long long)blk * bs + i % bs : -1;
-    if (pos >= nv) pos = -1;
-    pr[i] = (int32_t)pos;
-  }
-  if (threadIdx.x == 0) {
-    int nk = 0;
-    while (nk < n_keep && kr[nk] >= 0) ++nk;
-    long long n = 0;
-    if (nk > 0) {
-      const long long last = kr[nk - 1];
-      n = (long long)(nk - 1) * bs + min((long long)bs, nv - last * bs);
-    }
-    n_pool[row] = (int32_t)n;
   }
 }
 
@@ -298,11 +293,5 @@ cudaError_t launch_topk_feed(const FeedParams& p, bool from_lists, int out_seg, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_pool_expand(const int32_t* kept, const int32_t* n_visible, int n_rows, int n_keep,
-                               int block_size, int32_t* pool, int32_t* n_pool, cudaStream_t stream) {
-  if (n_rows == 0) return cudaSuccess;
-  pool_expand_kernel<<<n_rows, 256, 0, stream>>>(kept, n_visible, n_keep, block_size, pool, n_pool);
-  return cudaGetLastError();
-}
 
 }  // namespace csa2
