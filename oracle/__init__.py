@@ -28,3 +28,4 @@ values the pages print, closed forms, library routines or brute force; no
 function here is "parity unpinned".
 """
 from .csa2 import *  # noqa: F401,F403
+from .writer import *  # noqa: F401,F403

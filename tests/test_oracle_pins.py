@@ -94,6 +94,95 @@ def test_fp8_row_scale():
     assert v.tolist() == [[0.25, -0.25, 112.0]]
 
 
+# ================================================================ cache writer
+def test_writer_e4m3_rounding_matches_torch():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(100_000) * rng.choice([1e-3, 1.0, 100.0], 100_000)).astype(np.float32)
+    x = np.concatenate([x, np.float32([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, -(2.0 ** -10), 464.0, 1000.0])])
+    ref = torch.from_numpy(x).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_round(x), ref)
+
+
+def test_writer_e2m1_page_example_levels_and_ties():
+    g = gold("fp4_course_lesson.json")
+    # the lesson's example: 3.2 at scale 1 stores level 3 and reads back 3.0 (error -0.2)
+    c = O.e2m1_round(np.float32([3.2]))
+    assert O.e2m1_to_f64(c)[0] == g["store_3p2_scale1_level"]
+    assert abs(float(O.e2m1_to_f64(c)[0]) - 3.2 - (-0.2)) < 1e-6
+    # every level is its own code, with either sign
+    lev = np.float32(g["e2m1_magnitudes"])
+    assert np.array_equal(O.e2m1_to_f64(O.e2m1_round(lev)), lev)
+    assert np.array_equal(O.e2m1_to_f64(O.e2m1_round(-lev[1:])), -lev[1:])
+    # midpoints go to the even code; beyond 6 saturates
+    mids = np.float32([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 9.0])
+    assert O.e2m1_to_f64(O.e2m1_round(mids)).tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0]
+    # nearest level off the midpoints (brute force)
+    q = np.linspace(-7, 7, 2801).astype(np.float32)
+    q = q[~np.isin(np.abs(q), mids)]
+    got = O.e2m1_to_f64(O.e2m1_round(q))
+    allv = np.concatenate([lev, -lev])
+    ref = allv[np.argmin(np.abs(q[:, None].astype(np.float64) - allv[None, :]), axis=1)]
+    assert np.array_equal(got, ref)
+
+
+def test_writer_fp4_scale_rule_and_error_bound():
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((64, 512)) * np.exp2(rng.integers(-12, 8, (64, 1)))).astype(np.float32)
+    x[3] = 0.0
+    for group in (16, 32):
+        codes, scodes = O.fp4_quantize(x, group)
+        assert codes.shape == (64, 256) and scodes.shape == (64, 512 // group)
+        amax = np.abs(x.reshape(64, -1, group)).max(-1).astype(np.float64)
+        sval = O.e4m3_to_f64(scodes)
+        prev = O.e4m3_to_f64(np.maximum(scodes.astype(np.int64) - 1, 0).astype(np.uint8))
+        s = (amax.astype(np.float32) / np.float32(6.0)).astype(np.float64)
+        # the smallest E4M3 value at or above amax / 6
+        assert np.all(sval >= s) and np.all((scodes == 0) | (prev < s))
+        deq = O.fp4_to_f64(codes, scodes, group)
+        # no clipping; every value within half a level step of the scaled grid (step <= 2)
+        err = np.abs(deq - x.astype(np.float64)).reshape(64, -1, group)
+        assert np.all(err <= sval[..., None] * 1.0 + 1e-30)
+        assert np.all(deq[3] == 0.0)
+        # groups on an exact grid (level x scale, one element at +-6 x scale, so the group's
+        # scale is that scale) come back code for code
+        sc = rng.integers(8, 110, (64, 512 // group)).astype(np.uint8)
+        lv = rng.integers(0, 16, (64, 512)).astype(np.uint8)
+        lv[lv == 8] = 0  # no negative zero
+        lv.reshape(64, -1, group)[..., 0] = rng.choice([7, 15], (64, 512 // group))
+        grid = (O.e2m1_to_f64(lv) * np.repeat(O.e4m3_to_f64(sc), group, -1)).astype(np.float32)
+        c2, s2 = O.fp4_quantize(grid, group)
+        assert np.array_equal(s2, sc)
+        assert np.array_equal(c2, (lv[:, 0::2] | (lv[:, 1::2] << 4)).astype(np.uint8))
+
+
+def test_writer_fp8_rows_round_trip():
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal((32, 512)) * 3).astype(np.float32)
+    x[5] = 0.0
+    codes, scale = O.fp8_quantize_rows(x)
+    assert np.array_equal(scale[5:6], np.float32([1.0]))
+    assert np.allclose(scale[:5], np.abs(x[:5]).max(-1) / 448, rtol=1e-7)
+    deq = O.fp8_rows_to_f64(codes, scale)
+    # relative error of E4M3 (3 mantissa bits) at most 2^-4 of each value, plus the subnormal step
+    assert np.all(np.abs(deq - x) <= np.abs(x) * 2.0 ** -4 + scale[:, None] * 2.0 ** -10)
+    assert np.all((codes[:5] & 0x7F).max(-1) == 0x7E)  # each row's largest magnitude is 448
+
+
+def test_writer_rotation_is_rope_in_float32():
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((8, 512)).astype(np.float32)
+    pos = np.array([0, 1, 7, 100, 4095, 65536, 1_000_000, 2_000_000])
+    r = O.rotate_f32(x, pos, 10000.0)
+    ref = np.stack([O.rope(x[i].astype(np.float64), int(pos[i]), 10000.0, 64) for i in range(8)])
+    assert np.array_equal(r[:, :448], x[:, :448])
+    assert np.allclose(r, ref, rtol=0, atol=1e-5)
+    assert np.array_equal(r[0], x[0])  # position 0 turns nothing
+    # float32 products and sums exactly as written
+    c = np.cos(np.float64(100) * 10000.0 ** (-2.0 * 3 / 64)).astype(np.float32)
+    sn = np.sin(np.float64(100) * 10000.0 ** (-2.0 * 3 / 64)).astype(np.float32)
+    assert r[3, 454] == (x[3, 454] * c) - (x[3, 455] * sn)
+
+
 # ================================================================ indexer score
 def test_index_score_hand_case():
     q = np.array([[1.0, 2.0], [-1.0, 0.0]])
