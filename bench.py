@@ -365,6 +365,42 @@ def run_scan_only(args, local):
     return {"fmt": fmt, "rows": rows, "records": n, "ms": ms, "key_gbs": rows * n * rec / (ms / 1e3) / 1e9}
 
 
+def run_writer(local, peaks, n=262144, iters=20):
+    """Cache writer: n records (float32, before rotation) rotated by their positions and
+    written to an FP4 (E2M1, E4M3 scale per 16) cache and to an FP8-row cache at scattered
+    rows; bytes = records read + codes, scales, positions and rows; median of CUDA-event
+    times after 3 calls."""
+    import torch
+    import sparse_attention_csa2_gb300 as S
+    dev = f"cuda:{local}"
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(n, 512, generator=g).to(dev)
+    pos = torch.randint(0, 1 << 20, (n,), generator=g).to(dev)
+    dst = torch.randperm(n, generator=g).to(dev)
+    hbm = float(peaks.get("hbm_gbs", 6800.0)) if peaks else 6800.0
+    out = {}
+    for name, codes, scales, dt, wbytes in (
+            ("fp4_g16", torch.empty(n, 256, dtype=torch.uint8, device=dev),
+             torch.empty(n, 32, dtype=torch.uint8, device=dev), S.FP4_E2M1_G16, 256 + 32),
+            ("fp8_rows", torch.empty(n, 512, dtype=torch.uint8, device=dev),
+             torch.empty(n, dtype=torch.float32, device=dev), S.FP8_E4M3_ROWSCALE, 512 + 4)):
+        call = lambda: S.write_records(x, dst, codes, scales, dt, pos=pos)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for e0, e1 in ev:
+            e0.record()
+            call()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        nbytes = n * (512 * 4 + 8 + 8 + wbytes)
+        out[name] = {"records": n, "ms": ms, "records_per_s": n / (ms / 1e3), "gbs": nbytes / (ms / 1e3) / 1e9,
+                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
+    return out
+
+
 def run_prefill(args, local, peaks):
     """Prefill chunk (B=1, T=4096 queries at positions 32768.., N=36864 bf16 keys): the
     indexer GEMM on the tensor cores alone, then the whole chunk (scores -> per-query top-512
@@ -557,6 +593,7 @@ def run_gb300(args, world, rank, local):
         prefill = run_prefill(args, local, peaks if peak_src == "measured" else None)
     if not args.no_configs:
         configs = run_configs(local, peaks if peak_src == "measured" else None)
+        configs["cache_writer"] = run_writer(local, peaks if peak_src == "measured" else None)
 
     cpu = None
     if not args.no_cpu_baseline:

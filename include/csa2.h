@@ -285,6 +285,43 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a);
 csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Cache writer: appends records to a main-KV (latent) cache or a sliding-window cache in its
+ * storage format.  Each record's rotary coordinates (dims 448..511, pairs (448+2i, 449+2i),
+ * frequencies theta^(-2i/64)) are turned by its position first, since the cache holds
+ * rotated values and is quantized after RoPE (course, FP4 lesson, section 4, "Quantize after
+ * RoPE"); then:
+ *   FP4 (CSA2_FP4_E2M1_G16 / _G32): per group of 16 / 32 channels the E4M3 scale is the
+ *     smallest E4M3 value >= amax / 6 (so no element clips; saturating at 448), and each
+ *     value / scale rounds to the nearest E2M1 level, ties to the even code; codes two per
+ *     byte, low nibble = even channel ("DeepSeek-V4.1-Flash explained", section 7: one E4M3
+ *     scale per 16 channels; the scale selection itself is not described by the pages);
+ *   FP8 (CSA2_FP8_E4M3_ROWSCALE): one fp32 scale amax / 448 per row (1 for an all-zero row),
+ *     codes = E4M3(value / scale), round to nearest even (the local cache stays FP8, same
+ *     lesson, section 4).
+ * Every decision (divisions, the rotation's products and sums) is taken in IEEE float32; the
+ * rotation's cos and sin are computed in double and rounded to float.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int64_t n_rows;             /* records to write */
+  const void* x;              /* [n_rows, 512] values before rotation: float32 (x_f32 = 1) or bf16 */
+  int32_t x_f32;
+  const int64_t* pos;         /* [n_rows] position of each record, or NULL: no rotation */
+  float rope_theta;
+  const int64_t* dst_row;     /* [n_rows] row of the cache written (sequence * N + position for a
+                                 [seq, N, ...] cache); rows outside [0, cache_rows) are skipped
+                                 and reported through dev_status */
+  int64_t cache_rows;
+  int32_t out_dtype;          /* CSA2_FP4_E2M1_G16, CSA2_FP4_E2M1_G32 or CSA2_FP8_E4M3_ROWSCALE */
+  void* codes;                /* [cache_rows, 256] (FP4) or [cache_rows, 512] (FP8) uint8 */
+  void* scales;               /* FP4: [cache_rows, 512 / G] E4M3 uint8; FP8: [cache_rows] float32 */
+  int32_t* dev_status;        /* optional device int32: CSA2_EDEVICE_INDEX on a skipped row */
+} csa2_write_args;
+
+/* All pointers device, 16-byte aligned (pos, dst_row and FP8 scales: 8 / 8 / 4).  Rows are
+ * written in any order; two records with the same dst_row leave either one. */
+csa2_status csa2_write_records(const csa2_write_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Utilities
  * ------------------------------------------------------------------------------------ */
 const char* csa2_status_string(csa2_status s);

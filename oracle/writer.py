@@ -95,7 +95,10 @@ def fp8_quantize_rows(x):
 def rotate_f32(x, pos, theta: float, R: int = 64):
     """RoPE of the last R coordinates of float32 record(s) [..., D] at positions pos [...]:
     pair i = (D-R+2i, D-R+2i+1) turns by pos * theta^(-2i/R); cos and sin in float64,
-    rounded to float32; each product and sum in float32."""
+    rounded to float32; each product and sum in float32.  (The float64 cos and sin may
+    differ from another implementation's in the last bit; the float32 values they round to
+    then differ only when a value lies within 1e-16 relative of a float32 rounding
+    boundary.)"""
     x = np.array(x, np.float32, copy=True)
     D = x.shape[-1]
     i = np.arange(R // 2, dtype=np.float64)

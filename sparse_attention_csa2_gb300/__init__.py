@@ -71,6 +71,12 @@ class DecodeArgs(C.Structure):
                 ("stage_events", _vp * 4)]
 
 
+class WriteArgs(C.Structure):
+    _fields_ = [("n_rows", _i64), ("x", _vp), ("x_f32", _i32), ("pos", _vp), ("rope_theta", _f32),
+                ("dst_row", _vp), ("cache_rows", _i64), ("out_dtype", _i32), ("codes", _vp), ("scales", _vp),
+                ("dev_status", _vp)]
+
+
 def _sig(name, argtypes, restype):
     f = getattr(_lib, name)
     f.argtypes = argtypes
@@ -90,6 +96,7 @@ _sparse_attn = _sig("csa2_sparse_attn", [C.POINTER(AttnArgs), _vp], C.c_int)
 _decode_ws = _sig("csa2_fused_decode_workspace_size", [C.POINTER(DecodeArgs)], _sz)
 _fused_decode = _sig("csa2_fused_decode", [C.POINTER(DecodeArgs), _vp], C.c_int)
 _decode_launches = _sig("csa2_fused_decode_launch_count", [C.POINTER(DecodeArgs)], C.c_int32)
+_write_records = _sig("csa2_write_records", [C.POINTER(WriteArgs), _vp], C.c_int)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
 
@@ -239,6 +246,29 @@ def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, s
     a.workspace, a.workspace_bytes = _ptr(ws), nb
     _check(_sparse_attn(C.byref(a), _stream()), "csa2_sparse_attn")
     return out, sm
+
+
+FP8_E4M3_ROWSCALE, FP4_E2M1_G32, FP4_E2M1_G16 = 1, 2, 3
+
+
+def write_records(x, dst_row, codes, scales, out_dtype: int, pos=None, theta: float = 10000.0, dev_status=None):
+    """Writes records x [n, 512] (float32 or bf16, before rotation) into a cache at rows
+    dst_row [n] (int64): codes [rows, 256] uint8 + scales [rows, 512/G] uint8 (FP4), or codes
+    [rows, 512] uint8 + scales [rows] float32 (FP8).  pos [n] (int64): positions whose rotary
+    coordinates the records take first (None: no rotation)."""
+    a = WriteArgs()
+    a.n_rows = x.shape[0]
+    a.x = _ptr(x)
+    a.x_f32 = 1 if x.dtype == torch.float32 else 0
+    if a.x_f32 == 0 and x.dtype != torch.bfloat16:
+        raise ValueError("x must be float32 or bfloat16")
+    a.pos = _ptr(pos)
+    a.rope_theta = float(theta)
+    a.dst_row = _ptr(dst_row)
+    a.cache_rows = codes.shape[0]
+    a.out_dtype = int(out_dtype)
+    a.codes, a.scales, a.dev_status = _ptr(codes), _ptr(scales), _ptr(dev_status)
+    _check(_write_records(C.byref(a), _stream()), "csa2_write_records")
 
 
 class DecodeLayer:

@@ -574,6 +574,31 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
   return st;
 }
 
+csa2_status csa2_write_records(const csa2_write_args* a, void* stream) {
+  if (!a || a->n_rows < 0) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->x || !a->dst_row || !a->codes || !a->scales || a->cache_rows < 1) return CSA2_EINVAL;
+  const bool fp8 = a->out_dtype == CSA2_FP8_E4M3_ROWSCALE;
+  if (!fp8 && a->out_dtype != CSA2_FP4_E2M1_G16 && a->out_dtype != CSA2_FP4_E2M1_G32) return CSA2_EINVAL;
+  if (!aligned(a->x, 16) || !aligned(a->codes, 16) || !aligned(a->dst_row, 8) || (a->pos && !aligned(a->pos, 8)) ||
+      (fp8 && !aligned(a->scales, 4)))
+    return CSA2_EINVAL;
+  WriteParams p{};
+  p.n_rows = a->n_rows;
+  p.x = a->x;
+  p.x_f32 = a->x_f32 != 0;
+  p.pos = a->pos;
+  for (int i = 0; i < CSA2_ROPE_DIM / 2; ++i)
+    p.inv_freq[i] = std::pow((double)a->rope_theta, -2.0 * i / (double)CSA2_ROPE_DIM);
+  p.dst_row = a->dst_row;
+  p.cache_rows = a->cache_rows;
+  p.out_dtype = a->out_dtype;
+  p.codes = a->codes;
+  p.scales = a->scales;
+  p.dev_status = a->dev_status;
+  return cuda_status(launch_write_records(p, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
   if (!a || a->attn.n_rows <= 0) return 0;
   int n_seg = 1;

@@ -122,6 +122,22 @@ struct AttnParams {
   int32_t* dev_status;        // optional: CSA2_EDEVICE_INDEX on an out-of-range record index
 };
 
+// Cache writer (csa2_write_records).
+struct WriteParams {
+  long long n_rows;
+  const void* x;          // [n_rows, 512] float32 (x_f32) or bf16
+  int x_f32;
+  const int64_t* pos;     // [n_rows] or null (no rotation)
+  double inv_freq[32];    // theta^(-2i/64), computed on the host in double
+  const int64_t* dst_row; // [n_rows]
+  long long cache_rows;
+  int out_dtype;          // CSA2_FP4_E2M1_G16 / _G32 or CSA2_FP8_E4M3_ROWSCALE
+  void* codes;
+  void* scales;
+  int32_t* dev_status;
+};
+cudaError_t launch_write_records(const WriteParams& p, cudaStream_t stream);
+
 int attn_smem_bytes();
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream);
 
