@@ -183,6 +183,37 @@ def test_writer_rotation_is_rope_in_float32():
     assert r[3, 454] == (x[3, 454] * c) - (x[3, 455] * sn)
 
 
+# ================================================================ compressor
+def test_compressor_special_cases_and_invariants():
+    rng = np.random.default_rng(21)
+    kv = rng.standard_normal((10, 512))
+    gate = rng.standard_normal((10, 512)) * 3
+    # ratio 1: no pooling (softmax over one token is 1)
+    assert np.allclose(O.compress(kv, gate, 1), kv, rtol=0, atol=0)
+    # equal gates: the mean of the pair; an odd tail yields no entry
+    e = O.compress(kv[:9], np.zeros((9, 512)), 2)
+    assert e.shape == (4, 512) and np.allclose(e, (kv[0:8:2] + kv[1:8:2]) / 2, rtol=0, atol=1e-15)
+    # per channel, the entry lies between its two tokens (a convex combination) ...
+    e2 = O.compress(kv, gate, 2)
+    lo = np.minimum(kv[0::2], kv[1::2]); hi = np.maximum(kv[0::2], kv[1::2])
+    assert np.all(e2 >= lo - 1e-12) and np.all(e2 <= hi + 1e-12)
+    # ... with the two-token softmax weight, channel by channel
+    w0 = 1.0 / (1.0 + np.exp(gate[1::2] - gate[0::2]))
+    assert np.allclose(e2, w0 * kv[0::2] + (1 - w0) * kv[1::2], rtol=1e-12, atol=1e-12)
+    # a dominant gate picks its token
+    g = np.zeros((2, 512)); g[1, :256] = 60.0; g[0, 256:] = 60.0
+    one = O.compress(kv[:2], g, 2)[0]
+    assert np.allclose(one[:256], kv[1, :256]) and np.allclose(one[256:], kv[0, 256:])
+    # adding a per-channel constant to both gates changes nothing
+    assert np.allclose(O.compress(kv, gate + rng.standard_normal(512), 2), e2, rtol=1e-12, atol=1e-12)
+
+
+def test_compressor_causal_visibility():
+    # an entry is visible once both its tokens are: positions 0 1 2 3 4 -> 0 1 1 2 2 entries
+    assert O.visible_entries(np.arange(5), 2).tolist() == [0, 1, 1, 2, 2]
+    assert O.visible_entries(np.arange(4), 1).tolist() == [1, 2, 3, 4]
+
+
 # ================================================================ indexer score
 def test_index_score_hand_case():
     q = np.array([[1.0, 2.0], [-1.0, 0.0]])
