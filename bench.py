@@ -398,6 +398,22 @@ def run_writer(local, peaks, n=262144, iters=20):
         nbytes = n * (512 * 4 + 8 + 8 + wbytes)
         out[name] = {"records": n, "ms": ms, "records_per_s": n / (ms / 1e3), "gbs": nbytes / (ms / 1e3) / 1e9,
                      "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
+    # the encoder's compressor at ratio 2: 2n tokens (kv and gate, float32) -> n entries
+    kv = torch.randn(2 * n, 512, generator=g).to(dev)
+    gate = torch.randn(2 * n, 512, generator=g).to(dev)
+    for _ in range(3):
+        S.compress(kv, gate, 2)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in ev:
+        e0.record()
+        S.compress(kv, gate, 2)
+        e1.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    nbytes = 2 * n * 512 * 4 * 2 + n * 512 * 4
+    out["compress_ratio2"] = {"entries": n, "ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9,
+                              "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
     return out
 
 

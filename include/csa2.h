@@ -322,6 +322,28 @@ typedef struct {
 csa2_status csa2_write_records(const csa2_write_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Sequence compressor of the encoder's global banks: entry e pools the `ratio` consecutive
+ * tokens ratio*e .. ratio*e + ratio - 1 with channel-wise softmax gates,
+ *   entry[e, c] = sum_j softmax_j(gate[ratio*e + j, c]) * kv[ratio*e + j, c]
+ * (course, "How CSA2 compresses, shares, and selects attention memory": learned,
+ * channel-wise softmax gates above ratio 1, no pooling at ratio 1; the encoder's banks use
+ * ratio 2).  kv and gate are the tokens' projections (their weights are outside this call).
+ * An entry is visible to a query at position p when all its tokens are: the first
+ * (p + 1) / ratio entries, to be passed as n_visible to the indexer and attention calls.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int64_t n_entries;          /* entries formed */
+  int32_t ratio;              /* 1 .. 8 */
+  const void* kv;             /* [n_entries * ratio, 512] float32 (x_f32 = 1) or bf16 */
+  const void* gate;           /* [n_entries * ratio, 512], the same type */
+  int32_t x_f32;
+  float* out;                 /* [n_entries, 512] float32 */
+} csa2_compress_args;
+
+/* All pointers device, 16-byte aligned. */
+csa2_status csa2_compress(const csa2_compress_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Utilities
  * ------------------------------------------------------------------------------------ */
 const char* csa2_status_string(csa2_status s);

@@ -77,6 +77,10 @@ class WriteArgs(C.Structure):
                 ("dev_status", _vp)]
 
 
+class CompressArgs(C.Structure):
+    _fields_ = [("n_entries", _i64), ("ratio", _i32), ("kv", _vp), ("gate", _vp), ("x_f32", _i32), ("out", _vp)]
+
+
 def _sig(name, argtypes, restype):
     f = getattr(_lib, name)
     f.argtypes = argtypes
@@ -97,6 +101,7 @@ _decode_ws = _sig("csa2_fused_decode_workspace_size", [C.POINTER(DecodeArgs)], _
 _fused_decode = _sig("csa2_fused_decode", [C.POINTER(DecodeArgs), _vp], C.c_int)
 _decode_launches = _sig("csa2_fused_decode_launch_count", [C.POINTER(DecodeArgs)], C.c_int32)
 _write_records = _sig("csa2_write_records", [C.POINTER(WriteArgs), _vp], C.c_int)
+_compress = _sig("csa2_compress", [C.POINTER(CompressArgs), _vp], C.c_int)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
 
@@ -269,6 +274,21 @@ def write_records(x, dst_row, codes, scales, out_dtype: int, pos=None, theta: fl
     a.out_dtype = int(out_dtype)
     a.codes, a.scales, a.dev_status = _ptr(codes), _ptr(scales), _ptr(dev_status)
     _check(_write_records(C.byref(a), _stream()), "csa2_write_records")
+
+
+def compress(kv, gate, ratio: int):
+    """Entries [T // ratio, 512] float32 pooled from tokens kv, gate [T, 512] (float32 or bf16)
+    with channel-wise softmax gates."""
+    if kv.shape != gate.shape or kv.dtype != gate.dtype:
+        raise ValueError("kv and gate must have the same shape and dtype")
+    n = kv.shape[0] // ratio
+    out = torch.empty((n, kv.shape[1]), dtype=torch.float32, device=kv.device)
+    a = CompressArgs()
+    a.n_entries, a.ratio = n, int(ratio)
+    a.kv, a.gate, a.out = _ptr(kv), _ptr(gate), _ptr(out)
+    a.x_f32 = 1 if kv.dtype == torch.float32 else 0
+    _check(_compress(C.byref(a), _stream()), "csa2_compress")
+    return out
 
 
 class DecodeLayer:

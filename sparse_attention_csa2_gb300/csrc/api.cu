@@ -599,6 +599,15 @@ csa2_status csa2_write_records(const csa2_write_args* a, void* stream) {
   return cuda_status(launch_write_records(p, static_cast<cudaStream_t>(stream)));
 }
 
+csa2_status csa2_compress(const csa2_compress_args* a, void* stream) {
+  if (!a || a->n_entries < 0) return CSA2_EINVAL;
+  if (a->n_entries == 0) return CSA2_OK;
+  if (!a->kv || !a->gate || !a->out || a->ratio < 1 || a->ratio > 8) return CSA2_EINVAL;
+  if (!aligned(a->kv, 16) || !aligned(a->gate, 16) || !aligned(a->out, 16)) return CSA2_EINVAL;
+  return cuda_status(launch_compress(a->n_entries, a->ratio, a->kv, a->gate, a->x_f32 != 0, a->out,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
   if (!a || a->attn.n_rows <= 0) return 0;
   int n_seg = 1;

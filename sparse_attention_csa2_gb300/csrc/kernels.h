@@ -137,6 +137,9 @@ struct WriteParams {
   int32_t* dev_status;
 };
 cudaError_t launch_write_records(const WriteParams& p, cudaStream_t stream);
+// Sequence compressor (csa2_compress).
+cudaError_t launch_compress(long long n_entries, int ratio, const void* kv, const void* gate, bool x_f32, float* out,
+                            cudaStream_t stream);
 
 int attn_smem_bytes();
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream);

@@ -33,26 +33,21 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
 }
 
-__global__ void __launch_bounds__(kWriteWarps * 32) write_records_kernel(const WriteParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long r = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
-  if (r >= p.n_rows) return;
-  const long long dst = p.dst_row[r];
-  if (dst < 0 || dst >= p.cache_rows) {
-    if (lane == 0 && p.dev_status) atomicExch(p.dev_status, (int)CSA2_EDEVICE_INDEX);
-    return;
-  }
-  // the lane's 16 values
-  float v[16];
-  if (p.x_f32) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + r * kHeadDim + 16 * lane);
+// Sequence compressor: one warp per entry, lane l holding channels 16l .. 16l+15; per
+// channel a softmax over the entry's `ratio` gate logits weighs its tokens' values (the
+// encoder's banks pool consecutive tokens with learned channel-wise softmax gates, course,
+// "How CSA2 compresses, shares, and selects attention memory").
+template <bool F32>
+__device__ __forceinline__ void load16(const void* base, long long row, int lane, float (&v)[16]) {
+  if (F32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kHeadDim + 16 * lane);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float4 f = __ldg(src + q);
       v[4 * q] = f.x, v[4 * q + 1] = f.y, v[4 * q + 2] = f.z, v[4 * q + 3] = f.w;
     }
   } else {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + r * kHeadDim + 16 * lane);
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + row * kHeadDim + 16 * lane);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const uint4 u = __ldg(src + q);
@@ -64,6 +59,23 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_records_kernel(const W
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(kWriteWarps * 32) write_records_kernel(const WriteParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+  if (r >= p.n_rows) return;
+  const long long dst = p.dst_row[r];
+  if (dst < 0 || dst >= p.cache_rows) {
+    if (lane == 0 && p.dev_status) atomicExch(p.dev_status, (int)CSA2_EDEVICE_INDEX);
+    return;
+  }
+  // the lane's 16 values
+  float v[16];
+  if (p.x_f32)
+    load16<true>(p.x, r, lane, v);
+  else
+    load16<false>(p.x, r, lane, v);
   // rotation: lane i forms cos and sin of pair i (angle pos * theta^(-2i/64), reduced modulo
   // 2 pi in double with a two-part 2 pi, then double sincos of |r| <= pi, rounded to float);
   // lanes 28..31 hold the pairs (448 + 2i, 449 + 2i), 8 each, and fetch theirs
@@ -126,7 +138,49 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_records_kernel(const W
   else if ((lane & 1) == 0) sc[dst * (kHeadDim / 32) + lane / 2] = (uint8_t)code;
 }
 
+template <bool F32>
+__global__ void __launch_bounds__(kWriteWarps * 32)
+    compress_kernel(long long n_entries, int ratio, const void* kv, const void* gate, float* out) {
+  const int lane = threadIdx.x & 31;
+  const long long e = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+  if (e >= n_entries) return;
+  float m[16], den[16], num[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) m[k] = -INFINITY, den[k] = 0.f, num[k] = 0.f;
+  // online softmax over the entry's tokens, channel by channel
+#pragma unroll 1
+  for (int j = 0; j < ratio; ++j) {
+    float g[16], x[16];
+    load16<F32>(gate, e * ratio + j, lane, g);
+    load16<F32>(kv, e * ratio + j, lane, x);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float mn = fmaxf(m[k], g[k]);
+      const float a = __expf(m[k] - mn), b = __expf(g[k] - mn);
+      den[k] = den[k] * a + b;
+      num[k] = num[k] * a + b * x[k];
+      m[k] = mn;
+    }
+  }
+  float4* dst = reinterpret_cast<float4*>(out + e * kHeadDim + 16 * lane);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    dst[q] = make_float4(num[4 * q] / den[4 * q], num[4 * q + 1] / den[4 * q + 1], num[4 * q + 2] / den[4 * q + 2],
+                         num[4 * q + 3] / den[4 * q + 3]);
+}
+
 }  // namespace
+
+cudaError_t launch_compress(long long n_entries, int ratio, const void* kv, const void* gate, bool x_f32, float* out,
+                            cudaStream_t stream) {
+  if (n_entries == 0) return cudaSuccess;
+  const long long blocks = (n_entries + kWriteWarps - 1) / kWriteWarps;
+  if (x_f32)
+    compress_kernel<true><<<(unsigned)blocks, kWriteWarps * 32, 0, stream>>>(n_entries, ratio, kv, gate, out);
+  else
+    compress_kernel<false><<<(unsigned)blocks, kWriteWarps * 32, 0, stream>>>(n_entries, ratio, kv, gate, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_write_records(const WriteParams& p, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;

@@ -109,3 +109,26 @@ def test_writer_skips_and_reports_out_of_range_rows():
     rc, rs = O.write_records(x, pos, 10000.0, "fp4", 16)
     ok = np.arange(8) != 5
     assert np.array_equal(_zero_sign_free_fp4(codes.cpu().numpy()[dst[ok]]), _zero_sign_free_fp4(rc[ok]))
+
+
+# ------------------------------------------------------------------ compressor
+@pytest.mark.parametrize("ratio", [1, 2, 4, 8])
+@pytest.mark.parametrize("x_dtype", ["f32", "bf16"])
+def test_compressor_matches_oracle(ratio, x_dtype):
+    _cuda()
+    rng = np.random.default_rng(50 + ratio)
+    T = 1000 * ratio + ratio - 1  # an incomplete last group: no entry
+    kv = rng.standard_normal((T, 512)).astype(np.float32)
+    gate = (rng.standard_normal((T, 512)) * 4).astype(np.float32)
+    gate[0, :8] = 80.0  # a saturated gate: its token takes the whole weight of those channels
+    kt, gt = torch.from_numpy(kv), torch.from_numpy(gate)
+    if x_dtype == "bf16":
+        kt, gt = kt.to(torch.bfloat16), gt.to(torch.bfloat16)
+        kv, gate = kt.to(torch.float32).numpy(), gt.to(torch.float32).numpy()
+    out = S.compress(kt.cuda(), gt.cuda(), ratio)
+    torch.cuda.synchronize()
+    ref = O.compress(kv, gate, ratio)
+    got = out.cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape == (T // ratio, 512)
+    # fp32 softmax weights: error a few ulps of the largest token value
+    assert np.max(np.abs(got - ref)) <= 1e-5 * np.max(np.abs(kv))
