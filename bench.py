@@ -50,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the tiny / hierarchical / long-context lines")
-    ap.add_argument("--only-config", choices=["tiny_decode", "hierarchical", "long_decode"],
+    ap.add_argument("--only-config", choices=["tiny_decode", "hierarchical", "long_decode", "long_decode_mxfp4"],
                     help="time only this decode workload (profiling)")
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
@@ -272,7 +272,7 @@ def group_bytes(wl) -> float:
     """Algorithmic bytes of one decode step of a layer group (all rows): indexer keys of the
     full scan, the pool's keys for every Reindex layer, and per layer the selected latents,
     the window rows, q, q^I (scoring layers) and the fp32 output."""
-    key_rec = wl.DI + 4 if wl.key_fmt == "fp8" else wl.DI * 2
+    key_rec = wl.DI + 4 if wl.key_fmt == "fp8" else wl.DI // 2 + wl.DI // 32 if wl.key_fmt == "mxfp4" else wl.DI * 2
     lat_rec = wl.D // 2 + wl.D // wl.lat_group if wl.lat_fmt == "fp4" else wl.D * 2
     swa_row = wl.D + 4 if wl.swa_fmt == "fp8" else wl.D * 2
     per_q = wl.N * key_rec
@@ -286,7 +286,7 @@ def group_bytes(wl) -> float:
     return float(wl.Bq * per_q)
 
 
-def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "long_decode")):
+def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "long_decode", "long_decode_mxfp4")):
     """The other decode workloads, each timed as back-to-back group steps with CUDA events
     after 3 warm-up steps: tiny decode (latency), hierarchical group (6 layers), long-context
     decode (FP8 keys, FP4 latents, FP8 window)."""

@@ -67,7 +67,12 @@ typedef enum csa2_dtype {
   CSA2_FP4_E2M1_G32 = 2,      /* E2M1 codes, two per byte (low nibble = even channel), and one
                                  E4M3 scale per 32 channels in a separate array:
                                  value = level * scale ("DeepSeek-V4.1-Flash explained", section 7) */
-  CSA2_FP4_E2M1_G16 = 3       /* the same with one scale per 16 channels, as the pages state */
+  CSA2_FP4_E2M1_G16 = 3,      /* the same with one scale per 16 channels, as the pages state */
+  CSA2_MXFP4 = 4              /* indexer keys only: OCP MXFP4, E2M1 codes two per byte (low nibble
+                                 = even element) and one UE8M0 exponent per block of 32 in
+                                 k_scale [n_seq, n_records, 4] uint8: value = level * 2^(e-127)
+                                 (the pages' indexer precision, "DeepSeek-V4.1-Flash explained",
+                                 section 7) */
 } csa2_dtype;
 
 /* Layer modes of a CSA2 sharing group ("DeepSeek-V4.1-Flash explained", section 2, mode
@@ -88,6 +93,9 @@ typedef enum csa2_mode {
  *   scores[r, j] = sum_h w[r, h] * max(0, q_idx[r, h, :] . key(j))       for a candidate j
  *   scores[r, j] = -inf                                                   otherwise
  * One indexer key per record, shared by all 32 heads.  FP8 keys: key(j) = code * k_scale[j].
+ * MXFP4 keys (k_dtype CSA2_MXFP4, k_idx [n_seq, n_records, 64] uint8, k_scale the exponents
+ * [n_seq, n_records, 4] uint8): key(j)[d] = level(d) * 2^(e(j, d / 32) - 127).  MXFP4
+ * indexer queries are given as their (exact) bf16 values.
  * Without `cand`, j runs over records 0..n_records-1 and records >= n_visible[r] are not
  * candidates.  With `cand`, j runs over cand[r, 0..L) (record positions, strictly
  * ascending, e.g. a block pool) and entries >= n_cand[r] are not candidates.
@@ -98,7 +106,8 @@ typedef struct csa2_index_args {
   const void* q_idx;          /* [n_rows, 32, 128] bf16 */
   const float* w;             /* [n_rows, 32] */
   const void* k_idx;          /* [n_seq, n_records, 128]: bf16, or E4M3 bytes (k_dtype FP8) */
-  const float* k_scale;       /* [n_seq, n_records] row scales for FP8 keys, else NULL */
+  const float* k_scale;       /* [n_seq, n_records] row scales for FP8 keys; MXFP4: the exponent
+                                 bytes [n_seq, n_records, 4] (passed through this pointer); else NULL */
   int32_t k_dtype;            /* CSA2_BF16 or CSA2_FP8_E4M3_ROWSCALE */
   int32_t n_rows;             /* query rows (>= 0) */
   int32_t n_seq;              /* sequences sharing the key layout */

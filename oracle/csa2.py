@@ -17,7 +17,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "bf16_to_f64", "e4m3_to_f64", "e2m1_to_f64", "fp4_to_f64", "fp8_rows_to_f64",
+    "bf16_to_f64", "e4m3_to_f64", "e2m1_to_f64", "fp4_to_f64", "fp8_rows_to_f64", "mxfp4_to_f64",
     "index_scores", "topk_order", "topk_set", "block_max", "block_pool", "rope",
     "sink_softmax", "attend", "csa2_attention_row", "scored_positions",
     "keys_of", "latents_of", "swa_rows_of", "index_scores_rows", "topk_rows",
@@ -74,6 +74,20 @@ def fp4_to_f64(codes, scales, group: int) -> np.ndarray:
     lev[..., 0::2] = e2m1_to_f64(codes & 0xF)
     lev[..., 1::2] = e2m1_to_f64(codes >> 4)
     return lev * np.repeat(e4m3_to_f64(scales), group, axis=-1)
+
+
+def mxfp4_to_f64(codes, exps) -> np.ndarray:
+    """OCP MXFP4 (the pages' indexer precision: "DeepSeek-V4.1-Flash explained", section 7
+    table, "Indexer queries and keys: OCP MXFP4"): blocks of 32 E2M1 elements share one
+    UE8M0 scale 2^(e - 127), e = 255 being NaN (OCP Microscaling specification).  codes
+    [..., D/2] two per byte, low nibble the even element; exps [..., D/32]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    e = np.asarray(exps, dtype=np.uint8).astype(np.float64)
+    scale = np.where(e == 255, np.nan, np.exp2(e - 127.0))
+    lev = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), np.float64)
+    lev[..., 0::2] = e2m1_to_f64(codes & 0xF)
+    lev[..., 1::2] = e2m1_to_f64(codes >> 4)
+    return lev * np.repeat(scale, 32, axis=-1)
 
 
 def fp8_rows_to_f64(codes, row_scale) -> np.ndarray:
@@ -212,6 +226,8 @@ def keys_of(inp, b: int, positions=None) -> np.ndarray:
     if p["key_fmt"] == "bf16":
         return bf16_to_f64(k)
     sc = c["k_scale"][b] if positions is None else c["k_scale"][b][positions]
+    if p["key_fmt"] == "mxfp4":
+        return mxfp4_to_f64(k, sc)
     return fp8_rows_to_f64(k, sc)
 
 

@@ -17,7 +17,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 # ------------------------------------------------------------------ constants (csa2.h)
 OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EWORKSPACE, EDEVICE_INDEX = range(7)
-BF16, FP8_E4M3_ROWSCALE, FP4_E2M1_G32, FP4_E2M1_G16 = range(4)
+BF16, FP8_E4M3_ROWSCALE, FP4_E2M1_G32, FP4_E2M1_G16, MXFP4 = range(5)
 MODE_FULL, MODE_FULL_POOL, MODE_REINDEX, MODE_REUSE = range(4)
 IDX_HEADS, IDX_DIM, HEADS, HEAD_DIM, ROPE_DIM, MAX_TOPK = 32, 128, 64, 512, 64, 1024
 MODES = {"full": MODE_FULL, "full_pool": MODE_FULL_POOL, "reindex": MODE_REINDEX, "reuse": MODE_REUSE}
@@ -144,9 +144,13 @@ def _ws(nbytes: int, device):
 def _key_dtype(k_idx, k_scale):
     if k_idx.element_size() == 2:
         return BF16
+    if k_idx.element_size() == 1 and k_scale is not None and k_scale.dtype == torch.uint8:
+        if k_idx.shape[-1] != 64 or k_scale.shape[-1] != 4:
+            raise ValueError("MXFP4 keys are [..., 64] code bytes with [..., 4] exponent bytes")
+        return MXFP4
     if k_idx.element_size() == 1 and k_scale is not None:
         return FP8_E4M3_ROWSCALE
-    raise ValueError("indexer keys must be bf16 (2-byte) or E4M3 bytes with row scales")
+    raise ValueError("indexer keys must be bf16 (2-byte), E4M3 bytes with fp32 row scales, or MXFP4")
 
 
 def _lat_dtype(lat, lat_scale):
@@ -251,9 +255,6 @@ def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, s
     a.workspace, a.workspace_bytes = _ptr(ws), nb
     _check(_sparse_attn(C.byref(a), _stream()), "csa2_sparse_attn")
     return out, sm
-
-
-FP8_E4M3_ROWSCALE, FP4_E2M1_G32, FP4_E2M1_G16 = 1, 2, 3
 
 
 def write_records(x, dst_row, codes, scales, out_dtype: int, pos=None, theta: float = 10000.0, dev_status=None):

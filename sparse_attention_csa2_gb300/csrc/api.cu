@@ -75,7 +75,8 @@ enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill };
 int tc05_segments(int n_rows, long long L, int unit, long long min_seg = 4096);
 
 ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0) {
-  if (!mma_indexer_available() || env_int("CSA2_SCAN_WARP_MMA", 0) != 0) return ScanPath::kWarpMma;
+  if (!mma_indexer_available() || env_int("CSA2_SCAN_WARP_MMA", 0) != 0 || a->k_dtype == CSA2_MXFP4)
+    return ScanPath::kWarpMma;
   if (a->cand != nullptr && !(want_topk && cand_run > 0 && cand_run % 64 == 0)) return ScanPath::kWarpMma;
   const bool fp8 = a->k_dtype == CSA2_FP8_E4M3_ROWSCALE;
   if (!want_topk && a->block_max == nullptr && a->n_seq == 1 && a->n_rows >= 64)
@@ -123,7 +124,8 @@ cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk,
                                a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, s);
     }
     default:
-      return launch_index_scan(p, a->k_dtype == CSA2_FP8_E4M3_ROWSCALE, a->cand != nullptr, n_seg, s);
+      return launch_index_scan(p, a->k_dtype == CSA2_FP8_E4M3_ROWSCALE ? 1 : a->k_dtype == CSA2_MXFP4 ? 2 : 0,
+                               a->cand != nullptr, n_seg, s);
   }
 }
 
@@ -146,8 +148,9 @@ csa2_status check_index(const csa2_index_args* a, bool need_outputs) {
   if (a->n_rows == 0) return CSA2_OK;
   if (!a->q_idx || !a->w || !a->k_idx || !a->seq_of_row || !a->n_visible) return CSA2_EINVAL;
   if (!aligned(a->q_idx, 16) || !aligned(a->k_idx, 16) || !aligned(a->w, 4)) return CSA2_EINVAL;
-  if (a->k_dtype != CSA2_BF16 && a->k_dtype != CSA2_FP8_E4M3_ROWSCALE) return CSA2_EINVAL;
-  if (a->k_dtype == CSA2_FP8_E4M3_ROWSCALE && (!a->k_scale || !aligned(a->k_scale, 4))) return CSA2_EINVAL;
+  if (a->k_dtype != CSA2_BF16 && a->k_dtype != CSA2_FP8_E4M3_ROWSCALE && a->k_dtype != CSA2_MXFP4)
+    return CSA2_EINVAL;
+  if (a->k_dtype != CSA2_BF16 && (!a->k_scale || !aligned(a->k_scale, 4))) return CSA2_EINVAL;
   if (a->cand) {
     if (!a->n_cand || a->L < 1 || a->L > (1LL << 31) - 1) return CSA2_EINVAL;
   }

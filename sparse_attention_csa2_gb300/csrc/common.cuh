@@ -43,6 +43,12 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool va
                "r"(valid ? 16 : 0)
                : "memory");
 }
+// 4-byte global->shared copy (4-byte aligned); when !valid the 4 bytes are zeroed.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -100,6 +106,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t h;
   asm("{\n .reg .b32 t;\n cvt.rn.f16x2.e4m3x2 t, %1;\n mov.b32 %0, t;\n}\n" : "=r"(h) : "h"(v));
+  return h;
+}
+// One byte of two E2M1 codes (low nibble first) -> two f16 (packed, exact), by the hardware
+// conversion.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n" : "=r"(h) : "r"(byte));
   return h;
 }
 // Two bf16 (packed) -> two fp16 (packed), round to nearest.

@@ -26,19 +26,29 @@ constexpr int kScanWarps = 16;
 constexpr int kScanThreads = kScanWarps * 32;
 constexpr int kRoundTiles = kRoundEntries / 16;  // 8 tiles of 16 records between checks
 
-template <bool FP8>
+// Key formats of the scan: bf16 rows, FP8 E4M3 rows with an fp32 scale, OCP MXFP4 rows
+// (E2M1 codes, one UE8M0 exponent per block of 32; the pages' indexer precision).
+enum { kKeyBF16 = 0, kKeyFP8 = 1, kKeyMX = 2 };
+
+template <int FMT>
 struct ScanCfg {
-  static constexpr int kRowBytes = FP8 ? 128 : 256;  // bytes of one indexer key
-  static constexpr int kStageBytes = 16 * kRowBytes;  // one 16-record tile
-  static constexpr int kStages = FP8 ? 4 : 2;
+  static constexpr int kRowBytes = FMT == kKeyBF16 ? 256 : FMT == kKeyFP8 ? 128 : 64;  // one indexer key
+  // one 16-record tile; MXFP4: the records' four exponent bytes follow the codes
+  static constexpr int kStageBytes = 16 * kRowBytes + (FMT == kKeyMX ? 64 : 0);
+  static constexpr int kStages = FMT == kKeyBF16 ? 2 : FMT == kKeyFP8 ? 4 : 6;
   static constexpr int kRingBytes = kScanWarps * kStages * kStageBytes;
 };
 
 // Index (in 32-bit words of a 128-dim bf16 row) of the q^I pair that meets A-fragment word
 // `hi` (0 = k-lo pair, 1 = k-hi pair) of k-step s for the thread with c = lane % 4.
-template <bool FP8>
+template <int FMT>
 __device__ __forceinline__ int q_word(int s, int c, int hi) {
-  if (FP8) {
+  if (FMT == kKeyMX) {
+    // 16-byte chunk c of the 64-byte MXFP4 row is block c (dims 32c .. 32c+31, two per
+    // byte); k-step s uses its bytes 2s (dims 32c + 4s + {0,1}) and 2s+1 ({2,3})
+    return 16 * c + 2 * s + hi;
+  }
+  if (FMT == kKeyFP8) {
     // 16-byte chunk (4*(s/4) + c) of the 128-byte FP8 row holds 16 dims; k-step s uses its
     // word s%4: dims 16*chunk + 4*(s%4) + {0,1} (lo) and {2,3} (hi).
     const int chunk = 4 * (s >> 2) + c;
@@ -51,9 +61,10 @@ __device__ __forceinline__ int q_word(int s, int c, int hi) {
   }
 }
 
-template <bool FP8, bool GATHER>
+template <int FMT, bool GATHER>
 __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanParams p) {
-  using Cfg = ScanCfg<FP8>;
+  constexpr bool FP8 = FMT == kKeyFP8, MX = FMT == kKeyMX, WIDE = FMT != kKeyBF16;  // WIDE: f16 MMA
+  using Cfg = ScanCfg<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   Engine<kScanWarps> eng;
@@ -92,8 +103,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const uint32_t* qh = qrow + (8 * nt + g) * (kIdxDim / 2);
-        qf[s][nt][0] = __ldg(qh + q_word<FP8>(s, c, 0));
-        qf[s][nt][1] = __ldg(qh + q_word<FP8>(s, c, 1));
+        qf[s][nt][0] = __ldg(qh + q_word<FMT>(s, c, 0));
+        qf[s][nt][1] = __ldg(qh + q_word<FMT>(s, c, 1));
       }
   }
   float wv[4][2];
@@ -102,7 +113,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
     wv[nt][0] = __ldg(p.w + (size_t)row * kIdxHeads + 8 * nt + 2 * c);
     wv[nt][1] = __ldg(p.w + (size_t)row * kIdxHeads + 8 * nt + 2 * c + 1);
   }
-  if (FP8) {
+  if (WIDE) {
     // q^I to f16: the four lanes of a group hold head 8nt+g's 128 dims between them
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -148,7 +159,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
       const bool valid = j < e1;
       const long long rec = valid ? record_of(j) : 0;
       const uint8_t* src = kbase + (seq_off + (size_t)rec) * Cfg::kRowBytes;
-      if (FP8) {
+      if (MX) {
+        // chunk c (block c) of the row; lane c = 0 of each group also copies the row's
+        // four exponent bytes
+        cp_async16(st + rh * 512 + lane * 16, src + c * 16, valid);
+        if (c == 0)
+          cp_async4(st + 1024 + (g + 8 * rh) * 4,
+                    reinterpret_cast<const uint8_t*>(p.k_scale) + (seq_off + (size_t)rec) * 4, valid);
+      } else if (FP8) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           cp_async16(st + (2 * i + rh) * 512 + lane * 16, src + (4 * i + c) * 16, valid);
@@ -187,7 +205,38 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
         float acc[4][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        if (FP8) {
+        if (MX) {
+          // the row's largest block exponent E scales the dot product (below); block c's
+          // codes take 2^(e_c - E) in f16 (exact while e_c - E >= -23)
+          const uint4 r0 = *reinterpret_cast<const uint4*>(st + lane * 16);
+          const uint4 r1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);
+          const uint32_t x0 = *reinterpret_cast<const uint32_t*>(st + 1024 + g * 4);
+          const uint32_t x1 = *reinterpret_cast<const uint32_t*>(st + 1024 + (g + 8) * 4);
+          auto block_factor = [&](uint32_t x) -> __half2 {
+            const uint32_t e0 = x & 0xffu, e1 = (x >> 8) & 0xffu, e2 = (x >> 16) & 0xffu, e3 = x >> 24;
+            const int E = (int)max(max(e0, e1), max(e2, e3));
+            const int d = (int)((x >> (8 * c)) & 0xffu) - E;  // <= 0
+            const float f = d < -126 ? 0.f : __int_as_float((d + 127) << 23);
+            return __float2half2_rn(f);
+          };
+          const __half2 f0 = block_factor(x0), f1 = block_factor(x1);
+          const uint32_t w0v[4] = {r0.x, r0.y, r0.z, r0.w};
+          const uint32_t w1v[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint32_t b0 = (w0v[s >> 1] >> (16 * (s & 1))) & 0xffffu;  // bytes 2s, 2s+1 of row g
+            const uint32_t b1 = (w1v[s >> 1] >> (16 * (s & 1))) & 0xffffu;  // ... of row g+8
+            auto wid = [](uint32_t byte, __half2 f) -> uint32_t {
+              uint32_t h = e2m1x2_to_f16x2(byte);
+              __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h), f);
+              return *reinterpret_cast<const uint32_t*>(&v);
+            };
+            const uint32_t a0 = wid(b0 & 0xffu, f0), a2 = wid(b0 >> 8, f0);
+            const uint32_t a1 = wid(b1 & 0xffu, f1), a3 = wid(b1 >> 8, f1);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) mma_f16(acc[nt], a0, a1, a2, a3, qf[s][nt][0], qf[s][nt][1]);
+          }
+        } else if (FP8) {
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const uint4 r0 = *reinterpret_cast<const uint4*>(st + (2 * i) * 512 + lane * 16);
@@ -230,10 +279,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
           sc_lo = __ldg(p.k_scale + seq_off + rec_lo);
           sc_hi = __ldg(p.k_scale + seq_off + rec_hi);
         }
+        if (MX) {
+          // 2^(E - 127) of the row's largest block exponent E (from the stage)
+          auto row_scale = [](uint32_t x) -> float {
+            const uint32_t E = max(max(x & 0xffu, (x >> 8) & 0xffu), max((x >> 16) & 0xffu, x >> 24));
+            return E == 0u ? __int_as_float(1 << 22) : __int_as_float((int)E << 23);  // 2^(E-127), exact
+          };
+          const uint8_t* st = my_ring + (int)(t % Cfg::kStages) * Cfg::kStageBytes;
+          sc_lo = row_scale(*reinterpret_cast<const uint32_t*>(st + 1024 + g * 4));
+          sc_hi = row_scale(*reinterpret_cast<const uint32_t*>(st + 1024 + (g + 8) * 4));
+        }
         float s_lo = 0.f, s_hi = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-          if (FP8) {
+          if (WIDE) {
             s_lo = fmaf(wv[nt][0], fmaxf(acc[nt][0] * sc_lo, 0.f), s_lo);
             s_lo = fmaf(wv[nt][1], fmaxf(acc[nt][1] * sc_lo, 0.f), s_lo);
             s_hi = fmaf(wv[nt][0], fmaxf(acc[nt][2] * sc_hi, 0.f), s_hi);
@@ -301,15 +360,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) index_scan_kernel(const ScanP
 
 }  // namespace
 
-size_t scan_smem_bytes(bool fp8, int K) {
-  const size_t ring = fp8 ? ScanCfg<true>::kRingBytes : ScanCfg<false>::kRingBytes;
+size_t scan_smem_bytes(int fmt, int K) {
+  const size_t ring = fmt == kKeyFP8 ? ScanCfg<kKeyFP8>::kRingBytes
+                      : fmt == kKeyMX ? ScanCfg<kKeyMX>::kRingBytes
+                                      : ScanCfg<kKeyBF16>::kRingBytes;
   size_t s = ring + sizeof(EngShared);
   if (K > 0) s += (size_t)kScanWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;
   return s;
 }
 
-cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_seg, cudaStream_t stream) {
-  const size_t smem = scan_smem_bytes(fp8, p.K);
+cudaError_t launch_index_scan(const ScanParams& p, int fmt, bool gather, int n_seg, cudaStream_t stream) {
+  const size_t smem = scan_smem_bytes(fmt, p.K);
   dim3 grid(n_seg, p.n_rows), block(kScanThreads);
   if (p.n_rows == 0) return cudaSuccess;
 #define CSA2_LAUNCH_SCAN(F, G)                                                                         \
@@ -319,10 +380,12 @@ cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_
     if (e != cudaSuccess) return e;                                                                    \
     index_scan_kernel<F, G><<<grid, block, smem, stream>>>(p);                                         \
   } while (0)
-  if (fp8) {
-    if (gather) CSA2_LAUNCH_SCAN(true, true); else CSA2_LAUNCH_SCAN(true, false);
+  if (fmt == kKeyFP8) {
+    if (gather) CSA2_LAUNCH_SCAN(kKeyFP8, true); else CSA2_LAUNCH_SCAN(kKeyFP8, false);
+  } else if (fmt == kKeyMX) {
+    if (gather) CSA2_LAUNCH_SCAN(kKeyMX, true); else CSA2_LAUNCH_SCAN(kKeyMX, false);
   } else {
-    if (gather) CSA2_LAUNCH_SCAN(false, true); else CSA2_LAUNCH_SCAN(false, false);
+    if (gather) CSA2_LAUNCH_SCAN(kKeyBF16, true); else CSA2_LAUNCH_SCAN(kKeyBF16, false);
   }
 #undef CSA2_LAUNCH_SCAN
   return cudaGetLastError();

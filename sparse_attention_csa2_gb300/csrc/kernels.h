@@ -45,7 +45,8 @@ struct ScanParams {
                               // after it with programmatic dependent launch may start early
 };
 
-size_t scan_smem_bytes(bool fp8, int K);
+// key format of the warp-MMA scan: 0 bf16, 1 FP8 rows, 2 MXFP4
+size_t scan_smem_bytes(int fmt, int K);
 
 // tcgen05 indexer: decode rows (bf16 or FP8 keys, records in place) and prefill tiles (bf16).
 bool mma_indexer_available();
@@ -56,7 +57,7 @@ bool mma_decode_cluster_ok(int n_seg, int n_rows, int K, int max_seg_blocks, boo
 cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_seg, int max_seg_blocks, bool fp8,
                               cudaStream_t stream);
 cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream);
-cudaError_t launch_index_scan(const ScanParams& p, bool fp8, bool gather, int n_seg, cudaStream_t stream);
+cudaError_t launch_index_scan(const ScanParams& p, int fmt, bool gather, int n_seg, cudaStream_t stream);
 
 // Streaming top-K over per-row entry streams (scores, or the lists of earlier segments).
 struct FeedParams {

@@ -114,6 +114,45 @@ def _fp4_encode_chunk(x: torch.Tensor, group: int):
     return packed.numpy(), scode.to(torch.uint8).numpy()
 
 
+def _e2m1_codes(q: torch.Tensor) -> torch.Tensor:
+    """E2M1 code of each value: nearest level, ties to the even code, saturating at 6."""
+    mag = q.abs().contiguous()
+    idx = torch.searchsorted(_E2M1_MIDS, mag, right=False)
+    tie = (idx < 7) & (mag == _E2M1_MIDS[idx.clamp(max=6)])
+    idx = torch.where(tie & (idx % 2 == 1), idx + 1, idx)
+    return idx | torch.where(q < 0, 8, 0)
+
+
+def mxfp4_blocks(x: torch.Tensor):
+    """OCP MXFP4 encoding of float32 rows [..., D]: per block of 32 the shared UE8M0 scale
+    2^(floor(log2 amax) - 2) (2 = the exponent of E2M1's largest value, 6 = 1.5 * 2^2; an
+    all-zero block takes 2^-127), each element the nearest E2M1 level of x / scale, ties to
+    the even code, saturating at 6.  Returns (codes [..., D/2] low nibble = even element,
+    biased exponents [..., D/32] uint8)."""
+    lead, d = x.shape[:-1], x.shape[-1]
+    xb = x.reshape(*lead, d // 32, 32)
+    amax = xb.abs().amax(-1)
+    e = torch.where(amax > 0, torch.floor(torch.log2(amax.clamp(min=1e-38))) - 2, torch.full_like(amax, -127.0))
+    e = e.clamp(-127, 127)
+    q = xb / torch.exp2(e).unsqueeze(-1)
+    code = _e2m1_codes(q).to(torch.uint8).reshape(*lead, d)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).to(torch.uint8)
+    return packed.numpy(), (e + 127).to(torch.uint8).numpy()
+
+
+def mxfp4_round_trip(x: torch.Tensor) -> torch.Tensor:
+    """The values of x's MXFP4 encoding, as float32 (exact)."""
+    codes, exps = mxfp4_blocks(x)
+    c = torch.from_numpy(codes).to(torch.int64)
+    lv = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    def dec(n):
+        m = lv[n & 7]
+        return torch.where((n & 8) != 0, -m, m)
+    vals = torch.stack([dec(c & 0xF), dec(c >> 4)], -1).reshape(*x.shape)
+    sc = torch.exp2(torch.from_numpy(exps).to(torch.float32) - 127.0)
+    return vals * sc.repeat_interleave(32, -1)
+
+
 def fp4_groups(x: torch.Tensor, group: int):
     """FP4 encoding: E2M1 codes (two per byte, low nibble = even channel) and one E4M3
     scale code per ``group`` channels.  The scale is the smallest E4M3 value >= amax/6;
@@ -189,6 +228,8 @@ def make_inputs(wl: Workload, seed: int, mode: str = "gauss") -> dict:
                 w = uniform((Bq, HI), seed, _stream(10, l, 1))
             if l == 0:
                 q_idx0 = qi
+            if wl.key_fmt == "mxfp4":
+                qi = mxfp4_round_trip(qi)  # the pages' MXFP4 indexer queries, exact in bf16
             lay["q_idx"] = bf16_bits(qi)
             lay["w"] = w.numpy().astype(np.float32)
         q = normal((Bq, H, D), seed, _stream(10, l, 2))
@@ -218,6 +259,9 @@ def make_inputs(wl: Workload, seed: int, mode: str = "gauss") -> dict:
                     k[b, c * wl.block_size:(c + 1) * wl.block_size] += 0.5 * qmean[b]
     if wl.key_fmt == "bf16":
         cache = dict(k_idx=bf16_bits(k), k_scale=None)
+    elif wl.key_fmt == "mxfp4":
+        codes, exps = mxfp4_blocks(k)
+        cache = dict(k_idx=codes, k_scale=exps)
     else:
         codes, scale = fp8_rows(k, unit_scale=(mode == "grid"))
         cache = dict(k_idx=codes, k_scale=scale)

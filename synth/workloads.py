@@ -27,7 +27,7 @@ class Workload:
     DI: int = 128          # indexer head dim
     K: int = 512           # top-K
     W: int = 128           # sliding window (rows attended, current token included)
-    key_fmt: str = "bf16"  # indexer keys: "bf16" | "fp8" (E4M3 + fp32 row scale)
+    key_fmt: str = "bf16"  # indexer keys: "bf16" | "fp8" (E4M3 + fp32 row scale) | "mxfp4" (OCP MXFP4)
     lat_fmt: str = "bf16"  # latents: "bf16" | "fp4" (E2M1 + E4M3 group scale)
     lat_group: int = 32
     swa_fmt: str = "bf16"  # sliding-window rows: "bf16" | "fp8" (E4M3 + fp32 row scale)
@@ -64,6 +64,9 @@ WORKLOADS = {
     "prefill_chunk": Workload("prefill_chunk", B=1, N=36864, Bq=4096, T=4096, P0=32768),
     "long_decode": Workload("long_decode", B=4, N=1048576, Bq=4, key_fmt="fp8",
                             lat_fmt="fp4", lat_group=32, swa_fmt="fp8"),
+    # the pages' own indexer precision (OCP MXFP4 queries and keys) on the long-context shape
+    "long_decode_mxfp4": Workload("long_decode_mxfp4", B=4, N=1048576, Bq=4, key_fmt="mxfp4",
+                                  lat_fmt="fp4", lat_group=16, swa_fmt="fp8"),
 }
 
 

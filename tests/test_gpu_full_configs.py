@@ -86,6 +86,16 @@ def test_long_context_full_size(mode):
     _check_layers(inp, g, rows, mode, exact_layers={0})
 
 
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_long_context_mxfp4_full_size(mode):
+    """B=4 x N=1,048,576 with the pages' indexer precision: OCP MXFP4 keys and queries, FP4
+    latents (E4M3 per 16), FP8 window rows."""
+    _cuda()
+    rows = [0, 3]
+    inp, g = _decode_case("long_decode_mxfp4", mode, seed=6, rows=rows)
+    _check_layers(inp, g, rows, mode, exact_layers={0})
+
+
 def test_prefill_chunk_full_size():
     """T=4,096 queries at positions 32,768.. over N=36,864 records: 256 sampled query rows
     including the first and the last, indices (Gaussian: near-ties only) and outputs."""

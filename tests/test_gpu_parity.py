@@ -28,7 +28,7 @@ def small(name, seed=7, mode="gauss", **kw):
 
 
 # ------------------------------------------------------------------ index scores
-@pytest.mark.parametrize("key_fmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("key_fmt", ["bf16", "fp8", "mxfp4"])
 @pytest.mark.parametrize("mode", ["grid", "gauss"])
 def test_index_scores(key_fmt, mode):
     _cuda()
@@ -168,7 +168,8 @@ def test_sparse_attn(lat_fmt, group, swa_fmt):
 
 
 # ------------------------------------------------------------------ fused decode layers
-@pytest.mark.parametrize("key_fmt,lat_fmt,swa_fmt", [("bf16", "bf16", "bf16"), ("fp8", "fp4", "fp8")])
+@pytest.mark.parametrize("key_fmt,lat_fmt,swa_fmt", [("bf16", "bf16", "bf16"), ("fp8", "fp4", "fp8"),
+                                                     ("mxfp4", "fp4", "fp8")])
 def test_fused_full_grid_exact_indices(key_fmt, lat_fmt, swa_fmt):
     _cuda()
     inp = small("batched_decode", seed=4, mode="grid", B=3, N=9001, key_fmt=key_fmt, lat_fmt=lat_fmt,

@@ -88,6 +88,22 @@ def test_generator_fp4_encoder_page_example():
     assert vals[0, 0] == g["store_3p2_scale1_level"] and vals[0, 1] == 6.0
 
 
+def test_mxfp4_decoder_spec_points():
+    # OCP MX: UE8M0 scale 2^(e - 127) per block of 32 E2M1 elements; e = 255 is NaN
+    codes = np.zeros((1, 64), np.uint8)  # 128 elements
+    codes[0, 0] = 0x7 | (0xA << 4)       # el 0 = +6, el 1 = -1.0
+    codes[0, 16] = 0x1                    # el 32 = +0.5
+    codes[0, 63] = 0x30                   # el 127 = +1.5
+    v = O.mxfp4_to_f64(codes, np.array([[127, 130, 0, 255]], np.uint8))
+    assert v[0, 0] == 6.0 and v[0, 1] == -1.0 and v[0, 2:32].tolist() == [0.0] * 30
+    assert v[0, 32] == 0.5 * 8.0  # the second block scales by 2^3
+    assert v[0, 64] == 0.0 and np.all(np.isnan(v[0, 96:]))  # 2^-127 * 0; the NaN block
+    # every code with a unit scale is its E2M1 level (low nibble = even element)
+    allc = np.arange(256, dtype=np.uint8)[None, :32].repeat(2, 0).reshape(1, 64)
+    vv = O.mxfp4_to_f64(allc, np.array([[127, 127, 127, 127]], np.uint8))
+    assert np.array_equal(vv[0, 0::2], O.e2m1_to_f64(allc[0] & 0xF)) and np.array_equal(vv[0, 1::2], O.e2m1_to_f64(allc[0] >> 4))
+
+
 def test_fp8_row_scale():
     codes = np.array([[0x38, 0xB8, 0x7E]], np.uint8)
     v = O.fp8_rows_to_f64(codes, np.array([0.25], np.float32))
