@@ -30,3 +30,4 @@ function here is "parity unpinned".
 from .csa2 import *  # noqa: F401,F403
 from .writer import *  # noqa: F401,F403
 from .compressor import *  # noqa: F401,F403
+from .projections import *  # noqa: F401,F403

@@ -20,7 +20,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 import torch
 
-from .workloads import Workload, WORKLOADS, scaled  # noqa: F401
+from .workloads import Workload, WORKLOADS, scaled, ProjShape, PROJECTIONS  # noqa: F401
 
 _CHUNK = 1 << 22
 _THREADS = max(1, min(16, os.cpu_count() or 1))
@@ -305,3 +305,25 @@ def to_device(inp: dict, device="cuda") -> dict:
     out["layers"] = [{k: (_t(v, device) if isinstance(v, np.ndarray) else v) for k, v in lay.items()}
                      for lay in inp["layers"]]
     return out
+
+
+# ---------------------------------------------------------------- projections
+def projection_inputs(shape, seed: int) -> dict:
+    """Hidden states, attention outputs and random-init weights (N(0, 1/fan_in)) for the
+    projections around attention, all bf16 tensors on the host, gains float32 near 1."""
+    s = shape
+    hd = s.heads * s.head_dim
+
+    def bf(sh, stream, std):
+        return normal(sh, seed, stream, std).to(torch.bfloat16)
+
+    return {
+        "x": bf((s.tokens, s.hidden), 1, 1.0),
+        "w_dq": bf((s.q_rank, s.hidden), 2, s.hidden ** -0.5),
+        "g_q": 1.0 + 0.1 * normal((s.q_rank,), seed, 3),
+        "w_uq": bf((hd, s.q_rank), 4, s.q_rank ** -0.5),
+        "g_head": 1.0 + 0.1 * normal((s.head_dim,), seed, 5),
+        "o": bf((s.tokens, s.heads, s.head_dim), 6, 0.1),
+        "w_oa": bf((s.groups, s.o_rank, hd // s.groups), 7, (hd // s.groups) ** -0.5),
+        "w_ob": bf((s.hidden, s.groups * s.o_rank), 8, (s.groups * s.o_rank) ** -0.5),
+    }

@@ -77,3 +77,24 @@ def scaled(wl: Workload, **kw) -> Workload:
     if "B" in kw and "Bq" not in kw and wl.T == 0:
         kw["Bq"] = kw["B"]
     return replace(wl, **kw)
+
+
+@dataclass(frozen=True)
+class ProjShape:
+    """Sizes of the projections around attention: tokens, hidden size, query rank, heads,
+    head size, output groups and output rank (the Flash config: hidden 4096, q rank 1024,
+    64 heads of 512, 8 output groups; the output rank is not stated, 1024 is used)."""
+    name: str
+    tokens: int
+    hidden: int = 4096
+    q_rank: int = 1024
+    heads: int = 64
+    head_dim: int = 512
+    groups: int = 8
+    o_rank: int = 1024
+
+
+PROJECTIONS = {
+    "decode": ProjShape("decode", tokens=32),      # one decode step of the 32-sequence batch
+    "prefill": ProjShape("prefill", tokens=4096),  # one 4096-token prefill chunk
+}

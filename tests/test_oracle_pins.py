@@ -507,3 +507,96 @@ def test_grid_mode_scores_are_exact_integers_over_16():
     assert np.all(s * 16 == np.round(s * 16))
     assert np.all(np.abs(s) < 2 ** 16)
     assert inp["params"]["mode"] == "gauss"
+
+
+# ================================================================ projections
+def test_rms_norm_closed_form():
+    # [3, 4]: mean square 12.5
+    y = O.rms_norm([3.0, 4.0], eps=0.0)
+    assert np.allclose(y, [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=0, atol=1e-15)
+    assert np.allclose(O.rms_norm([3.0, 4.0], [2.0, 0.5], eps=0.0), [0.8485281374238570 * 2, 1.1313708498984760 * 0.5])
+    # eps enters under the root: mean square 12.5 + eps 12.5 -> divide by 5
+    assert np.allclose(O.rms_norm([3.0, 4.0], eps=12.5), [0.6, 0.8], rtol=0, atol=1e-15)
+    # normalized over the last axis only
+    v = np.array([[3.0, 4.0], [30.0, 40.0]])
+    assert np.allclose(O.rms_norm(v, eps=0.0)[0], O.rms_norm(v, eps=0.0)[1])
+
+
+def _toy_query_weights():
+    # hidden 3 -> rank 2 -> 2 heads of 2
+    w_dq = np.array([[1.0, 0.0, 0.0], [0.0, 1.0, 1.0]])
+    w_uq = np.array([[1.0, 0.0], [0.0, 1.0],      # head 0 = c
+                     [2.0, 0.0], [0.0, 0.0]])     # head 1 = (2 c0, 0)
+    return w_dq, w_uq
+
+
+def test_query_proj_hand_worked():
+    w_dq, w_uq = _toy_query_weights()
+    x = np.array([[1.0, 2.0, 2.0]])               # c = (1, 4), mean square 8.5
+    q = O.query_proj(x, w_dq, None, w_uq, None, n_heads=2, eps=0.0)
+    assert q.shape == (1, 2, 2)
+    assert np.allclose(q[0, 0], [1 / math.sqrt(8.5), 4 / math.sqrt(8.5)], atol=1e-14)
+    assert np.allclose(q[0, 1], [math.sqrt(2.0), 0.0], atol=1e-14)
+    # the rank gain acts before the up-projection: c * g = (1, 8) -> head 0 = (1, 8) / sqrt(32.5)
+    q = O.query_proj(x, w_dq, [1.0, 2.0], w_uq, None, n_heads=2, eps=0.0)
+    assert np.allclose(q[0, 0], [1 / math.sqrt(32.5), 8 / math.sqrt(32.5)], atol=1e-14)
+    # the head gain acts last, per coordinate of every head
+    q = O.query_proj(x, w_dq, None, w_uq, [1.0, -3.0], n_heads=2, eps=0.0)
+    assert np.allclose(q[0, 0], [1 / math.sqrt(8.5), -12 / math.sqrt(8.5)], atol=1e-14)
+    # eps in both norms: c / sqrt(8.5 + 8.5) = (1, 4) / sqrt(17); head 0 has mean square 1/2,
+    # so it is divided by sqrt(0.5 + 8.5) = 3
+    q = O.query_proj(x, w_dq, None, w_uq, None, n_heads=2, eps=8.5)
+    assert np.allclose(q[0, 0], [1 / math.sqrt(17) / 3, 4 / math.sqrt(17) / 3], atol=1e-14)
+
+
+def test_query_proj_invariants():
+    rng = np.random.default_rng(5)
+    T, d, r, H, D = 4, 64, 32, 3, 16
+    x = rng.standard_normal((T, d))
+    w_dq = rng.standard_normal((r, d))
+    w_uq = rng.standard_normal((H * D, r))
+    g_q = rng.uniform(0.5, 1.5, r)
+    q = O.query_proj(x, w_dq, g_q, w_uq, None, H, eps=0.0)
+    # every head has unit RMS; a per-token scale of x and a scale of either weight cancel
+    assert np.allclose(np.sqrt(np.mean(q ** 2, -1)), 1.0, atol=1e-12)
+    assert np.allclose(O.query_proj(7.0 * x, w_dq, g_q, w_uq, None, H, eps=0.0), q, atol=1e-12)
+    assert np.allclose(O.query_proj(x, 0.25 * w_dq, g_q, 3.0 * w_uq, None, H, eps=0.0), q, atol=1e-12)
+    # heads are independent: head 1's rows of w_uq do not change head 0
+    w2 = w_uq.copy()
+    w2[D:2 * D] = rng.standard_normal((D, r))
+    q2 = O.query_proj(x, w_dq, g_q, w2, None, H, eps=0.0)
+    assert np.allclose(q2[:, 0], q[:, 0], atol=1e-12) and not np.allclose(q2[:, 1], q[:, 1])
+    # with eps 0 and unit gains the path is the normalized product of the two matrices
+    ref = x @ w_dq.T
+    ref = ref / np.linalg.norm(ref, axis=-1, keepdims=True)
+    ref = (ref @ w_uq.T).reshape(T, H, D)
+    ref = ref / np.linalg.norm(ref, axis=-1, keepdims=True) * math.sqrt(D)
+    assert np.allclose(O.query_proj(x, w_dq, None, w_uq, None, H, eps=0.0), ref, atol=1e-12)
+
+
+def test_out_proj_hand_worked():
+    o = np.array([[[1.0], [2.0], [3.0], [4.0]]])  # 4 heads of 1, groups {0,1} and {2,3}
+    w_oa = np.array([[[1.0, 1.0]], [[1.0, -1.0]]])  # group 0 -> 1 + 2 = 3, group 1 -> 3 - 4 = -1
+    w_ob = np.array([[1.0, 0.0], [2.0, 3.0]])
+    assert np.allclose(O.out_proj(o, w_oa, w_ob), [[3.0, 3.0]], atol=0)
+
+
+def test_out_proj_is_a_block_diagonal_product():
+    import scipy.linalg
+    rng = np.random.default_rng(9)
+    T, H, D, G, r, d = 3, 8, 4, 4, 5, 6
+    o = rng.standard_normal((T, H, D))
+    w_oa = rng.standard_normal((G, r, H // G * D))
+    w_ob = rng.standard_normal((d, G * r))
+    dense = scipy.linalg.block_diag(*list(w_oa))   # [G r, H D]
+    ref = (o.reshape(T, H * D) @ dense.T) @ w_ob.T
+    assert np.allclose(O.out_proj(o, w_oa, w_ob), ref, atol=1e-12)
+    # one group: a plain two-stage low-rank product
+    w_oa1 = rng.standard_normal((1, r, H * D))
+    assert np.allclose(O.out_proj(o, w_oa1, w_ob[:, :r]), (o.reshape(T, H * D) @ w_oa1[0].T) @ w_ob[:, :r].T)
+    # a head only reaches the hidden state through its own group's rank slice
+    o2 = o.copy()
+    o2[:, 5] += 1.0                                 # head 5 is in group 2 (heads 4, 5)
+    w_ob2 = w_ob.copy()
+    w_ob2[:, 2 * r:3 * r] = 0.0
+    assert np.allclose(O.out_proj(o2, w_oa, w_ob2), O.out_proj(o, w_oa, w_ob2), atol=1e-12)
