@@ -237,7 +237,7 @@ typedef struct csa2_attn_args {
   const float* sink;          /* [64] sink logits */
   float rope_theta;           /* > 0 */
   float softmax_scale;
-  float* out;                 /* out [n_rows, 64, 512] fp32 */
+  void* out;                  /* out [n_rows, 64, 512] fp32 (bf16 with out_bf16) */
   float* sink_mass;           /* out [n_rows, 64] or NULL */
   void* workspace;            /* csa2_sparse_attn_workspace_size bytes: the partial results of
                                  each 128-entry tile (K + window entries per row) */
@@ -246,6 +246,9 @@ typedef struct csa2_attn_args {
                                  record index outside [0, n_records) other than -1, or to
                                  CSA2_ETIMEOUT when a bounded wait on the tensor cores gave up
                                  (outputs then undefined); or NULL */
+  int32_t out_bf16;           /* 0: out is fp32; 1: out is bf16 [n_rows, 64, 512] (each value the
+                                 fp32 result rounded to nearest even), the input of
+                                 csa2_out_proj */
 } csa2_attn_args;
 
 size_t csa2_sparse_attn_workspace_size(const csa2_attn_args* a);
@@ -351,6 +354,69 @@ typedef struct {
 
 /* All pointers device, 16-byte aligned. */
 csa2_status csa2_compress(const csa2_compress_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Projections on either side of attention ("DeepSeek V4.1-Flash. Every layer, connected",
+ * "The query and output paths": low-rank query projection, grouped output projection;
+ * "DeepSeek V4 Inside": query rank 1024, RMSNorm on the query head, 64 heads in 8 output
+ * groups).  RMSNorm(v) = v / sqrt(mean(v^2) + eps) over the last axis.
+ *
+ * csa2_query_proj - the attention query of hidden states x:
+ *   c   = W_DQ x                          (hidden -> q_rank)
+ *   c   = RMSNorm(c) * g_q
+ *   q   = W_UQ c                          (q_rank -> n_heads x 512)
+ *   q_h = RMSNorm(q_h) * g_head           per head, one gain vector shared by the heads
+ * The rotation of the head's last 64 coordinates is attention's (csa2_sparse_attn).
+ * Tensor cores, bf16 inputs, fp32 accumulation; c is held in bf16 as c * g_q with its
+ * RMSNorm factor applied to the up-projection's fp32 result.  Two kernel launches.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t n_tokens;           /* T >= 0 */
+  int32_t hidden;             /* multiple of 64 */
+  int32_t q_rank;             /* multiple of 128 */
+  int32_t n_heads;            /* >= 1 (heads of 512) */
+  const void* x;              /* [T, hidden] bf16 */
+  const void* w_dq;           /* [q_rank, hidden] bf16 (row f = the weights of feature f) */
+  const float* g_q;           /* [q_rank] or NULL (gain 1) */
+  const void* w_uq;           /* [n_heads * 512, q_rank] bf16 */
+  const float* g_head;        /* [512] or NULL (gain 1) */
+  float eps;                  /* >= 0 */
+  void* q;                    /* out [T, n_heads, 512] bf16 */
+  void* workspace;            /* csa2_query_proj_workspace_size bytes, any contents */
+  size_t workspace_bytes;
+  int32_t* dev_status;        /* optional device int32: CSA2_ETIMEOUT when a bounded wait on the
+                                 tensor cores gave up (outputs then undefined); or NULL */
+} csa2_query_proj_args;
+
+/* Pointers device; x, the weights, q and workspace 16-byte aligned. */
+size_t csa2_query_proj_workspace_size(const csa2_query_proj_args* a);
+csa2_status csa2_query_proj(const csa2_query_proj_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * csa2_out_proj - grouped low-rank output projection of attention's output o (taken after
+ * attention's inverse rotation): the heads split into n_groups groups of consecutive heads;
+ *   y_g = W_OA[g] concat(o_h, h in group g)    (n_heads / n_groups * 512 -> o_rank)
+ *   out = W_OB concat(y_0, .., y_{G-1})        (n_groups * o_rank -> hidden)
+ * Tensor cores, bf16 inputs, fp32 accumulation, y held in bf16.  Two kernel launches.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t n_tokens;           /* T >= 0 */
+  int32_t n_heads;            /* multiple of n_groups */
+  int32_t n_groups;           /* >= 1 */
+  int32_t o_rank;             /* multiple of 128 */
+  int32_t hidden;             /* multiple of 128 */
+  const void* o;              /* [T, n_heads, 512] bf16 */
+  const void* w_oa;           /* [n_groups, o_rank, n_heads / n_groups * 512] bf16 */
+  const void* w_ob;           /* [hidden, n_groups * o_rank] bf16 */
+  void* out;                  /* out [T, hidden] bf16 */
+  void* workspace;            /* csa2_out_proj_workspace_size bytes, any contents */
+  size_t workspace_bytes;
+  int32_t* dev_status;        /* as in csa2_query_proj_args */
+} csa2_out_proj_args;
+
+/* Pointers device, 16-byte aligned. */
+size_t csa2_out_proj_workspace_size(const csa2_out_proj_args* a);
+csa2_status csa2_out_proj(const csa2_out_proj_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Utilities

@@ -61,7 +61,7 @@ class AttnArgs(C.Structure):
                 ("idx", _vp), ("K", _i32), ("swa", _vp), ("swa_scale", _vp), ("swa_dtype", _i32),
                 ("swa_rows", _i64), ("swa_pos0", _vp), ("window", _i32), ("sink", _vp),
                 ("rope_theta", _f32), ("softmax_scale", _f32), ("out", _vp), ("sink_mass", _vp),
-                ("workspace", _vp), ("workspace_bytes", _sz), ("dev_status", _vp)]
+                ("workspace", _vp), ("workspace_bytes", _sz), ("dev_status", _vp), ("out_bf16", _i32)]
 
 
 class DecodeArgs(C.Structure):
@@ -79,6 +79,18 @@ class WriteArgs(C.Structure):
 
 class CompressArgs(C.Structure):
     _fields_ = [("n_entries", _i64), ("ratio", _i32), ("kv", _vp), ("gate", _vp), ("x_f32", _i32), ("out", _vp)]
+
+
+class QueryProjArgs(C.Structure):
+    _fields_ = [("n_tokens", _i32), ("hidden", _i32), ("q_rank", _i32), ("n_heads", _i32), ("x", _vp),
+                ("w_dq", _vp), ("g_q", _vp), ("w_uq", _vp), ("g_head", _vp), ("eps", _f32), ("q", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz), ("dev_status", _vp)]
+
+
+class OutProjArgs(C.Structure):
+    _fields_ = [("n_tokens", _i32), ("n_heads", _i32), ("n_groups", _i32), ("o_rank", _i32), ("hidden", _i32),
+                ("o", _vp), ("w_oa", _vp), ("w_ob", _vp), ("out", _vp), ("workspace", _vp),
+                ("workspace_bytes", _sz), ("dev_status", _vp)]
 
 
 def _sig(name, argtypes, restype):
@@ -102,6 +114,10 @@ _fused_decode = _sig("csa2_fused_decode", [C.POINTER(DecodeArgs), _vp], C.c_int)
 _decode_launches = _sig("csa2_fused_decode_launch_count", [C.POINTER(DecodeArgs)], C.c_int32)
 _write_records = _sig("csa2_write_records", [C.POINTER(WriteArgs), _vp], C.c_int)
 _compress = _sig("csa2_compress", [C.POINTER(CompressArgs), _vp], C.c_int)
+_query_proj = _sig("csa2_query_proj", [C.POINTER(QueryProjArgs), _vp], C.c_int)
+_query_proj_ws = _sig("csa2_query_proj_workspace_size", [C.POINTER(QueryProjArgs)], _sz)
+_out_proj = _sig("csa2_out_proj", [C.POINTER(OutProjArgs), _vp], C.c_int)
+_out_proj_ws = _sig("csa2_out_proj_workspace_size", [C.POINTER(OutProjArgs)], _sz)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
 
@@ -240,14 +256,16 @@ def _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, K, swa, swa_scale,
     a.swa_rows, a.swa_pos0, a.window = swa.shape[1], _ptr(swa_pos0), window
     a.sink, a.rope_theta, a.softmax_scale = _ptr(sink), float(theta), float(softmax_scale)
     a.out, a.sink_mass = _ptr(out), _ptr(sink_mass)
+    a.out_bf16 = 1 if out.dtype == torch.bfloat16 else 0
     return a
 
 
 def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, swa_pos0, window: int, sink,
-                theta: float = 1e4, softmax_scale: float = HEAD_DIM ** -0.5):
-    """Attention output [n_rows, 64, 512] fp32 and sink mass [n_rows, 64]."""
+                theta: float = 1e4, softmax_scale: float = HEAD_DIM ** -0.5, out_dtype=torch.float32):
+    """Attention output [n_rows, 64, 512] (fp32, or bf16 with out_dtype=torch.bfloat16) and
+    sink mass [n_rows, 64]."""
     dev = _dev(q)
-    out = torch.empty((q.shape[0], HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+    out = torch.empty((q.shape[0], HEADS, HEAD_DIM), dtype=out_dtype, device=dev)
     sm = torch.empty((q.shape[0], HEADS), dtype=torch.float32, device=dev)
     a = _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, idx.shape[1], swa, swa_scale, swa_pos0, window,
                    sink, theta, softmax_scale, out, sm)
@@ -298,11 +316,12 @@ class DecodeLayer:
 
     def __init__(self, mode, *, q_idx=None, w=None, k_idx=None, k_scale=None, seq_of_row, n_visible, q, q_pos,
                  latents, lat_scale, swa, swa_scale, swa_pos0, window, sink, K=512, theta=1e4,
-                 softmax_scale=HEAD_DIM ** -0.5, block_size=64, n_keep=64, pool=None, n_pool=None, idx=None):
+                 softmax_scale=HEAD_DIM ** -0.5, block_size=64, n_keep=64, pool=None, n_pool=None, idx=None,
+                 out_dtype=torch.float32):
         self.mode = MODES[mode] if isinstance(mode, str) else int(mode)
         dev = _dev(q)
         n_rows = q.shape[0]
-        self.out = torch.empty((n_rows, HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+        self.out = torch.empty((n_rows, HEADS, HEAD_DIM), dtype=out_dtype, device=dev)
         self.sink_mass = torch.empty((n_rows, HEADS), dtype=torch.float32, device=dev)
         if self.mode == MODE_REUSE:
             if idx is None:
@@ -357,3 +376,79 @@ def fused_decode(mode, **kw):
     layer = DecodeLayer(mode, **kw)
     layer()
     return layer
+
+
+# ------------------------------------------------------------------ projections
+def _bf16_2d(t, name):
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 tensor")
+    return t
+
+
+class QueryProj:
+    """A prepared csa2_query_proj call (weights, output and workspace bound once):
+    q [T, heads, 512] bf16 from hidden states x [T, hidden] bf16 through the low-rank path
+    W_DQ [q_rank, hidden] -> RMSNorm * g_q -> W_UQ [heads * 512, q_rank] -> per-head RMSNorm
+    * g_head."""
+
+    def __init__(self, x, w_dq, w_uq, g_q=None, g_head=None, eps: float = 1e-6):
+        for t, n in ((x, "x"), (w_dq, "w_dq"), (w_uq, "w_uq")):
+            _bf16_2d(t, n)
+        for g, n in ((g_q, "g_q"), (g_head, "g_head")):
+            if g is not None and (g.dtype != torch.float32 or not g.is_contiguous()):
+                raise ValueError(f"{n} must be a contiguous float32 tensor")
+        T, hidden = x.shape
+        q_rank = w_dq.shape[0]
+        heads = w_uq.shape[0] // HEAD_DIM
+        if w_dq.shape[1] != hidden or w_uq.shape[1] != q_rank or w_uq.shape[0] != heads * HEAD_DIM:
+            raise ValueError("weight shapes do not match")
+        self.q = torch.empty((T, heads, HEAD_DIM), dtype=torch.bfloat16, device=x.device)
+        a = QueryProjArgs()
+        a.n_tokens, a.hidden, a.q_rank, a.n_heads = T, hidden, q_rank, heads
+        a.x, a.w_dq, a.w_uq, a.q = _ptr(x), _ptr(w_dq), _ptr(w_uq), _ptr(self.q)
+        a.g_q, a.g_head, a.eps = _ptr(g_q), _ptr(g_head), float(eps)
+        self._ws, a.workspace_bytes = _ws(int(_query_proj_ws(C.byref(a))), x.device)
+        a.workspace = _ptr(self._ws)
+        self._args = a
+        self._keep = (x, w_dq, w_uq, g_q, g_head)
+
+    def __call__(self):
+        _check(_query_proj(C.byref(self._args), _stream()), "csa2_query_proj")
+        return self.q
+
+
+class OutProj:
+    """A prepared csa2_out_proj call: out [T, hidden] bf16 from attention's output o
+    [T, heads, 512] bf16 through the grouped low-rank projection W_OA [G, o_rank,
+    heads / G * 512] (per group of consecutive heads), then W_OB [hidden, G * o_rank]."""
+
+    def __init__(self, o, w_oa, w_ob):
+        for t, n in ((o, "o"), (w_oa, "w_oa"), (w_ob, "w_ob")):
+            _bf16_2d(t, n)
+        T, heads, _ = o.shape
+        G, o_rank, kg = w_oa.shape
+        hidden = w_ob.shape[0]
+        if kg * G != heads * HEAD_DIM or w_ob.shape[1] != G * o_rank:
+            raise ValueError("weight shapes do not match")
+        self.out = torch.empty((T, hidden), dtype=torch.bfloat16, device=o.device)
+        a = OutProjArgs()
+        a.n_tokens, a.n_heads, a.n_groups, a.o_rank, a.hidden = T, heads, G, o_rank, hidden
+        a.o, a.w_oa, a.w_ob, a.out = _ptr(o), _ptr(w_oa), _ptr(w_ob), _ptr(self.out)
+        self._ws, a.workspace_bytes = _ws(int(_out_proj_ws(C.byref(a))), o.device)
+        a.workspace = _ptr(self._ws)
+        self._args = a
+        self._keep = (o, w_oa, w_ob)
+
+    def __call__(self):
+        _check(_out_proj(C.byref(self._args), _stream()), "csa2_out_proj")
+        return self.out
+
+
+def query_proj(x, w_dq, w_uq, g_q=None, g_head=None, eps: float = 1e-6):
+    """Attention queries [T, heads, 512] bf16 of hidden states x (see QueryProj)."""
+    return QueryProj(x, w_dq, w_uq, g_q, g_head, eps)()
+
+
+def out_proj(o, w_oa, w_ob):
+    """Hidden-size output [T, hidden] bf16 of attention's output o (see OutProj)."""
+    return OutProj(o, w_oa, w_ob)()

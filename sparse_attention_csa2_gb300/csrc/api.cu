@@ -230,6 +230,7 @@ AttnParams attn_params(const csa2_attn_args* a, const int32_t* idx) {
   for (int i = 0; i < CSA2_ROPE_DIM / 2; ++i)
     p.inv_freq[i] = std::pow((double)a->rope_theta, -2.0 * i / (double)CSA2_ROPE_DIM);
   p.out = a->out;
+  p.out_bf16 = a->out_bf16 != 0;
   p.sink_mass = a->sink_mass;
   p.dev_status = a->dev_status;
   return p;
@@ -247,6 +248,46 @@ csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, c
   p.part_o = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM);
   p.part_ml = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * 2);
   return cuda_status(launch_sparse_attn(p, n_split, s));
+}
+
+// ------------------------------------------------------------------ projections
+// Launch shape of one projection GEMM: token tile bn (the MMA's N), pipeline stages and the
+// K split ks.  The cost model counts pipeline steps of the busiest SM (blocks per SM x steps
+// per block) plus the split's reduction, and takes the cheapest; ties go to fewer splits.
+struct ProjPlan {
+  int bn, stages, ks;
+};
+
+int proj_bn(int n_tok) { return n_tok <= 32 ? 32 : n_tok <= 64 ? 64 : n_tok <= 128 ? 128 : 256; }
+
+// tiles: blocks of one K split (feature tiles x token tiles x groups)
+ProjPlan proj_plan(int n_tok, int k_steps, int tiles, bool allow_split) {
+  ProjPlan best{proj_bn(n_tok), 0, 1};
+  const size_t stage = 128 * 128 + (size_t)best.bn * 128;
+  // two blocks per SM for narrow token tiles (more loads in flight), else one with deep pipelines
+  const size_t budget = best.bn <= 64 ? 96 * 1024 : 200 * 1024;
+  const int base_stages = (int)std::min<size_t>(8, budget / stage);
+  const int sms = sm_count();
+  const int forced = env_int("CSA2_PROJ_KS", 0);
+  double best_cost = 1e30;
+  for (int ks = 1; ks <= 8; ks *= 2) {
+    if (ks > 1 && (!allow_split || ks > k_steps)) break;
+    if (forced > 0 && ks != forced) continue;
+    const size_t need = (size_t)(ks - 1) * best.bn * 128 * 4;  // block 0's slots for the partials
+    int stages = base_stages;
+    while ((size_t)stages * stage < need && stages < 8) ++stages;
+    if ((size_t)stages * stage < need || proj_smem_bytes(best.bn, stages) > 227 * 1024) continue;
+    const long long blocks = (long long)tiles * ks;
+    const double steps = (double)((k_steps + ks - 1) / ks);
+    const double cost = (double)((blocks + sms - 1) / sms) * steps + (ks > 1 ? 1.0 + 0.5 * (ks - 1) * best.bn / 32 : 0.0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best.ks = ks;
+      best.stages = stages;
+    }
+  }
+  if (best.stages == 0) best = ProjPlan{best.bn, base_stages, 1};  // a forced split that does not fit
+  return best;
 }
 
 // ------------------------------------------------------------------ top-K plumbing
@@ -609,6 +650,151 @@ csa2_status csa2_compress(const csa2_compress_args* a, void* stream) {
   if (!aligned(a->kv, 16) || !aligned(a->gate, 16) || !aligned(a->out, 16)) return CSA2_EINVAL;
   return cuda_status(launch_compress(a->n_entries, a->ratio, a->kv, a->gate, a->x_f32 != 0, a->out,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa2_query_proj_workspace_size(const csa2_query_proj_args* a) {
+  if (!a || a->n_tokens <= 0 || a->q_rank <= 0) return 0;
+  return align_up((size_t)a->n_tokens * a->q_rank * 2) + align_up((size_t)(a->q_rank / 128) * a->n_tokens * 4);
+}
+
+csa2_status csa2_query_proj(const csa2_query_proj_args* a, void* stream) {
+  if (!a || a->n_tokens < 0) return CSA2_EINVAL;
+  if (a->n_tokens == 0) return CSA2_OK;
+  if (a->hidden < 64 || a->hidden % 64 || a->q_rank < 128 || a->q_rank % 128 || a->n_heads < 1 ||
+      a->n_heads > 4096 || !(a->eps >= 0.f))
+    return CSA2_EINVAL;
+  if (!a->x || !a->w_dq || !a->w_uq || !a->q || !aligned(a->x, 16) || !aligned(a->w_dq, 16) ||
+      !aligned(a->w_uq, 16) || !aligned(a->q, 16))
+    return CSA2_EINVAL;
+  if (!a->workspace || !aligned(a->workspace, 16) || a->workspace_bytes < csa2_query_proj_workspace_size(a))
+    return CSA2_EWORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = a->n_tokens;
+  Carve c{static_cast<uint8_t*>(a->workspace)};
+  uint16_t* cq = c.take<uint16_t>((size_t)T * a->q_rank);
+  float* ss = c.take<float>((size_t)(a->q_rank / 128) * T);
+  // down-projection: c * g_q in bf16 and per-token partial sums of squares
+  {
+    const int m_tiles = a->q_rank / 128, k_steps = a->hidden / 64;
+    const ProjPlan pl = proj_plan(T, k_steps, m_tiles * ((T + proj_bn(T) - 1) / proj_bn(T)), true);
+    CUtensorMap tmA, tmB;
+    if (!make_tmap_bf16(&tmA, a->w_dq, a->hidden, a->q_rank, (unsigned long long)a->hidden * 2, 128) ||
+        !make_tmap_bf16(&tmB, a->x, a->hidden, T, (unsigned long long)a->hidden * 2, pl.bn))
+      return CSA2_ECUDA;
+    ProjParams p{};
+    p.mode = kProjDown;
+    p.n_tok = T;
+    p.k_steps = k_steps;
+    p.m_tiles = m_tiles;
+    p.ks = pl.ks;
+    p.bn = pl.bn;
+    p.stages = pl.stages;
+    p.out = cq;
+    p.out_ld = a->q_rank;
+    p.gain = a->g_q;
+    p.ss = ss;
+    p.dev_status = a->dev_status;
+    const cudaError_t e = launch_proj(tmA, tmB, p, 1, s);
+    if (e != cudaSuccess) return CSA2_ECUDA;
+  }
+  // up-projection with the RMSNorm factors and the per-head RMSNorm
+  {
+    const int m_tiles = a->n_heads * (CSA2_HEAD_DIM / 128), k_steps = a->q_rank / 64;
+    const ProjPlan pl = proj_plan(T, k_steps, m_tiles * ((T + proj_bn(T) - 1) / proj_bn(T)), false);
+    CUtensorMap tmA, tmB;
+    if (!make_tmap_bf16(&tmA, a->w_uq, a->q_rank, (unsigned long long)a->n_heads * CSA2_HEAD_DIM,
+                        (unsigned long long)a->q_rank * 2, 128) ||
+        !make_tmap_bf16(&tmB, cq, a->q_rank, T, (unsigned long long)a->q_rank * 2, pl.bn))
+      return CSA2_ECUDA;
+    ProjParams p{};
+    p.mode = kProjUp;
+    p.n_tok = T;
+    p.k_steps = k_steps;
+    p.m_tiles = m_tiles;
+    p.ks = 1;
+    p.bn = pl.bn;
+    p.stages = pl.stages;
+    p.out = a->q;
+    p.out_ld = (long long)a->n_heads * CSA2_HEAD_DIM;
+    p.gain = a->g_head;
+    p.ss = ss;
+    p.ss_tiles = a->q_rank / 128;
+    p.inv_rank = 1.f / (float)a->q_rank;
+    p.eps = a->eps;
+    p.dev_status = a->dev_status;
+    const cudaError_t e = launch_proj(tmA, tmB, p, 1, s);
+    if (e != cudaSuccess) return CSA2_ECUDA;
+  }
+  return CSA2_OK;
+}
+
+size_t csa2_out_proj_workspace_size(const csa2_out_proj_args* a) {
+  if (!a || a->n_tokens <= 0 || a->n_groups <= 0 || a->o_rank <= 0) return 0;
+  return align_up((size_t)a->n_tokens * a->n_groups * a->o_rank * 2);
+}
+
+csa2_status csa2_out_proj(const csa2_out_proj_args* a, void* stream) {
+  if (!a || a->n_tokens < 0) return CSA2_EINVAL;
+  if (a->n_tokens == 0) return CSA2_OK;
+  if (a->n_groups < 1 || a->n_heads < a->n_groups || a->n_heads % a->n_groups || a->n_heads > 4096 ||
+      a->o_rank < 128 || a->o_rank % 128 || a->hidden < 128 || a->hidden % 128)
+    return CSA2_EINVAL;
+  if (!a->o || !a->w_oa || !a->w_ob || !a->out || !aligned(a->o, 16) || !aligned(a->w_oa, 16) ||
+      !aligned(a->w_ob, 16) || !aligned(a->out, 16))
+    return CSA2_EINVAL;
+  if (!a->workspace || !aligned(a->workspace, 16) || a->workspace_bytes < csa2_out_proj_workspace_size(a))
+    return CSA2_EWORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = a->n_tokens, G = a->n_groups;
+  const long long kg = (long long)a->n_heads / G * CSA2_HEAD_DIM, cols = (long long)a->n_heads * CSA2_HEAD_DIM;
+  const long long yr = (long long)G * a->o_rank;
+  uint16_t* y = static_cast<uint16_t*>(a->workspace);
+  // per group: y_g = W_OA[g] o_g
+  {
+    const int m_tiles = a->o_rank / 128, k_steps = (int)(kg / 64);
+    const ProjPlan pl = proj_plan(T, k_steps, m_tiles * G * ((T + proj_bn(T) - 1) / proj_bn(T)), true);
+    CUtensorMap tmA, tmB;
+    if (!make_tmap_bf16(&tmA, a->w_oa, kg, (unsigned long long)yr, (unsigned long long)kg * 2, 128) ||
+        !make_tmap_bf16(&tmB, a->o, cols, T, (unsigned long long)cols * 2, pl.bn))
+      return CSA2_ECUDA;
+    ProjParams p{};
+    p.mode = kProjPlain;
+    p.n_tok = T;
+    p.k_steps = k_steps;
+    p.m_tiles = m_tiles;
+    p.ks = pl.ks;
+    p.bn = pl.bn;
+    p.stages = pl.stages;
+    p.a_rows_per_group = a->o_rank;
+    p.b_cols_per_group = (int)kg;
+    p.out = y;
+    p.out_ld = yr;
+    p.out_cols_per_group = a->o_rank;
+    p.dev_status = a->dev_status;
+    if (launch_proj(tmA, tmB, p, G, s) != cudaSuccess) return CSA2_ECUDA;
+  }
+  // out = W_OB y
+  {
+    const int m_tiles = a->hidden / 128, k_steps = (int)(yr / 64);
+    const ProjPlan pl = proj_plan(T, k_steps, m_tiles * ((T + proj_bn(T) - 1) / proj_bn(T)), true);
+    CUtensorMap tmA, tmB;
+    if (!make_tmap_bf16(&tmA, a->w_ob, yr, a->hidden, (unsigned long long)yr * 2, 128) ||
+        !make_tmap_bf16(&tmB, y, yr, T, (unsigned long long)yr * 2, pl.bn))
+      return CSA2_ECUDA;
+    ProjParams p{};
+    p.mode = kProjPlain;
+    p.n_tok = T;
+    p.k_steps = k_steps;
+    p.m_tiles = m_tiles;
+    p.ks = pl.ks;
+    p.bn = pl.bn;
+    p.stages = pl.stages;
+    p.out = a->out;
+    p.out_ld = a->hidden;
+    p.dev_status = a->dev_status;
+    if (launch_proj(tmA, tmB, p, 1, s) != cudaSuccess) return CSA2_ECUDA;
+  }
+  return CSA2_OK;
 }
 
 int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {

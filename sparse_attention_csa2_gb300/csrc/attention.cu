@@ -585,7 +585,14 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
       o[2 * j + 1] = x * sn + y * c;
     }
   }
-  *reinterpret_cast<float4*>(p.out + ((size_t)row * kHeads + h) * kHeadDim + d) = make_float4(o[0], o[1], o[2], o[3]);
+  const size_t at = ((size_t)row * kHeads + h) * kHeadDim + d;
+  if (p.out_bf16) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]), hi = __floats2bfloat162_rn(o[2], o[3]);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + at) = make_float4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 }  // namespace

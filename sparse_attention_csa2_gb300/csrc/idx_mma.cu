@@ -799,6 +799,19 @@ size_t dec_smem_bytes(int K, int max_seg_blocks, bool fp8) {
 
 bool mma_indexer_available() { return encode_fn() != nullptr; }
 
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, unsigned long long cols, unsigned long long rows,
+                    unsigned long long row_bytes, unsigned box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int mma_decode_max_seg_blocks() { return 2048; }
 
 int mma_decode_max_segment() { return kDecSegMax; }

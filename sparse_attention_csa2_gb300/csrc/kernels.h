@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace csa2 {
@@ -50,6 +51,10 @@ size_t scan_smem_bytes(int fmt, int K);
 
 // tcgen05 indexer: decode rows (bf16 or FP8 keys, records in place) and prefill tiles (bf16).
 bool mma_indexer_available();
+// Tensor map of a row-major bf16 matrix [rows x cols] (rows row_bytes apart): boxes of 64
+// columns x box_rows rows in the 128-byte swizzle, zeros outside the matrix.
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, unsigned long long cols, unsigned long long rows,
+                    unsigned long long row_bytes, unsigned box_rows);
 int mma_decode_max_seg_blocks();
 int mma_decode_max_segment();  // most records one decode segment may hold
 bool mma_decode_can_merge(int n_seg, int K);  // the decode scan can merge its segments' lists itself
@@ -118,7 +123,8 @@ struct AttnParams {
   double inv_freq[32];        // theta^(-2i/64), i = 0..31 (computed on the host in double)
   float* part_o;              // [n_rows, n_split, 64, 512]
   float* part_ml;             // [n_rows, n_split, 64, 2]
-  float* out;
+  void* out;                  // fp32, or bf16 when out_bf16
+  int out_bf16;
   float* sink_mass;
   int32_t* dev_status;        // optional: CSA2_EDEVICE_INDEX on an out-of-range record index
 };
@@ -141,6 +147,34 @@ cudaError_t launch_write_records(const WriteParams& p, cudaStream_t stream);
 // Sequence compressor (csa2_compress).
 cudaError_t launch_compress(long long n_entries, int ratio, const void* kv, const void* gate, bool x_f32, float* out,
                             cudaStream_t stream);
+
+// Projections around attention (csa2_query_proj, csa2_out_proj): one tcgen05 GEMM
+// out[t, f] = sum_k A[f, k] B[t, k] per launch, A = weights (features x K), B = activations
+// (tokens x K), with the epilogue of `mode`.
+enum ProjMode { kProjPlain = 0, kProjDown = 1, kProjUp = 2 };
+struct ProjParams {
+  int mode;
+  int n_tok;
+  int k_steps;                // K / 64 of one group
+  int m_tiles;                // features of one group / 128
+  int ks;                     // K splits, reduced across a cluster of ks blocks (1 for kProjUp)
+  int bn;                     // token tile: 32, 64, 128 or 256
+  int stages;
+  int a_rows_per_group;       // A row offset of group g: g * a_rows_per_group
+  int b_cols_per_group;       // B column offset of group g
+  void* out;                  // bf16 [n_tok, out_ld]; group g's features start at column g * out_cols_per_group
+  long long out_ld;
+  int out_cols_per_group;
+  const float* gain;          // kProjDown: [features]; kProjUp: [512], by feature % 512; null: 1
+  float* ss;                  // kProjDown: out [m_tiles, n_tok] sums of squares; kProjUp: in [ss_tiles, n_tok]
+  int ss_tiles;
+  float inv_rank;             // kProjUp: 1 / (ss_tiles * 128)
+  float eps;
+  int32_t* dev_status;
+};
+size_t proj_smem_bytes(int bn, int stages);
+cudaError_t launch_proj(const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjParams& p, int groups,
+                        cudaStream_t stream);
 
 int attn_smem_bytes();
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream);
