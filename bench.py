@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
     ap.add_argument("--prefill-t", type=int, default=4096, help="queries of the prefill chunk (profiling)")
+    ap.add_argument("--proj-only", choices=["decode", "prefill", "both"],
+                    help="time only the projections around attention (profiling)")
     ap.add_argument("--scan-only", metavar="FMT:ROWS:N",
                     help="time only the indexer scores of ROWS rows of N records (FMT bf16 or fp8; profiling)")
     return ap.parse_args(argv)
@@ -417,6 +419,69 @@ def run_writer(local, peaks, n=262144, iters=20):
     return out
 
 
+def run_projections(local, peaks, names=("decode", "prefill"), iters=20):
+    """Query low-rank path (csa2_query_proj) and grouped low-rank output projection
+    (csa2_out_proj) at the Flash shapes (hidden 4096, q rank 1024, 64 heads of 512, 8 output
+    groups of rank 1024): decode, 32 tokens, streams the 210 MB of weights (HBM-bound: bytes =
+    weights + activations and intermediates read and written); prefill, 4096 tokens, is
+    tensor-bound (2 x the four GEMMs' multiply-adds).  A 256 MiB buffer is written before each
+    timed call, so the weights come from HBM, not L2.  The same four GEMMs through
+    torch.matmul / bmm (cuBLAS, without the normalizations) are timed beside them."""
+    import torch
+    import synth
+    import sparse_attention_csa2_gb300 as S
+    dev = f"cuda:{local}"
+    hbm = float(peaks.get("hbm_gbs", 6800.0)) if peaks else 6800.0
+    tf = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(iters):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    out = {}
+    for name in names:
+        sh = synth.PROJECTIONS[name]
+        inp = {k: v.to(dev) for k, v in synth.projection_inputs(sh, seed=21).items()}
+        T, G, r, hd = sh.tokens, sh.groups, sh.o_rank, sh.heads * sh.head_dim
+        kg = hd // G
+        qp = S.QueryProj(inp["x"], inp["w_dq"], inp["w_uq"], inp["g_q"], inp["g_head"])
+        op = S.OutProj(inp["o"], inp["w_oa"], inp["w_ob"])
+        ms_q, ms_o = timed(qp), timed(op)
+        ms = timed(lambda: (qp(), op()))
+        x, wdq, wuq, o, woa, wob = (inp[k] for k in ("x", "w_dq", "w_uq", "o", "w_oa", "w_ob"))
+
+        def cublas():
+            q = (x @ wdq.T) @ wuq.T
+            y = torch.bmm(o.view(T, G, kg).transpose(0, 1), woa.transpose(1, 2))
+            return q, y.transpose(0, 1).reshape(T, G * r) @ wob.T
+
+        ms_cb = timed(cublas)
+        wbytes = sum(inp[k].numel() * 2 for k in ("w_dq", "w_uq", "w_oa", "w_ob"))
+        # x, q, o and out once; the rank-sized intermediates written and read once each
+        abytes = 2 * T * (sh.hidden + hd + hd + sh.hidden) + 2 * 2 * T * (sh.q_rank + G * r)
+        flops = 2.0 * T * (sh.hidden * sh.q_rank + sh.q_rank * hd + hd * r + G * r * sh.hidden)
+        nbytes = wbytes + abytes
+        out[name] = {"tokens": T, "ms": ms, "query_proj_ms": ms_q, "out_proj_ms": ms_o, "launches": 4,
+                     "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm,
+                     "tflops": flops / (ms / 1e3) / 1e12, "tensor_frac": flops / (ms / 1e3) / 1e12 / tf,
+                     "cublas_same_gemms_ms": ms_cb}
+        del qp, op, inp
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill(args, local, peaks):
     """Prefill chunk (B=1, T=4096 queries at positions 32768.., N=36864 bf16 keys): the
     indexer GEMM on the tensor cores alone, then the whole chunk (scores -> per-query top-512
@@ -487,6 +552,14 @@ def run_gb300(args, world, rank, local):
         return 0
     if args.scan_only:
         print(json.dumps({"scan": run_scan_only(args, local)}), flush=True)
+        return 0
+    if args.proj_only:
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except (OSError, ValueError):
+            peaks = None
+        names = ("decode", "prefill") if args.proj_only == "both" else (args.proj_only,)
+        print(json.dumps({"projections": run_projections(local, peaks, names)}), flush=True)
         return 0
     if args.prefill_only:
         try:
@@ -610,6 +683,7 @@ def run_gb300(args, world, rank, local):
     if not args.no_configs:
         configs = run_configs(local, peaks if peak_src == "measured" else None)
         configs["cache_writer"] = run_writer(local, peaks if peak_src == "measured" else None)
+        configs["projections"] = run_projections(local, peaks if peak_src == "measured" else None)
 
     cpu = None
     if not args.no_cpu_baseline:

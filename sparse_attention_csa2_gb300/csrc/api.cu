@@ -252,8 +252,11 @@ csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, c
 
 // ------------------------------------------------------------------ projections
 // Launch shape of one projection GEMM: token tile bn (the MMA's N), pipeline stages and the
-// K split ks.  The cost model counts pipeline steps of the busiest SM (blocks per SM x steps
-// per block) plus the split's reduction, and takes the cheapest; ties go to fewer splits.
+// K split ks (a cluster of ks blocks per tile).  The split is the smallest that puts a block
+// on at least 3/4 of the SMs (HBM streaming wants most SMs busy; every split adds a
+// distributed-shared-memory exchange).  A grid that fits on the SMs runs one block per SM with
+// a deep pipeline (~200 KB of loads in flight per SM); a larger one, with narrow token tiles,
+// two blocks per SM with half the stages each.
 struct ProjPlan {
   int bn, stages, ks;
 };
@@ -262,32 +265,23 @@ int proj_bn(int n_tok) { return n_tok <= 32 ? 32 : n_tok <= 64 ? 64 : n_tok <= 1
 
 // tiles: blocks of one K split (feature tiles x token tiles x groups)
 ProjPlan proj_plan(int n_tok, int k_steps, int tiles, bool allow_split) {
-  ProjPlan best{proj_bn(n_tok), 0, 1};
-  const size_t stage = 128 * 128 + (size_t)best.bn * 128;
-  // two blocks per SM for narrow token tiles (more loads in flight), else one with deep pipelines
-  const size_t budget = best.bn <= 64 ? 96 * 1024 : 200 * 1024;
-  const int base_stages = (int)std::min<size_t>(8, budget / stage);
+  const int bn = proj_bn(n_tok);
+  const size_t stage = 128 * 128 + (size_t)bn * 128;
   const int sms = sm_count();
+  int ks = 1;
   const int forced = env_int("CSA2_PROJ_KS", 0);
-  double best_cost = 1e30;
-  for (int ks = 1; ks <= 8; ks *= 2) {
-    if (ks > 1 && (!allow_split || ks > k_steps)) break;
-    if (forced > 0 && ks != forced) continue;
-    const size_t need = (size_t)(ks - 1) * best.bn * 128 * 4;  // block 0's slots for the partials
-    int stages = base_stages;
-    while ((size_t)stages * stage < need && stages < 8) ++stages;
-    if ((size_t)stages * stage < need || proj_smem_bytes(best.bn, stages) > 227 * 1024) continue;
-    const long long blocks = (long long)tiles * ks;
-    const double steps = (double)((k_steps + ks - 1) / ks);
-    const double cost = (double)((blocks + sms - 1) / sms) * steps + (ks > 1 ? 1.0 + 0.5 * (ks - 1) * best.bn / 32 : 0.0);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best.ks = ks;
-      best.stages = stages;
-    }
+  if (forced > 0) {
+    while (ks * 2 <= forced && ks < 8) ks *= 2;
+  } else {
+    while (allow_split && ks < 8 && (long long)tiles * ks * 4 < 3LL * sms) ks *= 2;
   }
-  if (best.stages == 0) best = ProjPlan{best.bn, base_stages, 1};  // a forced split that does not fit
-  return best;
+  if (!allow_split) ks = 1;
+  while (ks > 1 && ks > k_steps) ks /= 2;
+  const bool two_per_sm = (long long)tiles * ks > sms && bn <= 64;
+  const size_t budget = two_per_sm ? 100 * 1024 : 200 * 1024;
+  int stages = (int)std::min<size_t>(kProjMaxStages, budget / stage);
+  while ((size_t)stages * stage < proj_epilogue_bytes(bn, ks) && stages < kProjMaxStages) ++stages;
+  return ProjPlan{bn, stages, ks};
 }
 
 // ------------------------------------------------------------------ top-K plumbing
@@ -654,7 +648,7 @@ csa2_status csa2_compress(const csa2_compress_args* a, void* stream) {
 
 size_t csa2_query_proj_workspace_size(const csa2_query_proj_args* a) {
   if (!a || a->n_tokens <= 0 || a->q_rank <= 0) return 0;
-  return align_up((size_t)a->n_tokens * a->q_rank * 2) + align_up((size_t)(a->q_rank / 128) * a->n_tokens * 4);
+  return align_up((size_t)a->n_tokens * a->q_rank * 2) + align_up((size_t)(a->q_rank / 128) * 8 * a->n_tokens * 4);
 }
 
 csa2_status csa2_query_proj(const csa2_query_proj_args* a, void* stream) {
@@ -672,7 +666,8 @@ csa2_status csa2_query_proj(const csa2_query_proj_args* a, void* stream) {
   const int T = a->n_tokens;
   Carve c{static_cast<uint8_t*>(a->workspace)};
   uint16_t* cq = c.take<uint16_t>((size_t)T * a->q_rank);
-  float* ss = c.take<float>((size_t)(a->q_rank / 128) * T);
+  float* ss = c.take<float>((size_t)(a->q_rank / 128) * 8 * T);  // per feature tile and K split
+  int ss_tiles = 0;
   // down-projection: c * g_q in bf16 and per-token partial sums of squares
   {
     const int m_tiles = a->q_rank / 128, k_steps = a->hidden / 64;
@@ -694,6 +689,7 @@ csa2_status csa2_query_proj(const csa2_query_proj_args* a, void* stream) {
     p.gain = a->g_q;
     p.ss = ss;
     p.dev_status = a->dev_status;
+    ss_tiles = m_tiles * pl.ks;
     const cudaError_t e = launch_proj(tmA, tmB, p, 1, s);
     if (e != cudaSuccess) return CSA2_ECUDA;
   }
@@ -718,7 +714,7 @@ csa2_status csa2_query_proj(const csa2_query_proj_args* a, void* stream) {
     p.out_ld = (long long)a->n_heads * CSA2_HEAD_DIM;
     p.gain = a->g_head;
     p.ss = ss;
-    p.ss_tiles = a->q_rank / 128;
+    p.ss_tiles = ss_tiles;
     p.inv_rank = 1.f / (float)a->q_rank;
     p.eps = a->eps;
     p.dev_status = a->dev_status;

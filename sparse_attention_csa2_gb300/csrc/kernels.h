@@ -152,6 +152,7 @@ cudaError_t launch_compress(long long n_entries, int ratio, const void* kv, cons
 // out[t, f] = sum_k A[f, k] B[t, k] per launch, A = weights (features x K), B = activations
 // (tokens x K), with the epilogue of `mode`.
 enum ProjMode { kProjPlain = 0, kProjDown = 1, kProjUp = 2 };
+constexpr int kProjMaxStages = 12;
 struct ProjParams {
   int mode;
   int n_tok;
@@ -166,13 +167,16 @@ struct ProjParams {
   long long out_ld;
   int out_cols_per_group;
   const float* gain;          // kProjDown: [features]; kProjUp: [512], by feature % 512; null: 1
-  float* ss;                  // kProjDown: out [m_tiles, n_tok] sums of squares; kProjUp: in [ss_tiles, n_tok]
+  float* ss;                  // kProjDown: out [m_tiles * ks, n_tok] sums of squares; kProjUp: in [ss_tiles, n_tok]
   int ss_tiles;
-  float inv_rank;             // kProjUp: 1 / (ss_tiles * 128)
+  float inv_rank;             // kProjUp: 1 / (rank of the low-rank vector)
   float eps;
   int32_t* dev_status;
 };
 size_t proj_smem_bytes(int bn, int stages);
+// Bytes of the pipeline buffers the epilogue reuses (the staged output tile; with ks > 1 the
+// rows received from the cluster's blocks).
+size_t proj_epilogue_bytes(int bn, int ks);
 cudaError_t launch_proj(const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjParams& p, int groups,
                         cudaStream_t stream);
 

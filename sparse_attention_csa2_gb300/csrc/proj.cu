@@ -11,14 +11,16 @@
 // run the epilogue, one accumulator lane (feature) per thread.  Epilogues:
 //   plain  bf16 store; grouped, group g reads its own columns of B (its heads) and writes its
 //          own columns of out;
-//   down   bf16 store of acc * g_q[f], and per token the block's sum of acc^2 (the RMSNorm of
-//          the query's low-rank vector is finished by the next launch);
+//   down   bf16 store of acc * g_q[f], and per token the sum of acc^2 over the block's
+//          features (the RMSNorm of the query's low-rank vector is finished by the next
+//          launch);
 //   up     acc times the token's low-rank RMSNorm factor, then RMSNorm over each head's 512
 //          features: the four blocks of a head form a cluster and exchange their per-token
 //          sums of squares through distributed shared memory; then the head gain.
-// With ks > 1 the K range is split over a cluster of ks blocks: after every block's MMAs are
-// done, blocks 1..ks-1 write their accumulators into block 0's idle pipeline buffers and block
-// 0 adds them in rank order.
+// The output tile is staged in the (then idle) pipeline buffers as token rows and written with
+// 16-byte stores.  With ks > 1 the K range is split over a cluster of ks blocks; each block
+// stages its fp32 accumulator, and block r reads rows [r R, r R + R) (R = 128 / ks) of every
+// block's staged tile, adds them in rank order and finishes those rows.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -27,7 +29,6 @@ namespace csa2 {
 namespace {
 
 constexpr int kProjThreads = 192;
-constexpr int kProjMaxStages = 8;
 constexpr int kATile = 128 * 128;  // 128 weight rows x 64 bf16 (128 bytes)
 
 struct ProjShared {
@@ -37,9 +38,10 @@ struct ProjShared {
   uint32_t tmem_base;
   int timeout;
   int issued, consumed;
-  float tok[256];     // up: per-token factor
+  alignas(16) float tok[256];  // up: per-token factor (read as float4)
   float red[4][256];  // per epilogue warp and token: sums of squares over the warp's 32 features
   float xch[4][256];  // up: per cluster rank and token: that block's sum of squares
+  float gain[128];    // the gain of each of the tile's features (1 without gains)
 };
 
 __device__ __forceinline__ uint8_t* align1024_proj(uint8_t* p) {
@@ -52,6 +54,19 @@ __device__ __forceinline__ void proj_timeout(int* flag, int32_t* dev_status) {
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
 __device__ __forceinline__ void cluster_st_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
+
+// A load from another block's shared memory that the compiler may schedule freely (the data
+// is ordered by the cluster barrier before it).
+__device__ __forceinline__ uint4 cluster_ld_v4_nv(uint32_t addr) {
+  uint4 v;
+  asm("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // 32 values per lane -> lane l returns the warp's sum of value l (a butterfly: at each step a
@@ -171,6 +186,13 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         sh.tok[j] = rsqrtf(s * p.inv_rank + p.eps);
       }
     }
+    // the tile's gains, read while the MMAs run
+    {
+      const int f = m_tile * 128 + et;
+      sh.gain[et] = p.gain == nullptr || p.mode == kProjPlain ? 1.f
+                    : __ldg(p.gain + (p.mode == kProjUp ? (f & (kHeadDim - 1)) : f));
+    }
+    epi_sync();  // the gains are read by other threads than their writers
     if (!tc05::mbar_wait(&sh.done, 0) && lane == 0) proj_timeout(&sh.timeout, p.dev_status);
     tc05::fence_after();
   }
@@ -178,37 +200,97 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   __syncthreads();
   const bool clustered = p.ks > 1 || p.mode == kProjUp;
   const uint32_t rank = clustered ? cluster_rank() : 0u;
-  if (clustered) cluster_sync();  // every block of the cluster has its accumulator
+  // every block of the cluster has its accumulator, so every pipeline buffer is idle
+  if (clustered) cluster_sync();
 
   const int quarter = warp & 3;                 // TMEM lanes 32 * quarter .. + 31
   const int row = 32 * quarter + lane;          // this thread's feature within the tile
-  const int f = m_tile * 128 + row;             // ... within the group
   const int et = tid - 64;
+  const bool epi = warp >= 2;
   const uint32_t t_lane = tmem + ((uint32_t)(32 * quarter) << 16);
-  float* slots = reinterpret_cast<float*>(ring);  // block 0: [ks - 1][bn][128] partial accumulators
   const int n_chunks = p.bn / 32;
+  __nv_bfloat16* const outg = static_cast<__nv_bfloat16*>(p.out) + (size_t)g * p.out_cols_per_group + m_tile * 128;
 
-  if (warp >= 2) {
-    if (p.ks > 1 && rank != 0) {
-      // ---------------------------------------------------------------- split-K: send
-      const uint32_t dst = cluster_map(slots, 0) + (uint32_t)(((int)(rank - 1) * p.bn) * 128 + row) * 4u;
+  if (p.ks > 1) {
+    // ---------------------------------------------------------------- split K
+    // every block stages its accumulator as token rows, [bn][128 + 4] fp32; block r then reads
+    // rows [r R, r R + R) (R = 128 / ks) of every block's staged tile through distributed shared
+    // memory, adds them in rank order and finishes those features, 8 per thread and token
+    constexpr int kLd = 128 + 4;
+    float* stg = reinterpret_cast<float*>(ring);
+    if (epi) {
       for (int c = 0; c < n_chunks; ++c) {
         uint32_t v[32];
         tc05::tmem_ld32(t_lane + 32 * c, v);
         tc05::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) cluster_st_f32(dst + (uint32_t)((32 * c + j) * 128) * 4u, __uint_as_float(v[j]));
+        for (int j = 0; j < 32; ++j) stg[(32 * c + j) * kLd + row] = __uint_as_float(v[j]);
       }
-    } else if (p.mode == kProjUp) {
-      // ---------------------------------------------------------------- up: head sums
+    }
+    cluster_sync();  // every block's tile is staged
+    if (epi) {
+      const int R = 128 / p.ks, n_oct = R / 8, f0 = (int)rank * R;
+      // bn * n_oct is a multiple of 64, so whole warps take part in every iteration
+      for (int i = et; i < p.bn * n_oct; i += 128) {
+        const int t = i / n_oct, o = i - t * n_oct, tok = n0 + t;
+        const uint32_t off = (uint32_t)(t * kLd + f0 + 8 * o) * 4u;
+        // all of the (at most 8) blocks' pieces are requested before any is added, so the
+        // remote loads overlap
+        uint4 lo[8], hi[8];
+#pragma unroll
+        for (int src = 0; src < 8; ++src) {
+          if (src < p.ks) {
+            const uint32_t at = cluster_map(stg, (uint32_t)src) + off;
+            lo[src] = cluster_ld_v4_nv(at);
+            hi[src] = cluster_ld_v4_nv(at + 16u);
+          }
+        }
+        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int src = 0; src < 8; ++src) {
+          if (src < p.ks) {
+            y[0] += __uint_as_float(lo[src].x), y[1] += __uint_as_float(lo[src].y);
+            y[2] += __uint_as_float(lo[src].z), y[3] += __uint_as_float(lo[src].w);
+            y[4] += __uint_as_float(hi[src].x), y[5] += __uint_as_float(hi[src].y);
+            y[6] += __uint_as_float(hi[src].z), y[7] += __uint_as_float(hi[src].w);
+          }
+        }
+        float ss = 0.f;
+        if (p.mode == kProjDown) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ss = fmaf(y[k], y[k], ss);
+            y[k] *= sh.gain[f0 + 8 * o + k];
+          }
+          for (int w = n_oct >> 1; w >= 1; w >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, w);
+        }
+        if (tok < p.n_tok) {
+          uint4 w;
+          w.x = pack_bf16x2(y[0], y[1]), w.y = pack_bf16x2(y[2], y[3]);
+          w.z = pack_bf16x2(y[4], y[5]), w.w = pack_bf16x2(y[6], y[7]);
+          *reinterpret_cast<uint4*>(outg + (size_t)tok * p.out_ld + f0 + 8 * o) = w;
+          if (p.mode == kProjDown && o == 0) p.ss[(size_t)(m_tile * p.ks + (int)rank) * p.n_tok + tok] = ss;
+        }
+      }
+    }
+    cluster_sync();  // no block leaves while the others read its staged tile
+  } else {
+    // ---------------------------------------------------------------- whole K in this block
+    if (epi && p.mode == kProjUp) {
+      // per token, this block's sum of squares over its 128 features, sent to the cluster
       for (int c = 0; c < n_chunks; ++c) {
         uint32_t v[32];
         tc05::tmem_ld32(t_lane + 32 * c, v);
-        tc05::tmem_ld_wait();
         float a[32];
 #pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 q = *reinterpret_cast<const float4*>(&sh.tok[32 * c + j]);
+          a[j] = q.x, a[j + 1] = q.y, a[j + 2] = q.z, a[j + 3] = q.w;
+        }
+        tc05::tmem_ld_wait();
+#pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float x = __uint_as_float(v[j]) * sh.tok[32 * c + j];
+          const float x = __uint_as_float(v[j]) * a[j];
           a[j] = x * x;
         }
         sh.red[quarter][32 * c + lane] = warp_sum_scatter32(a, lane);
@@ -219,54 +301,61 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         for (uint32_t r = 0; r < 4; ++r) cluster_st_f32(cluster_map(&sh.xch[rank][j], r), part);
       }
     }
-  }
-  if (clustered) cluster_sync();  // partial accumulators and head sums are in place
-
-  if (warp >= 2 && (p.ks == 1 || rank == 0)) {
-    // ---------------------------------------------------------------- finish and store
-    if (p.mode == kProjUp) {
-      for (int j = et; j < p.bn; j += 128) {
-        const float tot = (sh.xch[0][j] + sh.xch[1][j]) + (sh.xch[2][j] + sh.xch[3][j]);
-        sh.tok[j] *= rsqrtf(tot * (1.f / (float)kHeadDim) + p.eps);
+    if (clustered) cluster_sync();  // the head sums are in place
+    if (epi) {
+      if (p.mode == kProjUp) {
+        for (int j = et; j < p.bn; j += 128) {
+          const float tot = (sh.xch[0][j] + sh.xch[1][j]) + (sh.xch[2][j] + sh.xch[3][j]);
+          sh.tok[j] *= rsqrtf(tot * (1.f / (float)kHeadDim) + p.eps);
+        }
+        epi_sync();
+      }
+      // the tile's output goes through shared memory, [bn tokens][128 features] bf16 rows
+      // (padded), and out to global memory in 16-byte pieces
+      constexpr int kSld = 128 + 8;
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(ring);
+      const float gain = sh.gain[row];
+      for (int c = 0; c < n_chunks; ++c) {
+        uint32_t v[32];
+        tc05::tmem_ld32(t_lane + 32 * c, v);
+        // per-token factors in registers first: the staging stores below could alias them
+        float fac[32];
+        if (p.mode == kProjUp) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(&sh.tok[32 * c + j]);
+            fac[j] = q.x * gain, fac[j + 1] = q.y * gain, fac[j + 2] = q.z * gain, fac[j + 3] = q.w * gain;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) fac[j] = p.mode == kProjDown ? gain : 1.f;
+        }
+        tc05::tmem_ld_wait();
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = __uint_as_float(v[j]);
+          stage[(32 * c + j) * kSld + row] = __float2bfloat16_rn(acc[j] * fac[j]);
+        }
+        if (p.mode == kProjDown) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] *= acc[j];
+          sh.red[quarter][32 * c + lane] = warp_sum_scatter32(acc, lane);
+        }
       }
       epi_sync();
-    }
-    const float gain = p.gain == nullptr ? 1.f : __ldg(p.gain + (p.mode == kProjUp ? (f & (kHeadDim - 1)) : f));
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)g * p.out_cols_per_group + f;
-    for (int c = 0; c < n_chunks; ++c) {
-      uint32_t v[32];
-      tc05::tmem_ld32(t_lane + 32 * c, v);
-      tc05::tmem_ld_wait();
-      float acc[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(v[j]);
-      for (int r = 1; r < p.ks; ++r) {
-        const float* src = slots + ((size_t)(r - 1) * p.bn + 32 * c) * 128 + row;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] += src[j * 128];
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int t = n0 + 32 * c + j;
-        float y = acc[j];
-        if (p.mode == kProjDown)
-          y *= gain;
-        else if (p.mode == kProjUp)
-          y = y * sh.tok[32 * c + j] * gain;
-        if (t < p.n_tok) out[(size_t)t * p.out_ld] = __float2bfloat16_rn(y);
+      for (int i = et; i < p.bn * 16; i += 128) {
+        const int t = i >> 4, pc = i & 15;
+        if (n0 + t < p.n_tok)
+          *reinterpret_cast<uint4*>(outg + (size_t)(n0 + t) * p.out_ld + pc * 8) =
+              *reinterpret_cast<const uint4*>(stage + t * kSld + pc * 8);
       }
       if (p.mode == kProjDown) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] *= acc[j];
-        sh.red[quarter][32 * c + lane] = warp_sum_scatter32(acc, lane);
-      }
-    }
-    if (p.mode == kProjDown) {
-      epi_sync();
-      for (int j = et; j < p.bn; j += 128) {
-        const int t = n0 + j;
-        if (t < p.n_tok)
-          p.ss[(size_t)m_tile * p.n_tok + t] = (sh.red[0][j] + sh.red[1][j]) + (sh.red[2][j] + sh.red[3][j]);
+        for (int j = et; j < p.bn; j += 128) {
+          const int t = n0 + j;
+          if (t < p.n_tok)
+            p.ss[(size_t)m_tile * p.n_tok + t] = (sh.red[0][j] + sh.red[1][j]) + (sh.red[2][j] + sh.red[3][j]);
+        }
       }
     }
   }
@@ -289,6 +378,11 @@ __global__ void __launch_bounds__(kProjThreads, 1)
 
 }  // namespace
 
+size_t proj_epilogue_bytes(int bn, int ks) {
+  // the staged tile: fp32 accumulators with a K split, else the bf16 output
+  return ks > 1 ? (size_t)bn * (128 + 4) * 4 : (size_t)bn * (128 + 8) * 2;
+}
+
 size_t proj_smem_bytes(int bn, int stages) {
   return 1024 + (size_t)stages * (kATile + (size_t)bn * 128) + sizeof(ProjShared);
 }
@@ -297,6 +391,8 @@ cudaError_t launch_proj(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pr
                         cudaStream_t stream) {
   if (p.stages < 1 || p.stages > kProjMaxStages) return cudaErrorInvalidValue;
   const size_t smem = proj_smem_bytes(p.bn, p.stages);
+  if (smem > 227 * 1024 || (size_t)p.stages * (kATile + (size_t)p.bn * 128) < proj_epilogue_bytes(p.bn, p.ks))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // may start before the preceding kernel in the stream has finished (programmatic dependent

@@ -3,13 +3,14 @@ projection) with the oracle, from tiny shapes with ragged token counts to the Fl
 decode (32 tokens) and prefill (4096 tokens, sampled rows); and the attention's bf16 output,
 the output projection's input.
 
-Tolerance, from the arithmetic: both paths take bf16 inputs exactly; the kernels accumulate
-in fp32 (error far below what follows), round the rank-sized intermediate (c * g_q, or y) to
-bf16 (relative error <= 2^-9 per element; summed over the next projection's K terms with
-random weights it adds an error of standard deviation about 2^-9 / sqrt(3) of the output's
-RMS, 0.0011) and round the output to bf16 (<= 2^-9 relative).  The bound checked per element
-is 2^-8 |ref| + 8e-3 RMS(ref): twice the output rounding plus about seven standard deviations
-of the intermediate's.
+Tolerance, from the arithmetic (bf16 keeps 8 significant bits: unit roundoff u = 2^-8): both
+paths take bf16 inputs exactly; the kernels accumulate in fp32 (error far below what
+follows), round the rank-sized intermediate (c * g_q, or y) to bf16 (relative error <= u per
+element, spread about uniformly; summed over the next projection's K terms with random
+weights it adds an error of standard deviation at most u / sqrt(3) of the output's RMS,
+0.0023) and round the output to bf16 (<= u relative).  The bound checked per element is
+u |ref| + 1.6e-2 RMS(ref): the output rounding plus seven standard deviations of the
+intermediate's.
 """
 from __future__ import annotations
 
@@ -38,8 +39,9 @@ def _check(got, ref):
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     rms = np.sqrt(np.mean(ref ** 2))
     err = np.abs(got - ref)
-    bound = 2.0 ** -8 * np.abs(ref) + 8e-3 * rms
+    bound = 2.0 ** -8 * np.abs(ref) + 1.6e-2 * rms
     worst = float(np.max(err / bound))
+    print(f"[worst {worst:.3f} of the bound]", end=" ")
     assert worst <= 1.0, f"worst error {worst:.3f} of the bound (max abs {err.max():.3e}, rms {rms:.3e})"
     return worst
 
