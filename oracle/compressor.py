@@ -17,12 +17,25 @@ Readings (the pages print no formula):
 * causality: an entry is visible to a query at position p only when all its tokens are,
   i.e. the first (p + 1) // m entries (the V4 page's causal rule for compressed entries:
   an entry holding a future token is forbidden to core attention).
+
+The encoder bank's memory (encoder_memory), from "Every layer, connected" (the global and
+index paths: global memory is created once and indexer keys are derived from the main KV) and
+the V4 page (the compressed KV carries absolute positions; the cache is rotated before it is
+stored):
+* the compressor's output is float32 (the type it hands on);
+* entry e's position is that of its last token, m*e + m - 1 (the position at which it
+  becomes visible), and its latent cache row is the writer's bf16 record rotated there;
+* its indexer key is W_IK times the entry (unrotated, in bf16), rounded once to bf16.
 """
 from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["compress", "visible_entries"]
+from .csa2 import bf16_to_f64
+from .projections import linear
+from .writer import write_records
+
+__all__ = ["compress", "visible_entries", "bf16_round_f64", "encoder_memory"]
 
 
 def compress(kv, gate, ratio: int) -> np.ndarray:
@@ -42,3 +55,24 @@ def compress(kv, gate, ratio: int) -> np.ndarray:
 def visible_entries(pos, ratio: int):
     """Entries visible to a query at position pos: those whose every token is at or before it."""
     return (np.asarray(pos, np.int64) + 1) // ratio
+
+
+def bf16_round_f64(x) -> np.ndarray:
+    """bf16 bit patterns of float64 values rounded once to bf16's 8 significant bits, to
+    nearest with ties to even (no intermediate float32 rounding); normal range only."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)                          # x = m 2^e, 0.5 <= |m| < 1
+    r = np.rint(m * 256.0) * np.exp2(e - 8.0)   # 8 significant bits, ties to even
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def encoder_memory(kv, gate, ratio: int, w_ik, theta: float = 10000.0) -> dict:
+    """One encoder bank's memory from its tokens' projections kv, gate [T, 512]: entries
+    (float32), their positions, the latent cache rows (bf16 bits, rotated) and the indexer
+    keys (bf16 bits) = W_IK [128, 512] times the unrotated bf16 entry."""
+    entries = compress(kv, gate, ratio).astype(np.float32)
+    pos = np.arange(entries.shape[0], dtype=np.int64) * ratio + ratio - 1
+    lat, _ = write_records(entries, pos, theta, "bf16")
+    plain, _ = write_records(entries, None, theta, "bf16")
+    keys = bf16_round_f64(linear(bf16_to_f64(plain), w_ik))
+    return {"entries": entries, "pos": pos, "lat": lat, "k_idx": keys}

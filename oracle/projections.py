@@ -26,7 +26,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["rms_norm", "query_proj", "out_proj"]
+__all__ = ["rms_norm", "query_proj", "out_proj", "linear"]
 
 
 def rms_norm(v, gain=None, eps: float = 1e-6) -> np.ndarray:
@@ -66,3 +66,8 @@ def out_proj(o, w_oa, w_ob) -> np.ndarray:
         og = o[:, g * (H // G):(g + 1) * (H // G), :].reshape(T, kg)   # the group's heads, concatenated
         y[:, g * r:(g + 1) * r] = og @ w_oa[g].T
     return y @ np.asarray(w_ob, np.float64).T
+
+
+def linear(x, w) -> np.ndarray:
+    """x [T, in] times w [out, in] transposed, in float64."""
+    return np.asarray(x, np.float64) @ np.asarray(w, np.float64).T

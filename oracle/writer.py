@@ -29,7 +29,8 @@ import numpy as np
 
 from .csa2 import e4m3_to_f64, e2m1_to_f64
 
-__all__ = ["e4m3_round", "e2m1_round", "fp4_quantize", "fp8_quantize_rows", "rotate_f32", "write_records"]
+__all__ = ["e4m3_round", "e2m1_round", "bf16_round", "fp4_quantize", "fp8_quantize_rows", "rotate_f32",
+           "write_records"]
 
 # the 127 non-negative finite E4M3 values, in code order (0x00 .. 0x7E)
 _E4M3 = e4m3_to_f64(np.arange(127, dtype=np.uint8))
@@ -57,6 +58,15 @@ def e4m3_round(x) -> np.ndarray:
     x = np.asarray(x, np.float32).astype(np.float64)
     idx = _round_to_table(np.abs(x), _E4M3)
     return (idx | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)  # the sign survives a zero result
+
+
+def bf16_round(x) -> np.ndarray:
+    """bf16 bit patterns (uint16) of float32 values: the upper 16 bits after rounding the lower
+    16 to nearest, ties to an even upper half (IEEE round-to-nearest-even into bf16's 8
+    significant bits); finite inputs only."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
 
 
 def e2m1_round(q) -> np.ndarray:
@@ -114,7 +124,8 @@ def rotate_f32(x, pos, theta: float, R: int = 64):
 
 def write_records(x, pos, theta: float, fmt: str, group: int = 16):
     """The writer on records x [n, D] float32 at positions pos [n] (None: no rotation):
-    fmt 'fp4' -> (codes [n, D/2], scale codes [n, D/group]); 'fp8' -> (codes [n, D], scales [n])."""
+    fmt 'fp4' -> (codes [n, D/2], scale codes [n, D/group]); 'fp8' -> (codes [n, D], scales [n]);
+    'bf16' -> (bf16 bit patterns [n, D], None)."""
     x = np.asarray(x, np.float32)
     if pos is not None:
         x = rotate_f32(x, pos, theta)
@@ -122,4 +133,6 @@ def write_records(x, pos, theta: float, fmt: str, group: int = 16):
         return fp4_quantize(x, group)
     if fmt == "fp8":
         return fp8_quantize_rows(x)
+    if fmt == "bf16":
+        return bf16_round(x), None
     raise ValueError(fmt)

@@ -600,3 +600,52 @@ def test_out_proj_is_a_block_diagonal_product():
     w_ob2 = w_ob.copy()
     w_ob2[:, 2 * r:3 * r] = 0.0
     assert np.allclose(O.out_proj(o2, w_oa, w_ob2), O.out_proj(o, w_oa, w_ob2), atol=1e-12)
+
+
+def test_bf16_round_matches_torch_and_ties_to_even():
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(50000) * np.exp2(rng.integers(-30, 30, 50000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.bf16_round(x), ref)
+    # exact ties: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 -> even (1); 1 + 3 * 2^-8 -> 1 + 2^-6
+    t = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8)], np.float32)
+    assert list(O.bf16_round(t)) == [0x3F80, 0x3F82, 0xBF80]
+
+
+def test_bf16_round_f64_rounds_once():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal(20000).astype(np.float32).astype(np.float64)  # float32 values: no double rounding
+    assert np.array_equal(O.bf16_round_f64(x), O.bf16_round(x.astype(np.float32)))
+    # just above a bf16 tie: float32 would round to the tie first and then to even
+    y = np.array([1 + 2 ** -8 + 2 ** -30, -(1 + 2 ** -8 + 2 ** -30), 1 + 2 ** -8])
+    assert list(O.bf16_round_f64(y)) == [0x3F81, 0xBF81, 0x3F80]
+    assert list(O.bf16_round(y.astype(np.float32))) == [0x3F80, 0xBF80, 0x3F80]
+
+
+def test_encoder_memory_positions_causality_and_parts():
+    rng = np.random.default_rng(23)
+    T = 41  # 20 entries of two tokens; the last token forms no entry
+    kv = rng.standard_normal((T, 512)).astype(np.float32)
+    gate = rng.standard_normal((T, 512)).astype(np.float32)
+    w_ik = (rng.standard_normal((128, 512)) / np.sqrt(512)).astype(np.float32)
+    m = O.encoder_memory(kv, gate, 2, w_ik)
+    assert m["lat"].shape == (20, 512) and m["k_idx"].shape == (20, 128)
+    assert list(m["pos"][:3]) == [1, 3, 5] and int(m["pos"][-1]) == 39
+    # an entry becomes visible with its last token
+    assert [int(O.visible_entries(p, 2)) for p in (0, 1, 2, 3, 39, 40)] == [0, 1, 1, 2, 20, 20]
+    # entries depend only on their own tokens: changing tokens 10.. leaves entries 0..4 alone
+    kv2, gate2 = kv.copy(), gate.copy()
+    kv2[10:] += 1.0
+    gate2[10:] -= 2.0
+    m2 = O.encoder_memory(kv2, gate2, 2, w_ik)
+    assert np.array_equal(m2["lat"][:5], m["lat"][:5]) and np.array_equal(m2["k_idx"][:5], m["k_idx"][:5])
+    assert not np.array_equal(m2["lat"][5], m["lat"][5])
+    # the latent row is the entry rotated at its position, within bf16 rounding
+    lat = O.bf16_to_f64(m["lat"])
+    rot = O.rotate_f32(m["entries"], m["pos"], 10000.0).astype(np.float64)
+    assert np.all(np.abs(lat - rot) <= 2.0 ** -8 * np.abs(rot))
+    assert np.array_equal(lat[:, :448], O.bf16_to_f64(O.bf16_round(m["entries"][:, :448])))
+    # the key is W_IK times the unrotated bf16 entry, within bf16 rounding
+    plain = O.bf16_to_f64(O.bf16_round(m["entries"]))
+    ref = plain @ w_ik.astype(np.float64).T
+    assert np.all(np.abs(O.bf16_to_f64(m["k_idx"]) - ref) <= 2.0 ** -8 * np.abs(ref))
