@@ -323,9 +323,12 @@ typedef struct {
                                  [seq, N, ...] cache); rows outside [0, cache_rows) are skipped
                                  and reported through dev_status */
   int64_t cache_rows;
-  int32_t out_dtype;          /* CSA2_FP4_E2M1_G16, CSA2_FP4_E2M1_G32 or CSA2_FP8_E4M3_ROWSCALE */
-  void* codes;                /* [cache_rows, 256] (FP4) or [cache_rows, 512] (FP8) uint8 */
-  void* scales;               /* FP4: [cache_rows, 512 / G] E4M3 uint8; FP8: [cache_rows] float32 */
+  int32_t out_dtype;          /* CSA2_FP4_E2M1_G16, CSA2_FP4_E2M1_G32, CSA2_FP8_E4M3_ROWSCALE or
+                                 CSA2_BF16 (the rotated record rounded to nearest even) */
+  void* codes;                /* [cache_rows, 256] (FP4) or [cache_rows, 512] (FP8) uint8, or
+                                 [cache_rows, 512] bf16 */
+  void* scales;               /* FP4: [cache_rows, 512 / G] E4M3 uint8; FP8: [cache_rows] float32;
+                                 bf16: unused (may be NULL) */
   int32_t* dev_status;        /* optional device int32: CSA2_EDEVICE_INDEX on a skipped row */
 } csa2_write_args;
 
@@ -417,6 +420,26 @@ typedef struct {
 /* Pointers device, 16-byte aligned. */
 size_t csa2_out_proj_workspace_size(const csa2_out_proj_args* a);
 csa2_status csa2_out_proj(const csa2_out_proj_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * csa2_linear - one plain projection out = x W^T on the tensor cores (bf16 inputs, fp32
+ * accumulation, bf16 output rounded to nearest even): the building block of the path's
+ * other linear maps, e.g. the encoder's indexer keys derived from its compressed entries
+ * ("DeepSeek V4.1-Flash. Every layer, connected", "The global and index paths": indexer
+ * keys come from the main KV).  One kernel launch.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t n_tokens;           /* T >= 0 */
+  int32_t in_features;        /* multiple of 64 */
+  int32_t out_features;       /* multiple of 128 */
+  const void* x;              /* [T, in_features] bf16 */
+  const void* w;              /* [out_features, in_features] bf16 */
+  void* out;                  /* out [T, out_features] bf16 */
+  int32_t* dev_status;        /* as in csa2_query_proj_args */
+} csa2_linear_args;
+
+/* Pointers device, 16-byte aligned. */
+csa2_status csa2_linear(const csa2_linear_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Utilities

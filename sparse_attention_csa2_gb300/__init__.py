@@ -87,6 +87,11 @@ class QueryProjArgs(C.Structure):
                 ("workspace", _vp), ("workspace_bytes", _sz), ("dev_status", _vp)]
 
 
+class LinearArgs(C.Structure):
+    _fields_ = [("n_tokens", _i32), ("in_features", _i32), ("out_features", _i32), ("x", _vp), ("w", _vp),
+                ("out", _vp), ("dev_status", _vp)]
+
+
 class OutProjArgs(C.Structure):
     _fields_ = [("n_tokens", _i32), ("n_heads", _i32), ("n_groups", _i32), ("o_rank", _i32), ("hidden", _i32),
                 ("o", _vp), ("w_oa", _vp), ("w_ob", _vp), ("out", _vp), ("workspace", _vp),
@@ -118,6 +123,7 @@ _query_proj = _sig("csa2_query_proj", [C.POINTER(QueryProjArgs), _vp], C.c_int)
 _query_proj_ws = _sig("csa2_query_proj_workspace_size", [C.POINTER(QueryProjArgs)], _sz)
 _out_proj = _sig("csa2_out_proj", [C.POINTER(OutProjArgs), _vp], C.c_int)
 _out_proj_ws = _sig("csa2_out_proj_workspace_size", [C.POINTER(OutProjArgs)], _sz)
+_linear = _sig("csa2_linear", [C.POINTER(LinearArgs), _vp], C.c_int)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
 
@@ -277,8 +283,9 @@ def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, s
 
 def write_records(x, dst_row, codes, scales, out_dtype: int, pos=None, theta: float = 10000.0, dev_status=None):
     """Writes records x [n, 512] (float32 or bf16, before rotation) into a cache at rows
-    dst_row [n] (int64): codes [rows, 256] uint8 + scales [rows, 512/G] uint8 (FP4), or codes
-    [rows, 512] uint8 + scales [rows] float32 (FP8).  pos [n] (int64): positions whose rotary
+    dst_row [n] (int64): codes [rows, 256] uint8 + scales [rows, 512/G] uint8 (FP4), codes
+    [rows, 512] uint8 + scales [rows] float32 (FP8), or codes [rows, 512] bf16 and scales None
+    (BF16).  pos [n] (int64): positions whose rotary
     coordinates the records take first (None: no rotation)."""
     a = WriteArgs()
     a.n_rows = x.shape[0]
@@ -452,3 +459,18 @@ def query_proj(x, w_dq, w_uq, g_q=None, g_head=None, eps: float = 1e-6):
 def out_proj(o, w_oa, w_ob):
     """Hidden-size output [T, hidden] bf16 of attention's output o (see OutProj)."""
     return OutProj(o, w_oa, w_ob)()
+
+
+def linear(x, w):
+    """out [T, out_features] bf16 = x [T, in_features] bf16 times w [out_features,
+    in_features] bf16 transposed (fp32 accumulation on the tensor cores)."""
+    _bf16_2d(x, "x")
+    _bf16_2d(w, "w")
+    if x.shape[1] != w.shape[1]:
+        raise ValueError("x and w disagree on in_features")
+    out = torch.empty((x.shape[0], w.shape[0]), dtype=torch.bfloat16, device=x.device)
+    a = LinearArgs()
+    a.n_tokens, a.in_features, a.out_features = x.shape[0], x.shape[1], w.shape[0]
+    a.x, a.w, a.out = _ptr(x), _ptr(w), _ptr(out)
+    _check(_linear(C.byref(a), _stream()), "csa2_linear")
+    return out

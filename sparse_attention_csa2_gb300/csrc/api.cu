@@ -615,9 +615,10 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
 csa2_status csa2_write_records(const csa2_write_args* a, void* stream) {
   if (!a || a->n_rows < 0) return CSA2_EINVAL;
   if (a->n_rows == 0) return CSA2_OK;
-  if (!a->x || !a->dst_row || !a->codes || !a->scales || a->cache_rows < 1) return CSA2_EINVAL;
-  const bool fp8 = a->out_dtype == CSA2_FP8_E4M3_ROWSCALE;
-  if (!fp8 && a->out_dtype != CSA2_FP4_E2M1_G16 && a->out_dtype != CSA2_FP4_E2M1_G32) return CSA2_EINVAL;
+  if (!a->x || !a->dst_row || !a->codes || (!a->scales && a->out_dtype != CSA2_BF16) || a->cache_rows < 1)
+    return CSA2_EINVAL;
+  const bool fp8 = a->out_dtype == CSA2_FP8_E4M3_ROWSCALE, bf16 = a->out_dtype == CSA2_BF16;
+  if (!fp8 && !bf16 && a->out_dtype != CSA2_FP4_E2M1_G16 && a->out_dtype != CSA2_FP4_E2M1_G32) return CSA2_EINVAL;
   if (!aligned(a->x, 16) || !aligned(a->codes, 16) || !aligned(a->dst_row, 8) || (a->pos && !aligned(a->pos, 8)) ||
       (fp8 && !aligned(a->scales, 4)))
     return CSA2_EINVAL;
@@ -791,6 +792,33 @@ csa2_status csa2_out_proj(const csa2_out_proj_args* a, void* stream) {
     if (launch_proj(tmA, tmB, p, 1, s) != cudaSuccess) return CSA2_ECUDA;
   }
   return CSA2_OK;
+}
+
+csa2_status csa2_linear(const csa2_linear_args* a, void* stream) {
+  if (!a || a->n_tokens < 0) return CSA2_EINVAL;
+  if (a->n_tokens == 0) return CSA2_OK;
+  if (a->in_features < 64 || a->in_features % 64 || a->out_features < 128 || a->out_features % 128)
+    return CSA2_EINVAL;
+  if (!a->x || !a->w || !a->out || !aligned(a->x, 16) || !aligned(a->w, 16) || !aligned(a->out, 16))
+    return CSA2_EINVAL;
+  const int T = a->n_tokens, m_tiles = a->out_features / 128, k_steps = a->in_features / 64;
+  const ProjPlan pl = proj_plan(T, k_steps, m_tiles * ((T + proj_bn(T) - 1) / proj_bn(T)), true);
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_bf16(&tmA, a->w, a->in_features, a->out_features, (unsigned long long)a->in_features * 2, 128) ||
+      !make_tmap_bf16(&tmB, a->x, a->in_features, T, (unsigned long long)a->in_features * 2, pl.bn))
+    return CSA2_ECUDA;
+  ProjParams p{};
+  p.mode = kProjPlain;
+  p.n_tok = T;
+  p.k_steps = k_steps;
+  p.m_tiles = m_tiles;
+  p.ks = pl.ks;
+  p.bn = pl.bn;
+  p.stages = pl.stages;
+  p.out = a->out;
+  p.out_ld = a->out_features;
+  p.dev_status = a->dev_status;
+  return cuda_status(launch_proj(tmA, tmB, p, 1, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {

@@ -7,7 +7,9 @@
 //   gather   the tile's 128 latent rows (bf16 by cp.async; FP4 latents and FP8 window rows
 //            widened to bf16 in registers, which is exact) and the row's query q' = RoPE(q)
 //            into shared memory, both in the 128-byte-swizzled K-major layout;
-//   S^T      = K q'^T: M = 128 entries x N = 64 heads x K = 512, bf16 in, fp32 in TMEM;
+//   S^T      = K q'^T: M = 128 entries x N = 64 heads x K = 512, bf16 in, fp32 in TMEM; the
+//            rotated dims of q' enter as two bf16 terms (hi + lo, four more K-steps against
+//            the tile's rotary panel), so only the stored latents and query are bf16;
 //   softmax  one thread per entry reads its 64 logits from TMEM, scales them (FP8 window
 //            rows: times their row scale), and the tile's per-head maximum M_h and sum l_h
 //            are reduced over the 128 entries; P = exp(S - M) is written back to shared
@@ -33,7 +35,9 @@ constexpr int kAttnThreads = 256;                  // 8 warps
 constexpr int kTileE = 128;                        // attended entries per block (MMA M)
 constexpr int kQPanel = kHeads * 128;              // 8 KB: 64 heads x 64 dims (bf16)
 constexpr int kKPanel = kTileE * 128;              // 16 KB: 128 entries x 64 dims
-constexpr int kQBytes = 8 * kQPanel;               // 64 KB (P_hi, P_lo after the first GEMM)
+// q' in eight panels, then the low bf16 parts of its rotary dims (448..511) as a ninth; P_hi,
+// P_lo after the first GEMM
+constexpr int kQBytes = 9 * kQPanel;               // 72 KB
 constexpr int kKBytes = 8 * kKPanel;               // 128 KB
 constexpr int kPBytes = kTileE * 128;              // 16 KB: 128 entries x 64 heads (bf16)
 constexpr uint32_t kTmemCols = 512;                // S^T in columns 0..63, then O^T in all 512
@@ -256,21 +260,28 @@ __device__ __forceinline__ void copy_query(const AttnParams& p, int row, uint8_t
     cp_async16(qs + sw128_off(h, ch, kHeads), qsrc + (size_t)idx * 16, true);
   }
 }
+// The rotated coordinates go to the tensor cores as two bf16 terms, hi = bf16(x') in panel 7
+// and lo = bf16(x' - hi) in panel 8 (a ninth K-panel of the first GEMM), so the logits see x'
+// to ~2^-16 instead of bf16's 2^-8: with peaked attention that rounding was the largest error
+// of the output.
 __device__ __forceinline__ void rotate_query(uint8_t* qs, const float* cs) {
 #pragma unroll
   for (int k = 0; k < kHeads * 8 / kAttnThreads; ++k) {
     const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 3, ch = 56 + (idx & 7);
     uint4* q4 = reinterpret_cast<uint4*>(qs + sw128_off(h, ch, kHeads));
     const uint4 v = *q4;
-    uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    uint32_t w4[4] = {v.x, v.y, v.z, v.w}, lo4[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = (ch - 56) * 4 + j;  // rotary pair index
       const float x = bf16_lo(w4[j]), y = bf16_hi(w4[j]);
       const float c = cs[i], sn = cs[32 + i];
-      w4[j] = pack_bf16x2(x * c - y * sn, x * sn + y * c);
+      const float xr = x * c - y * sn, yr = x * sn + y * c;
+      w4[j] = pack_bf16x2(xr, yr);
+      lo4[j] = pack_bf16x2(xr - bf16_lo(w4[j]), yr - bf16_hi(w4[j]));
     }
     *q4 = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(q4) + kQPanel) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
   }
 }
 
@@ -381,6 +392,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
         tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + (kk >> 2) * kKPanel + sub),
                        tc05::sw128_desc(qs_u + (kk >> 2) * kQPanel + sub), idesc, kk > 0);
       }
+      // the low parts of the rotated query against the tile's rotary panel
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + 7 * kKPanel + kk * 32),
+                       tc05::sw128_desc(qs_u + 8 * kQPanel + kk * 32), idesc, 1u);
       tc05::mma_commit(&sh.bar_s);
       sh.s_issued = 1;
     }

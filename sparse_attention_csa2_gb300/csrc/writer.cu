@@ -1,5 +1,5 @@
 // Cache writer: records into a main-KV cache (FP4: E2M1 codes with one E4M3 scale per 16 or
-// 32 channels) or a sliding-window cache (FP8 rows with one fp32 scale), each record's rotary
+// 32 channels; or bf16) or a sliding-window cache (FP8 rows with one fp32 scale), each record's rotary
 // coordinates turned by its position first (the course's FP4 lesson, section 4: the cache is
 // quantized after RoPE; "DeepSeek-V4.1-Flash explained", section 7: E2M1 with one E4M3
 // scale per 16 channels; the local cache stays FP8).
@@ -97,6 +97,18 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_records_kernel(const W
         v[2 * k + 1] = __fadd_rn(__fmul_rn(x, s), __fmul_rn(y, c));
       }
     }
+  }
+  if (p.out_dtype == CSA2_BF16) {  // rotated record in bf16, rounded to nearest even
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    uint4* row = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.codes) + dst * kHeadDim + 16 * lane);
+    row[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    row[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    return;
   }
   float amax = 0.f;
 #pragma unroll
