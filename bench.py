@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
     ap.add_argument("--prefill-t", type=int, default=4096, help="queries of the prefill chunk (profiling)")
+    ap.add_argument("--writer-only", action="store_true",
+                    help="time only the cache writer, compressor and encoder memory lines (profiling)")
     ap.add_argument("--proj-only", choices=["decode", "prefill", "both"],
                     help="time only the projections around attention (profiling)")
     ap.add_argument("--scan-only", metavar="FMT:ROWS:N",
@@ -416,6 +418,37 @@ def run_writer(local, peaks, n=262144, iters=20):
     nbytes = 2 * n * 512 * 4 * 2 + n * 512 * 4
     out["compress_ratio2"] = {"entries": n, "ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9,
                               "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
+    # the encoder bank's memory: compress 2n tokens, write the entries as bf16 latent rows
+    # rotated at their last token's position and as unrotated bf16 rows, derive the indexer
+    # keys (128 x 512 projection); four launches
+    pos = torch.arange(n, dtype=torch.int64, device=dev) * 2 + 1
+    rows = torch.arange(n, dtype=torch.int64, device=dev)
+    lat = torch.empty((n, 512), dtype=torch.bfloat16, device=dev)
+    plain = torch.empty((n, 512), dtype=torch.bfloat16, device=dev)
+    w_ik = (torch.randn(128, 512, generator=g) / 512 ** 0.5).to(torch.bfloat16).to(dev)
+
+    def memory():
+        e = S.compress(kv, gate, 2)
+        S.write_records(e, rows, lat, None, S.BF16, pos=pos)
+        S.write_records(e, rows, plain, None, S.BF16)
+        return S.linear(plain, w_ik)
+
+    for _ in range(3):
+        memory()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in ev:
+        e0.record()
+        memory()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    # compress (tokens read, entries written), two writer passes (entries read, bf16 rows and
+    # positions written / read), keys (bf16 rows read, keys written)
+    nbytes = (2 * n * 512 * 4 * 2 + n * 512 * 4) + 2 * (n * 512 * 4 + n * 512 * 2 + n * 16) + (n * 512 * 2 + n * 128 * 2)
+    out["encoder_memory_ratio2"] = {"tokens": 2 * n, "entries": n, "ms": ms, "launches": 4,
+                                    "entries_per_s": n / (ms / 1e3), "gbs": nbytes / (ms / 1e3) / 1e9,
+                                    "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
     return out
 
 
@@ -552,6 +585,13 @@ def run_gb300(args, world, rank, local):
         return 0
     if args.scan_only:
         print(json.dumps({"scan": run_scan_only(args, local)}), flush=True)
+        return 0
+    if args.writer_only:
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except (OSError, ValueError):
+            peaks = None
+        print(json.dumps({"cache_writer": run_writer(local, peaks)}), flush=True)
         return 0
     if args.proj_only:
         try:
