@@ -254,7 +254,7 @@ __device__ __forceinline__ void gather_tile(const TileSrc& m, uint8_t* ks, const
 // the rotary pairs (dims 448 + 2i, 448 + 2i + 1) in place once the copies have landed.
 __device__ __forceinline__ void copy_query(const AttnParams& p, int row, uint8_t* qs) {
   const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q) + (size_t)row * kHeads * kHeadDim * 2;
-#pragma unroll 4
+#pragma unroll 1  // run-once code: kept small for the instruction cache (measured)
   for (int k = 0; k < kHeads * kHeadDim / 8 / kAttnThreads; ++k) {
     const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 6, ch = idx & 63;
     cp_async16(qs + sw128_off(h, ch, kHeads), qsrc + (size_t)idx * 16, true);
@@ -265,7 +265,7 @@ __device__ __forceinline__ void copy_query(const AttnParams& p, int row, uint8_t
 // to ~2^-16 instead of bf16's 2^-8: with peaked attention that rounding was the largest error
 // of the output.
 __device__ __forceinline__ void rotate_query(uint8_t* qs, const float* cs) {
-#pragma unroll
+#pragma unroll 1  // run-once code: kept small for the instruction cache (measured)
   for (int k = 0; k < kHeads * 8 / kAttnThreads; ++k) {
     const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 3, ch = 56 + (idx & 7);
     uint4* q4 = reinterpret_cast<uint4*>(qs + sw128_off(h, ch, kHeads));
