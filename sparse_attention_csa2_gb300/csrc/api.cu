@@ -252,11 +252,13 @@ csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, c
 
 // ------------------------------------------------------------------ projections
 // Launch shape of one projection GEMM: token tile bn (the MMA's N), pipeline stages and the
-// K split ks (a cluster of ks blocks per tile).  The split is the smallest that puts a block
-// on at least 3/4 of the SMs (HBM streaming wants most SMs busy; every split adds a
-// distributed-shared-memory exchange).  A grid that fits on the SMs runs one block per SM with
-// a deep pipeline (~200 KB of loads in flight per SM); a larger one, with narrow token tiles,
-// two blocks per SM with half the stages each.
+// K split ks (a cluster of ks blocks per tile).  The split is the smallest that gives 1.5
+// blocks per SM for narrow token tiles (two fit on an SM) and 3/4 for wide ones, capped at 8:
+// HBM streaming wants every SM busy, and two blocks per SM, each with its own pipeline, hid the
+// load latency better than one with twice the stages (decode output projection: 45.6 against
+// 47.6 us); every split adds a distributed-shared-memory exchange.  A grid that fits on the SMs runs one block per SM with a deep pipeline (~200 KB of
+// loads in flight per SM); a larger one, with narrow token tiles, two blocks per SM with half
+// the stages each.
 struct ProjPlan {
   int bn, stages, ks;
 };
@@ -273,7 +275,13 @@ ProjPlan proj_plan(int n_tok, int k_steps, int tiles, bool allow_split) {
   if (forced > 0) {
     while (ks * 2 <= forced && ks < 8) ks *= 2;
   } else {
-    while (allow_split && ks < 8 && (long long)tiles * ks * 4 < 3LL * sms) ks *= 2;
+    // narrow token tiles (two blocks fit on an SM) aim for 1.5 blocks per SM, wide ones for 3/4
+    const long long target4 = bn <= 64 ? 6LL * sms : 3LL * sms;  // 4 x the block target
+    while (allow_split && ks < 8 && (long long)tiles * ks * 4 < target4) ks *= 2;
+    // an 8-block cluster's exchange costs more than it gains unless a split of 4 leaves more
+    // than half the SMs idle (decode: the final output stage 47.4 us at 8 against 45.6 at 4;
+    // the 8 tiles of the down-projection 31.3 at 8 against 33.3 at 4)
+    if (ks == 8 && (long long)tiles * 4 * 2 >= sms) ks = 4;
   }
   if (!allow_split) ks = 1;
   while (ks > 1 && ks > k_steps) ks /= 2;
