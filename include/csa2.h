@@ -422,6 +422,23 @@ size_t csa2_out_proj_workspace_size(const csa2_out_proj_args* a);
 csa2_status csa2_out_proj(const csa2_out_proj_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * csa2_expand_mxfp4 - MXFP4 indexer keys (OCP Microscaling: blocks of 32 E2M1 elements with
+ * one UE8M0 exponent; "DeepSeek-V4.1-Flash explained", section 7 table) to their bf16 values,
+ * out[j, d] = level(j, d) * 2^(e(j, d / 32) - 127): exact (every such value is a bf16 value;
+ * e = 255 gives NaN).  A prefill chunk reuses its keys for every query, so it expands them
+ * once and runs csa2_index_scores on the bf16 copy (the tensor-core prefill GEMM).
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int64_t n_records;          /* records (all sequences) */
+  const void* codes;          /* [n_records, 64] uint8, two E2M1 codes per byte, low nibble first */
+  const void* exps;           /* [n_records, 4] uint8 */
+  void* out;                  /* out [n_records, 128] bf16 */
+} csa2_expand_args;
+
+/* Pointers device; codes and out 16-byte aligned. */
+csa2_status csa2_expand_mxfp4(const csa2_expand_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * csa2_linear - one plain projection out = x W^T on the tensor cores (bf16 inputs, fp32
  * accumulation, bf16 output rounded to nearest even): the building block of the path's
  * other linear maps, e.g. the encoder's indexer keys derived from its compressed entries

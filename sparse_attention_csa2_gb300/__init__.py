@@ -87,6 +87,10 @@ class QueryProjArgs(C.Structure):
                 ("workspace", _vp), ("workspace_bytes", _sz), ("dev_status", _vp)]
 
 
+class ExpandArgs(C.Structure):
+    _fields_ = [("n_records", _i64), ("codes", _vp), ("exps", _vp), ("out", _vp)]
+
+
 class LinearArgs(C.Structure):
     _fields_ = [("n_tokens", _i32), ("in_features", _i32), ("out_features", _i32), ("x", _vp), ("w", _vp),
                 ("out", _vp), ("dev_status", _vp)]
@@ -124,6 +128,7 @@ _query_proj_ws = _sig("csa2_query_proj_workspace_size", [C.POINTER(QueryProjArgs
 _out_proj = _sig("csa2_out_proj", [C.POINTER(OutProjArgs), _vp], C.c_int)
 _out_proj_ws = _sig("csa2_out_proj_workspace_size", [C.POINTER(OutProjArgs)], _sz)
 _linear = _sig("csa2_linear", [C.POINTER(LinearArgs), _vp], C.c_int)
+_expand = _sig("csa2_expand_mxfp4", [C.POINTER(ExpandArgs), _vp], C.c_int)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
 
@@ -473,4 +478,17 @@ def linear(x, w):
     a.n_tokens, a.in_features, a.out_features = x.shape[0], x.shape[1], w.shape[0]
     a.x, a.w, a.out = _ptr(x), _ptr(w), _ptr(out)
     _check(_linear(C.byref(a), _stream()), "csa2_linear")
+    return out
+
+
+def expand_mxfp4(codes, exps):
+    """MXFP4 keys (codes [..., 64] uint8, exponents [..., 4] uint8) -> their exact bf16 values
+    [..., 128] (for the prefill indexer, which reuses a chunk's keys for every query)."""
+    if codes.dtype != torch.uint8 or exps.dtype != torch.uint8 or codes.shape[-1] != 64 or exps.shape[-1] != 4:
+        raise ValueError("expected uint8 codes [..., 64] and exponents [..., 4]")
+    out = torch.empty(codes.shape[:-1] + (128,), dtype=torch.bfloat16, device=codes.device)
+    a = ExpandArgs()
+    a.n_records = codes.numel() // 64
+    a.codes, a.exps, a.out = _ptr(codes), _ptr(exps), _ptr(out)
+    _check(_expand(C.byref(a), _stream()), "csa2_expand_mxfp4")
     return out

@@ -802,6 +802,14 @@ csa2_status csa2_out_proj(const csa2_out_proj_args* a, void* stream) {
   return CSA2_OK;
 }
 
+csa2_status csa2_expand_mxfp4(const csa2_expand_args* a, void* stream) {
+  if (!a || a->n_records < 0) return CSA2_EINVAL;
+  if (a->n_records == 0) return CSA2_OK;
+  if (!a->codes || !a->exps || !a->out || !aligned(a->codes, 16) || !aligned(a->out, 16)) return CSA2_EINVAL;
+  return cuda_status(
+      launch_expand_mxfp4(a->n_records, a->codes, a->exps, a->out, static_cast<cudaStream_t>(stream)));
+}
+
 csa2_status csa2_linear(const csa2_linear_args* a, void* stream) {
   if (!a || a->n_tokens < 0) return CSA2_EINVAL;
   if (a->n_tokens == 0) return CSA2_OK;

@@ -144,6 +144,9 @@ struct WriteParams {
   int32_t* dev_status;
 };
 cudaError_t launch_write_records(const WriteParams& p, cudaStream_t stream);
+// MXFP4 records -> bf16 records (csa2_expand_mxfp4).
+cudaError_t launch_expand_mxfp4(long long n_records, const void* codes, const void* exps, void* out,
+                                cudaStream_t stream);
 // Sequence compressor (csa2_compress).
 cudaError_t launch_compress(long long n_entries, int ratio, const void* kv, const void* gate, bool x_f32, float* out,
                             cudaStream_t stream);

@@ -181,7 +181,47 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
                          num[4 * q + 3] / den[4 * q + 3]);
 }
 
+// MXFP4 rows (64 code bytes + 4 UE8M0 exponents per 128-element record) -> their bf16 values:
+// one thread per block of 32 elements (16 code bytes, one exponent); every E2M1 level times a
+// power of two 2^(e - 127), e < 255, is a bf16 value (normal or subnormal), so the expansion
+// is exact; e = 255 (the OCP NaN scale) gives NaN.
+__global__ void __launch_bounds__(256) expand_mxfp4_kernel(long long n_blocks, const uint8_t* codes,
+                                                            const uint8_t* exps, uint16_t* out) {
+  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= n_blocks) return;
+  const uint4 c = __ldg(reinterpret_cast<const uint4*>(codes) + b);
+  const uint32_t e = __ldg(exps + b);
+  const float scale = e == 255u ? __uint_as_float(0x7fc00000u)
+                      : e == 0u ? __uint_as_float(0x00400000u)  // 2^-127, a subnormal
+                                : __uint_as_float(e << 23);
+  const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+  uint32_t o[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int byte = 0; byte < 4; ++byte) {
+      const uint32_t h = e2m1x2_to_f16x2((w4[k] >> (8 * byte)) & 0xffu);
+      const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xffffu))) * scale;
+      const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16))) * scale;
+      const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+      o[4 * k + byte] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + b * 32);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
 }  // namespace
+
+cudaError_t launch_expand_mxfp4(long long n_records, const void* codes, const void* exps, void* out,
+                                cudaStream_t stream) {
+  if (n_records == 0) return cudaSuccess;
+  const long long n_blocks = n_records * 4;
+  expand_mxfp4_kernel<<<(unsigned)((n_blocks + 255) / 256), 256, 0, stream>>>(
+      n_blocks, static_cast<const uint8_t*>(codes), static_cast<const uint8_t*>(exps), static_cast<uint16_t*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_compress(long long n_entries, int ratio, const void* kv, const void* gate, bool x_f32, float* out,
                             cudaStream_t stream) {

@@ -274,3 +274,41 @@ def test_prefill_index_scores(mode):
     # every row: -inf exactly from its causal boundary on
     nv = inp["rows"]["n_visible"]
     assert all(np.isfinite(s[r, :nv[r]]).all() and np.isneginf(s[r, nv[r]:]).all() for r in range(wl.T))
+
+
+# ------------------------------------------------------------------ MXFP4 keys for prefill
+def test_expand_mxfp4_bit_exact():
+    _cuda()
+    rng = np.random.default_rng(70)
+    n = 5000
+    codes = rng.integers(0, 256, (n, 64)).astype(np.uint8)
+    exps = rng.integers(0, 255, (n, 4)).astype(np.uint8)
+    exps[:6, 0] = [0, 1, 100, 127, 200, 254]
+    got = S.expand_mxfp4(torch.from_numpy(codes).cuda(), torch.from_numpy(exps).cuda())
+    torch.cuda.synchronize()
+    ref = O.bf16_round(O.mxfp4_to_f64(codes, exps).astype(np.float32))
+    assert np.array_equal(got.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+def test_prefill_index_scores_mxfp4(mode):
+    """A prefill chunk with MXFP4 keys: the keys expanded once to their exact bf16 values, then
+    the tensor-core prefill indexer, against the oracle's scores of the MXFP4 keys."""
+    _cuda()
+    wl = synth.scaled(synth.WORKLOADS["prefill_chunk"], N=3077, T=203, P0=2874, key_fmt="mxfp4")
+    inp = synth.make_inputs(wl, seed=71, mode=mode)
+    dv = synth.to_device(inp)
+    c, lay, rw = dv["cache"], dv["layers"][0], dv["rows"]
+    keys = S.expand_mxfp4(c["k_idx"], c["k_scale"])
+    s = S.index_scores(lay["q_idx"], lay["w"], keys, None, rw["seq_of_row"], rw["n_visible"])
+    s = s.cpu().numpy().astype(np.float64)
+    rows = [0, 1, 7, 8, 100, 201, 202]
+    ref = O.index_scores_rows(inp, 0, rows=rows)
+    got = s[rows]
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    if mode == "grid":
+        assert np.array_equal(got[fin], ref[fin])
+    else:
+        bound = score_bound(inp, 0, rows)
+        assert np.all(np.abs(got - ref)[fin] <= np.repeat(bound[:, None], got.shape[1], 1)[fin])
