@@ -53,3 +53,62 @@ def test_invalid_calls_are_rejected_on_the_host(lib):
         assert f(None, None) == 1, n
     lib.csa2_read_device_status.restype = ctypes.c_int
     assert lib.csa2_read_device_status(None, None, None) == 1
+
+
+def test_next_row_calls_reject_invalid_arguments_on_the_host(lib):
+    """The writer, compressor, expansion and projection entry points validate shapes, pointers
+    and alignment before any launch (no GPU needed to reach these answers)."""
+    for n in ("csa2_write_records", "csa2_compress", "csa2_expand_mxfp4", "csa2_linear", "csa2_query_proj",
+              "csa2_out_proj"):
+        f = getattr(lib, n)
+        f.restype = ctypes.c_int
+        assert f(None, None) == 1, n
+
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+    class Linear(ctypes.Structure):
+        _fields_ = [("n_tokens", i32), ("in_features", i32), ("out_features", i32), ("x", vp), ("w", vp),
+                    ("out", vp), ("dev_status", vp)]
+
+    class QueryProj(ctypes.Structure):
+        _fields_ = [("n_tokens", i32), ("hidden", i32), ("q_rank", i32), ("n_heads", i32), ("x", vp), ("w_dq", vp),
+                    ("g_q", vp), ("w_uq", vp), ("g_head", vp), ("eps", f32), ("q", vp), ("workspace", vp),
+                    ("workspace_bytes", sz), ("dev_status", vp)]
+
+    class OutProj(ctypes.Structure):
+        _fields_ = [("n_tokens", i32), ("n_heads", i32), ("n_groups", i32), ("o_rank", i32), ("hidden", i32),
+                    ("o", vp), ("w_oa", vp), ("w_ob", vp), ("out", vp), ("workspace", vp), ("workspace_bytes", sz),
+                    ("dev_status", vp)]
+
+    class Expand(ctypes.Structure):
+        _fields_ = [("n_records", i64), ("codes", vp), ("exps", vp), ("out", vp)]
+
+    A = 1 << 20  # a 16-byte-aligned stand-in address: never dereferenced, every case fails validation first
+    lin = lib.csa2_linear
+    assert lin(ctypes.byref(Linear(0, 64, 128, None, None, None, None)), None) == 0   # nothing to do
+    assert lin(ctypes.byref(Linear(4, 65, 128, A, A, A, None)), None) == 1            # K not a multiple of 64
+    assert lin(ctypes.byref(Linear(4, 64, 100, A, A, A, None)), None) == 1            # features not of 128
+    assert lin(ctypes.byref(Linear(4, 64, 128, A + 8, A, A, None)), None) == 1        # misaligned x
+    assert lin(ctypes.byref(Linear(-1, 64, 128, A, A, A, None)), None) == 1
+
+    qp = lib.csa2_query_proj
+    qp_ws = lib.csa2_query_proj_workspace_size
+    qp_ws.restype = sz
+    good = QueryProj(32, 4096, 1024, 64, A, A, None, A, None, 1e-6, A, A, 0, None)
+    need = qp_ws(ctypes.byref(good))
+    assert need == (32 * 1024 * 2 + 255) // 256 * 256 + (8 * 8 * 32 * 4 + 255) // 256 * 256
+    assert qp(ctypes.byref(good), None) == 5                                          # workspace too small
+    for field, bad in (("q_rank", 1000), ("hidden", 100), ("n_heads", 0), ("eps", -1.0)):
+        a = QueryProj(32, 4096, 1024, 64, A, A, None, A, None, 1e-6, A, A, need, None)
+        setattr(a, field, bad)
+        assert qp(ctypes.byref(a), None) == 1, field
+
+    op = lib.csa2_out_proj
+    for args in ((4, 64, 7, 1024, 4096), (4, 64, 8, 1000, 4096), (4, 64, 8, 1024, 4000), (4, 4, 8, 1024, 4096)):
+        assert op(ctypes.byref(OutProj(*args, A, A, A, A, A, 1 << 30, None)), None) == 1, args
+    assert op(ctypes.byref(OutProj(4, 64, 8, 1024, 4096, A, A, A, A, None, 0, None)), None) == 5
+
+    ex = lib.csa2_expand_mxfp4
+    assert ex(ctypes.byref(Expand(0, None, None, None)), None) == 0
+    assert ex(ctypes.byref(Expand(10, A + 4, A, A)), None) == 1                       # misaligned codes
+    assert ex(ctypes.byref(Expand(10, A, None, A)), None) == 1
