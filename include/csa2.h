@@ -15,6 +15,11 @@
  *      in the softmax denominator, RoPE on the last 64 dims of q and inverse RoPE on the
  *      output's rotary coordinates.
  *
+ * Around the step (the calls after csa2_fused_decode below): the cache writer (records
+ * rotated and stored as FP4, FP8 or bf16 rows), the encoder's sequence compressor, the
+ * expansion of MXFP4 indexer keys for prefill, a plain projection (csa2_linear), and the
+ * query low-rank path and grouped output projection on either side of attention.
+ *
  * Conventions shared by every call
  *   - Every pointer in an args struct is a DEVICE pointer owned by the caller, unless a
  *     field says otherwise.  The library keeps no pointer after the call returns.
