@@ -52,7 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-configs", action="store_true", help="skip the tiny / hierarchical / long-context lines")
     ap.add_argument("--only-config", choices=["tiny_decode", "hierarchical", "long_decode", "long_decode_mxfp4"],
                     help="time only this decode workload (profiling)")
-    ap.add_argument("--prefill-iters", type=int, default=10)
+    ap.add_argument("--prefill-iters", type=int, default=100)
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill chunk (profiling)")
     ap.add_argument("--prefill-t", type=int, default=4096, help="queries of the prefill chunk (profiling)")
     ap.add_argument("--writer-only", action="store_true",
@@ -205,6 +205,28 @@ def host_threads() -> int:
     return os.cpu_count() or 1
 
 
+def spread(times_ms):
+    """Median and the 10th / 90th percentiles of per-iteration times (ms)."""
+    t = np.asarray(list(times_ms), np.float64)
+    return {"iters": int(t.size), "p10_ms": float(np.percentile(t, 10)), "p50_ms": float(np.percentile(t, 50)),
+            "p90_ms": float(np.percentile(t, 90))}
+
+
+def evented(fn, iters, before=None):
+    """Runs fn `iters` times, each bracketed by its own pair of CUDA events on the current
+    stream (`before`, untimed, runs ahead of each pair); returns the per-iteration ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in ev:
+        if before is not None:
+            before()
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_setup(args)
@@ -290,10 +312,11 @@ def group_bytes(wl) -> float:
     return float(wl.Bq * per_q)
 
 
-def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "long_decode", "long_decode_mxfp4")):
-    """The other decode workloads, each timed as back-to-back group steps with CUDA events
-    after 3 warm-up steps: tiny decode (latency), hierarchical group (6 layers), long-context
-    decode (FP8 keys, FP4 latents, FP8 window)."""
+def run_configs(local, peaks, steps=100, names=("tiny_decode", "hierarchical", "long_decode", "long_decode_mxfp4")):
+    """The other decode workloads, each timed as `steps` back-to-back group steps with CUDA
+    events after 3 warm-up steps (ms_per_step), then `steps` steps each between its own pair
+    of events (median, p10, p90): tiny decode (latency), hierarchical group (6 layers),
+    long-context decode (FP8 keys, FP4 latents, FP8 window), and the same with MXFP4 keys."""
     import torch
     import synth
     hbm = float(peaks.get("hbm_gbs", 6800.0)) if peaks else 6800.0
@@ -313,6 +336,7 @@ def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "l
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
+        spr = spread(evented(step, steps))
         # stage breakdown per layer (a separate run: scan, top-K merge, attention)
         n_st = 10
         evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers] for _ in range(n_st)]
@@ -327,7 +351,7 @@ def run_configs(local, peaks, steps=50, names=("tiny_decode", "hierarchical", "l
                  for i in range(len(layers))]
         nbytes = group_bytes(wl)
         gbs = nbytes / (ms / 1e3) / 1e9
-        out[name] = {"B": wl.B, "N": wl.N, "layers": len(layers), "ms_per_step": ms,
+        out[name] = {"B": wl.B, "N": wl.N, "layers": len(layers), "ms_per_step": ms, "spread": spr,
                      "queries_per_s": wl.Bq / (ms / 1e3), "algorithmic_bytes": nbytes, "gbs": gbs,
                      "hbm_frac": gbs / hbm, "launches_per_step": sum(l.launches for l in layers),
                      "stage_ms_per_layer": {"scan_topk_merge_attn": stage}}
@@ -517,8 +541,9 @@ def run_projections(local, peaks, names=("decode", "prefill"), iters=20):
 
 def run_prefill(args, local, peaks):
     """Prefill chunk (B=1, T=4096 queries at positions 32768.., N=36864 bf16 keys): the
-    indexer GEMM on the tensor cores alone, then the whole chunk (scores -> per-query top-512
-    -> attention with each query's window)."""
+    indexer GEMM on the tensor cores alone (the median of `prefill_iters` evented calls, with
+    p10 / p90), then the whole chunk (scores -> per-query top-512 -> attention with each
+    query's window) and its three stages, each between its own events."""
     import torch
     import synth
     import sparse_attention_csa2_gb300 as S
@@ -533,39 +558,54 @@ def run_prefill(args, local, peaks):
     for _ in range(3):
         scores = idx_call()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.prefill_iters)]
-    for e0, e1 in ev:
-        e0.record()
-        scores = idx_call()
-        e1.record()
-    torch.cuda.synchronize()
-    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    spr = spread(evented(idx_call, args.prefill_iters))
+    ms = spr["p50_ms"]
     flops = prefill_flops(wl)
     tflops = flops / (ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
+    hbm = float(peaks.get("hbm_gbs", 6800.0)) if peaks else 6800.0
 
-    def chunk():
-        sc = idx_call()
-        idx = S.topk(sc, rw["n_visible"], p["K"])
-        return S.sparse_attn(lay["q"], rw["q_pos"], rw["seq_of_row"], c["lat"], c["lat_scales"], idx, lay["swa"],
-                             lay["swa_scale"], rw["swa_pos0"], p["W"], lay["sink"], p["theta"], p["softmax_scale"])
-    chunk()
+    # the chunk's stages: scores, top-K over the materialised scores, attention
+    state = {}
+    stage_fns = [
+        lambda: state.__setitem__("sc", idx_call()),
+        lambda: state.__setitem__("idx", S.topk(state["sc"], rw["n_visible"], p["K"])),
+        lambda: S.sparse_attn(lay["q"], rw["q_pos"], rw["seq_of_row"], c["lat"], c["lat_scales"], state["idx"],
+                              lay["swa"], lay["swa_scale"], rw["swa_pos0"], p["W"], lay["sink"], p["theta"],
+                              p["softmax_scale"]),
+    ]
+    for _ in range(2):
+        for f in stage_fns:
+            f()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_chunk = 3
-    e0.record()
-    for _ in range(n_chunk):
-        chunk()
-    e1.record()
+    n_chunk = max(3, min(args.prefill_iters, 30))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_chunk)]
+    for it in range(n_chunk):
+        ev[it][0].record()
+        for k, f in enumerate(stage_fns):
+            f()
+            ev[it][k + 1].record()
     torch.cuda.synchronize()
-    chunk_ms = e0.elapsed_time(e1) / n_chunk
+    chunk = [ev[i][0].elapsed_time(ev[i][3]) for i in range(n_chunk)]
+    st = [statistics.median(ev[i][k].elapsed_time(ev[i][k + 1]) for i in range(n_chunk)) for k in range(3)]
+    chunk_ms = statistics.median(chunk)
+    T, N, K, W = wl.T, wl.N, wl.K, wl.W
+    score_bytes = T * N * 4
+    attn_flops = 2.0 * 2 * wl.H * wl.D * T * (K + W)  # two GEMMs per attended entry and head
     return {"workload": f"prefill chunk: B=1, T={wl.T} queries at positions {wl.P0}..{wl.P0 + wl.T - 1}, "
                         f"N={wl.N} bf16 indexer keys, causal, top-{wl.K}, window {wl.W}",
-            "indexer_ms": ms, "indexer_tflops": tflops, "indexer_flops": flops,
+            "indexer_ms": ms, "indexer_spread": spr, "indexer_tflops": tflops, "indexer_flops": flops,
             "roofline": {"bound": "tensor", "kernel": "idx_mma_prefill_kernel (tcgen05, M=128 records x N=256)",
                          "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"},
-            "chunk_ms": chunk_ms, "chunk_tokens_per_s": wl.T / (chunk_ms / 1e3)}
+            "chunk_ms": chunk_ms, "chunk_spread": spread(chunk), "chunk_tokens_per_s": wl.T / (chunk_ms / 1e3),
+            "stages_ms": {"index_scores": st[0], "topk": st[1], "attention": st[2]},
+            "stages_roofline": {
+                "topk": {"bound": "hbm", "bytes": score_bytes + T * K * 4,
+                         "gbs": (score_bytes + T * K * 4) / (st[1] / 1e3) / 1e9,
+                         "frac": (score_bytes + T * K * 4) / (st[1] / 1e3) / 1e9 / hbm},
+                "attention": {"bound": "tensor", "flops": attn_flops, "tflops": attn_flops / (st[2] / 1e3) / 1e12,
+                              "frac": attn_flops / (st[2] / 1e3) / 1e12 / peak}}}
 
 
 def run_gb300(args, world, rank, local):
@@ -646,6 +686,9 @@ def run_gb300(args, world, rank, local):
         dist.barrier()
     elapsed = start.elapsed_time(stop) / 1e3
     value, max_elapsed = aggregate(wl.B * args.steps, elapsed)
+
+    # ---- per-step spread (a separate run: each step between its own pair of events)
+    step_spread = spread(evented(layer, max(100, min(args.steps, 1000))))
 
     # ---- stage breakdown (a separate run: the library records an event between the stages,
     # which would otherwise add its own gaps to the timed steps)
@@ -747,6 +790,19 @@ def run_gb300(args, world, rank, local):
                       "stage_ms": {"scan": statistics.mean(scan_ms), "topk_merge": statistics.mean(topk_ms),
                                    "attention": statistics.mean(attn_ms)},
                       "launches_per_step": launches_per_step, "prefill": prefill, "configs": configs}}
+    # short summaries last, where a truncated tail of the line still shows them: the whole
+    # step against HBM, its per-step spread, and the prefill indexer against the tensor peak
+    step_gbs = step_bytes_q * wl.B * world / step_s / 1e9
+    line["step"] = {"algorithmic_bytes": step_bytes_q * wl.B, "gbs": step_gbs, "hbm_frac": step_gbs / peak,
+                    "spread": step_spread}
+    roofline["step_hbm_frac"] = step_gbs / peak
+    if prefill is not None:
+        line["prefill_indexer"] = {"ms": prefill["indexer_ms"], "flops": prefill["indexer_flops"],
+                                   "tflops": prefill["indexer_tflops"], "peak": prefill["roofline"]["peak"],
+                                   "frac": prefill["roofline"]["frac"], "unit": "TFLOP/s",
+                                   "p10_ms": prefill["indexer_spread"]["p10_ms"],
+                                   "p90_ms": prefill["indexer_spread"]["p90_ms"]}
+        roofline["prefill_indexer"] = line["prefill_indexer"]
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

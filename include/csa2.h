@@ -26,6 +26,8 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
  *     legacy default stream).  They never synchronize and never allocate; scratch memory
  *     comes from the caller through `workspace` (size from the matching *_workspace_size).
+ *     One call is the exception: csa2_read_device_status copies a status word to the host
+ *     and therefore synchronizes its stream.
  *   - Arrays are dense row-major; base pointers must be 16-byte aligned.
  *   - Arguments are validated on the host before anything is launched.  An invalid call
  *     returns CSA2_EINVAL (or CSA2_EUNSUPPORTED for a valid request outside the
@@ -113,7 +115,7 @@ typedef struct csa2_index_args {
   const void* k_idx;          /* [n_seq, n_records, 128]: bf16, or E4M3 bytes (k_dtype FP8) */
   const float* k_scale;       /* [n_seq, n_records] row scales for FP8 keys; MXFP4: the exponent
                                  bytes [n_seq, n_records, 4] (passed through this pointer); else NULL */
-  int32_t k_dtype;            /* CSA2_BF16 or CSA2_FP8_E4M3_ROWSCALE */
+  int32_t k_dtype;            /* CSA2_BF16, CSA2_FP8_E4M3_ROWSCALE or CSA2_MXFP4 */
   int32_t n_rows;             /* query rows (>= 0) */
   int32_t n_seq;              /* sequences sharing the key layout */
   int64_t n_records;          /* records per sequence (>= 1) */
@@ -164,11 +166,17 @@ csa2_status csa2_topk(const csa2_topk_args* a, void* stream);
  * GPU loading the library holds until the process exits.  The call allocates nothing; the
  * caller passes inputs and outputs exactly as for csa2_topk (a->workspace is ignored).
  *   - Results are those of csa2_topk.
- *   - Requests whose scratch would exceed the array return CSA2_EUNSUPPORTED.  The scratch
- *     is 8 bytes per (row segment, K) pair plus 8 per row segment, and rows are split into
- *     at most one segment per SM in total, so up to K = 1024 on a 240-SM GPU it fits.
+ *   - The scratch is 8 bytes per (row segment, K) pair plus 8 per row segment, and rows
+ *     are split into at most one segment per multiprocessor in total, so on the supported
+ *     GPU (152 multiprocessors) every valid request needs at most 1.3 MB and fits: the
+ *     CSA2_EUNSUPPORTED answer for a request whose scratch would exceed the array is a
+ *     guard that such a device never reaches.
+ *   - `stream` must belong to the current device (the array and the segment count are
+ *     those of the current device); a stream of another device returns CSA2_EINVAL.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *     with that device current; make that first call before any stream capture.  The
+ *     address is remembered for the life of the process: after cudaDeviceReset the library
+ *     must not be used again on that device.
  *   - All calls on a device share the one array, which keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls that may overlap on the GPU - on
  *     different streams without ordering between them - race on it and must be serialised
@@ -472,6 +480,29 @@ const char* csa2_status_string(csa2_status s);
 csa2_status csa2_read_device_status(const int32_t* dev_status, int32_t* host_out, void* stream);
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int32_t csa2_version(void);
+
+/* Overrides of the launch heuristics, process-wide, for tests and tuning.  By default every
+ * call chooses its launch shapes from the problem's shapes and the device; results do not
+ * depend on these settings beyond the fp32 summation order of csa2_query_proj /
+ * csa2_out_proj / csa2_linear.  Not thread-safe with respect to calls in flight on the host
+ * (a call reads each setting once). */
+typedef enum csa2_tuning {
+  CSA2_TUNE_SCAN_SEGMENTS = 0,  /* segments per row of an indexer scan; 0 = automatic, 1..64 */
+  CSA2_TUNE_SCAN_WARP_MMA = 1,  /* 1: every scan takes the warp-MMA kernel; 0 = automatic */
+  CSA2_TUNE_SCAN_CLUSTER = 2,   /* 0: the tcgen05 decode scan's segments merge through lists
+                                   instead of selecting as a cluster; 1 = automatic (default) */
+  CSA2_TUNE_PROJ_KSPLIT = 3,    /* K split of the projection GEMMs, 1..8; 0 = automatic */
+  CSA2_TUNE_COUNT = 4
+} csa2_tuning;
+/* Returns CSA2_EINVAL for an unknown knob or a value outside its range. */
+csa2_status csa2_set_tuning(int32_t knob, int32_t value);
+
+/* Self-test of the bounded device wait the tensor-core kernels use (no counterpart in the
+ * pages: failure handling of this library).  Launches one block that waits, `tries` times
+ * (1 .. 2^20), on an mbarrier nothing signals; the wait gives up and stores CSA2_ETIMEOUT in
+ * the device int32 *dev_status, as the kernels do, and the block returns normally.  Returns
+ * CSA2_EINVAL for a NULL dev_status or tries out of range, CSA2_ECUDA for a failed launch. */
+csa2_status csa2_selftest_wait_timeout(int32_t* dev_status, int32_t tries, void* stream);
 
 #ifdef __cplusplus
 }

@@ -131,10 +131,40 @@ _linear = _sig("csa2_linear", [C.POINTER(LinearArgs), _vp], C.c_int)
 _expand = _sig("csa2_expand_mxfp4", [C.POINTER(ExpandArgs), _vp], C.c_int)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
+_set_tuning = _sig("csa2_set_tuning", [C.c_int32, C.c_int32], C.c_int)
+_selftest_wait = _sig("csa2_selftest_wait_timeout", [_vp, C.c_int32, _vp], C.c_int)
+
+# launch-heuristic overrides (csa2_tuning)
+TUNE_SCAN_SEGMENTS, TUNE_SCAN_WARP_MMA, TUNE_SCAN_CLUSTER, TUNE_PROJ_KSPLIT = 0, 1, 2, 3
+_TUNE_DEFAULTS = {TUNE_SCAN_SEGMENTS: 0, TUNE_SCAN_WARP_MMA: 0, TUNE_SCAN_CLUSTER: 1, TUNE_PROJ_KSPLIT: 0}
 
 
 def version() -> int:
     return int(_version())
+
+
+def read_device_status(dev_status) -> int:
+    """The status word [1] int32 that kernels wrote (csa2_read_device_status: synchronizes
+    the current stream)."""
+    out = C.c_int32(0)
+    _check(_read_status(C.c_void_p(_ptr(dev_status)), C.byref(out), _stream()), "csa2_read_device_status")
+    return int(out.value)
+
+
+def selftest_wait_timeout(dev_status, tries: int = 1000) -> None:
+    """Runs the bounded-wait self-test: dev_status (int32 device tensor) receives ETIMEOUT."""
+    _check(_selftest_wait(C.c_void_p(_ptr(dev_status)), int(tries), _stream()), "csa2_selftest_wait_timeout")
+
+
+def set_tuning(knob: int, value: int) -> None:
+    """Process-wide override of one launch heuristic (csa2_set_tuning)."""
+    _check(_set_tuning(int(knob), int(value)), "csa2_set_tuning")
+
+
+def reset_tuning() -> None:
+    """Every launch heuristic back to automatic."""
+    for k, v in _TUNE_DEFAULTS.items():
+        set_tuning(k, v)
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -272,14 +302,17 @@ def _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, K, swa, swa_scale,
 
 
 def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, swa_pos0, window: int, sink,
-                theta: float = 1e4, softmax_scale: float = HEAD_DIM ** -0.5, out_dtype=torch.float32):
+                theta: float = 1e4, softmax_scale: float = HEAD_DIM ** -0.5, out_dtype=torch.float32,
+                dev_status=None):
     """Attention output [n_rows, 64, 512] (fp32, or bf16 with out_dtype=torch.bfloat16) and
-    sink mass [n_rows, 64]."""
+    sink mass [n_rows, 64].  dev_status: optional int32 device tensor of one element that
+    the kernels set to a status code (out-of-range index, timed-out wait)."""
     dev = _dev(q)
     out = torch.empty((q.shape[0], HEADS, HEAD_DIM), dtype=out_dtype, device=dev)
     sm = torch.empty((q.shape[0], HEADS), dtype=torch.float32, device=dev)
     a = _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, idx.shape[1], swa, swa_scale, swa_pos0, window,
                    sink, theta, softmax_scale, out, sm)
+    a.dev_status = _ptr(dev_status)
     ws, nb = _ws(int(_attn_ws(C.byref(a))), dev)
     a.workspace, a.workspace_bytes = _ptr(ws), nb
     _check(_sparse_attn(C.byref(a), _stream()), "csa2_sparse_attn")

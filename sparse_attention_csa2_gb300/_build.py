@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libcsa2.so")
-SOURCES = ["api.cu", "index_scan.cu", "idx_mma.cu", "topk.cu", "attention.cu", "topk_static.cu", "writer.cu", "proj.cu"]
+SOURCES = ["api.cu", "index_scan.cu", "idx_mma.cu", "topk.cu", "attention.cu", "topk_static.cu", "writer.cu", "proj.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -3,13 +3,38 @@
 #include <atomic>
 #include <chrono>
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 
 #include "../../include/csa2.h"
 #include "kernels.h"
 
 namespace csa2 {
+
+// Multiprocessor count per device, queried once per device (launch plans are sized by it on
+// every call).
+int device_sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < kMaxDev) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  if (dev >= 0 && dev < kMaxDev) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Process-wide overrides of the launch heuristics (csa2_set_tuning); the defaults mean
+// "chosen per call from the shapes and the device".
+namespace {
+std::atomic<int> g_tuning[CSA2_TUNE_COUNT] = {{0}, {0}, {1}, {0}};
+}  // namespace
+
+int tuning(int knob) { return g_tuning[knob].load(std::memory_order_relaxed); }
+
 namespace {
 
 // Tag of one fused decode call for the scan's per-row completion counters: consecutive calls
@@ -28,23 +53,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bool pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
 size_t align_up(size_t v, size_t a = 256) { return (v + a - 1) / a * a; }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
-}
-
-int env_int(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : dflt;
-}
+int sm_count() { return device_sm_count(); }
 
 // Segments per row of the indexer scan: one resident block per SM, one wave; every segment
 // keeps at least min_seg records (4096 for full scans) so the per-segment top-K and pipeline
 // start-up stay small.
 int scan_segments(int n_rows, long long L, long long min_seg = 4096) {
-  const int forced = env_int("CSA2_SCAN_SEGMENTS", 0);
+  const int forced = tuning(CSA2_TUNE_SCAN_SEGMENTS);
   if (forced > 0) return forced;
   const int slots = sm_count();
   if (n_rows >= slots) return 1;
@@ -75,7 +90,7 @@ enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill };
 int tc05_segments(int n_rows, long long L, int unit, long long min_seg = 4096);
 
 ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0) {
-  if (!mma_indexer_available() || env_int("CSA2_SCAN_WARP_MMA", 0) != 0 || a->k_dtype == CSA2_MXFP4)
+  if (!mma_indexer_available() || tuning(CSA2_TUNE_SCAN_WARP_MMA) != 0 || a->k_dtype == CSA2_MXFP4)
     return ScanPath::kWarpMma;
   if (a->cand != nullptr && !(want_topk && cand_run > 0 && cand_run % 64 == 0)) return ScanPath::kWarpMma;
   const bool fp8 = a->k_dtype == CSA2_FP8_E4M3_ROWSCALE;
@@ -271,7 +286,7 @@ ProjPlan proj_plan(int n_tok, int k_steps, int tiles, bool allow_split) {
   const size_t stage = 128 * 128 + (size_t)bn * 128;
   const int sms = sm_count();
   int ks = 1;
-  const int forced = env_int("CSA2_PROJ_KS", 0);
+  const int forced = tuning(CSA2_TUNE_PROJ_KSPLIT);
   if (forced > 0) {
     while (ks * 2 <= forced && ks < 8) ks *= 2;
   } else {
@@ -339,6 +354,14 @@ const char* csa2_status_string(csa2_status s) {
 }
 
 int32_t csa2_version(void) { return 0x000100; }
+
+csa2_status csa2_set_tuning(int32_t knob, int32_t value) {
+  if (knob < 0 || knob >= CSA2_TUNE_COUNT || value < 0) return CSA2_EINVAL;
+  if (knob == CSA2_TUNE_SCAN_SEGMENTS && value > 64) return CSA2_EINVAL;
+  if (knob == CSA2_TUNE_PROJ_KSPLIT && value > 8) return CSA2_EINVAL;
+  g_tuning[knob].store(value, std::memory_order_relaxed);
+  return CSA2_OK;
+}
 
 csa2_status csa2_read_device_status(const int32_t* dev_status, int32_t* host_out, void* stream) {
   if (!dev_status || !host_out) return CSA2_EINVAL;
@@ -536,7 +559,10 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
   auto mark = [&](int i) {
     if (a->stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(a->stage_events[i]), s);
   };
-  if (a->mode == CSA2_MODE_REUSE) mark(0);
+  if (a->mode == CSA2_MODE_REUSE) {  // no indexing stages: events 0 and 1 mark the same point
+    mark(0);
+    mark(1);
+  }
   if (a->mode != CSA2_MODE_REUSE) {
     ScanParams p = scan_params(ix);
     p.K = a->K;
@@ -572,7 +598,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
     const int seg_blocks = p.block_max ? (int)(((ic.n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg)
                            : p.cand   ? (int)(2 * (((ic.L + p.unit - 1) / p.unit + n_seg - 1) / n_seg))
                                       : 0;
-    p.cluster_merge = tc05 && env_int("CSA2_SCAN_CLUSTER", 1) != 0 && mma_decode_cluster_ok(n_seg, n_rows, a->K, seg_blocks, ic.k_dtype == CSA2_FP8_E4M3_ROWSCALE);
+    p.cluster_merge = tc05 && tuning(CSA2_TUNE_SCAN_CLUSTER) != 0 && mma_decode_cluster_ok(n_seg, n_rows, a->K, seg_blocks, ic.k_dtype == CSA2_FP8_E4M3_ROWSCALE);
     const bool fused_merge = tc05 && !p.cluster_merge && mma_decode_can_merge(n_seg, a->K);
     if (n_seg > 1) {
       p.row_done = c.take<unsigned long long>((size_t)n_rows);
@@ -853,7 +879,7 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
         a->mode == CSA2_MODE_FULL_POOL ? (int)(((ic.n_records + unit - 1) / unit + n_seg - 1) / n_seg)
         : a->mode == CSA2_MODE_REINDEX ? (int)(2 * (((ic.L + unit - 1) / unit + n_seg - 1) / n_seg))
                                        : 0;
-    const bool merged = tc05 && ((env_int("CSA2_SCAN_CLUSTER", 1) != 0 &&
+    const bool merged = tc05 && ((tuning(CSA2_TUNE_SCAN_CLUSTER) != 0 &&
                                   mma_decode_cluster_ok(n_seg, a->attn.n_rows, a->K, seg_blocks, ic.k_dtype == CSA2_FP8_E4M3_ROWSCALE)) ||
                                  mma_decode_can_merge(n_seg, a->K));
     n += 1 + (n_seg > 1 && !merged ? 1 : 0);  // the tcgen05 scan merges its segments itself

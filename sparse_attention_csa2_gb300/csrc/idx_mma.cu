@@ -894,9 +894,7 @@ cudaError_t launch_mma_decode_t(const ScanParams& p, long long n_seq_rows, int n
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ScanParams q = p;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-    q.pdl_trigger = (long long)n_seg * p.n_rows <= sms;  // one CTA per SM: a single wave
+  q.pdl_trigger = (long long)n_seg * p.n_rows <= device_sm_count();  // one CTA per SM: a single wave
   // Programmatic dependent launch: the blocks may become resident while the previous kernel
   // in the stream finishes; they wait for it before reading anything.
   cudaLaunchAttribute attr[2] = {};

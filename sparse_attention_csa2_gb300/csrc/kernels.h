@@ -8,6 +8,11 @@
 
 namespace csa2 {
 
+// Multiprocessors of the current device (queried once per device).
+int device_sm_count();
+// Current value of a launch-heuristic override (csa2_tuning in csa2.h).
+int tuning(int knob);
+
 // Indexer scan over one query row per grid row, n_seg segments per row.
 struct ScanParams {
   const void* q_idx;          // [n_rows, 32, 128] bf16

@@ -10,7 +10,8 @@
 // The array is a file-scope __device__ variable of CSA2_TOPK_STATIC_SCRATCH_BYTES bytes, so
 // every GPU on which the library is loaded holds it until the process exits.  Host code
 // cannot use the variable's name as a device address; the device address is obtained once
-// per device with cudaGetSymbolAddress, with that device current, on the first call on it.
+// per device with cudaGetSymbolAddress, with that device current, on the first call on it,
+// and kept for the life of the process (a cudaDeviceReset is not noticed).
 #include <mutex>
 
 #include "../../include/csa2.h"
@@ -54,8 +55,16 @@ extern "C" csa2_status csa2_topk_static(const csa2_topk_args* a, void* stream) {
   if (a->n_rows == 0) return CSA2_OK;
   if (!a->scores || !a->n_valid || !a->idx || a->L < 1 || a->L > (1LL << 24)) return CSA2_EINVAL;
   if (a->K < 1 || a->K > CSA2_MAX_TOPK) return CSA2_EUNSUPPORTED;
-  const int n_seg = topk_segments(a->n_rows, a->L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The scratch address and the segment count are the current device's; kernels on a stream
+  // of another device would be handed this device's address, so such a stream is refused.
+  // The default stream handles always belong to the current device.
+  if (s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread) {
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess) return CSA2_ECUDA;
+    if (sdev != cur) return CSA2_EINVAL;
+  }
+  const int n_seg = topk_segments(a->n_rows, a->L);
   FeedParams f{};
   f.n_rows = a->n_rows;
   f.K = a->K;

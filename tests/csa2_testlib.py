@@ -96,3 +96,46 @@ def score_bound(inp, layer, rows=None):
         kn = np.linalg.norm(O.keys_of(inp, b), axis=1).max()
         out.append(1e-5 * float(np.sum(np.asarray(lay["w"][r], np.float64) * qn)) * kn + 1e-6)
     return np.array(out)
+
+
+def scores_by_position(ref_layer, n_records):
+    """Oracle scores of one layer indexed by record position (-inf where the record is not a
+    candidate): a full layer's rows as they are; a Reindex layer's pool slots placed at their
+    positions."""
+    s = ref_layer["scores"]
+    if ref_layer["mode"] != "reindex":
+        return s
+    out = np.full((s.shape[0], n_records), -np.inf)
+    pool, n_pool = ref_layer["pool"], ref_layer["n_pool"]
+    for r in range(s.shape[0]):
+        n = int(n_pool[r])
+        out[r, pool[r, :n]] = s[r, :n]
+    return out
+
+
+def check_pool_near_ties(pool_gpu, n_pool_gpu, scores_ora, n_visible, bs, n_keep, bound):
+    """A GPU block pool against the oracle's scores of the same rows.  The pool must list every
+    visible position of its kept blocks in ascending order (-1 after them) and keep
+    min(n_keep, blocks) blocks; the kept blocks may differ from the oracle's only by swaps
+    across the n_keep boundary between blocks whose oracle block maxima lie within `bound` of
+    the oracle's n_keep-th block maximum.  Returns the number of swapped blocks."""
+    swaps = 0
+    for r in range(len(n_visible)):
+        nv = int(n_visible[r])
+        _, bm, kept_ora = O.block_pool(scores_ora[r, :nv], bs, n_keep)
+        n = int(n_pool_gpu[r])
+        p = np.asarray(pool_gpu[r], np.int64)
+        kept = np.unique(p[:n] // bs)
+        expect = np.concatenate([np.arange(c * bs, min((c + 1) * bs, nv)) for c in kept])
+        assert np.array_equal(p[:n], expect) and np.all(p[n:] == -1), r
+        assert len(kept) == len(kept_ora), r
+        a, b = set(int(c) for c in kept), set(int(c) for c in kept_ora)
+        if a == b:
+            continue
+        kth = min(bm[c] for c in b)
+        for c in a - b:
+            assert bm[c] >= kth - bound[r], (r, c, bm[c], kth)
+        for c in b - a:
+            assert bm[c] <= kth + bound[r], (r, c, bm[c], kth)
+        swaps += len(a - b)
+    return swaps

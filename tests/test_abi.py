@@ -112,3 +112,48 @@ def test_next_row_calls_reject_invalid_arguments_on_the_host(lib):
     assert ex(ctypes.byref(Expand(0, None, None, None)), None) == 0
     assert ex(ctypes.byref(Expand(10, A + 4, A, A)), None) == 1                       # misaligned codes
     assert ex(ctypes.byref(Expand(10, A, None, A)), None) == 1
+
+
+class _TopkArgs(ctypes.Structure):
+    _fields_ = [("scores", ctypes.c_void_p), ("cand", ctypes.c_void_p), ("n_valid", ctypes.c_void_p),
+                ("n_rows", ctypes.c_int32), ("L", ctypes.c_int64), ("K", ctypes.c_int32), ("idx", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+@pytest.mark.parametrize("name", ["csa2_topk", "csa2_topk_static"])
+def test_topk_entry_points_validate_on_the_host(lib, name):
+    """Both top-K entry points reject the same invalid requests before touching CUDA: a NULL
+    argument struct, NULL scores / n_valid / idx, L outside 1 .. 2^24 (EINVAL), K outside
+    1 .. CSA2_MAX_TOPK (EUNSUPPORTED); zero rows is a valid call that does nothing."""
+    f = getattr(lib, name)
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(_TopkArgs), ctypes.c_void_p]
+    assert f(None, None) == 1
+    A = 1 << 20  # an aligned stand-in address: every case below fails validation before any use
+
+    def call(**kw):
+        a = _TopkArgs(A, None, A, 4, 1000, 64, A, None, 0)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return f(ctypes.byref(a), None)
+
+    assert call(n_rows=0) == 0
+    assert call(n_rows=-1) == 1
+    assert call(scores=None) == 1
+    assert call(n_valid=None) == 1
+    assert call(idx=None) == 1
+    assert call(L=0) == 1
+    assert call(L=(1 << 24) + 1) == 1
+    assert call(K=0) == 2
+    assert call(K=1025) == 2
+
+
+def test_tuning_overrides_are_range_checked(lib):
+    st = lib.csa2_set_tuning
+    st.restype = ctypes.c_int
+    st.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    assert st(-1, 0) == 1 and st(4, 0) == 1            # unknown knobs
+    assert st(0, 65) == 1 and st(0, -1) == 1           # scan segments 0..64
+    assert st(3, 9) == 1                               # projection K split 0..8
+    assert st(0, 8) == 0 and st(0, 0) == 0             # set, and back to automatic
+    assert st(2, 0) == 0 and st(2, 1) == 0

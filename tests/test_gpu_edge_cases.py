@@ -61,12 +61,16 @@ def test_short_rows(key_fmt, lat_fmt, swa_fmt):
 
 
 @pytest.mark.parametrize("B", [2, 5])
-def test_segment_counts_without_clusters(B, monkeypatch):
+def test_segment_counts_without_clusters(B):
     """The same rows with the scan's cluster selection switched off: the segments write lists
     and the last segment of each row to finish merges them."""
     _cuda()
-    monkeypatch.setenv("CSA2_SCAN_CLUSTER", "0")
+    import sparse_attention_csa2_gb300 as S
     wl = synth.scaled(synth.WORKLOADS["batched_decode"], B=B, N=65536)
     inp = synth.make_inputs(wl, seed=40 + B, mode="grid")
-    g = gpu_group(synth.to_device(inp))
+    S.set_tuning(S.TUNE_SCAN_CLUSTER, 0)
+    try:
+        g = gpu_group(synth.to_device(inp))
+    finally:
+        S.reset_tuning()
     _check(inp, g, sorted({0, B - 1}))

@@ -127,14 +127,17 @@ def test_out_proj_flash_shape(name):
 
 
 @pytest.mark.parametrize("ks", [1, 2, 8])
-def test_split_counts_agree(ks, monkeypatch):
+def test_split_counts_agree(ks):
     """The K split (a cluster reduction) changes only the fp32 summation order."""
     _cuda()
     shape = synth.ProjShape("t", tokens=32, hidden=1024, q_rank=256, heads=8, groups=8, o_rank=128)
     inp = synth.projection_inputs(shape, seed=12)
-    monkeypatch.setenv("CSA2_PROJ_KS", str(ks))
-    out = _f(_run_out(inp))
-    q = _f(_run_query(inp))
+    S.set_tuning(S.TUNE_PROJ_KSPLIT, ks)
+    try:
+        out = _f(_run_out(inp))
+        q = _f(_run_query(inp))
+    finally:
+        S.reset_tuning()
     _check(out, O.out_proj(_f(inp["o"]), _f(inp["w_oa"]), _f(inp["w_ob"])))
     _check(q, _query_ref(inp, np.arange(32)))
 
