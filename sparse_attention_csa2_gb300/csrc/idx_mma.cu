@@ -70,6 +70,12 @@ constexpr int kDecEpiFirst = 4;
 constexpr int kDecEpiWarps = 8;  // two groups of 4 warps (one per TMEM lane quarter), alternate tiles
 constexpr int kDecQHalf = 32 * 128;  // bf16: 32 heads x 64 dims x 2 B
 constexpr int kDecSegMax = 16384;    // records of one segment (their keys stay in shared memory)
+// Cluster selection with marked candidates: at most this many marked entries per row (their
+// keys and positions, then the selection's lists, fit in the idle tile ring), and the bytes of
+// the per-segment bitmap of marked entries.
+constexpr int kFastCap = 6144;
+constexpr int kFastBytes = kDecSegMax / 8;
+constexpr int kMaxClusterSeg = 16;
 
 struct DecBars {
   uint64_t full[8], empty[8], tfull[2], tempty[2], qfull, qready;
@@ -80,6 +86,16 @@ struct DecBars {
   int drained;    // tiles whose accumulators the epilogue read
   int last;       // this block is the last segment of its row to finish
   int qexp[32];   // FP8: power-of-two exponent applied to each head of q^I
+  // marked-candidate selection
+  int tile_keys[16];   // per tile slot (t mod 16): epilogue warps that stored tile t's keys
+  uint32_t maxkey;     // largest key the lister has seen (read by the other blocks' listers)
+  int lister_fail;     // the lister's wait gave up
+  int cand_cnt[kMaxClusterSeg];      // per block: its marked entries (-1: not usable), pushed by it
+  uint32_t cand_lo[kMaxClusterSeg];  // per block: its lister's last bound (<= the row's K-th key)
+  uint32_t cand_hi[kMaxClusterSeg];  // per block: the largest key of its segment
+  uint32_t bound;                    // this block's lister's last bound
+  int cand_off[kMaxClusterSeg + 1];  // per block: offset of its entries in the row's list; [n] = total
+  int cand_go;         // the row's marked entries fit: block 0 selects among them
 };
 
 // The last segment block of a row merges the row's lists: every list entry's key goes into
@@ -137,6 +153,247 @@ __device__ void merge_row_lists(const ArrSel<NW>& sel, uint32_t* keys, const Sca
   for (int r = sel.tid; r < K; r += NT) out[r] = r < kept ? (pos_s ? pos_s[sel_idx[r]] : __ldcg(pos + sel_idx[r])) : -1;
 }
 
+// ---- marked-candidate selection (the segments of a row form a cluster)
+//
+// While the tiles stream, one otherwise idle warp of every segment block (the lister) follows
+// the epilogue tile by tile.  After half and after three quarters of its tiles it derives a lower
+// bound on the row's K-th key from the level-1 histograms of all blocks of the cluster: the
+// highest bin whose count from the top reaches K.  The counts only grow and each counts keys
+// that exist, so however stale a remote read is, at least K keys of the row lie at or above
+// that bin's lower edge, and so does the row's K-th key.  The lister marks, in a bitmap of its
+// segment, every key at or above its latest bound (the tiles before the first bound once it
+// exists); every selected entry of the row is therefore marked.  After the stream each block
+// compacts its marked entries, and one block selects the row's top-K among all of them.
+
+// Waits until the four epilogue warps that drain tile t have stored its keys (a per-slot
+// count that grows by four per tile of the slot).  Bounded; false when it gave up.
+__device__ __forceinline__ bool wait_tile_keys(const int* tile_keys, int t) {
+  const int need = 4 * (t / 16 + 1);
+  const volatile int* c = tile_keys + (t & 15);
+  for (uint32_t i = 0; i < tc05::kSpinLimit; ++i) {
+    if (*c >= need) {
+      __threadfence_block();
+      return true;
+    }
+    __nanosleep(32);
+  }
+  return false;
+}
+
+// Lower bound on the row's K-th key from the cluster's level-1 histograms (key >> 20), read
+// from the top: blocks publish the largest key they have seen, the warp sums 128 bins of every
+// block per step (lane l: the four bins hi - 4l - 3 .. hi - 4l) until the count from the top
+// reaches K.  Returns that bin's lower edge, or 0 while fewer than K keys are counted.
+__device__ __forceinline__ uint32_t row_key_bound(const int* hist, const uint32_t* maxkey, uint32_t n_cta, int K) {
+  const int lane = threadIdx.x & 31;
+  uint32_t top = 0u;
+  if ((uint32_t)lane < n_cta) top = (uint32_t)cluster_ld_s32(cluster_map(maxkey, (uint32_t)lane));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) top = max(top, __shfl_xor_sync(0xffffffffu, top, o));
+  if (top == 0u) return 0u;
+  int cum = 0;
+#pragma unroll 1
+  for (int hi = (int)(top >> 20) | 3; hi >= 3; hi -= 128) {
+    const int b0 = hi - 4 * lane - 3;  // a multiple of 4
+    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+    if (b0 >= 0) {
+#pragma unroll 1
+      for (uint32_t r = 0; r < n_cta; ++r) {
+        const uint4 v = cluster_ld_v4(cluster_map(hist + b0, r));
+        s0 += (int)v.x;
+        s1 += (int)v.y;
+        s2 += (int)v.z;
+        s3 += (int)v.w;
+      }
+    }
+    const int c = s0 + s1 + s2 + s3;
+    int inc = c;  // lanes in order = bins from the top down
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    if (cum + tot >= K) {
+      const unsigned m = __ballot_sync(0xffffffffu, cum + inc >= K);
+      const int L = __ffs(m) - 1;
+      int bin = b0;
+      const int acc = cum + inc - c;
+      if (acc + s3 >= K) bin = b0 + 3;
+      else if (acc + s3 + s2 >= K) bin = b0 + 2;
+      else if (acc + s3 + s2 + s1 >= K) bin = b0 + 1;
+      bin = __shfl_sync(0xffffffffu, bin, L);
+      return (uint32_t)bin << 20;
+    }
+    cum += tot;
+  }
+  return 0u;
+}
+
+// Marks tile t's keys at or above `bound` (lane l: keys 32u + l of the tile, u = 0..3; word
+// 4t + u of the bitmap holds keys 32u .. 32u + 31).
+__device__ __forceinline__ void mark_tile(uint32_t* listed, const uint32_t* keys, int t, int seg_len, uint32_t bound) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int j = t * kTileKeys + 32 * u + lane;
+    const uint32_t k = j < seg_len ? keys[j] : 0u;
+    const unsigned m = __ballot_sync(0xffffffffu, k != 0u && k >= bound);
+    if (lane == u) listed[4 * t + u] = m;
+  }
+}
+
+// Exact top-K among n marked entries (keys ck[0..n), record positions cp[0..n) in position
+// order; n <= kFastCap), written to out[0..K) as ascending positions, -1 padded.  The caller
+// gives lo <= the K-th key and hi >= every key (the listers' bounds and maxima) and has zeroed
+// sh.hist and sh.aux.  One histogram of (key - lo) >> shift over 4096 bins (shift the smallest
+// that fits [lo, hi]) with a coarse copy of 64 bins finds, in one warp, the bin of the K-th key
+// and the count above it; the few keys of that bin go to one warp, which finds the K-th key T
+// and how many entries equal to T are kept (the lowest positions first) by counting; a bin of
+// more than 32 keys (ties) takes further histogram levels instead.  Each thread then takes a
+// contiguous run of entries and one block scan places the selected ones.
+template <int NW>
+__device__ __noinline__ void select_marked(const ArrSel<NW>& s, const uint32_t* ck, const int32_t* cp, int n, int K,
+                                           uint32_t lo, uint32_t hi, int32_t* out) {
+  constexpr int NT = NW * 32;
+  ArrSelShared& sh = *s.sh;
+  const int tid = s.tid, lane = tid & 31;
+  int* coarse = reinterpret_cast<int*>(sh.aux);        // 64 bins of 64 bins
+  uint32_t* few = sh.aux + 64;                          // the keys of the K-th key's bin (<= 32)
+  int* few_n = reinterpret_cast<int*>(sh.aux + 96);
+  const int c = (n + NT - 1) / NT;
+  const int a0 = min(n, tid * c), a1 = min(n, a0 + c);
+  uint32_t thr = 0u;
+  int n_eq = 0;
+  if (n > K) {
+    const int width = 32 - __clz(max(hi - lo, 1u));
+    const int shift = max(0, width - 12);
+#pragma unroll 2
+    for (int i = a0; i < a1; ++i)
+      if (ck[i] >= lo) {
+        const uint32_t f = (ck[i] - lo) >> shift;
+        atomicAdd(&sh.hist[f], 1);
+        atomicAdd(&coarse[f >> 6], 1);
+      }
+    s.sync();
+    if (s.warp() == 0) {
+      // from the top: the coarse bin where the count reaches K, then its fine bin
+      int above = 0, bin = 0;
+#pragma unroll 1
+      for (int stage = 0; stage < 2; ++stage) {
+        const int* h = stage == 0 ? coarse : sh.hist + 64 * bin;
+        const int x0 = h[63 - 2 * lane], x1 = h[62 - 2 * lane];
+        int inc = x0 + x1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const int L = __ffs(__ballot_sync(0xffffffffu, above + inc >= K)) - 1;
+        const int acc = above + inc - (x0 + x1);
+        const int hit = acc + x0 >= K ? 63 - 2 * lane : 62 - 2 * lane;
+        const int acc2 = acc + x0 >= K ? acc : acc + x0;
+        const int b2 = __shfl_sync(0xffffffffu, hit, L);
+        above = __shfl_sync(0xffffffffu, acc2, L);
+        bin = stage == 0 ? b2 : 64 * bin + b2;
+      }
+      if (lane == 0) {
+        sh.bin = bin;
+        sh.before = above;
+      }
+    }
+    s.sync();
+    int need = K - sh.before;
+    uint32_t base = lo + ((uint32_t)sh.bin << shift);
+    if (shift == 0) {
+      thr = base;
+      n_eq = need;
+    } else {
+      const uint64_t top = (uint64_t)base + (1ull << shift);
+#pragma unroll 2
+      for (int i = a0; i < a1; ++i)
+        if (ck[i] >= base && (uint64_t)ck[i] < top) {
+          const int slot = atomicAdd(few_n, 1);
+          if (slot < 32) few[slot] = ck[i];
+        }
+      s.sync();
+      const int p = *few_n;
+      if (p <= 32) {
+        if (s.warp() == 0) {
+          // the need-th largest of the bin's keys, by counting
+          const uint32_t x = lane < p ? few[lane] : 0u;
+          int gt = 0, ge = 0;
+#pragma unroll 1
+          for (int j = 0; j < p; ++j) {
+            const uint32_t y = __shfl_sync(0xffffffffu, x, j);
+            gt += y > x;
+            ge += y >= x;
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, lane < p && gt < need && need <= ge);
+          const int L = __ffs(m) - 1;
+          if (lane == L) {
+            sh.thr = x;
+            sh.n_eq = need - gt;
+          }
+        }
+        s.sync();
+        thr = sh.thr;
+        n_eq = sh.n_eq;
+      } else {
+        // many keys in the bin (ties): 4096-bin levels over it until the bins are single keys
+        int width2 = shift;
+#pragma unroll 1
+        while (true) {
+          const int sh2 = max(0, width2 - 12);
+          s.sync();
+          for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0;
+          s.sync();
+          const uint64_t top2 = (uint64_t)base + (1ull << width2);
+#pragma unroll 2
+          for (int i = a0; i < a1; ++i)
+            if (ck[i] >= base && (uint64_t)ck[i] < top2) atomicAdd(&sh.hist[(ck[i] - base) >> sh2], 1);
+          s.sync();
+          s.template pick<kHistBins>(need);
+          need -= sh.before;
+          base += (uint32_t)sh.bin << sh2;
+          if (sh2 == 0) break;
+          width2 = sh2;
+        }
+        thr = base;
+        n_eq = need;
+      }
+    }
+  }
+  // compaction: the thread's run of entries, placed by one block scan
+  int gt = 0, eq = 0;
+  if (n <= K) {
+    gt = a1 - a0;
+  } else {
+#pragma unroll 2
+    for (int i = a0; i < a1; ++i) {
+      gt += ck[i] > thr;
+      eq += ck[i] == thr;
+    }
+  }
+  int tot;
+  const int before = s.scan((gt << 16) | eq, &tot);
+  const int eq_b = before & 0xffff;
+  int at = (before >> 16) + min(eq_b, n_eq);
+  int take = max(0, min(eq, n_eq - eq_b));
+#pragma unroll 2
+  for (int i = a0; i < a1; ++i) {
+    const uint32_t k = ck[i];
+    bool keep = n <= K || k > thr;
+    if (!keep && k == thr && take > 0) {
+      keep = true;
+      --take;
+    }
+    if (keep) out[at++] = cp[i];
+  }
+  const int kept = (tot >> 16) + min(tot & 0xffff, n_eq);
+  for (int r = kept + tid; r < K; r += NT) out[r] = -1;
+}
+
 template <bool FP8>
 __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
@@ -158,6 +415,8 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
   uint32_t* bkeys = keys + kDecSegMax;                      // block maxima of the segment (keys)
   // candidate mode: the record position where each 64-slot run of the segment starts
   int32_t* hstart = reinterpret_cast<int32_t*>(bkeys);
+  // marked-candidate selection: one bit per entry of the segment
+  uint32_t* listed = bkeys + p.seg_table;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
@@ -195,6 +454,9 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     tc05::mbar_init(&bars.qfull, 1);
     bars.timeout = 0;
     bars.issued = bars.consumed = bars.drained = 0;
+    for (int i = 0; i < 16; ++i) bars.tile_keys[i] = 0;
+    bars.maxkey = 0u;
+    bars.lister_fail = 0;
     tc05::fence_barrier_init();
   }
   if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, C::kTmemCols);
@@ -203,9 +465,14 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     for (int i = tid; i < (seg_len + 63) / 64; i += kThreads)
       hstart[i] = p.cand[(size_t)row * p.cand_stride + e0 + 64 * i];
   if (do_topk) sel.zero_hist(kHistBins);
+  const bool fast = do_topk && p.cluster_merge && p.fast_select;
+  if (fast)
+    for (int i = tid; i < kDecSegMax / 32; i += kThreads) listed[i] = 0u;
   tc05::fence_before();
   __syncthreads();
   tc05::fence_after();
+  // the histograms are zeroed: the other blocks' listers may read this one after this phase
+  if (fast) cluster_arrive();
   const uint32_t tmem = bars.tmem_base;
   // Every block of a single-wave grid is resident: a dependent kernel (the attention) may be
   // scheduled onto the SMs left free; it waits for this grid before it reads the indices.
@@ -290,6 +557,49 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
         bars.consumed = t + 1;
       }
       if (!ok) report_timeout(&bars.timeout, p.dev_status);
+    }
+    __syncwarp();
+  } else if (warp == 2 && fast) {
+    // ---------------------------------------------------------------- candidate lister
+    cluster_wait();  // every block of the cluster has zeroed its histogram
+    uint32_t bound = 0u, mx = 0u;
+    bool have = false, ok = true;
+    const int x1 = max(1, n_tiles / 2), x2 = max(x1 + 1, (3 * n_tiles) / 4);
+#pragma unroll 1
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!wait_tile_keys(bars.tile_keys, t)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = t * kTileKeys + 32 * u + lane;
+        if (j < seg_len) mx = max(mx, keys[j]);
+      }
+      if (t + 1 == x1 || t + 1 == x2) {
+        uint32_t m = mx;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&bars.maxkey) = m;
+        __syncwarp();
+        bound = max(bound, row_key_bound(selsh->hist, &bars.maxkey, (uint32_t)n_seg, p.K));
+        if (!have) {
+#pragma unroll 1
+          for (int t2 = 0; t2 < t; ++t2) mark_tile(listed, keys, t2, seg_len, bound);
+          have = true;
+        }
+      }
+      if (have) mark_tile(listed, keys, t, seg_len, bound);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) {
+      bars.maxkey = mx;  // every key of the segment (all tiles were read)
+      bars.bound = bound;
+    }
+    if (!ok && lane == 0) {
+      bars.lister_fail = 1;
+      report_timeout(&bars.timeout, p.dev_status);
     }
     __syncwarp();
   } else if (warp >= kDecEpiFirst) {
@@ -412,6 +722,13 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
         keys[jl] = key;
         if (valid) atomicAdd(&selsh->hist[key >> 20], 1);
       }
+      if (fast) {  // this warp's keys of tile t are stored: one count for the lister
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicAdd(&bars.tile_keys[t & 15], 1);
+        }
+      }
       if (srow && valid) srow[e0 + jl] = sc;
       if (seg_blocks && valid) atomicMax(&bkeys[jl / bs], key);
     }
@@ -428,6 +745,8 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     constexpr int kScratchWords = (kDecRingBytes + C::kQBytes) / 4;
     constexpr int kListRoom = kScratchWords - CSA2_MAX_TOPK;
     static_assert(ArrSel<kThreads / 32>::list_words(kDecSegMax) <= kListRoom, "selection lists fit in the scratch");
+    static_assert(2 * kFastCap + ArrSel<kThreads / 32>::list_words(kFastCap) <= kListRoom,
+                  "marked entries and their selection lists fit in the scratch");
     sel.scratch = reinterpret_cast<uint32_t*>(ring);
     int32_t* sel_idx = reinterpret_cast<int32_t*>(ring) + kListRoom;
     // record position of the segment's entry i
@@ -443,7 +762,103 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
         for (long long blk = (L_row + bs - 1) / bs + tid; blk < p.n_blocks; blk += kThreads)
           p.block_max[(size_t)row * p.bmax_stride + blk] = -INFINITY;
     }
-    if (do_topk && p.cluster_merge) {
+    bool fast_done = false;
+    if (fast) {
+      // ------------------------------------------------ selection among the marked entries
+      const uint32_t rank = cluster_rank();
+      if (warp != 2) cluster_wait();  // (the lister warp waited for this phase already)
+      // this block's marked entries, in entry order: keys at ring[0 ..), record positions at
+      // ring[kFastCap ..)
+      uint32_t* ck = reinterpret_cast<uint32_t*>(ring);
+      int32_t* cp = reinterpret_cast<int32_t*>(ring) + kFastCap;
+      const int n_words = (seg_len + 31) / 32;
+      uint32_t wa = 0u, wb = 0u;  // thread t: bitmap words 2t, 2t + 1
+      if (live && 2 * tid < n_words) wa = listed[2 * tid];
+      if (live && 2 * tid + 1 < n_words) wb = listed[2 * tid + 1];
+      int n_mine;
+      int at = sel.scan(__popc(wa) + __popc(wb), &n_mine);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t m = h ? wb : wa;
+        const int base = 32 * (2 * tid + h);
+        while (m) {
+          const int i = base + __ffs(m) - 1;
+          m &= m - 1u;
+          if (at < kFastCap) {
+            ck[at] = keys[i];
+            cp[at] = pos_of(i);
+          }
+          ++at;
+        }
+      }
+      // every block learns every block's count (pushed into each block's table)
+      if (tid < n_seg) {
+        cluster_st_s32(cluster_map(&bars.cand_cnt[rank], (uint32_t)tid), (!live || bars.lister_fail) ? -1 : n_mine);
+        cluster_st_s32(cluster_map(&bars.cand_lo[rank], (uint32_t)tid), (int)bars.bound);
+        cluster_st_s32(cluster_map(&bars.cand_hi[rank], (uint32_t)tid), (int)bars.maxkey);
+      }
+      cluster_sync();  // every block's marked entries and count are published
+      if (warp == 0) {
+        const int c = lane < n_seg ? bars.cand_cnt[lane] : 0;
+        const bool bad = __any_sync(0xffffffffu, c < 0);
+        int inc = max(c, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        if (lane <= n_seg) bars.cand_off[lane] = inc - max(c, 0);
+        const int total = __shfl_sync(0xffffffffu, inc, 31);
+        if (lane == 0) bars.cand_go = !bad && total <= kFastCap;
+      }
+      __syncthreads();
+      if (bars.cand_go) {
+        fast_done = true;
+        const int total = bars.cand_off[n_seg];
+        if (rank == 0) {
+          // the selection's histograms start at zero
+          for (int i = tid; i < kHistBins; i += kThreads) selsh->hist[i] = 0;
+          if (tid < 128) selsh->aux[tid] = 0u;
+          // block 0 appends the other blocks' lists to its own (same layout in every block)
+          // (16-byte loads of four entries; a list's last group may read up to three words past
+          // its end, inside the ring)
+#pragma unroll 1
+          for (int g = tid;; g += kThreads) {
+            int r = 1, g0 = 0;
+            while (r < n_seg && g >= g0 + (bars.cand_off[r + 1] - bars.cand_off[r] + 3) / 4) {
+              g0 += (bars.cand_off[r + 1] - bars.cand_off[r] + 3) / 4;
+              ++r;
+            }
+            if (r >= n_seg) break;
+            const int i = 4 * (g - g0), n_r = bars.cand_off[r + 1] - bars.cand_off[r], f = bars.cand_off[r] + i;
+            const uint4 kv = cluster_ld_v4(cluster_map(ck + i, (uint32_t)r));
+            const uint4 pv = cluster_ld_v4(cluster_map(cp + i, (uint32_t)r));
+            const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w}, pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (i + u < n_r) {
+                ck[f + u] = kk[u];
+                cp[f + u] = (int32_t)pp[u];
+              }
+          }
+          __syncthreads();
+          cluster_arrive();  // the other blocks' shared memory is no longer read
+          uint32_t lo = 0u, hi = 0u;
+          for (int r = 0; r < n_seg; ++r) {
+            lo = max(lo, bars.cand_lo[r]);
+            hi = max(hi, bars.cand_hi[r]);
+          }
+          select_marked(sel, ck, cp, total, p.K, lo, hi, p.idx + (size_t)row * p.K);
+          cluster_wait();
+        } else {
+          cluster_arrive();
+          cluster_wait();
+        }
+      }
+    }
+    if (fast_done) {
+      // (block 0 wrote the row's indices)
+    } else if (do_topk && p.cluster_merge) {
       // The row's segments form a thread-block cluster (rank = segment): the histogram
       // levels are summed over the cluster, so the blocks select the row's top-K together and
       // each writes its share of the row's indices at its offset; no lists leave the chip.
@@ -889,11 +1304,14 @@ cudaError_t launch_mma_decode_t(const ScanParams& p, long long n_seq_rows, int n
                         : make_tmap(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys) &&
                               make_tmap(&tmK64, p.k_idx, (unsigned long long)n_seq_rows, 64);
   if (!maps || !make_tmap(&tmQ, p.q_idx, (unsigned long long)p.n_rows * 32, 32)) return cudaErrorInvalidValue;
-  const size_t smem = dec_smem_bytes(p.K, max_seg_blocks, FP8);
+  ScanParams q = p;
+  q.seg_table = max_seg_blocks;
+  // the bitmap of marked entries follows the block table when it fits in shared memory
+  q.fast_select = p.cluster_merge && p.K > 0 && dec_smem_bytes(p.K, max_seg_blocks, FP8) + kFastBytes <= 232448;
+  const size_t smem = dec_smem_bytes(p.K, max_seg_blocks, FP8) + (q.fast_select ? kFastBytes : 0);
   auto kern = idx_mma_decode_kernel<FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ScanParams q = p;
   q.pdl_trigger = (long long)n_seg * p.n_rows <= device_sm_count();  // one CTA per SM: a single wave
   // Programmatic dependent launch: the blocks may become resident while the previous kernel
   // in the stream finishes; they wait for it before reading anything.

@@ -49,6 +49,10 @@ struct ScanParams {
   int32_t* dev_status;        // optional: CSA2_ETIMEOUT when a bounded wait gives up
   int pdl_trigger;            // set by the launcher: the grid is one wave, so a kernel launched
                               // after it with programmatic dependent launch may start early
+  int seg_table;              // set by the launcher: entries of the per-segment block table
+  int fast_select;            // set by the launcher (cluster selection): candidates are marked
+                              // during the stream against a running bound, and one block of the
+                              // cluster selects among them after it
 };
 
 // key format of the warp-MMA scan: 0 bf16, 1 FP8 rows, 2 MXFP4
