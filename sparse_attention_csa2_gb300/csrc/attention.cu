@@ -21,6 +21,7 @@
 //   partial  (M_h, l_h, O) of the tile go to the workspace.
 // A second kernel merges a row's tiles (log-sum-exp), adds the sink to the denominator,
 // normalises and turns the output's rotary coordinates back by -position.
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -356,11 +357,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   tc05::fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  copy_query(p, row, qs);  // the query is an input of the step, not of the previous kernel
+  // the query is an input of the step, not of the previous kernel: it is copied and rotated
+  // before the wait below
+  copy_query(p, row, qs);
   cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  rotate_query(qs, sh.cs);
   // With programmatic dependent launch this block may run while the kernel that writes the
-  // selected indices is still finishing: tiles with selected entries wait for it here (the
-  // query copies are in flight meanwhile).
+  // selected indices is still finishing: tiles with selected entries wait for it here.
   if (needs_idx) asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (tid < kTileE) {
     const EntrySrc s = entry_source(p, row, b, qp, lo, pos0, tile * kTileE + tid);
@@ -373,8 +378,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   gather_tile(sh.src, ks, p.q);
   cp_async_commit();
   cp_async_wait<0>();
-  __syncthreads();
-  rotate_query(qs, sh.cs);
   // generic-proxy writes (cp.async and stores) become visible to the tensor cores
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   tc05::fence_before();
@@ -540,74 +543,98 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   }
 }
 
-// Merges the tiles of one row for one head (block = (row, head), thread = 4 dims): per head
-// the log-sum-exp over the tiles plus the sink (in the denominator only), the normalised sum
-// of the tiles' outputs, and the inverse RoPE on dims 448..511.  Every tile's partial of the
-// thread's dims is loaded at once (one memory round trip).
+// Merges the tiles of a row for one head: the log-sum-exp over the tiles plus the sink (in the
+// denominator only), the normalised sum of the tiles' outputs, and the inverse RoPE on dims
+// 448..511.  One warp per (row, head) item, lane l holding dims 4l + 128j (j = 0..3); a grid
+// of one block per SM (16 warps) walks the items, one round for up to 16 items per SM (the
+// merge is bound by the latency of its L2 reads, so the items should all be in flight at
+// once).  A warp issues the loads of all of an item's tile partials (up to kCombPre tiles at
+// once) and its tile statistics together, then forms the factors; the rotary cos / sin of its
+// row come from one lane per pair by shuffles.
 constexpr int kMaxTiles = 16;  // K + window <= 2048 entries
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int n_tiles) {
-  __shared__ float fac[kMaxTiles];
-  __shared__ float inv_den;
-  __shared__ float cs[kRopeDim];
+constexpr int kCombWarps = 16;
+constexpr int kCombPre = 6;    // tiles whose partials a lane holds at once
+__global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const AttnParams p, int n_tiles) {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the tiles' partials are complete
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const long long qp = p.q_pos[row];
-  if (tid < 32) {
-    // the row's tile statistics for head h, one tile per lane
-    const float sk = __ldg(p.sink + h);
+  const int lane = threadIdx.x & 31;
+  const int n_items = p.n_rows * kHeads;
+#pragma unroll 1
+  for (int item = blockIdx.x * kCombWarps + (threadIdx.x >> 5); item < n_items; item += gridDim.x * kCombWarps) {
+    const int row = item / kHeads, h = item % kHeads;
+    const float* base = p.part_o + ((size_t)row * n_tiles * kHeads + h) * kHeadDim + 4 * lane;
+    const size_t tile_stride = (size_t)kHeads * kHeadDim;
+    float4 v[kCombPre][4];
+#pragma unroll
+    for (int t = 0; t < kCombPre; ++t)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[t][j] = t < n_tiles ? __ldcg(reinterpret_cast<const float4*>(base + t * tile_stride + 128 * j))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    // this lane's tile statistics (lane t: tile t) and the row's rotary pair `lane`
     float m = -INFINITY, l = 0.f;
-    if (tid < n_tiles) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + ((size_t)row * n_tiles + tid) * kHeads + h);
-      m = v.x;
-      l = v.y;
+    if (lane < n_tiles) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + ((size_t)row * n_tiles + lane) * kHeads + h);
+      m = ml.x;
+      l = ml.y;
     }
+    float cs_c, cs_s;
+    rope_cs(p.q_pos[row], p.inv_freq[lane], -1.f, &cs_c, &cs_s);
+    const float sk = __ldg(p.sink + h);
     const float M = fmaxf(warp_max(m), sk);
     const float f = m == -INFINITY ? 0.f : __expf(m - M);
     const float den = warp_sum(l * f) + __expf(sk - M);
-    if (tid < n_tiles) fac[tid] = f;
-    if (tid == 0) {
-      inv_den = 1.f / den;
-      if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + h] = __expf(sk - M) / den;
+    const float inv_den = 1.f / den;
+    if (lane == 0 && p.sink_mass) p.sink_mass[(size_t)row * kHeads + h] = __expf(sk - M) * inv_den;
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < kCombPre; ++t) {
+      const float ft = __shfl_sync(0xffffffffu, f, t);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j].x = fmaf(ft, v[t][j].x, acc[j].x);
+        acc[j].y = fmaf(ft, v[t][j].y, acc[j].y);
+        acc[j].z = fmaf(ft, v[t][j].z, acc[j].z);
+        acc[j].w = fmaf(ft, v[t][j].w, acc[j].w);
+      }
     }
-  } else if (tid < 64) {
-    rope_cs(qp, p.inv_freq[tid - 32], -1.f, &cs[tid - 32], &cs[tid]);
-  }
-  const int d = 4 * tid;
-  const float* base = p.part_o + ((size_t)row * n_tiles * kHeads + h) * kHeadDim + d;
-  float4 v[kMaxTiles];
+#pragma unroll 1
+    for (int t = kCombPre; t < n_tiles; ++t) {  // rows with more tiles than a lane holds
+      const float ft = __shfl_sync(0xffffffffu, f, t);
 #pragma unroll
-  for (int t = 0; t < kMaxTiles; ++t)
-    v[t] = t < n_tiles ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)t * kHeads * kHeadDim))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-  __syncthreads();
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int t = 0; t < kMaxTiles; ++t) {
-    const float f = t < n_tiles ? fac[t] : 0.f;
-    acc.x = fmaf(f, v[t].x, acc.x);
-    acc.y = fmaf(f, v[t].y, acc.y);
-    acc.z = fmaf(f, v[t].z, acc.z);
-    acc.w = fmaf(f, v[t].w, acc.w);
-  }
-  float o[4] = {acc.x * inv_den, acc.y * inv_den, acc.z * inv_den, acc.w * inv_den};
-  if (d >= kHeadDim - kRopeDim) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int pi = (d + 2 * j - (kHeadDim - kRopeDim)) >> 1;
-      const float c = cs[pi], sn = cs[32 + pi];
-      const float x = o[2 * j], y = o[2 * j + 1];
-      o[2 * j] = x * c - y * sn;
-      o[2 * j + 1] = x * sn + y * c;
+      for (int j = 0; j < 4; ++j) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(base + t * tile_stride + 128 * j));
+        acc[j].x = fmaf(ft, x.x, acc[j].x);
+        acc[j].y = fmaf(ft, x.y, acc[j].y);
+        acc[j].z = fmaf(ft, x.z, acc[j].z);
+        acc[j].w = fmaf(ft, x.w, acc[j].w);
+      }
     }
-  }
-  const size_t at = ((size_t)row * kHeads + h) * kHeadDim + d;
-  if (p.out_bf16) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]), hi = __floats2bfloat162_rn(o[2], o[3]);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-  } else {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + at) = make_float4(o[0], o[1], o[2], o[3]);
+    // inverse rotation: dims 448 + 4(l - 16) .. of chunk j = 3 hold pairs 2(l - 16) and 2(l - 16) + 1
+    const int pa = 2 * (lane & 15), pb = pa + 1;
+    const float ca = __shfl_sync(0xffffffffu, cs_c, pa), sa = __shfl_sync(0xffffffffu, cs_s, pa);
+    const float cb = __shfl_sync(0xffffffffu, cs_c, pb), sb = __shfl_sync(0xffffffffu, cs_s, pb);
+    float4 o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = make_float4(acc[j].x * inv_den, acc[j].y * inv_den, acc[j].z * inv_den, acc[j].w * inv_den);
+    if (lane >= 16) {
+      const float x0 = o[3].x, y0 = o[3].y, x1 = o[3].z, y1 = o[3].w;
+      o[3] = make_float4(x0 * ca - y0 * sa, x0 * sa + y0 * ca, x1 * cb - y1 * sb, x1 * sb + y1 * cb);
+    }
+    const size_t at = ((size_t)row * kHeads + h) * kHeadDim + 4 * lane;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (p.out_bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(o[j].x, o[j].y), hi = __floats2bfloat162_rn(o[j].z, o[j].w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at + 128 * j) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + at + 128 * j) = o[j];
+      }
+    }
   }
 }
 
@@ -634,8 +661,10 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_tc05_kernel, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(p.n_rows, kHeads);
-  cfg.blockDim = dim3(128);
+  const int items = p.n_rows * kHeads;
+  const int blocks = std::min(device_sm_count(), (items + kCombWarps - 1) / kCombWarps);
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kCombWarps * 32);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, n_split);
 }
