@@ -501,11 +501,19 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
     ic.block_max = nullptr;
     const int cand_run = a->mode == CSA2_MODE_REINDEX ? a->block_size : 0;
-    if (scan_path(&ic, true, cand_run) == ScanPath::kTc05Decode)
-      n_seg = tc05_segments(n_rows, L, a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128,
-                            a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
-    else  // candidate lists (Reindex) are short: smaller segments keep enough blocks busy
+    if (scan_path(&ic, true, cand_run) == ScanPath::kTc05Decode) {
+      const int unit = a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128;
+      n_seg = tc05_segments(n_rows, L, unit, a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
+      // A row's segments select its top-K together as one thread-block cluster of at most 16
+      // blocks; where more segments were planned, 16 per row still keep at least 64 blocks
+      // streaming and each segment within shared memory, and save the list merge.
+      const long long units = (L + unit - 1) / unit;
+      if (n_seg > 16 && (long long)n_rows * 16 >= 64 && (units + 15) / 16 <= mma_decode_max_seg_blocks() &&
+          (units + 15) / 16 <= mma_decode_max_segment() / unit)
+        n_seg = 16;
+    } else {  // candidate lists (Reindex) are short: smaller segments keep enough blocks busy
       n_seg = scan_segments(n_rows, L, a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
+    }
     ws += lists_bytes(n_rows, n_seg, a->K);
     if (n_seg > 1) ws += align_up((size_t)n_rows * 8);  // per-row completion counters
     if (a->mode == CSA2_MODE_FULL_POOL) {

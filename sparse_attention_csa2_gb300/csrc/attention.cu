@@ -41,7 +41,6 @@ constexpr int kKPanel = kTileE * 128;              // 16 KB: 128 entries x 64 di
 constexpr int kQBytes = 9 * kQPanel;               // 72 KB
 constexpr int kKBytes = 8 * kKPanel;               // 128 KB
 constexpr int kPBytes = kTileE * 128;              // 16 KB: 128 entries x 64 heads (bf16)
-constexpr uint32_t kTmemCols = 512;                // S^T in columns 0..63, then O^T in all 512
 
 struct TileSrc {
   const uint8_t* ptr[kTileE];   // first byte of each entry's row (codes for FP formats)
@@ -250,26 +249,29 @@ __device__ __forceinline__ void gather_tile(const TileSrc& m, uint8_t* ks, const
   }
 }
 
-// The row's query (64 heads x 512 dims) into `qs` (panel layout, 64 rows) by cp.async, one
-// 16-byte chunk per copy (consecutive threads on consecutive chunks); rotate_query then turns
-// the rotary pairs (dims 448 + 2i, 448 + 2i + 1) in place once the copies have landed.
-__device__ __forceinline__ void copy_query(const AttnParams& p, int row, uint8_t* qs) {
-  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q) + (size_t)row * kHeads * kHeadDim * 2;
+// Heads h0 .. h0+NH-1 of the row's query (NH x 512 dims) into `qs` (panel layout, NH rows per
+// 64-dim panel) by cp.async, one 16-byte chunk per copy (consecutive threads on consecutive
+// chunks); rotate_query then turns the rotary pairs (dims 448 + 2i, 448 + 2i + 1) in place once
+// the copies have landed.
+template <int NH>
+__device__ __forceinline__ void copy_query(const AttnParams& p, int row, int h0, uint8_t* qs) {
+  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q) + ((size_t)row * kHeads + h0) * kHeadDim * 2;
 #pragma unroll 1  // run-once code: kept small for the instruction cache (measured)
-  for (int k = 0; k < kHeads * kHeadDim / 8 / kAttnThreads; ++k) {
+  for (int k = 0; k < NH * kHeadDim / 8 / kAttnThreads; ++k) {
     const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 6, ch = idx & 63;
-    cp_async16(qs + sw128_off(h, ch, kHeads), qsrc + (size_t)idx * 16, true);
+    cp_async16(qs + sw128_off(h, ch, NH), qsrc + (size_t)idx * 16, true);
   }
 }
 // The rotated coordinates go to the tensor cores as two bf16 terms, hi = bf16(x') in panel 7
 // and lo = bf16(x' - hi) in panel 8 (a ninth K-panel of the first GEMM), so the logits see x'
 // to ~2^-16 instead of bf16's 2^-8: with peaked attention that rounding was the largest error
 // of the output.
+template <int NH>
 __device__ __forceinline__ void rotate_query(uint8_t* qs, const float* cs) {
 #pragma unroll 1  // run-once code: kept small for the instruction cache (measured)
-  for (int k = 0; k < kHeads * 8 / kAttnThreads; ++k) {
-    const int idx = k * kAttnThreads + threadIdx.x, h = idx >> 3, ch = 56 + (idx & 7);
-    uint4* q4 = reinterpret_cast<uint4*>(qs + sw128_off(h, ch, kHeads));
+  for (int idx = threadIdx.x; idx < NH * 8; idx += kAttnThreads) {
+    const int h = idx >> 3, ch = 56 + (idx & 7);
+    uint4* q4 = reinterpret_cast<uint4*>(qs + sw128_off(h, ch, NH));
     const uint4 v = *q4;
     uint32_t w4[4] = {v.x, v.y, v.z, v.w}, lo4[4];
 #pragma unroll
@@ -282,7 +284,7 @@ __device__ __forceinline__ void rotate_query(uint8_t* qs, const float* cs) {
       lo4[j] = pack_bf16x2(xr - bf16_lo(w4[j]), yr - bf16_hi(w4[j]));
     }
     *q4 = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(q4) + kQPanel) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(q4) + NH * 128) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
   }
 }
 
@@ -318,11 +320,21 @@ __device__ __forceinline__ void report_timeout_attn(int* flag, int32_t* dev_stat
   if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
 }
 
-// One block: tile blockIdx.x (entries 128*x .. 128*x+127) of query row blockIdx.y, all 64
-// heads.  Warp 0 allocates tensor memory and issues the MMAs (one thread); every warp
-// gathers, runs the softmax for 32 entries x 32 heads (one thread per TMEM lane = entry)
-// and writes partials.
+// One block: tile t (entries 128t .. 128t+127) of query row blockIdx.x, for NH of the 64
+// heads (NH = 64, or 32 / 16 where rows x tiles alone would leave most SMs idle: the heads
+// split across 64 / NH blocks, each gathering the tile).  Warp 0 allocates tensor memory and
+// issues the MMAs (one thread); every warp gathers, runs the softmax for 32 entries x NH / 2
+// heads (one thread per TMEM lane = entry) and writes partials.
+template <int NH>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnParams p) {
+  constexpr int HALF = NH / 2;            // heads of a warp's softmax share
+  constexpr int NG = HALF / 8;            // groups of 8 of them
+  constexpr int QPANEL = NH * 128;        // one 64-dim panel of the query: NH rows x 128 B
+  constexpr int NO = 2 * NH;              // second GEMM's N: P_hi | P_lo
+  constexpr uint32_t kCols = 4 * NO;      // tensor memory: O^T, four chunks of 128 dims
+  constexpr int HS = kHeads / NH;         // blocks per tile
+  static_assert(NH == 64 || NH == 32 || NH == 16, "heads per block");
+  static_assert(9 * QPANEL <= kQBytes, "query panels fit");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1k(smem_raw);
   uint8_t* qs = smem;              // q' (first GEMM), then P_hi | P_lo (second GEMM)
@@ -330,11 +342,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   AttnShared& sh = *reinterpret_cast<AttnShared*>(ks + kKBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // blockIdx.y = k orders the tiles so that the window-only tiles (which need nothing from
-  // the previous kernel) come first; tile = (k + tiles holding selected entries) mod tiles
-  const int row = blockIdx.x, n_tiles = gridDim.y;
+  // blockIdx.y = HS k + head group orders the tiles so that the window-only tiles (which need
+  // nothing from the previous kernel) come first; tile = (k + tiles holding selected entries)
+  // mod tiles
+  const int row = blockIdx.x, n_tiles = gridDim.y / HS, h0 = (blockIdx.y % HS) * NH;
   const int sel_tiles = min(n_tiles, (p.K + kTileE - 1) / kTileE);
-  const int tile = (blockIdx.y + sel_tiles) % n_tiles;
+  const int tile = (blockIdx.y / HS + sel_tiles) % n_tiles;
   const bool needs_idx = tile * kTileE < p.K;
   const int b = p.seq_of_row[row];
   const long long qp = p.q_pos[row];
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
     sh.s_issued = sh.o_issued = 0;
     tc05::fence_barrier_init();
   }
-  if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kTmemCols);
+  if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kCols);
   rope_table(sh.cs, p, qp, 1.f);
   // the next kernel in the stream may launch now (it waits for this grid before reading)
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -359,11 +372,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
 
   // the query is an input of the step, not of the previous kernel: it is copied and rotated
   // before the wait below
-  copy_query(p, row, qs);
+  copy_query<NH>(p, row, h0, qs);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
-  rotate_query(qs, sh.cs);
+  rotate_query<NH>(qs, sh.cs);
   // With programmatic dependent launch this block may run while the kernel that writes the
   // selected indices is still finishing: tiles with selected entries wait for it here.
   if (needs_idx) asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -388,18 +401,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   // ---------------------------------------------------------------- S^T = K q'^T
   if (warp == 0) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc05::idesc_bf16(128, kHeads);
+      constexpr uint32_t idesc = tc05::idesc_bf16(128, NH);
 #pragma unroll 1
       for (int kk = 0; kk < kHeadDim / 16; ++kk) {
         const uint32_t sub = (kk & 3) * 32;
         tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + (kk >> 2) * kKPanel + sub),
-                       tc05::sw128_desc(qs_u + (kk >> 2) * kQPanel + sub), idesc, kk > 0);
+                       tc05::sw128_desc(qs_u + (kk >> 2) * QPANEL + sub), idesc, kk > 0);
       }
       // the low parts of the rotated query against the tile's rotary panel
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk)
         tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + 7 * kKPanel + kk * 32),
-                       tc05::sw128_desc(qs_u + 8 * kQPanel + kk * 32), idesc, 1u);
+                       tc05::sw128_desc(qs_u + 8 * QPANEL + kk * 32), idesc, 1u);
       tc05::mma_commit(&sh.bar_s);
       sh.s_issued = 1;
     }
@@ -407,10 +420,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   }
 
   // ---------------------------------------------------------------- softmax over the tile
-  // warp w: TMEM lanes 32*(w&3) .. +31 (entry e = one lane), heads 32*(w>>2) .. +31, in four
-  // groups of 8 heads read from TMEM as needed (rolled loops keep this run-once code small
-  // enough for the instruction cache)
-  const int qw = warp & 3, hb = 32 * (warp >> 2), e = 32 * qw + lane;
+  // warp w: TMEM lanes 32*(w&3) .. +31 (entry e = one lane), heads HALF*(w>>2) .. + HALF - 1
+  // of the block's NH, in groups of 8 (rolled loops keep this run-once code small enough for
+  // the instruction cache)
+  const int qw = warp & 3, hb = HALF * (warp >> 2), e = 32 * qw + lane;
   const int lh = (lane >> 2) & 7;  // head within a group of 8 whose result this lane ends with
   {
     const bool ok = tc05::mbar_wait(&sh.bar_s, 0);
@@ -421,18 +434,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
     const bool on = ok && f >= 0;  // off: masked entry (logit -inf)
     const float zs = p.scale * rs;
     const uint32_t trow = tmem + ((uint32_t)(32 * qw) << 16) + (uint32_t)hb;
-    // the thread's 32 logits (entry e, heads hb .. hb+31) stay in registers for both passes
-    float z[32];
+    // the thread's HALF logits (entry e, heads hb .. hb + HALF - 1) stay in registers for both
+    // passes
+    float z[HALF];
     {
-      uint32_t v[32];
-      tc05::tmem_ld32(trow, v);
+      uint32_t v[HALF];
+      tc05::tmem_ld<HALF>(trow, v);
       tc05::tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
+      for (int k = 0; k < HALF; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
     }
     // per-head maximum over the tile's entries
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < NG; ++g) {
       float m[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) m[k] = z[8 * g + k];
@@ -440,14 +454,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
       if ((lane & 3) == 0) sh.red[qw][hb + 8 * g + lh] = m[0];
     }
     __syncthreads();
-    if (qw == 0)
+    if (qw == 0 && lane < HALF)
       sh.mfin[hb + lane] = fmaxf(fmaxf(sh.red[0][hb + lane], sh.red[1][hb + lane]),
                                  fmaxf(sh.red[2][hb + lane], sh.red[3][hb + lane]));
     __syncthreads();
-    // P = exp(z - M) as P_hi | P_lo rows (entry e, MN-major for the second GEMM), the FP8
-    // row scale on the weights; per-head sums of the unscaled P
+    // P = exp(z - M) as P_hi | P_lo rows (entry e, MN-major for the second GEMM: 64 heads of
+    // P_hi in one 128-byte row and P_lo in a second chunk kPBytes on; with fewer heads P_lo
+    // follows P_hi in the same row), the FP8 row scale on the weights; per-head sums of the
+    // unscaled P
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < NG; ++g) {
       const float4 m0 = *reinterpret_cast<const float4*>(&sh.mfin[hb + 8 * g]);
       const float4 m1 = *reinterpret_cast<const float4*>(&sh.mfin[hb + 8 * g + 4]);
       const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
@@ -461,9 +477,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
         hi[k] = pack_bf16x2(a0, a1);
         lw[k] = pack_bf16x2(a0 - bf16_lo(hi[k]), a1 - bf16_hi(hi[k]));
       }
-      const int off = e * 128 + (((hb / 8 + g) ^ (e & 7)) << 4);
+      const int ci = hb / 8 + g;  // 16-byte chunk of this group's heads
+      const int off = e * 128 + ((ci ^ (e & 7)) << 4);
+      const int off_lo = NH == 64 ? kPBytes + off : e * 128 + (((NH / 8 + ci) ^ (e & 7)) << 4);
       *reinterpret_cast<uint4*>(qs + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(qs + kPBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4*>(qs + off_lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       group_reduce8<false>(pe);
       if ((lane & 3) == 0) sh.red_sum[qw][hb + 8 * g + lh] = pe[0];
     }
@@ -474,18 +492,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   tc05::fence_after();
 
   // ---------------------------------------------------------------- O^T = V^T [P_hi | P_lo]^T
-  // S^T is dead now: chunk c of 128 dims accumulates into columns 128c .. 128c+127, the
-  // P_hi products in the first 64, the P_lo products in the last 64.
+  // S^T is dead now: chunk c of 128 dims accumulates into columns NO*c .. NO*c + NO - 1, the
+  // P_hi products in the first NH, the P_lo products in the last NH.
   if (warp == 0) {
     if (lane == 0 && !sh.timeout) {
       // A = V^T (dims x entries, MN-major: 64-dim panels 16 KB apart, 8-entry groups 1 KB
       // apart); B = [P_hi | P_lo]^T (entries x 128, MN-major: two 64-column chunks 16 KB
       // apart, 8-entry groups 1 KB apart)
-      constexpr uint32_t idesc = tc05::idesc_bf16(128, 2 * kHeads) | (1u << 15) | (1u << 16);
+      constexpr uint32_t idesc = tc05::idesc_bf16(128, NO) | (1u << 15) | (1u << 16);
 #pragma unroll 1
       for (int i = 0; i < 4 * (kTileE / 16); ++i) {
         const int c = i >> 3, kk = i & 7;
-        tc05::mma_bf16(tmem + 128 * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel + kk * 2048, kKPanel, 1024),
+        tc05::mma_bf16(tmem + NO * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel + kk * 2048, kKPanel, 1024),
                        sw128_desc_lbo(qs_u + kk * 2048, kPBytes, 1024), idesc, kk > 0);
       }
       tc05::mma_commit(&sh.bar_o);
@@ -502,29 +520,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   if (!live && sh.o_issued && lane == 0) report_timeout_attn(&sh.timeout, p.dev_status);
   tc05::fence_after();
   if (live) {
-    float* po = p.part_o + ((size_t)row * n_tiles + tile) * kHeads * kHeadDim;
+    constexpr int W = NH < 32 ? NH : 32;  // heads per TMEM load
+    float* po = p.part_o + (((size_t)row * n_tiles + tile) * kHeads + h0) * kHeadDim;
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      const int c = 2 * (warp >> 2) + (i >> 1), g = i & 1;  // heads 32g .. 32g+31 of dim chunk c
+    for (int i = 0; i < 2 * (NH / W); ++i) {
+      const int c = 2 * (warp >> 2) + i / (NH / W), g = i % (NH / W);  // heads W*g .. of dim chunk c
       const int d = 128 * c + 32 * qw + lane;
-      uint32_t vh[32], vl[32];
-      const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + 128 * c + 32 * g;
-      tc05::tmem_ld32(ta, vh);
-      tc05::tmem_ld32(ta + 64, vl);
+      uint32_t vh[W], vl[W];
+      const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + NO * c + W * g;
+      tc05::tmem_ld<W>(ta, vh);
+      tc05::tmem_ld<W>(ta + NH, vl);
       tc05::tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        po[(size_t)(32 * g + k) * kHeadDim + d] = __uint_as_float(vh[k]) + __uint_as_float(vl[k]);
+      for (int k = 0; k < W; ++k)
+        po[(size_t)(W * g + k) * kHeadDim + d] = __uint_as_float(vh[k]) + __uint_as_float(vl[k]);
     }
   }
   if (warp == 4) {
-    float* pm = p.part_ml + ((size_t)row * n_tiles + tile) * kHeads * 2;
+    float* pm = p.part_ml + (((size_t)row * n_tiles + tile) * kHeads + h0) * 2;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int h = 2 * lane + j;
-      const float l = (sh.red_sum[0][h] + sh.red_sum[1][h]) + (sh.red_sum[2][h] + sh.red_sum[3][h]);
-      pm[2 * h] = live ? sh.mfin[h] : -INFINITY;
-      pm[2 * h + 1] = live ? l : 0.f;
+      if (h < NH) {
+        const float l = (sh.red_sum[0][h] + sh.red_sum[1][h]) + (sh.red_sum[2][h] + sh.red_sum[3][h]);
+        pm[2 * h] = live ? sh.mfin[h] : -INFINITY;
+        pm[2 * h + 1] = live ? l : 0.f;
+      }
     }
   }
 
@@ -539,7 +560,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   __syncthreads();
   if (warp == 0) {
     tc05::fence_after();
-    tc05::tmem_dealloc(tmem, kTmemCols);
+    tc05::tmem_dealloc(tmem, kCols);
   }
 }
 
@@ -644,8 +665,13 @@ int attn_smem_bytes() { return kAttnSmemBytes; }
 
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+  // Heads per block: all 64, or 32 / 16 where rows x tiles blocks would leave most SMs idle
+  // (the tile chain then runs on half / a quarter of the heads, in parallel).
+  const int sms = device_sm_count();
+  const long long tiles = (long long)p.n_rows * n_split;
+  const int nh = tiles * 4 <= sms ? 16 : tiles * 2 <= sms ? 32 : 64;
+  auto kern = nh == 16 ? attn_tc05_kernel<16> : nh == 32 ? attn_tc05_kernel<32> : attn_tc05_kernel<64>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
   if (e != cudaSuccess) return e;
   // Both kernels may start before their predecessor in the stream has finished (programmatic
   // dependent launch); each waits for it where it reads its results.
@@ -653,13 +679,13 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_rows, n_split);
+  cfg.gridDim = dim3(p.n_rows, n_split * (kHeads / nh));
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = kAttnSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc05_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   const int items = p.n_rows * kHeads;
   const int blocks = std::min(device_sm_count(), (items + kCombWarps - 1) / kCombWarps);

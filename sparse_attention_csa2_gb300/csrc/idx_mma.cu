@@ -730,7 +730,15 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
         }
       }
       if (srow && valid) srow[e0 + jl] = sc;
-      if (seg_blocks && valid) atomicMax(&bkeys[jl / bs], key);
+      if (seg_blocks) {
+        // block maxima: a warp's 32 records lie in one block when bs >= 32 (one atomic per warp)
+        if (bs >= 32) {
+          const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+          if (lane == 0 && m != 0u) atomicMax(&bkeys[(t * kTileKeys + 32 * quarter) / bs], m);
+        } else if (valid) {
+          atomicMax(&bkeys[jl / bs], key);
+        }
+      }
     }
   }
 
