@@ -492,7 +492,10 @@ typedef enum csa2_tuning {
   CSA2_TUNE_SCAN_CLUSTER = 2,   /* 0: the tcgen05 decode scan's segments merge through lists
                                    instead of selecting as a cluster; 1 = automatic (default) */
   CSA2_TUNE_PROJ_KSPLIT = 3,    /* K split of the projection GEMMs, 1..8; 0 = automatic */
-  CSA2_TUNE_COUNT = 4
+  CSA2_TUNE_ATTN_ROWS = 4,      /* attention kernel: 1 = a block per (row, 128-entry tile) and a
+                                   merge kernel; 2 / 3 = a block per (row, 32 / 16 heads) over all
+                                   of the row's tiles; 0 = automatic */
+  CSA2_TUNE_COUNT = 5
 } csa2_tuning;
 /* Returns CSA2_EINVAL for an unknown knob or a value outside its range. */
 csa2_status csa2_set_tuning(int32_t knob, int32_t value);

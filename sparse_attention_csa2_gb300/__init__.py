@@ -135,8 +135,9 @@ _set_tuning = _sig("csa2_set_tuning", [C.c_int32, C.c_int32], C.c_int)
 _selftest_wait = _sig("csa2_selftest_wait_timeout", [_vp, C.c_int32, _vp], C.c_int)
 
 # launch-heuristic overrides (csa2_tuning)
-TUNE_SCAN_SEGMENTS, TUNE_SCAN_WARP_MMA, TUNE_SCAN_CLUSTER, TUNE_PROJ_KSPLIT = 0, 1, 2, 3
-_TUNE_DEFAULTS = {TUNE_SCAN_SEGMENTS: 0, TUNE_SCAN_WARP_MMA: 0, TUNE_SCAN_CLUSTER: 1, TUNE_PROJ_KSPLIT: 0}
+TUNE_SCAN_SEGMENTS, TUNE_SCAN_WARP_MMA, TUNE_SCAN_CLUSTER, TUNE_PROJ_KSPLIT, TUNE_ATTN_ROWS = 0, 1, 2, 3, 4
+_TUNE_DEFAULTS = {TUNE_SCAN_SEGMENTS: 0, TUNE_SCAN_WARP_MMA: 0, TUNE_SCAN_CLUSTER: 1, TUNE_PROJ_KSPLIT: 0,
+                  TUNE_ATTN_ROWS: 0}
 
 
 def version() -> int:

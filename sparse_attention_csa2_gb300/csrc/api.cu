@@ -30,7 +30,7 @@ int device_sm_count() {
 // Process-wide overrides of the launch heuristics (csa2_set_tuning); the defaults mean
 // "chosen per call from the shapes and the device".
 namespace {
-std::atomic<int> g_tuning[CSA2_TUNE_COUNT] = {{0}, {0}, {1}, {0}};
+std::atomic<int> g_tuning[CSA2_TUNE_COUNT] = {{0}, {0}, {1}, {0}, {0}};
 }  // namespace
 
 int tuning(int knob) { return g_tuning[knob].load(std::memory_order_relaxed); }
@@ -359,6 +359,7 @@ csa2_status csa2_set_tuning(int32_t knob, int32_t value) {
   if (knob < 0 || knob >= CSA2_TUNE_COUNT || value < 0) return CSA2_EINVAL;
   if (knob == CSA2_TUNE_SCAN_SEGMENTS && value > 64) return CSA2_EINVAL;
   if (knob == CSA2_TUNE_PROJ_KSPLIT && value > 8) return CSA2_EINVAL;
+  if (knob == CSA2_TUNE_ATTN_ROWS && value > 3) return CSA2_EINVAL;
   g_tuning[knob].store(value, std::memory_order_relaxed);
   return CSA2_OK;
 }

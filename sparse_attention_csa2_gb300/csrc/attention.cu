@@ -564,6 +564,320 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   }
 }
 
+// ===================================================================================== rows
+// One block: every tile of query row blockIdx.x for the NH heads h0 = NH * blockIdx.y .., one
+// tile after another with the softmax carried across the tiles.  Each head keeps a reference
+// maximum M: the first tile's maximum, moved only when a later tile's maximum exceeds it by
+// more than kRowTau (the output accumulated in tensor memory and the running sum are then
+// scaled by exp(M_old - M_new)), so P = exp(z - M) <= e^kRowTau and every tile's second GEMM
+// accumulates into the same tensor memory.  After the last tile the sink joins the
+// denominator, the output is normalised, its rotary coordinates are turned back by -position
+// and it is written directly: no partials and no merge kernel.  The window tile (which needs
+// nothing from the previous kernel) comes first.
+constexpr float kRowTau = 8.f;
+
+struct RowShared {
+  TileSrc src;
+  float red[4][32];  // per TMEM lane quarter: per-head maxima, then sums, over its 32 entries
+  float mref[32];    // reference maximum per head
+  float alpha[32];   // this tile's rescale factor per head (1: unchanged), then the output factor
+  float lsum[32];    // running sum of P per head, relative to mref
+  float cs[kRopeDim];
+  uint64_t bar_s, bar_o;  // first / second GEMM of the current tile completed
+  uint32_t tmem_base;
+  int timeout;
+  int rescale;  // some head's reference moved at this tile
+  int s_issued, o_issued;  // tiles whose first / second GEMM was issued
+};
+
+template <int NH>
+constexpr int row_smem_bytes() {
+  return 1024 + 9 * NH * 128 + kPBytes + kKBytes + (int)sizeof(RowShared);
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_row_kernel(const AttnParams p) {
+  constexpr int HALF = NH / 2;            // heads of a warp's softmax share
+  constexpr int NG = HALF / 8;            // groups of 8 of them
+  constexpr int QPANEL = NH * 128;        // one 64-dim panel of the query
+  constexpr int NO = 2 * NH;              // second GEMM's N: P_hi | P_lo
+  constexpr uint32_t kS0 = 4 * NO;        // tensor memory: O in [0, kS0), S^T in [kS0, kS0 + NH)
+  constexpr uint32_t kCols = NH == 32 ? 512 : 256;
+  static_assert(NH == 16 || NH == 32, "heads per block");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1k(smem_raw);
+  uint8_t* qs = smem;                     // q' (nine panels), kept for every tile
+  uint8_t* ps = qs + 9 * QPANEL;          // P_hi | P_lo of the current tile
+  uint8_t* ks = ps + kPBytes;             // the current tile's latents
+  RowShared& sh = *reinterpret_cast<RowShared*>(ks + kKBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = blockIdx.x, h0 = blockIdx.y * NH;
+  const int n_tiles = (p.K + p.window + kTileE - 1) / kTileE;
+  const int sel_tiles = min(n_tiles, (p.K + kTileE - 1) / kTileE);
+  const int b = p.seq_of_row[row];
+  const long long qp = p.q_pos[row];
+  const long long pos0 = p.swa_pos0[b];
+  const long long lo = max(qp - (long long)p.window + 1, pos0);
+
+  if (tid == 0) {
+    tc05::mbar_init(&sh.bar_s, 1);
+    tc05::mbar_init(&sh.bar_o, 1);
+    sh.timeout = 0;
+    sh.rescale = 0;
+    sh.s_issued = sh.o_issued = 0;
+    tc05::fence_barrier_init();
+  }
+  if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kCols);
+  rope_table(sh.cs, p, qp, 1.f);
+  if (tid < NH) {
+    sh.mref[tid] = -INFINITY;
+    sh.lsum[tid] = 0.f;
+  }
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  const uint32_t qs_u = smem_u32(qs), ps_u = smem_u32(ps), ks_u = smem_u32(ks);
+
+  // the query is an input of the step: copied and rotated before any wait
+  copy_query<NH>(p, row, h0, qs);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  rotate_query<NH>(qs, sh.cs);
+
+  const int qw = warp & 3, hb = HALF * (warp >> 2), e = 32 * qw + lane;
+  const int lh = (lane >> 2) & 7;  // head within a group of 8 whose result this lane ends with
+  bool waited = false;
+#pragma unroll 1
+  for (int kt = 0; kt < n_tiles; ++kt) {
+    const int tile = (kt + sel_tiles) % n_tiles;
+    // tiles with selected entries wait for the kernel that writes the indices
+    if (!waited && tile * kTileE < p.K) {
+      asm volatile("griddepcontrol.wait;\n" ::: "memory");
+      waited = true;
+    }
+    // the previous tile's second GEMM is done: its latents and P may be overwritten
+    if (kt > 0 && !sh.timeout && !tc05::mbar_wait(&sh.bar_o, (kt - 1) & 1) && lane == 0)
+      report_timeout_attn(&sh.timeout, p.dev_status);
+    if (tid < kTileE) {
+      const EntrySrc sr = entry_source(p, row, b, qp, lo, pos0, tile * kTileE + tid);
+      sh.src.ptr[tid] = sr.valid ? sr.ptr : nullptr;
+      sh.src.sptr[tid] = sr.sptr;
+      sh.src.rs[tid] = sr.rs;
+      sh.src.fmt[tid] = sr.valid ? sr.fmt : -1;
+    }
+    if (tid == 0) sh.rescale = 0;
+    __syncthreads();
+    gather_tile(sh.src, ks, p.q);
+    cp_async_commit();
+    cp_async_wait<0>();
+    // generic-proxy writes (cp.async, stores, the rotated query) become visible to the tensor cores
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    tc05::fence_before();
+    __syncthreads();
+    tc05::fence_after();
+
+    // ------------------------------------------------------------ S^T = K q'^T
+    if (warp == 0) {
+      if (lane == 0 && !sh.timeout) {
+        constexpr uint32_t idesc = tc05::idesc_bf16(128, NH);
+#pragma unroll 1
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t sub = (kk & 3) * 32;
+          tc05::mma_bf16(tmem + kS0, tc05::sw128_desc(ks_u + (kk >> 2) * kKPanel + sub),
+                         tc05::sw128_desc(qs_u + (kk >> 2) * QPANEL + sub), idesc, kk > 0);
+        }
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk)
+          tc05::mma_bf16(tmem + kS0, tc05::sw128_desc(ks_u + 7 * kKPanel + kk * 32),
+                         tc05::sw128_desc(qs_u + 8 * QPANEL + kk * 32), idesc, 1u);
+        tc05::mma_commit(&sh.bar_s);
+        sh.s_issued = kt + 1;
+      }
+      __syncwarp();
+    }
+
+    // ------------------------------------------------------------ softmax of the tile
+    const bool ok = !sh.timeout && tc05::mbar_wait(&sh.bar_s, kt & 1);
+    if (!ok && lane == 0 && !sh.timeout) report_timeout_attn(&sh.timeout, p.dev_status);
+    tc05::fence_after();
+    const int f = sh.src.fmt[e];
+    const float rs = sh.src.rs[e];
+    const bool on = ok && f >= 0;
+    const float zs = p.scale * rs;
+    float z[HALF];
+    {
+      uint32_t v[HALF];
+      tc05::tmem_ld<HALF>(tmem + ((uint32_t)(32 * qw) << 16) + kS0 + (uint32_t)hb, v);
+      tc05::tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < HALF; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
+    }
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float m[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m[k] = z[8 * g + k];
+      group_reduce8<true>(m);
+      if ((lane & 3) == 0) sh.red[qw][hb + 8 * g + lh] = m[0];
+    }
+    __syncthreads();
+    if (qw == 0 && lane < HALF) {
+      // this tile's maximum; the reference moves when it is exceeded by more than kRowTau
+      const int h = hb + lane;
+      const float mt = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
+      const float mr = sh.mref[h];
+      float a = 1.f;
+      if (mr == -INFINITY) {
+        sh.mref[h] = mt;  // first finite maximum: the accumulated output and sum are still zero
+      } else if (mt > mr + kRowTau) {
+        a = __expf(mr - mt);
+        sh.mref[h] = mt;
+        sh.rescale = 1;
+      }
+      sh.alpha[h] = a;
+    }
+    tc05::fence_before();
+    __syncthreads();
+    tc05::fence_after();
+    if (sh.rescale && kt > 0) {
+      // O *= alpha per head: lane l of TMEM holds dim 32 qw + l of each 128-dim chunk; columns
+      // NO c + j are head j % NH (P_hi products, then P_lo products)
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * (warp >> 2) + cc;
+#pragma unroll 1
+        for (int part = 0; part < NO / 32; ++part) {
+          const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + NO * c + 32 * part;
+          uint32_t v[32];
+          tc05::tmem_ld32(ta, v);
+          tc05::tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * sh.alpha[(32 * part + k) % NH]);
+          tc05::tmem_st32(ta, v);
+        }
+      }
+      tc05::tmem_st_wait();
+    }
+    // P = exp(z - M) as P_hi | P_lo rows (entry e, MN-major for the second GEMM: P_hi in
+    // columns 0 .. NH-1, P_lo in NH .. 2NH-1 of a 128-byte row), the FP8 row scale on the
+    // weights; per-head sums of the unscaled P
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float pe[8];
+      uint32_t hi[4], lw[4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float M = sh.mref[hb + 8 * g + k];
+        pe[k] = on ? __expf(z[8 * g + k] - (M == -INFINITY ? 0.f : M)) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a0 = pe[2 * k] * rs, a1 = pe[2 * k + 1] * rs;
+        hi[k] = pack_bf16x2(a0, a1);
+        lw[k] = pack_bf16x2(a0 - bf16_lo(hi[k]), a1 - bf16_hi(hi[k]));
+      }
+      const int ci = hb / 8 + g;
+      *reinterpret_cast<uint4*>(ps + e * 128 + ((ci ^ (e & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(ps + e * 128 + (((NH / 8 + ci) ^ (e & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      group_reduce8<false>(pe);
+      if ((lane & 3) == 0) sh.red[qw][hb + 8 * g + lh] = pe[0];
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    tc05::fence_before();
+    __syncthreads();
+    tc05::fence_after();
+    if (qw == 0 && lane < HALF) {
+      const int h = hb + lane;
+      sh.lsum[h] = sh.lsum[h] * sh.alpha[h] + ((sh.red[0][h] + sh.red[1][h]) + (sh.red[2][h] + sh.red[3][h]));
+    }
+
+    // ------------------------------------------------------------ O^T += V^T [P_hi | P_lo]^T
+    if (warp == 0) {
+      if (lane == 0 && !sh.timeout) {
+        constexpr uint32_t idesc = tc05::idesc_bf16(128, NO) | (1u << 15) | (1u << 16);
+#pragma unroll 1
+        for (int i = 0; i < 4 * (kTileE / 16); ++i) {
+          const int c = i >> 3, kk = i & 7;
+          tc05::mma_bf16(tmem + NO * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel + kk * 2048, kKPanel, 1024),
+                         sw128_desc_lbo(ps_u + kk * 2048, kPBytes, 1024), idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc05::mma_commit(&sh.bar_o);
+        sh.o_issued = kt + 1;
+      }
+      __syncwarp();
+    }
+  }
+
+  // ---------------------------------------------------------------- output
+  __syncthreads();  // the last tile's running sums are final
+  const bool live = !sh.timeout && tc05::mbar_wait(&sh.bar_o, (n_tiles - 1) & 1);
+  if (!live && !sh.timeout && lane == 0) report_timeout_attn(&sh.timeout, p.dev_status);
+  tc05::fence_after();
+  if (tid < NH) {
+    // the sink joins the denominator: o = O e^{M - Mf} / (l e^{M - Mf} + e^{sink - Mf})
+    const float M = sh.mref[tid], sk = __ldg(p.sink + h0 + tid);
+    const float Mf = fmaxf(M, sk);
+    const float so = M == -INFINITY ? 0.f : __expf(M - Mf);
+    const float es = __expf(sk - Mf);
+    const float den = sh.lsum[tid] * so + es;
+    sh.alpha[tid] = so / den;
+    if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + h0 + tid] = es / den;
+  }
+  __syncthreads();
+  if (live) {
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * (warp >> 2) + cc;
+      const int d = 128 * c + 32 * qw + lane;
+      uint32_t v[32], v2[32];
+      const uint32_t ta = tmem + ((uint32_t)(32 * qw) << 16) + NO * c;
+      tc05::tmem_ld32(ta, v);
+      if (NH == 32) tc05::tmem_ld32(ta + 32, v2);
+      tc05::tmem_ld_wait();
+      float o[NH];
+#pragma unroll
+      for (int k = 0; k < NH; ++k)
+        o[k] = (NH == 32 ? __uint_as_float(v[k]) + __uint_as_float(v2[k])
+                         : __uint_as_float(v[k]) + __uint_as_float(v[k + NH])) * sh.alpha[k];
+      if (d >= kHeadDim - kRopeDim) {
+        // turned back by -position: pairs (448 + 2i, 449 + 2i) sit in adjacent lanes
+        const int i = (d - (kHeadDim - kRopeDim)) >> 1;
+        const float cn = sh.cs[i], sn = sh.cs[32 + i];
+        const bool even = (d & 1) == 0;
+#pragma unroll
+        for (int k = 0; k < NH; ++k) {
+          const float other = __shfl_xor_sync(0xffffffffu, o[k], 1);
+          o[k] = even ? o[k] * cn + other * sn : o[k] * cn - other * sn;
+        }
+      }
+      const size_t at = ((size_t)row * kHeads + h0) * kHeadDim + d;
+#pragma unroll
+      for (int k = 0; k < NH; ++k) {
+        if (p.out_bf16) static_cast<__nv_bfloat16*>(p.out)[at + (size_t)k * kHeadDim] = __float2bfloat16_rn(o[k]);
+        else static_cast<float*>(p.out)[at + (size_t)k * kHeadDim] = o[k];
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc05::fence_before();
+  __syncthreads();
+  if (sh.timeout && tid == 0) {
+    // let issued MMAs finish (bounded) before the tensor memory is freed
+    if (sh.s_issued > 0) tc05::mbar_wait(&sh.bar_s, (sh.s_issued - 1) & 1);
+    if (sh.o_issued > 0) tc05::mbar_wait(&sh.bar_o, (sh.o_issued - 1) & 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc05::fence_after();
+    tc05::tmem_dealloc(tmem, kCols);
+  }
+}
+
 // Merges the tiles of a row for one head: the log-sum-exp over the tiles plus the sink (in the
 // denominator only), the normalised sum of the tiles' outputs, and the inverse RoPE on dims
 // 448..511.  One warp per (row, head) item, lane l holding dims 4l + 128j (j = 0..3); a grid
@@ -659,12 +973,47 @@ __global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const Att
   }
 }
 
+// The row kernel runs its tiles one after another in one block, a chain per tile that the
+// tile kernel runs in parallel blocks: measured slower for every decode workload (B=32
+// 0.134-0.138 against 0.118 ms; tiny 54-57 against 34 us) and no faster for the prefill
+// chunk, whose partials it saves (2.53 ms either way), so it is chosen only through
+// CSA2_TUNE_ATTN_ROWS.
+bool use_row_kernel(const AttnParams& p, int n_split) {
+  (void)p;
+  (void)n_split;
+  return false;
+}
+int row_kernel_heads(const AttnParams& p) {
+  (void)p;
+  return 32;
+}
+
 }  // namespace
 
 int attn_smem_bytes() { return kAttnSmemBytes; }
 
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
+  const int rows_mode = tuning(CSA2_TUNE_ATTN_ROWS);
+  if (rows_mode >= 2 || (rows_mode == 0 && use_row_kernel(p, n_split))) {
+    // whole rows per block, no partials and no merge
+    const int nh = rows_mode == 3 ? 16 : rows_mode == 2 ? 32 : row_kernel_heads(p);
+    auto kern = nh == 16 ? attn_row_kernel<16> : attn_row_kernel<32>;
+    const int smem = nh == 16 ? row_smem_bytes<16>() : row_smem_bytes<32>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_rows, kHeads / nh);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+  }
   // Heads per block: all 64, or 32 / 16 where rows x tiles blocks would leave most SMs idle
   // (the tile chain then runs on half / a quarter of the heads, in parallel).
   const int sms = device_sm_count();

@@ -152,7 +152,7 @@ def test_tuning_overrides_are_range_checked(lib):
     st = lib.csa2_set_tuning
     st.restype = ctypes.c_int
     st.argtypes = [ctypes.c_int32, ctypes.c_int32]
-    assert st(-1, 0) == 1 and st(4, 0) == 1            # unknown knobs
+    assert st(-1, 0) == 1 and st(5, 0) == 1            # unknown knobs
     assert st(0, 65) == 1 and st(0, -1) == 1           # scan segments 0..64
     assert st(3, 9) == 1                               # projection K split 0..8
     assert st(0, 8) == 0 and st(0, 0) == 0             # set, and back to automatic

@@ -325,3 +325,44 @@ def test_prefill_index_scores_mxfp4(mode):
     else:
         bound = score_bound(inp, 0, rows)
         assert np.all(np.abs(got - ref)[fin] <= np.repeat(bound[:, None], got.shape[1], 1)[fin])
+
+
+# ------------------------------------------------------------------ attention kernels
+@pytest.mark.parametrize("kernel", [1, 2, 3])  # tiles + merge; rows with 32 heads; rows with 16 heads
+@pytest.mark.parametrize("lat_fmt,group,swa_fmt", [("bf16", 32, "bf16"), ("fp4", 32, "fp8")])
+def test_attention_kernels_agree_with_the_oracle(kernel, lat_fmt, group, swa_fmt):
+    """Both attention kernels (a block per (row, tile) with a merge kernel, and a block per
+    (row, head group) carrying the softmax across the row's tiles) against the oracle, on rows
+    where a later tile's logits exceed the first (window) tile's by far more than the row
+    kernel's rescale threshold, so its running reference moves and the accumulated output is
+    rescaled; -1 pads and a short row included."""
+    _cuda()
+    inp = small("batched_decode", seed=31, B=3, N=4000, lat_fmt=lat_fmt, lat_group=group, swa_fmt=swa_fmt)
+    set_rows(inp, [4000, 3000, 100])
+    rng = np.random.default_rng(9)
+    K = 512
+    idx = np.full((3, K), -1, np.int64)
+    for r, nv in enumerate([4000, 3000, 100]):
+        sel = np.sort(rng.choice(nv, min(K, nv) - 3, replace=False))
+        idx[r, :len(sel)] = sel
+    if lat_fmt == "bf16":
+        # records aligned with some heads' query (rotary dims left out): logits near 20 against ~0.1
+        q = O.bf16_to_f64(inp["layers"][0]["q"][0])  # row 0, [64, 512]
+        for j, h in enumerate((0, 17, 40)):
+            v = 23.0 * q[h] / np.linalg.norm(q[h])  # logit ~ 23 * 0.875 ~ 20 for head h
+            v[448:] = 0.0
+            inp["cache"]["lat"][0, idx[0, 100 + j]] = synth.bf16_bits(torch.from_numpy(v.astype(np.float32)))
+    dv = synth.to_device(inp)
+    c, lay, rw, p = dv["cache"], dv["layers"][0], dv["rows"], dv["params"]
+    S.set_tuning(S.TUNE_ATTN_ROWS, kernel)
+    try:
+        out, sm = S.sparse_attn(lay["q"], rw["q_pos"], rw["seq_of_row"], c["lat"], c["lat_scales"],
+                                torch.from_numpy(idx.astype(np.int32)).cuda(), lay["swa"], lay["swa_scale"],
+                                rw["swa_pos0"], p["W"], lay["sink"], p["theta"], p["softmax_scale"])
+        torch.cuda.synchronize()
+    finally:
+        S.reset_tuning()
+    o_ref, sm_ref = O.sparse_attn_rows(inp, 0, idx)
+    err = rel_err(out.cpu().numpy(), o_ref)
+    assert err <= out_tol(inp["params"]), err
+    assert np.max(np.abs(sm.cpu().numpy() - sm_ref)) < 1e-4
