@@ -310,6 +310,107 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a);
 csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Splitting one sequence's records across devices.  A long context's records can be cut into
+ * contiguous ranges, one per device: every record's score needs only that record's key, and
+ * the row's top-K is a subset of the union of every range's own top-K, so each device
+ *   1. scores its range (csa2_index_scores with the range's keys, n_records = the range's
+ *      length and n_visible = the row's visible records inside the range),
+ *   2. keeps the range's exact top-K as a candidate list (csa2_shard_candidates),
+ * the lists of all ranges are gathered (all ranges' lists, in range order, on every device),
+ *   3. every device merges them into the row's top-K (csa2_merge_candidates: the same answer
+ *      on every device, bit for bit),
+ *   4. attends over the selected records of its own range (its indices, the others -1) and,
+ *      on the device that holds them, the window rows, into partials
+ *      (csa2_sparse_attn_partial: per 128-entry tile and head the maximum logit, the sum of
+ *      exp(logit - maximum) and the output relative to it),
+ * the partials are gathered, and
+ *   5. csa2_attn_merge combines them: log-sum-exp over every part's tiles, the sink in the
+ *      denominator, normalisation and the inverse rotation ("DeepSeek V4 Inside", eq. (27)).
+ * The result equals csa2_fused_decode's FULL layer on the whole sequence (indices bit-exact).
+ * On one device the ranges simply run one after another.
+ * ------------------------------------------------------------------------------------ */
+typedef struct csa2_shard_args {
+  const float* scores;        /* [n_rows, L] the range's indexer scores */
+  const int32_t* n_valid;     /* [n_rows] visible records of the range (its columns 0 .. n_valid-1) */
+  int32_t n_rows;
+  int64_t L;                  /* records in the range, 1 .. 2^24 */
+  int32_t K;                  /* 1 .. CSA2_MAX_TOPK */
+  int64_t first_record;       /* record position of column 0 (>= 0) */
+  float* out_scores;          /* out [n_rows, K] the selected entries' scores in ascending position
+                                 order, -inf after them */
+  int32_t* out_pos;           /* out [n_rows, K] their record positions (first_record + column), -1
+                                 after them */
+  int32_t* out_cnt;           /* out [n_rows] entries listed: min(K, n_valid) */
+  void* workspace;            /* csa2_shard_candidates_workspace_size bytes */
+  size_t workspace_bytes;
+} csa2_shard_args;
+
+size_t csa2_shard_candidates_workspace_size(const csa2_shard_args* a);
+csa2_status csa2_shard_candidates(const csa2_shard_args* a, void* stream);
+
+/* The row's top-K of n_lists candidate lists (the K best by score descending, position
+ * ascending, of every list's first cnt entries), returned as the ascending set of positions,
+ * -1 padded.  The lists come as gathered, list-major (list l = range l's csa2_shard_candidates
+ * output), in ascending position ranges (each list ascending). */
+typedef struct csa2_merge_args {
+  const float* scores;        /* [n_lists, n_rows, K_in] */
+  const int32_t* pos;         /* [n_lists, n_rows, K_in] */
+  const int32_t* cnt;         /* [n_lists, n_rows] entries of each list, 0 .. K_in */
+  int32_t n_rows;
+  int32_t n_lists;            /* 1 .. 64 */
+  int32_t K_in;               /* 1 .. CSA2_MAX_TOPK */
+  int32_t K;                  /* 1 .. CSA2_MAX_TOPK */
+  int32_t* idx;               /* out [n_rows, K] */
+  void* workspace;            /* csa2_merge_candidates_workspace_size bytes, 16-byte aligned */
+  size_t workspace_bytes;
+} csa2_merge_args;
+
+size_t csa2_merge_candidates_workspace_size(const csa2_merge_args* a);
+csa2_status csa2_merge_candidates(const csa2_merge_args* a, void* stream);
+
+/* Attention partials of one device's share: csa2_sparse_attn's arguments (attn.out, sink_mass,
+ * sink and workspace are not used) with attn.idx holding the selected records of this
+ * device's range (-1 elsewhere) and attn.window the window rows it holds (0 for none).
+ * Writes, per row, 128-entry tile t (entries K + window in tiles, csa2_attn_partial_tiles) and
+ * head h: part_ml[row, t, h] = (maximum logit m, sum of exp(logit - m)) and
+ * part_o[row, t, h, :] = sum of exp(logit - m) * row, before the inverse rotation. */
+typedef struct csa2_partial_args {
+  csa2_attn_args attn;
+  float* part_o;              /* out [n_rows, tiles, 64, 512], 16-byte aligned */
+  float* part_ml;             /* out [n_rows, tiles, 64, 2] */
+  int64_t range_first;        /* with range_count > 0: attn.idx holds global positions (the merged
+                                 selection); those outside [range_first, range_first + range_count)
+                                 are skipped and the others read attn.latents at position -
+                                 range_first (this device's records only); range_count == 0: attn.idx
+                                 indexes attn.latents directly */
+  int64_t range_count;
+  int32_t skip_window;        /* 1: the window entries are masked (another device attends to them);
+                                 the tiles stay csa2_attn_partial_tiles(K, window) */
+} csa2_partial_args;
+
+int32_t csa2_attn_partial_tiles(int32_t K, int32_t window);
+csa2_status csa2_sparse_attn_partial(const csa2_partial_args* a, void* stream);
+
+/* The output of n_parts gathered partials (part k = one device's part_o / part_ml, stacked):
+ * o_h = sum over every tile of exp(m - M) o_tile / (sum exp(m - M) l_tile + exp(sink[h] - M)),
+ * then turned back by -q_pos on dims 448..511; sink_mass as csa2_sparse_attn's. */
+typedef struct csa2_attn_merge_args {
+  const float* part_o;        /* [n_parts, n_rows, part_tiles, 64, 512] */
+  const float* part_ml;       /* [n_parts, n_rows, part_tiles, 64, 2] */
+  int32_t n_parts;
+  int32_t part_tiles;         /* n_parts * part_tiles <= 32 */
+  int32_t n_rows;
+  const int64_t* q_pos;       /* [n_rows] */
+  const float* sink;          /* [64] */
+  float rope_theta;
+  void* out;                  /* out [n_rows, 64, 512] fp32, or bf16 with out_bf16 */
+  int32_t out_bf16;
+  float* sink_mass;           /* out [n_rows, 64] or NULL */
+} csa2_attn_merge_args;
+
+csa2_status csa2_attn_merge(const csa2_attn_merge_args* a, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Cache writer: appends records to a main-KV (latent) cache or a sliding-window cache in its
  * storage format.  Each record's rotary coordinates (dims 448..511, pairs (448+2i, 449+2i),
  * frequencies theta^(-2i/64)) are turned by its position first, since the cache holds

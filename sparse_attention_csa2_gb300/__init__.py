@@ -71,6 +71,28 @@ class DecodeArgs(C.Structure):
                 ("stage_events", _vp * 4)]
 
 
+class ShardArgs(C.Structure):
+    _fields_ = [("scores", _vp), ("n_valid", _vp), ("n_rows", _i32), ("L", _i64), ("K", _i32),
+                ("first_record", _i64), ("out_scores", _vp), ("out_pos", _vp), ("out_cnt", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class MergeArgs(C.Structure):
+    _fields_ = [("scores", _vp), ("pos", _vp), ("cnt", _vp), ("n_rows", _i32), ("n_lists", _i32),
+                ("K_in", _i32), ("K", _i32), ("idx", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class PartialArgs(C.Structure):
+    _fields_ = [("attn", AttnArgs), ("part_o", _vp), ("part_ml", _vp), ("range_first", _i64),
+                ("range_count", _i64), ("skip_window", _i32)]
+
+
+class AttnMergeArgs(C.Structure):
+    _fields_ = [("part_o", _vp), ("part_ml", _vp), ("n_parts", _i32), ("part_tiles", _i32), ("n_rows", _i32),
+                ("q_pos", _vp), ("sink", _vp), ("rope_theta", _f32), ("out", _vp), ("out_bf16", _i32),
+                ("sink_mass", _vp)]
+
+
 class WriteArgs(C.Structure):
     _fields_ = [("n_rows", _i64), ("x", _vp), ("x_f32", _i32), ("pos", _vp), ("rope_theta", _f32),
                 ("dst_row", _vp), ("cache_rows", _i64), ("out_dtype", _i32), ("codes", _vp), ("scales", _vp),
@@ -132,6 +154,13 @@ _expand = _sig("csa2_expand_mxfp4", [C.POINTER(ExpandArgs), _vp], C.c_int)
 _version = _sig("csa2_version", [], C.c_int32)
 _read_status = _sig("csa2_read_device_status", [_vp, C.POINTER(C.c_int32), _vp], C.c_int)
 _set_tuning = _sig("csa2_set_tuning", [C.c_int32, C.c_int32], C.c_int)
+_shard_ws = _sig("csa2_shard_candidates_workspace_size", [C.POINTER(ShardArgs)], _sz)
+_shard = _sig("csa2_shard_candidates", [C.POINTER(ShardArgs), _vp], C.c_int)
+_merge_ws = _sig("csa2_merge_candidates_workspace_size", [C.POINTER(MergeArgs)], _sz)
+_merge = _sig("csa2_merge_candidates", [C.POINTER(MergeArgs), _vp], C.c_int)
+_partial_tiles = _sig("csa2_attn_partial_tiles", [C.c_int32, C.c_int32], C.c_int32)
+_partial = _sig("csa2_sparse_attn_partial", [C.POINTER(PartialArgs), _vp], C.c_int)
+_attn_merge = _sig("csa2_attn_merge", [C.POINTER(AttnMergeArgs), _vp], C.c_int)
 _selftest_wait = _sig("csa2_selftest_wait_timeout", [_vp, C.c_int32, _vp], C.c_int)
 
 # launch-heuristic overrides (csa2_tuning)
@@ -298,7 +327,7 @@ def _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, K, swa, swa_scale,
     a.swa_rows, a.swa_pos0, a.window = swa.shape[1], _ptr(swa_pos0), window
     a.sink, a.rope_theta, a.softmax_scale = _ptr(sink), float(theta), float(softmax_scale)
     a.out, a.sink_mass = _ptr(out), _ptr(sink_mass)
-    a.out_bf16 = 1 if out.dtype == torch.bfloat16 else 0
+    a.out_bf16 = 1 if (out is not None and out.dtype == torch.bfloat16) else 0
     return a
 
 
@@ -317,6 +346,73 @@ def sparse_attn(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, s
     ws, nb = _ws(int(_attn_ws(C.byref(a))), dev)
     a.workspace, a.workspace_bytes = _ptr(ws), nb
     _check(_sparse_attn(C.byref(a), _stream()), "csa2_sparse_attn")
+    return out, sm
+
+
+# ------------------------------------------------------------------ record-range split
+def shard_candidates(scores, n_valid, K: int, first_record: int):
+    """A record range's exact top-K as a candidate list (csa2_shard_candidates): scores [rows,
+    K] (ascending positions, -inf pads), positions [rows, K] (-1 pads) and counts [rows]."""
+    dev = _dev(scores)
+    rows, L = scores.shape
+    out_s = torch.empty((rows, K), dtype=torch.float32, device=dev)
+    out_p = torch.empty((rows, K), dtype=torch.int32, device=dev)
+    out_c = torch.empty((rows,), dtype=torch.int32, device=dev)
+    a = ShardArgs(_ptr(scores), _ptr(n_valid), rows, L, K, int(first_record), _ptr(out_s), _ptr(out_p), _ptr(out_c),
+                  None, 0)
+    ws, nb = _ws(int(_shard_ws(C.byref(a))), dev)
+    a.workspace, a.workspace_bytes = _ptr(ws), nb
+    _check(_shard(C.byref(a), _stream()), "csa2_shard_candidates")
+    return out_s, out_p, out_c
+
+
+def merge_candidates(scores, pos, cnt, K: int):
+    """The rows' top-K of gathered candidate lists scores / pos [lists, rows, K_in] with counts
+    [lists, rows] (csa2_merge_candidates): the ascending set of positions [rows, K]."""
+    dev = _dev(scores)
+    n_lists, rows, k_in = scores.shape
+    idx = torch.empty((rows, K), dtype=torch.int32, device=dev)
+    a = MergeArgs(_ptr(scores), _ptr(pos), _ptr(cnt), rows, n_lists, k_in, K, _ptr(idx), None, 0)
+    ws, nb = _ws(int(_merge_ws(C.byref(a))), dev)
+    a.workspace, a.workspace_bytes = _ptr(ws), nb
+    _check(_merge(C.byref(a), _stream()), "csa2_merge_candidates")
+    return idx
+
+
+def attn_partial_tiles(K: int, window: int) -> int:
+    return int(_partial_tiles(int(K), int(window)))
+
+
+def sparse_attn_partial(q, q_pos, seq_of_row, latents, lat_scale, idx, swa, swa_scale, swa_pos0, window: int,
+                        theta: float = 1e4, softmax_scale: float = HEAD_DIM ** -0.5, range_first: int = 0,
+                        range_count: int = 0, skip_window: bool = False):
+    """Attention partials of one range's share (csa2_sparse_attn_partial): part_o [rows, tiles,
+    64, 512] and part_ml [rows, tiles, 64, 2].  With range_count > 0, idx holds global positions
+    and latents only the records [range_first, range_first + range_count)."""
+    dev = _dev(q)
+    rows = q.shape[0]
+    tiles = attn_partial_tiles(idx.shape[1], window)
+    part_o = torch.empty((rows, tiles, HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+    part_ml = torch.empty((rows, tiles, HEADS, 2), dtype=torch.float32, device=dev)
+    a = PartialArgs()
+    a.attn = _attn_args(q, q_pos, seq_of_row, latents, lat_scale, idx, idx.shape[1], swa, swa_scale, swa_pos0, window,
+                        None, theta, softmax_scale, None, None)
+    a.part_o, a.part_ml = _ptr(part_o), _ptr(part_ml)
+    a.range_first, a.range_count, a.skip_window = int(range_first), int(range_count), 1 if skip_window else 0
+    _check(_partial(C.byref(a), _stream()), "csa2_sparse_attn_partial")
+    return part_o, part_ml
+
+
+def attn_merge(part_o, part_ml, q_pos, sink, theta: float = 1e4, out_dtype=torch.float32):
+    """The output of stacked partials part_o [parts, rows, tiles, 64, 512] / part_ml [parts,
+    rows, tiles, 64, 2] (csa2_attn_merge): out [rows, 64, 512] and sink mass [rows, 64]."""
+    dev = _dev(part_o)
+    n_parts, rows, tiles = part_o.shape[:3]
+    out = torch.empty((rows, HEADS, HEAD_DIM), dtype=out_dtype, device=dev)
+    sm = torch.empty((rows, HEADS), dtype=torch.float32, device=dev)
+    a = AttnMergeArgs(_ptr(part_o), _ptr(part_ml), n_parts, tiles, rows, _ptr(q_pos), _ptr(sink), float(theta),
+                      _ptr(out), 1 if out_dtype == torch.bfloat16 else 0, _ptr(sm))
+    _check(_attn_merge(C.byref(a), _stream()), "csa2_attn_merge")
     return out, sm
 
 

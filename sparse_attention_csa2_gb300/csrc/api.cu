@@ -195,15 +195,17 @@ ScanParams scan_params(const csa2_index_args* a) {
 }
 
 // ------------------------------------------------------------------ attention validation
-csa2_status check_attn(const csa2_attn_args* a, bool need_idx) {
+csa2_status check_attn(const csa2_attn_args* a, bool need_idx, bool need_out = true) {
   if (!a) return CSA2_EINVAL;
   if (a->n_rows < 0 || a->n_seq < 1 || a->n_records < 1 || a->n_records > (1LL << 31) - 1) return CSA2_EINVAL;
   if (a->n_rows == 0) return CSA2_OK;
-  if (!a->q || !a->q_pos || !a->seq_of_row || !a->sink || !a->out || !a->swa_pos0) return CSA2_EINVAL;
+  if (!a->q || !a->q_pos || !a->seq_of_row || !a->swa_pos0) return CSA2_EINVAL;
+  if (need_out && (!a->sink || !a->out)) return CSA2_EINVAL;
   if (a->K < 0 || a->K > CSA2_MAX_TOPK || a->window < 0 || a->window > 1024) return CSA2_EUNSUPPORTED;
   if (a->K + a->window < 1) return CSA2_EINVAL;
   if (a->K > 0 && (!a->latents || (need_idx && !a->idx))) return CSA2_EINVAL;
-  if (!aligned(a->q, 16) || !aligned(a->out, 16) || (a->latents && !aligned(a->latents, 16))) return CSA2_EINVAL;
+  if (!aligned(a->q, 16) || (need_out && !aligned(a->out, 16)) || (a->latents && !aligned(a->latents, 16)))
+    return CSA2_EINVAL;
   if (a->lat_dtype == CSA2_FP4_E2M1_G32 || a->lat_dtype == CSA2_FP4_E2M1_G16) {
     if (a->K > 0 && !a->lat_scale) return CSA2_EINVAL;
   } else if (a->lat_dtype != CSA2_BF16) {
@@ -870,6 +872,117 @@ csa2_status csa2_linear(const csa2_linear_args* a, void* stream) {
   p.out_ld = a->out_features;
   p.dev_status = a->dev_status;
   return cuda_status(launch_proj(tmA, tmB, p, 1, static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------- record-range split
+size_t csa2_shard_candidates_workspace_size(const csa2_shard_args* a) {
+  if (!a || a->n_rows <= 0 || a->K < 1) return 0;
+  csa2_topk_args t{};
+  t.n_rows = a->n_rows;
+  t.L = a->L;
+  t.K = a->K;
+  return csa2_topk_workspace_size(&t);
+}
+
+csa2_status csa2_shard_candidates(const csa2_shard_args* a, void* stream) {
+  if (!a || a->n_rows < 0) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->scores || !a->n_valid || !a->out_scores || !a->out_pos || !a->out_cnt || a->first_record < 0 ||
+      a->L < 1 || a->L > (1LL << 24) || a->first_record + a->L > (1LL << 31) - 1)
+    return CSA2_EINVAL;
+  if (a->K < 1 || a->K > CSA2_MAX_TOPK) return CSA2_EUNSUPPORTED;
+  // the range's exact top-K columns (into out_pos), then their scores and record positions
+  csa2_topk_args t{};
+  t.scores = a->scores;
+  t.n_valid = a->n_valid;
+  t.n_rows = a->n_rows;
+  t.L = a->L;
+  t.K = a->K;
+  t.idx = a->out_pos;
+  t.workspace = a->workspace;
+  t.workspace_bytes = a->workspace_bytes;
+  const csa2_status st = csa2_topk(&t, stream);
+  if (st != CSA2_OK) return st;
+  return cuda_status(launch_shard_list(a->n_rows, a->K, a->out_pos, a->scores, a->L, a->first_record, a->out_scores,
+                                       a->out_pos, a->out_cnt, static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa2_merge_candidates_workspace_size(const csa2_merge_args* a) {
+  if (!a || a->n_rows <= 0 || a->n_lists < 1 || a->K_in < 1) return 0;
+  return 2 * align_up((size_t)a->n_rows * a->n_lists * a->K_in * 4) + align_up((size_t)a->n_rows * a->n_lists * 4);
+}
+
+csa2_status csa2_merge_candidates(const csa2_merge_args* a, void* stream) {
+  if (!a || a->n_rows < 0) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->scores || !a->pos || !a->cnt || !a->idx || a->n_lists < 1 || a->K_in < 1) return CSA2_EINVAL;
+  if (a->n_lists > 64 || a->K_in > CSA2_MAX_TOPK || a->K < 1 || a->K > CSA2_MAX_TOPK) return CSA2_EUNSUPPORTED;
+  const size_t need = csa2_merge_candidates_workspace_size(a);
+  if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 16)) return CSA2_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carve c{static_cast<uint8_t*>(a->workspace)};
+  uint32_t* keys = c.take<uint32_t>((size_t)a->n_rows * a->n_lists * a->K_in);
+  int32_t* pos = c.take<int32_t>((size_t)a->n_rows * a->n_lists * a->K_in);
+  int32_t* cnt = c.take<int32_t>((size_t)a->n_rows * a->n_lists);
+  if (launch_lists_to_rows(a->n_rows, a->n_lists, a->K_in, a->scores, a->pos, a->cnt, keys, pos, cnt, s) != cudaSuccess)
+    return CSA2_ECUDA;
+  FeedParams m{};
+  m.n_rows = a->n_rows;
+  m.K = a->K;
+  m.in_keys = keys;
+  m.in_pos = pos;
+  m.in_cnt = cnt;
+  m.in_thr = nullptr;
+  m.in_seg = a->n_lists;
+  m.in_K = a->K_in;
+  m.idx = a->idx;
+  return cuda_status(launch_lists_merge(m, s));
+}
+
+int32_t csa2_attn_partial_tiles(int32_t K, int32_t window) {
+  if (K < 0 || window < 0 || K + window < 1) return 0;
+  return (K + window + 127) / 128;
+}
+
+csa2_status csa2_sparse_attn_partial(const csa2_partial_args* a, void* stream) {
+  if (!a) return CSA2_EINVAL;
+  const csa2_status st = check_attn(&a->attn, true, false);
+  if (st != CSA2_OK || a->attn.n_rows == 0) return st;
+  if (!a->part_o || !a->part_ml || !aligned(a->part_o, 16) || !aligned(a->part_ml, 8)) return CSA2_EINVAL;
+  if (a->range_count < 0 || a->range_first < 0 || (a->range_count > 0 && a->range_count > a->attn.n_records))
+    return CSA2_EINVAL;
+  AttnParams p = attn_params(&a->attn, a->attn.idx);
+  p.part_o = a->part_o;
+  p.part_ml = a->part_ml;
+  p.range_first = a->range_first;
+  p.range_count = a->range_count;
+  p.skip_window = a->skip_window != 0;
+  return cuda_status(launch_attn_tiles(p, csa2_attn_partial_tiles(a->attn.K, a->attn.window),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+csa2_status csa2_attn_merge(const csa2_attn_merge_args* a, void* stream) {
+  if (!a || a->n_rows < 0) return CSA2_EINVAL;
+  if (a->n_rows == 0) return CSA2_OK;
+  if (!a->part_o || !a->part_ml || !a->q_pos || !a->sink || !a->out || a->n_parts < 1 || a->part_tiles < 1 ||
+      !aligned(a->part_o, 16) || !aligned(a->part_ml, 8) || !aligned(a->out, 16) || !(a->rope_theta > 0.f))
+    return CSA2_EINVAL;
+  if ((long long)a->n_parts * a->part_tiles > 32) return CSA2_EUNSUPPORTED;
+  AttnParams p{};
+  p.n_rows = a->n_rows;
+  p.q_pos = a->q_pos;
+  p.sink = a->sink;
+  for (int i = 0; i < CSA2_ROPE_DIM / 2; ++i)
+    p.inv_freq[i] = std::pow((double)a->rope_theta, -2.0 * i / (double)CSA2_ROPE_DIM);
+  p.part_o = const_cast<float*>(a->part_o);
+  p.part_ml = const_cast<float*>(a->part_ml);
+  p.part_tiles = a->part_tiles;
+  p.part_stride_o = (long long)a->n_rows * a->part_tiles * CSA2_HEADS * CSA2_HEAD_DIM;
+  p.part_stride_ml = (long long)a->n_rows * a->part_tiles * CSA2_HEADS * 2;
+  p.out = a->out;
+  p.out_bf16 = a->out_bf16 != 0;
+  p.sink_mass = a->sink_mass;
+  return cuda_status(launch_attn_merge(p, a->n_parts * a->part_tiles, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {

@@ -132,7 +132,10 @@ __device__ __forceinline__ EntrySrc entry_source(const AttnParams& p, int row, i
                                                  long long pos0, int e) {
   EntrySrc s{nullptr, nullptr, 1.f, CSA2_BF16, false};
   if (e < p.K) {
-    const int rec = __ldg(p.idx + (size_t)row * p.K + e);
+    int rec = __ldg(p.idx + (size_t)row * p.K + e);
+    if (p.range_count > 0 && rec >= 0) {  // another device's record, or this device's
+      rec = (rec < p.range_first || rec >= p.range_first + p.range_count) ? -1 : (int)(rec - p.range_first);
+    }
     if (rec < -1 || rec >= p.N) {
       if (p.dev_status != nullptr) atomicExch(p.dev_status, (int)CSA2_EDEVICE_INDEX);
     } else if (rec >= 0) {
@@ -147,7 +150,7 @@ __device__ __forceinline__ EntrySrc entry_source(const AttnParams& p, int row, i
         s.sptr = p.lat_scale + r * (kHeadDim / g);
       }
     }
-  } else if (e < p.K + p.window) {
+  } else if (e < p.K + p.window && !p.skip_window) {
     const long long pos = lo + (e - p.K);
     if (pos <= qp && pos - pos0 < p.swa_rows) {
       s.valid = true;
@@ -886,7 +889,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_row_kernel(const AttnPar
 // once).  A warp issues the loads of all of an item's tile partials (up to kCombPre tiles at
 // once) and its tile statistics together, then forms the factors; the rotary cos / sin of its
 // row come from one lane per pair by shuffles.
-constexpr int kMaxTiles = 16;  // K + window <= 2048 entries
 constexpr int kCombWarps = 16;
 constexpr int kCombPre = 6;    // tiles whose partials a lane holds at once
 __global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const AttnParams p, int n_tiles) {
@@ -897,19 +899,24 @@ __global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const Att
 #pragma unroll 1
   for (int item = blockIdx.x * kCombWarps + (threadIdx.x >> 5); item < n_items; item += gridDim.x * kCombWarps) {
     const int row = item / kHeads, h = item % kHeads;
-    const float* base = p.part_o + ((size_t)row * n_tiles * kHeads + h) * kHeadDim + 4 * lane;
-    const size_t tile_stride = (size_t)kHeads * kHeadDim;
+    // tile t of the row: part t / T, tile t % T of that part (one part: T = n_tiles)
+    const int T = p.part_tiles > 0 ? p.part_tiles : n_tiles;
+    auto tile_o = [&](int t) -> const float* {
+      return p.part_o + (size_t)(t / T) * p.part_stride_o + (((size_t)row * T + t % T) * kHeads + h) * kHeadDim +
+             4 * lane;
+    };
     float4 v[kCombPre][4];
 #pragma unroll
     for (int t = 0; t < kCombPre; ++t)
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        v[t][j] = t < n_tiles ? __ldcg(reinterpret_cast<const float4*>(base + t * tile_stride + 128 * j))
+        v[t][j] = t < n_tiles ? __ldcg(reinterpret_cast<const float4*>(tile_o(t) + 128 * j))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
     // this lane's tile statistics (lane t: tile t) and the row's rotary pair `lane`
     float m = -INFINITY, l = 0.f;
     if (lane < n_tiles) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + ((size_t)row * n_tiles + lane) * kHeads + h);
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (size_t)(lane / T) * p.part_stride_ml) +
+                               ((size_t)row * T + lane % T) * kHeads + h);
       m = ml.x;
       l = ml.y;
     }
@@ -940,7 +947,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const Att
       const float ft = __shfl_sync(0xffffffffu, f, t);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(base + t * tile_stride + 128 * j));
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(tile_o(t) + 128 * j));
         acc[j].x = fmaf(ft, x.x, acc[j].x);
         acc[j].y = fmaf(ft, x.y, acc[j].y);
         acc[j].z = fmaf(ft, x.z, acc[j].z);
@@ -1014,6 +1021,15 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
   }
+  const cudaError_t e = launch_attn_tiles(p, n_split, stream);
+  if (e != cudaSuccess) return e;
+  return launch_attn_merge(p, n_split, stream);
+}
+
+// Both kernels may start before their predecessor in the stream has finished (programmatic
+// dependent launch); each waits for it where it reads its results.
+cudaError_t launch_attn_tiles(const AttnParams& p, int n_split, cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
   // Heads per block: all 64, or 32 / 16 where rows x tiles blocks would leave most SMs idle
   // (the tile chain then runs on half / a quarter of the heads, in parallel).
   const int sms = device_sm_count();
@@ -1022,8 +1038,6 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   auto kern = nh == 16 ? attn_tc05_kernel<16> : nh == 32 ? attn_tc05_kernel<32> : attn_tc05_kernel<64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
   if (e != cudaSuccess) return e;
-  // Both kernels may start before their predecessor in the stream has finished (programmatic
-  // dependent launch); each waits for it where it reads its results.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1034,14 +1048,24 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t st
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, p);
-  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_attn_merge(const AttnParams& p, int n_tiles, cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  if (n_tiles < 1 || n_tiles > 32) return cudaErrorInvalidValue;  // one lane per tile's statistics
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
   const int items = p.n_rows * kHeads;
-  const int blocks = std::min(device_sm_count(), (items + kCombWarps - 1) / kCombWarps);
-  cfg.gridDim = dim3(blocks);
+  cfg.gridDim = dim3(std::min(device_sm_count(), (items + kCombWarps - 1) / kCombWarps));
   cfg.blockDim = dim3(kCombWarps * 32);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, n_split);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, n_tiles);
 }
 
 }  // namespace csa2

@@ -132,6 +132,18 @@ struct AttnParams {
   double inv_freq[32];        // theta^(-2i/64), i = 0..31 (computed on the host in double)
   float* part_o;              // [n_rows, n_split, 64, 512]
   float* part_ml;             // [n_rows, n_split, 64, 2]
+  // a device's share of a record-range split: idx holds global positions; those outside
+  // [range_first, range_first + range_count) are skipped, the others index the latents at
+  // position - range_first (range_count == 0: no range); skip_window masks the window entries
+  long long range_first;
+  long long range_count;
+  int skip_window;
+  // merge of partials from several parts (record ranges): part k's tiles of row r sit at
+  // part_o + k * part_stride_o + (r * part_tiles + t) * 64 * 512 (part_ml likewise, 64 * 2
+  // per tile); part_tiles == 0: one part of n_split tiles (the layout above)
+  int part_tiles;
+  long long part_stride_o;
+  long long part_stride_ml;
   void* out;                  // fp32, or bf16 when out_bf16
   int out_bf16;
   float* sink_mass;
@@ -194,5 +206,20 @@ cudaError_t launch_proj(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pr
 
 int attn_smem_bytes();
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream);
+// The tile kernel alone (partials of n_split tiles per row) and the merge alone (n_tiles
+// partials per row in the layout p describes, sink, normalisation, inverse RoPE).
+cudaError_t launch_attn_tiles(const AttnParams& p, int n_split, cudaStream_t stream);
+cudaError_t launch_attn_merge(const AttnParams& p, int n_tiles, cudaStream_t stream);
+// Candidate lists of a record range: from the selected columns idx [n_rows, K] (-1 padded) of
+// scores [n_rows, stride], writes scores and positions (offset + column) of the selected
+// entries, -inf / -1 padded, and their count per row.
+cudaError_t launch_shard_list(int n_rows, int K, const int32_t* idx, const float* scores, long long stride,
+                              long long offset, float* out_scores, int32_t* out_pos, int32_t* out_cnt,
+                              cudaStream_t stream);
+// Gathered candidate lists (list-major scores / positions [n_lists, n_rows, k_in], counts
+// [n_lists, n_rows]) to the list merge's row-major keys, positions and counts.
+cudaError_t launch_lists_to_rows(int n_rows, int n_lists, int k_in, const float* scores, const int32_t* pos,
+                                 const int32_t* cnt, uint32_t* keys, int32_t* pos_out, int32_t* cnt_out,
+                                 cudaStream_t stream);
 
 }  // namespace csa2

@@ -244,7 +244,63 @@ size_t merge_smem_bytes(int seg_per_cta, int Kin, int K) {
          (size_t)std::max(ArrSel<kMergeWarps>::list_words(cap), kHistBins) * 4;
 }
 
+// A record range's candidate list: the selected columns idx[row] (ascending, -1 padded) to
+// their scores and record positions (offset + column); one warp per row.
+__global__ void shard_list_kernel(int n_rows, int K, const int32_t* idx, const float* scores, long long stride,
+                                  long long offset, float* out_scores, int32_t* out_pos, int32_t* out_cnt) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  int n = 0;
+#pragma unroll 1
+  for (int i = lane; i < K; i += 32) {
+    const int32_t j = idx[(size_t)row * K + i];
+    const bool ok = j >= 0;
+    out_scores[(size_t)row * K + i] = ok ? scores[(size_t)row * stride + j] : -INFINITY;
+    out_pos[(size_t)row * K + i] = ok ? (int32_t)(offset + j) : -1;
+    n += ok;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if (lane == 0) out_cnt[row] = n;
+}
+
+// Gathered candidate lists, list-major [n_lists, n_rows, k_in] (and counts [n_lists, n_rows]),
+// to the list merge's row-major order: keys (order-preserving images of the scores), positions
+// and counts.
+__global__ void lists_to_rows_kernel(int n_rows, int n_lists, int k_in, const float* scores, const int32_t* pos,
+                                     const int32_t* cnt, uint32_t* keys, int32_t* pos_out, int32_t* cnt_out) {
+  const long long n = (long long)n_rows * n_lists * k_in;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(i % k_in);
+    const long long lr = i / k_in;
+    const int r = (int)(lr % n_rows), l = (int)(lr / n_rows);  // source: list l, row r
+    const size_t o = ((size_t)r * n_lists + l) * k_in + k;
+    keys[o] = score_key(scores[i]);
+    pos_out[o] = pos[i];
+    if (k == 0) cnt_out[(size_t)r * n_lists + l] = cnt[lr];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_shard_list(int n_rows, int K, const int32_t* idx, const float* scores, long long stride,
+                              long long offset, float* out_scores, int32_t* out_pos, int32_t* out_cnt,
+                              cudaStream_t stream) {
+  if (n_rows == 0) return cudaSuccess;
+  shard_list_kernel<<<(n_rows + 7) / 8, 256, 0, stream>>>(n_rows, K, idx, scores, stride, offset, out_scores, out_pos,
+                                                          out_cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lists_to_rows(int n_rows, int n_lists, int k_in, const float* scores, const int32_t* pos,
+                                 const int32_t* cnt, uint32_t* keys, int32_t* pos_out, int32_t* cnt_out,
+                                 cudaStream_t stream) {
+  const long long n = (long long)n_rows * n_lists * k_in;
+  if (n == 0) return cudaSuccess;
+  const long long blocks = std::min<long long>((n + 255) / 256, 4096);
+  lists_to_rows_kernel<<<(int)blocks, 256, 0, stream>>>(n_rows, n_lists, k_in, scores, pos, cnt, keys, pos_out, cnt_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
