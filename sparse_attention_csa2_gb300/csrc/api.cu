@@ -423,6 +423,9 @@ csa2_status csa2_topk(const csa2_topk_args* a, void* stream) {
   f.cand_stride = a->L;
   if (t.n_seg == 1) {
     f.idx = a->idx;
+    // rows far longer than K (a prefill chunk's): radix selection over the row in memory;
+    // otherwise the streaming engine
+    if (a->L >= 8LL * a->K) return cuda_status(launch_row_topk(f, s));
     return cuda_status(launch_topk_feed(f, false, 1, s));
   }
   Carve c{static_cast<uint8_t*>(a->workspace)};

@@ -109,6 +109,9 @@ size_t feed_smem_bytes(int K);
 int topk_segments(int n_rows, long long L);  // segments csa2_topk splits each row into
 cudaError_t launch_topk_feed(const FeedParams& p, bool from_lists, int out_seg, cudaStream_t stream);
 cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream);  // segment lists -> final idx
+// Exact top-K of every row by multi-pass radix selection over the row in memory (source A
+// with n_valid, optional cand; rows far longer than K), one block per row.
+cudaError_t launch_row_topk(const FeedParams& p, cudaStream_t stream);
 struct AttnParams {
   const void* q;
   const int64_t* q_pos;

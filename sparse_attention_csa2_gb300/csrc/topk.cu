@@ -244,6 +244,217 @@ size_t merge_smem_bytes(int seg_per_cta, int Kin, int K) {
          (size_t)std::max(ArrSel<kMergeWarps>::list_words(cap), kHistBins) * 4;
 }
 
+// Exact top-K of one long row of materialised scores per block, by radix selection over the
+// row held in memory (for many rows, each far longer than K: the prefill chunk's rows).
+// Pass 1 counts the keys' top 12 bits; pass 2 counts the next 12 bits of the keys in the
+// threshold's bin and lists those keys in shared memory (their number is about the bin's
+// population), so the last 8 bits come from the list; when the bin holds more keys than the
+// list, pass 3 counts them over the row again.  The K-th key T and the number of entries equal
+// to it that are kept (the lowest positions first) then place every kept entry: one pass counts
+// each warp's kept entries over its contiguous range, one pass writes them at the warp's
+// offset, in position order.  Loads are 16-byte where the row allows.
+constexpr int kRtWarps = 8;
+constexpr int kRtThreads = kRtWarps * 32;
+constexpr int kRtList = 2048;
+
+struct RowTopkShared {
+  int hist[kHistBins];
+  uint32_t list[kRtList];
+  int n_list;
+  int bin, before;
+  int warp_gt[kRtWarps], warp_eq[kRtWarps];
+};
+
+// Walks entries [a, b) of the row in order, 32 per step per warp lane-contiguous; f(i, key).
+template <class F>
+__device__ __forceinline__ void rt_walk(const float* row, long long a, long long b, bool vec, F f) {
+  const int lane = threadIdx.x & 31;
+  if (vec) {
+    // 128 entries per warp step, lane l: entries 4l .. 4l+3 (a is a multiple of 4 here)
+    for (long long i0 = a; i0 < b; i0 += 128) {
+      const long long i = i0 + 4 * lane;
+      if (i + 3 < b) {
+        const float4 v = *reinterpret_cast<const float4*>(row + i);
+        f(i, score_key(v.x));
+        f(i + 1, score_key(v.y));
+        f(i + 2, score_key(v.z));
+        f(i + 3, score_key(v.w));
+      } else {
+        for (long long k = i; k < b && k < i + 4; ++k) f(k, score_key(row[k]));
+      }
+    }
+  } else {
+    for (long long i = a + lane; i < b; i += 32) f(i, score_key(row[i]));
+  }
+}
+
+// The bin (of nb, from the top) where the count from the top reaches `need`: one warp, coarse
+// groups of 64 bins then the group's bins; sets sh.bin and sh.before.
+__device__ __forceinline__ void rt_pick(RowTopkShared& sh, int nb, int need) {
+  const int lane = threadIdx.x & 31;
+  const int ng = nb / 64;  // groups (1 or 64)
+  // group sums: lane l sums groups ng-1-2l and ng-2-2l (from the top)
+  int g0 = 0, g1 = 0;
+  const int ga = ng - 1 - 2 * lane, gb = ng - 2 - 2 * lane;
+#pragma unroll 4
+  for (int k = 0; k < 64; ++k) {
+    if (ga >= 0) g0 += sh.hist[64 * ga + k];
+    if (gb >= 0) g1 += sh.hist[64 * gb + k];
+  }
+  int inc = g0 + g1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  int L = __ffs(__ballot_sync(0xffffffffu, inc >= need)) - 1;
+  const int acc = inc - g0 - g1;
+  int grp = acc + g0 >= need ? ga : gb;
+  int above = acc + g0 >= need ? acc : acc + g0;
+  grp = __shfl_sync(0xffffffffu, grp, L);
+  above = __shfl_sync(0xffffffffu, above, L);
+  // the group's bins: lane l takes bins 63-2l and 62-2l of the group
+  const int x0 = sh.hist[64 * grp + 63 - 2 * lane], x1 = sh.hist[64 * grp + 62 - 2 * lane];
+  inc = x0 + x1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  L = __ffs(__ballot_sync(0xffffffffu, above + inc >= need)) - 1;
+  const int acc2 = above + inc - x0 - x1;
+  const int bin = acc2 + x0 >= need ? 63 - 2 * lane : 62 - 2 * lane;
+  const int bef = acc2 + x0 >= need ? acc2 : acc2 + x0;
+  if (lane == L) {
+    sh.bin = 64 * grp + bin;
+    sh.before = bef;
+  }
+}
+
+__global__ void __launch_bounds__(kRtThreads) row_topk_kernel(const FeedParams p) {
+  __shared__ RowTopkShared sh;
+  const int row = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // n_valid is in [0, L] by contract; clamped so that no value reaches past the row
+  const long long L = min((long long)max(p.n_valid[row], 0), p.scores_stride);
+  const float* rs = p.scores + (size_t)row * p.scores_stride;
+  const int K = p.K;
+  int32_t* out = p.idx + (size_t)row * K;
+  auto position = [&](long long j) -> int32_t {
+    return p.cand != nullptr ? p.cand[(size_t)row * p.cand_stride + j] : (int32_t)j;
+  };
+  if (L <= K) {  // every candidate is kept
+    for (int r = tid; r < K; r += kRtThreads) out[r] = r < L ? position(r) : -1;
+    return;
+  }
+  const bool vec = ((reinterpret_cast<uintptr_t>(rs) & 15) == 0);
+  // warp w's contiguous range (a multiple of 128 entries, for the 16-byte walk)
+  const long long per = ((L + kRtWarps - 1) / kRtWarps + 127) / 128 * 128;
+  const long long a = min(L, warp * per), b = min(L, a + per);
+  // ---- level 1: bits 31..20
+  for (int i = tid; i < kHistBins; i += kRtThreads) sh.hist[i] = 0;
+  if (tid == 0) sh.n_list = 0;
+  __syncthreads();
+  rt_walk(rs, a, b, vec, [&](long long, uint32_t key) { atomicAdd(&sh.hist[key >> 20], 1); });
+  __syncthreads();
+  if (warp == 0) rt_pick(sh, kHistBins, K);
+  __syncthreads();
+  const uint32_t b1 = (uint32_t)sh.bin;
+  int need = K - sh.before;
+  __syncthreads();
+  // ---- level 2: bits 19..8 of the keys in bin b1, which are listed on the way
+  for (int i = tid; i < kHistBins; i += kRtThreads) sh.hist[i] = 0;
+  __syncthreads();
+  rt_walk(rs, a, b, vec, [&](long long, uint32_t key) {
+    if ((key >> 20) == b1) {
+      atomicAdd(&sh.hist[(key >> 8) & 0xfffu], 1);
+      const int slot = atomicAdd(&sh.n_list, 1);
+      if (slot < kRtList) sh.list[slot] = key;
+    }
+  });
+  __syncthreads();
+  if (warp == 0) rt_pick(sh, kHistBins, need);
+  __syncthreads();
+  const uint32_t hi24 = (b1 << 12) | (uint32_t)sh.bin;
+  need -= sh.before;
+  const int n_list = sh.n_list;
+  __syncthreads();
+  // ---- level 3: bits 7..0 of the keys in (b1, b2): from the list, or the row again
+  for (int i = tid; i < 256; i += kRtThreads) sh.hist[i] = 0;
+  __syncthreads();
+  if (n_list <= kRtList) {
+    for (int i = tid; i < n_list; i += kRtThreads)
+      if ((sh.list[i] >> 8) == hi24) atomicAdd(&sh.hist[sh.list[i] & 0xffu], 1);
+  } else {
+    rt_walk(rs, a, b, vec, [&](long long, uint32_t key) {
+      if ((key >> 8) == hi24) atomicAdd(&sh.hist[key & 0xffu], 1);
+    });
+  }
+  __syncthreads();
+  if (warp == 0) rt_pick(sh, 256, need);
+  __syncthreads();
+  const uint32_t T = (hi24 << 8) | (uint32_t)sh.bin;
+  const int n_eq = need - sh.before;
+  // ---- placement: each warp's kept entries, counted, then written in order
+  int gt = 0, eq = 0;
+  rt_walk(rs, a, b, vec, [&](long long, uint32_t key) {
+    gt += key > T;
+    eq += key == T;
+  });
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+  }
+  if (lane == 0) {
+    sh.warp_gt[warp] = gt;
+    sh.warp_eq[warp] = eq;
+  }
+  __syncthreads();
+  int base = 0, eq_before = 0;
+  for (int w = 0; w < warp; ++w) {
+    eq_before += sh.warp_eq[w];
+    base += sh.warp_gt[w] + max(0, min(sh.warp_eq[w], n_eq - (eq_before - sh.warp_eq[w])));
+  }
+  // in order: 32 (or 128) entries per step, ballots place them
+  int eq_seen = 0;
+  const unsigned lt = lanemask_lt();
+  auto emit = [&](long long i, uint32_t key, bool valid) {
+    const bool is_gt = valid && key > T, is_eq = valid && key == T;
+    const unsigned em = __ballot_sync(0xffffffffu, is_eq);
+    const bool keep = is_gt || (is_eq && eq_before + eq_seen + __popc(em & lt) < n_eq);
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    if (keep) out[base + __popc(km & lt)] = position(i);
+    base += __popc(km);
+    eq_seen += __popc(em);
+  };
+  if (vec) {
+    for (long long i0 = a; i0 < b; i0 += 128) {
+      // lane l holds entries i0 + 4l .. +3; emit them in order: step u covers entries
+      // i0 + 4l + u for every lane, which is not position order across lanes, so the four
+      // are emitted one at a time after a transpose through shuffles
+      float v4[4];
+      const long long i = i0 + 4 * lane;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v4[u] = i + u < b ? rs[i + u] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        // entry i0 + 32u + lane sits in lane (32u + lane) / 4, slot (32u + lane) % 4
+        const int src = (32 * u + lane) >> 2, slot = (32 * u + lane) & 3;
+        const float x0 = __shfl_sync(0xffffffffu, v4[0], src), x1 = __shfl_sync(0xffffffffu, v4[1], src);
+        const float x2 = __shfl_sync(0xffffffffu, v4[2], src), x3 = __shfl_sync(0xffffffffu, v4[3], src);
+        const float x = slot == 0 ? x0 : slot == 1 ? x1 : slot == 2 ? x2 : x3;
+        const long long e = i0 + 32 * u + lane;
+        emit(e, score_key(x), e < b);
+      }
+    }
+  } else {
+    for (long long i0 = a; i0 < b; i0 += 32) {
+      const long long i = i0 + lane;
+      emit(i, i < b ? score_key(rs[i]) : 0u, i < b);
+    }
+  }
+}
+
 // A record range's candidate list: the selected columns idx[row] (ascending, -1 padded) to
 // their scores and record positions (offset + column); one warp per row.
 __global__ void shard_list_kernel(int n_rows, int K, const int32_t* idx, const float* scores, long long stride,
@@ -282,6 +493,12 @@ __global__ void lists_to_rows_kernel(int n_rows, int n_lists, int k_in, const fl
 }
 
 }  // namespace
+
+cudaError_t launch_row_topk(const FeedParams& p, cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  row_topk_kernel<<<p.n_rows, kRtThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_shard_list(int n_rows, int K, const int32_t* idx, const float* scores, long long stride,
                               long long offset, float* out_scores, int32_t* out_pos, int32_t* out_cnt,

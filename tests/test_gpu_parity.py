@@ -366,3 +366,26 @@ def test_attention_kernels_agree_with_the_oracle(kernel, lat_fmt, group, swa_fmt
     err = rel_err(out.cpu().numpy(), o_ref)
     assert err <= out_tol(inp["params"]), err
     assert np.max(np.abs(sm.cpu().numpy() - sm_ref)) < 1e-4
+
+
+@pytest.mark.parametrize("L,K", [(60_001, 512), (36_864, 512), (20_001, 512), (9_000, 1024), (4_099, 37)])
+def test_topk_many_long_rows(L, K):
+    """More rows than SMs, each far longer than K (the prefill chunk's shape): the radix
+    selection over rows in memory, bit-exact against the oracle, with ties (quarter-step
+    integers), +-0, rows of every visible length (including at most K) and a candidate map.
+    Row strides both 16-byte aligned and not."""
+    _cuda()
+    rows = 200
+    sc = synth.integers((rows, L), 13, L % 89, -300, 300).float() / 4.0
+    sc[1::4] = synth.normal((len(range(1, rows, 4)), L), 13, 2)  # no ties
+    sc[2, ::2] = -0.0
+    sc[2, 1::2] = 0.0
+    rng = np.random.default_rng(L)
+    n_valid = rng.integers(1, L + 1, rows).astype(np.int32)
+    n_valid[:4] = [L, L - 1, K, 1]
+    idx = S.topk(sc.cuda(), torch.from_numpy(n_valid).cuda(), K).cpu().numpy()
+    ref = O.topk_rows(sc.numpy().astype(np.float64), n_valid, K)
+    assert np.array_equal(idx, ref)
+    cand = np.sort(rng.choice(10 ** 7, (rows, L), replace=True), axis=1).astype(np.int32) + np.arange(L, dtype=np.int32)
+    idx_c = S.topk(sc.cuda(), torch.from_numpy(n_valid).cuda(), K, cand=torch.from_numpy(cand).cuda()).cpu().numpy()
+    assert np.array_equal(idx_c, O.topk_rows(sc.numpy().astype(np.float64), n_valid, K, cand=cand))
