@@ -595,7 +595,10 @@ typedef enum csa2_tuning {
   CSA2_TUNE_PROJ_KSPLIT = 3,    /* K split of the projection GEMMs, 1..8; 0 = automatic */
   CSA2_TUNE_ATTN_ROWS = 4,      /* attention kernel: 1 = a block per (row, 128-entry tile) and a
                                    merge kernel; 2 / 3 = a block per (row, 32 / 16 heads) over all
-                                   of the row's tiles; 0 = automatic */
+                                   of the row's tiles; 4 = a block per (row, 32 heads) with the
+                                   tiles' copies and arithmetic pipelined (bf16 latents and window
+                                   only, otherwise 1); 0 = automatic (4 for at least two rows per
+                                   SM with bf16 latents and window, else 1) */
   CSA2_TUNE_COUNT = 5
 } csa2_tuning;
 /* Returns CSA2_EINVAL for an unknown knob or a value outside its range. */

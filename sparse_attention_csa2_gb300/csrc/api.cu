@@ -361,7 +361,7 @@ csa2_status csa2_set_tuning(int32_t knob, int32_t value) {
   if (knob < 0 || knob >= CSA2_TUNE_COUNT || value < 0) return CSA2_EINVAL;
   if (knob == CSA2_TUNE_SCAN_SEGMENTS && value > 64) return CSA2_EINVAL;
   if (knob == CSA2_TUNE_PROJ_KSPLIT && value > 8) return CSA2_EINVAL;
-  if (knob == CSA2_TUNE_ATTN_ROWS && value > 3) return CSA2_EINVAL;
+  if (knob == CSA2_TUNE_ATTN_ROWS && value > 4) return CSA2_EINVAL;
   g_tuning[knob].store(value, std::memory_order_relaxed);
   return CSA2_OK;
 }

@@ -318,6 +318,31 @@ __device__ __forceinline__ void group_reduce8(float (&v)[8]) {
   }
 }
 
+// Four K-steps of 16 over one 64-dim panel of two K-major 128-byte-swizzled operands (32
+// bytes apart); `acc` = accumulate into D from the first step on.
+__device__ __forceinline__ void mma4(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, bool acc) {
+  tc05::mma_bf16(d, ad, bd, idesc, acc ? 1u : 0u);
+#pragma unroll
+  for (int k = 1; k < 4; ++k) tc05::mma_bf16(d, tc05::desc_adv(ad, 32 * k), tc05::desc_adv(bd, 32 * k), idesc, 1u);
+}
+// S^T = K q'^T over the tile's eight 64-dim panels (16 KB apart) against the query's (QPANEL
+// apart), then the low parts of the rotated query (ninth query panel) against the rotary panel.
+template <int QPANEL>
+__device__ __forceinline__ void gemm1_issue(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc) {
+#pragma unroll 1
+  for (int pnl = 0; pnl < 8; ++pnl)
+    mma4(d, tc05::desc_adv(ad, pnl * kKPanel), tc05::desc_adv(bd, pnl * QPANEL), idesc, pnl > 0);
+  mma4(d, tc05::desc_adv(ad, 7 * kKPanel), tc05::desc_adv(bd, 8 * QPANEL), idesc, true);
+}
+// One 128-dim chunk of O^T += V^T [P_hi | P_lo]^T: eight K-steps of 16 entries (2 KB apart in
+// both MN-major operands); `acc` = accumulate into D from the first step on.
+__device__ __forceinline__ void gemm2_chunk_issue(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, bool acc) {
+  tc05::mma_bf16(d, ad, bd, idesc, acc ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < kTileE / 16; ++kk)
+    tc05::mma_bf16(d, tc05::desc_adv(ad, 2048 * kk), tc05::desc_adv(bd, 2048 * kk), idesc, 1u);
+}
+
 __device__ __forceinline__ void report_timeout_attn(int* flag, int32_t* dev_status) {
   atomicExch(flag, 1);
   if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
@@ -405,17 +430,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   if (warp == 0) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc05::idesc_bf16(128, NH);
-#pragma unroll 1
-      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-        const uint32_t sub = (kk & 3) * 32;
-        tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + (kk >> 2) * kKPanel + sub),
-                       tc05::sw128_desc(qs_u + (kk >> 2) * QPANEL + sub), idesc, kk > 0);
-      }
-      // the low parts of the rotated query against the tile's rotary panel
-#pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk)
-        tc05::mma_bf16(tmem, tc05::sw128_desc(ks_u + 7 * kKPanel + kk * 32),
-                       tc05::sw128_desc(qs_u + 8 * QPANEL + kk * 32), idesc, 1u);
+      const uint64_t ad = tc05::sw128_desc(ks_u), bd = tc05::sw128_desc(qs_u);
+      gemm1_issue<QPANEL>(tmem, ad, bd, idesc);
       tc05::mma_commit(&sh.bar_s);
       sh.s_issued = 1;
     }
@@ -504,11 +520,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
       // apart, 8-entry groups 1 KB apart)
       constexpr uint32_t idesc = tc05::idesc_bf16(128, NO) | (1u << 15) | (1u << 16);
 #pragma unroll 1
-      for (int i = 0; i < 4 * (kTileE / 16); ++i) {
-        const int c = i >> 3, kk = i & 7;
-        tc05::mma_bf16(tmem + NO * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel + kk * 2048, kKPanel, 1024),
-                       sw128_desc_lbo(qs_u + kk * 2048, kPBytes, 1024), idesc, kk > 0);
-      }
+      for (int c = 0; c < 4; ++c)
+        gemm2_chunk_issue(tmem + NO * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel, kKPanel, 1024),
+                          sw128_desc_lbo(qs_u, kPBytes, 1024), idesc, false);
       tc05::mma_commit(&sh.bar_o);
       sh.o_issued = 1;
     }
@@ -687,16 +701,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_row_kernel(const AttnPar
     if (warp == 0) {
       if (lane == 0 && !sh.timeout) {
         constexpr uint32_t idesc = tc05::idesc_bf16(128, NH);
-#pragma unroll 1
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint32_t sub = (kk & 3) * 32;
-          tc05::mma_bf16(tmem + kS0, tc05::sw128_desc(ks_u + (kk >> 2) * kKPanel + sub),
-                         tc05::sw128_desc(qs_u + (kk >> 2) * QPANEL + sub), idesc, kk > 0);
-        }
-#pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk)
-          tc05::mma_bf16(tmem + kS0, tc05::sw128_desc(ks_u + 7 * kKPanel + kk * 32),
-                         tc05::sw128_desc(qs_u + 8 * QPANEL + kk * 32), idesc, 1u);
+        gemm1_issue<QPANEL>(tmem + kS0, tc05::sw128_desc(ks_u), tc05::sw128_desc(qs_u), idesc);
         tc05::mma_commit(&sh.bar_s);
         sh.s_issued = kt + 1;
       }
@@ -803,11 +808,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_row_kernel(const AttnPar
       if (lane == 0 && !sh.timeout) {
         constexpr uint32_t idesc = tc05::idesc_bf16(128, NO) | (1u << 15) | (1u << 16);
 #pragma unroll 1
-        for (int i = 0; i < 4 * (kTileE / 16); ++i) {
-          const int c = i >> 3, kk = i & 7;
-          tc05::mma_bf16(tmem + NO * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel + kk * 2048, kKPanel, 1024),
-                         sw128_desc_lbo(ps_u + kk * 2048, kPBytes, 1024), idesc, (kt > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int c = 0; c < 4; ++c)
+          gemm2_chunk_issue(tmem + NO * c, sw128_desc_lbo(ks_u + 2 * c * kKPanel, kKPanel, 1024),
+                            sw128_desc_lbo(ps_u, kPBytes, 1024), idesc, kt > 0);
         tc05::mma_commit(&sh.bar_o);
         sh.o_issued = kt + 1;
       }
@@ -875,6 +878,411 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_row_kernel(const AttnPar
     if (sh.o_issued > 0) tc05::mbar_wait(&sh.bar_o, (sh.o_issued - 1) & 1);
   }
   __syncthreads();
+  if (warp == 0) {
+    tc05::fence_after();
+    tc05::tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ===================================================================================== pipeline
+// Batches of many rows (a prefill chunk: thousands of query rows): one block per (row, 32
+// heads) over all of the row's tiles, as in the row kernel, with the tile stream pipelined
+// across warp roles so that a tile's copies overlap the previous tile's arithmetic:
+//   copies             the latent rows go by cp.async into a ring of five 32 KB slots, one
+//                      slot per pair of 64-dim panels (fill u = pair u mod 4 of tile u / 4
+//                      goes to slot u mod 5); the copy warps (4) form each tile's entry
+//                      sources and copy its pairs 0 and 1, the two halves of the softmax
+//                      warps copy pairs 2 and 3 before the tile's softmax (they would
+//                      otherwise wait for it idle); each group of 128 threads reports its slot
+//                      full once its copies have landed;
+//   MMA thread         S^T = K q'^T pair by pair as the slots fill; then, once the softmax has
+//                      written P, O^T += V^T [P_hi | P_lo]^T chunk by chunk, each chunk's
+//                      commit freeing the slot it read;
+//   softmax warps (8)  as in the row kernel: a reference maximum per head that moves only by
+//                      more than kRowTau (the output in tensor memory rescaled then), P to
+//                      shared memory as hi + lo bf16 terms, running sums.
+// Tile t+1's first pair goes to the fifth slot while tile t is processed, its other pairs as
+// tile t's second GEMM frees slots.  MMAs complete in issue order, so once the softmax sees
+// tile t+1's logits, tile t's second GEMM has finished: P (one buffer) may be rewritten and
+// the output rescaled.  bf16 latents and window rows only (they are copied as they are).
+constexpr int kPipeThreads = 512;     // warp 0 MMA, warps 4..11 softmax, warps 12..15 copies
+constexpr int kPipeSoftFirst = 4, kPipeCopyFirst = 12;
+constexpr int kPipeSlots = 5;
+constexpr int kPipeSlotBytes = 2 * kKPanel;  // 32 KB: 128 entries x 128 dims
+constexpr int kPipeNH = 32;
+constexpr uint32_t kPipeSpin = 1u << 20;
+
+struct PipeShared {
+  const uint8_t* ptr[2][kTileE];  // per tile parity: entry rows
+  int fmt[2][kTileE];          // per tile parity: entry format, -1 = masked
+  float rs[2][kTileE];         // per tile parity: FP8 row scale (1 for bf16)
+  float red_max[4][32];        // per TMEM lane quarter: per-head maxima over its 32 entries
+  float red_sum[4][32];        // ... and sums of P
+  float mref[32], alpha[32], lsum[32];
+  float cs[kRopeDim];
+  uint64_t full[kPipeSlots], empty[kPipeSlots];  // slot filled (copies) / freed (second GEMM)
+  uint64_t src_ready[2];                          // per tile parity: the entry sources are written
+  uint64_t s_full, p_full, o_done, fin;           // first GEMM done / P written / last GEMM / all MMAs
+  uint32_t tmem_base;
+  int timeout;
+  int rescale_tile;  // last tile at which some head's reference moved
+};
+
+constexpr int pipe_smem_bytes() {
+  return 1024 + 9 * kPipeNH * 128 + kPBytes + kPipeSlots * kPipeSlotBytes + (int)sizeof(PipeShared);
+}
+static_assert(pipe_smem_bytes() <= 232448, "the pipeline's shared memory fits one block per SM");
+
+// Bounded wait that also gives up when another role has recorded a timeout.
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, const int* abort) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < kPipeSpin; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred P1;\n mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n selp.b32 %0, 1, 0, P1;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (*reinterpret_cast<const volatile int*>(abort)) return false;
+  }
+  return false;
+}
+
+// Barrier `id` over `count` threads (whole warps, converged first).
+__device__ __forceinline__ void named_bar(int id, int count) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
+// Pair c of tile t (fill u = 4t + c) by 128 threads (thread g: 16-byte chunk g & 15 of the
+// pair's 256 bytes of entries (g >> 4) + 8k): waits for the slot, copies, and reports the slot
+// full once its copies have landed.  Returns false after a failed wait (warp-uniform).
+__device__ __forceinline__ bool pipe_copy_pair(PipeShared& sh, uint8_t* ring, int t, int c, int g, int32_t* dev_status) {
+  const int u = 4 * t + c, slot = u % kPipeSlots;
+  const bool got = pipe_wait(&sh.empty[slot], ((u / kPipeSlots) & 1) ^ 1, &sh.timeout);
+  if (!__all_sync(0xffffffffu, got)) {
+    if (!sh.timeout) report_timeout_attn(&sh.timeout, dev_status);
+    return false;
+  }
+  uint8_t* dst = ring + slot * kPipeSlotBytes;
+  const int j = g & 15, r0 = g >> 4;
+  const uint8_t* const* ptr = sh.ptr[t & 1];
+  const int* fmt = sh.fmt[t & 1];
+#pragma unroll 4
+  for (int k = 0; k < kTileE / 8; ++k) {
+    const int r = r0 + 8 * k;
+    cp_async16(dst + sw128_off(r, j, kTileE), ptr[r] + 256 * c + 16 * j, fmt[r] >= 0);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the copies are read by the tensor cores
+  tc05::mbar_arrive(&sh.full[slot]);
+  return true;
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 1) attn_pipe_kernel(const AttnParams p) {
+  constexpr int NH = kPipeNH, HALF = NH / 2, NG = HALF / 8;
+  constexpr int QPANEL = NH * 128;
+  constexpr int NO = 2 * NH;              // second GEMM's N: P_hi | P_lo
+  constexpr uint32_t kS0 = 4 * NO;        // tensor memory: O in [0, kS0), S^T in [kS0, kS0 + NH)
+  constexpr uint32_t kCols = 512;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1k(smem_raw);
+  uint8_t* qs = smem;                     // q' (nine panels), kept for every tile
+  uint8_t* ps = qs + 9 * QPANEL;          // P_hi | P_lo of the current tile
+  uint8_t* ring = ps + kPBytes;           // five slots of two latent panels
+  PipeShared& sh = *reinterpret_cast<PipeShared*>(ring + kPipeSlots * kPipeSlotBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = blockIdx.x, h0 = blockIdx.y * NH;
+  const int n_tiles = (p.K + p.window + kTileE - 1) / kTileE;
+  const int sel_tiles = min(n_tiles, (p.K + kTileE - 1) / kTileE);
+  const int b = p.seq_of_row[row];
+  const long long qp = p.q_pos[row];
+  const long long pos0 = p.swa_pos0[b];
+  const long long lo = max(qp - (long long)p.window + 1, pos0);
+
+  if (tid == 0) {
+    for (int i = 0; i < kPipeSlots; ++i) {
+      tc05::mbar_init(&sh.full[i], kTileE);  // one arrive per copy thread
+      tc05::mbar_init(&sh.empty[i], 1);
+    }
+    tc05::mbar_init(&sh.s_full, 1);
+    tc05::mbar_init(&sh.p_full, 1);
+    tc05::mbar_init(&sh.o_done, 1);
+    tc05::mbar_init(&sh.fin, 1);
+    tc05::mbar_init(&sh.src_ready[0], 1);
+    tc05::mbar_init(&sh.src_ready[1], 1);
+    sh.timeout = 0;
+    sh.rescale_tile = -1;
+    tc05::fence_barrier_init();
+  }
+  if (warp == 0) tc05::tmem_alloc(&sh.tmem_base, kCols);
+  rope_table(sh.cs, p, qp, 1.f);
+  if (tid < NH) {
+    sh.mref[tid] = -INFINITY;
+    sh.lsum[tid] = 0.f;
+  }
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  __syncthreads();
+  // the query is an input of the step: copied and rotated before any wait
+  if (tid < kAttnThreads) copy_query<NH>(p, row, h0, qs);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < kAttnThreads) rotate_query<NH>(qs, sh.cs);
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // q' is read by the tensor cores
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  const uint32_t qs_u = smem_u32(qs), ps_u = smem_u32(ps), ring_u = smem_u32(ring);
+
+  if (warp >= kPipeCopyFirst) {
+    // ---------------------------------------------------------------- copies: sources, pairs 0 and 1
+    const int g = tid - kPipeCopyFirst * 32;  // entry g of each tile
+    bool waited = false, ok = true;
+    // every copy thread runs every iteration (the named barriers); after a failed wait it only
+    // skips the work
+#pragma unroll 1
+    for (int t = 0; t < n_tiles; ++t) {
+      const int tile = (t + sel_tiles) % n_tiles;
+      if (!waited && tile * kTileE < p.K) {  // the selected indices come from the previous kernel
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        waited = true;
+      }
+      // parity t & 1 was last read for tile t - 2, whose softmax (and so its copies) finished
+      // before the slot this loop waited on for tile t - 1's pair 1 was freed
+      const EntrySrc sr = entry_source(p, row, b, qp, lo, pos0, tile * kTileE + g);
+      sh.ptr[t & 1][g] = sr.valid ? sr.ptr : reinterpret_cast<const uint8_t*>(p.q);
+      sh.fmt[t & 1][g] = sr.valid ? sr.fmt : -1;
+      sh.rs[t & 1][g] = sr.rs;
+      named_bar(2, 128);
+      if (g == 0) tc05::mbar_arrive(&sh.src_ready[t & 1]);
+      if (ok) {
+        ok = pipe_copy_pair(sh, ring, t, 0, g, p.dev_status) && pipe_copy_pair(sh, ring, t, 1, g, p.dev_status);
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == 0) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      bool ok = true;
+      constexpr uint32_t idesc1 = tc05::idesc_bf16(128, NH);
+      constexpr uint32_t idesc2 = tc05::idesc_bf16(128, NO) | (1u << 15) | (1u << 16);
+      const uint64_t qd = tc05::sw128_desc(qs_u), pd = sw128_desc_lbo(ps_u, kPBytes, 1024);
+#pragma unroll 1
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        // S^T = K q'^T, pair by pair
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const int u = 4 * t + c, slot = u % kPipeSlots;
+          if (!pipe_wait(&sh.full[slot], (u / kPipeSlots) & 1, &sh.timeout)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          const uint64_t ad = tc05::sw128_desc(ring_u + slot * kPipeSlotBytes);
+          const uint64_t bd = tc05::desc_adv(qd, 2 * c * QPANEL);
+          mma4(tmem + kS0, ad, bd, idesc1, c > 0);
+          mma4(tmem + kS0, tc05::desc_adv(ad, kKPanel), tc05::desc_adv(bd, QPANEL), idesc1, true);
+          // the low parts of the rotated query against the rotary panel (the last pair's second)
+          if (c == 3) mma4(tmem + kS0, tc05::desc_adv(ad, kKPanel), tc05::desc_adv(qd, 8 * QPANEL), idesc1, true);
+        }
+        if (!ok) break;
+        tc05::mma_commit(&sh.s_full);
+        // O^T += V^T [P_hi | P_lo]^T once the softmax has written P
+        if (!pipe_wait(&sh.p_full, t & 1, &sh.timeout)) {
+          ok = false;
+          break;
+        }
+        tc05::fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const int slot = (4 * t + c) % kPipeSlots;
+          gemm2_chunk_issue(tmem + NO * c, sw128_desc_lbo(ring_u + slot * kPipeSlotBytes, kKPanel, 1024), pd, idesc2,
+                            t > 0);
+          tc05::mma_commit(&sh.empty[slot]);
+        }
+      }
+      if (ok) tc05::mma_commit(&sh.o_done);
+      else if (!sh.timeout) report_timeout_attn(&sh.timeout, p.dev_status);
+      // every MMA issued has completed before the tensor memory is freed
+      tc05::mma_commit(&sh.fin);
+      tc05::mbar_wait(&sh.fin, 0);
+    }
+    __syncwarp();
+  } else if (warp >= kPipeSoftFirst) {
+    // ---------------------------------------------------------------- softmax
+    const int sw = warp - kPipeSoftFirst;
+    const int qw = sw & 3, hb = HALF * (sw >> 2), e = 32 * qw + lane;
+    const int lh = (lane >> 2) & 7;  // head within a group of 8 whose result this lane ends with
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * qw) << 16);
+    const int cgrp = sw >> 2, cg = tid - (kPipeSoftFirst + 4 * cgrp) * 32;  // copies pair 2 + cgrp
+    bool ok = true;
+    // every softmax thread runs every iteration (the named barriers); after a failed wait it
+    // computes nothing that reaches tensor memory or the MMA thread
+#pragma unroll 1
+    for (int t = 0; t < n_tiles; ++t) {
+      // this half's pair of the tile, once the copy warps have written its sources
+      if (ok) {
+        const bool src = pipe_wait(&sh.src_ready[t & 1], (t >> 1) & 1, &sh.timeout);
+        ok = __all_sync(0xffffffffu, src) && pipe_copy_pair(sh, ring, t, 2 + cgrp, cg, p.dev_status);
+        if (!ok && !sh.timeout) report_timeout_attn(&sh.timeout, p.dev_status);
+      }
+      // warp-uniform: the tensor-memory loads and stores below are warp-wide
+      ok = __all_sync(0xffffffffu, ok && pipe_wait(&sh.s_full, t & 1, &sh.timeout));
+      tc05::fence_after();
+      const int f = sh.fmt[t & 1][e];
+      const float rs = sh.rs[t & 1][e];
+      const bool on = ok && f >= 0;
+      const float zs = p.scale * rs;
+      float z[HALF];
+      if (ok) {
+        uint32_t v[HALF];
+        tc05::tmem_ld<HALF>(lane_base + kS0 + (uint32_t)hb, v);
+        tc05::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < HALF; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
+      } else {
+#pragma unroll
+        for (int k = 0; k < HALF; ++k) z[k] = -INFINITY;
+      }
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        float m[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m[k] = z[8 * gi + k];
+        group_reduce8<true>(m);
+        if ((lane & 3) == 0) sh.red_max[qw][hb + 8 * gi + lh] = m[0];
+      }
+      named_bar(1, 256);
+      if (qw == 0 && lane < HALF) {
+        const int h = hb + lane;
+        const float mt = fmaxf(fmaxf(sh.red_max[0][h], sh.red_max[1][h]), fmaxf(sh.red_max[2][h], sh.red_max[3][h]));
+        const float mr = sh.mref[h];
+        float a = 1.f;
+        if (mr == -INFINITY) {
+          sh.mref[h] = mt;  // first finite maximum: the accumulated output and sum are still zero
+        } else if (mt > mr + kRowTau) {
+          a = __expf(mr - mt);
+          sh.mref[h] = mt;
+          sh.rescale_tile = t;
+        }
+        sh.alpha[h] = a;
+      }
+      named_bar(1, 256);
+      if (ok && sh.rescale_tile == t && t > 0) {
+        // O *= alpha per head (the previous tile's second GEMM has completed: this tile's
+        // first GEMM was issued after it and has completed)
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * (sw >> 2) + cc;
+#pragma unroll 1
+          for (int part = 0; part < NO / 32; ++part) {
+            const uint32_t ta = lane_base + NO * c + 32 * part;
+            uint32_t v[32];
+            tc05::tmem_ld32(ta, v);
+            tc05::tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * sh.alpha[(32 * part + k) % NH]);
+            tc05::tmem_st32(ta, v);
+          }
+        }
+        tc05::tmem_st_wait();
+      }
+      // P = exp(z - M) as P_hi | P_lo rows (P_hi in columns 0 .. NH-1, P_lo in NH .. 2NH-1 of
+      // the entry's 128-byte row), the FP8 row scale on the weights; per-head sums of P
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        float pe[8];
+        uint32_t hi[4], lw[4];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float M = sh.mref[hb + 8 * gi + k];
+          pe[k] = on ? __expf(z[8 * gi + k] - (M == -INFINITY ? 0.f : M)) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a0 = pe[2 * k] * rs, a1 = pe[2 * k + 1] * rs;
+          hi[k] = pack_bf16x2(a0, a1);
+          lw[k] = pack_bf16x2(a0 - bf16_lo(hi[k]), a1 - bf16_hi(hi[k]));
+        }
+        const int ci = hb / 8 + gi;
+        if (ok) {  // (after a failed wait P may still be read by an earlier second GEMM)
+          *reinterpret_cast<uint4*>(ps + e * 128 + ((ci ^ (e & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(ps + e * 128 + (((NH / 8 + ci) ^ (e & 7)) << 4)) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        group_reduce8<false>(pe);
+        if ((lane & 3) == 0) sh.red_sum[qw][hb + 8 * gi + lh] = pe[0];
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc05::fence_before();
+      named_bar(1, 256);
+      if (qw == 0 && lane < HALF) {
+        const int h = hb + lane;
+        sh.lsum[h] = sh.lsum[h] * sh.alpha[h] +
+                     ((sh.red_sum[0][h] + sh.red_sum[1][h]) + (sh.red_sum[2][h] + sh.red_sum[3][h]));
+      }
+      if (ok && sw == 0 && lane == 0) tc05::mbar_arrive(&sh.p_full);
+    }
+    if (!ok && !sh.timeout) report_timeout_attn(&sh.timeout, p.dev_status);
+    // ------------------------------------------------------------ output
+    const bool live = __all_sync(0xffffffffu, ok && pipe_wait(&sh.o_done, 0, &sh.timeout));
+    if (ok && !live && lane == 0 && !sh.timeout) report_timeout_attn(&sh.timeout, p.dev_status);
+    tc05::fence_after();
+    named_bar(1, 256);  // the last tile's running sums are final
+    if (sw == 0) {
+      // the sink joins the denominator: o = O e^{M - Mf} / (l e^{M - Mf} + e^{sink - Mf})
+      const int h = lane;
+      const float M = sh.mref[h], sk = __ldg(p.sink + h0 + h);
+      const float Mf = fmaxf(M, sk);
+      const float so = M == -INFINITY ? 0.f : __expf(M - Mf);
+      const float es = __expf(sk - Mf);
+      const float den = sh.lsum[h] * so + es;
+      sh.alpha[h] = so / den;
+      if (p.sink_mass) p.sink_mass[(size_t)row * kHeads + h0 + h] = es / den;
+    }
+    named_bar(1, 256);
+    if (live) {
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * (sw >> 2) + cc;
+        const int d = 128 * c + 32 * qw + lane;
+        uint32_t v[32], v2[32];
+        const uint32_t ta = lane_base + NO * c;
+        tc05::tmem_ld32(ta, v);
+        tc05::tmem_ld32(ta + 32, v2);
+        tc05::tmem_ld_wait();
+        float o[NH];
+#pragma unroll
+        for (int k = 0; k < NH; ++k) o[k] = (__uint_as_float(v[k]) + __uint_as_float(v2[k])) * sh.alpha[k];
+        if (d >= kHeadDim - kRopeDim) {
+          // turned back by -position: pairs (448 + 2i, 449 + 2i) sit in adjacent lanes
+          const int i = (d - (kHeadDim - kRopeDim)) >> 1;
+          const float cn = sh.cs[i], sn = sh.cs[32 + i];
+          const bool even = (d & 1) == 0;
+#pragma unroll
+          for (int k = 0; k < NH; ++k) {
+            const float other = __shfl_xor_sync(0xffffffffu, o[k], 1);
+            o[k] = even ? o[k] * cn + other * sn : o[k] * cn - other * sn;
+          }
+        }
+        const size_t at = ((size_t)row * kHeads + h0) * kHeadDim + d;
+#pragma unroll
+        for (int k = 0; k < NH; ++k) {
+          if (p.out_bf16) static_cast<__nv_bfloat16*>(p.out)[at + (size_t)k * kHeadDim] = __float2bfloat16_rn(o[k]);
+          else static_cast<float*>(p.out)[at + (size_t)k * kHeadDim] = o[k];
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc05::fence_before();
+  __syncthreads();  // the MMA thread saw every MMA complete
   if (warp == 0) {
     tc05::fence_after();
     tc05::tmem_dealloc(tmem, kCols);
@@ -1002,7 +1410,27 @@ int attn_smem_bytes() { return kAttnSmemBytes; }
 cudaError_t launch_sparse_attn(const AttnParams& p, int n_split, cudaStream_t stream) {
   if (p.n_rows == 0) return cudaSuccess;
   const int rows_mode = tuning(CSA2_TUNE_ATTN_ROWS);
-  if (rows_mode >= 2 || (rows_mode == 0 && use_row_kernel(p, n_split))) {
+  // Many rows (a prefill chunk), bf16 latents and window: the pipelined row kernel, two
+  // blocks per row (32 heads each).  With fewer rows than two per SM its serial tiles cost
+  // more latency than the tile kernel's parallel ones.
+  const bool pipe_ok = p.lat_fmt == CSA2_BF16 && (p.swa_fmt == CSA2_BF16 || p.window == 0) && p.range_count == 0;
+  if (pipe_ok && (rows_mode == 4 || (rows_mode == 0 && p.n_rows >= 2 * device_sm_count()))) {
+    cudaError_t e = cudaFuncSetAttribute(attn_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         pipe_smem_bytes());
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_rows, kHeads / kPipeNH);
+    cfg.blockDim = dim3(kPipeThreads);
+    cfg.dynamicSmemBytes = pipe_smem_bytes();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_pipe_kernel, p);
+  }
+  if (rows_mode == 2 || rows_mode == 3 || (rows_mode == 0 && use_row_kernel(p, n_split))) {
     // whole rows per block, no partials and no merge
     const int nh = rows_mode == 3 ? 16 : rows_mode == 2 ? 32 : row_kernel_heads(p);
     auto kern = nh == 16 ? attn_row_kernel<16> : attn_row_kernel<32>;

@@ -157,3 +157,5 @@ def test_tuning_overrides_are_range_checked(lib):
     assert st(3, 9) == 1                               # projection K split 0..8
     assert st(0, 8) == 0 and st(0, 0) == 0             # set, and back to automatic
     assert st(2, 0) == 0 and st(2, 1) == 0
+    assert st(4, 5) == 1 and st(4, -1) == 1           # attention kernel 0..4
+    assert st(4, 4) == 0 and st(4, 0) == 0

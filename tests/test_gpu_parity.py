@@ -328,14 +328,15 @@ def test_prefill_index_scores_mxfp4(mode):
 
 
 # ------------------------------------------------------------------ attention kernels
-@pytest.mark.parametrize("kernel", [1, 2, 3])  # tiles + merge; rows with 32 heads; rows with 16 heads
+# tiles + merge; rows with 32 heads; rows with 16 heads; pipelined rows (bf16 only, else tiles)
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("lat_fmt,group,swa_fmt", [("bf16", 32, "bf16"), ("fp4", 32, "fp8")])
 def test_attention_kernels_agree_with_the_oracle(kernel, lat_fmt, group, swa_fmt):
-    """Both attention kernels (a block per (row, tile) with a merge kernel, and a block per
-    (row, head group) carrying the softmax across the row's tiles) against the oracle, on rows
-    where a later tile's logits exceed the first (window) tile's by far more than the row
-    kernel's rescale threshold, so its running reference moves and the accumulated output is
-    rescaled; -1 pads and a short row included."""
+    """Every attention kernel (a block per (row, tile) with a merge kernel; a block per (row,
+    head group) carrying the softmax across the row's tiles, plain or with the tiles' copies
+    pipelined) against the oracle, on rows where a later tile's logits exceed the first
+    (window) tile's by far more than the row kernels' rescale threshold, so their running
+    reference moves and the accumulated output is rescaled; -1 pads and a short row included."""
     _cuda()
     inp = small("batched_decode", seed=31, B=3, N=4000, lat_fmt=lat_fmt, lat_group=group, swa_fmt=swa_fmt)
     set_rows(inp, [4000, 3000, 100])
