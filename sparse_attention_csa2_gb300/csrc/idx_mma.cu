@@ -529,7 +529,8 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t idesc = FP8 ? tc05::idesc_e4m3(128, C::kN) : tc05::idesc_bf16(128, C::kN);
       bool ok = tc05::mbar_wait(FP8 ? &bars.qready : &bars.qfull, 0);
-      const uint32_t q_u = smem_u32(qs);
+      const uint64_t qd = tc05::sw128_desc(smem_u32(qs));
+      const uint64_t ring_d = tc05::sw128_desc(smem_u32(ring));
       for (int t = 0; ok && t < n_tiles; ++t) {
         const int s = t % kStages, a = t & 1;
         if (!tc05::mbar_wait(&bars.full[s], (t / kStages) & 1) ||
@@ -538,18 +539,18 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
           break;
         }
         tc05::fence_after();
-        const uint32_t a_u = smem_u32(ring + s * C::kTileBytes);
+        const uint64_t ad = tc05::desc_adv(ring_d, s * C::kTileBytes);
         const uint32_t d_t = tmem + (uint32_t)a * C::kAccCols;
         if (FP8) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc05::mma_e4m3(d_t, tc05::sw128_desc(a_u + kk * 32), tc05::sw128_desc(q_u + kk * 32), idesc, kk > 0);
+            tc05::mma_e4m3(d_t, tc05::desc_adv(ad, kk * 32), tc05::desc_adv(qd, kk * 32), idesc, kk > 0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kKeyHalf + (kk & 3) * 32;
             const uint32_t qoff = (kk >> 2) * kDecQHalf + (kk & 3) * 32;
-            tc05::mma_bf16(d_t, tc05::sw128_desc(a_u + off), tc05::sw128_desc(q_u + qoff), idesc, kk > 0);
+            tc05::mma_bf16(d_t, tc05::desc_adv(ad, off), tc05::desc_adv(qd, qoff), idesc, kk > 0);
           }
         }
         tc05::mma_commit(&bars.empty[s]);
