@@ -6,7 +6,8 @@ visible records each, bf16 indexer keys and latents, top-512, window 128, 64x512
 indexer scan + per-segment top-K -> top-K merge -> sparse attention -> split combine, all
 through the library's C ABI (csa2_fused_decode).  `value` is queries/s with the cache
 resident in HBM; `e2e` is the same metric with every step's query inputs copied from
-pinned host memory and the outputs read back.  The indexer scan (the dominant kernel) is
+pinned host memory and the outputs read back, as a serving loop runs it: two buffer sets, a
+step's copies overlapping the other set's compute.  The indexer scan (the dominant kernel) is
 timed live with CUDA events recorded by the library at its stage boundaries.
 
 Multi-GPU (torchrun, one process per GPU): every rank runs its own batch (independent
@@ -654,11 +655,16 @@ def run_gb300(args, world, rank, local):
     inp = synth.make_inputs(wl, seed=2 + rank)
     dv = synth.to_device(inp, f"cuda:{local}")
     p, rw, c, lay = dv["params"], dv["rows"], dv["cache"], dv["layers"][0]
-    layer = S.DecodeLayer("full", q_idx=lay["q_idx"], w=lay["w"], k_idx=c["k_idx"], k_scale=c["k_scale"],
-                          seq_of_row=rw["seq_of_row"], n_visible=rw["n_visible"], q=lay["q"], q_pos=rw["q_pos"],
-                          latents=c["lat"], lat_scale=c["lat_scales"], swa=lay["swa"], swa_scale=lay["swa_scale"],
-                          swa_pos0=rw["swa_pos0"], window=p["W"], sink=lay["sink"], K=p["K"], theta=p["theta"],
-                          softmax_scale=p["softmax_scale"])
+
+    def make_layer(q_idx, w, q, q_pos, n_visible):
+        """A FULL decode layer over the resident caches with this step's query-side inputs."""
+        return S.DecodeLayer("full", q_idx=q_idx, w=w, k_idx=c["k_idx"], k_scale=c["k_scale"],
+                             seq_of_row=rw["seq_of_row"], n_visible=n_visible, q=q, q_pos=q_pos,
+                             latents=c["lat"], lat_scale=c["lat_scales"], swa=lay["swa"], swa_scale=lay["swa_scale"],
+                             swa_pos0=rw["swa_pos0"], window=p["W"], sink=lay["sink"], K=p["K"], theta=p["theta"],
+                             softmax_scale=p["softmax_scale"])
+
+    layer = make_layer(lay["q_idx"], lay["w"], lay["q"], rw["q_pos"], rw["n_visible"])
     stream = torch.cuda.current_stream()
     launches_per_step = layer.launches
 
@@ -703,33 +709,66 @@ def run_gb300(args, world, rank, local):
     attn_ms = [ev[s][2].elapsed_time(ev[s][3]) for s in range(n_stage)]
     layer.set_stage_events([])
 
-    # ---- end to end: per-step query inputs from pinned host memory, outputs read back
+    # ---- end to end: per-step query inputs from pinned host memory, outputs read back.  Two
+    # buffer sets (two layers over the same resident caches) let a step's input copies (one copy
+    # stream) and the previous step's read-back (another) run while the other set computes;
+    # every step's copies are inside the timed region.
     e2e = None
     if not args.no_e2e:
         host_in = [t.cpu().pin_memory() for t in (lay["q_idx"], lay["w"], lay["q"], rw["q_pos"], rw["n_visible"])]
-        dev_in = [lay["q_idx"], lay["w"], lay["q"], rw["q_pos"], rw["n_visible"]]
-        host_out = [torch.empty_like(layer.out, device="cpu").pin_memory(),
-                    torch.empty_like(layer.idx, device="cpu").pin_memory()]
+        sets = []
+        for _ in range(2):
+            d_in = [t.clone() for t in (lay["q_idx"], lay["w"], lay["q"], rw["q_pos"], rw["n_visible"])]
+            lay_k = make_layer(*d_in)
+            h_out = [torch.empty_like(lay_k.out, device="cpu").pin_memory(),
+                     torch.empty_like(lay_k.idx, device="cpu").pin_memory()]
+            lay_k()
+            sets.append((d_in, lay_k, h_out))
         h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
         e_steps = max(10, args.steps // 4)
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]    # set k's inputs copied
+        ev_done = [torch.cuda.Event() for _ in range(2)]  # set k's step computed
+        ev_out = [torch.cuda.Event() for _ in range(2)]   # set k's outputs read back
+
+        def e2e_steps(n):
+            for i in range(n):
+                k = i & 1
+                d_in, lay_k, h_out = sets[k]
+                with torch.cuda.stream(h2d_s):
+                    if i >= 2:
+                        h2d_s.wait_event(ev_done[k])  # step i - 2 no longer reads these inputs
+                    for d, h in zip(d_in, host_in):
+                        d.copy_(h, non_blocking=True)
+                    ev_in[k].record(h2d_s)
+                stream.wait_event(ev_in[k])
+                if i >= 2:
+                    stream.wait_event(ev_out[k])  # step i - 2's outputs were read back
+                lay_k()
+                ev_done[k].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(ev_done[k])
+                    h_out[0].copy_(lay_k.out, non_blocking=True)
+                    h_out[1].copy_(lay_k.idx, non_blocking=True)
+                    ev_out[k].record(d2h_s)
+            stream.wait_stream(h2d_s)
+            stream.wait_stream(d2h_s)
+
+        e2e_steps(4)  # warm-up
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e_steps):
-            for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)
-            layer()
-            host_out[0].copy_(layer.out, non_blocking=True)
-            host_out[1].copy_(layer.idx, non_blocking=True)
+        e2e_steps(e_steps)
         e1.record(stream)
         torch.cuda.synchronize()
         e_val, _ = aggregate(wl.B * e_steps, e0.elapsed_time(e1) / 1e3)
         e2e = {"value": e_val, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e_steps, "note": "KV cache resident in HBM; per-step query inputs host->device, "
-                                         "attention output and indices device->host"}
+                                         "attention output and indices device->host, each step's copies "
+                                         "overlapping the other buffer set's compute (two copy streams)"}
 
     if rank != 0:
         if world > 1:
