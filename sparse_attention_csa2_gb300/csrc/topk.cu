@@ -250,12 +250,17 @@ size_t merge_smem_bytes(int seg_per_cta, int Kin, int K) {
 // threshold's bin and lists those keys in shared memory (their number is about the bin's
 // population), so the last 8 bits come from the list; when the bin holds more keys than the
 // list, pass 3 counts them over the row again.  The K-th key T and the number of entries equal
-// to it that are kept (the lowest positions first) then place every kept entry: one pass counts
-// each warp's kept entries over its contiguous range, one pass writes them at the warp's
-// offset, in position order.  Loads are 16-byte where the row allows.
+// to it that are kept (the lowest positions first) then place every kept entry.  Rows of up to
+// 64 K entries take one more pass, which marks the entries above T and those equal to it in two
+// bitmaps (in the histogram's shared memory, free by then); the first n_eq ties in position
+// order join the kept bits (a block prefix over the words' counts) and a second prefix places
+// every kept entry in position order.  Longer rows take two passes: one counts each warp's kept
+// entries over its contiguous range, one writes them at the warp's offset.  Loads are 16-byte
+// where the row allows.
 constexpr int kRtWarps = 8;
 constexpr int kRtThreads = kRtWarps * 32;
 constexpr int kRtList = 2048;
+constexpr long long kRtBitmapMax = 65536;  // entries: two bitmaps of this many bits in `hist`
 
 struct RowTopkShared {
   int hist[kHistBins];
@@ -331,6 +336,126 @@ __device__ __forceinline__ void rt_pick(RowTopkShared& sh, int nb, int need) {
   }
 }
 
+// Exclusive prefix of v over the block in thread order; `total` gets the block's sum.  Uses
+// sh.warp_gt as scratch (callers separate two uses by a barrier).
+__device__ __forceinline__ int rt_block_scan(RowTopkShared& sh, int v, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh.warp_gt[warp] = x;
+  __syncthreads();
+  int before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kRtWarps; ++w) {
+    const int c = sh.warp_gt[w];
+    before += w < warp ? c : 0;
+    total += c;
+  }
+  return before + x - v;
+}
+
+// Placement of a row of at most kRtBitmapMax entries once the K-th key T and the number n_eq of
+// entries equal to it that are kept are known: one pass over the row marks, in position order,
+// the entries above T (`keep`) and equal to it (`tie`); the first n_eq tie bits join `keep`; the
+// kept entries are written in position order.  Warp ranges [a, b) start on multiples of 128.
+template <class Pos>
+__device__ __forceinline__ void rt_place_bitmap(RowTopkShared& sh, const float* rs, long long a, long long b, bool vec,
+                                                uint32_t T, int n_eq, long long L, int32_t* out, Pos position) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* keep = reinterpret_cast<uint32_t*>(sh.hist);
+  uint32_t* tie = keep + kRtBitmapMax / 32;
+  constexpr int kWords = (int)(kRtBitmapMax / 32), kWpt = kWords / kRtThreads;  // words per thread
+  static_assert(2 * kWords <= kHistBins, "both bitmaps fit in the histogram");
+  __syncthreads();  // every thread has read the last pick's results
+  for (int i = tid; i < 2 * kWords; i += kRtThreads) keep[i] = 0u;
+  __syncthreads();
+  if (vec) {
+    for (long long i0 = a; i0 < b; i0 += 128) {
+      // lane l holds entries i0 + 4l .. +3: word (i0 / 32) + l / 8, bits 4 (l % 8) .. +3
+      const long long i = i0 + 4 * lane;
+      float v4[4];
+      if (i + 3 < b) {
+        const float4 v = *reinterpret_cast<const float4*>(rs + i);
+        v4[0] = v.x, v4[1] = v.y, v4[2] = v.z, v4[3] = v.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v4[u] = i + u < b ? rs[i + u] : 0.f;
+      }
+      uint32_t kb = 0u, tb = 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool valid = i + u < b;
+        const uint32_t key = score_key(v4[u]);
+        kb |= (uint32_t)(valid && key > T) << u;
+        tb |= (uint32_t)(valid && key == T) << u;
+      }
+      uint32_t kw = kb << (4 * (lane & 7)), tw = tb << (4 * (lane & 7));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        kw |= __shfl_xor_sync(0xffffffffu, kw, o);
+        tw |= __shfl_xor_sync(0xffffffffu, tw, o);
+      }
+      if ((lane & 7) == 0) {
+        const long long wi = (i0 >> 5) + (lane >> 3);
+        keep[wi] = kw;
+        tie[wi] = tw;
+      }
+    }
+  } else {
+    for (long long i0 = a; i0 < b; i0 += 32) {
+      const long long i = i0 + lane;
+      const bool valid = i < b;
+      const uint32_t key = valid ? score_key(rs[i]) : 0u;
+      const uint32_t kw = __ballot_sync(0xffffffffu, valid && key > T);
+      const uint32_t tw = __ballot_sync(0xffffffffu, valid && key == T);
+      if (lane == 0) {
+        keep[i0 >> 5] = kw;
+        tie[i0 >> 5] = tw;
+      }
+    }
+  }
+  __syncthreads();
+  // the first n_eq ties in position order join the kept entries (thread t: words kWpt t ..)
+  const int n_words = (int)((L + 31) / 32), w0 = tid * kWpt;
+  int tc = 0;
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) tc += w0 + j < n_words ? __popc(tie[w0 + j]) : 0;
+  int total;
+  int rank = rt_block_scan(sh, tc, total);
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) {
+    if (w0 + j >= n_words) break;
+    uint32_t m = tie[w0 + j], sel = 0u;
+    while (m != 0u && rank < n_eq) {  // lowest bits (positions) first
+      const uint32_t low = m & (0u - m);
+      sel |= low;
+      m ^= low;
+      ++rank;
+    }
+    keep[w0 + j] |= sel;
+  }
+  __syncthreads();  // the scan's scratch is reused below
+  int kc = 0;
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) kc += w0 + j < n_words ? __popc(keep[w0 + j]) : 0;
+  int at = rt_block_scan(sh, kc, total);
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) {
+    if (w0 + j >= n_words) break;
+    uint32_t m = keep[w0 + j];
+    while (m != 0u) {
+      const int bit = __ffs(m) - 1;
+      out[at++] = position(32LL * (w0 + j) + bit);
+      m &= m - 1u;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRtThreads) row_topk_kernel(const FeedParams p) {
   __shared__ RowTopkShared sh;
   const int row = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -394,6 +519,10 @@ __global__ void __launch_bounds__(kRtThreads) row_topk_kernel(const FeedParams p
   __syncthreads();
   const uint32_t T = (hi24 << 8) | (uint32_t)sh.bin;
   const int n_eq = need - sh.before;
+  if (L <= kRtBitmapMax) {
+    rt_place_bitmap(sh, rs, a, b, vec, T, n_eq, L, out, position);
+    return;
+  }
   // ---- placement: each warp's kept entries, counted, then written in order
   int gt = 0, eq = 0;
   rt_walk(rs, a, b, vec, [&](long long, uint32_t key) {

@@ -369,12 +369,13 @@ def test_attention_kernels_agree_with_the_oracle(kernel, lat_fmt, group, swa_fmt
     assert np.max(np.abs(sm.cpu().numpy() - sm_ref)) < 1e-4
 
 
-@pytest.mark.parametrize("L,K", [(60_001, 512), (36_864, 512), (20_001, 512), (9_000, 1024), (4_099, 37)])
+@pytest.mark.parametrize("L,K", [(70_001, 512), (60_001, 512), (36_864, 512), (20_001, 512), (9_000, 1024), (4_099, 37)])
 def test_topk_many_long_rows(L, K):
     """More rows than SMs, each far longer than K (the prefill chunk's shape): the radix
     selection over rows in memory, bit-exact against the oracle, with ties (quarter-step
     integers), +-0, rows of every visible length (including at most K) and a candidate map.
-    Row strides both 16-byte aligned and not."""
+    Row strides both 16-byte aligned and not; rows up to 65,536 entries place the kept entries
+    through bitmaps, longer ones (70,001) by counting and writing passes."""
     _cuda()
     rows = 200
     sc = synth.integers((rows, L), 13, L % 89, -300, 300).float() / 4.0
