@@ -398,9 +398,6 @@ template <bool FP8>
 __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     idx_mma_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK64, const ScanParams p) {
-  // launched with programmatic dependent launch: wait for the previous kernel in the stream
-  // before reading any input
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   using C = DecCfg<FP8>;
   constexpr int kStages = C::kStages, kThreads = C::kThreads;
   extern __shared__ uint8_t smem_raw[];
@@ -420,27 +417,14 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
-  const int b = p.seq_of_row[row];
-  // Candidate mode (Reindex over a block pool): the row's records are its candidate slots,
-  // ascending positions in runs of cand_run consecutive records; every 64-slot half of a tile
-  // is one contiguous run, loaded by its own 64-row TMA box.
-  const bool cmode = p.cand != nullptr;
-  const long long L_row = cmode ? (long long)p.n_cand[row] : min((long long)p.n_visible[row], p.N);
-  const int U = p.unit;
-  const long long n_units = (L_row + U - 1) / U;
-  long long u0, u1;
-  split_range(n_units, n_seg, seg, u0, u1);
-  const long long e0 = u0 * U, e1 = min(u1 * U, L_row);
-  const int n_tiles = e1 > e0 ? (int)((e1 - e0 + kTileKeys - 1) / kTileKeys) : 0;
-  const int seg_len = (int)(e1 - e0);
-
   const bool do_topk = p.K > 0;
   ArrSel<kThreads / 32> sel;  // the whole block, once the stream is done
   sel.sh = selsh;
   sel.tid = tid;
-  const int bs = p.block_max ? U : 1;
-  const int seg_blocks = p.block_max ? (int)((e1 - e0 + bs - 1) / bs) : 0;
+  const bool fast = do_topk && p.cluster_merge && p.fast_select;
 
+  // ---- set-up that reads no input: it overlaps the previous kernel's tail (programmatic
+  // dependent launch)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc05::mbar_init(&bars.full[s], 1);
@@ -460,14 +444,33 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     tc05::fence_barrier_init();
   }
   if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, C::kTmemCols);
-  for (int i = tid; i < seg_blocks; i += kThreads) bkeys[i] = 0u;
+  // the whole block-maxima table (this segment's blocks are known once the inputs are read)
+  if (p.block_max)
+    for (int i = tid; i < p.seg_table; i += kThreads) bkeys[i] = 0u;
+  if (do_topk) sel.zero_hist(kHistBins);
+  if (fast)
+    for (int i = tid; i < kDecSegMax / 32; i += kThreads) listed[i] = 0u;
+
+  // ---- wait for the previous kernel in the stream before reading any input
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  const int b = p.seq_of_row[row];
+  // Candidate mode (Reindex over a block pool): the row's records are its candidate slots,
+  // ascending positions in runs of cand_run consecutive records; every 64-slot half of a tile
+  // is one contiguous run, loaded by its own 64-row TMA box.
+  const bool cmode = p.cand != nullptr;
+  const long long L_row = cmode ? (long long)p.n_cand[row] : min((long long)p.n_visible[row], p.N);
+  const int U = p.unit;
+  const long long n_units = (L_row + U - 1) / U;
+  long long u0, u1;
+  split_range(n_units, n_seg, seg, u0, u1);
+  const long long e0 = u0 * U, e1 = min(u1 * U, L_row);
+  const int n_tiles = e1 > e0 ? (int)((e1 - e0 + kTileKeys - 1) / kTileKeys) : 0;
+  const int seg_len = (int)(e1 - e0);
+  const int bs = p.block_max ? U : 1;
+  const int seg_blocks = p.block_max ? (int)((e1 - e0 + bs - 1) / bs) : 0;
   if (cmode)
     for (int i = tid; i < (seg_len + 63) / 64; i += kThreads)
       hstart[i] = p.cand[(size_t)row * p.cand_stride + e0 + 64 * i];
-  if (do_topk) sel.zero_hist(kHistBins);
-  const bool fast = do_topk && p.cluster_merge && p.fast_select;
-  if (fast)
-    for (int i = tid; i < kDecSegMax / 32; i += kThreads) listed[i] = 0u;
   tc05::fence_before();
   __syncthreads();
   tc05::fence_after();
