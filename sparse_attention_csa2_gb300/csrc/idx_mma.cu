@@ -197,14 +197,20 @@ __device__ __forceinline__ uint32_t row_key_bound(const int* hist, const uint32_
     const int b0 = hi - 4 * lane - 3;  // a multiple of 4
     int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
     if (b0 >= 0) {
-#pragma unroll 1
-      for (uint32_t r = 0; r < n_cta; ++r) {
-        const uint4 v = cluster_ld_v4(cluster_map(hist + b0, r));
-        s0 += (int)v.x;
-        s1 += (int)v.y;
-        s2 += (int)v.z;
-        s3 += (int)v.w;
-      }
+      // every block's four bins at once: the remote loads' round trips overlap (one after
+      // another they cost ~2 us per bound at 8 blocks)
+      uint4 v[kMaxClusterSeg];
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSeg; ++r)
+        if ((uint32_t)r < n_cta) v[r] = cluster_ld_v4(cluster_map(hist + b0, (uint32_t)r));
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSeg; ++r)
+        if ((uint32_t)r < n_cta) {
+          s0 += (int)v[r].x;
+          s1 += (int)v[r].y;
+          s2 += (int)v[r].z;
+          s3 += (int)v[r].w;
+        }
     }
     const int c = s0 + s1 + s2 + s3;
     int inc = c;  // lanes in order = bins from the top down
