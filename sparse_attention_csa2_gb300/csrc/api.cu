@@ -510,7 +510,9 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     const int cand_run = a->mode == CSA2_MODE_REINDEX ? a->block_size : 0;
     if (scan_path(&ic, true, cand_run) == ScanPath::kTc05Decode) {
       const int unit = a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128;
-      n_seg = tc05_segments(n_rows, L, unit, a->mode == CSA2_MODE_REINDEX ? 512 : 4096);
+      // segments of at least 512 records: short rows (a 2,048-record decode row: four
+      // segments) stream in parallel blocks and select as a cluster (34.4 -> 29.1 us)
+      n_seg = tc05_segments(n_rows, L, unit, 512);
       // A row's segments select its top-K together as one thread-block cluster of at most 16
       // blocks; where more segments were planned, 16 per row still keep at least 64 blocks
       // streaming and each segment within shared memory, and save the list merge.
