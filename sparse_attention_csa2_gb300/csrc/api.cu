@@ -253,9 +253,10 @@ AttnParams attn_params(const csa2_attn_args* a, const int32_t* idx) {
   return p;
 }
 
+// attention partials (O, then m and l per tile and head) and each row's rotary cos / sin
 size_t attn_workspace(const csa2_attn_args* a, int n_split) {
   return align_up((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM * 4) +
-         align_up((size_t)a->n_rows * n_split * CSA2_HEADS * 2 * 4);
+         align_up((size_t)a->n_rows * n_split * CSA2_HEADS * 2 * 4) + align_up((size_t)a->n_rows * CSA2_ROPE_DIM * 4);
 }
 
 csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, cudaStream_t s) {
@@ -264,6 +265,7 @@ csa2_status run_attn(const csa2_attn_args* a, const int32_t* idx, uint8_t* ws, c
   Carve c{ws};
   p.part_o = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * CSA2_HEAD_DIM);
   p.part_ml = c.take<float>((size_t)a->n_rows * n_split * CSA2_HEADS * 2);
+  p.rope_cs = c.take<float>((size_t)a->n_rows * CSA2_ROPE_DIM);
   return cuda_status(launch_sparse_attn(p, n_split, s));
 }
 

@@ -397,6 +397,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc05_kernel(const AttnPa
   __syncthreads();
   tc05::fence_after();
   const uint32_t tmem = sh.tmem_base;
+  // one block per row hands its rotary table to the merge
+  if (p.rope_cs != nullptr && blockIdx.y == 0 && tid < kRopeDim) p.rope_cs[(size_t)row * kRopeDim + tid] = sh.cs[tid];
 
   // the query is an input of the step, not of the previous kernel: it is copied and rotated
   // before the wait below
@@ -1304,8 +1306,10 @@ __global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const Att
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int n_items = p.n_rows * kHeads;
+  // items interleaved over the blocks (item = block + gridDim.x * k): few items spread over many
+  // SMs, whose load bandwidth the partials' loads need
 #pragma unroll 1
-  for (int item = blockIdx.x * kCombWarps + (threadIdx.x >> 5); item < n_items; item += gridDim.x * kCombWarps) {
+  for (int item = blockIdx.x + gridDim.x * (threadIdx.x >> 5); item < n_items; item += gridDim.x * kCombWarps) {
     const int row = item / kHeads, h = item % kHeads;
     // tile t of the row: part t / T, tile t % T of that part (one part: T = n_tiles)
     const int T = p.part_tiles > 0 ? p.part_tiles : n_tiles;
@@ -1328,8 +1332,13 @@ __global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const Att
       m = ml.x;
       l = ml.y;
     }
-    float cs_c, cs_s;
-    rope_cs(p.q_pos[row], p.inv_freq[lane], -1.f, &cs_c, &cs_s);
+    float cs_c, cs_s;  // turned back by -position: cos, -sin of the row's angles
+    if (p.rope_cs != nullptr) {
+      cs_c = __ldcg(p.rope_cs + (size_t)row * kRopeDim + lane);
+      cs_s = -__ldcg(p.rope_cs + (size_t)row * kRopeDim + 32 + lane);
+    } else {
+      rope_cs(p.q_pos[row], p.inv_freq[lane], -1.f, &cs_c, &cs_s);
+    }
     const float sk = __ldg(p.sink + h);
     const float M = fmaxf(warp_max(m), sk);
     const float f = m == -INFINITY ? 0.f : __expf(m - M);
@@ -1487,7 +1496,7 @@ cudaError_t launch_attn_merge(const AttnParams& p, int n_tiles, cudaStream_t str
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   const int items = p.n_rows * kHeads;
-  cfg.gridDim = dim3(std::min(device_sm_count(), (items + kCombWarps - 1) / kCombWarps));
+  cfg.gridDim = dim3(std::min(device_sm_count(), items));
   cfg.blockDim = dim3(kCombWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -135,6 +135,9 @@ struct AttnParams {
   double inv_freq[32];        // theta^(-2i/64), i = 0..31 (computed on the host in double)
   float* part_o;              // [n_rows, n_split, 64, 512]
   float* part_ml;             // [n_rows, n_split, 64, 2]
+  // optional [n_rows, 64]: the row's rotary cos (0..31) and sin (32..63) at +q_pos, written by
+  // one tile block per row for the merge (null: the merge computes them)
+  float* rope_cs;
   // a device's share of a record-range split: idx holds global positions; those outside
   // [range_first, range_first + range_count) are skipped, the others index the latents at
   // position - range_first (range_count == 0: no range); skip_window masks the window entries
