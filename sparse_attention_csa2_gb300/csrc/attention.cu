@@ -987,8 +987,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) attn_pipe_kernel(const AttnPa
   constexpr int NH = kPipeNH, HALF = NH / 2, NG = HALF / 8;
   constexpr int QPANEL = NH * 128;
   constexpr int NO = 2 * NH;              // second GEMM's N: P_hi | P_lo
-  constexpr uint32_t kS0 = 4 * NO;        // tensor memory: O in [0, kS0), S^T in [kS0, kS0 + NH)
+  constexpr uint32_t kS0 = 4 * NO;        // tensor memory: O in [0, kS0), two S^T buffers from kS0
   constexpr uint32_t kCols = 512;
+  static_assert(kS0 + 2 * NH <= kCols, "output and two logit buffers fit");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1k(smem_raw);
   uint8_t* qs = smem;                     // q' (nine panels), kept for every tile
@@ -1074,26 +1075,43 @@ __global__ void __launch_bounds__(kPipeThreads, 1) attn_pipe_kernel(const AttnPa
       constexpr uint32_t idesc1 = tc05::idesc_bf16(128, NH);
       constexpr uint32_t idesc2 = tc05::idesc_bf16(128, NO) | (1u << 15) | (1u << 16);
       const uint64_t qd = tc05::sw128_desc(qs_u), pd = sw128_desc_lbo(ps_u, kPBytes, 1024);
+      // S^T(t) = K q'^T, pair c, into logit buffer t & 1 (the caller made sure the pair landed)
+      auto gemm1_pair = [&](int t, int c) {
+        const int slot = (4 * t + c) % kPipeSlots;
+        const uint32_t sc = tmem + kS0 + (uint32_t)(t & 1) * NH;
+        const uint64_t ad = tc05::sw128_desc(ring_u + slot * kPipeSlotBytes);
+        const uint64_t bd = tc05::desc_adv(qd, 2 * c * QPANEL);
+        mma4(sc, ad, bd, idesc1, c > 0);
+        mma4(sc, tc05::desc_adv(ad, kKPanel), tc05::desc_adv(bd, QPANEL), idesc1, true);
+        // the low parts of the rotated query against the rotary panel (the last pair's second)
+        if (c == 3) mma4(sc, tc05::desc_adv(ad, kKPanel), tc05::desc_adv(qd, 8 * QPANEL), idesc1, true);
+      };
+      auto wait_pair = [&](int t, int c) {
+        const int u = 4 * t + c;
+        if (!pipe_wait(&sh.full[u % kPipeSlots], (u / kPipeSlots) & 1, &sh.timeout)) return false;
+        tc05::fence_after();
+        return true;
+      };
+      // tile 0's first GEMM
+#pragma unroll 1
+      for (int c = 0; c < 4 && ok; ++c) {
+        ok = wait_pair(0, c);
+        if (ok) gemm1_pair(0, c);
+      }
+      if (ok) tc05::mma_commit(&sh.s_full);
 #pragma unroll 1
       for (int t = 0; t < n_tiles && ok; ++t) {
-        // S^T = K q'^T, pair by pair
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const int u = 4 * t + c, slot = u % kPipeSlots;
-          if (!pipe_wait(&sh.full[slot], (u / kPipeSlots) & 1, &sh.timeout)) {
-            ok = false;
-            break;
+        // the next tile's first pair (the spare slot) goes in while this tile's softmax runs,
+        // if it has landed (its own logit buffer: the softmax reads buffer t & 1)
+        int next_c = 0;
+        if (t + 1 < n_tiles) {
+          const int u = 4 * (t + 1);
+          if (tc05::mbar_test(&sh.full[u % kPipeSlots], (u / kPipeSlots) & 1)) {
+            tc05::fence_after();
+            gemm1_pair(t + 1, 0);
+            next_c = 1;
           }
-          tc05::fence_after();
-          const uint64_t ad = tc05::sw128_desc(ring_u + slot * kPipeSlotBytes);
-          const uint64_t bd = tc05::desc_adv(qd, 2 * c * QPANEL);
-          mma4(tmem + kS0, ad, bd, idesc1, c > 0);
-          mma4(tmem + kS0, tc05::desc_adv(ad, kKPanel), tc05::desc_adv(bd, QPANEL), idesc1, true);
-          // the low parts of the rotated query against the rotary panel (the last pair's second)
-          if (c == 3) mma4(tmem + kS0, tc05::desc_adv(ad, kKPanel), tc05::desc_adv(qd, 8 * QPANEL), idesc1, true);
         }
-        if (!ok) break;
-        tc05::mma_commit(&sh.s_full);
         // O^T += V^T [P_hi | P_lo]^T once the softmax has written P
         if (!pipe_wait(&sh.p_full, t & 1, &sh.timeout)) {
           ok = false;
@@ -1106,6 +1124,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1) attn_pipe_kernel(const AttnPa
           gemm2_chunk_issue(tmem + NO * c, sw128_desc_lbo(ring_u + slot * kPipeSlotBytes, kKPanel, 1024), pd, idesc2,
                             t > 0);
           tc05::mma_commit(&sh.empty[slot]);
+        }
+        // the rest of the next tile's first GEMM as its pairs land (the slots this GEMM freed)
+        if (t + 1 < n_tiles) {
+#pragma unroll 1
+          for (int c = next_c; c < 4 && ok; ++c) {
+            ok = wait_pair(t + 1, c);
+            if (ok) gemm1_pair(t + 1, c);
+          }
+          // its commit also covers this tile's second GEMM: the softmax of tile t + 1 may
+          // rescale the output and rewrite P once it sees the logits
+          if (ok) tc05::mma_commit(&sh.s_full);
         }
       }
       if (ok) tc05::mma_commit(&sh.o_done);
@@ -1143,7 +1172,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) attn_pipe_kernel(const AttnPa
       float z[HALF];
       if (ok) {
         uint32_t v[HALF];
-        tc05::tmem_ld<HALF>(lane_base + kS0 + (uint32_t)hb, v);
+        tc05::tmem_ld<HALF>(lane_base + kS0 + (uint32_t)(t & 1) * NH + (uint32_t)hb, v);
         tc05::tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < HALF; ++k) z[k] = on ? __uint_as_float(v[k]) * zs : -INFINITY;
