@@ -1,5 +1,6 @@
 // The C ABI of the CSA2 attention step (include/csa2.h): host-side validation, workspace
 // layout, work decomposition and launch sequencing.  Nothing here synchronizes or allocates.
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <cmath>
@@ -83,13 +84,15 @@ csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA
 // Which indexer kernel runs a scan: the tcgen05 decode kernel takes bf16 or FP8 keys read in
 // place, the tcgen05 prefill kernel bf16 keys; other FP8 scans and candidate lists not in runs
 // of 64 records take the warp-MMA scan.
-enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill };
+enum class ScanPath { kWarpMma, kTc05Decode, kTc05Prefill, kTc05Stream };
 
 // cand_run: the candidates come in runs of that many consecutive records (a Reindex pool of
 // whole blocks); runs of a multiple of 64 let the tcgen05 scan load them with TMA.
+// stream_k: the top-K of a FULL decode layer (no block maxima), which the streaming FP8 scan
+// can take; 0 otherwise.
 int tc05_segments(int n_rows, long long L, int unit, long long min_seg = 4096);
 
-ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0) {
+ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0, int stream_k = 0) {
   if (!mma_indexer_available() || tuning(CSA2_TUNE_SCAN_WARP_MMA) != 0 || a->k_dtype == CSA2_MXFP4)
     return ScanPath::kWarpMma;
   if (a->cand != nullptr && !(want_topk && cand_run > 0 && cand_run % 64 == 0)) return ScanPath::kWarpMma;
@@ -97,11 +100,14 @@ ScanPath scan_path(const csa2_index_args* a, bool want_topk, int cand_run = 0) {
   if (!want_topk && a->block_max == nullptr && a->n_seq == 1 && a->n_rows >= 64)
     return fp8 ? ScanPath::kWarpMma : ScanPath::kTc05Prefill;
   if (fp8) {
-    // A tcgen05 block streams FP8 tiles at about a third of the rate it streams bf16 ones, so
-    // the FP8 scan takes it only where its grid is one wave (a second, partial wave of
-    // 16K-record segments costs more than the warp-MMA scan's one wave of longer segments).
+    // The decode kernel keeps every key of a segment in shared memory, one block per SM, so
+    // it takes FP8 rows only where its grid is one wave (a second, partial wave of 16K-record
+    // segments costs more than one wave of longer segments elsewhere).  Longer FULL rows take
+    // the streaming FP8 scan (bounded top-K buffers, two blocks per SM), else the warp-MMA scan.
     const long long L = a->cand != nullptr ? a->L : a->n_records;
-    if ((long long)a->n_rows * tc05_segments(a->n_rows, L, 128) > sm_count()) return ScanPath::kWarpMma;
+    if ((long long)a->n_rows * tc05_segments(a->n_rows, L, 128) > sm_count())
+      return want_topk && stream_k > 0 && a->cand == nullptr && fp8_stream_ok(stream_k) ? ScanPath::kTc05Stream
+                                                                                       : ScanPath::kWarpMma;
   }
   return ScanPath::kTc05Decode;
 }
@@ -117,8 +123,22 @@ int tc05_segments(int n_rows, long long L, int unit, long long min_seg) {
   return n;
 }
 
-cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk, int n_seg, cudaStream_t s) {
-  switch (scan_path(a, want_topk, p.cand_run)) {
+// Segments per row for the streaming FP8 scan: two resident blocks per SM, at most 128 lists
+// per row (the lists merge's table), none shorter than 2,048 records.
+int stream_segments(int n_rows, long long L) {
+  const int forced = tuning(CSA2_TUNE_SCAN_SEGMENTS);
+  if (forced > 0) return forced;
+  long long s = 2LL * sm_count() / (n_rows > 0 ? n_rows : 1);
+  s = std::min(s, std::max(1LL, L / 2048));
+  s = std::min(s, 128LL);
+  return s < 1 ? 1 : (int)s;
+}
+
+cudaError_t launch_scan(ScanParams& p, const csa2_index_args* a, bool want_topk, int n_seg, cudaStream_t s,
+                        int stream_k = 0) {
+  switch (scan_path(a, want_topk, p.cand_run, stream_k)) {
+    case ScanPath::kTc05Stream:
+      return launch_fp8_stream(p, (long long)a->n_seq * a->n_records, n_seg, s);
     case ScanPath::kTc05Prefill: {
       // work items: (8-query tile, share of its key tiles); enough items to balance the
       // persistent grid, none shorter than ~16 key tiles
@@ -510,7 +530,10 @@ static size_t decode_ws(const csa2_decode_args* a, int* n_seg_out) {
     ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
     ic.block_max = nullptr;
     const int cand_run = a->mode == CSA2_MODE_REINDEX ? a->block_size : 0;
-    if (scan_path(&ic, true, cand_run) == ScanPath::kTc05Decode) {
+    const ScanPath path = scan_path(&ic, true, cand_run, a->mode == CSA2_MODE_FULL ? a->K : 0);
+    if (path == ScanPath::kTc05Stream) {
+      n_seg = stream_segments(n_rows, L);
+    } else if (path == ScanPath::kTc05Decode) {
       const int unit = a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128;
       // segments of at least 512 records: short rows (a 2,048-record decode row: four
       // segments) stream in parallel blocks and select as a cluster (34.4 -> 29.1 us)
@@ -632,8 +655,10 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
       ic.cand = a->pool;
       ic.L = a->pool_len;
     }
-    const bool tc05 = scan_path(&ic, true, p.cand_run) == ScanPath::kTc05Decode;
-    if (tc05 && a->mode != CSA2_MODE_FULL_POOL) p.unit = 128;
+    const int stream_k = a->mode == CSA2_MODE_FULL ? a->K : 0;
+    const ScanPath path = scan_path(&ic, true, p.cand_run, stream_k);
+    const bool tc05 = path == ScanPath::kTc05Decode;
+    if ((tc05 && a->mode != CSA2_MODE_FULL_POOL) || path == ScanPath::kTc05Stream) p.unit = 128;
     p.dev_status = at.dev_status;
     const int seg_blocks = p.block_max ? (int)(((ic.n_records + p.unit - 1) / p.unit + n_seg - 1) / n_seg)
                            : p.cand   ? (int)(2 * (((ic.L + p.unit - 1) / p.unit + n_seg - 1) / n_seg))
@@ -647,7 +672,7 @@ csa2_status csa2_fused_decode(const csa2_decode_args* a, void* stream) {
     }
     if (p.cluster_merge) p.seg_keys = nullptr, p.seg_pos = nullptr, p.seg_cnt = nullptr, p.seg_thr = nullptr;
     mark(0);  // stage 0: the indexer scan kernel alone
-    e = launch_scan(p, &ic, true, n_seg, s);
+    e = launch_scan(p, &ic, true, n_seg, s, stream_k);
     if (e != cudaSuccess) return CSA2_ECUDA;
     mark(1);
     if (n_seg > 1 && !fused_merge && !p.cluster_merge) {
@@ -1024,7 +1049,8 @@ int32_t csa2_fused_decode_launch_count(const csa2_decode_args* a) {
     ic.cand = a->mode == CSA2_MODE_REINDEX ? a->pool : nullptr;
     ic.block_max = nullptr;
     if (a->mode == CSA2_MODE_REINDEX) ic.L = a->pool_len;
-    const bool tc05 = scan_path(&ic, true, a->mode == CSA2_MODE_REINDEX ? a->block_size : 0) == ScanPath::kTc05Decode;
+    const bool tc05 = scan_path(&ic, true, a->mode == CSA2_MODE_REINDEX ? a->block_size : 0,
+                                a->mode == CSA2_MODE_FULL ? a->K : 0) == ScanPath::kTc05Decode;
     const int unit = a->mode == CSA2_MODE_FULL_POOL ? a->block_size : 128;
     const int seg_blocks =
         a->mode == CSA2_MODE_FULL_POOL ? (int)(((ic.n_records + unit - 1) / unit + n_seg - 1) / n_seg)

@@ -41,6 +41,48 @@ __device__ __forceinline__ void report_timeout(int* flag, int32_t* dev_status) {
   if (dev_status != nullptr) atomicExch(dev_status, (int)CSA2_ETIMEOUT);
 }
 
+// E4M3 terms of q^I for the FP8 decode scans (construction in the comment below): thread et
+// (0..255) takes head et / 8, dims 16 (et % 8) .. +15, and writes its three terms into the B
+// operand qs (row 32 * term + head, 128 bytes per row, 128-byte swizzle); the thread with
+// et % 8 == 0 stores the head's power-of-two exponent in qexp[head].
+__device__ __forceinline__ void fp8_q_terms(const void* q_idx, int row, int et, uint8_t* qs, int* qexp) {
+  const int h = et >> 3, c = et & 7;
+  const uint4* src = reinterpret_cast<const uint4*>(q_idx) + ((size_t)row * 32 + h) * 16 + 2 * c;
+  const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+  const uint32_t qw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx = max(mx, max(qw[k] & 0x7fffu, (qw[k] >> 16) & 0x7fffu));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  // largest magnitude 2^ex * m, m in [1, 2): scale by 2^(7 - ex) into [128, 256)
+  const int ex = (int)((mx >> 7) & 0xffu) - 127;
+  const int e = mx == 0u ? 0 : min(126, max(-126, 7 - ex));
+  const float f = __int_as_float((e + 127) << 23);
+  uint32_t term[3][4];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float x[2] = {__uint_as_float(qw[k] << 16) * f, __uint_as_float(qw[k] & 0xffff0000u) * f};
+#pragma unroll
+    for (int tm = 0; tm < 3; ++tm) {
+      const uint16_t b2 = __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hb = e4m3x2_to_f16x2(b2);
+      const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hb));
+      x[0] = (x[0] - back.x) * 16.f;  // exact: the residual has at most 4 significant bits
+      x[1] = (x[1] - back.y) * 16.f;
+      if (k & 1) term[tm][k >> 1] |= (uint32_t)b2 << 16;
+      else term[tm][k >> 1] = b2;
+    }
+  }
+#pragma unroll
+  for (int tm = 0; tm < 3; ++tm) {
+    const int n = 32 * tm + h;  // B row; 16-byte chunk c sits at slot c ^ (n & 7)
+    *reinterpret_cast<uint4*>(qs + n * 128 + ((c ^ (n & 7)) << 4)) =
+        make_uint4(term[tm][0], term[tm][1], term[tm][2], term[tm][3]);
+  }
+  if (c == 0) qexp[h] = e;
+}
+
 // ===================================================================================== decode
 // bf16 keys: TMA tiles of 128 records x 256 bytes; D[128 x 32] += K_tile * Q^T in eight
 // kind::f16 K-steps of 16.
@@ -623,42 +665,7 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
     for (int h = 0; h < 32; ++h) w[h] = __ldg(p.w + (size_t)row * kIdxHeads + h);
     bool dead = false;
     if (FP8 && n_tiles > 0) {
-      // E4M3 terms of q^I: thread (head h, chunk c) takes dims 16c .. 16c+15 of head h
-      const int et = tid - kDecEpiFirst * 32, h = et >> 3, c = et & 7;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_idx) + ((size_t)row * 32 + h) * 16 + 2 * c;
-      const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-      const uint32_t qw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      uint32_t mx = 0u;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx = max(mx, max(qw[k] & 0x7fffu, (qw[k] >> 16) & 0x7fffu));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      // largest magnitude 2^ex * m, m in [1, 2): scale by 2^(7 - ex) into [128, 256)
-      const int ex = (int)((mx >> 7) & 0xffu) - 127;
-      const int e = mx == 0u ? 0 : min(126, max(-126, 7 - ex));
-      const float f = __int_as_float((e + 127) << 23);
-      uint32_t term[3][4];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float x[2] = {__uint_as_float(qw[k] << 16) * f, __uint_as_float(qw[k] & 0xffff0000u) * f};
-#pragma unroll
-        for (int tm = 0; tm < 3; ++tm) {
-          const uint16_t b2 = __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hb = e4m3x2_to_f16x2(b2);
-          const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hb));
-          x[0] = (x[0] - back.x) * 16.f;  // exact: the residual has at most 4 significant bits
-          x[1] = (x[1] - back.y) * 16.f;
-          if (k & 1) term[tm][k >> 1] |= (uint32_t)b2 << 16;
-          else term[tm][k >> 1] = b2;
-        }
-      }
-#pragma unroll
-      for (int tm = 0; tm < 3; ++tm) {
-        const int n = 32 * tm + h;  // B row; 16-byte chunk c sits at slot c ^ (n & 7)
-        *reinterpret_cast<uint4*>(qs + n * 128 + ((c ^ (n & 7)) << 4)) =
-            make_uint4(term[tm][0], term[tm][1], term[tm][2], term[tm][3]);
-      }
-      if (c == 0) bars.qexp[h] = e;
+      fp8_q_terms(p.q_idx, row, tid - kDecEpiFirst * 32, qs, bars.qexp);
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the MMA reads B through the async proxy
       __syncwarp();
       if (lane == 0) tc05::mbar_arrive(&bars.qready);
@@ -951,6 +958,296 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
   if (warp == 1) {
     tc05::fence_after();
     tc05::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ============================================================================ FP8 decode, streaming
+// FP8 decode rows too long for one wave of the decode kernel's segments (every key of a
+// segment stays in that kernel's shared memory): the same tile pipeline (TMA ring, four
+// kind::f8f6f4 MMAs per 128-record tile against the E4M3 terms of q^I, two accumulators in
+// tensor memory, two groups of four epilogue warps on alternate tiles), but the epilogue feeds
+// the exact streaming top-K engine (select.cuh: per-warp buffers of about K entries, entries
+// below the running K-th key dropped on arrival) instead of keeping every key.  A block then
+// needs about 110 KB of shared memory and 256 tensor-memory columns, so two blocks share an
+// SM: one block streams FP8 tiles at about two thirds of an SM's share of the HBM rate (its
+// copy thread, MMA thread and epilogue warps form one dependent chain per tile and contend
+// for the SM's issue slots), two blocks per SM interleave two such chains.
+// Each block writes its segment's list (at most K entries in position order, and its K-th
+// key) for the lists merge, or the row's indices when the row is a single segment.
+constexpr int kStrStages = 3;
+constexpr int kStrTile = kTileKeys * 128;  // 16 KB: 128 records x 128 E4M3 dims
+constexpr int kStrThreads = 12 * 32;       // warp 0 TMA, warp 1 MMA + tensor memory, warps 4..11 epilogue
+constexpr int kStrEpiFirst = 4;
+constexpr int kStrEpiWarps = 8;
+constexpr int kStrQBytes = 96 * 128;       // B: the three E4M3 terms of the 32 heads
+constexpr uint32_t kStrAccCols = 128;      // columns per accumulator (96 used)
+constexpr uint32_t kStrTmemCols = 256;
+constexpr int kStrRound = kRoundEntries / 32;  // tiles per epilogue warp between engine checks
+
+struct StrBars {
+  alignas(16) float w[32];  // head weights times the inverse of q^I's head scale
+  uint64_t full[kStrStages], empty[kStrStages], tfull[2], tempty[2], qready;
+  uint32_t tmem_base;
+  int timeout;
+  int issued;    // tiles whose TMA loads were issued
+  int consumed;  // tiles whose MMAs were issued
+  int drained;   // tiles whose accumulators the epilogue read
+  int bitmap;    // the survivors are placed through a position bitmap in the idle ring
+  int qexp[32];  // power-of-two exponent applied to each head of q^I
+};
+
+__host__ __device__ constexpr size_t str_align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+size_t str_smem_bytes(int K) {
+  return 1024 + (size_t)kStrStages * kStrTile + kStrQBytes + str_align16(sizeof(StrBars)) +
+         str_align16(sizeof(EngShared)) + (size_t)kStrEpiWarps * (K + kRoundEntries) * 8 + (size_t)K * 8;
+}
+
+__global__ void __launch_bounds__(kStrThreads, 2)
+    idx_fp8_stream_kernel(const __grid_constant__ CUtensorMap tmK, const ScanParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ring = smem;
+  uint8_t* qs = ring + kStrStages * kStrTile;
+  StrBars& bars = *reinterpret_cast<StrBars*>(qs + kStrQBytes);
+  uint8_t* rest = reinterpret_cast<uint8_t*>(&bars) + str_align16(sizeof(StrBars));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = blockIdx.y, seg = blockIdx.x, n_seg = gridDim.x;
+  Engine<kStrEpiWarps> eng;  // the epilogue warps (named barrier 1)
+  eng.sh = reinterpret_cast<EngShared*>(rest);
+  eng.cap = p.K + kRoundEntries;
+  eng.keys = reinterpret_cast<uint32_t*>(rest + str_align16(sizeof(EngShared)));
+  eng.js = reinterpret_cast<int32_t*>(eng.keys + kStrEpiWarps * eng.cap);
+  eng.out_key = reinterpret_cast<uint32_t*>(eng.js + kStrEpiWarps * eng.cap);
+  eng.out_j = reinterpret_cast<int32_t*>(eng.out_key + p.K);
+  eng.bar_id = 1;
+  eng.tid = tid - kStrEpiFirst * 32;
+
+  // ---- set-up that reads no input (overlaps the previous kernel's tail)
+  if (tid == 0) {
+    for (int s = 0; s < kStrStages; ++s) {
+      tc05::mbar_init(&bars.full[s], 1);
+      tc05::mbar_init(&bars.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc05::mbar_init(&bars.tfull[a], 1);
+      tc05::mbar_init(&bars.tempty[a], 4);  // one arrive per warp of the draining group
+    }
+    tc05::mbar_init(&bars.qready, kStrEpiWarps);
+    bars.timeout = 0;
+    bars.issued = bars.consumed = bars.drained = 0;
+    tc05::fence_barrier_init();
+  }
+  if (warp == 1) tc05::tmem_alloc(&bars.tmem_base, kStrTmemCols);
+
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  const int b = p.seq_of_row[row];
+  const long long L_row = max(0LL, min((long long)p.n_visible[row], p.N));
+  long long u0, u1;
+  split_range((L_row + kTileKeys - 1) / kTileKeys, n_seg, seg, u0, u1);
+  const long long e0 = u0 * kTileKeys, e1 = min(u1 * kTileKeys, L_row);
+  const int n_tiles = e1 > e0 ? (int)((e1 - e0 + kTileKeys - 1) / kTileKeys) : 0;
+  const int seg_len = e1 > e0 ? (int)(e1 - e0) : 0;
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      const long long y0 = (long long)b * p.N + e0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStrStages;
+        if (!tc05::mbar_wait(&bars.empty[s], ((t / kStrStages) & 1) ^ 1)) {
+          report_timeout(&bars.timeout, p.dev_status);
+          break;
+        }
+        tc05::mbar_expect_tx(&bars.full[s], kStrTile);
+        tc05::tma_load_2d(ring + s * kStrTile, &tmK, 0, (int)(y0 + (long long)t * kTileKeys), &bars.full[s]);
+        bars.issued = t + 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idesc = tc05::idesc_e4m3(128, 96);
+      bool ok = tc05::mbar_wait(&bars.qready, 0);
+      const uint64_t qd = tc05::sw128_desc(smem_u32(qs));
+      const uint64_t ring_d = tc05::sw128_desc(smem_u32(ring));
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int s = t % kStrStages, a = t & 1;
+        if (!tc05::mbar_wait(&bars.full[s], (t / kStrStages) & 1) ||
+            !tc05::mbar_wait(&bars.tempty[a], ((t >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc05::fence_after();
+        const uint64_t ad = tc05::desc_adv(ring_d, s * kStrTile);
+        const uint32_t d_t = tmem + (uint32_t)a * kStrAccCols;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc05::mma_e4m3(d_t, tc05::desc_adv(ad, kk * 32), tc05::desc_adv(qd, kk * 32), idesc, kk > 0);
+        tc05::mma_commit(&bars.empty[s]);
+        tc05::mma_commit(&bars.tfull[a]);
+        bars.consumed = t + 1;
+      }
+      if (!ok) report_timeout(&bars.timeout, p.dev_status);
+    }
+    __syncwarp();
+  } else if (warp >= kStrEpiFirst) {
+    // ---------------------------------------------------------------- epilogue + top-K
+    // group 0 drains the even tiles (accumulator 0), group 1 the odd ones; each warp's
+    // records arrive in ascending position order, as the engine's buffers require
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int grp = (warp - kStrEpiFirst) >> 2;
+    eng_init(eng);
+    bool dead = false;
+    if (n_tiles > 0) {
+      fp8_q_terms(p.q_idx, row, eng.tid, qs, bars.qexp);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the MMA reads B through the async proxy
+      __syncwarp();
+      if (lane == 0) tc05::mbar_arrive(&bars.qready);
+      dead = !tc05::mbar_wait(&bars.qready, 0);
+      if (dead && lane == 0) report_timeout(&bars.timeout, p.dev_status);
+      // the heads of q^I were scaled by 2^qexp[h]: the weights take the inverse factor (kept
+      // in shared memory, read as broadcasts: registers are scarce at two blocks per SM)
+      if (eng.tid < 32)
+        bars.w[eng.tid] = __ldg(p.w + (size_t)row * kIdxHeads + eng.tid) * __int_as_float((127 - bars.qexp[eng.tid]) << 23);
+      eng.sync();
+    }
+    const float4* w4 = reinterpret_cast<const float4*>(bars.w);
+    const float* kscale = p.k_scale + (size_t)b * p.N + e0;
+    // the scale of this thread's record in the group's next tiles, loaded kScalePre tiles ahead
+    constexpr int kScalePre = 4;
+    auto scale_of = [&](int pr) -> float {
+      const int jl = (2 * pr + grp) * kTileKeys + 32 * quarter + lane;
+      return jl < seg_len ? __ldg(kscale + jl) : 1.f;
+    };
+    float kpre[kScalePre];
+#pragma unroll
+    for (int i = 0; i < kScalePre; ++i) kpre[i] = scale_of(i);
+    const int n_pairs = (n_tiles + 1) / 2;
+    int cnt = 0;
+    uint32_t thr = 0u;
+    for (int pr = 0; pr < n_pairs; ++pr) {
+      const int t = 2 * pr + grp, a = grp;
+      const bool have = t < n_tiles;
+      const int jl = t * kTileKeys + 32 * quarter + lane;  // record index within the segment
+      const float ksc = kpre[0];
+#pragma unroll
+      for (int i = 0; i + 1 < kScalePre; ++i) kpre[i] = kpre[i + 1];
+      kpre[kScalePre - 1] = scale_of(pr + kScalePre);
+      if (have && !dead && !tc05::mbar_wait(&bars.tfull[a], pr & 1)) {
+        dead = true;
+        if (lane == 0) report_timeout(&bars.timeout, p.dev_status);
+      }
+      float sc = 0.f;
+      if (have && !dead) {
+        tc05::fence_after();
+        const uint32_t d_t = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)a * kStrAccCols;
+        // D1 + (D2 + D3 / 16) / 16 per head, eight heads at a time
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t v1[8], v2[8], v3[8];
+          tc05::tmem_ld8(d_t + 8 * c8, v1);
+          tc05::tmem_ld8(d_t + 32 + 8 * c8, v2);
+          tc05::tmem_ld8(d_t + 64 + 8 * c8, v3);
+          tc05::tmem_ld_wait();
+          const float4 wa = w4[2 * c8], wb = w4[2 * c8 + 1];
+          const float wc[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x = fmaf(fmaf(__uint_as_float(v3[i]), 0.0625f, __uint_as_float(v2[i])), 0.0625f,
+                                 __uint_as_float(v1[i]));
+            sc = fmaf(wc[i], fmaxf(x * ksc, 0.f), sc);
+          }
+        }
+        tc05::fence_before();
+        __syncwarp();
+        if (lane == 0) tc05::mbar_arrive(&bars.tempty[a]);
+        if (warp == kStrEpiFirst + 4 * grp && lane == 0) atomicMax(&bars.drained, t + 1);
+      }
+      const bool valid = have && !dead && jl < seg_len;
+      eng_append(eng, cnt, thr, valid, score_key(sc), (int32_t)(e0 + jl));
+      if (pr % kStrRound == kStrRound - 1 || pr == n_pairs - 1) thr = eng_check(eng, p.K, cnt);
+    }
+    // ---- the segment's K best, in position order
+    constexpr int NT = kStrEpiWarps * 32;
+    if (lane == 0) eng.sh->warp_cnt[eng.warp()] = cnt;
+    eng.sync();
+    eng_select(eng, p.K);
+    uint32_t* thr_out = n_seg > 1 ? p.seg_thr + (size_t)row * n_seg + seg : nullptr;
+    // Survivors' ranks through a bitmap of their positions in the segment and a prefix over
+    // its words (the ring is idle once every tile was drained; after a timeout copies may
+    // still land there, and segments longer than the bitmap rank by binary search instead).
+    constexpr int kBitmapWords = kStrStages * kStrTile / 8;  // bitmap, then its word prefixes
+    const int nw = (seg_len + 31) / 32;
+    if (eng.tid == 0) bars.bitmap = !bars.timeout && nw <= kBitmapWords;
+    eng.sync();
+    int n;
+    if (bars.bitmap) {
+      uint32_t* bm = reinterpret_cast<uint32_t*>(ring);
+      int32_t* pre = reinterpret_cast<int32_t*>(bm + nw);
+      const int w = eng.warp(), mycnt = eng.sh->warp_cnt[w];
+      const uint32_t* gk = eng.keys + w * eng.cap;
+      const int32_t* gj = eng.js + w * eng.cap;
+      for (int i = eng.tid; i < nw; i += NT) bm[i] = 0u;
+      eng.sync();
+      for (int i = lane; i < mycnt; i += 32) {
+        const int off = (int)(gj[i] - e0);
+        atomicOr(&bm[off >> 5], 1u << (off & 31));
+      }
+      eng.sync();
+      const int per = (nw + NT - 1) / NT, w0 = min(nw, eng.tid * per), w1 = min(nw, w0 + per);
+      int local = 0;
+      for (int i = w0; i < w1; ++i) local += __popc(bm[i]);
+      int total_bits;
+      int before = eng.scan(local, &total_bits);
+      for (int i = w0; i < w1; ++i) {
+        pre[i] = before;
+        before += __popc(bm[i]);
+      }
+      eng.sync();
+      for (int i = lane; i < mycnt; i += 32) {
+        const int off = (int)(gj[i] - e0);
+        const int r = pre[off >> 5] + __popc(bm[off >> 5] & ((1u << (off & 31)) - 1u));
+        eng.out_key[r] = gk[i];
+        eng.out_j[r] = gj[i];
+      }
+      n = total_bits;
+      if (eng.tid == 0 && thr_out) *thr_out = n >= p.K ? eng.sh->thr : 0u;
+      eng.sync();
+    } else {
+      n = eng_rank(eng, p.K, thr_out);
+    }
+    if (n_seg == 1) {
+      int32_t* out = p.idx + (size_t)row * p.K;
+      for (int i = eng.tid; i < p.K; i += NT) out[i] = i < n ? eng.out_j[i] : -1;
+    } else {
+      const size_t o = ((size_t)row * n_seg + seg) * p.K;
+      for (int i = eng.tid; i < n; i += NT) {
+        p.seg_keys[o + i] = eng.out_key[i];
+        p.seg_pos[o + i] = eng.out_j[i];
+      }
+      if (eng.tid == 0) p.seg_cnt[(size_t)row * n_seg + seg] = n;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (bars.timeout && tid == 0) {
+    // drain loads and MMAs still in flight (bounded), then free tensor memory
+    for (int t = max(0, bars.issued - kStrStages); t < bars.issued; ++t)
+      tc05::mbar_wait(&bars.full[t % kStrStages], (t / kStrStages) & 1);
+    for (int t = max(0, bars.drained - 1); t < bars.consumed; ++t)
+      tc05::mbar_wait(&bars.tfull[t & 1], (t >> 1) & 1);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc05::fence_after();
+    tc05::tmem_dealloc(tmem, kStrTmemCols);
   }
 }
 
@@ -1368,6 +1665,73 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
   if (fp8 && p.k_scale == nullptr) return cudaErrorInvalidValue;
   return fp8 ? launch_mma_decode_t<true>(p, n_seq_rows, n_seg, max_seg_blocks, stream)
              : launch_mma_decode_t<false>(p, n_seq_rows, n_seg, max_seg_blocks, stream);
+}
+
+// FP8 streaming decode scan: usable for this K where two blocks fit on an SM.
+bool fp8_stream_ok(int K) {
+  if (K < 1 || K > kEngMaxK) return false;
+  struct Entry {
+    int dev, K;
+    bool ok;
+  };
+  static Entry cache[16];
+  static int n_cache = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].dev == dev && cache[i].K == K) return cache[i].ok;
+  bool ok = false;
+  const size_t smem = str_smem_bytes(K);
+  // The occupancy query reports one block per SM for every kernel that allocates tensor memory
+  // whatever its resources, so the fit of two blocks is checked here from the resources
+  // themselves (tensor memory: two blocks of 256 of the SM's 512 columns).
+  cudaFuncAttributes fa{};
+  int smem_sm = 0, reserved = 0, regs_sm = 0;
+  if (cudaFuncSetAttribute(idx_fp8_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(idx_fp8_stream_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess &&
+      cudaFuncGetAttributes(&fa, idx_fp8_stream_kernel) == cudaSuccess &&
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) == cudaSuccess) {
+    const size_t block_smem = smem + fa.sharedSizeBytes + (size_t)reserved;
+    const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp in units of 256
+    ok = 2 * block_smem <= (size_t)smem_sm && 2 * warp_regs * (kStrThreads / 32) <= regs_sm;
+  }
+  cudaGetLastError();
+  cache[n_cache % 16] = Entry{dev, K, ok};
+  if (n_cache < 16) ++n_cache;
+  return ok;
+}
+
+cudaError_t launch_fp8_stream(const ScanParams& p, long long n_seq_rows, int n_seg, cudaStream_t stream) {
+  if (p.n_rows == 0) return cudaSuccess;
+  if (p.K < 1 || p.K > kEngMaxK || p.k_scale == nullptr || p.cand != nullptr || p.block_max != nullptr ||
+      p.scores != nullptr || (n_seg > 1 && (p.seg_keys == nullptr || p.seg_pos == nullptr || p.seg_cnt == nullptr ||
+                                            p.seg_thr == nullptr)))
+    return cudaErrorInvalidValue;
+  CUtensorMap tmK;
+  if (!make_tmap_u8(&tmK, p.k_idx, (unsigned long long)n_seq_rows, kTileKeys)) return cudaErrorInvalidValue;
+  const size_t smem = str_smem_bytes(p.K);
+  cudaError_t e = cudaFuncSetAttribute(idx_fp8_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // programmatic dependent launch: the set-up overlaps the previous kernel in the stream
+  cudaLaunchAttribute attr[1] = {};
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_seg, p.n_rows);
+  cfg.blockDim = dim3(kStrThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, idx_fp8_stream_kernel, tmK, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 size_t mma_prefill_smem_bytes() { return 1024 + (size_t)kPreStages * kKeyTile + 2 * kPreQHalf + sizeof(PreBars); }

@@ -72,6 +72,10 @@ cudaError_t launch_mma_decode(const ScanParams& p, long long n_seq_rows, int n_s
                               cudaStream_t stream);
 cudaError_t launch_mma_prefill(const ScanParams& p, int n_ctas, int n_parts, cudaStream_t stream);
 cudaError_t launch_index_scan(const ScanParams& p, int fmt, bool gather, int n_seg, cudaStream_t stream);
+// tcgen05 FP8 decode scan with the streaming top-K engine (two blocks per SM): FULL rows of
+// any length, top-K of at most kEngMaxK, no block maxima, candidates or scores.
+bool fp8_stream_ok(int K);
+cudaError_t launch_fp8_stream(const ScanParams& p, long long n_seq_rows, int n_seg, cudaStream_t stream);
 
 // Streaming top-K over per-row entry streams (scores, or the lists of earlier segments).
 struct FeedParams {

@@ -275,14 +275,11 @@ __device__ __forceinline__ uint32_t eng_check(const Engine<NW>& e, int k, int& c
   return thr;
 }
 
-// Final select; the survivors, sorted by entry index, go to out_key / out_j [0..n) and n is
-// returned.  *thr_out gets the k-th key when k survive, else 0 (every dropped entry has a
-// key <= it, and the row's k-th key is at least it).  k <= kEngMaxK.
+// Places the survivors of a select, sorted by entry index, in out_key / out_j [0..n) and
+// returns n.  *thr_out gets the k-th key when k survive, else 0 (every dropped entry has a
+// key <= it, and the row's k-th key is at least it).
 template <int NW>
-__device__ int eng_finish(const Engine<NW>& e, int k, int cnt, uint32_t* thr_out) {
-  if (e.lane() == 0) e.sh->warp_cnt[e.warp()] = cnt;
-  e.sync();
-  eng_select(e, k);
+__device__ int eng_rank(const Engine<NW>& e, int k, uint32_t* thr_out) {
   int total = 0;
 #pragma unroll
   for (int i = 0; i < NW; ++i) total += e.sh->warp_cnt[i];
@@ -313,6 +310,15 @@ __device__ int eng_finish(const Engine<NW>& e, int k, int cnt, uint32_t* thr_out
   if (e.tid == 0 && thr_out) *thr_out = total >= k ? e.sh->thr : 0u;
   e.sync();
   return total;
+}
+
+// Final select, then eng_rank.  k <= kEngMaxK.
+template <int NW>
+__device__ int eng_finish(const Engine<NW>& e, int k, int cnt, uint32_t* thr_out) {
+  if (e.lane() == 0) e.sh->warp_cnt[e.warp()] = cnt;
+  e.sync();
+  eng_select(e, k);
+  return eng_rank(e, k, thr_out);
 }
 
 // Balanced split of [0, n) into `parts` contiguous ranges; range `i`.

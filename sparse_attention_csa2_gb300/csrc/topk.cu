@@ -140,10 +140,11 @@ __global__ void __launch_bounds__(kFeedThreads, 1) topk_feed_kernel(const FeedPa
 constexpr int kMergeWarps = 12;
 constexpr int kMergeThreads = kMergeWarps * 32;
 constexpr int kMergeMaxCta = 8;
+constexpr int kMergeMaxLists = 128;  // lists (segments) per row
 
 struct MergeShared {
-  int cnt[64];
-  uint32_t thr[64];
+  int cnt[kMergeMaxLists];
+  uint32_t thr[kMergeMaxLists];
   uint32_t kext[2 + 2 * kMergeMaxCta];  // this block's extremes; block 0: every block's
 };
 
@@ -653,7 +654,7 @@ cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream) {
   const int n_cta = std::min(kMergeMaxCta, std::max(2, p.in_seg));
   const int per = (p.in_seg + n_cta - 1) / n_cta;
   const size_t smem = merge_smem_bytes(per, p.in_K, p.K);
-  if (p.in_seg > 64 || p.K > CSA2_MAX_TOPK || per * p.in_K >= 65536 || smem > 160u * 1024u)
+  if (p.in_seg > kMergeMaxLists || p.K > CSA2_MAX_TOPK || per * p.in_K >= 65536 || smem > 160u * 1024u)
     return launch_topk_feed(p, true, 1, stream);  // beyond the staged segment table or shared memory
   cudaError_t e = cudaFuncSetAttribute(lists_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -193,6 +193,43 @@ def test_fused_full_gauss():
     assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
 
 
+@pytest.mark.parametrize("mode", ["grid", "gauss"])
+@pytest.mark.parametrize("forced_seg,B,N,rows", [
+    (40, 4, 50_000, [50_000, 49_999, 7_777, 300]),  # two waves of segments: lists, then the merge
+    (0, 160, 3_000, None),                          # more rows than SMs: one segment per row
+])
+def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows):
+    """FP8 keys over more work than one wave of the decode kernel's segments (each segment's
+    keys kept in shared memory, one block per SM): the FULL layer takes the streaming FP8
+    scan (per-warp top-K buffers, two blocks per SM), then the lists merge when a row has
+    several segments.  Forcing 40 segments on 4 rows makes such a grid at a size the oracle
+    finishes quickly; a 300-record row leaves most of its segments empty.  Grid mode: indices
+    bit-exact; Gaussian mode: near-tie swaps only (none on these seeds)."""
+    _cuda()
+    inp = small("long_decode", seed=21, mode=mode, B=B, N=N)
+    if rows is not None:
+        set_rows(inp, rows)
+    if forced_seg:
+        S.set_tuning(S.TUNE_SCAN_SEGMENTS, forced_seg)
+    try:
+        dv = synth.to_device(inp)
+        with torch.profiler.profile(activities=[torch.profiler.ProfilerActivity.CUDA]) as prof:
+            g = gpu_group(dv)
+            torch.cuda.synchronize()
+    finally:
+        S.reset_tuning()
+    kernels = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    if kernels:  # (empty when the profiler cannot trace kernels on this machine)
+        assert any("idx_fp8_stream_kernel" in k for k in kernels), sorted(set(kernels))
+    ref = O.csa2_group(inp)
+    idx = g[0].idx.cpu().numpy()
+    if mode == "grid":
+        assert np.array_equal(idx, ref[0]["idx"])
+    else:
+        assert check_idx_near_ties(idx, ref[0]["idx"], ref[0]["scores"], score_bound(inp, 0)) == 0
+    assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
+
+
 @pytest.mark.parametrize("mode,key_fmt", [("grid", "bf16"), ("gauss", "bf16"), ("grid", "fp8"), ("gauss", "fp8")])
 def test_fused_hierarchical_group(mode, key_fmt):
     """FULL_POOL -> 3 x REINDEX -> 2 x REUSE.  Grid mode: pool and every layer's indices
