@@ -1171,7 +1171,9 @@ __global__ void __launch_bounds__(kStrThreads, 2)
       }
       const bool valid = have && !dead && jl < seg_len;
       eng_append(eng, cnt, thr, valid, score_key(sc), (int32_t)(e0 + jl));
-      if (pr % kStrRound == kStrRound - 1 || pr == n_pairs - 1) thr = eng_check(eng, p.K, cnt);
+      // (a buffer near capacity: one-pass prune, the exact select only when that leaves too
+      // little room; the stream waits on the epilogue meanwhile)
+      if (pr % kStrRound == kStrRound - 1 || pr == n_pairs - 1) thr = eng_check_fast(eng, p.K, cnt);
     }
     // ---- the segment's K best, in position order
     constexpr int NT = kStrEpiWarps * 32;

@@ -259,6 +259,100 @@ __device__ __noinline__ void eng_select(const Engine<NW> e, int k) {
   e.sync();
 }
 
+// Shrinks the group's buffers with one histogram pass instead of eng_select's exact passes:
+// over the 8 highest bits where the keys differ, the digit holding the k-th best key is found
+// and every entry whose digit is below it is dropped (at least k entries lie at or above that
+// digit's lower edge T, so every dropped entry ranks behind k others).  sh->thr becomes T, a
+// valid append threshold (the exact k-th key is at least T).  Returns whether every buffer
+// now has room for a round; when not (a crowded digit, or keys all equal) the caller selects
+// exactly.  All threads of the group must call it.
+template <int NW>
+__device__ __noinline__ bool eng_prune(const Engine<NW> e, int k) {
+  EngShared& s = *e.sh;
+  const int t = e.tid, ln = e.lane(), w = e.warp();
+  const int mycnt = s.warp_cnt[w];
+  uint32_t* kb = e.keys + w * e.cap;
+  int32_t* jb = e.js + w * e.cap;
+  uint32_t k_and = 0xffffffffu, k_or = 0u;
+  for (int i = ln; i < mycnt; i += 32) {
+    k_and &= kb[i];
+    k_or |= kb[i];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    k_and &= __shfl_xor_sync(0xffffffffu, k_and, o);
+    k_or |= __shfl_xor_sync(0xffffffffu, k_or, o);
+  }
+  if (t == 0) {
+    s.all_and = 0xffffffffu;
+    s.all_or = 0u;
+  }
+  for (int i = t; i < 256; i += NW * 32) s.hist[i] = 0;
+  e.sync();
+  if (ln == 0 && mycnt > 0) {
+    atomicAnd(&s.all_and, k_and);
+    atomicOr(&s.all_or, k_or);
+  }
+  e.sync();
+  const uint32_t diff = s.all_and ^ s.all_or;
+  if (diff == 0u) {  // every key equal: only the indices can decide
+    e.sync();
+    return false;
+  }
+  const int hi = 31 - __clz(diff), lo = hi >= 7 ? hi - 7 : 0;
+  const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;  // hi - lo <= 7
+  for (int base = 0; base < mycnt; base += 32) {
+    const int i = base + ln;
+    warp_hist_add(s.hist, i < mycnt ? (int)((kb[i] >> lo) & dmask) : -1);
+  }
+  e.sync();
+  eng_pick_digit(e, k, true);
+  const uint32_t above = hi == 31 ? 0u : ~((2u << hi) - 1u);  // bits shared by every key
+  const uint32_t T = (s.all_and & above) | (static_cast<uint32_t>(s.sel_digit) << lo);
+  int wr = 0;
+  for (int base = 0; base < mycnt; base += 32) {
+    const int i = base + ln;
+    const bool in = i < mycnt;
+    const uint32_t key = in ? kb[i] : 0u;
+    const int32_t j = in ? jb[i] : 0;
+    const bool keep = in && key >= T;
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int o = wr + __popc(km & lanemask_lt());
+      kb[o] = key;
+      jb[o] = j;
+    }
+    wr += __popc(km);
+    __syncwarp();
+  }
+  e.sync();
+  if (ln == 0) s.warp_cnt[w] = wr;
+  if (t == 0) s.thr = max(s.thr, T);
+  e.sync();
+  bool room = true;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) room &= s.warp_cnt[i] <= e.cap - kRoundEntries;
+  e.sync();
+  return room;
+}
+
+// eng_check that first tries the one-pass prune (eng_prune) when some buffer could overflow
+// before the next check, and selects exactly only when that leaves too little room.  Returns
+// the threshold and refreshes `cnt`.
+template <int NW>
+__device__ __forceinline__ uint32_t eng_check_fast(const Engine<NW>& e, int k, int& cnt) {
+  if (e.lane() == 0) e.sh->warp_cnt[e.warp()] = cnt;
+  e.sync();
+  bool need = false;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) need |= e.sh->warp_cnt[i] > e.cap - kRoundEntries;
+  if (need && !eng_prune(e, k)) eng_select(e, k);  // uniform: every thread read the same counts
+  cnt = e.sh->warp_cnt[e.warp()];
+  const uint32_t thr = e.sh->thr;
+  e.sync();
+  return thr;
+}
+
 // Publishes the warp counts and selects when some buffer could overflow before the next
 // check.  Returns the (possibly raised) threshold and refreshes `cnt`.
 template <int NW>

@@ -193,7 +193,7 @@ def test_fused_full_gauss():
     assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
 
 
-@pytest.mark.parametrize("mode", ["grid", "gauss"])
+@pytest.mark.parametrize("mode", ["grid", "gauss", "ties"])
 @pytest.mark.parametrize("forced_seg,B,N,rows", [
     (40, 4, 50_000, [50_000, 49_999, 7_777, 300]),  # two waves of segments: lists, then the merge
     (0, 160, 3_000, None),                          # more rows than SMs: one segment per row
@@ -204,9 +204,13 @@ def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows):
     scan (per-warp top-K buffers, two blocks per SM), then the lists merge when a row has
     several segments.  Forcing 40 segments on 4 rows makes such a grid at a size the oracle
     finishes quickly; a 300-record row leaves most of its segments empty.  Grid mode: indices
-    bit-exact; Gaussian mode: near-tie swaps only (none on these seeds)."""
+    bit-exact; Gaussian mode: near-tie swaps only (none on these seeds).  Ties: a zero indexer
+    query makes every score 0, so each row keeps its lowest positions (every selection step
+    decides by position alone)."""
     _cuda()
-    inp = small("long_decode", seed=21, mode=mode, B=B, N=N)
+    inp = small("long_decode", seed=21, mode="grid" if mode == "ties" else mode, B=B, N=N)
+    if mode == "ties":
+        inp["layers"][0]["q_idx"][...] = 0
     if rows is not None:
         set_rows(inp, rows)
     if forced_seg:
@@ -223,10 +227,10 @@ def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows):
         assert any("idx_fp8_stream_kernel" in k for k in kernels), sorted(set(kernels))
     ref = O.csa2_group(inp)
     idx = g[0].idx.cpu().numpy()
-    if mode == "grid":
-        assert np.array_equal(idx, ref[0]["idx"])
-    else:
+    if mode == "gauss":
         assert check_idx_near_ties(idx, ref[0]["idx"], ref[0]["scores"], score_bound(inp, 0)) == 0
+    else:
+        assert np.array_equal(idx, ref[0]["idx"])
     assert rel_err(g[0].out.cpu().numpy(), ref[0]["o"]) <= out_tol(inp["params"])
 
 
