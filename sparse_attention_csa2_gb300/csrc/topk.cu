@@ -164,6 +164,11 @@ __global__ void __launch_bounds__(kMergeThreads, 1) lists_merge_kernel(const Fee
   s.tid = threadIdx.x;
   s.scratch = reinterpret_cast<uint32_t*>(sel_idx + ((K + 3) & ~3));  // lists, 16-byte aligned
   const int ln = s.lane();
+  // Programmatic dependent launch: the next kernel (the attention, whose tiles over the window
+  // need no indices) may start while the row selections run; it waits for this grid before it
+  // reads them.  The lists are the previous kernel's output: wait for it first.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   for (int i = s.tid; i < S; i += kMergeThreads) {
     ms.cnt[i] = min(__ldcg(p.in_cnt + (size_t)row * S + i), Kin);
     ms.thr[i] = p.in_thr ? __ldcg(p.in_thr + (size_t)row * S + i) : 0u;
@@ -663,13 +668,15 @@ cudaError_t launch_lists_merge(const FeedParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)n_cta;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, lists_merge_kernel, p, per);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
