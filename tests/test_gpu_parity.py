@@ -197,13 +197,16 @@ def test_fused_full_gauss():
 @pytest.mark.parametrize("forced_seg,B,N,rows", [
     (40, 4, 50_000, [50_000, 49_999, 7_777, 300]),  # two waves of segments: lists, then the merge
     (0, 160, 3_000, None),                          # more rows than SMs: one segment per row
+    (1, 12, 200_000, None),                         # one segment longer than the placement bitmap
 ])
 def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows):
     """FP8 keys over more work than one wave of the decode kernel's segments (each segment's
     keys kept in shared memory, one block per SM): the FULL layer takes the streaming FP8
     scan (per-warp top-K buffers, two blocks per SM), then the lists merge when a row has
     several segments.  Forcing 40 segments on 4 rows makes such a grid at a size the oracle
-    finishes quickly; a 300-record row leaves most of its segments empty.  Grid mode: indices
+    finishes quickly; a 300-record row leaves most of its segments empty; one forced segment of
+    200,000 records per row is longer than the bitmap that places a segment's survivors, so
+    they are placed by the engine's searches instead.  Grid mode: indices
     bit-exact; Gaussian mode: near-tie swaps only (none on these seeds).  Ties: a zero indexer
     query makes every score 0, so each row keeps its lowest positions (every selection step
     decides by position alone)."""
