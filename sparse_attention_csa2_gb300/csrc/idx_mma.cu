@@ -972,8 +972,13 @@ __global__ void __launch_bounds__(DecCfg<FP8>::kThreads, 1)
 // SM: one block streams FP8 tiles at about two thirds of an SM's share of the HBM rate (its
 // copy thread, MMA thread and epilogue warps form one dependent chain per tile and contend
 // for the SM's issue slots), two blocks per SM interleave two such chains.
-// Each block writes its segment's list (at most K entries in position order, and its K-th
-// key) for the lists merge, or the row's indices when the row is a single segment.
+// The epilogue checks the buffers every 4 tiles; one near capacity is first pruned by one
+// histogram pass (eng_prune), the exact select runs only when that leaves too little room,
+// since the stream waits on the epilogue meanwhile.  At the end the exact select leaves the
+// segment's K best, placed in position order through a bitmap of their offsets in the idle
+// ring (or, for a segment longer than the bitmap, by the engine's searches).  Each block
+// writes its segment's list (at most K entries in position order, and its K-th key) for the
+// lists merge, or the row's indices when the row is a single segment.
 constexpr int kStrStages = 3;
 constexpr int kStrTile = kTileKeys * 128;  // 16 KB: 128 records x 128 E4M3 dims
 constexpr int kStrThreads = 12 * 32;       // warp 0 TMA, warp 1 MMA + tensor memory, warps 4..11 epilogue
