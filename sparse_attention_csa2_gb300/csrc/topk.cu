@@ -252,7 +252,12 @@ size_t merge_smem_bytes(int seg_per_cta, int Kin, int K) {
 
 // Exact top-K of one long row of materialised scores per block, by radix selection over the
 // row held in memory (for many rows, each far longer than K: the prefill chunk's rows).
-// Pass 1 counts the keys' top 12 bits; pass 2 counts the next 12 bits of the keys in the
+// Rows of up to 64 K entries first sample every 8th run of 128 entries for a level-1 bin g
+// at or below the K-th key's (twice the proportional share of K reaches it); the level-1 pass
+// also lists every entry of bin g and above, and when the K-th key's bin is at least g and the
+// list held them all, the rest of the selection and the placement read only the list: about
+// 1.1 passes over the row.  Otherwise, and for longer rows, pass 1 counts the keys' top 12
+// bits; pass 2 counts the next 12 bits of the keys in the
 // threshold's bin and lists those keys in shared memory (their number is about the bin's
 // population), so the last 8 bits come from the list; when the bin holds more keys than the
 // list, pass 3 counts them over the row again.  The K-th key T and the number of entries equal
@@ -271,7 +276,9 @@ constexpr long long kRtBitmapMax = 65536;  // entries: two bitmaps of this many 
 struct RowTopkShared {
   int hist[kHistBins];
   uint32_t list[kRtList];
+  int32_t list_pos[kRtList];  // one-pass rows: the listed entries' indices in the row
   int n_list;
+  int n_sample;
   int bin, before;
   int warp_gt[kRtWarps], warp_eq[kRtWarps];
 };
@@ -365,6 +372,52 @@ __device__ __forceinline__ int rt_block_scan(RowTopkShared& sh, int v, int& tota
   return before + x - v;
 }
 
+// The second half of the bitmap placement: `keep` and `tie` (in sh.hist) hold, in position
+// order, the entries above T and those equal to it; the first n_eq tie bits join `keep` (a
+// block prefix over the words' counts) and every kept entry is written in position order.
+template <class Pos>
+__device__ __forceinline__ void rt_place_marked(RowTopkShared& sh, int n_eq, long long L, int32_t* out, Pos position) {
+  const int tid = threadIdx.x;
+  uint32_t* keep = reinterpret_cast<uint32_t*>(sh.hist);
+  uint32_t* tie = keep + kRtBitmapMax / 32;
+  constexpr int kWords = (int)(kRtBitmapMax / 32), kWpt = kWords / kRtThreads;  // words per thread
+  __syncthreads();
+  // the first n_eq ties in position order join the kept entries (thread t: words kWpt t ..)
+  const int n_words = (int)((L + 31) / 32), w0 = tid * kWpt;
+  int tc = 0;
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) tc += w0 + j < n_words ? __popc(tie[w0 + j]) : 0;
+  int total;
+  int rank = rt_block_scan(sh, tc, total);
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) {
+    if (w0 + j >= n_words) break;
+    uint32_t m = tie[w0 + j], sel = 0u;
+    while (m != 0u && rank < n_eq) {  // lowest bits (positions) first
+      const uint32_t low = m & (0u - m);
+      sel |= low;
+      m ^= low;
+      ++rank;
+    }
+    keep[w0 + j] |= sel;
+  }
+  __syncthreads();  // the scan's scratch is reused below
+  int kc = 0;
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) kc += w0 + j < n_words ? __popc(keep[w0 + j]) : 0;
+  int at = rt_block_scan(sh, kc, total);
+#pragma unroll
+  for (int j = 0; j < kWpt; ++j) {
+    if (w0 + j >= n_words) break;
+    uint32_t m = keep[w0 + j];
+    while (m != 0u) {
+      const int bit = __ffs(m) - 1;
+      out[at++] = position(32LL * (w0 + j) + bit);
+      m &= m - 1u;
+    }
+  }
+}
+
 // Placement of a row of at most kRtBitmapMax entries once the K-th key T and the number n_eq of
 // entries equal to it that are kept are known: one pass over the row marks, in position order,
 // the entries above T (`keep`) and equal to it (`tie`); the first n_eq tie bits join `keep`; the
@@ -375,7 +428,7 @@ __device__ __forceinline__ void rt_place_bitmap(RowTopkShared& sh, const float* 
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t* keep = reinterpret_cast<uint32_t*>(sh.hist);
   uint32_t* tie = keep + kRtBitmapMax / 32;
-  constexpr int kWords = (int)(kRtBitmapMax / 32), kWpt = kWords / kRtThreads;  // words per thread
+  constexpr int kWords = (int)(kRtBitmapMax / 32);
   static_assert(2 * kWords <= kHistBins, "both bitmaps fit in the histogram");
   __syncthreads();  // every thread has read the last pick's results
   for (int i = tid; i < 2 * kWords; i += kRtThreads) keep[i] = 0u;
@@ -425,41 +478,7 @@ __device__ __forceinline__ void rt_place_bitmap(RowTopkShared& sh, const float* 
       }
     }
   }
-  __syncthreads();
-  // the first n_eq ties in position order join the kept entries (thread t: words kWpt t ..)
-  const int n_words = (int)((L + 31) / 32), w0 = tid * kWpt;
-  int tc = 0;
-#pragma unroll
-  for (int j = 0; j < kWpt; ++j) tc += w0 + j < n_words ? __popc(tie[w0 + j]) : 0;
-  int total;
-  int rank = rt_block_scan(sh, tc, total);
-#pragma unroll
-  for (int j = 0; j < kWpt; ++j) {
-    if (w0 + j >= n_words) break;
-    uint32_t m = tie[w0 + j], sel = 0u;
-    while (m != 0u && rank < n_eq) {  // lowest bits (positions) first
-      const uint32_t low = m & (0u - m);
-      sel |= low;
-      m ^= low;
-      ++rank;
-    }
-    keep[w0 + j] |= sel;
-  }
-  __syncthreads();  // the scan's scratch is reused below
-  int kc = 0;
-#pragma unroll
-  for (int j = 0; j < kWpt; ++j) kc += w0 + j < n_words ? __popc(keep[w0 + j]) : 0;
-  int at = rt_block_scan(sh, kc, total);
-#pragma unroll
-  for (int j = 0; j < kWpt; ++j) {
-    if (w0 + j >= n_words) break;
-    uint32_t m = keep[w0 + j];
-    while (m != 0u) {
-      const int bit = __ffs(m) - 1;
-      out[at++] = position(32LL * (w0 + j) + bit);
-      m &= m - 1u;
-    }
-  }
+  rt_place_marked(sh, n_eq, L, out, position);
 }
 
 __global__ void __launch_bounds__(kRtThreads) row_topk_kernel(const FeedParams p) {
@@ -481,19 +500,105 @@ __global__ void __launch_bounds__(kRtThreads) row_topk_kernel(const FeedParams p
   // warp w's contiguous range (a multiple of 128 entries, for the 16-byte walk)
   const long long per = ((L + kRtWarps - 1) / kRtWarps + 127) / 128 * 128;
   const long long a = min(L, warp * per), b = min(L, a + per);
-  // ---- level 1: bits 31..20
+  // ---- one pass for rows the bitmaps cover: a sample of the row (every 8th run of 128
+  // entries) gives a level-1 bin g that about twice the proportional share of K entries reach;
+  // the level-1 pass then also lists every entry of bin g and above (key and index).  When the
+  // K-th key's bin b1 is at least g and the list held every such entry, the two finer levels
+  // and the placement come from the list; otherwise the row continues below from level 2 (the
+  // level-1 histogram is complete either way).
+  const bool one_pass = L <= kRtBitmapMax;
+  uint32_t g = 0xffffffffu;  // no listing in the level-1 pass
+  if (one_pass) {
+    for (int i = tid; i < kHistBins; i += kRtThreads) sh.hist[i] = 0;
+    if (tid == 0) sh.n_sample = 0;
+    __syncthreads();
+    const long long n_chunks = (L + 127) / 128;
+    int taken = 0;
+    for (long long c = 8LL * warp; c < n_chunks; c += 8LL * kRtWarps) {
+      const long long c0 = c * 128, c1 = min(L, c0 + 128);
+      if (vec && c0 + 4 * lane + 3 < c1) {
+        const float4 v = *reinterpret_cast<const float4*>(rs + c0 + 4 * lane);
+        atomicAdd(&sh.hist[score_key(v.x) >> 20], 1);
+        atomicAdd(&sh.hist[score_key(v.y) >> 20], 1);
+        atomicAdd(&sh.hist[score_key(v.z) >> 20], 1);
+        atomicAdd(&sh.hist[score_key(v.w) >> 20], 1);
+        taken += 4;
+      } else {
+        for (long long i = c0 + (vec ? 4 * lane : lane); i < c1 && i < c0 + (vec ? 4 * lane + 4 : 128); i += vec ? 1 : 32) {
+          atomicAdd(&sh.hist[score_key(rs[i]) >> 20], 1);
+          ++taken;
+        }
+      }
+    }
+    atomicAdd(&sh.n_sample, taken);
+    __syncthreads();
+    const int n_s = sh.n_sample;  // >= 1: the first run is sampled
+    const int target = (int)min((long long)n_s, (2LL * K * n_s + L - 1) / L + 16);
+    if (warp == 0) rt_pick(sh, kHistBins, target);
+    __syncthreads();
+    g = (uint32_t)sh.bin;
+    __syncthreads();
+  }
+  // ---- level 1: bits 31..20 (one pass: the entries of bin g and above are also listed)
   for (int i = tid; i < kHistBins; i += kRtThreads) sh.hist[i] = 0;
   if (tid == 0) sh.n_list = 0;
   __syncthreads();
-  rt_walk(rs, a, b, vec, [&](long long, uint32_t key) { atomicAdd(&sh.hist[key >> 20], 1); });
+  rt_walk(rs, a, b, vec, [&](long long j, uint32_t key) {
+    atomicAdd(&sh.hist[key >> 20], 1);
+    if ((key >> 20) >= g) {
+      const int slot = atomicAdd(&sh.n_list, 1);
+      if (slot < kRtList) {
+        sh.list[slot] = key;
+        sh.list_pos[slot] = (int32_t)j;
+      }
+    }
+  });
   __syncthreads();
   if (warp == 0) rt_pick(sh, kHistBins, K);
   __syncthreads();
   const uint32_t b1 = (uint32_t)sh.bin;
   int need = K - sh.before;
+  const int n_listed = sh.n_list;
   __syncthreads();
+  if (one_pass && b1 >= g && n_listed <= kRtList) {
+    // every entry of bin b1 and above is listed
+    for (int i = tid; i < kHistBins; i += kRtThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_listed; i += kRtThreads)
+      if ((sh.list[i] >> 20) == b1) atomicAdd(&sh.hist[(sh.list[i] >> 8) & 0xfffu], 1);
+    __syncthreads();
+    if (warp == 0) rt_pick(sh, kHistBins, need);
+    __syncthreads();
+    const uint32_t h24 = (b1 << 12) | (uint32_t)sh.bin;
+    need -= sh.before;
+    __syncthreads();
+    for (int i = tid; i < 256; i += kRtThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_listed; i += kRtThreads)
+      if ((sh.list[i] >> 8) == h24) atomicAdd(&sh.hist[sh.list[i] & 0xffu], 1);
+    __syncthreads();
+    if (warp == 0) rt_pick(sh, 256, need);
+    __syncthreads();
+    const uint32_t T1 = (h24 << 8) | (uint32_t)sh.bin;
+    const int n_eq1 = need - sh.before;
+    __syncthreads();
+    // the listed entries above T and equal to it, marked by position
+    uint32_t* keep = reinterpret_cast<uint32_t*>(sh.hist);
+    uint32_t* tie = keep + kRtBitmapMax / 32;
+    for (int i = tid; i < (int)(2 * kRtBitmapMax / 32); i += kRtThreads) keep[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n_listed; i += kRtThreads) {
+      const uint32_t key = sh.list[i];
+      const int j = sh.list_pos[i];
+      if (key > T1) atomicOr(&keep[j >> 5], 1u << (j & 31));
+      else if (key == T1) atomicOr(&tie[j >> 5], 1u << (j & 31));
+    }
+    rt_place_marked(sh, n_eq1, L, out, position);
+    return;
+  }
   // ---- level 2: bits 19..8 of the keys in bin b1, which are listed on the way
   for (int i = tid; i < kHistBins; i += kRtThreads) sh.hist[i] = 0;
+  if (tid == 0) sh.n_list = 0;
   __syncthreads();
   rt_walk(rs, a, b, vec, [&](long long, uint32_t key) {
     if ((key >> 20) == b1) {
