@@ -194,12 +194,13 @@ def test_fused_full_gauss():
 
 
 @pytest.mark.parametrize("mode", ["grid", "gauss", "ties"])
-@pytest.mark.parametrize("forced_seg,B,N,rows", [
-    (40, 4, 50_000, [50_000, 49_999, 7_777, 300]),  # two waves of segments: lists, then the merge
-    (0, 160, 3_000, None),                          # more rows than SMs: one segment per row
-    (1, 12, 200_000, None),                         # one segment longer than the placement bitmap
+@pytest.mark.parametrize("forced_seg,B,N,rows,K", [
+    (40, 4, 50_000, [50_000, 49_999, 7_777, 300], 512),  # two waves of segments: lists, then the merge
+    (40, 4, 50_000, [50_000, 49_999, 7_777, 300], 64),   # small K: the buffers prune and select often
+    (0, 160, 3_000, None, 512),                          # more rows than SMs: one segment per row
+    (1, 12, 200_000, None, 512),                         # one segment longer than the placement bitmap
 ])
-def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows):
+def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows, K):
     """FP8 keys over more work than one wave of the decode kernel's segments (each segment's
     keys kept in shared memory, one block per SM): the FULL layer takes the streaming FP8
     scan (per-warp top-K buffers, two blocks per SM), then the lists merge when a row has
@@ -211,7 +212,7 @@ def test_fused_full_fp8_streaming_scan(mode, forced_seg, B, N, rows):
     query makes every score 0, so each row keeps its lowest positions (every selection step
     decides by position alone)."""
     _cuda()
-    inp = small("long_decode", seed=21, mode="grid" if mode == "ties" else mode, B=B, N=N)
+    inp = small("long_decode", seed=21, mode="grid" if mode == "ties" else mode, B=B, N=N, K=K)
     if mode == "ties":
         inp["layers"][0]["q_idx"][...] = 0
     if rows is not None:
